@@ -1,0 +1,185 @@
+"""CPU oracle for top-k sparse decode attention with GQA -- TEST INFRASTRUCTURE ONLY.
+
+This package wraps ``oracle.c`` (plain fp64 loops, one function per step of the method)
+with numpy in / numpy out.  Only the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import it; the CUDA library never does, and the two
+share no code.  Each wrapper restates which passage of the source pages its step
+follows (see the C source for the full citations).
+
+Arrays: fp32 data is a float32 array; bfloat16 data is a uint16 array of raw bits (or a
+CPU torch tensor of dtype bfloat16, which is viewed as such without copying).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+F32, BF16 = 0, 1
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        D = ctypes.c_double
+        lib.oracle_num_threads.restype = I
+        lib.oracle_index_score.argtypes = [P, I, P, I, I, I, I, I, I, P]
+        lib.oracle_block_pool.argtypes = [P, I, I, I, I, I, I, P]
+        lib.oracle_topk.argtypes = [P, I, I, I, P]
+        lib.oracle_gather_attend.argtypes = [P, P, P, I, P, I, I, I, I, I, I, I, I, D, P, P, P]
+        lib.oracle_score_accumulate.argtypes = [P, P, P, I, I, I, I, I, I, I, D, P]
+        lib.oracle_tier_classify.argtypes = [P, I, I, P, I, I, P, P]
+        lib.oracle_quantize_rows_int8.argtypes = [P, I, P, I, I, I, I, P, P]
+        for name in ("oracle_index_score", "oracle_block_pool", "oracle_topk",
+                     "oracle_gather_attend", "oracle_score_accumulate", "oracle_tier_classify",
+                     "oracle_quantize_rows_int8"):
+            getattr(lib, name).restype = I
+        _lib = lib
+    return _lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _check(rc, what):
+    if rc == -1:
+        raise OracleError(f"{what}: invalid argument")
+    if rc == -2:
+        raise OracleError(f"{what}: selected row index out of range")
+    if rc != 0:
+        raise OracleError(f"{what}: error {rc}")
+
+
+def _as_data(x):
+    """Return (contiguous numpy array, dtype code) for fp32 or bfloat16 data."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            if x.dtype == torch.bfloat16:
+                return x.view(torch.int16).numpy().view(np.uint16), BF16
+            if x.dtype == torch.float32:
+                return x.numpy(), F32
+            raise TypeError(f"unsupported tensor dtype {x.dtype}")
+    except ImportError:
+        pass
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        return x, F32
+    if x.dtype == np.uint16:
+        return x, BF16
+    raise TypeError(f"unsupported array dtype {x.dtype} (float32, or uint16 bfloat16 bits)")
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle runs on (all host cores unless OMP_NUM_THREADS says)."""
+    return _load().oracle_num_threads()
+
+
+def index_score(q_idx, k_idx, B, Hkv, V, N, dI):
+    """Compact indexer score, max over the V verify queries (SparDA, "Indexador de
+    Previsao Compacto").  Returns fp64 [B,Hkv,N]."""
+    q, qd = _as_data(q_idx)
+    k, kd = _as_data(k_idx)
+    assert q.size == B * Hkv * V * dI and k.size == B * Hkv * N * dI
+    out = np.empty((B, Hkv, N), dtype=np.float64)
+    _check(_load().oracle_index_score(_ptr(q), qd, _ptr(k), kd, B, Hkv, V, N, dI, _ptr(out)),
+           "index_score")
+    return out
+
+
+def block_pool(k_idx, B, Hkv, T, dI, block):
+    """Mean of each disjoint block of `block` indexer keys (SparDA, block grid).
+    Returns fp64 [B,Hkv,T/block,dI]."""
+    k, kd = _as_data(k_idx)
+    assert k.size == B * Hkv * T * dI
+    out = np.empty((B, Hkv, T // block, dI), dtype=np.float64)
+    _check(_load().oracle_block_pool(_ptr(k), kd, B, Hkv, T, dI, block, _ptr(out)), "block_pool")
+    return out
+
+
+def topk(scores, k):
+    """Exact top-k per row, ties to the lower index, ascending output (Illusion,
+    "Oracle Top-K").  scores [..., N] (any float type, compared as fp64) -> int32 [..., k]."""
+    s = np.ascontiguousarray(scores, dtype=np.float64)
+    N = s.shape[-1]
+    rows = s.size // N if N > 0 else int(np.prod(s.shape[:-1]))
+    out = np.empty(s.shape[:-1] + (k,), dtype=np.int32)
+    _check(_load().oracle_topk(_ptr(s), rows, N, k, _ptr(out)), "topk")
+    return out
+
+
+def gather_attend(q, K, Vv, idx, B, V, Hq, Hkv, d, T, n_idx, block, scale, want_logits=False):
+    """Exact softmax attention of every query row over the selected rows only
+    (Illusion sec. 2 / 3C).  idx None means dense (all T rows).
+    Returns (out fp64 [B,V,Hq,d], lse fp64 [B,V,Hq], logits fp64 [B,V,Hq,n_idx*block] or None)."""
+    qa, qd = _as_data(q)
+    ka, kd = _as_data(K)
+    va, vd = _as_data(Vv)
+    assert qd == kd == vd, "q, K and V must share one dtype"
+    assert qa.size == B * V * Hq * d and ka.size == B * Hkv * T * d and va.size == ka.size
+    ia = None
+    if idx is not None:
+        ia = np.ascontiguousarray(idx, dtype=np.int32)
+        assert ia.size == B * Hkv * n_idx
+    out = np.empty((B, V, Hq, d), dtype=np.float64)
+    lse = np.empty((B, V, Hq), dtype=np.float64)
+    logits = np.empty((B, V, Hq, n_idx * block), dtype=np.float64) if want_logits else None
+    _check(_load().oracle_gather_attend(_ptr(qa), _ptr(ka), _ptr(va), qd, _ptr(ia), B, V, Hq, Hkv,
+                                        d, T, n_idx, block, float(scale), _ptr(out), _ptr(lse),
+                                        _ptr(logits)), "gather_attend")
+    return out, lse, logits
+
+
+def score_accumulate(logits, lse, idx, s, B, V, Hq, Hkv, n_idx, block, T, weight):
+    """One layer's term of the cumulative importance score (Not All Thoughts Need HBM,
+    Metodologia 2), added in place to the fp64 array s [B,T]."""
+    la = np.ascontiguousarray(logits, dtype=np.float64)
+    ea = np.ascontiguousarray(lse, dtype=np.float64)
+    assert s.dtype == np.float64 and s.flags.c_contiguous and s.size == B * T
+    ia = None if idx is None else np.ascontiguousarray(idx, dtype=np.int32)
+    _check(_load().oracle_score_accumulate(_ptr(la), _ptr(ea), _ptr(ia), B, V, Hq, Hkv, n_idx,
+                                           block, T, float(weight), _ptr(s)), "score_accumulate")
+    return s
+
+
+def tier_classify(s, cum_frac, n_sink=0, n_recent=0):
+    """Four-tier split by importance rank (Not All Thoughts Need HBM, Metodologia 1).
+    s [B,T] -> (tier uint8 [B,T], counts int32 [B,4])."""
+    sa = np.ascontiguousarray(s, dtype=np.float64)
+    B, T = sa.shape
+    fr = np.ascontiguousarray(cum_frac, dtype=np.float64)
+    assert fr.size == 3
+    tier = np.empty((B, T), dtype=np.uint8)
+    counts = np.empty((B, 4), dtype=np.int32)
+    _check(_load().oracle_tier_classify(_ptr(sa), B, T, _ptr(fr), n_sink, n_recent, _ptr(tier),
+                                        _ptr(counts)), "tier_classify")
+    return tier, counts
+
+
+def quantize_rows_int8(x, tier, B, Hkv, T, d, codes=None, scales=None):
+    """Symmetric per-row int8 codes of the rows whose tier is 2 (Not All Thoughts Need
+    HBM, Metodologia 1, T2).  Rows of other tiers keep what `codes`/`scales` held (zeros
+    if they are created here).  Returns (codes int8 [B,Hkv,T,d], scales fp32 [B,Hkv,T])."""
+    xa, xd = _as_data(x)
+    ta = np.ascontiguousarray(tier, dtype=np.uint8)
+    assert xa.size == B * Hkv * T * d and ta.size == B * T
+    if codes is None:
+        codes = np.zeros((B, Hkv, T, d), dtype=np.int8)
+    if scales is None:
+        scales = np.zeros((B, Hkv, T), dtype=np.float32)
+    _check(_load().oracle_quantize_rows_int8(_ptr(xa), xd, _ptr(ta), B, Hkv, T, d, _ptr(codes),
+                                             _ptr(scales)), "quantize_rows_int8")
+    return codes, scales
