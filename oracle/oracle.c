@@ -208,6 +208,7 @@ int oracle_gather_attend(const void* q, const void* K, const void* Vv, int dtype
                 const size_t qrow = (((size_t)b * V + v) * Hq + h);
                 double* qv = (double*)malloc(sizeof(double) * (size_t)d);
                 double* kr = (double*)malloc(sizeof(double) * (size_t)d);
+                double* acc = (double*)malloc(sizeof(double) * (size_t)d);
                 double* z = (double*)malloc(sizeof(double) * (size_t)(n_rows > 0 ? n_rows : 1));
                 long* rows = (long*)malloc(sizeof(long) * (size_t)(n_rows > 0 ? n_rows : 1));
                 orc_load_row(q, dtype, qrow * d, d, qv);
@@ -229,20 +230,23 @@ int oracle_gather_attend(const void* q, const void* K, const void* Vv, int dtype
                     z[j] = scale * dot;
                     if (z[j] > m) m = z[j];
                 }
+                /* w_j = exp(z_j - m), evaluated once per row; every column sums its terms
+                   in ascending j. */
                 double l = 0.0;
-                for (long j = 0; j < n_rows; ++j) l += exp(z[j] - m);
-                for (int c = 0; c < d; ++c) {
-                    double acc = 0.0;
-                    for (long j = 0; j < n_rows; ++j)
-                        acc += exp(z[j] - m) *
-                               orc_elem(Vv, dtype, (((size_t)b * Hkv + kvh) * T + rows[j]) * d + c);
-                    out[qrow * d + c] = (n_rows > 0) ? acc / l : 0.0;
+                for (int c = 0; c < d; ++c) acc[c] = 0.0;
+                for (long j = 0; j < n_rows; ++j) {
+                    const double wj = exp(z[j] - m);
+                    l += wj;
+                    orc_load_row(Vv, dtype, (((size_t)b * Hkv + kvh) * T + rows[j]) * d, d, kr);
+                    for (int c = 0; c < d; ++c) acc[c] += wj * kr[c];
                 }
+                for (int c = 0; c < d; ++c) out[qrow * d + c] = (n_rows > 0) ? acc[c] / l : 0.0;
                 lse[qrow] = (n_rows > 0) ? m + log(l) : -INFINITY;
                 if (logits != NULL)
                     for (long j = 0; j < n_rows; ++j) logits[qrow * n_rows + j] = z[j];
                 free(qv);
                 free(kr);
+                free(acc);
                 free(z);
                 free(rows);
             }
