@@ -1,0 +1,215 @@
+/*
+ * sd.h -- C ABI of libsdgqa: top-k sparse decode attention with GQA on GB300 (sm_103a).
+ *
+ * The library is one hand-written CUDA kernel (or a short fixed sequence of them) per
+ * call.  Every call is asynchronous on the CUDA stream passed as `stream` (a
+ * cudaStream_t, given as void* so this header needs no CUDA include; NULL = the legacy
+ * default stream).  Arguments are validated on the host before anything is launched; a
+ * rejected call launches nothing and returns SD_ERR_INVALID_ARG or SD_ERR_UNSUPPORTED
+ * (sd_last_error_message() tells why).  A failed launch returns SD_ERR_CUDA.
+ *
+ * Ownership: the caller owns every buffer.  The library allocates no device or host
+ * memory on any call; calls that need scratch space take a caller-provided workspace
+ * whose size is queried first.  Pointers are device pointers unless stated otherwise;
+ * "pinned host" pointers must come from cudaHostAlloc / cudaHostRegister (page-locked
+ * and mapped into the device address space).  All tensors are dense, row-major, with the
+ * layouts given below; data pointers must be 16-byte aligned.
+ *
+ * Device-side faults: a selected row or pool slot outside its tensor is never read; the
+ * kernel skips it and ORs a bit into *err_word (a caller-owned device int32, nullable:
+ * NULL means such errors are not reported).  Every wait inside a kernel is bounded; a
+ * wait that runs out sets SD_DEVERR_TIMEOUT and the kernel returns.  No kernel traps.
+ *
+ * Element types: SD_F32 = IEEE binary32, SD_BF16 = bfloat16 (upper half of a binary32).
+ * Arithmetic is fp32 (fp64 for the importance score) whatever the storage type.
+ *
+ * Sources the operations follow (web pages, cited by title and section):
+ *   [SparDA]    "SparDA: Atencao Esparsa Desacoplada para Inferencia Eficiente de LLMs de
+ *               Longo Contexto" (gist.science technical summary), sec. 2.
+ *   [Illusion]  "Esparsidade de Contexto no Tempo de Inferencia: Ilusao ou Oportunidade?"
+ *               (gist.science technical summary), sec. 2 and 3C.
+ *   [HBM]       "Nem Todos os Pensamentos Necessitam de HBM" (gist.science technical
+ *               summary), Metodologia 1-4.
+ *   [DHiSparse] "O Fim do Gargalo de Memoria: Como o Adaptive DHiSparse Revolutiona LLMs
+ *               de Contexto Longo" (news page), "A Inovacao", "Metodologia e Eficiencia".
+ */
+#ifndef SDGQA_SD_H
+#define SDGQA_SD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SD_OK = 0,
+    SD_ERR_INVALID_ARG = 1,   /* shape, pointer, alignment or workspace check failed */
+    SD_ERR_UNSUPPORTED = 2,   /* valid request outside the compiled kernels (e.g. d) */
+    SD_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    SD_ERR_DEVICE_BOUNDS = 4, /* reserved: reported through *err_word, see below */
+    SD_ERR_TIMEOUT = 5        /* reserved: reported through *err_word, see below */
+} sd_status;
+
+typedef enum { SD_F32 = 0, SD_BF16 = 1 } sd_dtype;
+
+/* Bits a kernel ORs into *err_word. */
+#define SD_DEVERR_INDEX 0x1   /* a selected index outside [0, N) or [0, T) was skipped */
+#define SD_DEVERR_SLOT 0x2    /* a slot_map entry outside [-1, pool_rows) was skipped */
+#define SD_DEVERR_TIMEOUT 0x4 /* a bounded wait ran out; the kernel's outputs are invalid */
+
+/* Library version: 100 * major + minor. */
+int sd_version(void);
+
+/* Static text for a status code. */
+const char* sd_status_string(sd_status status);
+
+/* Detail of the last failed call on this host thread ("" if none). */
+const char* sd_last_error_message(void);
+
+/*
+ * sd_index_score -- compact indexer score of every cached token.
+ * [SparDA] sec. 2 "Indexador de Previsao Compacto": one indexer head per GQA group
+ * (= per KV head) scores each token with a plain dot product, with no softmax and no
+ * loop over query heads.  With V > 1 query tokens sharing one selection (a speculative
+ * verify batch whose tokens share the fetch of missing rows, [DHiSparse] "Metodologia")
+ * the score is the maximum over the V queries:
+ *     scores[b,h,t] = max_v  sum_j q_idx[b,h,v,j] * k_idx[b,h,t,j]
+ * q_idx  [B,Hkv,V,d_idx] of q_dtype; k_idx [B,Hkv,N,d_idx] of k_dtype (token keys, or
+ * the pooled block keys of sd_block_pool for block-granular selection, then N = blocks);
+ * scores [B,Hkv,N] fp32 (written).  fp32 products and sums: integer-valued inputs with
+ * |sum| < 2^24 give exact scores.  Limits: d_idx in {64, 128}, 1 <= V <= 8, N >= 0.
+ * err_word: nullable device int32 (only SD_DEVERR_TIMEOUT can be set).
+ */
+sd_status sd_index_score(const void* q_idx, sd_dtype q_dtype, const void* k_idx,
+                         sd_dtype k_dtype, int B, int Hkv, int V, int N, int d_idx,
+                         float* scores, int32_t* err_word, void* stream);
+
+/*
+ * sd_block_pool -- block keys for block-granular selection (cache-build helper).
+ * [SparDA] sec. 2 item 1 (top-k blocks) and "Estrategia de Treinamento" (pooling onto the
+ * block grid).  Disjoint blocks of `block` tokens; the key of block n is the mean of its
+ * tokens' indexer keys, computed in fp32 (exact for integer keys and power-of-two block):
+ *     pooled[b,h,n,j] = (1/block) * sum_{t in [n*block, (n+1)*block)} k_idx[b,h,t,j]
+ * k_idx [B,Hkv,T,d_idx] of k_dtype; pooled [B,Hkv,T/block,d_idx] fp32 (written).
+ * T must be a multiple of block.  Limits: d_idx in {64, 128}, 1 <= block <= 4096.
+ */
+sd_status sd_block_pool(const void* k_idx, sd_dtype k_dtype, int B, int Hkv, int T, int d_idx,
+                        int block, float* pooled, void* stream);
+
+/*
+ * sd_topk -- exact top-k per row.
+ * [Illusion] sec. 2 "Mecanismos de Esparsidade" (Oracle Top-K: exact selection of the k
+ * highest-scoring tokens); [SparDA] sec. 2 item 1 (top-k blocks).  Per row r, the k
+ * entries first in the order (score descending, index ascending) -- ties go to the lower
+ * index -- written in ascending index order.  -0.0 and +0.0 compare equal.
+ * scores [rows,N] fp32 (NaN is outside the contract); idx [rows,k] int32 (written).
+ * 0 <= k <= N.  Uses no workspace in this version: sd_topk_workspace_bytes returns 0 and
+ * `workspace` may be NULL.
+ */
+size_t sd_topk_workspace_bytes(int rows, int N, int k);
+sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/*
+ * sd_gather_attend -- exact softmax attention over only the selected K/V rows.
+ * [Illusion] sec. 2 (custom sparse decode kernels, irregular per token) and sec. 3C
+ * (memory traffic O(k*d) instead of O(N*d)); [DHiSparse] "A Inovacao" (history in host
+ * memory, only the selected rows fetched, fused with attention) and "Metodologia"
+ * (queries share the fetch of missing rows); [HBM] Metodologia 3 (a row contributes the
+ * same terms wherever it is stored).
+ *
+ * For query row (b, v, h) with kvh = h / (Hq/Hkv):
+ *   rows_j = idx[b,kvh, j / block] * block + j % block, j < n_idx*block  (idx == NULL:
+ *            dense, rows_j = j and n_idx*block must equal T)
+ *   z_j    = scale * q[b,v,h,:] . K[b,kvh,rows_j,:]
+ *   out[b,v,h,:] = sum_j softmax(z)_j V[b,kvh,rows_j,:],  lse[b,v,h] = log sum_j exp(z_j)
+ *   logits[b,v,h,j] = z_j (optional).  No rows: out = 0, lse = -inf.
+ * Row source: with slot_map == NULL every row is read from k_cache/v_cache, which then
+ * hold the whole cache [B,Hkv,T,d] (pool_rows == T).  With slot_map [B,T] int32, a row t
+ * with slot_map[b,t] = s >= 0 is read from the HBM pool k_cache/v_cache [B,Hkv,pool_rows,d]
+ * at slot s, and s == -1 reads it from pinned host memory k_host/v_host [B,Hkv,T,d]
+ * through the device's mapping of that memory.  Each selected row is read once per
+ * (b, kvh) and shared by all G*V query rows of the group.  The result does not depend on
+ * where the rows were read from: bit-identical outputs for any slot_map.
+ * Accumulation order depends only on (n_idx, block, splits), never on the data source.
+ * Limits: d in {64, 128}; G*V <= 32; dtype F32 or BF16 for q, K and V alike.
+ * The split-K partition over selected rows needs workspace (sd_gather_attend_workspace_bytes;
+ * 0 when one split suffices).  splits = 0 picks a split count for this GPU.
+ */
+typedef struct {
+    const void* q;            /* [B,V,Hq,d] */
+    const void* k_cache;      /* [B,Hkv,pool_rows,d]: HBM pool, or full cache if !slot_map */
+    const void* v_cache;      /* same layout as k_cache */
+    const void* k_host;       /* pinned host [B,Hkv,T,d], or NULL when slot_map == NULL */
+    const void* v_host;       /* pinned host [B,Hkv,T,d], or NULL when slot_map == NULL */
+    const int32_t* slot_map;  /* [B,T] slot or -1, or NULL */
+    const int32_t* idx;       /* [B,Hkv,n_idx] selected tokens or blocks, or NULL (dense) */
+    sd_dtype dtype;
+    int B, V, Hq, Hkv, d, T, pool_rows, n_idx, block;
+    float scale;              /* softmax scale, e.g. 1/sqrt(d) */
+    float* out;               /* [B,V,Hq,d] fp32, written */
+    float* lse;               /* [B,V,Hq] fp32 natural-log log-sum-exp, written */
+    float* logits;            /* [B,V,Hq,n_idx*block] fp32, written if not NULL */
+    int32_t* err_word;        /* nullable device int32 */
+    void* workspace;          /* device scratch of workspace_bytes */
+    size_t workspace_bytes;
+    int splits;               /* 0 = automatic */
+} sd_attend_args;
+
+size_t sd_gather_attend_workspace_bytes(const sd_attend_args* args);
+sd_status sd_gather_attend(const sd_attend_args* args, void* stream);
+
+/*
+ * sd_score_accumulate -- one layer's term of the cumulative attention-importance score.
+ * [HBM] Metodologia 2:  s_i(t) = s_i(t-1) + (1/|L|) sum_l (1/H) sum_h alpha_{l,h}(t)[i].
+ * Adds, for every query row (b, v, h) and selected row j (expanded as in
+ * sd_gather_attend, kvh = h / (Hq/Hkv)):
+ *     s[b, rows_j] += weight * exp(logits[b,v,h,j] - lse[b,v,h])
+ * so calling it once per layer with weight = 1/(|L| * Hq) applies the equation.
+ * logits [B,V,Hq,n_idx*block] and lse [B,V,Hq] fp32 as written by sd_gather_attend;
+ * idx [B,Hkv,n_idx] or NULL (dense); s [B,T] fp64, updated in place.
+ * Rows not selected receive nothing.  Order of additions into one s entry is not fixed
+ * when several KV groups select it (fp64 atomics); the result varies only by rounding.
+ */
+sd_status sd_score_accumulate(const float* logits, const float* lse, const int32_t* idx, int B,
+                              int V, int Hq, int Hkv, int n_idx, int block, int T, double weight,
+                              double* s, int32_t* err_word, void* stream);
+
+/*
+ * sd_tier_classify -- four-tier residency classes from the importance score.
+ * [HBM] Metodologia 1: T0 (HBM) = protected tokens (prompt/sinks = the first n_sink
+ * positions, recent window = the last n_recent) and the most important; T1 (host DDR,
+ * full precision); T2 (8-bit); T3 (evicted, the least important tail).  Metodologia 4:
+ * the caller re-runs it every Delta = 64 decode steps.
+ * Per sequence: protected positions rank first (in index order), then the others by
+ * (s descending, index ascending).  With c_m = floor(cum_frac[m] * T):
+ *   rank < c_0 -> 0, < c_1 -> 1, < c_2 -> 2, else 3; protected positions are always 0.
+ * s [B,T] fp64; tier [B,T] uint8 and counts [B,4] int32 (written).
+ * cum_frac must be nondecreasing within [0, 1].  Workspace: sd_tier_classify_workspace_bytes.
+ */
+size_t sd_tier_classify_workspace_bytes(int B, int T);
+sd_status sd_tier_classify(const double* s, int B, int T, const double cum_frac[3], int n_sink,
+                           int n_recent, uint8_t* tier, int32_t* counts, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
+ * sd_quantize_rows_int8 -- 8-bit storage of the T2 rows of one K or V cache.
+ * [HBM] Metodologia 1 (T2 keeps low-importance tokens at reduced precision, "e.g. 8-bit").
+ * The pages give no scheme; this is symmetric per-row absmax: a = max_j |x_j| (fp32);
+ * a == 0 gives scale 0 and zero codes; else scale = a/127 and
+ * code_j = clamp(rint(x_j * (127/a)), -127, 127), each division and the product a
+ * correctly rounded fp32 operation, rint = round half to even.
+ * x [B,Hkv,T,d] of dtype; tier [B,T] uint8; only rows with tier == 2 are written:
+ * codes [B,Hkv,T,d] int8, scales [B,Hkv,T] fp32.  Limits: d in {64, 128}.
+ */
+sd_status sd_quantize_rows_int8(const void* x, sd_dtype dtype, const uint8_t* tier, int B,
+                                int Hkv, int T, int d, int8_t* codes, float* scales,
+                                void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDGQA_SD_H */

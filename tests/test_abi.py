@@ -1,0 +1,75 @@
+"""The C-ABI library builds, loads and exports every symbol include/sd.h declares; host-side
+argument validation rejects bad calls before anything is launched.  No GPU needed: no
+call here reaches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from top_sparse_decode_gqa_gb300 import build, binding
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "sd.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sd_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from top_sparse_decode_gqa_gb300 import binding
+    decl = declared_functions()
+    assert decl == sorted(binding.EXPORTS)
+    for name in decl:
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.sd_version() == 100
+    assert lib.sd_status_string(0) == b"ok"
+    assert lib.sd_status_string(1) == b"invalid argument"
+    assert lib.sd_status_string(99) == b"unknown status"
+
+
+def test_host_validation_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+    dummy = P(16)
+    # k > N
+    assert lib.sd_topk(dummy, 1, 10, 11, dummy, None, 0, None) == 1
+    assert b"k (11)" in lib.sd_last_error_message()
+    # unsupported indexer dim
+    assert lib.sd_index_score(dummy, 1, dummy, 1, 1, 1, 1, 10, 96, dummy, None, None) == 2
+    # V out of range
+    assert lib.sd_index_score(dummy, 1, dummy, 1, 1, 1, 9, 10, 128, dummy, None, None) == 1
+    # ragged block pooling
+    assert lib.sd_block_pool(dummy, 1, 1, 1, 100, 128, 64, dummy, None) == 1
+    # non-monotone tier fractions
+    fr = (ctypes.c_double * 3)(0.5, 0.2, 0.9)
+    assert lib.sd_tier_classify(dummy, 1, 10, fr, 0, 0, dummy, dummy, None, 0, None) == 1
+    # empty work is a successful no-op
+    assert lib.sd_topk(None, 0, 10, 3, None, None, 0, None) == 0
+    assert lib.sd_index_score(None, 1, None, 1, 0, 8, 1, 100, 128, None, None, None) == 0
+
+
+def test_attend_validation_and_workspace_query(lib):
+    from top_sparse_decode_gqa_gb300.binding import sd_attend_args
+    a = sd_attend_args()
+    a.q = a.k_cache = a.v_cache = a.out = a.lse = 16
+    a.dtype, a.B, a.V, a.Hq, a.Hkv, a.d, a.T = 1, 2, 1, 32, 8, 128, 4096
+    a.pool_rows, a.n_idx, a.block, a.scale = 4096, 4096, 1, 0.1
+    # dense without idx is fine; workspace is a pure host computation
+    assert lib.sd_gather_attend_workspace_bytes(ctypes.byref(a)) >= 0
+    a.d = 96
+    assert lib.sd_gather_attend(ctypes.byref(a), None) == 2
+    a.d, a.V = 128, 9  # G*V = 36 > 32
+    assert lib.sd_gather_attend(ctypes.byref(a), None) == 2
+    a.V, a.n_idx = 1, 100  # dense mode with n_idx*block != T
+    assert lib.sd_gather_attend(ctypes.byref(a), None) == 1

@@ -7,11 +7,4 @@ loaded on first use and its absence is an error: there is no CPU fallback.
 """
 from . import workloads  # noqa: F401
 
-__all__ = ["workloads", "binding"]
-
-
-def __getattr__(name):
-    if name == "binding":
-        from . import binding
-        return binding
-    raise AttributeError(name)
+__all__ = ["workloads", "binding", "build"]

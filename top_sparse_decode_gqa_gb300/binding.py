@@ -1,0 +1,287 @@
+"""Thin Python binding over libsdgqa's C ABI (include/sd.h), with the same call names.
+
+Argument marshalling only: shapes are read off torch tensors, pointers and the current
+CUDA stream are passed through, and a non-OK status raises ``SdError``.  Every step of
+the computation runs in the library's CUDA kernels; there is no fallback of any kind, and
+a missing library is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsdgqa.so")
+
+SD_OK, SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED, SD_ERR_CUDA = 0, 1, 2, 3
+SD_F32, SD_BF16 = 0, 1
+SD_DEVERR_INDEX, SD_DEVERR_SLOT, SD_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+
+# Every symbol include/sd.h declares (checked by the tests against the built library).
+EXPORTS = (
+    "sd_version", "sd_status_string", "sd_last_error_message", "sd_index_score", "sd_block_pool",
+    "sd_topk_workspace_bytes", "sd_topk", "sd_gather_attend_workspace_bytes", "sd_gather_attend",
+    "sd_score_accumulate", "sd_tier_classify_workspace_bytes", "sd_tier_classify",
+    "sd_quantize_rows_int8",
+)
+
+
+class SdError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+class sd_attend_args(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+        ("k_host", ctypes.c_void_p), ("v_host", ctypes.c_void_p), ("slot_map", ctypes.c_void_p),
+        ("idx", ctypes.c_void_p), ("dtype", ctypes.c_int),
+        ("B", ctypes.c_int), ("V", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+        ("d", ctypes.c_int), ("T", ctypes.c_int), ("pool_rows", ctypes.c_int),
+        ("n_idx", ctypes.c_int), ("block", ctypes.c_int), ("scale", ctypes.c_float),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("logits", ctypes.c_void_p),
+        ("err_word", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t), ("splits", ctypes.c_int),
+    ]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libsdgqa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with top_sparse_decode_gqa_gb300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, Z, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_double
+        L.sd_version.restype = I
+        L.sd_status_string.restype = ctypes.c_char_p
+        L.sd_status_string.argtypes = [I]
+        L.sd_last_error_message.restype = ctypes.c_char_p
+        L.sd_index_score.argtypes = [P, I, P, I, I, I, I, I, I, P, P, P]
+        L.sd_block_pool.argtypes = [P, I, I, I, I, I, I, P, P]
+        L.sd_topk_workspace_bytes.argtypes = [I, I, I]
+        L.sd_topk_workspace_bytes.restype = Z
+        L.sd_topk.argtypes = [P, I, I, I, P, P, Z, P]
+        L.sd_gather_attend_workspace_bytes.argtypes = [ctypes.POINTER(sd_attend_args)]
+        L.sd_gather_attend_workspace_bytes.restype = Z
+        L.sd_gather_attend.argtypes = [ctypes.POINTER(sd_attend_args), P]
+        L.sd_score_accumulate.argtypes = [P, P, P, I, I, I, I, I, I, I, D, P, P, P]
+        L.sd_tier_classify_workspace_bytes.argtypes = [I, I]
+        L.sd_tier_classify_workspace_bytes.restype = Z
+        L.sd_tier_classify.argtypes = [P, I, I, P, I, I, P, P, P, Z, P]
+        L.sd_quantize_rows_int8.argtypes = [P, I, P, I, I, I, I, P, P, P]
+        for name in ("sd_index_score", "sd_block_pool", "sd_topk", "sd_gather_attend",
+                     "sd_score_accumulate", "sd_tier_classify", "sd_quantize_rows_int8"):
+            getattr(L, name).restype = I
+        _lib = L
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != SD_OK:
+        msg = lib().sd_last_error_message().decode() or lib().sd_status_string(status).decode()
+        raise SdError(status, f"{what}: {msg}")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SD_F32
+    if t.dtype == torch.bfloat16:
+        return SD_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def sd_version() -> int:
+    return lib().sd_version()
+
+
+def sd_index_score(q_idx: torch.Tensor, k_idx: torch.Tensor, scores: Optional[torch.Tensor] = None,
+                   err_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Indexer scores [B,Hkv,N] fp32 from q_idx [B,Hkv,V,dI] and k_idx [B,Hkv,N,dI]."""
+    _dev(q_idx, "q_idx")
+    _dev(k_idx, "k_idx")
+    B, Hkv, V, dI = q_idx.shape
+    N = k_idx.shape[2]
+    if tuple(k_idx.shape) != (B, Hkv, N, dI):
+        raise ValueError("k_idx shape must be [B,Hkv,N,dI] matching q_idx")
+    if scores is None:
+        scores = torch.empty((B, Hkv, N), dtype=torch.float32, device=k_idx.device)
+    _check(lib().sd_index_score(_ptr(q_idx), _dtype_code(q_idx), _ptr(k_idx), _dtype_code(k_idx), B,
+                                Hkv, V, N, dI, _ptr(scores), _ptr(err_word), _stream(stream)),
+           "sd_index_score")
+    return scores
+
+
+def sd_block_pool(k_idx: torch.Tensor, block: int, pooled: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
+    """Mean-pooled block keys [B,Hkv,T/block,dI] fp32 of k_idx [B,Hkv,T,dI]."""
+    _dev(k_idx, "k_idx")
+    B, Hkv, T, dI = k_idx.shape
+    if pooled is None:
+        pooled = torch.empty((B, Hkv, T // block, dI), dtype=torch.float32, device=k_idx.device)
+    _check(lib().sd_block_pool(_ptr(k_idx), _dtype_code(k_idx), B, Hkv, T, dI, block, _ptr(pooled),
+                               _stream(stream)), "sd_block_pool")
+    return pooled
+
+
+def sd_topk(scores: torch.Tensor, k: int, idx: Optional[torch.Tensor] = None,
+            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Top-k indices (ascending, ties to the lower index) of each row of scores [..., N]."""
+    _dev(scores, "scores")
+    if scores.dtype != torch.float32:
+        raise TypeError("scores must be float32")
+    N = scores.shape[-1]
+    rows = scores.numel() // N if N > 0 else math.prod(scores.shape[:-1])
+    if idx is None:
+        idx = torch.empty(scores.shape[:-1] + (k,), dtype=torch.int32, device=scores.device)
+    ws_bytes = lib().sd_topk_workspace_bytes(rows, N, k)
+    if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=scores.device)
+    _check(lib().sd_topk(_ptr(scores), rows, N, k, _ptr(idx), _ptr(workspace), ws_bytes,
+                         _stream(stream)), "sd_topk")
+    return idx
+
+
+def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=None, scale=None,
+                     k_host=None, v_host=None, slot_map=None, out=None, lse=None, logits=None,
+                     want_logits=False, err_word=None, splits=0) -> tuple:
+    """Fill an sd_attend_args from tensors; returns (args, out, lse, logits)."""
+    _dev(q, "q")
+    B, V, Hq, d = q.shape
+    Hkv = k_cache.shape[1]
+    pool_rows = k_cache.shape[2]
+    if T is None:
+        T = k_host.shape[2] if k_host is not None else pool_rows
+    if idx is not None:
+        _dev(idx, "idx")
+        n_idx = idx.shape[-1]
+    elif n_idx is None:
+        n_idx = T // block
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, V, Hq, d), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, V, Hq), dtype=torch.float32, device=dev)
+    if logits is None and want_logits:
+        logits = torch.empty((B, V, Hq, n_idx * block), dtype=torch.float32, device=dev)
+    for name, t in (("k_host", k_host), ("v_host", v_host)):
+        if t is not None and (t.is_cuda or not t.is_pinned() or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous pinned host tensor")
+    a = sd_attend_args()
+    a.q, a.k_cache, a.v_cache = q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr()
+    a.k_host = k_host.data_ptr() if k_host is not None else None
+    a.v_host = v_host.data_ptr() if v_host is not None else None
+    a.slot_map = slot_map.data_ptr() if slot_map is not None else None
+    a.idx = idx.data_ptr() if idx is not None else None
+    a.dtype = _dtype_code(q)
+    a.B, a.V, a.Hq, a.Hkv, a.d, a.T = B, V, Hq, Hkv, d, T
+    a.pool_rows, a.n_idx, a.block = pool_rows, n_idx, block
+    a.scale = scale
+    a.out, a.lse = out.data_ptr(), lse.data_ptr()
+    a.logits = logits.data_ptr() if logits is not None else None
+    a.err_word = err_word.data_ptr() if err_word is not None else None
+    a.splits = splits
+    return a, out, lse, logits
+
+
+def sd_gather_attend_workspace_bytes(args: sd_attend_args) -> int:
+    return lib().sd_gather_attend_workspace_bytes(ctypes.byref(args))
+
+
+def sd_gather_attend(args: sd_attend_args, workspace: Optional[torch.Tensor] = None,
+                     stream=None) -> None:
+    """Runs one sd_gather_attend call described by `args` (see make_attend_args)."""
+    need = sd_gather_attend_workspace_bytes(args)
+    if need:
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            raise ValueError(f"sd_gather_attend needs a workspace of {need} bytes")
+        args.workspace = workspace.data_ptr()
+        args.workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().sd_gather_attend(ctypes.byref(args), _stream(stream)), "sd_gather_attend")
+
+
+def gather_attend(q, k_cache, v_cache, idx=None, workspace=None, stream=None, **kw):
+    """Convenience wrapper: builds the args, sizes a workspace if none is given, runs the
+    call and returns (out, lse, logits)."""
+    a, out, lse, logits = make_attend_args(q, k_cache, v_cache, idx, **kw)
+    need = sd_gather_attend_workspace_bytes(a)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    sd_gather_attend(a, workspace, stream)
+    return out, lse, logits
+
+
+def sd_score_accumulate(logits: torch.Tensor, lse: torch.Tensor, idx: Optional[torch.Tensor],
+                        s: torch.Tensor, Hkv: int, block: int, weight: float,
+                        err_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """s [B,T] fp64 += weight * sum over query rows of the softmax weight of each selected row."""
+    _dev(logits, "logits")
+    _dev(lse, "lse")
+    _dev(s, "s")
+    if s.dtype != torch.float64:
+        raise TypeError("s must be float64")
+    B, V, Hq, n_rows = logits.shape
+    T = s.shape[1]
+    n_idx = idx.shape[-1] if idx is not None else n_rows // block
+    _check(lib().sd_score_accumulate(_ptr(logits), _ptr(lse), _ptr(idx), B, V, Hq, Hkv, n_idx, block,
+                                     T, float(weight), _ptr(s), _ptr(err_word), _stream(stream)),
+           "sd_score_accumulate")
+    return s
+
+
+def sd_tier_classify(s: torch.Tensor, cum_frac: Sequence[float] = (0.2, 0.6, 0.9), n_sink: int = 0,
+                     n_recent: int = 0, tier: Optional[torch.Tensor] = None,
+                     counts: Optional[torch.Tensor] = None, stream=None):
+    """(tier uint8 [B,T], counts int32 [B,4]) from the importance score s [B,T] fp64."""
+    _dev(s, "s")
+    B, T = s.shape
+    if tier is None:
+        tier = torch.empty((B, T), dtype=torch.uint8, device=s.device)
+    if counts is None:
+        counts = torch.empty((B, 4), dtype=torch.int32, device=s.device)
+    fr = (ctypes.c_double * 3)(*[float(f) for f in cum_frac])
+    ws_bytes = lib().sd_tier_classify_workspace_bytes(B, T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=s.device) if ws_bytes else None
+    _check(lib().sd_tier_classify(_ptr(s), B, T, fr, n_sink, n_recent, _ptr(tier), _ptr(counts),
+                                  _ptr(ws), ws_bytes, _stream(stream)), "sd_tier_classify")
+    return tier, counts
+
+
+def sd_quantize_rows_int8(x: torch.Tensor, tier: torch.Tensor, codes: Optional[torch.Tensor] = None,
+                          scales: Optional[torch.Tensor] = None, stream=None):
+    """int8 codes [B,Hkv,T,d] and fp32 scales [B,Hkv,T] of the rows whose tier is 2."""
+    _dev(x, "x")
+    _dev(tier, "tier")
+    B, Hkv, T, d = x.shape
+    if codes is None:
+        codes = torch.zeros((B, Hkv, T, d), dtype=torch.int8, device=x.device)
+    if scales is None:
+        scales = torch.zeros((B, Hkv, T), dtype=torch.float32, device=x.device)
+    _check(lib().sd_quantize_rows_int8(_ptr(x), _dtype_code(x), _ptr(tier), B, Hkv, T, d, _ptr(codes),
+                                       _ptr(scales), _stream(stream)), "sd_quantize_rows_int8")
+    return codes, scales

@@ -1,0 +1,183 @@
+// sd_common.cuh -- device helpers shared by the libsdgqa kernels (sm_103a).
+//
+// Inline PTX for the Blackwell data-movement primitives the kernels use: mbarrier
+// (init / expect-tx / bounded try_wait), 1-D bulk copies global -> shared completed on an
+// mbarrier (the TMA unit's untiled path), and 16-byte cp.async.  Every wait is bounded by
+// a wall-clock deadline read from %globaltimer; a wait that runs out reports
+// SD_DEVERR_TIMEOUT instead of hanging.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sd.h"
+
+#define SD_DEVINL __device__ __forceinline__
+
+namespace sd {
+
+// Deadline for any single bounded wait: 1 s of wall-clock time.
+constexpr uint64_t kWaitDeadlineNs = 1000000000ull;
+
+SD_DEVINL uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+SD_DEVINL void report(int32_t* err_word, int bits) {
+    if (err_word != nullptr) atomicOr(reinterpret_cast<int*>(err_word), bits);
+}
+
+SD_DEVINL uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+SD_DEVINL void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+SD_DEVINL void fence_mbarrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before later
+// async-proxy (bulk copy) accesses to the same memory.
+SD_DEVINL void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+SD_DEVINL void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+SD_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.  Returns false when the
+// deadline passed first.
+SD_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitDeadlineNs) return false;
+    }
+}
+
+// 1-D bulk copy (TMA, untiled) of `bytes` (multiple of 16, both addresses 16-byte
+// aligned) from global to this CTA's shared memory, completing on `bar`.
+SD_DEVINL void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// ---------------------------------------------------------------- cp.async (16 B)
+
+SD_DEVINL void cp_async16(void* dst_smem, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src)
+                 : "memory");
+}
+SD_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+SD_DEVINL void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------- element access
+
+// Two bfloat16 packed in a 32-bit word -> two fp32 (exact).
+SD_DEVINL float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+SD_DEVINL float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+SD_DEVINL float load_elem(const void* base, int dtype, size_t i) {
+    if (dtype == SD_F32) return reinterpret_cast<const float*>(base)[i];
+    const uint16_t b = reinterpret_cast<const uint16_t*>(base)[i];
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// 16 bytes of storage -> fp32 values (8 for bf16, 4 for fp32).
+template <typename T>
+struct Unpack16;
+template <>
+struct Unpack16<float> {
+    static constexpr int kElems = 4;
+    SD_DEVINL static void run(const uint4& r, float* x) {
+        x[0] = __uint_as_float(r.x);
+        x[1] = __uint_as_float(r.y);
+        x[2] = __uint_as_float(r.z);
+        x[3] = __uint_as_float(r.w);
+    }
+};
+struct bf16_t {
+    uint16_t bits;
+};
+template <>
+struct Unpack16<bf16_t> {
+    static constexpr int kElems = 8;
+    SD_DEVINL static void run(const uint4& r, float* x) {
+        x[0] = bf16lo(r.x);
+        x[1] = bf16hi(r.x);
+        x[2] = bf16lo(r.y);
+        x[3] = bf16hi(r.y);
+        x[4] = bf16lo(r.z);
+        x[5] = bf16hi(r.z);
+        x[6] = bf16lo(r.w);
+        x[7] = bf16hi(r.w);
+    }
+};
+
+SD_DEVINL uint4 lds128(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// ---------------------------------------------------------------- warp reductions
+
+SD_DEVINL float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+SD_DEVINL float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+SD_DEVINL uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Order-preserving map of fp32 to uint32 (a < b as floats <=> key(a) < key(b)), with
+// -0.0 mapped like +0.0 so the two compare equal.
+SD_DEVINL uint32_t float_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u << 1) == 0u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Same for fp64 -> uint64.
+SD_DEVINL uint64_t double_key(double f) {
+    uint64_t u = static_cast<uint64_t>(__double_as_longlong(f));
+    if ((u << 1) == 0ull) u = 0ull;
+    return (u & 0x8000000000000000ull) ? ~u : (u | 0x8000000000000000ull);
+}
+
+}  // namespace sd

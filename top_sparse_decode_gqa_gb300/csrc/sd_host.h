@@ -1,0 +1,58 @@
+// sd_host.h -- host-side helpers shared by the libsdgqa entry points (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cstdarg>
+#include <cstdio>
+
+#include "../../include/sd.h"
+
+namespace sd {
+
+// Records the detail of a failed call for sd_last_error_message() (thread-local).
+void set_error(const char* fmt, ...);
+void clear_error();
+
+// Number of SMs of the current device (queried once per device, then cached).
+int num_sms();
+
+// Maximum opt-in dynamic shared memory per block of the current device (cached).
+int max_smem_optin();
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline bool valid_dtype(int dt) { return dt == SD_F32 || dt == SD_BF16; }
+inline int dtype_bytes(int dt) { return dt == SD_F32 ? 4 : 2; }
+
+// Maps the last launch error to a status (and records it).
+inline sd_status launch_status(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("%s: launch failed: %s", what, cudaGetErrorString(e));
+        return SD_ERR_CUDA;
+    }
+    return SD_OK;
+}
+
+}  // namespace sd
+
+#define SD_REQUIRE(cond, ...)                 \
+    do {                                      \
+        if (!(cond)) {                        \
+            ::sd::set_error(__VA_ARGS__);     \
+            return SD_ERR_INVALID_ARG;        \
+        }                                     \
+    } while (0)
+
+#define SD_CUDA_CHECK(call, what)                                                     \
+    do {                                                                              \
+        cudaError_t e_ = (call);                                                      \
+        if (e_ != cudaSuccess) {                                                      \
+            ::sd::set_error("%s: %s", what, cudaGetErrorString(e_));                  \
+            return SD_ERR_CUDA;                                                       \
+        }                                                                             \
+    } while (0)
