@@ -154,7 +154,8 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         const uint32_t eqm = __ballot_sync(0xffffffffu, is_eq);
         const bool sel = is_gt || (is_eq && (int)(eq_seen + __popc(eqm & lt)) < krem);
         const uint32_t selm = __ballot_sync(0xffffffffu, sel);
-        if (sel) orow[pos + __popc(selm & lt)] = i;
+        const uint32_t at = pos + __popc(selm & lt);
+        if (sel && at < (uint32_t)k) orow[at] = i;
         pos += __popc(selm);
         eq_seen += __popc(eqm);
     }
