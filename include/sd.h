@@ -122,7 +122,8 @@ sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx, voi
  *
  * For query row (b, v, h) with kvh = h / (Hq/Hkv):
  *   rows_j = idx[b,kvh, j / block] * block + j % block, j < n_idx*block  (idx == NULL:
- *            dense, rows_j = j and n_idx*block must equal T)
+ *            dense, rows_j = j and n_idx*block must equal T; n_idx == 0 is an empty
+ *            selection whatever idx is)
  *   z_j    = scale * q[b,v,h,:] . K[b,kvh,rows_j,:]
  *   out[b,v,h,:] = sum_j softmax(z)_j V[b,kvh,rows_j,:],  lse[b,v,h] = log sum_j exp(z_j)
  *   logits[b,v,h,j] = z_j (optional).  No rows: out = 0, lse = -inf.

@@ -434,7 +434,7 @@ static sd_status validate_attend(const sd_attend_args* a) {
     SD_REQUIRE(valid_dtype(a->dtype), "sd_gather_attend: bad dtype");
     SD_REQUIRE(a->block >= 1 && a->n_idx >= 0, "sd_gather_attend: bad block / n_idx");
     SD_REQUIRE((long)a->n_idx * a->block <= (1L << 30), "sd_gather_attend: selection too large");
-    if (a->idx == nullptr)
+    if (a->idx == nullptr && a->n_idx > 0)
         SD_REQUIRE((long)a->n_idx * a->block == a->T, "sd_gather_attend: dense mode needs n_idx*block == T");
     if (a->d != 64 && a->d != 128) {
         set_error("sd_gather_attend: d must be 64 or 128 (got %d)", a->d);
@@ -459,8 +459,6 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
     if (vs != SD_OK) return vs;
     if (a->B == 0) return SD_OK;
     SD_REQUIRE(a->q && a->out && a->lse, "sd_gather_attend: null q/out/lse");
-    SD_REQUIRE(a->n_idx == 0 || a->idx != nullptr || a->T == (long)a->n_idx * a->block,
-               "sd_gather_attend: idx");
     SplitPlan sp = plan_splits(a);
     AttendParams p{};
     p.q = a->q;

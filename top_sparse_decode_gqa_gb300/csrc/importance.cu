@@ -296,7 +296,7 @@ extern "C" sd_status sd_score_accumulate(const float* logits, const float* lse, 
     SD_REQUIRE(B >= 0 && V >= 1 && Hq >= 1 && Hkv >= 1 && T >= 0 && n_idx >= 0 && block >= 1,
                "sd_score_accumulate: bad sizes");
     SD_REQUIRE(Hq % Hkv == 0, "sd_score_accumulate: Hq must be a multiple of Hkv");
-    if (idx == nullptr)
+    if (idx == nullptr && n_idx > 0)
         SD_REQUIRE((long)n_idx * block == T, "sd_score_accumulate: dense mode needs n_idx*block == T");
     const long n_rows = (long)n_idx * block;
     if (B == 0 || n_rows == 0) return SD_OK;
