@@ -163,6 +163,24 @@ size_t sd_gather_attend_workspace_bytes(const sd_attend_args* args);
 sd_status sd_gather_attend(const sd_attend_args* args, void* stream);
 
 /*
+ * sd_gather_attend_noalloc -- sd_gather_attend for callers that cannot allocate device
+ * memory.  The source pages have no counterpart: this is a library convenience.
+ * Some callers cannot provide the split-K scratch buffer: a plugin that only receives
+ * input and output pointers from a framework owning all device memory, an engine that
+ * fixes its memory budget at start-up, or a C caller with no allocator at hand.  This call
+ * computes exactly what sd_gather_attend computes (same arguments, same split plan) but
+ * ignores args->workspace / workspace_bytes and uses a 16 MiB array of device memory
+ * compiled into the library, which every GPU that loads the library holds until exit.
+ * It allocates nothing.  The array's device address is looked up on the first call made
+ * on each device (with that device current): make that first call before any stream
+ * capture.  All calls share the array and it keeps the last call's contents; nothing in it
+ * needs to start at zero, but calls whose kernels overlap on the GPU race on it.  A request
+ * whose split-K partials need more than 16 MiB returns SD_ERR_INVALID_ARG without
+ * launching (pass a smaller `splits`, or use sd_gather_attend with a workspace).
+ */
+sd_status sd_gather_attend_noalloc(const sd_attend_args* args, void* stream);
+
+/*
  * sd_score_accumulate -- one layer's term of the cumulative attention-importance score.
  * [HBM] Metodologia 2:  s_i(t) = s_i(t-1) + (1/|L|) sum_l (1/H) sum_h alpha_{l,h}(t)[i].
  * Adds, for every query row (b, v, h) and selected row j (expanded as in

@@ -26,7 +26,7 @@ EXPORTS = (
     "sd_version", "sd_status_string", "sd_last_error_message", "sd_index_score", "sd_block_pool",
     "sd_topk_workspace_bytes", "sd_topk", "sd_gather_attend_workspace_bytes", "sd_gather_attend",
     "sd_score_accumulate", "sd_tier_classify_workspace_bytes", "sd_tier_classify",
-    "sd_quantize_rows_int8",
+    "sd_quantize_rows_int8", "sd_gather_attend_noalloc",
 )
 
 
@@ -73,13 +73,15 @@ def lib() -> ctypes.CDLL:
         L.sd_gather_attend_workspace_bytes.argtypes = [ctypes.POINTER(sd_attend_args)]
         L.sd_gather_attend_workspace_bytes.restype = Z
         L.sd_gather_attend.argtypes = [ctypes.POINTER(sd_attend_args), P]
+        L.sd_gather_attend_noalloc.argtypes = [ctypes.POINTER(sd_attend_args), P]
         L.sd_score_accumulate.argtypes = [P, P, P, I, I, I, I, I, I, I, D, P, P, P]
         L.sd_tier_classify_workspace_bytes.argtypes = [I, I]
         L.sd_tier_classify_workspace_bytes.restype = Z
         L.sd_tier_classify.argtypes = [P, I, I, P, I, I, P, P, P, Z, P]
         L.sd_quantize_rows_int8.argtypes = [P, I, P, I, I, I, I, P, P, P]
         for name in ("sd_index_score", "sd_block_pool", "sd_topk", "sd_gather_attend",
-                     "sd_score_accumulate", "sd_tier_classify", "sd_quantize_rows_int8"):
+                     "sd_score_accumulate", "sd_tier_classify", "sd_quantize_rows_int8",
+                     "sd_gather_attend_noalloc"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -223,6 +225,14 @@ def sd_gather_attend(args: sd_attend_args, workspace: Optional[torch.Tensor] = N
         args.workspace = workspace.data_ptr()
         args.workspace_bytes = workspace.numel() * workspace.element_size()
     _check(lib().sd_gather_attend(ctypes.byref(args), _stream(stream)), "sd_gather_attend")
+
+
+def sd_gather_attend_noalloc(args: sd_attend_args, stream=None) -> None:
+    """Runs one sd_gather_attend_noalloc call: the same computation as sd_gather_attend,
+    with the split-K scratch taken from the library's own static device array (for callers
+    that cannot allocate); args.workspace is ignored."""
+    _check(lib().sd_gather_attend_noalloc(ctypes.byref(args), _stream(stream)),
+           "sd_gather_attend_noalloc")
 
 
 def gather_attend(q, k_cache, v_cache, idx=None, workspace=None, stream=None, **kw):
