@@ -168,57 +168,190 @@ def profiled_traffic(workload: str, kernel: str, digest: str):
 # ----------------------------------------------------------------------------- the step
 
 
+class StepMarks:
+    """CUDA events of one timed step: start/end of the step and a (before, after) pair
+    around every launch of the step's dominant kernel, plus named phase boundaries."""
+
+    def __init__(self, n_dominant: int, phases=()):
+        import torch
+        ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        self.start, self.end = ev(), ev()
+        self.dom = [(ev(), ev()) for _ in range(n_dominant)]
+        self.phase = {name: ev() for name in phases}
+
+    def step_ms(self):
+        return self.start.elapsed_time(self.end)
+
+    def dominant_ms(self):
+        return [a.elapsed_time(b) for a, b in self.dom]
+
+
 class SparseDecodeStep:
-    """Device buffers and the launch sequence of one decode step (all inputs resident)."""
+    """One sparse decode step (indexer -> top-k -> gather-attend), inputs resident.  For a
+    tiered workload the full K/V cache stays in pinned host memory and only the resident
+    share sits in the HBM pool."""
+
+    dominant = "sd_index_score"
+    phases = ("after_topk",)
 
     def __init__(self, w, x, device):
         import torch
         from top_sparse_decode_gqa_gb300 import binding as sd
         self.sd, self.w, self.dev = sd, w, device
-        g = {k: v.to(device) for k, v in x.items() if isinstance(v, torch.Tensor)}
-        self.q_idx, self.k_idx, self.q = g["q_idx"], g["k_idx"], g["q"]
-        self.k, self.v = g["k"], g["v"]
+        self.tiered = w.resident_frac < 1.0
+        self.q_idx, self.k_idx, self.q = (x[k].to(device) for k in ("q_idx", "k_idx", "q"))
         self.scores = torch.empty(w.B, w.Hkv, w.N, dtype=torch.float32, device=device)
         self.idx = torch.empty(w.B, w.Hkv, w.k, dtype=torch.int32, device=device)
+        self.key_hist = sd.key_hist_buffer(w.B * w.Hkv, device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        if self.tiered:
+            self.k_cache, self.v_cache = x["k_pool"].to(device), x["v_pool"].to(device)
+            self.slot_map = x["slot_map"].to(device)
+            self.k_host, self.v_host = x["k"].pin_memory(), x["v"].pin_memory()
+            kw = dict(k_host=self.k_host, v_host=self.v_host, slot_map=self.slot_map)
+        else:
+            self.k_cache, self.v_cache = x["k"].to(device), x["v"].to(device)
+            kw = {}
         self.args, self.out, self.lse, _ = sd.make_attend_args(
-            self.q, self.k, self.v, self.idx, block=w.block, T=w.T, err_word=self.err)
+            self.q, self.k_cache, self.v_cache, self.idx, block=w.block, T=w.T, err_word=self.err, **kw)
         need = sd.sd_gather_attend_workspace_bytes(self.args)
-        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
-        self.splits_merge = need > 0
+        self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=device)
         self.keys = self.k_idx
         if w.block > 1:
             self.keys = sd.sd_block_pool(self.k_idx, w.block)
+        self.host_rows = None
 
-    @property
-    def launches_per_step(self) -> int:
-        return 3 + (1 if self.splits_merge else 0)
+    launches_per_step = 3
+    dominant_per_step = 1
 
-    def run(self, ev=None):
+    def run(self, m: "StepMarks" = None):
         sd = self.sd
-        if ev is not None:
-            ev[0].record()
-        sd.sd_index_score(self.q_idx, self.keys, self.scores, self.err)
-        if ev is not None:
-            ev[1].record()
-        sd.sd_topk(self.scores, self.w.k, self.idx)
-        if ev is not None:
-            ev[2].record()
+        if m is not None:
+            m.start.record()
+            m.dom[0][0].record()
+        sd.sd_index_score(self.q_idx, self.keys, self.scores, self.err, key_hist=self.key_hist)
+        if m is not None:
+            m.dom[0][1].record()
+        sd.sd_topk(self.scores, self.w.k, self.idx, key_hist=self.key_hist)
+        if m is not None:
+            m.phase["after_topk"].record()
         sd.sd_gather_attend(self.args, self.ws)
-        if ev is not None:
-            ev[3].record()
+        if m is not None:
+            m.end.record()
 
-    def algorithmic_bytes(self):
-        """(index_score bytes per launch, whole-step bytes): what the method must move."""
+    def after_warmup(self):
+        """Counts the selected rows that live in host memory (fixed by the inputs)."""
+        if self.tiered:
+            import torch
+            rows = self.idx.long() * self.w.block
+            b = torch.arange(self.w.B, device=self.dev)[:, None, None]
+            self.host_rows = int((self.slot_map[b, rows] < 0).sum().item())
+
+    def bytes(self):
+        """Algorithmic bytes: per launch of the dominant kernel; per step from HBM and from
+        host memory (what the method must move: keys, selected K/V rows, queries, outputs)."""
         w = self.w
         e = w.elem_bytes
         key_bytes = w.B * w.Hkv * w.N * w.dI * (4 if w.block > 1 else e)
         q_idx_bytes = w.B * w.Hkv * w.V * w.dI * e
         score_bytes = w.B * w.Hkv * w.N * 4
-        kv_bytes = w.B * w.Hkv * w.n_rows * w.d * e * 2
+        row_bytes = w.d * e * 2
+        kv_rows = w.B * w.Hkv * w.n_rows
+        host_rows = self.host_rows or 0
         q_bytes = w.B * w.V * w.Hq * w.d * e
         out_bytes = w.B * w.V * w.Hq * (w.d + 1) * 4 + w.B * w.Hkv * w.k * 4
-        return key_bytes + q_idx_bytes + score_bytes, key_bytes + q_idx_bytes + kv_bytes + q_bytes + out_bytes
+        hbm = key_bytes + q_idx_bytes + (kv_rows - host_rows) * row_bytes + q_bytes + out_bytes
+        return {"dominant": key_bytes + q_idx_bytes + score_bytes, "hbm": hbm,
+                "host": host_rows * row_bytes}
+
+
+class DenseScoringStep:
+    """One decode step of the importance-scoring workload: for every layer, dense attention
+    over all cached rows (logits kept) and that layer's term of the importance score."""
+
+    dominant = "sd_gather_attend"
+    phases = ()
+
+    def __init__(self, w, x, device):
+        import torch
+        from top_sparse_decode_gqa_gb300 import binding as sd
+        self.sd, self.w, self.dev = sd, w, device
+        self.ks = [k.to(device) for k in x["k"]]
+        self.vs = [v.to(device) for v in x["v"]]
+        self.qall = x["q"].to(device)              # [steps, layers, B, V, Hq, d]
+        self.s = torch.zeros(w.B, w.T, dtype=torch.float64, device=device)
+        self.logits = torch.empty(w.B, w.V, w.Hq, w.T, dtype=torch.float32, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.q = torch.empty_like(self.qall[0, 0])
+        self.args = []
+        for layer in range(w.layers):
+            a, out, lse, _ = sd.make_attend_args(self.q, self.ks[layer], self.vs[layer], None, T=w.T,
+                                                 logits=self.logits, err_word=self.err)
+            self.args.append((a, out, lse))
+        need = sd.sd_gather_attend_workspace_bytes(self.args[0][0])
+        self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=device)
+        self.step_no = 0
+        self.weight = 1.0 / (w.layers * w.Hq)
+        self.out, self.lse = self.args[-1][1], self.args[-1][2]
+
+    @property
+    def launches_per_step(self):
+        return 2 * self.w.layers
+
+    @property
+    def dominant_per_step(self):
+        return self.w.layers
+
+    def run(self, m: "StepMarks" = None):
+        sd, w = self.sd, self.w
+        if m is not None:
+            m.start.record()
+        qs = self.qall[self.step_no % w.steps]
+        self.step_no += 1
+        for layer in range(w.layers):
+            a, out, lse = self.args[layer]
+            a.q = qs[layer].data_ptr()
+            if m is not None:
+                m.dom[layer][0].record()
+            sd.sd_gather_attend(a, self.ws)
+            if m is not None:
+                m.dom[layer][1].record()
+            sd.sd_score_accumulate(self.logits, lse, None, self.s, w.Hkv, 1, self.weight, err_word=self.err)
+        if m is not None:
+            m.end.record()
+
+    def after_warmup(self):
+        pass
+
+    def bytes(self):
+        w = self.w
+        kv = w.B * w.Hkv * w.T * w.d * w.elem_bytes * 2
+        q = w.B * w.V * w.Hq * w.d * w.elem_bytes
+        logits = w.B * w.V * w.Hq * w.T * 4
+        out = w.B * w.V * w.Hq * (w.d + 1) * 4
+        # dominant kernel per launch: one layer's K and V, its query, logits and outputs out
+        return {"dominant": kv + q + logits + out, "hbm": w.layers * (kv + q + out) + w.B * w.T * 8 * 2,
+                "host": 0}
+
+
+def make_step(w, x, device):
+    return DenseScoringStep(w, x, device) if w.layers > 1 else SparseDecodeStep(w, x, device)
+
+
+def host_link_gbs(device, nbytes=512 << 20):
+    """Host->device bandwidth of one pinned copy (CUDA events), the host-row roofline term."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    for _ in range(2):
+        d.copy_(h, non_blocking=True)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(3):
+        d.copy_(h, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    return 3 * nbytes / (a.elapsed_time(b) / 1e3) / 1e9
 
 
 # ----------------------------------------------------------------------------- arms
@@ -241,21 +374,26 @@ def run_ours(args):
         dist.barrier()
     w = WORKLOADS[args.workload]
     x = generate(w)
-    step = SparseDecodeStep(w, x, device)
-    stream = torch.cuda.current_stream()
+    step = make_step(w, x, device)
     props = torch.cuda.get_device_properties(device)
     flush = torch.empty(2 * max(int(getattr(props, "L2_cache_size", 0)), 128 << 20), dtype=torch.uint8,
                         device=device)
 
+    def clean_l2():
+        # write a buffer of 2x L2, then read it back so the step starts on a cold, clean L2
+        flush.fill_(1)
+        flush.view(torch.int32).sum()
+
     for _ in range(args.warmup):
-        flush.zero_()
+        clean_l2()
         step.run()
     torch.cuda.synchronize()
     if int(step.err.item()) != 0:
         raise RuntimeError(f"device error word {int(step.err.item())}")
+    step.after_warmup()
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    marks = [StepMarks(step.dominant_per_step, step.phases) for _ in range(K)]
     clocks = ClockSampler(local)
     clocks.start()
     if world > 1:
@@ -263,33 +401,51 @@ def run_ours(args):
     torch.cuda.synchronize()
     clocks.mark(True)
     for i in range(K):
-        flush.zero_()
-        step.run(evs[i])
+        clean_l2()
+        step.run(marks[i])
     torch.cuda.synchronize()
     clocks.mark(False)
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
 
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    idx_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    topk_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    att_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    step_ms = [m.step_ms() for m in marks]
+    dom_ms = [t for m in marks for t in m.dominant_ms()]
     total_s = reduce_max(sum(step_ms) / 1e3, world, device)
-    queries = w.queries_per_step * K
-    value = aggregate(queries, world, total_s)
+    value = aggregate(w.queries_per_step * K, world, total_s)
     ms_per_step = total_s * 1e3 / K
 
-    # ---- end to end through the public API: host query in, host result out
-    e2e = measure_e2e(step, w, x, flush, K=min(K, 200))
+    e2e = measure_e2e(step, w, x, clean_l2, K=min(K, 200))
 
     peak, peak_kind = load_peaks()
-    idx_bytes, step_bytes = step.algorithmic_bytes()
-    idx_avg_s = statistics.mean(idx_ms) / 1e3
-    achieved = idx_bytes / idx_avg_s / 1e9
-    digest = source_digest("index_score.cu", "sd_common.cuh")
-    traffic = profiled_traffic(args.workload, "index_score", digest)
-    step_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
+    by = step.bytes()
+    dom_s = statistics.mean(dom_ms) / 1e3
+    achieved = by["dominant"] / dom_s / 1e9
+    if isinstance(step, SparseDecodeStep):
+        kernel_file, kernel_tag = ("index_score.cu", "sd_common.cuh"), "index_score"
+    else:
+        kernel_file, kernel_tag = ("gather_attend.cu", "sd_common.cuh"), "gather_attend"
+    traffic = profiled_traffic(args.workload, kernel_tag, source_digest(*kernel_file))
+    step_s = ms_per_step / 1e3
+    step_roof = {"bound": "hbm", "hbm_bytes": by["hbm"], "unit": "GB/s",
+                 "achieved": round(by["hbm"] / step_s / 1e9, 1)}
+    t_roof = by["hbm"] / (peak * 1e9)
+    if by["host"]:
+        host_gbs = host_link_gbs(device)
+        t_roof += by["host"] / (host_gbs * 1e9)
+        step_roof.update({"host_bytes": by["host"], "host_link_gbs_measured": round(host_gbs, 1),
+                          "bound": "hbm+host"})
+    step_roof["t_roof_us"] = round(t_roof * 1e6, 2)
+    step_roof["frac"] = round(t_roof / step_s, 4)
+    if isinstance(step, SparseDecodeStep):
+        after_topk = [m.dom[0][1].elapsed_time(m.phase["after_topk"]) for m in marks]
+        tail = [m.phase["after_topk"].elapsed_time(m.end) for m in marks]
+        step_roof["kernel_us"] = {"index_score": round(statistics.mean(dom_ms) * 1e3, 2),
+                                  "topk": round(statistics.mean(after_topk) * 1e3, 2),
+                                  "gather_attend": round(statistics.mean(tail) * 1e3, 2)}
+    else:
+        step_roof["kernel_us"] = {"gather_attend_per_layer": round(statistics.mean(dom_ms) * 1e3, 2),
+                                  "layers": w.layers}
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -301,23 +457,19 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic (seeded; integer indexer keys in [-8,8], N(0,1) q/K/V, 2% planted heavy hitters)",
+        "dtype": "f32" if w.dtype == "f32" else "bf16",
+        "data": "synthetic (seeded; integer indexer keys in [-8,8], N(0,1) q/K/V)",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "T": w.T,
-                   "k": w.k, "block": w.block, "V": w.V, "queries_per_step": w.queries_per_step,
-                   "l2": "flushed between timed steps (write of 2x L2 outside the events)",
+                   "k": w.k, "block": w.block, "V": w.V, "layers": w.layers,
+                   "queries_per_step": w.queries_per_step,
+                   "l2": "flushed between timed steps: 2x L2 written then read, outside the events",
                    "parallelism": f"replica x{world} (each rank its own batch)"},
-        "roofline": {"bound": "hbm", "kernel": "sd_index_score", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": step.dominant, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
-                     "algorithmic_bytes_per_launch": idx_bytes,
-                     "avg_launch_us": round(idx_avg_s * 1e6, 2)},
-        "step_roofline": {"bound": "hbm", "algorithmic_bytes": step_bytes,
-                          "achieved": round(step_gbs, 1), "unit": "GB/s",
-                          "frac": round(step_gbs / peak, 4),
-                          "kernel_us": {"index_score": round(statistics.mean(idx_ms) * 1e3, 2),
-                                        "topk": round(statistics.mean(topk_ms) * 1e3, 2),
-                                        "gather_attend": round(statistics.mean(att_ms) * 1e3, 2)}},
+                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)", "traffic": traffic,
+                     "algorithmic_bytes_per_launch": by["dominant"],
+                     "avg_launch_us": round(dom_s * 1e6, 2)},
+        "step_roofline": step_roof,
         "e2e": e2e,
         "gpu_launches": step.launches_per_step * K,
         "clocks": clk,
@@ -330,32 +482,33 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def measure_e2e(step, w, x, flush, K):
+def measure_e2e(step, w, x, clean_l2, K):
     """The same metric through the public calls with host buffers: every step copies the
-    step's query tensors from pinned host memory, runs the three calls, and reads the
-    result (out, lse, selected indices) back into pinned host memory."""
+    step's query tensors from pinned host memory, runs the calls, and reads the result
+    (attention output, lse and, for sparse steps, the selected indices) back into pinned
+    host memory; host wall clock per step, including the copies and the final sync."""
     import torch
-    q_h = x["q"].pin_memory()
-    qi_h = x["q_idx"].pin_memory()
-    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    lse_h = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
-    idx_h = torch.empty(step.idx.shape, dtype=step.idx.dtype).pin_memory()
+    ins = [(step.q, x["q"][0, 0] if w.layers > 1 else x["q"])]
+    if isinstance(step, SparseDecodeStep):
+        ins.append((step.q_idx, x["q_idx"]))
+    ins = [(dst, src.contiguous().pin_memory()) for dst, src in ins]
+    outs = [step.out, step.lse] + ([step.idx] if isinstance(step, SparseDecodeStep) else [step.s])
+    outs = [(src, torch.empty(src.shape, dtype=src.dtype).pin_memory()) for src in outs]
     times = []
     for i in range(K + 3):
-        flush.zero_()
+        clean_l2()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        step.q.copy_(q_h, non_blocking=True)
-        step.q_idx.copy_(qi_h, non_blocking=True)
+        for dst, src in ins:
+            dst.copy_(src, non_blocking=True)
         step.run()
-        out_h.copy_(step.out, non_blocking=True)
-        lse_h.copy_(step.lse, non_blocking=True)
-        idx_h.copy_(step.idx, non_blocking=True)
+        for src, dst in outs:
+            dst.copy_(src, non_blocking=True)
         torch.cuda.current_stream().synchronize()
         if i >= 3:
             times.append(time.perf_counter() - t0)
-    bi = q_h.numel() * q_h.element_size() + qi_h.numel() * qi_h.element_size()
-    bo = sum(t.numel() * t.element_size() for t in (out_h, lse_h, idx_h))
+    bi = sum(src.numel() * src.element_size() for _, src in ins)
+    bo = sum(dst.numel() * dst.element_size() for _, dst in outs)
     return {"value": round(w.queries_per_step * len(times) / sum(times), 1), "unit": "queries/s",
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "timing": "host wall clock per step incl. copies and sync"}
@@ -363,17 +516,29 @@ def measure_e2e(step, w, x, flush, K):
 
 def oracle_step(w, x, b0, b1):
     """The whole step on the CPU oracle for sequences [b0, b1)."""
+    import numpy as np
     import oracle
     nb = b1 - b0
+    scale = 1.0 / math.sqrt(w.d)
+    if w.layers > 1:  # dense attention per layer and the layer's importance-score term
+        s = np.zeros((nb, w.T))
+        for layer in range(w.layers):
+            _, lse, z = oracle.gather_attend(x["q"][0, layer, b0:b1].contiguous(),
+                                             x["k"][layer][b0:b1].contiguous(),
+                                             x["v"][layer][b0:b1].contiguous(), None, nb, w.V, w.Hq,
+                                             w.Hkv, w.d, w.T, w.T, 1, scale, True)
+            oracle.score_accumulate(z, lse, None, s, nb, w.V, w.Hq, w.Hkv, w.T, 1, w.T,
+                                    1.0 / (w.layers * w.Hq))
+        return s
     q_idx = x["q_idx"][b0:b1].contiguous()
     keys = x["k_idx"][b0:b1].contiguous()
     if w.block > 1:
         keys = oracle.block_pool(keys, nb, w.Hkv, w.T, w.dI, w.block).astype("float32")
-    s = oracle.index_score(q_idx, keys, nb, w.Hkv, w.V, w.N, w.dI)
-    idx = oracle.topk(s, w.k)
+    sc = oracle.index_score(q_idx, keys, nb, w.Hkv, w.V, w.N, w.dI)
+    idx = oracle.topk(sc, w.k)
     return oracle.gather_attend(x["q"][b0:b1].contiguous(), x["k"][b0:b1].contiguous(),
                                 x["v"][b0:b1].contiguous(), idx, nb, w.V, w.Hq, w.Hkv, w.d, w.T,
-                                w.k, w.block, 1.0 / math.sqrt(w.d))
+                                w.k, w.block, scale)
 
 
 def cpu_baseline(w, x, budget_s: float = 10.0, nseq: int = 1):

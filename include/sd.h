@@ -80,11 +80,17 @@ const char* sd_last_error_message(void);
  * the pooled block keys of sd_block_pool for block-granular selection, then N = blocks);
  * scores [B,Hkv,N] fp32 (written).  fp32 products and sums: integer-valued inputs with
  * |sum| < 2^24 give exact scores.  Limits: d_idx in {64, 128}, 1 <= V <= 8, N >= 0.
+ * key_hist: nullable [B*Hkv, SD_KEY_HIST_BINS] uint32 in/out.  When given, every score
+ * written adds 1 to the bin of its top 11 order-key bits (the order key maps fp32 to
+ * uint32 preserving order, -0.0 like +0.0).  Pass the same array to sd_topk for these
+ * scores: it then skips its own first pass and leaves the array zeroed again.  The caller
+ * zero-fills it once when it allocates it.
  * err_word: nullable device int32 (only SD_DEVERR_TIMEOUT can be set).
  */
+#define SD_KEY_HIST_BINS 2048
 sd_status sd_index_score(const void* q_idx, sd_dtype q_dtype, const void* k_idx,
                          sd_dtype k_dtype, int B, int Hkv, int V, int N, int d_idx,
-                         float* scores, int32_t* err_word, void* stream);
+                         float* scores, uint32_t* key_hist, int32_t* err_word, void* stream);
 
 /*
  * sd_block_pool -- block keys for block-granular selection (cache-build helper).
@@ -105,12 +111,15 @@ sd_status sd_block_pool(const void* k_idx, sd_dtype k_dtype, int B, int Hkv, int
  * entries first in the order (score descending, index ascending) -- ties go to the lower
  * index -- written in ascending index order.  -0.0 and +0.0 compare equal.
  * scores [rows,N] fp32 (NaN is outside the contract); idx [rows,k] int32 (written).
- * 0 <= k <= N.  Uses no workspace in this version: sd_topk_workspace_bytes returns 0 and
- * `workspace` may be NULL.
+ * 0 <= k <= N.  key_hist: nullable [rows, SD_KEY_HIST_BINS] uint32, the histogram
+ * sd_index_score accumulated for exactly these scores; when given, the select starts from
+ * it (one pass over the scores instead of three) and the call zero-fills it again.
+ * Uses no workspace in this version: sd_topk_workspace_bytes returns 0 and `workspace`
+ * may be NULL.
  */
 size_t sd_topk_workspace_bytes(int rows, int N, int k);
-sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx, void* workspace,
-                  size_t workspace_bytes, void* stream);
+sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx, uint32_t* key_hist,
+                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * sd_gather_attend -- exact softmax attention over only the selected K/V rows.
@@ -137,7 +146,15 @@ sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx, voi
  * Accumulation order depends only on (n_idx, block, splits), never on the data source.
  * Limits: d in {64, 128}; G*V <= 32; dtype F32 or BF16 for q, K and V alike.
  * The split-K partition over selected rows needs workspace (sd_gather_attend_workspace_bytes;
- * 0 when one split suffices).  splits = 0 picks a split count for this GPU.
+ * 0 when one split suffices): the splits' (m, l, o) partials and one completion counter
+ * per (b, kvh); the last split of a group to finish merges the partials in split order.
+ * The workspace must be zero-filled before its first use; every call leaves the counters
+ * at zero again, so a workspace can be reused without clearing.  Calls sharing one
+ * workspace must not overlap on the GPU.  splits = 0 picks one wave of CTAs for this GPU;
+ * a requested split count is adjusted to at least one 64-row chunk per split and at most
+ * 512 rows per split when rows are selected through idx or slot_map.
+ * The kernel is launched as a programmatic dependent of the preceding kernel in the
+ * stream (it waits for that kernel's results before reading anything).
  */
 typedef struct {
     const void* q;            /* [B,V,Hq,d] */
@@ -171,10 +188,12 @@ sd_status sd_gather_attend(const sd_attend_args* args, void* stream);
  * computes exactly what sd_gather_attend computes (same arguments, same split plan) but
  * ignores args->workspace / workspace_bytes and uses a 16 MiB array of device memory
  * compiled into the library, which every GPU that loads the library holds until exit.
- * It allocates nothing.  The array's device address is looked up on the first call made
- * on each device (with that device current): make that first call before any stream
- * capture.  All calls share the array and it keeps the last call's contents; nothing in it
- * needs to start at zero, but calls whose kernels overlap on the GPU race on it.  A request
+ * It allocates nothing.  On the first call made on each device (with that device
+ * current) the array's device address is looked up and the array is cleared once: make
+ * that first call before any stream capture.  All calls share the array and it keeps the
+ * last call's contents; the part that must start at zero (the per-group completion
+ * counters) is left at zero by every call, but calls whose kernels overlap on the GPU race
+ * on the array.  A request
  * whose split-K partials need more than 16 MiB returns SD_ERR_INVALID_ARG without
  * launching (pass a smaller `splits`, or use sd_gather_attend with a workspace).
  */

@@ -43,20 +43,20 @@ def test_host_validation_rejects_before_launch(lib):
     P = ctypes.c_void_p
     dummy = P(16)
     # k > N
-    assert lib.sd_topk(dummy, 1, 10, 11, dummy, None, 0, None) == 1
+    assert lib.sd_topk(dummy, 1, 10, 11, dummy, None, None, 0, None) == 1
     assert b"k (11)" in lib.sd_last_error_message()
     # unsupported indexer dim
-    assert lib.sd_index_score(dummy, 1, dummy, 1, 1, 1, 1, 10, 96, dummy, None, None) == 2
+    assert lib.sd_index_score(dummy, 1, dummy, 1, 1, 1, 1, 10, 96, dummy, None, None, None) == 2
     # V out of range
-    assert lib.sd_index_score(dummy, 1, dummy, 1, 1, 1, 9, 10, 128, dummy, None, None) == 1
+    assert lib.sd_index_score(dummy, 1, dummy, 1, 1, 1, 9, 10, 128, dummy, None, None, None) == 1
     # ragged block pooling
     assert lib.sd_block_pool(dummy, 1, 1, 1, 100, 128, 64, dummy, None) == 1
     # non-monotone tier fractions
     fr = (ctypes.c_double * 3)(0.5, 0.2, 0.9)
     assert lib.sd_tier_classify(dummy, 1, 10, fr, 0, 0, dummy, dummy, None, 0, None) == 1
     # empty work is a successful no-op
-    assert lib.sd_topk(None, 0, 10, 3, None, None, 0, None) == 0
-    assert lib.sd_index_score(None, 1, None, 1, 0, 8, 1, 100, 128, None, None, None) == 0
+    assert lib.sd_topk(None, 0, 10, 3, None, None, None, 0, None) == 0
+    assert lib.sd_index_score(None, 1, None, 1, 0, 8, 1, 100, 128, None, None, None, None) == 0
 
 
 def test_attend_validation_and_workspace_query(lib):

@@ -1,0 +1,79 @@
+"""Host logic of the benchmark's multi-rank path on CPU: two gloo ranks, the max-over-ranks
+time, the whole-job throughput, and the reference arm's rank-0-only rule.  Each rank of a
+real run processes its own full batch (weak scaling); nothing on the data path crosses
+ranks, so these are the only cross-rank steps."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+from conftest import ROOT
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    r, w, local = bench.dist_env()
+    t = bench.reduce_max(0.5 + rank, w)          # rank 1 is the slow one
+    v = bench.aggregate(800, w, t)
+    dist.barrier()
+    dist.destroy_process_group()
+    out.put((r, w, local, t, v))
+
+
+def test_two_gloo_ranks_take_the_max_time_and_sum_the_work():
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(out.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, (r, w, local, t, v) in enumerate(res):
+        assert (r, w, local) == (rank, 2, rank)
+        assert t == 1.5                    # max over ranks
+        assert v == pytest.approx(800 * 2 / 1.5)
+
+
+def test_single_rank_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.reduce_max(3.25, 1) == 3.25
+    assert bench.aggregate(10, 1, 2.0) == 5.0
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
+    assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_its_line(monkeypatch, capsys):
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    for var in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(var, raising=False)
+    bench.main(["--impl", "reference", "--steps", "2", "--warmup", "3", "--workload", "c1_tiny"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "queries/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0

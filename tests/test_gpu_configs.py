@@ -58,11 +58,14 @@ def test_c1_tiny_full():
 
 
 def test_c2_llama3_8b_gqa_full():
+    # the benchmark's launch configuration: indexer with the fused key histogram, top-k
+    # seeded by it, gather-attend with the automatic split plan
     w = W("c2_llama3_8b_gqa")
     x = gen(w)
     g = to_dev(x)
-    scores = sd().sd_index_score(g["q_idx"], g["k_idx"])
-    idx = sd().sd_topk(scores, w.k)
+    hist = sd().key_hist_buffer(w.B * w.Hkv)
+    scores = sd().sd_index_score(g["q_idx"], g["k_idx"], key_hist=hist)
+    idx = sd().sd_topk(scores, w.k, key_hist=hist)
     out, lse, _ = sd().gather_attend(g["q"], g["k"], g["v"], idx, T=w.T)
     rs = oracle.index_score(x["q_idx"], x["k_idx"], w.B, w.Hkv, w.V, w.T, w.dI)
     np.testing.assert_array_equal(scores.cpu().numpy().astype(np.float64), rs)
@@ -100,8 +103,9 @@ def test_c3_block_sparse_full():
 
 def _c4_run(w, x, g, k_host, v_host, slot_map, k_pool, v_pool):
     e = torch.zeros(1, dtype=torch.int32, device="cuda")
-    scores = sd().sd_index_score(g["q_idx"], g["k_idx"], err_word=e)
-    idx = sd().sd_topk(scores, w.k)
+    hist = sd().key_hist_buffer(w.B * w.Hkv)
+    scores = sd().sd_index_score(g["q_idx"], g["k_idx"], err_word=e, key_hist=hist)
+    idx = sd().sd_topk(scores, w.k, key_hist=hist)
     out, lse, _ = sd().gather_attend(g["q"], k_pool, v_pool, idx, T=w.T, k_host=k_host,
                                      v_host=v_host, slot_map=slot_map, err_word=e)
     torch.cuda.synchronize()
@@ -186,7 +190,7 @@ def test_c5_importance_tiering_full():
                                                   logits=logits, err_word=e)
             need = sd().sd_gather_attend_workspace_bytes(a)
             if ws is None or ws.numel() < need:
-                ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+                ws = torch.zeros(max(need, 1), dtype=torch.uint8, device="cuda")
             sd().sd_gather_attend(a, ws)
             sd().sd_score_accumulate(logits, lse, None, s, Hkv, 1, weight, err_word=e)
         if step == 0:

@@ -105,6 +105,35 @@ def test_topk_float_scores_and_signed_zero():
         np.testing.assert_array_equal(idx.cpu().numpy(), oracle.topk(s.astype(np.float64), k))
 
 
+@pytest.mark.parametrize("B,Hkv,V,N,k,flat", [
+    (2, 4, 1, 32768, 1024, False),
+    (1, 2, 8, 131072, 2048, False),
+    (1, 2, 1, 20000, 100, True),      # every score equal: one bin beyond the candidate capacity
+    (2, 2, 1, 5000, 4999, False),
+    (1, 1, 1, 3000, 0, False),
+    (1, 1, 1, 3000, 3000, False),
+    (3, 1, 3, 777, 13, False),
+])
+def test_index_topk_with_key_histogram(B, Hkv, V, N, k, flat):
+    g = torch.Generator().manual_seed(N + k)
+    q = rint(g, (B, Hkv, V, 128), torch.bfloat16)
+    if flat:
+        q.zero_()
+    kk = rint(g, (B, Hkv, N, 128), torch.bfloat16)
+    hist = sd().key_hist_buffer(B * Hkv)
+    s = sd().sd_index_score(q.cuda(), kk.cuda(), key_hist=hist)
+    assert torch.equal(hist.sum(1).cpu(), torch.full((B * Hkv,), N, dtype=torch.int64))
+    idx = sd().sd_topk(s, k, key_hist=hist)
+    torch.cuda.synchronize()
+    assert int(hist.abs().sum().item()) == 0, "the histogram must be left zeroed"
+    ref = oracle.topk(oracle.index_score(q, kk, B, Hkv, V, N, 128), k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref)
+    # a second step with the same buffers gives the same result
+    s = sd().sd_index_score(q.cuda(), kk.cuda(), key_hist=hist)
+    idx2 = sd().sd_topk(s, k, key_hist=hist)
+    assert torch.equal(idx2, idx)
+
+
 # --------------------------------------------------------------------------- gather + attend
 
 
@@ -233,7 +262,7 @@ def test_host_pointer_must_be_pinned():
     a.k_host = K.data_ptr()   # pageable host memory
     a.v_host = Vv.data_ptr()
     with pytest.raises(sd().SdError):
-        sd().sd_gather_attend(a, torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
+        sd().sd_gather_attend(a, torch.zeros(1 << 20, dtype=torch.uint8, device="cuda"))
 
 
 # --------------------------------------------------------------------------- importance

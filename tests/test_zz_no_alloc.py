@@ -39,7 +39,7 @@ def test_noalloc_matches_the_workspace_call_twice_in_a_row(sd):
         a_ref, out_ref, lse_ref, _ = sd.make_attend_args(q, K, V, idx, T=K.shape[2])
         need = sd.sd_gather_attend_workspace_bytes(a_ref)
         assert need > 0, "the case must use split-K scratch"
-        sd.sd_gather_attend(a_ref, torch.empty(need, dtype=torch.uint8, device="cuda"))
+        sd.sd_gather_attend(a_ref, torch.zeros(need, dtype=torch.uint8, device="cuda"))
         a, out, lse, _ = sd.make_attend_args(q, K, V, idx, T=K.shape[2])
         a.workspace, a.workspace_bytes = None, 0      # no caller scratch at all
         sd.sd_gather_attend_noalloc(a)

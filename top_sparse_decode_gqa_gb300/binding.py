@@ -65,11 +65,11 @@ def lib() -> ctypes.CDLL:
         L.sd_status_string.restype = ctypes.c_char_p
         L.sd_status_string.argtypes = [I]
         L.sd_last_error_message.restype = ctypes.c_char_p
-        L.sd_index_score.argtypes = [P, I, P, I, I, I, I, I, I, P, P, P]
+        L.sd_index_score.argtypes = [P, I, P, I, I, I, I, I, I, P, P, P, P]
         L.sd_block_pool.argtypes = [P, I, I, I, I, I, I, P, P]
         L.sd_topk_workspace_bytes.argtypes = [I, I, I]
         L.sd_topk_workspace_bytes.restype = Z
-        L.sd_topk.argtypes = [P, I, I, I, P, P, Z, P]
+        L.sd_topk.argtypes = [P, I, I, I, P, P, P, Z, P]
         L.sd_gather_attend_workspace_bytes.argtypes = [ctypes.POINTER(sd_attend_args)]
         L.sd_gather_attend_workspace_bytes.restype = Z
         L.sd_gather_attend.argtypes = [ctypes.POINTER(sd_attend_args), P]
@@ -120,9 +120,20 @@ def sd_version() -> int:
     return lib().sd_version()
 
 
+KEY_HIST_BINS = 2048
+
+
+def key_hist_buffer(rows: int, device="cuda") -> torch.Tensor:
+    """A zero-filled [rows, 2048] uint32 (held as int32) order-key histogram for
+    sd_index_score / sd_topk."""
+    return torch.zeros((rows, KEY_HIST_BINS), dtype=torch.int32, device=device)
+
+
 def sd_index_score(q_idx: torch.Tensor, k_idx: torch.Tensor, scores: Optional[torch.Tensor] = None,
-                   err_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Indexer scores [B,Hkv,N] fp32 from q_idx [B,Hkv,V,dI] and k_idx [B,Hkv,N,dI]."""
+                   err_word: Optional[torch.Tensor] = None, stream=None,
+                   key_hist: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Indexer scores [B,Hkv,N] fp32 from q_idx [B,Hkv,V,dI] and k_idx [B,Hkv,N,dI]
+    (optionally accumulating their order-key histogram into key_hist)."""
     _dev(q_idx, "q_idx")
     _dev(k_idx, "k_idx")
     B, Hkv, V, dI = q_idx.shape
@@ -132,7 +143,8 @@ def sd_index_score(q_idx: torch.Tensor, k_idx: torch.Tensor, scores: Optional[to
     if scores is None:
         scores = torch.empty((B, Hkv, N), dtype=torch.float32, device=k_idx.device)
     _check(lib().sd_index_score(_ptr(q_idx), _dtype_code(q_idx), _ptr(k_idx), _dtype_code(k_idx), B,
-                                Hkv, V, N, dI, _ptr(scores), _ptr(err_word), _stream(stream)),
+                                Hkv, V, N, dI, _ptr(scores), _ptr(key_hist), _ptr(err_word),
+                                _stream(stream)),
            "sd_index_score")
     return scores
 
@@ -150,8 +162,10 @@ def sd_block_pool(k_idx: torch.Tensor, block: int, pooled: Optional[torch.Tensor
 
 
 def sd_topk(scores: torch.Tensor, k: int, idx: Optional[torch.Tensor] = None,
-            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Top-k indices (ascending, ties to the lower index) of each row of scores [..., N]."""
+            workspace: Optional[torch.Tensor] = None, stream=None,
+            key_hist: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Top-k indices (ascending, ties to the lower index) of each row of scores [..., N];
+    key_hist: the histogram sd_index_score accumulated for these scores (zeroed again)."""
     _dev(scores, "scores")
     if scores.dtype != torch.float32:
         raise TypeError("scores must be float32")
@@ -162,8 +176,8 @@ def sd_topk(scores: torch.Tensor, k: int, idx: Optional[torch.Tensor] = None,
     ws_bytes = lib().sd_topk_workspace_bytes(rows, N, k)
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=scores.device)
-    _check(lib().sd_topk(_ptr(scores), rows, N, k, _ptr(idx), _ptr(workspace), ws_bytes,
-                         _stream(stream)), "sd_topk")
+    _check(lib().sd_topk(_ptr(scores), rows, N, k, _ptr(idx), _ptr(key_hist), _ptr(workspace),
+                         ws_bytes, _stream(stream)), "sd_topk")
     return idx
 
 
@@ -217,7 +231,8 @@ def sd_gather_attend_workspace_bytes(args: sd_attend_args) -> int:
 
 def sd_gather_attend(args: sd_attend_args, workspace: Optional[torch.Tensor] = None,
                      stream=None) -> None:
-    """Runs one sd_gather_attend call described by `args` (see make_attend_args)."""
+    """Runs one sd_gather_attend call described by `args` (see make_attend_args).  The
+    workspace must be zero-filled before its first use (torch.zeros); calls leave it so."""
     need = sd_gather_attend_workspace_bytes(args)
     if need:
         if workspace is None or workspace.numel() * workspace.element_size() < need:
@@ -241,7 +256,7 @@ def gather_attend(q, k_cache, v_cache, idx=None, workspace=None, stream=None, **
     a, out, lse, logits = make_attend_args(q, k_cache, v_cache, idx, **kw)
     need = sd_gather_attend_workspace_bytes(a)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     sd_gather_attend(a, workspace, stream)
     return out, lse, logits
 

@@ -10,14 +10,16 @@
 // a fixed array compiled into the library instead.
 //
 // The array is kNoAllocScratchBytes (16 MiB) of device memory that every GPU which loads
-// the library holds until the process exits.  Its device address is looked up once per
-// device with cudaGetSymbolAddress, on the first call made while that device is current
-// (so make that first call before any stream capture).  All calls share the one array and
-// it keeps whatever the last call left there: nothing in it needs to start at zero,
-// because each call writes every partial it later reads, but two calls whose kernels
-// overlap on the GPU (different streams, no ordering between them) race on it and give
-// wrong results.  Requests whose split-K partials need more than the array holds are
-// rejected with SD_ERR_INVALID_ARG before anything is launched.
+// the library holds until the process exits.  On the first call made while a device is
+// current, its device address is looked up with cudaGetSymbolAddress and the array is
+// cleared once with cudaMemset (so make that first call before any stream capture).  All
+// calls share the one array and it keeps whatever the last call left there.  The split
+// partials are rewritten by every call before they are read; the per-group completion
+// counters must start at zero, which the one-time clear ensures and every call restores.
+// Two calls whose kernels overlap on the GPU (different streams, no ordering between
+// them) race on the array and give wrong results.  Requests whose split-K scratch needs
+// more than the array holds are rejected with SD_ERR_INVALID_ARG before anything is
+// launched.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -52,6 +54,11 @@ sd_status scratch_address(void** out) {
         e = cudaGetSymbolAddress(&p, g_attend_scratch);
         if (e != cudaSuccess || p == nullptr) {
             sd::set_error("sd_gather_attend_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+            return SD_ERR_CUDA;
+        }
+        e = cudaMemset(p, 0, kNoAllocScratchBytes);  // the completion counters start at zero
+        if (e != cudaSuccess) {
+            sd::set_error("sd_gather_attend_noalloc: clearing the scratch: %s", cudaGetErrorString(e));
             return SD_ERR_CUDA;
         }
         g_scratch_addr[dev] = p;

@@ -25,9 +25,11 @@ namespace sd {
 namespace {
 
 constexpr int kAttThreads = 128;
-constexpr int kCH = 64;  // rows per staged chunk
+constexpr int kCH = 64;             // rows per staged chunk
+constexpr int kMaxSplitRows = 512;  // rows whose sources a CTA resolves up front
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
+constexpr int32_t kNoRow = INT32_MIN;  // source code of a skipped (invalid) row
 
 struct AttendParams {
     const void* q;
@@ -39,6 +41,7 @@ struct AttendParams {
     const int32_t* idx;
     int B, V, Hq, Hkv, G, R, T, pool_rows, n_idx, block, n_rows, rows_per_split, splits;
     int dtype;
+    int resolve;  // 1: sources resolved up front (idx or slot_map given)
     float scale_log2;
     float* out;
     float* lse;
@@ -47,52 +50,117 @@ struct AttendParams {
     float* ws_o;
     float* ws_m;
     float* ws_l;
+    uint32_t* counters;  // [B*Hkv], zero between calls
 };
 
 template <typename ST, int D, int RP>
 struct AttLayout {
-    static constexpr int kPadE = 16 / (int)sizeof(ST);      // 16-byte row pad for K
+    static constexpr int kPadE = 16 / (int)sizeof(ST);  // 16-byte row pad for K
     static constexpr int kKRow = (D + kPadE) * (int)sizeof(ST);
     static constexpr int kVRow = D * (int)sizeof(ST);
-    static constexpr int kPRow = RP + 4;                    // floats per p row
-    static constexpr int kSRow = kCH + 4;                   // floats per s row
+    static constexpr int kPRow = RP + 4;  // floats per p row
+    static constexpr int kSRow = kCH + 4;  // floats per s row
     static constexpr int oQ = 0;
     static constexpr int oK = oQ + RP * D * 4;
     static constexpr int oV = oK + 2 * kCH * kKRow;
     static constexpr int oP = oV + 2 * kCH * kVRow;
     static constexpr int oS = oP + kCH * kPRow * 4;
     static constexpr int oSrc = oS + RP * kSRow * 4;
-    static constexpr int oAlpha = oSrc + 2 * 2 * kCH * 8;
+    static constexpr int oAlpha = oSrc + kMaxSplitRows * 4;
     static constexpr int oM = oAlpha + RP * 4;
     static constexpr int oL = oM + RP * 4;
-    static constexpr int kBytes = oL + RP * 4;
+    static constexpr int oFlag = oL + RP * 4;
+    static constexpr int kBytes = oFlag + 16;
     static_assert(oV % 16 == 0 && oP % 16 == 0 && oS % 16 == 0 && oSrc % 16 == 0, "align");
     static_assert((RP == 4 ? 4 : 1) * RP * D * 4 <= 2 * kCH * kKRow, "reduction buffer must fit in K");
 };
+
+// Shared-memory CTAs per SM for a layout (228 KB per SM, 1 KB reserved per CTA), at most 3.
+int att_ctas_per_sm(int bytes) {
+    const int per = 233472 / (bytes + 1024);
+    return per < 1 ? 1 : (per > 3 ? 3 : per);
+}
+
+// Called by every CTA after it wrote its split's partial: the last CTA of the (b, kvh) to
+// arrive combines all splits' (m, l, o) partials in split order (deterministic) into out
+// and lse, then resets the group's counter for the next call.  `scratch` holds at least
+// `scratch_floats` floats of shared memory no longer in use.
+template <int D>
+SD_DEVINL void merge_if_last(const AttendParams& p, int b, int kvh, int RP, float* scratch,
+                             int scratch_floats, int* flag_s) {
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int bk = b * p.Hkv + kvh;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) flag_s[0] = atomicAdd(&p.counters[bk], 1u) == (uint32_t)(p.splits - 1) ? 1 : 0;
+    __syncthreads();
+    if (!flag_s[0]) return;
+    __threadfence();
+    const int S = p.splits;
+    const int cap = scratch_floats / RP - 1;  // splits whose weights fit at once
+    for (int s0 = 0; s0 < S; s0 += cap) {
+        const int s1 = min(S, s0 + cap);
+        __syncthreads();
+        if (tid < p.R) {
+            const int r = tid;
+            float M = -INFINITY;
+            for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(p.ws_m + ((size_t)bk * S + s) * RP + r));
+            float Ls = 0.f;
+            if (M != -INFINITY)
+                for (int s = 0; s < S; ++s) {
+                    const float m = __ldcg(p.ws_m + ((size_t)bk * S + s) * RP + r);
+                    if (m != -INFINITY) Ls = fmaf(__ldcg(p.ws_l + ((size_t)bk * S + s) * RP + r), exp2f(m - M), Ls);
+                }
+            for (int s = s0; s < s1; ++s) {
+                const float m = __ldcg(p.ws_m + ((size_t)bk * S + s) * RP + r);
+                scratch[(s - s0) * RP + r] = (Ls > 0.f && m != -INFINITY) ? exp2f(m - M) / Ls : 0.f;
+            }
+            if (s0 == 0) {
+                const int v = r / p.G, g = r % p.G;
+                const size_t qrow = ((size_t)b * p.V + v) * p.Hq + kvh * p.G + g;
+                p.lse[qrow] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < p.R * D; e += nthr) {
+            const int r = e / D, col = e % D;
+            const int v = r / p.G, g = r % p.G;
+            const size_t qrow = ((size_t)b * p.V + v) * p.Hq + kvh * p.G + g;
+            float o = s0 == 0 ? 0.f : p.out[qrow * D + col];
+            for (int s = s0; s < s1; ++s)
+                o = fmaf(scratch[(s - s0) * RP + r], __ldcg(p.ws_o + (((size_t)bk * S + s) * RP + r) * D + col), o);
+            p.out[qrow * D + col] = o;
+        }
+    }
+    if (tid == 0) p.counters[bk] = 0u;  // ready for the next call
+}
 
 template <typename ST, int D, int RP>
 __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams p) {
     using L = AttLayout<ST, D, RP>;
     using U = Unpack16<ST>;
-    constexpr int EPC = U::kElems;         // elements per 16 bytes
-    constexpr int PPR = L::kVRow / 16;     // 16-byte pieces per row
-    constexpr int CPL = D / 32;            // PV columns per lane
-    constexpr bool kKeySplit = (RP == 4);  // PV: warps split keys (else query rows)
+    constexpr int EPC = U::kElems;               // elements per 16 bytes
+    constexpr int PPR = L::kVRow / 16;           // 16-byte pieces per row
+    constexpr int CPL = D / 32;                  // PV columns per lane
+    constexpr bool kKeySplit = (RP == 4);        // PV: warps split keys (else query rows)
     constexpr int QW = kKeySplit ? RP : RP / 4;  // PV query rows per warp
 
     extern __shared__ __align__(128) uint8_t sm[];
     float* qs = reinterpret_cast<float*>(sm + L::oQ);
     float* ps = reinterpret_cast<float*>(sm + L::oP);
     float* ss = reinterpret_cast<float*>(sm + L::oS);
-    const uint8_t** srcs = reinterpret_cast<const uint8_t**>(sm + L::oSrc);  // [2 bufs][K,V][kCH]
+    int32_t* src = reinterpret_cast<int32_t*>(sm + L::oSrc);  // per row of the split
     float* alpha_s = reinterpret_cast<float*>(sm + L::oAlpha);
     float* m_s = reinterpret_cast<float*>(sm + L::oM);
     float* l_s = reinterpret_cast<float*>(sm + L::oL);
+    int* flag_s = reinterpret_cast<int*>(sm + L::oFlag);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int bk = b * p.Hkv + kvh;
     const size_t esz = sizeof(ST);
+
+    pdl_wait();  // everything below may read what the preceding kernel wrote
 
     // ---- query rows r = v*G + g (head h = kvh*G + g), pre-scaled by scale*log2(e)
     for (int e = tid; e < RP * D; e += kAttThreads) {
@@ -108,67 +176,61 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
 
     const int j0 = split * p.rows_per_split;
     const int j1 = min(p.n_rows, j0 + p.rows_per_split);
-    const int nch = j1 > j0 ? (j1 - j0 + kCH - 1) / kCH : 0;
+    const int nrows = max(0, j1 - j0);
+    const int nch = (nrows + kCH - 1) / kCH;
 
-    auto compute_src = [&](int c, int bf) {
-        if (tid < kCH) {
-            const int jg = j0 + c * kCH + tid;
-            const uint8_t* sk = nullptr;
-            const uint8_t* sv = nullptr;
-            if (jg < j1) {
-                long pos = jg;
-                bool ok = true;
-                if (p.idx != nullptr) {
-                    const long sel = p.idx[(size_t)bk * p.n_idx + jg / p.block];
-                    pos = sel * p.block + jg % p.block;
-                    if (sel < 0 || pos >= p.T) {
-                        report(p.err, SD_DEVERR_INDEX);
-                        ok = false;
-                    }
-                }
-                if (ok) {
-                    if (p.slot_map != nullptr) {
-                        const int slot = p.slot_map[(size_t)b * p.T + pos];
-                        if (slot >= 0 && slot < p.pool_rows) {
-                            const size_t row = (size_t)bk * p.pool_rows + slot;
-                            sk = p.kc + row * L::kVRow;
-                            sv = p.vc + row * L::kVRow;
-                        } else if (slot == -1) {
-                            const size_t row = (size_t)bk * p.T + pos;
-                            sk = p.kh + row * L::kVRow;
-                            sv = p.vh + row * L::kVRow;
-                        } else {
-                            report(p.err, SD_DEVERR_SLOT);
-                        }
-                    } else {
-                        const size_t row = (size_t)bk * p.T + pos;
-                        sk = p.kc + row * L::kVRow;
-                        sv = p.vc + row * L::kVRow;
-                    }
-                }
+    // ---- resolve every row's source once: >= 0 device row (pool slot, or cache
+    // position without a slot map), < 0 host row -1 - position, kNoRow skipped
+    auto resolve_row = [&](int jg) -> int32_t {
+        long pos = jg;
+        if (p.idx != nullptr) {
+            const long sel = p.idx[(size_t)bk * p.n_idx + jg / p.block];
+            pos = sel * p.block + jg % p.block;
+            if (sel < 0 || pos >= p.T) {
+                report(p.err, SD_DEVERR_INDEX);
+                return kNoRow;
             }
-            srcs[(bf * 2 + 0) * kCH + tid] = sk;
-            srcs[(bf * 2 + 1) * kCH + tid] = sv;
         }
+        if (p.slot_map == nullptr) return (int32_t)pos;
+        const int slot = p.slot_map[(size_t)b * p.T + pos];
+        if (slot >= 0 && slot < p.pool_rows) return slot;
+        if (slot == -1) return (int32_t)(-1 - pos);
+        report(p.err, SD_DEVERR_SLOT);
+        return kNoRow;
     };
-    auto issue = [&](int bf) {
+    if (p.resolve)
+        for (int j = tid; j < nrows; j += kAttThreads) src[j] = resolve_row(j0 + j);
+    __syncthreads();
+    auto row_code = [&](int j) -> int32_t { return p.resolve ? src[j] : (int32_t)(j0 + j); };
+
+    auto issue = [&](int c, int bf) {
         uint8_t* kdst = sm + L::oK + bf * kCH * L::kKRow;
         uint8_t* vdst = sm + L::oV + bf * kCH * L::kVRow;
+        const int rows_here = min(kCH, nrows - c * kCH);
         for (int pc = tid; pc < 2 * kCH * PPR; pc += kAttThreads) {
             const int which = pc / (kCH * PPR);
             const int rem = pc - which * (kCH * PPR);
             const int j = rem / PPR, part = rem % PPR;
-            const uint8_t* src = srcs[(bf * 2 + which) * kCH + j];
             uint8_t* dst = which ? vdst + j * L::kVRow + part * 16 : kdst + j * L::kKRow + part * 16;
-            if (src != nullptr)
-                cp_async16(dst, src + part * 16);
-            else
+            const int32_t code = j < rows_here ? row_code(c * kCH + j) : kNoRow;
+            if (code == kNoRow) {
                 *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+                continue;
+            }
+            const uint8_t* base;
+            size_t row;
+            if (code >= 0) {
+                base = which ? p.vc : p.kc;
+                row = (size_t)bk * p.pool_rows + code;
+            } else {
+                base = which ? p.vh : p.kh;
+                row = (size_t)bk * p.T + (size_t)(-1 - (long)code);
+            }
+            cp_async16(dst, base + row * L::kVRow + part * 16);
         }
         cp_async_commit();
     };
 
-    // softmax state: warp w owns query rows r = w + 4*i
     float m_reg[RP / 4], l_reg[RP / 4];
 #pragma unroll
     for (int i = 0; i < RP / 4; ++i) {
@@ -181,28 +243,21 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
 #pragma unroll
         for (int c = 0; c < CPL; ++c) acc[i][c] = 0.f;
 
-    if (nch > 0) {
-        compute_src(0, 0);
-        __syncthreads();
-        issue(0);
-    }
+    if (nch > 0) issue(0, 0);
+    if (nch > 1) issue(1, 1);
     for (int c = 0; c < nch; ++c) {
         const int bf = c & 1;
-        if (c + 1 < nch) {
-            compute_src(c + 1, bf ^ 1);
-            __syncthreads();
-            issue(bf ^ 1);
+        if (c + 1 < nch)
             cp_async_wait<1>();
-        } else {
+        else
             cp_async_wait<0>();
-        }
         __syncthreads();
 
         // ---- QK: thread -> key j, half hf of the query rows
         {
             const int j = tid & (kCH - 1), hf = tid / kCH;
             const uint8_t* krow = sm + L::oK + (bf * kCH + j) * L::kKRow;
-            const bool valid = srcs[(bf * 2) * kCH + j] != nullptr;
+            const bool valid = c * kCH + j < nrows && row_code(c * kCH + j) != kNoRow;
             float s[RP / 2];
 #pragma unroll
             for (int r = 0; r < RP / 2; ++r) s[r] = 0.f;
@@ -285,9 +340,11 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
                 }
             }
         }
+        __syncthreads();  // buffer bf is refilled next
+        if (c + 2 < nch) issue(c + 2, bf);
     }
 
-    // ---- publish m, l; reduce the key-split partial sums
+    // ---- publish m, l; combine the warps' partial sums
 #pragma unroll
     for (int i = 0; i < RP / 4; ++i)
         if (lane == 0) {
@@ -328,61 +385,411 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
             }
         }
     }
+    if (p.splits == 1) return;
+
+    // ---- the last CTA of this (b, kvh) to finish merges the partials in split order
+    merge_if_last<D>(p, b, kvh, RP, reinterpret_cast<float*>(sm + L::oK), (2 * kCH * L::kKRow) / 4, flag_s);
 }
 
-// Combines the split partials of one (b, kvh) in split order.
-template <int D>
-__global__ void attend_merge_kernel(const AttendParams p, int RP) {
-    const int bk = blockIdx.x;
-    const int b = bk / p.Hkv, kvh = bk % p.Hkv;
-    for (int e = threadIdx.x; e < p.R * D; e += blockDim.x) {
-        const int r = e / D, col = e % D;
-        const size_t base = (size_t)bk * p.splits * RP + r;
-        float M = -INFINITY;
-        for (int s = 0; s < p.splits; ++s) M = fmaxf(M, p.ws_m[base + (size_t)s * RP]);
-        float Lsum = 0.f, acc = 0.f;
-        if (M != -INFINITY) {
-            for (int s = 0; s < p.splits; ++s) {
-                const float m = p.ws_m[base + (size_t)s * RP];
-                if (m == -INFINITY) continue;
-                const float w = exp2f(m - M);
-                Lsum = fmaf(p.ws_l[base + (size_t)s * RP], w, Lsum);
-                acc = fmaf(p.ws_o[(base + (size_t)s * RP) * D + col], w, acc);
+// ------------------------------------------------------------------ bf16 path (warp MMA)
+
+constexpr int kSub = 16;     // keys per warp sub-chunk
+constexpr int kWStages = 2;  // sub-chunks in flight per warp
+
+template <int D, int RP>
+struct MmaLayout {
+    static constexpr int kRowB = D * 2 + 16;  // padded bf16 row: conflict-free ldmatrix
+    static constexpr int kStage = 2 * kSub * kRowB;  // K rows then V rows
+    static constexpr int oQ = 0;
+    static constexpr int oStage = ((RP * kRowB + 127) / 128) * 128;
+    static constexpr int oSrc = oStage + 4 * kWStages * kStage;
+    static constexpr int oBar = oSrc + kMaxSplitRows * 4;
+    static constexpr int oML = oBar + 4 * kWStages * 8;  // [4 warps][RP] m, then l
+    static constexpr int oFlag = oML + 2 * 4 * RP * 4;
+    static constexpr int kBytes = oFlag + 16;
+    static_assert(4 * RP * D * 4 <= 4 * kWStages * kStage, "warp outputs must fit in the stages");
+};
+
+// Grid (split, kvh, b), 4 warps.  The split's rows are cut into 16-key sub-chunks dealt
+// round-robin to the warps; each warp runs its own 2-deep pipeline (1-D bulk copies for
+// rows in HBM, 16-byte cp.async for rows in host memory, zero rows for skipped ones) and
+// its own online softmax, with QK^T and PV on the tensor cores: S[16q x 8k] tiles from Q
+// (ldmatrix) and K (ldmatrix), P split into bf16 hi + lo parts so the PV product keeps
+// ~16 significant bits, V fragments through ldmatrix.trans.  At the end the 4 warps'
+// (m, l, O) are combined through shared memory into the CTA's split partial.
+template <int D, int RP>
+__global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendParams p) {
+    using L = MmaLayout<D, RP>;
+    constexpr int MT = RP / 16;   // 16-row M tiles of query rows
+    constexpr int KS = D / 16;    // k-steps of QK
+    constexpr int NT = D / 8;     // 8-column n-tiles of PV
+    constexpr int PPR = D * 2 / 16;  // 16-byte pieces per row
+    extern __shared__ __align__(128) uint8_t sm[];
+    int32_t* src = reinterpret_cast<int32_t*>(sm + L::oSrc);
+    float* mlw = reinterpret_cast<float*>(sm + L::oML);
+    int* flag_s = reinterpret_cast<int*>(sm + L::oFlag);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int bk = b * p.Hkv + kvh;
+    uint8_t* stages = sm + L::oStage + warp * kWStages * L::kStage;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::oBar) + warp * kWStages;
+
+    pdl_wait();
+
+    // ---- query rows r = v*G + g' (head kvh*G + g'), bf16, zero beyond R
+    for (int e = tid; e < RP * PPR; e += kAttThreads) {
+        const int r = e / PPR, part = e % PPR;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (r < p.R) {
+            const int v = r / p.G, gg = r % p.G;
+            const uint8_t* qrow = static_cast<const uint8_t*>(p.q) +
+                                  ((((size_t)b * p.V + v) * p.Hq + kvh * p.G + gg) * D) * 2;
+            val = *reinterpret_cast<const uint4*>(qrow + part * 16);
+        }
+        *reinterpret_cast<uint4*>(sm + L::oQ + r * L::kRowB + part * 16) = val;
+    }
+
+    const int j0 = split * p.rows_per_split;
+    const int j1 = min(p.n_rows, j0 + p.rows_per_split);
+    const int nrows = max(0, j1 - j0);
+    auto resolve_row = [&](int jg) -> int32_t {
+        long pos = jg;
+        if (p.idx != nullptr) {
+            const long sel = p.idx[(size_t)bk * p.n_idx + jg / p.block];
+            pos = sel * p.block + jg % p.block;
+            if (sel < 0 || pos >= p.T) {
+                report(p.err, SD_DEVERR_INDEX);
+                return kNoRow;
             }
         }
-        const int v = r / p.G, g = r % p.G;
-        const size_t qrow = ((size_t)b * p.V + v) * p.Hq + kvh * p.G + g;
-        p.out[qrow * D + col] = Lsum > 0.f ? acc / Lsum : 0.f;
-        if (col == 0) p.lse[qrow] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+        if (p.slot_map == nullptr) return (int32_t)pos;
+        const int slot = p.slot_map[(size_t)b * p.T + pos];
+        if (slot >= 0 && slot < p.pool_rows) return slot;
+        if (slot == -1) return (int32_t)(-1 - pos);
+        report(p.err, SD_DEVERR_SLOT);
+        return kNoRow;
+    };
+    if (p.resolve)
+        for (int j = tid; j < nrows; j += kAttThreads) src[j] = resolve_row(j0 + j);
+    if (lane == 0) {
+        for (int s = 0; s < kWStages; ++s) mbar_init(&bars[s], 1);
+        fence_mbarrier_init();
     }
+    __syncthreads();
+    auto row_code = [&](int j) -> int32_t {
+        if (j >= nrows) return kNoRow;
+        return p.resolve ? src[j] : (int32_t)(j0 + j);
+    };
+
+    const int nsub = (nrows + kSub - 1) / kSub;
+    const int my_n = warp < nsub ? (nsub - warp + 3) / 4 : 0;
+
+    // ---- fill stage `st` with sub-chunk ci of this warp
+    auto issue = [&](int ci, int st) {
+        const int c = warp + 4 * ci;
+        uint8_t* kst = stages + st * L::kStage;
+        uint8_t* vst = kst + kSub * L::kRowB;
+        const int32_t code = lane < kSub ? row_code(c * kSub + lane) : kNoRow;
+        const bool dev = lane < kSub && code != kNoRow && code >= 0;
+        const uint32_t devm = __ballot_sync(0xffffffffu, dev);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[st], (uint32_t)__popc(devm) * (uint32_t)(2 * D * 2));
+        __syncwarp();
+        if (dev) {
+            const size_t row = (size_t)bk * p.pool_rows + code;
+            bulk_g2s(kst + lane * L::kRowB, p.kc + row * (D * 2), D * 2, &bars[st]);
+            bulk_g2s(vst + lane * L::kRowB, p.vc + row * (D * 2), D * 2, &bars[st]);
+        }
+        // host rows (cp.async) and skipped rows (zeros): all lanes share the pieces
+        for (int kk = 0; kk < kSub; ++kk) {
+            const int32_t ck = __shfl_sync(0xffffffffu, code, kk);
+            if (ck >= 0) continue;
+            for (int pc = lane; pc < 2 * PPR; pc += 32) {
+                const int which = pc / PPR, part = pc % PPR;
+                uint8_t* dst = (which ? vst : kst) + kk * L::kRowB + part * 16;
+                if (ck == kNoRow) {
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+                } else {
+                    const size_t row = (size_t)bk * p.T + (size_t)(-1 - (long)ck);
+                    cp_async16(dst, (which ? p.vh : p.kh) + row * (D * 2) + part * 16);
+                }
+            }
+        }
+        cp_async_commit();
+    };
+
+    float m_r[MT][2], l_r[MT][2];
+    float oacc[MT][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        m_r[mt][0] = m_r[mt][1] = -INFINITY;
+        l_r[mt][0] = l_r[mt][1] = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) oacc[mt][nt][e] = 0.f;
+    }
+
+    const uint32_t q_base = smem_addr(sm + L::oQ);
+    int issued = 0;
+    for (; issued < min(kWStages, my_n); ++issued) issue(issued, issued);
+    bool timed_out = false;
+    for (int ci = 0; ci < my_n; ++ci) {
+        const int st = ci % kWStages;
+        const bool ok = mbar_wait(&bars[st], (uint32_t)((ci / kWStages) & 1));
+        if (__any_sync(0xffffffffu, !ok)) {
+            timed_out = true;
+            break;
+        }
+        if (ci + 1 < issued)
+            cp_async_wait<1>();
+        else
+            cp_async_wait<0>();
+        __syncwarp();
+        const uint32_t k_base = smem_addr(stages + st * L::kStage);
+        const uint32_t v_base = k_base + kSub * L::kRowB;
+        const int c = warp + 4 * ci;
+
+        // ---- S = Q K^T for this warp's 16 keys: [MT][2 n-tiles][4]
+        float sacc[MT][2][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ks += 2) {
+            uint32_t bk0[4], bk1[4];  // n-tile 0 / 1: (b0, b1) of k-step ks, then of ks + 1
+            ldsm_x4(k_base + (0 * 8 + (lane & 7)) * L::kRowB + (ks * 16 + (lane >> 3) * 8) * 2, bk0[0], bk0[1], bk0[2], bk0[3]);
+            ldsm_x4(k_base + (1 * 8 + (lane & 7)) * L::kRowB + (ks * 16 + (lane >> 3) * 8) * 2, bk1[0], bk1[1], bk1[2], bk1[3]);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(q_base + (mt * 16 + (lane & 15)) * L::kRowB + ((ks + kk) * 16 + (lane >> 4) * 8) * 2, a0, a1, a2, a3);
+                    mma_bf16_16816(sacc[mt][0], a0, a1, a2, a3, bk0[2 * kk], bk0[2 * kk + 1]);
+                    mma_bf16_16816(sacc[mt][1], a0, a1, a2, a3, bk1[2 * kk], bk1[2 * kk + 1]);
+                }
+            }
+        }
+
+        // ---- online softmax (base 2); this lane holds keys 8*nt + 2*t4 + e of rows g, g + 8
+        bool kval[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) kval[nt][e] = row_code(c * kSub + nt * 8 + 2 * t4 + e) != kNoRow;
+        uint32_t ph[MT][4], pl[MT][4];  // P as A fragments (hi, lo)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float x[2][2];
+                float tmax = -INFINITY;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        x[nt][e] = kval[nt][e] ? sacc[mt][nt][2 * hf + e] * p.scale_log2 : -INFINITY;
+                        tmax = fmaxf(tmax, x[nt][e]);
+                    }
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+                const float mo = m_r[mt][hf];
+                const float mn = fmaxf(mo, tmax);
+                const float alpha = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
+                float rs = 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float pv = (x[nt][e] == -INFINITY) ? 0.f : exp2f(x[nt][e] - mn);
+                        sacc[mt][nt][2 * hf + e] = pv;
+                        rs += pv;
+                    }
+                rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+                rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+                l_r[mt][hf] = l_r[mt][hf] * alpha + rs;
+                m_r[mt][hf] = mn;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    oacc[mt][nt][2 * hf] *= alpha;
+                    oacc[mt][nt][2 * hf + 1] *= alpha;
+                }
+                const int r = mt * 16 + g + 8 * hf;
+                if (p.logits != nullptr && r < p.R) {
+                    const int v = r / p.G, gg = r % p.G;
+                    float* lrow = p.logits + (((size_t)b * p.V + v) * p.Hq + kvh * p.G + gg) * p.n_rows;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int j = c * kSub + nt * 8 + 2 * t4 + e;
+                            if (j < nrows) lrow[j0 + j] = x[nt][e] * kLn2;
+                        }
+                }
+            }
+            // A fragments: a0 = (g, keys 2t..), a1 = (g+8, 2t..), a2 = (g, 2t+8..), a3 = (g+8, 2t+8..)
+            split_bf16x2(sacc[mt][0][0], sacc[mt][0][1], ph[mt][0], pl[mt][0]);
+            split_bf16x2(sacc[mt][0][2], sacc[mt][0][3], ph[mt][1], pl[mt][1]);
+            split_bf16x2(sacc[mt][1][0], sacc[mt][1][1], ph[mt][2], pl[mt][2]);
+            split_bf16x2(sacc[mt][1][2], sacc[mt][1][3], ph[mt][3], pl[mt][3]);
+        }
+
+        // ---- O += P V: V fragments by ldmatrix.trans, 2 n-tiles per load
+#pragma unroll
+        for (int nt = 0; nt < NT; nt += 2) {
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_t(v_base + (lane & 15) * L::kRowB + (nt * 8 + (lane >> 4) * 8) * 2, v0, v1, v2, v3);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                mma_bf16_16816(oacc[mt][nt], ph[mt][0], ph[mt][1], ph[mt][2], ph[mt][3], v0, v1);
+                mma_bf16_16816(oacc[mt][nt], pl[mt][0], pl[mt][1], pl[mt][2], pl[mt][3], v0, v1);
+                mma_bf16_16816(oacc[mt][nt + 1], ph[mt][0], ph[mt][1], ph[mt][2], ph[mt][3], v2, v3);
+                mma_bf16_16816(oacc[mt][nt + 1], pl[mt][0], pl[mt][1], pl[mt][2], pl[mt][3], v2, v3);
+            }
+        }
+        __syncwarp();
+        if (ci + kWStages < my_n) {
+            fence_proxy_async_shared();
+            issue(ci + kWStages, st);
+            ++issued;
+        }
+    }
+    if (timed_out) {
+        if (lane == 0) report(p.err, SD_DEVERR_TIMEOUT);
+        cp_async_wait<0>();
+        // let this warp's bulk copies in flight land (bounded) before the stages are reused
+        for (int j = 0; j < issued; ++j) mbar_wait(&bars[j % kWStages], (uint32_t)((j / kWStages) & 1));
+    }
+
+    // ---- combine the 4 warps: m, l per row, then O rows scaled to the CTA maximum
+    if (t4 == 0) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int r = mt * 16 + g + 8 * hf;
+                mlw[warp * RP + r] = m_r[mt][hf];
+                mlw[4 * RP + warp * RP + r] = l_r[mt][hf];
+            }
+    }
+    __syncthreads();  // every warp is done with its stages: they hold the warps' O now
+    float* ow = reinterpret_cast<float*>(sm + L::oStage);  // [4][RP][D]
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int r = mt * 16 + g + 8 * hf;
+            const float mw = mlw[warp * RP + r];
+            float M = mlw[r];
+#pragma unroll
+            for (int w = 1; w < 4; ++w) M = fmaxf(M, mlw[w * RP + r]);
+            const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float2 o2 = make_float2(oacc[mt][nt][2 * hf] * f, oacc[mt][nt][2 * hf + 1] * f);
+                *reinterpret_cast<float2*>(ow + ((size_t)warp * RP + r) * D + nt * 8 + 2 * t4) = o2;
+            }
+        }
+    __syncthreads();
+    for (int e = tid; e < p.R * D; e += kAttThreads) {
+        const int r = e / D, col = e % D;
+        float M = mlw[r];
+#pragma unroll
+        for (int w = 1; w < 4; ++w) M = fmaxf(M, mlw[w * RP + r]);
+        float Ls = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float mw = mlw[w * RP + r];
+            if (mw != -INFINITY) Ls = fmaf(mlw[4 * RP + w * RP + r], exp2f(mw - M), Ls);
+        }
+        const float o = ow[(0 * RP + r) * D + col] + ow[(1 * RP + r) * D + col] + ow[(2 * RP + r) * D + col] +
+                        ow[(3 * RP + r) * D + col];
+        if (p.splits == 1) {
+            const int v = r / p.G, gg = r % p.G;
+            const size_t qrow = ((size_t)b * p.V + v) * p.Hq + kvh * p.G + gg;
+            p.out[qrow * D + col] = Ls > 0.f ? o / Ls : 0.f;
+            if (col == 0) p.lse[qrow] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+        } else {
+            const size_t prow = ((size_t)bk * p.splits + split) * RP + r;
+            p.ws_o[prow * D + col] = o;
+            if (col == 0) {
+                p.ws_m[prow] = M;
+                p.ws_l[prow] = Ls;
+            }
+        }
+    }
+    if (p.splits == 1) return;
+    __syncthreads();  // the stage area is scratch for the merge
+    merge_if_last<D>(p, b, kvh, RP, reinterpret_cast<float*>(sm + L::oStage), 4 * kWStages * L::kStage / 4, flag_s);
 }
 
 int padded_rows(int R) { return R <= 4 ? 4 : R <= 8 ? 8 : R <= 16 ? 16 : R <= 32 ? 32 : -1; }
 
+// Query rows per CTA as the kernel lays them out: 16 or 32 on the bf16 (tensor-core) path,
+// 4 / 8 / 16 / 32 on the fp32 path; -1 if G*V is beyond 32.
+int kernel_rows(int dtype, int R) {
+    if (R > 32 || R < 1) return -1;
+    if (dtype == SD_BF16) return R <= 16 ? 16 : 32;
+    return padded_rows(R);
+}
+
+int layout_bytes(int dtype, int d, int RP) {
+    if (dtype == SD_BF16) {
+        if (d == 128) return RP <= 16 ? MmaLayout<128, 16>::kBytes : MmaLayout<128, 32>::kBytes;
+        return RP <= 16 ? MmaLayout<64, 16>::kBytes : MmaLayout<64, 32>::kBytes;
+    }
+    switch ((d == 128 ? 0 : 4) + (RP <= 4 ? 0 : RP <= 8 ? 1 : RP <= 16 ? 2 : 3)) {
+        case 0: return AttLayout<float, 128, 4>::kBytes;
+        case 1: return AttLayout<float, 128, 8>::kBytes;
+        case 2: return AttLayout<float, 128, 16>::kBytes;
+        case 3: return AttLayout<float, 128, 32>::kBytes;
+        case 4: return AttLayout<float, 64, 4>::kBytes;
+        case 5: return AttLayout<float, 64, 8>::kBytes;
+        case 6: return AttLayout<float, 64, 16>::kBytes;
+        default: return AttLayout<float, 64, 32>::kBytes;
+    }
+}
+
 struct SplitPlan {
     int splits, rows_per_split, RP;
-    size_t ws_bytes;
+    size_t ws_bytes, counters_offset;
 };
 
+size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+// Split-K plan: one wave of CTAs over the GPU (unless the caller asks for a split count),
+// at least one chunk per split, and at most kMaxSplitRows rows per split when the rows'
+// sources are resolved up front.  Partials [bk][split][RP][d] + m, l, then counters.
 SplitPlan plan_splits(const sd_attend_args* a) {
     SplitPlan sp{};
     const long n_rows = (long)a->n_idx * a->block;
     const long bk = (long)a->B * a->Hkv;
-    sp.RP = padded_rows(a->Hkv > 0 ? (a->Hq / a->Hkv) * a->V : 0);
+    sp.RP = kernel_rows(a->dtype, a->Hkv > 0 ? (a->Hq / a->Hkv) * a->V : 0);
     const long chunks = (n_rows + kCH - 1) / kCH;
+    const bool resolve = a->idx != nullptr || a->slot_map != nullptr;
     long splits;
     if (a->splits > 0) {
         splits = a->splits;
     } else {
-        const long target = (long)num_sms() * 6;  // ~2 waves of 3 CTAs per SM
-        splits = bk > 0 ? (target + bk - 1) / bk : 1;
+        const long slots = (long)num_sms() * att_ctas_per_sm(layout_bytes(a->dtype, a->d, sp.RP));
+        splits = bk > 0 ? slots / bk : 1;
     }
     splits = std::max(1L, std::min(splits, std::max(1L, chunks)));
-    long rps = chunks > 0 ? ((chunks + splits - 1) / splits) * kCH : kCH;
+    long rps = n_rows > 0 ? (n_rows + splits - 1) / splits : 1;
+    if (resolve && rps > kMaxSplitRows) rps = kMaxSplitRows;
     splits = n_rows > 0 ? (n_rows + rps - 1) / rps : 1;
     sp.splits = (int)splits;
     sp.rows_per_split = (int)rps;
-    sp.ws_bytes = splits > 1 ? (size_t)bk * splits * sp.RP * (a->d + 2) * sizeof(float) : 0;
+    if (splits > 1) {
+        const size_t np = (size_t)bk * splits * sp.RP;
+        sp.counters_offset = align16(np * (a->d + 2) * sizeof(float));
+        sp.ws_bytes = sp.counters_offset + align16((size_t)bk * sizeof(uint32_t));
+    }
     return sp;
 }
 
@@ -392,21 +799,30 @@ sd_status launch_attend(const AttendParams& p, cudaStream_t st) {
     auto kern = attend_kernel<ST, D, RP>;
     SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes),
                   "sd_gather_attend: cudaFuncSetAttribute");
-    dim3 grid(p.splits, p.Hkv, p.B);
-    kern<<<grid, kAttThreads, L::kBytes, st>>>(p);
-    sd_status s = launch_status("sd_gather_attend");
-    if (s != SD_OK || p.splits == 1) return s;
-    attend_merge_kernel<D><<<p.B * p.Hkv, 256, 0, st>>>(p, RP);
-    return launch_status("sd_gather_attend (merge)");
+    SD_CUDA_CHECK(launch_pdl(kern, dim3(p.splits, p.Hkv, p.B), dim3(kAttThreads), L::kBytes, st, p),
+                  "sd_gather_attend: launch");
+    return launch_status("sd_gather_attend");
 }
 
-template <typename ST, int D>
-sd_status dispatch_rp(const AttendParams& p, int RP, cudaStream_t st) {
+template <int D, int RP>
+sd_status launch_attend_mma(const AttendParams& p, cudaStream_t st) {
+    using L = MmaLayout<D, RP>;
+    auto kern = attend_mma_kernel<D, RP>;
+    SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes),
+                  "sd_gather_attend: cudaFuncSetAttribute");
+    SD_CUDA_CHECK(launch_pdl(kern, dim3(p.splits, p.Hkv, p.B), dim3(kAttThreads), L::kBytes, st, p),
+                  "sd_gather_attend: launch");
+    return launch_status("sd_gather_attend");
+}
+
+template <int D>
+sd_status dispatch_rp(const AttendParams& p, int dtype, int RP, cudaStream_t st) {
+    if (dtype == SD_BF16) return RP <= 16 ? launch_attend_mma<D, 16>(p, st) : launch_attend_mma<D, 32>(p, st);
     switch (RP) {
-        case 4: return launch_attend<ST, D, 4>(p, st);
-        case 8: return launch_attend<ST, D, 8>(p, st);
-        case 16: return launch_attend<ST, D, 16>(p, st);
-        default: return launch_attend<ST, D, 32>(p, st);
+        case 4: return launch_attend<float, D, 4>(p, st);
+        case 8: return launch_attend<float, D, 8>(p, st);
+        case 16: return launch_attend<float, D, 16>(p, st);
+        default: return launch_attend<float, D, 32>(p, st);
     }
 }
 
@@ -440,7 +856,7 @@ static sd_status validate_attend(const sd_attend_args* a) {
         set_error("sd_gather_attend: d must be 64 or 128 (got %d)", a->d);
         return SD_ERR_UNSUPPORTED;
     }
-    if (padded_rows((a->Hq / a->Hkv) * a->V) < 0) {
+    if (kernel_rows(a->dtype, (a->Hq / a->Hkv) * a->V) < 0) {
         set_error("sd_gather_attend: G*V = %d exceeds 32", (a->Hq / a->Hkv) * a->V);
         return SD_ERR_UNSUPPORTED;
     }
@@ -459,6 +875,7 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
     if (vs != SD_OK) return vs;
     if (a->B == 0) return SD_OK;
     SD_REQUIRE(a->q && a->out && a->lse, "sd_gather_attend: null q/out/lse");
+    SD_REQUIRE(aligned16(a->q), "sd_gather_attend: q must be 16-byte aligned");
     SplitPlan sp = plan_splits(a);
     AttendParams p{};
     p.q = a->q;
@@ -509,9 +926,9 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
         p.ws_o = static_cast<float*>(a->workspace);
         p.ws_m = p.ws_o + np * a->d;
         p.ws_l = p.ws_m + np;
+        p.counters = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a->workspace) + sp.counters_offset);
     }
+    p.resolve = (a->idx != nullptr || a->slot_map != nullptr) ? 1 : 0;
     cudaStream_t st = as_stream(stream);
-    if (a->dtype == SD_BF16)
-        return a->d == 128 ? dispatch_rp<bf16_t, 128>(p, sp.RP, st) : dispatch_rp<bf16_t, 64>(p, sp.RP, st);
-    return a->d == 128 ? dispatch_rp<float, 128>(p, sp.RP, st) : dispatch_rp<float, 64>(p, sp.RP, st);
+    return a->d == 128 ? dispatch_rp<128>(p, a->dtype, sp.RP, st) : dispatch_rp<64>(p, a->dtype, sp.RP, st);
 }

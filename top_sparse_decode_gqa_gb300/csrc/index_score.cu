@@ -14,140 +14,171 @@
 namespace sd {
 namespace {
 
-constexpr int kIdxThreads = 256;
-constexpr int kIdxWarps = kIdxThreads / 32;
-constexpr int kTileBytes = 16384;
-constexpr int kStages = 4;
-constexpr int kCtasPerSm = 3;
-constexpr int kIdxSmem = kStages * kTileBytes + kStages * 8;
+constexpr int kIdxWarps = 12;
+constexpr int kIdxThreads = kIdxWarps * 32;
+constexpr int kWarpTileBytes = 4096;  // one bulk copy: 16 rows of 256 B (8 of 512 B, 32 of 128 B)
+constexpr int kWarpStages = 4;
+constexpr int kIdxSmem = kIdxWarps * kWarpStages * (kWarpTileBytes + 8);
 
-template <typename KT, int DI, int VT>
-__global__ void __launch_bounds__(kIdxThreads) index_score_kernel(
-    const void* __restrict__ q_idx, int q_dtype, const KT* __restrict__ k_idx, int rows, int V,
-    int N, float* __restrict__ scores, int32_t* err_word) {
-    using U = Unpack16<KT>;
-    constexpr int ROWB = DI * (int)sizeof(KT);  // bytes per key row
-    constexpr int LPR = ROWB / 16;              // lanes per row
-    constexpr int EPL = U::kElems;              // elements per lane
-    constexpr int RPW = 32 / LPR;               // rows per warp per step
-    constexpr int TT = kTileBytes / ROWB;       // rows per tile
-    static_assert(TT % (kIdxWarps * RPW) == 0, "tile must split evenly over the warps");
-
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kTileBytes);
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int sub = lane % LPR;
-    const int rsub = lane / LPR;
-    const long tiles_per_row = (N + TT - 1) / TT;
-    const long total = (long)rows * tiles_per_row;
-
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
-        fence_mbarrier_init();
-    }
-    __syncthreads();
-
-    auto issue = [&](long t, int s) {
-        const long r = t / tiles_per_row;
-        const long t0 = (t % tiles_per_row) * TT;
-        const uint32_t bytes = (uint32_t)(N - t0 < TT ? N - t0 : (long)TT) * ROWB;
-        mbar_arrive_expect_tx(&bars[s], bytes);
-        bulk_g2s(smem + s * kTileBytes, k_idx + (r * N + t0) * DI, bytes, &bars[s]);
-    };
-
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            const long t = blockIdx.x + (long)s * gridDim.x;
-            if (t < total) issue(t, s);
+// Reduce-scatter of kR partial sums across the L lanes that share them (lane bits below L):
+// after it, each lane holds the complete sum of one of the kR values, namely acc[0], and
+// the index of that value is returned.  Halving steps exchange half of the remaining
+// values with the partner lane; once one value is left, the remaining steps just add.
+template <int L, int kR>
+SD_DEVINL int reduce_scatter(float (&acc)[kR], int lane) {
+    int base = 0;
+    int count = kR;
+#pragma unroll
+    for (int o = L / 2; o > 0; o >>= 1) {
+        if (count > 1) {
+            const int half = count / 2;
+            const bool hi = (lane & o) != 0;
+#pragma unroll
+            for (int j = 0; j < half; ++j) {
+                const float send = hi ? acc[j] : acc[j + half];
+                const float keep = hi ? acc[j + half] : acc[j];
+                acc[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+            if (hi) base += half;
+            count = half;
+        } else {
+            acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
         }
     }
+    return base;
+}
+
+// Persistent CTAs of kIdxWarps independent warps.  Each warp owns a contiguous range of
+// 4 KB key tiles and runs its own kWarpStages-deep pipeline: lane 0 issues one bulk copy
+// per tile into the warp's ring, all lanes wait on that stage's mbarrier, score the tile
+// and hand the stage back to lane 0 with a warp barrier -- no CTA-wide synchronization.
+// Lane layout within a tile: lane = g * LPR + c; c picks the 16-byte chunk of a row, g
+// one of the GROUPS row groups; the lane accumulates 8 rows (g, g + GROUPS, ...) for its
+// chunk and a reduce-scatter over the LPR lanes leaves each lane one complete row sum.
+template <typename KT, int DI, int VT>
+__global__ void __launch_bounds__(kIdxThreads, 1) index_score_kernel(
+    const void* __restrict__ q_idx, int q_dtype, const KT* __restrict__ k_idx, int rows, int V,
+    int N, float* __restrict__ scores, uint32_t* __restrict__ key_hist, int32_t* err_word) {
+    using U = Unpack16<KT>;
+    constexpr int ROWB = DI * (int)sizeof(KT);  // bytes per key row: 128, 256 or 512
+    constexpr int LPR = ROWB / 16;              // lanes sharing a row
+    constexpr int EPL = U::kElems;              // elements per lane
+    constexpr int TR = kWarpTileBytes / ROWB;   // rows per tile
+    constexpr int GROUPS = 32 / LPR;            // row groups per warp
+    constexpr int RPL = TR / GROUPS;            // rows per lane
+    static_assert(RPL == 8, "each lane accumulates 8 rows");
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t* ring = smem + warp * kWarpStages * kWarpTileBytes;
+    uint64_t* bars =
+        reinterpret_cast<uint64_t*>(smem + kIdxWarps * kWarpStages * kWarpTileBytes) + warp * kWarpStages;
+    const int c = lane % LPR, g = lane / LPR;
+
+    // Tiles are dealt round-robin over all warps of the grid (tile = gw + i * nw), so the
+    // tiles in flight at any moment are neighbours in memory (DRAM page locality).
+    const uint32_t tpr = (uint32_t)((N + TR - 1) / TR);
+    const uint32_t total = (uint32_t)rows * tpr;
+    const uint32_t gw = blockIdx.x * kIdxWarps + warp;
+    const uint32_t nw = gridDim.x * kIdxWarps;
+    const uint32_t ntiles = gw < total ? (total - gw + nw - 1) / nw : 0u;
+
+    pdl_launch_dependents();
+    if (lane == 0) {
+        for (int s = 0; s < kWarpStages; ++s) mbar_init(&bars[s], 1);
+        fence_mbarrier_init();
+    }
+    __syncwarp();
+
+    auto issue = [&](uint32_t j, int s) {  // lane 0: tile j of this warp into stage s
+        const uint32_t t = gw + j * nw;
+        const uint32_t ir = t / tpr, it0 = (t - ir * tpr) * TR;
+        const uint32_t n = min((uint32_t)TR, (uint32_t)N - it0);
+        mbar_arrive_expect_tx(&bars[s], n * ROWB);
+        bulk_g2s(ring + s * kWarpTileBytes, k_idx + ((size_t)ir * N + it0) * DI, n * ROWB, &bars[s]);
+    };
+    if (lane == 0)
+        for (uint32_t s = 0; s < min((uint32_t)kWarpStages, ntiles); ++s) issue(s, (int)s);
 
     float q[VT][EPL];
-    long cur_row = -1;
-    long i = 0;
+    uint32_t q_row = 0xffffffffu;
+    uint32_t i = 0;
     bool timed_out = false;
-    for (;; ++i) {
-        const long t = blockIdx.x + i * gridDim.x;
-        if (t >= total) break;
-        const int s = (int)(i % kStages);
-        const long r = t / tiles_per_row;
-        const long t0 = (t % tiles_per_row) * TT;
-        const int n = (int)(N - t0 < TT ? N - t0 : (long)TT);
-        if (r != cur_row) {
-            cur_row = r;
+    for (; i < ntiles; ++i) {
+        const int s = (int)(i % kWarpStages);
+        const uint32_t t = gw + i * nw;
+        const uint32_t cr = t / tpr, ct0 = (t - cr * tpr) * TR;
+        if (cr != q_row) {
+            q_row = cr;
 #pragma unroll
             for (int v = 0; v < VT; ++v)
 #pragma unroll
                 for (int e = 0; e < EPL; ++e)
-                    q[v][e] = (v < V) ? load_elem(q_idx, q_dtype, (size_t)(r * V + v) * DI + sub * EPL + e)
-                                      : 0.f;
+                    q[v][e] = (v < V) ? load_elem(q_idx, q_dtype, ((size_t)cr * V + v) * DI + c * EPL + e) : 0.f;
         }
-        const bool ok = mbar_wait(&bars[s], (uint32_t)((i / kStages) & 1));
-        if (__syncthreads_or(!ok)) {
+        const bool ok = mbar_wait(&bars[s], (i / kWarpStages) & 1u);
+        if (__any_sync(0xffffffffu, !ok)) {
             timed_out = true;
             break;
         }
-        const uint8_t* tile = smem + s * kTileBytes;
-        float* out = scores + r * N + t0;
+        const uint8_t* tile = ring + s * kWarpTileBytes;
+        float acc[VT][RPL];
 #pragma unroll
-        for (int rr = warp * RPW + rsub; rr < TT; rr += kIdxWarps * RPW) {
+        for (int j = 0; j < RPL; ++j) {
             float x[EPL];
-            U::run(lds128(tile + rr * ROWB + sub * 16), x);
-            float acc[VT];
+            U::run(lds128(tile + (g + GROUPS * j) * ROWB + c * 16), x);
 #pragma unroll
             for (int v = 0; v < VT; ++v) {
-                acc[v] = 0.f;
+                float a = 0.f;
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[v] = fmaf(x[e], q[v][e], acc[v]);
+                for (int e = 0; e < EPL; ++e) a = fmaf(x[e], q[v][e], a);
+                acc[v][j] = a;
             }
-#pragma unroll
-            for (int o = LPR / 2; o > 0; o >>= 1)
-#pragma unroll
-                for (int v = 0; v < VT; ++v) acc[v] += __shfl_xor_sync(0xffffffffu, acc[v], o);
-            float best = acc[0];
-#pragma unroll
-            for (int v = 1; v < VT; ++v)
-                if (v < V) best = fmaxf(best, acc[v]);
-            if (sub == 0 && rr < n) out[rr] = best;
         }
-        __syncthreads();
-        if (tid == 0) {
-            const long tn = blockIdx.x + (i + kStages) * gridDim.x;
-            if (tn < total) {
-                fence_proxy_async_shared();
-                issue(tn, s);
-            }
+        int ridx = 0;
+#pragma unroll
+        for (int v = 0; v < VT; ++v) ridx = reduce_scatter<LPR>(acc[v], lane);
+        float best = acc[0][0];
+#pragma unroll
+        for (int v = 1; v < VT; ++v)
+            if (v < V) best = fmaxf(best, acc[v][0]);
+        // lanes holding a duplicate of the same row (bits below LPR/8) do not store
+        const int row = g + GROUPS * ridx;
+        const uint32_t n = min((uint32_t)TR, (uint32_t)N - ct0);
+        const bool store = (lane & (LPR / 8 - 1)) == 0 && (uint32_t)row < n;
+        if (store) scores[(size_t)cr * N + ct0 + row] = best;
+        if (key_hist != nullptr) {
+            const uint32_t dg = float_key(best) >> 21;
+            const uint32_t peers = __match_any_sync(0xffffffffu, store ? dg : 0xffffffffu);
+            if (store && lane == __ffs(peers) - 1)
+                atomicAdd(&key_hist[(size_t)cr * 2048 + dg], (uint32_t)__popc(peers));
+        }
+        __syncwarp();
+        if (lane == 0 && i + kWarpStages < ntiles) {
+            fence_proxy_async_shared();
+            issue(i + kWarpStages, s);
         }
     }
-    if (timed_out && tid == 0) {
+    if (timed_out && lane == 0) {
         report(err_word, SD_DEVERR_TIMEOUT);
-        // Let the copies this CTA still has in flight land (bounded) before exiting.
-        for (long j = i; j < i + kStages; ++j) {
-            const long t = blockIdx.x + j * gridDim.x;
-            if (t >= total) break;
-            mbar_wait(&bars[j % kStages], (uint32_t)((j / kStages) & 1));
-        }
+        // Let the copies this warp still has in flight land (bounded) before exiting.
+        for (uint32_t j = i; j < ntiles && j < i + kWarpStages; ++j)
+            mbar_wait(&bars[j % kWarpStages], (j / kWarpStages) & 1u);
     }
 }
 
 template <typename KT, int DI, int VT>
 sd_status launch_index_score(const void* q_idx, int q_dtype, const void* k_idx, int rows, int V,
-                             int N, float* scores, int32_t* err_word, cudaStream_t st) {
-    constexpr int ROWB = DI * (int)sizeof(KT);
-    constexpr int TT = kTileBytes / ROWB;
+                             int N, float* scores, uint32_t* key_hist, int32_t* err_word,
+                             cudaStream_t st) {
     auto kern = index_score_kernel<KT, DI, VT>;
-    static bool configured = false;  // attribute is per function; setting it twice is harmless
-    if (!configured) {
-        SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kIdxSmem),
-                      "sd_index_score: cudaFuncSetAttribute");
-        configured = true;
-    }
-    const long total = (long)rows * ((N + TT - 1) / TT);
-    const long grid = std::min<long>(total, (long)num_sms() * kCtasPerSm);
-    kern<<<(unsigned)grid, kIdxThreads, kIdxSmem, st>>>(q_idx, q_dtype,
-                                                        reinterpret_cast<const KT*>(k_idx), rows,
-                                                        V, N, scores, err_word);
+    SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kIdxSmem),
+                  "sd_index_score: cudaFuncSetAttribute");
+    constexpr int TR = kWarpTileBytes / (DI * (int)sizeof(KT));
+    const long tiles = (long)rows * ((N + TR - 1) / TR);
+    const long grid = std::min<long>((tiles + kIdxWarps - 1) / kIdxWarps, (long)num_sms());
+    kern<<<(unsigned)grid, kIdxThreads, kIdxSmem, st>>>(q_idx, q_dtype, reinterpret_cast<const KT*>(k_idx),
+                                                       rows, V, N, scores, key_hist, err_word);
     return launch_status("sd_index_score");
 }
 
@@ -169,7 +200,8 @@ using namespace sd;
 
 extern "C" sd_status sd_index_score(const void* q_idx, sd_dtype q_dtype, const void* k_idx,
                                     sd_dtype k_dtype, int B, int Hkv, int V, int N, int d_idx,
-                                    float* scores, int32_t* err_word, void* stream) {
+                                    float* scores, uint32_t* key_hist, int32_t* err_word,
+                                    void* stream) {
     clear_error();
     SD_REQUIRE(B >= 0 && Hkv >= 0 && N >= 0, "sd_index_score: negative size");
     SD_REQUIRE(valid_dtype(q_dtype) && valid_dtype(k_dtype), "sd_index_score: bad dtype");
@@ -182,21 +214,28 @@ extern "C" sd_status sd_index_score(const void* q_idx, sd_dtype q_dtype, const v
     if (rows == 0 || N == 0) return SD_OK;
     SD_REQUIRE(q_idx && k_idx && scores, "sd_index_score: null pointer");
     SD_REQUIRE(aligned16(k_idx) && aligned16(scores), "sd_index_score: pointers must be 16-byte aligned");
-    SD_REQUIRE(rows <= (1L << 30), "sd_index_score: too many rows");
+    SD_REQUIRE(rows <= (1L << 30) && rows * (long)N < (1L << 36), "sd_index_score: too many rows");
     cudaStream_t st = as_stream(stream);
     const int r = (int)rows;
+    // bf16 keys and queries: the contraction runs on the tensor cores (exact for the
+    // integer-valued indexer: products exact, fp32 sums of integers below 2^24 exact)
+    if (k_dtype == SD_BF16 && q_dtype == SD_BF16) {
+        SD_REQUIRE(aligned16(q_idx), "sd_index_score: q_idx must be 16-byte aligned");
+        SD_REQUIRE((long)rows * N < (1L << 31) && (long)rows * V < (1L << 31), "sd_index_score: too many rows");
+        return index_score_tc_launch(q_idx, k_idx, r, V, N, d_idx, scores, key_hist, err_word, st);
+    }
     if (k_dtype == SD_BF16) {
         if (d_idx == 128)
-            return V == 1 ? launch_index_score<bf16_t, 128, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, err_word, st)
-                          : launch_index_score<bf16_t, 128, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, err_word, st);
-        return V == 1 ? launch_index_score<bf16_t, 64, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, err_word, st)
-                      : launch_index_score<bf16_t, 64, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, err_word, st);
+            return V == 1 ? launch_index_score<bf16_t, 128, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st)
+                          : launch_index_score<bf16_t, 128, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st);
+        return V == 1 ? launch_index_score<bf16_t, 64, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st)
+                      : launch_index_score<bf16_t, 64, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st);
     }
     if (d_idx == 128)
-        return V == 1 ? launch_index_score<float, 128, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, err_word, st)
-                      : launch_index_score<float, 128, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, err_word, st);
-    return V == 1 ? launch_index_score<float, 64, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, err_word, st)
-                  : launch_index_score<float, 64, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, err_word, st);
+        return V == 1 ? launch_index_score<float, 128, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st)
+                      : launch_index_score<float, 128, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st);
+    return V == 1 ? launch_index_score<float, 64, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st)
+                  : launch_index_score<float, 64, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st);
 }
 
 extern "C" sd_status sd_block_pool(const void* k_idx, sd_dtype k_dtype, int B, int Hkv, int T,

@@ -89,6 +89,16 @@ SD_DEVINL void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes, ui
         : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic launch
+
+// Wait until the grids this launch depends on have completed and their writes are
+// visible (a no-op when the kernel was not launched as a programmatic dependent).
+SD_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next kernel in the stream, if launched as a programmatic dependent, to be
+// scheduled now; it still waits (pdl_wait) for this grid to finish before reading.
+SD_DEVINL void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- cp.async (16 B)
 
 SD_DEVINL void cp_async16(void* dst_smem, const void* src) {
@@ -99,6 +109,45 @@ SD_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "me
 template <int N>
 SD_DEVINL void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------- warp-level MMA (m16n8k16)
+
+// Four 8x8 b16 matrices from shared memory; lane l gives the address of row (l & 7) of
+// matrix (l >> 3).  The .trans form transposes each matrix.
+SD_DEVINL void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+SD_DEVINL void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col).
+SD_DEVINL void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two fp32 -> packed bf16x2 (round to nearest even), first value in the low half.
+SD_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): 16 significant bits in two bf16.
+SD_DEVINL void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16x2(x0, x1);
+    const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+    lo = pack_bf16x2(x0 - h0, x1 - h1);
 }
 
 // ---------------------------------------------------------------- element access

@@ -6,6 +6,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <utility>
 
 #include "../../include/sd.h"
 
@@ -36,6 +37,29 @@ inline sd_status launch_status(const char* what) {
         return SD_ERR_CUDA;
     }
     return SD_OK;
+}
+
+// The indexer on the tensor cores (index_score_tc.cu): bf16 keys and queries.
+sd_status index_score_tc_launch(const void* q_idx, const void* k_idx, int rows, int V, int N, int d_idx,
+                                float* scores, uint32_t* key_hist, int32_t* err_word, cudaStream_t st);
+
+// Launches `kern` as a programmatic dependent of the preceding kernel in the stream: it
+// may be scheduled before that kernel finishes and must call pdl_wait() before reading
+// anything the preceding work wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 }  // namespace sd

@@ -48,75 +48,71 @@ SD_DEVINL uint32_t block_inclusive_scan(uint32_t v, uint32_t* wsum) {
     return v + off;
 }
 
-__global__ void __launch_bounds__(kTkThreads, 1)
-    topk_kernel(const float* __restrict__ scores, int N, int k, int32_t* __restrict__ idx_out,
-                int cache_keys) {
-    extern __shared__ __align__(16) uint32_t keys_s[];
-    __shared__ uint32_t hist[kHistBins];
-    __shared__ uint32_t wsum[32];
-    __shared__ uint32_t sel_digit, sel_above;
-    __shared__ uint32_t cnt_gt[kTkWarps], cnt_eq[kTkWarps], base_out[kTkWarps], eq_before[kTkWarps];
+struct TopkShared {
+    uint32_t hist[kHistBins];
+    uint32_t wsum[32];
+    uint32_t sel_digit, sel_above, cand_n;
+    uint32_t cnt_gt[kTkWarps], cnt_eq[kTkWarps], base_out[kTkWarps], eq_before[kTkWarps];
+};
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float* srow = scores + (size_t)blockIdx.x * N;
-    int32_t* orow = idx_out + (size_t)blockIdx.x * k;
-    if (k == 0) return;
-    if (k == N) {
-        for (int i = tid; i < N; i += kTkThreads) orow[i] = i;
-        return;
+// Given the histogram of one digit (nb bins, higher bins = larger keys) of the entries
+// still in the running, pick the digit holding the krem-th largest: returns it and how
+// many of those entries lie in higher bins.  Thread t owns bins [nb - per*(t+1), nb - per*t).
+SD_DEVINL void select_digit(TopkShared& sh, uint32_t nb, int krem, uint32_t& digit, uint32_t& above) {
+    const int tid = threadIdx.x;
+    if (tid == 0) {  // defined even if no bin crosses (a histogram that does not match)
+        sh.sel_digit = 0;
+        sh.sel_above = 0;
     }
-    if (cache_keys) {
-        for (int i = tid; i < N; i += kTkThreads) keys_s[i] = float_key(srow[i]);
-        __syncthreads();
-    }
-    auto key_at = [&](int i) -> uint32_t { return cache_keys ? keys_s[i] : float_key(srow[i]); };
-
-    // ---- radix select of the k-th largest key
-    uint32_t prefix = 0, pmask = 0;
-    int krem = k;
-#pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-        const uint32_t nb = pass == 2 ? 1024u : 2048u;
-        for (int b = tid; b < kHistBins; b += kTkThreads) hist[b] = 0;
-        __syncthreads();
-        for (int base = warp * 32; base < N; base += kTkThreads) {
-            const int i = base + lane;
-            const bool valid = i < N;
-            const uint32_t kk = valid ? key_at(i) : 0u;
-            const bool in = valid && (kk & pmask) == prefix;
-            const uint32_t dg = (kk >> shift) & (nb - 1);
-            const uint32_t peers = __match_any_sync(0xffffffffu, in ? dg : 0xffffffffu);
-            if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], (uint32_t)__popc(peers));
-        }
-        __syncthreads();
-        // Thread t owns the bins [nb - per*(t+1), nb - per*t): thread 0 the highest.
-        const int per = (int)nb / kTkThreads;
-        const int hi = (int)nb - per * tid;  // exclusive upper bin
-        uint32_t local = 0;
-        for (int b = hi - per; b < hi; ++b) local += hist[b];
-        const uint32_t incl = block_inclusive_scan(local, wsum);
-        const uint32_t excl = incl - local;
-        if (excl < (uint32_t)krem && (uint32_t)krem <= incl) {
-            uint32_t above = excl;
-            for (int b = hi - 1; b >= hi - per; --b) {
-                if (above + hist[b] >= (uint32_t)krem) {
-                    sel_digit = (uint32_t)b;
-                    sel_above = above;
-                    break;
-                }
-                above += hist[b];
+    const int per = (int)nb / kTkThreads;
+    const int hi = (int)nb - per * tid;
+    uint32_t local = 0;
+    for (int b = hi - per; b < hi; ++b) local += sh.hist[b];
+    const uint32_t incl = block_inclusive_scan(local, sh.wsum);
+    const uint32_t excl = incl - local;
+    if (excl < (uint32_t)krem && (uint32_t)krem <= incl) {
+        uint32_t acc = excl;
+        for (int b = hi - 1; b >= hi - per; --b) {
+            if (acc + sh.hist[b] >= (uint32_t)krem) {
+                sh.sel_digit = (uint32_t)b;
+                sh.sel_above = acc;
+                break;
             }
+            acc += sh.hist[b];
         }
-        __syncthreads();
-        prefix |= sel_digit << shift;
-        pmask |= (nb - 1) << shift;
-        krem -= (int)sel_above;
-        __syncthreads();
     }
-    const uint32_t thr = prefix;
+    __syncthreads();
+    digit = sh.sel_digit;
+    above = sh.sel_above;
+    __syncthreads();
+}
 
-    // ---- ordered emit: warp w scans [w*seg, (w+1)*seg)
+// Histogram pass over all N keys: counts the digit (kk >> shift) & (nb - 1) of every key
+// whose bits under pmask equal prefix (warp-aggregated shared atomics).
+template <typename KeyAt>
+SD_DEVINL void hist_pass_all(TopkShared& sh, KeyAt key_at, int N, uint32_t prefix, uint32_t pmask,
+                             int shift, uint32_t nb) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int b = tid; b < kHistBins; b += kTkThreads) sh.hist[b] = 0;
+    __syncthreads();
+    for (int base = warp * 32; base < N; base += kTkThreads) {
+        const int i = base + lane;
+        const bool valid = i < N;
+        const uint32_t kk = valid ? key_at(i) : 0u;
+        const bool in = valid && (kk & pmask) == prefix;
+        const uint32_t dg = (kk >> shift) & (nb - 1);
+        const uint32_t peers = __match_any_sync(0xffffffffu, in ? dg : 0xffffffffu);
+        if (in && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[dg], (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+}
+
+// Ordered emit: every key > thr and the first krem keys == thr (lowest indices), written
+// in ascending index order.  Warp w scans the contiguous segment [w*seg, (w+1)*seg).
+template <typename KeyAt>
+SD_DEVINL void emit_selected(TopkShared& sh, KeyAt key_at, int N, int k, uint32_t thr, int krem,
+                             int32_t* orow) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int seg = ((N + kTkWarps - 1) / kTkWarps + 31) / 32 * 32;
     const int s0 = warp * seg, s1 = min(N, s0 + seg);
     uint32_t gt = 0, eq = 0;
@@ -128,22 +124,22 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         eq += __popc(__ballot_sync(0xffffffffu, valid && kk == thr));
     }
     if (lane == 0) {
-        cnt_gt[warp] = gt;
-        cnt_eq[warp] = eq;
+        sh.cnt_gt[warp] = gt;
+        sh.cnt_eq[warp] = eq;
     }
     __syncthreads();
     if (tid == 0) {
         uint32_t eqb = 0, ob = 0;
         for (int w = 0; w < kTkWarps; ++w) {
-            eq_before[w] = eqb;
-            const int take = max(0, min((int)cnt_eq[w], krem - (int)eqb));
-            base_out[w] = ob;
-            ob += cnt_gt[w] + (uint32_t)take;
-            eqb += cnt_eq[w];
+            sh.eq_before[w] = eqb;
+            const int take = max(0, min((int)sh.cnt_eq[w], krem - (int)eqb));
+            sh.base_out[w] = ob;
+            ob += sh.cnt_gt[w] + (uint32_t)take;
+            eqb += sh.cnt_eq[w];
         }
     }
     __syncthreads();
-    uint32_t eq_seen = eq_before[warp], pos = base_out[warp];
+    uint32_t eq_seen = sh.eq_before[warp], pos = sh.base_out[warp];
     const uint32_t lt = lanemask_lt();
     for (int base = s0; base < s1; base += 32) {
         const int i = base + lane;
@@ -161,6 +157,170 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     }
 }
 
+// Loads the order keys of row `srow` into keys_s.  A 16-byte aligned row goes in with one
+// bulk copy (TMA) completed on `bar`, converted in place afterwards; otherwise each thread
+// loads 8 scores before converting any, so every thread keeps 8 loads in flight.
+// Returns false (uniformly) if the bulk copy did not complete in time.
+SD_DEVINL bool stage_keys(const float* srow, int N, uint32_t* keys_s, uint64_t* bar) {
+    const int tid = threadIdx.x;
+    const bool bulk = ((reinterpret_cast<uintptr_t>(srow) | (uintptr_t)(N * 4)) & 15u) == 0;
+    if (bulk) {
+        if (tid == 0) {
+            mbar_init(bar, 1);
+            fence_mbarrier_init();
+            mbar_arrive_expect_tx(bar, (uint32_t)N * 4u);
+            bulk_g2s(keys_s, srow, (uint32_t)N * 4u, bar);
+        }
+        __syncthreads();
+        const bool ok = mbar_wait(bar, 0);
+        if (__syncthreads_or(!ok)) return false;
+        for (int i = tid; i < N; i += kTkThreads) keys_s[i] = float_key(__uint_as_float(keys_s[i]));
+    } else {
+        for (int base = tid; base < N; base += 8 * kTkThreads) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = base + u * kTkThreads;
+                v[u] = i < N ? srow[i] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = base + u * kTkThreads;
+                if (i < N) keys_s[i] = float_key(v[u]);
+            }
+        }
+    }
+    __syncthreads();
+    return true;
+}
+
+// Digit layout of the 32-bit order key: 11 + 11 + 10 bits, most significant first.
+__device__ constexpr int kShift[3] = {21, 10, 0};
+
+// Plain variant: three histogram passes over the row, then the ordered emit.
+__global__ void __launch_bounds__(kTkThreads, 1)
+    topk_kernel(const float* __restrict__ scores, int N, int k, int32_t* __restrict__ idx_out,
+                int cache_keys, int32_t* err_word) {
+    extern __shared__ __align__(16) uint32_t keys_s[];
+    __shared__ TopkShared sh;
+    __shared__ __align__(8) uint64_t stage_bar;
+    const int tid = threadIdx.x;
+    const float* srow = scores + (size_t)blockIdx.x * N;
+    int32_t* orow = idx_out + (size_t)blockIdx.x * k;
+    pdl_wait();
+    pdl_launch_dependents();
+    if (k == 0) return;
+    if (k == N) {
+        for (int i = tid; i < N; i += kTkThreads) orow[i] = i;
+        return;
+    }
+    if (cache_keys && !stage_keys(srow, N, keys_s, &stage_bar)) {
+        if (tid == 0) report(err_word, SD_DEVERR_TIMEOUT);
+        return;
+    }
+    auto key_at = [&](int i) -> uint32_t { return cache_keys ? keys_s[i] : float_key(srow[i]); };
+    uint32_t prefix = 0, pmask = 0;
+    int krem = k;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const uint32_t nb = pass == 2 ? 1024u : 2048u;
+        hist_pass_all(sh, key_at, N, prefix, pmask, kShift[pass], nb);
+        uint32_t dg, above;
+        select_digit(sh, nb, krem, dg, above);
+        prefix |= dg << kShift[pass];
+        pmask |= (nb - 1) << kShift[pass];
+        krem -= (int)above;
+    }
+    emit_selected(sh, key_at, N, k, prefix, krem, orow);
+}
+
+constexpr int kCandCap = 8192;
+
+// Histogram-seeded variant: the first digit's histogram comes from sd_index_score.  The
+// row's keys are staged in shared memory when they fit; one pass collects the keys of the
+// selected top digit (candidates); the remaining two digits are resolved among the
+// candidates; then the ordered emit.  Falls back to full passes when the candidates do not
+// fit.  Leaves the histogram row zeroed for the next call.
+__global__ void __launch_bounds__(kTkThreads, 1)
+    topk_hist_kernel(const float* __restrict__ scores, int N, int k, int32_t* __restrict__ idx_out,
+                     uint32_t* __restrict__ key_hist, int cache_keys, int32_t* err_word) {
+    extern __shared__ __align__(16) uint32_t dyn[];
+    __shared__ TopkShared sh;
+    __shared__ __align__(8) uint64_t stage_bar;
+    uint32_t* keys_s = dyn;
+    uint32_t* cand = dyn + (cache_keys ? N : 0);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float* srow = scores + (size_t)blockIdx.x * N;
+    int32_t* orow = idx_out + (size_t)blockIdx.x * k;
+    uint32_t* hrow = key_hist + (size_t)blockIdx.x * kHistBins;
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int b = tid; b < kHistBins; b += kTkThreads) {
+        sh.hist[b] = hrow[b];
+        hrow[b] = 0u;
+    }
+    if (tid == 0) sh.cand_n = 0;
+    __syncthreads();
+    if (k == 0) return;
+    if (k == N) {
+        for (int i = tid; i < N; i += kTkThreads) orow[i] = i;
+        return;
+    }
+    if (cache_keys && !stage_keys(srow, N, keys_s, &stage_bar)) {
+        if (tid == 0) report(err_word, SD_DEVERR_TIMEOUT);
+        return;
+    }
+    auto key_at = [&](int i) -> uint32_t { return cache_keys ? keys_s[i] : float_key(srow[i]); };
+    uint32_t d0, above;
+    select_digit(sh, 2048u, k, d0, above);
+    uint32_t n_cand = sh.hist[d0 & (kHistBins - 1)];
+    uint32_t prefix = d0 << 21, pmask = 0x7ffu << 21;
+    int krem = k - (int)above;
+    const bool gather = n_cand <= (uint32_t)kCandCap;
+    if (gather) {
+        const uint32_t lt = lanemask_lt();
+        for (int base = warp * 32; base < N; base += kTkThreads) {
+            const int i = base + lane;
+            const bool valid = i < N;
+            const uint32_t kk = valid ? key_at(i) : 0u;
+            const bool in = valid && (kk >> 21) == d0;
+            const uint32_t m = __ballot_sync(0xffffffffu, in);
+            if (m != 0u) {
+                const int leader = __ffs(m) - 1;
+                uint32_t at = 0;
+                if (lane == leader) at = atomicAdd(&sh.cand_n, (uint32_t)__popc(m));
+                at = __shfl_sync(0xffffffffu, at, leader);
+                const uint32_t slot = at + __popc(m & lt);
+                if (in && slot < (uint32_t)kCandCap) cand[slot] = kk;
+            }
+        }
+        __syncthreads();
+        n_cand = min(sh.cand_n, (uint32_t)kCandCap);
+    }
+#pragma unroll 1
+    for (int pass = 1; pass < 3; ++pass) {
+        const uint32_t nb = pass == 2 ? 1024u : 2048u;
+        const int shift = kShift[pass];
+        if (gather) {
+            for (int b = tid; b < kHistBins; b += kTkThreads) sh.hist[b] = 0;
+            __syncthreads();
+            for (uint32_t cidx = tid; cidx < n_cand; cidx += kTkThreads) {
+                const uint32_t ck = cand[cidx];
+                if ((ck & pmask) == prefix) atomicAdd(&sh.hist[(ck >> shift) & (nb - 1)], 1u);
+            }
+            __syncthreads();
+        } else {
+            hist_pass_all(sh, key_at, N, prefix, pmask, shift, nb);
+        }
+        uint32_t dg, ab;
+        select_digit(sh, nb, krem, dg, ab);
+        prefix |= dg << shift;
+        pmask |= (nb - 1) << shift;
+        krem -= (int)ab;
+    }
+    emit_selected(sh, key_at, N, k, prefix, krem, orow);
+}
+
 }  // namespace
 }  // namespace sd
 
@@ -174,22 +334,37 @@ extern "C" size_t sd_topk_workspace_bytes(int rows, int N, int k) {
 }
 
 extern "C" sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx,
-                             void* workspace, size_t workspace_bytes, void* stream) {
+                             uint32_t* key_hist, void* workspace, size_t workspace_bytes,
+                             void* stream) {
     (void)workspace;
     (void)workspace_bytes;
     clear_error();
     SD_REQUIRE(rows >= 0 && N >= 0, "sd_topk: negative size");
     SD_REQUIRE(k >= 0 && k <= N, "sd_topk: k (%d) must be in [0, N=%d]", k, N);
-    if (rows == 0 || k == 0) return SD_OK;
-    SD_REQUIRE(scores && idx, "sd_topk: null pointer");
+    if (rows == 0) return SD_OK;
+    if (key_hist == nullptr && k == 0) return SD_OK;
+    SD_REQUIRE(scores && (k == 0 || idx), "sd_topk: null pointer");
     const size_t key_bytes = (size_t)N * sizeof(uint32_t);
-    const size_t static_bytes = 16 * 1024;
-    const int cache = key_bytes + static_bytes <= (size_t)max_smem_optin() ? 1 : 0;
-    const size_t dyn = cache ? key_bytes : 0;
-    if (dyn > 48 * 1024)
-        SD_CUDA_CHECK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)dyn),
-                      "sd_topk: cudaFuncSetAttribute");
-    topk_kernel<<<rows, kTkThreads, dyn, as_stream(stream)>>>(scores, N, k, idx, cache);
+    const size_t cand_bytes = key_hist ? (size_t)kCandCap * sizeof(uint32_t) : 0;
+    const size_t static_bytes = sizeof(TopkShared) + 1024;
+    const size_t limit = (size_t)max_smem_optin();
+    const int cache = key_bytes + cand_bytes + static_bytes <= limit ? 1 : 0;
+    const size_t dyn = (cache ? key_bytes : 0) + cand_bytes;
+    cudaStream_t st = as_stream(stream);
+    if (key_hist != nullptr) {
+        if (dyn > 48 * 1024)
+            SD_CUDA_CHECK(cudaFuncSetAttribute(topk_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)dyn),
+                          "sd_topk: cudaFuncSetAttribute");
+        SD_CUDA_CHECK(launch_pdl(topk_hist_kernel, rows, kTkThreads, dyn, st, scores, N, k, idx, key_hist, cache, (int32_t*)nullptr),
+                      "sd_topk: launch");
+    } else {
+        if (dyn > 48 * 1024)
+            SD_CUDA_CHECK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)dyn),
+                          "sd_topk: cudaFuncSetAttribute");
+        SD_CUDA_CHECK(launch_pdl(topk_kernel, rows, kTkThreads, dyn, st, scores, N, k, idx, cache, (int32_t*)nullptr),
+                      "sd_topk: launch");
+    }
     return launch_status("sd_topk");
 }
