@@ -422,7 +422,7 @@ def run_ours(args):
     dom_s = statistics.mean(dom_ms) / 1e3
     achieved = by["dominant"] / dom_s / 1e9
     if isinstance(step, SparseDecodeStep):
-        kernel_file, kernel_tag = ("index_score.cu", "sd_common.cuh"), "index_score"
+        kernel_file, kernel_tag = ("index_score.cu", "index_score_tc.cu", "tc_common.cuh", "sd_common.cuh"), "index_score"
     else:
         kernel_file, kernel_tag = ("gather_attend.cu", "sd_common.cuh"), "gather_attend"
     traffic = profiled_traffic(args.workload, kernel_tag, source_digest(*kernel_file))

@@ -234,21 +234,39 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     emit_selected(sh, key_at, N, k, prefix, krem, orow);
 }
 
-constexpr int kCandCap = 8192;
+constexpr int kCandCap = 4096;
 
-// Histogram-seeded variant: the first digit's histogram comes from sd_index_score.  The
-// row's keys are staged in shared memory when they fit; one pass collects the keys of the
-// selected top digit (candidates); the remaining two digits are resolved among the
-// candidates; then the ordered emit.  Falls back to full passes when the candidates do not
-// fit.  Leaves the histogram row zeroed for the next call.
+// Block-wide exclusive prefix sum of one value per thread; also returns the total.
+SD_DEVINL uint32_t block_exclusive_scan(uint32_t v, uint32_t* wsum, uint32_t& total) {
+    const uint32_t incl = block_inclusive_scan(v, wsum);
+    if ((int)threadIdx.x == kTkThreads - 1) wsum[0] = incl;
+    __syncthreads();
+    total = wsum[0];
+    __syncthreads();
+    return incl - v;
+}
+
+// Histogram-seeded variant, bitmap emit.  The first digit's histogram comes from
+// sd_index_score and picks the top digit d0.  One pass over the row (staged in shared
+// memory when it fits) marks every entry whose digit is above d0 in a selection bitmap
+// (a warp's 32 consecutive entries = one bitmap word, written from a ballot) and collects
+// the entries of digit d0 (candidates, with their indices).  The last 21 bits are resolved
+// among the candidates; candidates above the threshold join the bitmap, those equal to it
+// go to a tie bitmap of which a prefix scan keeps the lowest-index ones still needed; a
+// prefix scan over the selection bitmap writes the indices in ascending order.  Falls back
+// to full passes when the candidates exceed their buffer.  Leaves the histogram zeroed.
 __global__ void __launch_bounds__(kTkThreads, 1)
     topk_hist_kernel(const float* __restrict__ scores, int N, int k, int32_t* __restrict__ idx_out,
                      uint32_t* __restrict__ key_hist, int cache_keys, int32_t* err_word) {
     extern __shared__ __align__(16) uint32_t dyn[];
     __shared__ TopkShared sh;
     __shared__ __align__(8) uint64_t stage_bar;
+    const int NW = (N + 31) / 32;  // bitmap words
     uint32_t* keys_s = dyn;
-    uint32_t* cand = dyn + (cache_keys ? N : 0);
+    uint32_t* cand_key = dyn + (cache_keys ? N : 0);
+    uint32_t* cand_idx = cand_key + kCandCap;
+    uint32_t* sel = cand_idx + kCandCap;
+    uint32_t* tie = sel + NW;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float* srow = scores + (size_t)blockIdx.x * N;
     int32_t* orow = idx_out + (size_t)blockIdx.x * k;
@@ -258,6 +276,10 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     for (int b = tid; b < kHistBins; b += kTkThreads) {
         sh.hist[b] = hrow[b];
         hrow[b] = 0u;
+    }
+    for (int w = tid; w < NW; w += kTkThreads) {
+        sel[w] = 0u;
+        tie[w] = 0u;
     }
     if (tid == 0) sh.cand_n = 0;
     __syncthreads();
@@ -273,52 +295,123 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     auto key_at = [&](int i) -> uint32_t { return cache_keys ? keys_s[i] : float_key(srow[i]); };
     uint32_t d0, above;
     select_digit(sh, 2048u, k, d0, above);
-    uint32_t n_cand = sh.hist[d0 & (kHistBins - 1)];
-    uint32_t prefix = d0 << 21, pmask = 0x7ffu << 21;
+    d0 &= (kHistBins - 1);
     int krem = k - (int)above;
-    const bool gather = n_cand <= (uint32_t)kCandCap;
-    if (gather) {
+    if (sh.hist[d0] > (uint32_t)kCandCap) {
+        // too many candidates for the buffer: resolve the remaining digits over the row
+        uint32_t prefix = d0 << 21, pmask = 0x7ffu << 21;
+#pragma unroll 1
+        for (int pass = 1; pass < 3; ++pass) {
+            const uint32_t nb = pass == 2 ? 1024u : 2048u;
+            hist_pass_all(sh, key_at, N, prefix, pmask, kShift[pass], nb);
+            uint32_t dg, ab;
+            select_digit(sh, nb, krem, dg, ab);
+            prefix |= dg << kShift[pass];
+            pmask |= (nb - 1) << kShift[pass];
+            krem -= (int)ab;
+        }
+        emit_selected(sh, key_at, N, k, prefix, krem, orow);
+        return;
+    }
+    // ---- one pass: bitmap of entries above d0, candidates of digit d0
+    {
         const uint32_t lt = lanemask_lt();
-        for (int base = warp * 32; base < N; base += kTkThreads) {
-            const int i = base + lane;
-            const bool valid = i < N;
-            const uint32_t kk = valid ? key_at(i) : 0u;
-            const bool in = valid && (kk >> 21) == d0;
-            const uint32_t m = __ballot_sync(0xffffffffu, in);
-            if (m != 0u) {
-                const int leader = __ffs(m) - 1;
-                uint32_t at = 0;
-                if (lane == leader) at = atomicAdd(&sh.cand_n, (uint32_t)__popc(m));
-                at = __shfl_sync(0xffffffffu, at, leader);
-                const uint32_t slot = at + __popc(m & lt);
-                if (in && slot < (uint32_t)kCandCap) cand[slot] = kk;
+        constexpr int U = 4;  // 32-entry groups a warp loads before using any
+        for (int g0 = warp; g0 < NW; g0 += U * kTkWarps) {
+            uint32_t kk[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = (g0 + u * kTkWarps) * 32 + lane;
+                kk[u] = (g0 + u * kTkWarps < NW && i < N) ? key_at(i) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int gw = g0 + u * kTkWarps;
+                if (gw >= NW) break;
+                const int i = gw * 32 + lane;
+                const bool valid = i < N;
+                const uint32_t dg = kk[u] >> 21;
+                const uint32_t sure = __ballot_sync(0xffffffffu, valid && dg > d0);
+                if (lane == 0) sel[gw] = sure;
+                const bool in = valid && dg == d0;
+                const uint32_t m = __ballot_sync(0xffffffffu, in);
+                if (m != 0u) {
+                    const int leader = __ffs(m) - 1;
+                    uint32_t at = 0;
+                    if (lane == leader) at = atomicAdd(&sh.cand_n, (uint32_t)__popc(m));
+                    at = __shfl_sync(0xffffffffu, at, leader);
+                    const uint32_t slot = at + __popc(m & lt);
+                    if (in && slot < (uint32_t)kCandCap) {
+                        cand_key[slot] = kk[u];
+                        cand_idx[slot] = (uint32_t)i;
+                    }
+                }
             }
         }
-        __syncthreads();
-        n_cand = min(sh.cand_n, (uint32_t)kCandCap);
     }
+    __syncthreads();
+    const uint32_t n_cand = min(sh.cand_n, (uint32_t)kCandCap);
+    // ---- remaining 21 bits among the candidates
+    uint32_t prefix = d0 << 21, pmask = 0x7ffu << 21;
 #pragma unroll 1
     for (int pass = 1; pass < 3; ++pass) {
         const uint32_t nb = pass == 2 ? 1024u : 2048u;
         const int shift = kShift[pass];
-        if (gather) {
-            for (int b = tid; b < kHistBins; b += kTkThreads) sh.hist[b] = 0;
-            __syncthreads();
-            for (uint32_t cidx = tid; cidx < n_cand; cidx += kTkThreads) {
-                const uint32_t ck = cand[cidx];
-                if ((ck & pmask) == prefix) atomicAdd(&sh.hist[(ck >> shift) & (nb - 1)], 1u);
-            }
-            __syncthreads();
-        } else {
-            hist_pass_all(sh, key_at, N, prefix, pmask, shift, nb);
+        for (int b = tid; b < kHistBins; b += kTkThreads) sh.hist[b] = 0;
+        __syncthreads();
+        for (uint32_t c = tid; c < n_cand; c += kTkThreads) {
+            const uint32_t ck = cand_key[c];
+            if ((ck & pmask) == prefix) atomicAdd(&sh.hist[(ck >> shift) & (nb - 1)], 1u);
         }
+        __syncthreads();
         uint32_t dg, ab;
         select_digit(sh, nb, krem, dg, ab);
         prefix |= dg << shift;
         pmask |= (nb - 1) << shift;
         krem -= (int)ab;
     }
-    emit_selected(sh, key_at, N, k, prefix, krem, orow);
+    const uint32_t thr = prefix;
+    for (uint32_t c = tid; c < n_cand; c += kTkThreads) {
+        const uint32_t ck = cand_key[c], ci = cand_idx[c];
+        if (ck > thr) atomicOr(&sel[ci >> 5], 1u << (ci & 31));
+        else if (ck == thr) atomicOr(&tie[ci >> 5], 1u << (ci & 31));
+    }
+    __syncthreads();
+    // ---- keep the krem lowest-index ties; thread t owns words [t*W, t*W + W)
+    const int W = (NW + kTkThreads - 1) / kTkThreads;
+    const int w0 = tid * W, w1 = min(NW, w0 + W);
+    {
+        uint32_t cnt = 0;
+        for (int w = w0; w < w1; ++w) cnt += __popc(tie[w]);
+        uint32_t total;
+        uint32_t before = block_exclusive_scan(cnt, sh.wsum, total);
+        for (int w = w0; w < w1; ++w) {
+            uint32_t bits = tie[w];
+            while (bits != 0u && (int)before < krem) {
+                const uint32_t low = bits & (0u - bits);
+                sel[w] |= low;
+                bits ^= low;
+                ++before;
+            }
+        }
+    }
+    __syncthreads();
+    // ---- ascending emit from the selection bitmap
+    {
+        uint32_t cnt = 0;
+        for (int w = w0; w < w1; ++w) cnt += __popc(sel[w]);
+        uint32_t total;
+        uint32_t at = block_exclusive_scan(cnt, sh.wsum, total);
+        for (int w = w0; w < w1; ++w) {
+            uint32_t bits = sel[w];
+            while (bits != 0u) {
+                const int bpos = __ffs(bits) - 1;
+                bits &= bits - 1u;
+                if (at < (uint32_t)k) orow[at] = w * 32 + bpos;
+                ++at;
+            }
+        }
+    }
 }
 
 }  // namespace
@@ -344,24 +437,32 @@ extern "C" sd_status sd_topk(const float* scores, int rows, int N, int k, int32_
     if (rows == 0) return SD_OK;
     if (key_hist == nullptr && k == 0) return SD_OK;
     SD_REQUIRE(scores && (k == 0 || idx), "sd_topk: null pointer");
-    const size_t key_bytes = (size_t)N * sizeof(uint32_t);
-    const size_t cand_bytes = key_hist ? (size_t)kCandCap * sizeof(uint32_t) : 0;
-    const size_t static_bytes = sizeof(TopkShared) + 1024;
-    const size_t limit = (size_t)max_smem_optin();
-    const int cache = key_bytes + cand_bytes + static_bytes <= limit ? 1 : 0;
-    const size_t dyn = (cache ? key_bytes : 0) + cand_bytes;
     cudaStream_t st = as_stream(stream);
+    const size_t limit = (size_t)max_smem_optin();
+    const size_t static_bytes = sizeof(TopkShared) + 1024;
+    const size_t key_bytes = (size_t)N * sizeof(uint32_t);
+    const size_t aux_bytes = (size_t)2 * kCandCap * sizeof(uint32_t) + (size_t)2 * ((N + 31) / 32) * sizeof(uint32_t);
+    if (key_hist != nullptr && aux_bytes + static_bytes > limit) {
+        // the bitmaps do not fit: plain select, and clear the histogram as promised
+        SD_CUDA_CHECK(cudaMemsetAsync(key_hist, 0, (size_t)rows * kHistBins * sizeof(uint32_t), st),
+                      "sd_topk: clearing key_hist");
+        key_hist = nullptr;
+        if (k == 0) return SD_OK;
+    }
     if (key_hist != nullptr) {
+        const int cache = key_bytes + aux_bytes + static_bytes <= limit ? 1 : 0;
+        const size_t dyn = (cache ? key_bytes : 0) + aux_bytes;
         if (dyn > 48 * 1024)
-            SD_CUDA_CHECK(cudaFuncSetAttribute(topk_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)dyn),
+            SD_CUDA_CHECK(cudaFuncSetAttribute(topk_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn),
                           "sd_topk: cudaFuncSetAttribute");
-        SD_CUDA_CHECK(launch_pdl(topk_hist_kernel, rows, kTkThreads, dyn, st, scores, N, k, idx, key_hist, cache, (int32_t*)nullptr),
+        SD_CUDA_CHECK(launch_pdl(topk_hist_kernel, rows, kTkThreads, dyn, st, scores, N, k, idx, key_hist, cache,
+                                 (int32_t*)nullptr),
                       "sd_topk: launch");
     } else {
+        const int cache = key_bytes + static_bytes <= limit ? 1 : 0;
+        const size_t dyn = cache ? key_bytes : 0;
         if (dyn > 48 * 1024)
-            SD_CUDA_CHECK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)dyn),
+            SD_CUDA_CHECK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn),
                           "sd_topk: cudaFuncSetAttribute");
         SD_CUDA_CHECK(launch_pdl(topk_kernel, rows, kTkThreads, dyn, st, scores, N, k, idx, cache, (int32_t*)nullptr),
                       "sd_topk: launch");
