@@ -88,8 +88,9 @@ def test_c3_block_sparse_full():
     pooled = sd().sd_block_pool(g["k_idx"], w.block)
     rp = oracle.block_pool(x["k_idx"], w.B, w.Hkv, w.T, w.dI, w.block)
     np.testing.assert_array_equal(pooled.cpu().numpy().astype(np.float64), rp)
-    scores = sd().sd_index_score(g["q_idx"], pooled)
-    idx = sd().sd_topk(scores, w.k)
+    hist = sd().key_hist_buffer(w.B * w.Hkv)
+    scores = sd().sd_index_score(g["q_idx"], pooled, key_hist=hist)
+    idx = sd().sd_topk(scores, w.k, key_hist=hist)
     out, lse, _ = sd().gather_attend(g["q"], g["k"], g["v"], idx, block=w.block, T=w.T)
     rs = oracle.index_score(x["q_idx"], rp.astype(np.float32), w.B, w.Hkv, w.V, w.N, w.dI)
     np.testing.assert_array_equal(scores.cpu().numpy().astype(np.float64), rs)

@@ -79,7 +79,7 @@ def test_block_pool_bit_exact(T, dI, block, dt):
 # --------------------------------------------------------------------------- top-k
 
 
-@pytest.mark.parametrize("N", [1, 7, 100, 1000, 4096, 32768, 65536, 131072])
+@pytest.mark.parametrize("N", [1, 7, 100, 1000, 2048, 4096, 32768, 65536, 131072])
 def test_topk_bit_exact_with_ties(N):
     rng = np.random.default_rng(N)
     rows = 5
@@ -113,6 +113,8 @@ def test_topk_float_scores_and_signed_zero():
     (1, 1, 1, 3000, 0, False),
     (1, 1, 1, 3000, 3000, False),
     (3, 1, 3, 777, 13, False),
+    (2, 3, 1, 2048, 64, False),       # block-selection shape: static + dynamic smem > 48 KB
+    (1, 2, 1, 12000, 50, False),      # N between the cached and uncached sizes
 ])
 def test_index_topk_with_key_histogram(B, Hkv, V, N, k, flat):
     g = torch.Generator().manual_seed(N + k)

@@ -26,7 +26,7 @@ namespace {
 
 constexpr int kAttThreads = 128;
 constexpr int kCH = 64;             // rows per staged chunk
-constexpr int kMaxSplitRows = 512;  // rows whose sources a CTA resolves up front
+constexpr int kMaxSplitRows = 448;  // rows whose sources a CTA resolves up front
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr int32_t kNoRow = INT32_MIN;  // source code of a skipped (invalid) row
@@ -96,24 +96,42 @@ SD_DEVINL void merge_if_last(const AttendParams& p, int b, int kvh, int RP, floa
     __syncthreads();
     if (!flag_s[0]) return;
     __threadfence();
-    const int S = p.splits;
-    const int cap = scratch_floats / RP - 1;  // splits whose weights fit at once
+    const int S = p.splits, R = p.R;
+    // scratch: m[S][R], then w[S][R] (weights), then lse-ready row maxima; all loads of the
+    // splits' m and l go out at once (one per thread), not as per-row loops
+    const int cap = scratch_floats / (2 * R) - 1;
     for (int s0 = 0; s0 < S; s0 += cap) {
-        const int s1 = min(S, s0 + cap);
+        const int s1 = min(S, s0 + cap), ns = s1 - s0;
+        float* mm = scratch;            // [ns][R]
+        float* ww = scratch + ns * R;   // [ns][R]
         __syncthreads();
-        if (tid < p.R) {
+        for (int e = tid; e < ns * R; e += nthr) {
+            const int s = s0 + e / R, r = e % R;
+            const size_t prow = ((size_t)bk * S + s) * RP + r;
+            mm[e] = __ldcg(p.ws_m + prow);
+            ww[e] = __ldcg(p.ws_l + prow);
+        }
+        __syncthreads();
+        if (tid < R) {
+            // global maximum and sum over all splits (the other chunks re-read m, l)
             const int r = tid;
-            float M = -INFINITY;
-            for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(p.ws_m + ((size_t)bk * S + s) * RP + r));
-            float Ls = 0.f;
+            float M = -INFINITY, Ls = 0.f;
+            for (int s = 0; s < S; ++s) {
+                const size_t prow = ((size_t)bk * S + s) * RP + r;
+                const float m = (s >= s0 && s < s1) ? mm[(s - s0) * R + r] : __ldcg(p.ws_m + prow);
+                M = fmaxf(M, m);
+            }
             if (M != -INFINITY)
                 for (int s = 0; s < S; ++s) {
-                    const float m = __ldcg(p.ws_m + ((size_t)bk * S + s) * RP + r);
-                    if (m != -INFINITY) Ls = fmaf(__ldcg(p.ws_l + ((size_t)bk * S + s) * RP + r), exp2f(m - M), Ls);
+                    const size_t prow = ((size_t)bk * S + s) * RP + r;
+                    const bool here = s >= s0 && s < s1;
+                    const float m = here ? mm[(s - s0) * R + r] : __ldcg(p.ws_m + prow);
+                    const float l = here ? ww[(s - s0) * R + r] : __ldcg(p.ws_l + prow);
+                    if (m != -INFINITY) Ls = fmaf(l, exp2f(m - M), Ls);
                 }
             for (int s = s0; s < s1; ++s) {
-                const float m = __ldcg(p.ws_m + ((size_t)bk * S + s) * RP + r);
-                scratch[(s - s0) * RP + r] = (Ls > 0.f && m != -INFINITY) ? exp2f(m - M) / Ls : 0.f;
+                const float m = mm[(s - s0) * R + r];
+                ww[(s - s0) * R + r] = (Ls > 0.f && m != -INFINITY) ? exp2f(m - M) / Ls : 0.f;
             }
             if (s0 == 0) {
                 const int v = r / p.G, g = r % p.G;
@@ -122,13 +140,20 @@ SD_DEVINL void merge_if_last(const AttendParams& p, int b, int kvh, int RP, floa
             }
         }
         __syncthreads();
-        for (int e = tid; e < p.R * D; e += nthr) {
+        for (int e = tid; e < R * D; e += nthr) {
             const int r = e / D, col = e % D;
             const int v = r / p.G, g = r % p.G;
             const size_t qrow = ((size_t)b * p.V + v) * p.Hq + kvh * p.G + g;
             float o = s0 == 0 ? 0.f : p.out[qrow * D + col];
-            for (int s = s0; s < s1; ++s)
-                o = fmaf(scratch[(s - s0) * RP + r], __ldcg(p.ws_o + (((size_t)bk * S + s) * RP + r) * D + col), o);
+            for (int s = s0; s < s1; s += 8) {  // up to eight independent loads in flight
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    x[u] = s + u < s1 ? __ldcg(p.ws_o + (((size_t)bk * S + s + u) * RP + r) * D + col) : 0.f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (s + u < s1) o = fmaf(ww[(s + u - s0) * R + r], x[u], o);
+            }
             p.out[qrow * D + col] = o;
         }
     }
@@ -403,30 +428,33 @@ struct MmaLayout {
     static constexpr int oQ = 0;
     static constexpr int oStage = ((RP * kRowB + 127) / 128) * 128;
     static constexpr int oSrc = oStage + 4 * kWStages * kStage;
-    static constexpr int oBar = oSrc + kMaxSplitRows * 4;
-    static constexpr int oML = oBar + 4 * kWStages * 8;  // [4 warps][RP] m, then l
-    static constexpr int oFlag = oML + 2 * 4 * RP * 4;
+    static constexpr int oML = oSrc + kMaxSplitRows * 4;  // [4 warps][RP] m, then l
+    static constexpr int oRow = oML + 2 * 4 * RP * 4;      // [RP] row max, sum; [4][RP] factors
+    static constexpr int oFlag = oRow + 6 * RP * 4;
     static constexpr int kBytes = oFlag + 16;
     static_assert(4 * RP * D * 4 <= 4 * kWStages * kStage, "warp outputs must fit in the stages");
 };
 
 // Grid (split, kvh, b), 4 warps.  The split's rows are cut into 16-key sub-chunks dealt
-// round-robin to the warps; each warp runs its own 2-deep pipeline (1-D bulk copies for
-// rows in HBM, 16-byte cp.async for rows in host memory, zero rows for skipped ones) and
-// its own online softmax, with QK^T and PV on the tensor cores: S[16q x 8k] tiles from Q
-// (ldmatrix) and K (ldmatrix), P split into bf16 hi + lo parts so the PV product keeps
-// ~16 significant bits, V fragments through ldmatrix.trans.  At the end the 4 warps'
-// (m, l, O) are combined through shared memory into the CTA's split partial.
+// round-robin to the warps; each warp runs its own 2-deep cp.async pipeline (16-byte
+// pieces, one warp instruction moves two 256-byte rows, from the HBM pool or from host
+// memory; zero rows for skipped entries) and its own online softmax, with QK^T and PV on
+// the tensor cores: S[16q x 8k] tiles from Q and K (ldmatrix), P split into bf16 hi + lo
+// parts so the PV product keeps ~16 significant bits, V fragments through ldmatrix.trans.
+// At the end the 4 warps' (m, l, O) are combined through shared memory into the CTA's
+// split partial, and the last CTA of each (b, kvh) merges the splits.
 template <int D, int RP>
 __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendParams p) {
     using L = MmaLayout<D, RP>;
-    constexpr int MT = RP / 16;   // 16-row M tiles of query rows
-    constexpr int KS = D / 16;    // k-steps of QK
-    constexpr int NT = D / 8;     // 8-column n-tiles of PV
+    constexpr int MT = RP / 16;      // 16-row M tiles of query rows
+    constexpr int KS = D / 16;       // k-steps of QK
+    constexpr int NT = D / 8;        // 8-column n-tiles of PV
     constexpr int PPR = D * 2 / 16;  // 16-byte pieces per row
+    static_assert(PPR == 16 || PPR == 8, "two rows per warp instruction need 16 or 8 pieces");
     extern __shared__ __align__(128) uint8_t sm[];
     int32_t* src = reinterpret_cast<int32_t*>(sm + L::oSrc);
     float* mlw = reinterpret_cast<float*>(sm + L::oML);
+    float* rowv = reinterpret_cast<float*>(sm + L::oRow);
     int* flag_s = reinterpret_cast<int*>(sm + L::oFlag);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -434,49 +462,59 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int bk = b * p.Hkv + kvh;
     uint8_t* stages = sm + L::oStage + warp * kWStages * L::kStage;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::oBar) + warp * kWStages;
 
     pdl_wait();
 
-    // ---- query rows r = v*G + g' (head kvh*G + g'), bf16, zero beyond R
+    // ---- prologue: query rows (cp.async, zero beyond R) and the rows' sources, together
     for (int e = tid; e < RP * PPR; e += kAttThreads) {
         const int r = e / PPR, part = e % PPR;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        uint8_t* dst = sm + L::oQ + r * L::kRowB + part * 16;
         if (r < p.R) {
             const int v = r / p.G, gg = r % p.G;
             const uint8_t* qrow = static_cast<const uint8_t*>(p.q) +
                                   ((((size_t)b * p.V + v) * p.Hq + kvh * p.G + gg) * D) * 2;
-            val = *reinterpret_cast<const uint4*>(qrow + part * 16);
+            cp_async16(dst, qrow + part * 16);
+        } else {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
         }
-        *reinterpret_cast<uint4*>(sm + L::oQ + r * L::kRowB + part * 16) = val;
     }
-
+    cp_async_commit();
     const int j0 = split * p.rows_per_split;
     const int j1 = min(p.n_rows, j0 + p.rows_per_split);
     const int nrows = max(0, j1 - j0);
-    auto resolve_row = [&](int jg) -> int32_t {
-        long pos = jg;
-        if (p.idx != nullptr) {
-            const long sel = p.idx[(size_t)bk * p.n_idx + jg / p.block];
-            pos = sel * p.block + jg % p.block;
-            if (sel < 0 || pos >= p.T) {
-                report(p.err, SD_DEVERR_INDEX);
-                return kNoRow;
+    if (p.resolve) {
+        for (int j = tid; j < nrows; j += kAttThreads) {
+            const int jg = j0 + j;
+            long pos = jg;
+            int32_t code;
+            bool ok = true;
+            if (p.idx != nullptr) {
+                const long sel = p.idx[(size_t)bk * p.n_idx + jg / p.block];
+                pos = sel * p.block + jg % p.block;
+                if (sel < 0 || pos >= p.T) {
+                    report(p.err, SD_DEVERR_INDEX);
+                    ok = false;
+                }
             }
+            if (!ok) {
+                code = kNoRow;
+            } else if (p.slot_map == nullptr) {
+                code = (int32_t)pos;
+            } else {
+                const int slot = p.slot_map[(size_t)b * p.T + pos];
+                if (slot >= 0 && slot < p.pool_rows) {
+                    code = slot;
+                } else if (slot == -1) {
+                    code = (int32_t)(-1 - pos);
+                } else {
+                    report(p.err, SD_DEVERR_SLOT);
+                    code = kNoRow;
+                }
+            }
+            src[j] = code;
         }
-        if (p.slot_map == nullptr) return (int32_t)pos;
-        const int slot = p.slot_map[(size_t)b * p.T + pos];
-        if (slot >= 0 && slot < p.pool_rows) return slot;
-        if (slot == -1) return (int32_t)(-1 - pos);
-        report(p.err, SD_DEVERR_SLOT);
-        return kNoRow;
-    };
-    if (p.resolve)
-        for (int j = tid; j < nrows; j += kAttThreads) src[j] = resolve_row(j0 + j);
-    if (lane == 0) {
-        for (int s = 0; s < kWStages; ++s) mbar_init(&bars[s], 1);
-        fence_mbarrier_init();
     }
+    cp_async_wait<0>();
     __syncthreads();
     auto row_code = [&](int j) -> int32_t {
         if (j >= nrows) return kNoRow;
@@ -486,34 +524,27 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     const int nsub = (nrows + kSub - 1) / kSub;
     const int my_n = warp < nsub ? (nsub - warp + 3) / 4 : 0;
 
-    // ---- fill stage `st` with sub-chunk ci of this warp
+    // ---- fill stage `st` with sub-chunk ci of this warp: instruction i moves K (i < 8) or
+    // V rows 2*(i % 8) and 2*(i % 8) + 1 (D = 128; D = 64 moves 4 rows per instruction)
+    constexpr int RPI = 32 / PPR;  // rows per warp instruction
     auto issue = [&](int ci, int st) {
         const int c = warp + 4 * ci;
         uint8_t* kst = stages + st * L::kStage;
-        uint8_t* vst = kst + kSub * L::kRowB;
-        const int32_t code = lane < kSub ? row_code(c * kSub + lane) : kNoRow;
-        const bool dev = lane < kSub && code != kNoRow && code >= 0;
-        const uint32_t devm = __ballot_sync(0xffffffffu, dev);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[st], (uint32_t)__popc(devm) * (uint32_t)(2 * D * 2));
-        __syncwarp();
-        if (dev) {
-            const size_t row = (size_t)bk * p.pool_rows + code;
-            bulk_g2s(kst + lane * L::kRowB, p.kc + row * (D * 2), D * 2, &bars[st]);
-            bulk_g2s(vst + lane * L::kRowB, p.vc + row * (D * 2), D * 2, &bars[st]);
-        }
-        // host rows (cp.async) and skipped rows (zeros): all lanes share the pieces
-        for (int kk = 0; kk < kSub; ++kk) {
-            const int32_t ck = __shfl_sync(0xffffffffu, code, kk);
-            if (ck >= 0) continue;
-            for (int pc = lane; pc < 2 * PPR; pc += 32) {
-                const int which = pc / PPR, part = pc % PPR;
-                uint8_t* dst = (which ? vst : kst) + kk * L::kRowB + part * 16;
-                if (ck == kNoRow) {
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-                } else {
-                    const size_t row = (size_t)bk * p.T + (size_t)(-1 - (long)ck);
-                    cp_async16(dst, (which ? p.vh : p.kh) + row * (D * 2) + part * 16);
-                }
+        const int32_t mycode = lane < kSub ? row_code(c * kSub + lane) : kNoRow;
+        const int part = lane % PPR, sub = lane / PPR;
+#pragma unroll
+        for (int i = 0; i < 2 * kSub / RPI; ++i) {
+            const int which = i / (kSub / RPI);
+            const int row = (i % (kSub / RPI)) * RPI + sub;
+            const int32_t code = __shfl_sync(0xffffffffu, mycode, row);
+            uint8_t* dst = kst + which * kSub * L::kRowB + row * L::kRowB + part * 16;
+            if (code == kNoRow) {
+                *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+            } else if (code >= 0) {
+                cp_async16(dst, (which ? p.vc : p.kc) + ((size_t)bk * p.pool_rows + code) * (D * 2) + part * 16);
+            } else {
+                cp_async16(dst, (which ? p.vh : p.kh) + ((size_t)bk * p.T + (size_t)(-1 - (long)code)) * (D * 2) +
+                                    part * 16);
             }
         }
         cp_async_commit();
@@ -534,14 +565,8 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     const uint32_t q_base = smem_addr(sm + L::oQ);
     int issued = 0;
     for (; issued < min(kWStages, my_n); ++issued) issue(issued, issued);
-    bool timed_out = false;
     for (int ci = 0; ci < my_n; ++ci) {
         const int st = ci % kWStages;
-        const bool ok = mbar_wait(&bars[st], (uint32_t)((ci / kWStages) & 1));
-        if (__any_sync(0xffffffffu, !ok)) {
-            timed_out = true;
-            break;
-        }
         if (ci + 1 < issued)
             cp_async_wait<1>();
         else
@@ -654,16 +679,9 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
         }
         __syncwarp();
         if (ci + kWStages < my_n) {
-            fence_proxy_async_shared();
             issue(ci + kWStages, st);
             ++issued;
         }
-    }
-    if (timed_out) {
-        if (lane == 0) report(p.err, SD_DEVERR_TIMEOUT);
-        cp_async_wait<0>();
-        // let this warp's bulk copies in flight land (bounded) before the stages are reused
-        for (int j = 0; j < issued; ++j) mbar_wait(&bars[j % kWStages], (uint32_t)((j / kWStages) & 1));
     }
 
     // ---- combine the 4 warps: m, l per row, then O rows scaled to the CTA maximum
@@ -678,17 +696,34 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
             }
     }
     __syncthreads();  // every warp is done with its stages: they hold the warps' O now
+    // per row: the CTA maximum, the sum of the warps' l rescaled to it, each warp's factor
+    float* rowM = rowv;            // [RP]
+    float* rowL = rowv + RP;       // [RP]
+    float* fac = rowv + 2 * RP;    // [4][RP]
+    if (tid < RP) {
+        const int r = tid;
+        float M = mlw[r];
+#pragma unroll
+        for (int w = 1; w < 4; ++w) M = fmaxf(M, mlw[w * RP + r]);
+        float Ls = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float mw = mlw[w * RP + r];
+            const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+            fac[w * RP + r] = f;
+            Ls = fmaf(mlw[4 * RP + w * RP + r], f, Ls);
+        }
+        rowM[r] = M;
+        rowL[r] = Ls;
+    }
+    __syncthreads();
     float* ow = reinterpret_cast<float*>(sm + L::oStage);  // [4][RP][D]
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             const int r = mt * 16 + g + 8 * hf;
-            const float mw = mlw[warp * RP + r];
-            float M = mlw[r];
-#pragma unroll
-            for (int w = 1; w < 4; ++w) M = fmaxf(M, mlw[w * RP + r]);
-            const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+            const float f = fac[warp * RP + r];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 float2 o2 = make_float2(oacc[mt][nt][2 * hf] * f, oacc[mt][nt][2 * hf + 1] * f);
@@ -698,27 +733,19 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     __syncthreads();
     for (int e = tid; e < p.R * D; e += kAttThreads) {
         const int r = e / D, col = e % D;
-        float M = mlw[r];
-#pragma unroll
-        for (int w = 1; w < 4; ++w) M = fmaxf(M, mlw[w * RP + r]);
-        float Ls = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float mw = mlw[w * RP + r];
-            if (mw != -INFINITY) Ls = fmaf(mlw[4 * RP + w * RP + r], exp2f(mw - M), Ls);
-        }
+        const float Ls = rowL[r];
         const float o = ow[(0 * RP + r) * D + col] + ow[(1 * RP + r) * D + col] + ow[(2 * RP + r) * D + col] +
                         ow[(3 * RP + r) * D + col];
         if (p.splits == 1) {
             const int v = r / p.G, gg = r % p.G;
             const size_t qrow = ((size_t)b * p.V + v) * p.Hq + kvh * p.G + gg;
             p.out[qrow * D + col] = Ls > 0.f ? o / Ls : 0.f;
-            if (col == 0) p.lse[qrow] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+            if (col == 0) p.lse[qrow] = Ls > 0.f ? (rowM[r] + log2f(Ls)) * kLn2 : -INFINITY;
         } else {
             const size_t prow = ((size_t)bk * p.splits + split) * RP + r;
             p.ws_o[prow * D + col] = o;
             if (col == 0) {
-                p.ws_m[prow] = M;
+                p.ws_m[prow] = rowM[r];
                 p.ws_l[prow] = Ls;
             }
         }

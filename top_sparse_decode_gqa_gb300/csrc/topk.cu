@@ -157,9 +157,9 @@ SD_DEVINL void emit_selected(TopkShared& sh, KeyAt key_at, int N, int k, uint32_
     }
 }
 
-// Loads the order keys of row `srow` into keys_s.  A 16-byte aligned row goes in with one
-// bulk copy (TMA) completed on `bar`, converted in place afterwards; otherwise each thread
-// loads 8 scores before converting any, so every thread keeps 8 loads in flight.
+// Loads the scores of row `srow` (raw fp32 bits; order keys are made on use) into keys_s.
+// A 16-byte aligned row goes in with one bulk copy (TMA) completed on `bar`; otherwise each
+// thread loads 8 scores before storing any, so every thread keeps 8 loads in flight.
 // Returns false (uniformly) if the bulk copy did not complete in time.
 SD_DEVINL bool stage_keys(const float* srow, int N, uint32_t* keys_s, uint64_t* bar) {
     const int tid = threadIdx.x;
@@ -174,7 +174,6 @@ SD_DEVINL bool stage_keys(const float* srow, int N, uint32_t* keys_s, uint64_t* 
         __syncthreads();
         const bool ok = mbar_wait(bar, 0);
         if (__syncthreads_or(!ok)) return false;
-        for (int i = tid; i < N; i += kTkThreads) keys_s[i] = float_key(__uint_as_float(keys_s[i]));
     } else {
         for (int base = tid; base < N; base += 8 * kTkThreads) {
             float v[8];
@@ -186,7 +185,7 @@ SD_DEVINL bool stage_keys(const float* srow, int N, uint32_t* keys_s, uint64_t* 
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int i = base + u * kTkThreads;
-                if (i < N) keys_s[i] = float_key(v[u]);
+                if (i < N) keys_s[i] = __float_as_uint(v[u]);
             }
         }
     }
@@ -218,7 +217,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         if (tid == 0) report(err_word, SD_DEVERR_TIMEOUT);
         return;
     }
-    auto key_at = [&](int i) -> uint32_t { return cache_keys ? keys_s[i] : float_key(srow[i]); };
+    auto key_at = [&](int i) -> uint32_t { return float_key(cache_keys ? __uint_as_float(keys_s[i]) : srow[i]); };
     uint32_t prefix = 0, pmask = 0;
     int krem = k;
 #pragma unroll 1
@@ -292,7 +291,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         if (tid == 0) report(err_word, SD_DEVERR_TIMEOUT);
         return;
     }
-    auto key_at = [&](int i) -> uint32_t { return cache_keys ? keys_s[i] : float_key(srow[i]); };
+    auto key_at = [&](int i) -> uint32_t { return float_key(cache_keys ? __uint_as_float(keys_s[i]) : srow[i]); };
     uint32_t d0, above;
     select_digit(sh, 2048u, k, d0, above);
     d0 &= (kHistBins - 1);
@@ -316,7 +315,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     // ---- one pass: bitmap of entries above d0, candidates of digit d0
     {
         const uint32_t lt = lanemask_lt();
-        constexpr int U = 4;  // 32-entry groups a warp loads before using any
+        constexpr int U = 8;  // 32-entry groups a warp loads before using any
         for (int g0 = warp; g0 < NW; g0 += U * kTkWarps) {
             uint32_t kk[U];
 #pragma unroll
@@ -452,18 +451,17 @@ extern "C" sd_status sd_topk(const float* scores, int rows, int N, int k, int32_
     if (key_hist != nullptr) {
         const int cache = key_bytes + aux_bytes + static_bytes <= limit ? 1 : 0;
         const size_t dyn = (cache ? key_bytes : 0) + aux_bytes;
-        if (dyn > 48 * 1024)
-            SD_CUDA_CHECK(cudaFuncSetAttribute(topk_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn),
-                          "sd_topk: cudaFuncSetAttribute");
+        // static + dynamic may exceed the 48 KB default even when dyn alone does not
+        SD_CUDA_CHECK(cudaFuncSetAttribute(topk_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn),
+                      "sd_topk: cudaFuncSetAttribute");
         SD_CUDA_CHECK(launch_pdl(topk_hist_kernel, rows, kTkThreads, dyn, st, scores, N, k, idx, key_hist, cache,
                                  (int32_t*)nullptr),
                       "sd_topk: launch");
     } else {
         const int cache = key_bytes + static_bytes <= limit ? 1 : 0;
         const size_t dyn = cache ? key_bytes : 0;
-        if (dyn > 48 * 1024)
-            SD_CUDA_CHECK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn),
-                          "sd_topk: cudaFuncSetAttribute");
+        SD_CUDA_CHECK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn),
+                      "sd_topk: cudaFuncSetAttribute");
         SD_CUDA_CHECK(launch_pdl(topk_kernel, rows, kTkThreads, dyn, st, scores, N, k, idx, cache, (int32_t*)nullptr),
                       "sd_topk: launch");
     }
