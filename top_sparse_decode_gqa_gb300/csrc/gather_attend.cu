@@ -140,21 +140,46 @@ SD_DEVINL void merge_if_last(const AttendParams& p, int b, int kvh, int RP, floa
             }
         }
         __syncthreads();
-        for (int e = tid; e < R * D; e += nthr) {
-            const int r = e / D, col = e % D;
-            const int v = r / p.G, g = r % p.G;
-            const size_t qrow = ((size_t)b * p.V + v) * p.Hq + kvh * p.G + g;
-            float o = s0 == 0 ? 0.f : p.out[qrow * D + col];
-            for (int s = s0; s < s1; s += 8) {  // up to eight independent loads in flight
-                float x[8];
+        const int items = R * (D / 4);  // (row, 4 columns)
+        for (int e0 = tid; e0 < items; e0 += 2 * nthr) {
+            float4 o[2];
+            int rr[2], cc[2];
+            size_t qrow[2];
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    x[u] = s + u < s1 ? __ldcg(p.ws_o + (((size_t)bk * S + s + u) * RP + r) * D + col) : 0.f;
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (s + u < s1) o = fmaf(ww[(s + u - s0) * R + r], x[u], o);
+            for (int t = 0; t < 2; ++t) {
+                const int e = e0 + t * nthr;
+                rr[t] = e < items ? e / (D / 4) : 0;
+                cc[t] = e < items ? (e % (D / 4)) * 4 : 0;
+                const int v = rr[t] / p.G, g = rr[t] % p.G;
+                qrow[t] = ((size_t)b * p.V + v) * p.Hq + kvh * p.G + g;
+                o[t] = (s0 == 0 || e >= items) ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                               : *reinterpret_cast<const float4*>(p.out + qrow[t] * D + cc[t]);
             }
-            p.out[qrow * D + col] = o;
+            for (int s = s0; s < s1; s += 8) {  // 2 items x 8 splits of loads in flight
+                float4 x[2][8];
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        x[t][u] = (s + u < s1 && e0 + t * nthr < items)
+                                      ? __ldcg(reinterpret_cast<const float4*>(
+                                            p.ws_o + (((size_t)bk * S + s + u) * RP + rr[t]) * D + cc[t]))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (s + u < s1) {
+                            const float wgt = ww[(s + u - s0) * R + rr[t]];
+                            o[t].x = fmaf(wgt, x[t][u].x, o[t].x);
+                            o[t].y = fmaf(wgt, x[t][u].y, o[t].y);
+                            o[t].z = fmaf(wgt, x[t][u].z, o[t].z);
+                            o[t].w = fmaf(wgt, x[t][u].w, o[t].w);
+                        }
+            }
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+                if (e0 + t * nthr < items) *reinterpret_cast<float4*>(p.out + qrow[t] * D + cc[t]) = o[t];
         }
     }
     if (tid == 0) p.counters[bk] = 0u;  // ready for the next call
@@ -450,7 +475,6 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     constexpr int KS = D / 16;       // k-steps of QK
     constexpr int NT = D / 8;        // 8-column n-tiles of PV
     constexpr int PPR = D * 2 / 16;  // 16-byte pieces per row
-    static_assert(PPR == 16 || PPR == 8, "two rows per warp instruction need 16 or 8 pieces");
     extern __shared__ __align__(128) uint8_t sm[];
     int32_t* src = reinterpret_cast<int32_t*>(sm + L::oSrc);
     float* mlw = reinterpret_cast<float*>(sm + L::oML);
@@ -524,27 +548,27 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     const int nsub = (nrows + kSub - 1) / kSub;
     const int my_n = warp < nsub ? (nsub - warp + 3) / 4 : 0;
 
-    // ---- fill stage `st` with sub-chunk ci of this warp: instruction i moves K (i < 8) or
-    // V rows 2*(i % 8) and 2*(i % 8) + 1 (D = 128; D = 64 moves 4 rows per instruction)
-    constexpr int RPI = 32 / PPR;  // rows per warp instruction
+    // ---- fill stage `st` with sub-chunk ci of this warp: lanes 2j and 2j+1 move row j of K
+    // and of V, alternating 16-byte pieces, so each lane pair reads whole 32-byte sectors;
+    // the row's source is resolved once per lane
     auto issue = [&](int ci, int st) {
         const int c = warp + 4 * ci;
         uint8_t* kst = stages + st * L::kStage;
-        const int32_t mycode = lane < kSub ? row_code(c * kSub + lane) : kNoRow;
-        const int part = lane % PPR, sub = lane / PPR;
+        const int row = lane >> 1, half = lane & 1;
+        const int32_t code = row_code(c * kSub + row);
 #pragma unroll
-        for (int i = 0; i < 2 * kSub / RPI; ++i) {
-            const int which = i / (kSub / RPI);
-            const int row = (i % (kSub / RPI)) * RPI + sub;
-            const int32_t code = __shfl_sync(0xffffffffu, mycode, row);
-            uint8_t* dst = kst + which * kSub * L::kRowB + row * L::kRowB + part * 16;
+        for (int which = 0; which < 2; ++which) {
+            uint8_t* dst = kst + which * kSub * L::kRowB + row * L::kRowB + half * 16;
             if (code == kNoRow) {
-                *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-            } else if (code >= 0) {
-                cp_async16(dst, (which ? p.vc : p.kc) + ((size_t)bk * p.pool_rows + code) * (D * 2) + part * 16);
+#pragma unroll
+                for (int i = 0; i < PPR / 2; ++i) *reinterpret_cast<uint4*>(dst + i * 32) = make_uint4(0u, 0u, 0u, 0u);
             } else {
-                cp_async16(dst, (which ? p.vh : p.kh) + ((size_t)bk * p.T + (size_t)(-1 - (long)code)) * (D * 2) +
-                                    part * 16);
+                const uint8_t* srow = code >= 0
+                    ? (which ? p.vc : p.kc) + ((size_t)bk * p.pool_rows + code) * (D * 2)
+                    : (which ? p.vh : p.kh) + ((size_t)bk * p.T + (size_t)(-1 - (long)code)) * (D * 2);
+                srow += half * 16;
+#pragma unroll
+                for (int i = 0; i < PPR / 2; ++i) cp_async16(dst + i * 32, srow + i * 32);
             }
         }
         cp_async_commit();
@@ -625,13 +649,13 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
                 tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
                 const float mo = m_r[mt][hf];
                 const float mn = fmaxf(mo, tmax);
-                const float alpha = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
+                const float alpha = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
                 float rs = 0.f;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const float pv = (x[nt][e] == -INFINITY) ? 0.f : exp2f(x[nt][e] - mn);
+                        const float pv = (x[nt][e] == -INFINITY) ? 0.f : fast_exp2(x[nt][e] - mn);
                         sacc[mt][nt][2 * hf + e] = pv;
                         rs += pv;
                     }
@@ -639,10 +663,12 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
                 rs += __shfl_xor_sync(0xffffffffu, rs, 2);
                 l_r[mt][hf] = l_r[mt][hf] * alpha + rs;
                 m_r[mt][hf] = mn;
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {  // only when a row's maximum moved
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    oacc[mt][nt][2 * hf] *= alpha;
-                    oacc[mt][nt][2 * hf + 1] *= alpha;
+                    for (int nt = 0; nt < NT; ++nt) {
+                        oacc[mt][nt][2 * hf] *= alpha;
+                        oacc[mt][nt][2 * hf + 1] *= alpha;
+                    }
                 }
                 const int r = mt * 16 + g + 8 * hf;
                 if (p.logits != nullptr && r < p.R) {
@@ -731,19 +757,27 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
             }
         }
     __syncthreads();
-    for (int e = tid; e < p.R * D; e += kAttThreads) {
-        const int r = e / D, col = e % D;
+    for (int e = tid; e < p.R * (D / 4); e += kAttThreads) {
+        const int r = e / (D / 4), col = (e % (D / 4)) * 4;
         const float Ls = rowL[r];
-        const float o = ow[(0 * RP + r) * D + col] + ow[(1 * RP + r) * D + col] + ow[(2 * RP + r) * D + col] +
-                        ow[(3 * RP + r) * D + col];
+        float4 o = *reinterpret_cast<const float4*>(ow + (0 * RP + r) * D + col);
+#pragma unroll
+        for (int w = 1; w < 4; ++w) {
+            const float4 x = *reinterpret_cast<const float4*>(ow + (w * RP + r) * D + col);
+            o.x += x.x;
+            o.y += x.y;
+            o.z += x.z;
+            o.w += x.w;
+        }
         if (p.splits == 1) {
             const int v = r / p.G, gg = r % p.G;
             const size_t qrow = ((size_t)b * p.V + v) * p.Hq + kvh * p.G + gg;
-            p.out[qrow * D + col] = Ls > 0.f ? o / Ls : 0.f;
+            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+            *reinterpret_cast<float4*>(p.out + qrow * D + col) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
             if (col == 0) p.lse[qrow] = Ls > 0.f ? (rowM[r] + log2f(Ls)) * kLn2 : -INFINITY;
         } else {
             const size_t prow = ((size_t)bk * p.splits + split) * RP + r;
-            p.ws_o[prow * D + col] = o;
+            *reinterpret_cast<float4*>(p.ws_o + prow * D + col) = o;
             if (col == 0) {
                 p.ws_m[prow] = rowM[r];
                 p.ws_l[prow] = Ls;
@@ -902,7 +936,7 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
     if (vs != SD_OK) return vs;
     if (a->B == 0) return SD_OK;
     SD_REQUIRE(a->q && a->out && a->lse, "sd_gather_attend: null q/out/lse");
-    SD_REQUIRE(aligned16(a->q), "sd_gather_attend: q must be 16-byte aligned");
+    SD_REQUIRE(aligned16(a->q) && aligned16(a->out), "sd_gather_attend: q and out must be 16-byte aligned");
     SplitPlan sp = plan_splits(a);
     AttendParams p{};
     p.q = a->q;

@@ -23,12 +23,17 @@ __global__ void score_accumulate_dense_kernel(const float* __restrict__ logits,
     const long n = (long)B * T;
     for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n; e += (long)gridDim.x * blockDim.x) {
         const int b = (int)(e / T), i = (int)(e % T);
+        const int rows = V * Hq;
+        const size_t q0 = (size_t)b * rows;
         float acc = 0.f;
-        for (int v = 0; v < V; ++v)
-            for (int h = 0; h < Hq; ++h) {
-                const size_t qrow = ((size_t)b * V + v) * Hq + h;
-                acc += expf(logits[qrow * T + i] - lse[qrow]);
-            }
+        for (int r0 = 0; r0 < rows; r0 += 8) {  // eight loads in flight before any use
+            float z[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) z[u] = r0 + u < rows ? logits[(q0 + r0 + u) * T + i] : 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (r0 + u < rows) acc += expf(z[u] - lse[q0 + r0 + u]);
+        }
         s[e] += weight * (double)acc;
     }
 }

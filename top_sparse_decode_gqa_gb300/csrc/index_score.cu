@@ -90,12 +90,14 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_score_kernel(
     }
     __syncwarp();
 
+    const uint64_t stream_policy = l2_evict_first_policy();  // keys are read once
     auto issue = [&](uint32_t j, int s) {  // lane 0: tile j of this warp into stage s
         const uint32_t t = gw + j * nw;
         const uint32_t ir = t / tpr, it0 = (t - ir * tpr) * TR;
         const uint32_t n = min((uint32_t)TR, (uint32_t)N - it0);
         mbar_arrive_expect_tx(&bars[s], n * ROWB);
-        bulk_g2s(ring + s * kWarpTileBytes, k_idx + ((size_t)ir * N + it0) * DI, n * ROWB, &bars[s]);
+        bulk_g2s_hint(ring + s * kWarpTileBytes, k_idx + ((size_t)ir * N + it0) * DI, n * ROWB, &bars[s],
+                      stream_policy);
     };
     if (lane == 0)
         for (uint32_t s = 0; s < min((uint32_t)kWarpStages, ntiles); ++s) issue(s, (int)s);

@@ -100,6 +100,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(
     uint32_t issued = 0;
     if (warp == 4) {
         if (lane == 0) {
+            // keys are read once: evict them first, so the scores written meanwhile stay in L2
+            const uint64_t stream_policy = l2_evict_first_policy();
             for (uint32_t i = 0; i < ntiles; ++i) {
                 const int s = (int)(i % kTcStages);
                 uint32_t r, t0;
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(
                 const int krow = (int)((uint64_t)r * N + t0);
 #pragma unroll
                 for (int a = 0; a < L::kAtoms; ++a) {
-                    tma_load_2d(st + a * kAtomA, &kmap, a * 64, krow, &full[s]);
+                    tma_load_2d_hint(st + a * kAtomA, &kmap, a * 64, krow, &full[s], stream_policy);
                     tma_load_2d(st + L::kStageA + a * kAtomB, &qmap, a * 64, (int)(r * V), &full[s]);
                 }
                 ++issued;

@@ -99,6 +99,33 @@ SD_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // scheduled now; it still waits (pdl_wait) for this grid to finish before reading.
 SD_DEVINL void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// ---------------------------------------------------------------- L2 policies
+
+// A cache policy that marks the lines a load brings into L2 as first to evict: for data
+// streamed once (so that it does not push out data that is read again soon).
+SD_DEVINL uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 1-D bulk copy with an L2 cache policy (see bulk_g2s).
+SD_DEVINL void bulk_g2s_hint(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar,
+                             uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22), flushing denormals.
+SD_DEVINL float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---------------------------------------------------------------- cp.async (16 B)
 
 SD_DEVINL void cp_async16(void* dst_smem, const void* src) {

@@ -91,6 +91,16 @@ SD_DEVINL void tma_load_2d(void* dst_smem, const CUtensorMap* map, int x, int y,
         : "memory");
 }
 
+// Same, with an L2 cache policy for the loaded lines.
+SD_DEVINL void tma_load_2d_hint(void* dst_smem, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
+            smem_addr(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 SD_DEVINL void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
