@@ -187,17 +187,20 @@ class StepMarks:
 
 
 class SparseDecodeStep:
-    """One sparse decode step (indexer -> top-k -> gather-attend), inputs resident.  For a
+    """One sparse decode step, inputs resident: the indexer, then either the fused select +
+    attend launch (bf16 workloads) or the separate top-k and gather-attend launches.  For a
     tiered workload the full K/V cache stays in pinned host memory and only the resident
     share sits in the HBM pool."""
 
     dominant = "sd_index_score"
-    phases = ("after_topk",)
 
-    def __init__(self, w, x, device):
+    def __init__(self, w, x, device, separate=False):
         import torch
         from top_sparse_decode_gqa_gb300 import binding as sd
         self.sd, self.w, self.dev = sd, w, device
+        self.fused = w.dtype == "bf16" and not separate
+        self.phases = () if self.fused else ("after_topk",)
+        self.launches_per_step = 2 if self.fused else 3
         self.tiered = w.resident_frac < 1.0
         self.q_idx, self.k_idx, self.q = (x[k].to(device) for k in ("q_idx", "k_idx", "q"))
         self.scores = torch.empty(w.B, w.Hkv, w.N, dtype=torch.float32, device=device)
@@ -213,15 +216,15 @@ class SparseDecodeStep:
             self.k_cache, self.v_cache = x["k"].to(device), x["v"].to(device)
             kw = {}
         self.args, self.out, self.lse, _ = sd.make_attend_args(
-            self.q, self.k_cache, self.v_cache, self.idx, block=w.block, T=w.T, err_word=self.err, **kw)
-        need = sd.sd_gather_attend_workspace_bytes(self.args)
+            self.q, self.k_cache, self.v_cache, None if self.fused else self.idx, n_idx=w.k,
+            block=w.block, T=w.T, err_word=self.err, **kw)
+        need = 0 if self.fused else sd.sd_gather_attend_workspace_bytes(self.args)
         self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=device)
         self.keys = self.k_idx
         if w.block > 1:
             self.keys = sd.sd_block_pool(self.k_idx, w.block)
         self.host_rows = None
 
-    launches_per_step = 3
     dominant_per_step = 1
 
     def run(self, m: "StepMarks" = None):
@@ -232,10 +235,13 @@ class SparseDecodeStep:
         sd.sd_index_score(self.q_idx, self.keys, self.scores, self.err, key_hist=self.key_hist)
         if m is not None:
             m.dom[0][1].record()
-        sd.sd_topk(self.scores, self.w.k, self.idx, key_hist=self.key_hist)
-        if m is not None:
-            m.phase["after_topk"].record()
-        sd.sd_gather_attend(self.args, self.ws)
+        if self.fused:
+            sd.sd_select_attend(self.scores, self.args, self.idx, key_hist=self.key_hist)
+        else:
+            sd.sd_topk(self.scores, self.w.k, self.idx, key_hist=self.key_hist)
+            if m is not None:
+                m.phase["after_topk"].record()
+            sd.sd_gather_attend(self.args, self.ws)
         if m is not None:
             m.end.record()
 
@@ -334,8 +340,8 @@ class DenseScoringStep:
                 "host": 0}
 
 
-def make_step(w, x, device):
-    return DenseScoringStep(w, x, device) if w.layers > 1 else SparseDecodeStep(w, x, device)
+def make_step(w, x, device, separate=False):
+    return DenseScoringStep(w, x, device) if w.layers > 1 else SparseDecodeStep(w, x, device, separate)
 
 
 def host_link_gbs(device, nbytes=512 << 20):
@@ -374,7 +380,7 @@ def run_ours(args):
         dist.barrier()
     w = WORKLOADS[args.workload]
     x = generate(w)
-    step = make_step(w, x, device)
+    step = make_step(w, x, device, args.separate)
     props = torch.cuda.get_device_properties(device)
     flush = torch.empty(2 * max(int(getattr(props, "L2_cache_size", 0)), 128 << 20), dtype=torch.uint8,
                         device=device)
@@ -437,7 +443,11 @@ def run_ours(args):
                           "bound": "hbm+host"})
     step_roof["t_roof_us"] = round(t_roof * 1e6, 2)
     step_roof["frac"] = round(t_roof / step_s, 4)
-    if isinstance(step, SparseDecodeStep):
+    if isinstance(step, SparseDecodeStep) and step.fused:
+        tail = [m.dom[0][1].elapsed_time(m.end) for m in marks]
+        step_roof["kernel_us"] = {"index_score": round(statistics.mean(dom_ms) * 1e3, 2),
+                                  "select_attend": round(statistics.mean(tail) * 1e3, 2)}
+    elif isinstance(step, SparseDecodeStep):
         after_topk = [m.dom[0][1].elapsed_time(m.phase["after_topk"]) for m in marks]
         tail = [m.phase["after_topk"].elapsed_time(m.end) for m in marks]
         step_roof["kernel_us"] = {"index_score": round(statistics.mean(dom_ms) * 1e3, 2),
@@ -462,6 +472,9 @@ def run_ours(args):
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "T": w.T,
                    "k": w.k, "block": w.block, "V": w.V, "layers": w.layers,
                    "queries_per_step": w.queries_per_step,
+                   "path": ("indexer + fused select/attend" if getattr(step, "fused", False)
+                            else "indexer + top-k + gather-attend" if isinstance(step, SparseDecodeStep)
+                            else "dense attention + score accumulate per layer"),
                    "l2": "flushed between timed steps: 2x L2 written then read, outside the events",
                    "parallelism": f"replica x{world} (each rank its own batch)"},
         "roofline": {"bound": "hbm", "kernel": step.dominant, "achieved": round(achieved, 1),
@@ -602,6 +615,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--separate", action="store_true",
+                    help="run top-k and gather-attend as two launches instead of the fused one")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -152,7 +152,7 @@ sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx, uin
  * at zero again, so a workspace can be reused without clearing.  Calls sharing one
  * workspace must not overlap on the GPU.  splits = 0 picks one wave of CTAs for this GPU;
  * a requested split count is adjusted to at least one 64-row chunk per split and at most
- * 512 rows per split when rows are selected through idx or slot_map.
+ * 448 rows per split when rows are selected through idx or slot_map.
  * The kernel is launched as a programmatic dependent of the preceding kernel in the
  * stream (it waits for that kernel's results before reading anything).
  */
@@ -198,6 +198,29 @@ sd_status sd_gather_attend(const sd_attend_args* args, void* stream);
  * launching (pass a smaller `splits`, or use sd_gather_attend with a workspace).
  */
 sd_status sd_gather_attend_noalloc(const sd_attend_args* args, void* stream);
+
+/*
+ * sd_select_attend -- sd_topk and sd_gather_attend fused in one launch.
+ * [Illusion] sec. 2 "Mecanismos de Esparsidade" (Oracle Top-K feeding a sparse decode
+ * kernel) and sec. 3C; [SparDA] sec. 2 item 1 (top-k blocks); [DHiSparse] "Metodologia"
+ * (the query rows of a group share each fetched row).
+ * Computes what sd_topk(scores, B*Hkv, N, n_idx, idx, key_hist) followed by
+ * sd_gather_attend(args with idx) computes: idx [B,Hkv,n_idx] int32 (written, ascending,
+ * bit-identical to sd_topk), out, lse and optional logits as sd_gather_attend defines
+ * them, with the selection list of every (b, kvh) taken from idx.  args->idx, workspace
+ * and workspace_bytes are ignored; k = args->n_idx.  scores [B*Hkv, N] fp32 with
+ * N * args->block == args->T (one score per token, or per block of `block` tokens).
+ * key_hist: nullable, as in sd_topk (the indexer's histogram of exactly these scores;
+ * zero-filled again by the call).  args->splits: CTAs per (b, kvh), 0 = automatic, at most
+ * 8; they form one thread-block cluster that exchanges the selection threshold and merges
+ * the attention partials through distributed shared memory, so no workspace is needed.
+ * The summation order of the attention depends on (N, n_idx, block, splits) and on which
+ * part of the row each selected entry falls in, never on where the rows are stored.
+ * Limits: bf16 q/K/V, d in {64, 128}, G*V <= 32 (other inputs: SD_ERR_UNSUPPORTED, use the
+ * two separate calls).  Launched as a programmatic dependent of the preceding kernel.
+ */
+sd_status sd_select_attend(const float* scores, int N, uint32_t* key_hist, int32_t* idx,
+                           const sd_attend_args* args, void* stream);
 
 /*
  * sd_score_accumulate -- one layer's term of the cumulative attention-importance score.

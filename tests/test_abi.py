@@ -73,3 +73,33 @@ def test_attend_validation_and_workspace_query(lib):
     assert lib.sd_gather_attend(ctypes.byref(a), None) == 2
     a.V, a.n_idx = 1, 100  # dense mode with n_idx*block != T
     assert lib.sd_gather_attend(ctypes.byref(a), None) == 1
+
+
+def test_select_attend_validation(lib):
+    from top_sparse_decode_gqa_gb300.binding import sd_attend_args
+    P = ctypes.c_void_p
+    dummy = P(16)
+    a = sd_attend_args()
+    a.q = a.k_cache = a.v_cache = a.out = a.lse = 16
+    a.dtype, a.B, a.V, a.Hq, a.Hkv, a.d, a.T = 1, 2, 1, 32, 8, 128, 4096
+    a.pool_rows, a.n_idx, a.block, a.scale = 4096, 64, 1, 0.1
+    # one score per token: N must equal T / block
+    assert lib.sd_select_attend(dummy, 4000, None, dummy, ctypes.byref(a), None) == 1
+    assert b"must equal T" in lib.sd_last_error_message()
+    # k beyond N
+    a.n_idx = 5000
+    assert lib.sd_select_attend(dummy, 4096, None, dummy, ctypes.byref(a), None) == 1
+    a.n_idx = 64
+    # the cluster holds at most 8 CTAs
+    a.splits = 9
+    assert lib.sd_select_attend(dummy, 4096, None, dummy, ctypes.byref(a), None) == 1
+    a.splits = 0
+    # fp32 inputs and G*V > 32 go through the separate calls
+    a.dtype = 0
+    assert lib.sd_select_attend(dummy, 4096, None, dummy, ctypes.byref(a), None) == 2
+    a.dtype, a.V = 1, 9
+    assert lib.sd_select_attend(dummy, 4096, None, dummy, ctypes.byref(a), None) == 2
+    # block selection: N blocks of `block` tokens
+    a.V, a.block, a.n_idx = 1, 64, 8
+    a.B = 0  # nothing to do: accepted without touching the pointers
+    assert lib.sd_select_attend(None, 64, None, None, ctypes.byref(a), None) == 0

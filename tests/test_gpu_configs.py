@@ -169,6 +169,74 @@ def test_c4_tiered_verify_full():
         torch.cuda.empty_cache()
 
 
+def test_c2_fused_select_attend_full():
+    # the benchmark's fused launch configuration: indexer with the key histogram, then one
+    # select + attend launch
+    w = W("c2_llama3_8b_gqa")
+    x = gen(w)
+    g = to_dev(x)
+    hist = sd().key_hist_buffer(w.B * w.Hkv)
+    scores = sd().sd_index_score(g["q_idx"], g["k_idx"], key_hist=hist)
+    idx, out, lse, _ = sd().select_attend(scores, w.k, g["q"], g["k"], g["v"], key_hist=hist, T=w.T)
+    rs = oracle.index_score(x["q_idx"], x["k_idx"], w.B, w.Hkv, w.V, w.T, w.dI)
+    ri = oracle.topk(rs, w.k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ri)
+    ro, rl, _ = oracle.gather_attend(x["q"], x["k"], x["v"], ri, w.B, w.V, w.Hq, w.Hkv, w.d, w.T,
+                                     w.k, 1, 1 / math.sqrt(w.d))
+    assert_attend_close(out, ro)
+    assert_attend_close(lse, rl, "lse")
+
+
+def test_c3_fused_select_attend_full():
+    w = W("c3_block_sparse")
+    x = gen(w)
+    g = to_dev(x)
+    pooled = sd().sd_block_pool(g["k_idx"], w.block)
+    hist = sd().key_hist_buffer(w.B * w.Hkv)
+    scores = sd().sd_index_score(g["q_idx"], pooled, key_hist=hist)
+    idx, out, lse, _ = sd().select_attend(scores, w.k, g["q"], g["k"], g["v"], key_hist=hist,
+                                          block=w.block, T=w.T)
+    rp = oracle.block_pool(x["k_idx"], w.B, w.Hkv, w.T, w.dI, w.block)
+    rs = oracle.index_score(x["q_idx"], rp.astype(np.float32), w.B, w.Hkv, w.V, w.N, w.dI)
+    ri = oracle.topk(rs, w.k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ri)
+    ro, rl, _ = oracle.gather_attend(x["q"], x["k"], x["v"], ri, w.B, w.V, w.Hq, w.Hkv, w.d, w.T,
+                                     w.k, w.block, 1 / math.sqrt(w.d))
+    assert_attend_close(out, ro)
+    assert_attend_close(lse, rl, "lse")
+
+
+def test_c4_fused_select_attend_full():
+    w = W("c4_tiered_verify")
+    x = gen(w)
+    dev = {k: x[k].cuda() for k in ("q_idx", "k_idx", "q", "slot_map", "k_pool", "v_pool")}
+    k_host, v_host = x["k"].pin_memory(), x["v"].pin_memory()
+    e = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hist = sd().key_hist_buffer(w.B * w.Hkv)
+    scores = sd().sd_index_score(dev["q_idx"], dev["k_idx"], key_hist=hist)
+    idx, out, lse, _ = sd().select_attend(scores, w.k, dev["q"], dev["k_pool"], dev["v_pool"], key_hist=hist,
+                                          T=w.T, k_host=k_host, v_host=v_host, slot_map=dev["slot_map"],
+                                          err_word=e)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    # the index sets are sd_topk's (pinned to the oracle by the separate-call test)
+    np.testing.assert_array_equal(idx.cpu().numpy(), sd().sd_topk(scores, w.k).cpu().numpy())
+    i_gpu = idx.cpu().numpy()
+    for b, h in ((0, 0), (w.B - 1, w.Hkv - 1)):
+        rs = oracle.index_score(x["q_idx"][b:b + 1, h:h + 1], x["k_idx"][b:b + 1, h:h + 1], 1, 1, w.V, w.T, w.dI)
+        ri = oracle.topk(rs, w.k)
+        np.testing.assert_array_equal(i_gpu[b:b + 1, h:h + 1], ri)
+        qh = x["q"][b:b + 1, :, h * w.G:(h + 1) * w.G].contiguous()
+        ro, rl, _ = oracle.gather_attend(qh, x["k"][b:b + 1, h:h + 1].contiguous(),
+                                         x["v"][b:b + 1, h:h + 1].contiguous(), ri, 1, w.V, w.G, 1,
+                                         w.d, w.T, w.k, 1, 1 / math.sqrt(w.d))
+        assert_attend_close(out[b:b + 1, :, h * w.G:(h + 1) * w.G], ro)
+        assert_attend_close(lse[b:b + 1, :, h * w.G:(h + 1) * w.G], rl, "lse")
+    # all rows in HBM: the same bits
+    idx2, out2, lse2, _ = sd().select_attend(scores, w.k, dev["q"], x["k"].cuda(), x["v"].cuda(), T=w.T)
+    assert torch.equal(idx2, idx) and torch.equal(out2, out) and torch.equal(lse2, lse)
+
+
 def test_c5_importance_tiering_full():
     """Dense decode over 28 layers for the full 64 steps, the score recurrence, then the
     four-tier split and the int8 encode of the T2 rows.  The oracle follows step 1 over all

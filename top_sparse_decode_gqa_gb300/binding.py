@@ -26,7 +26,7 @@ EXPORTS = (
     "sd_version", "sd_status_string", "sd_last_error_message", "sd_index_score", "sd_block_pool",
     "sd_topk_workspace_bytes", "sd_topk", "sd_gather_attend_workspace_bytes", "sd_gather_attend",
     "sd_score_accumulate", "sd_tier_classify_workspace_bytes", "sd_tier_classify",
-    "sd_quantize_rows_int8", "sd_gather_attend_noalloc",
+    "sd_quantize_rows_int8", "sd_gather_attend_noalloc", "sd_select_attend",
 )
 
 
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
         L.sd_gather_attend_workspace_bytes.restype = Z
         L.sd_gather_attend.argtypes = [ctypes.POINTER(sd_attend_args), P]
         L.sd_gather_attend_noalloc.argtypes = [ctypes.POINTER(sd_attend_args), P]
+        L.sd_select_attend.argtypes = [P, I, P, P, ctypes.POINTER(sd_attend_args), P]
         L.sd_score_accumulate.argtypes = [P, P, P, I, I, I, I, I, I, I, D, P, P, P]
         L.sd_tier_classify_workspace_bytes.argtypes = [I, I]
         L.sd_tier_classify_workspace_bytes.restype = Z
@@ -248,6 +249,29 @@ def sd_gather_attend_noalloc(args: sd_attend_args, stream=None) -> None:
     that cannot allocate); args.workspace is ignored."""
     _check(lib().sd_gather_attend_noalloc(ctypes.byref(args), _stream(stream)),
            "sd_gather_attend_noalloc")
+
+
+def sd_select_attend(scores: torch.Tensor, args: sd_attend_args, idx: torch.Tensor,
+                     key_hist: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Runs one sd_select_attend call: the top-args.n_idx selection of every row of scores
+    [B, Hkv, N] written to idx [B, Hkv, n_idx], and the attention `args` describes over it
+    (args.idx and the workspace are ignored)."""
+    _dev(scores, "scores")
+    _dev(idx, "idx")
+    if scores.dtype != torch.float32 or idx.dtype != torch.int32:
+        raise TypeError("scores must be float32 and idx int32")
+    _check(lib().sd_select_attend(_ptr(scores), scores.shape[-1], _ptr(key_hist), _ptr(idx),
+                                  ctypes.byref(args), _stream(stream)), "sd_select_attend")
+    return idx
+
+
+def select_attend(scores, k, q, k_cache, v_cache, key_hist=None, stream=None, **kw):
+    """Convenience wrapper: top-k selection fused with the attention over it; returns
+    (idx, out, lse, logits)."""
+    idx = torch.empty(scores.shape[:-1] + (k,), dtype=torch.int32, device=scores.device)
+    a, out, lse, logits = make_attend_args(q, k_cache, v_cache, None, n_idx=k, **kw)
+    sd_select_attend(scores, a, idx, key_hist, stream)
+    return idx, out, lse, logits
 
 
 def gather_attend(q, k_cache, v_cache, idx=None, workspace=None, stream=None, **kw):

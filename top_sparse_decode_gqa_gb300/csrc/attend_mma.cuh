@@ -1,0 +1,297 @@
+// attend_mma.cuh -- the per-warp exact-attention loop on the warp-level tensor cores
+// (mma.sync m16n8k16, bf16 in, fp32 accumulate), shared by sd_gather_attend and the
+// fused select + attend kernel.
+//
+// "Esparsidade de Contexto no Tempo de Inferencia" (gist.science summary), sec. 2: sparse
+// decode attention over an irregular per-token selection; Adaptive DHiSparse (news page),
+// "Metodologia": every query row of a group shares each fetched row.
+//
+// A CTA of 4 warps owns a list of `nrows` K/V rows.  The list is cut into 16-row
+// sub-chunks dealt round-robin to the warps; each warp runs its own 2-deep cp.async
+// pipeline (lanes 2j and 2j+1 move row j of K and of V in alternating 16-byte pieces) and
+// its own online softmax in base 2 over all RP query rows: S[16q x 8k] tiles from Q and K
+// through ldmatrix, P split into bf16 hi + lo parts so the PV product keeps ~16
+// significant bits, V fragments through ldmatrix.trans.  mma_combine_warps then merges
+// the 4 warps' (m, l, O) in shared memory.
+#pragma once
+
+#include <stdint.h>
+
+#include "sd_common.cuh"
+
+namespace sd {
+
+constexpr int kMmaWarps = 4;          // warps of a CTA that run the attention loop
+constexpr int kSub = 16;              // rows per warp sub-chunk
+constexpr int kWStages = 2;           // sub-chunks in flight per warp
+constexpr int32_t kNoRow = INT32_MIN;  // source code of a skipped row (contributes nothing)
+constexpr float kLn2f = 0.69314718055994530942f;
+
+template <int D>
+struct MmaRows {
+    static constexpr int kRowB = D * 2 + 16;         // padded bf16 row: conflict-free ldmatrix
+    static constexpr int kStage = 2 * kSub * kRowB;  // K rows then V rows
+    static constexpr int kWarpBytes = kWStages * kStage;
+    static constexpr int kStagesBytes = kMmaWarps * kWarpBytes;
+};
+
+// Where a row's bytes are: code >= 0 is row `code` of the device pool (k_pool + code * row
+// bytes, already offset to this (b, kvh)); code < 0 is host row -1 - code of the mapped
+// host cache (k_host likewise offset); kNoRow is skipped.
+struct RowSource {
+    const uint8_t* k_pool;
+    const uint8_t* v_pool;
+    const uint8_t* k_host;
+    const uint8_t* v_host;
+};
+
+template <int D, int RP>
+struct WarpAcc {
+    static constexpr int MT = RP / 16;  // 16-row M tiles of query rows
+    static constexpr int NT = D / 8;    // 8-column n-tiles of PV
+    float m[MT][2], l[MT][2];
+    float o[MT][NT][4];
+    SD_DEVINL void init() {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            m[mt][0] = m[mt][1] = -INFINITY;
+            l[mt][0] = l[mt][1] = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+        }
+    }
+};
+
+// One warp's share of the CTA's rows.  `stages` is this warp's kWarpBytes of shared
+// memory, `q_base` the shared address of the RP query rows (kRowB apart, pre-loaded, rows
+// beyond the real ones zero).  row_code(j) returns the source of list row j (kNoRow for a
+// skipped row; called only for j < nrows).  logit(r, j, x) receives every (query row,
+// list row) score in base-2 units (x * ln 2 is the natural logit) of valid rows.
+template <int D, int RP, class RowCode, class Logit>
+SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_base, int warp, int nrows,
+                               const RowSource& rs, float scale_log2, RowCode row_code, Logit logit) {
+    using L = MmaRows<D>;
+    constexpr int MT = RP / 16, KS = D / 16, NT = D / 8;
+    constexpr int PPR = D * 2 / 16;  // 16-byte pieces per row
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, t4 = lane & 3;
+    auto code_of = [&](int j) -> int32_t { return j < nrows ? row_code(j) : kNoRow; };
+    const int nsub = (nrows + kSub - 1) / kSub;
+    const int my_n = warp < nsub ? (nsub - warp + kMmaWarps - 1) / kMmaWarps : 0;
+
+    auto issue = [&](int ci, int st) {
+        const int c = warp + kMmaWarps * ci;
+        uint8_t* kst = stages + st * L::kStage;
+        const int row = lane >> 1, half = lane & 1;
+        const int32_t code = code_of(c * kSub + row);
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            uint8_t* dst = kst + which * kSub * L::kRowB + row * L::kRowB + half * 16;
+            if (code == kNoRow) {
+#pragma unroll
+                for (int i = 0; i < PPR / 2; ++i) *reinterpret_cast<uint4*>(dst + i * 32) = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                const uint8_t* srow = code >= 0 ? (which ? rs.v_pool : rs.k_pool) + (size_t)code * (D * 2)
+                                                : (which ? rs.v_host : rs.k_host) + (size_t)(-1 - (long)code) * (D * 2);
+                srow += half * 16;
+#pragma unroll
+                for (int i = 0; i < PPR / 2; ++i) cp_async16(dst + i * 32, srow + i * 32);
+            }
+        }
+        cp_async_commit();
+    };
+
+    int issued = 0;
+    for (; issued < min(kWStages, my_n); ++issued) issue(issued, issued);
+    for (int ci = 0; ci < my_n; ++ci) {
+        const int st = ci % kWStages;
+        if (ci + 1 < issued)
+            cp_async_wait<1>();
+        else
+            cp_async_wait<0>();
+        __syncwarp();
+        const uint32_t k_base = smem_addr(stages + st * L::kStage);
+        const uint32_t v_base = k_base + kSub * L::kRowB;
+        const int c = warp + kMmaWarps * ci;
+
+        // ---- S = Q K^T for this warp's 16 rows: [MT][2 n-tiles][4]
+        float sacc[MT][2][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ks += 2) {
+            uint32_t bk0[4], bk1[4];  // n-tile 0 / 1: (b0, b1) of k-step ks, then of ks + 1
+            ldsm_x4(k_base + (0 * 8 + (lane & 7)) * L::kRowB + (ks * 16 + (lane >> 3) * 8) * 2, bk0[0], bk0[1], bk0[2], bk0[3]);
+            ldsm_x4(k_base + (1 * 8 + (lane & 7)) * L::kRowB + (ks * 16 + (lane >> 3) * 8) * 2, bk1[0], bk1[1], bk1[2], bk1[3]);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(q_base + (mt * 16 + (lane & 15)) * L::kRowB + ((ks + kk) * 16 + (lane >> 4) * 8) * 2, a0, a1, a2, a3);
+                    mma_bf16_16816(sacc[mt][0], a0, a1, a2, a3, bk0[2 * kk], bk0[2 * kk + 1]);
+                    mma_bf16_16816(sacc[mt][1], a0, a1, a2, a3, bk1[2 * kk], bk1[2 * kk + 1]);
+                }
+            }
+        }
+
+        // ---- online softmax (base 2); this lane holds rows 8*nt + 2*t4 + e of query rows g, g + 8
+        bool kval[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) kval[nt][e] = code_of(c * kSub + nt * 8 + 2 * t4 + e) != kNoRow;
+        uint32_t ph[MT][4], pl[MT][4];  // P as A fragments (hi, lo)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float x[2][2];
+                float tmax = -INFINITY;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        x[nt][e] = kval[nt][e] ? sacc[mt][nt][2 * hf + e] * scale_log2 : -INFINITY;
+                        tmax = fmaxf(tmax, x[nt][e]);
+                    }
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+                const float mo = acc.m[mt][hf];
+                const float mn = fmaxf(mo, tmax);
+                const float alpha = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
+                float rsum = 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float pv = (x[nt][e] == -INFINITY) ? 0.f : fast_exp2(x[nt][e] - mn);
+                        sacc[mt][nt][2 * hf + e] = pv;
+                        rsum += pv;
+                    }
+                rsum += __shfl_xor_sync(0xffffffffu, rsum, 1);
+                rsum += __shfl_xor_sync(0xffffffffu, rsum, 2);
+                acc.l[mt][hf] = acc.l[mt][hf] * alpha + rsum;
+                acc.m[mt][hf] = mn;
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {  // only when a row's maximum moved
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        acc.o[mt][nt][2 * hf] *= alpha;
+                        acc.o[mt][nt][2 * hf + 1] *= alpha;
+                    }
+                }
+                const int r = mt * 16 + g + 8 * hf;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int j = c * kSub + nt * 8 + 2 * t4 + e;
+                        if (j < nrows) logit(r, j, x[nt][e]);
+                    }
+            }
+            // A fragments: a0 = (g, rows 2t..), a1 = (g+8, 2t..), a2 = (g, 2t+8..), a3 = (g+8, 2t+8..)
+            split_bf16x2(sacc[mt][0][0], sacc[mt][0][1], ph[mt][0], pl[mt][0]);
+            split_bf16x2(sacc[mt][0][2], sacc[mt][0][3], ph[mt][1], pl[mt][1]);
+            split_bf16x2(sacc[mt][1][0], sacc[mt][1][1], ph[mt][2], pl[mt][2]);
+            split_bf16x2(sacc[mt][1][2], sacc[mt][1][3], ph[mt][3], pl[mt][3]);
+        }
+
+        // ---- O += P V: V fragments by ldmatrix.trans, 2 n-tiles per load
+#pragma unroll
+        for (int nt = 0; nt < NT; nt += 2) {
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_t(v_base + (lane & 15) * L::kRowB + (nt * 8 + (lane >> 4) * 8) * 2, v0, v1, v2, v3);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                mma_bf16_16816(acc.o[mt][nt], ph[mt][0], ph[mt][1], ph[mt][2], ph[mt][3], v0, v1);
+                mma_bf16_16816(acc.o[mt][nt], pl[mt][0], pl[mt][1], pl[mt][2], pl[mt][3], v0, v1);
+                mma_bf16_16816(acc.o[mt][nt + 1], ph[mt][0], ph[mt][1], ph[mt][2], ph[mt][3], v2, v3);
+                mma_bf16_16816(acc.o[mt][nt + 1], pl[mt][0], pl[mt][1], pl[mt][2], pl[mt][3], v2, v3);
+            }
+        }
+        __syncwarp();
+        if (ci + kWStages < my_n) {
+            issue(ci + kWStages, st);
+            ++issued;
+        }
+    }
+}
+
+// Combines the 4 warps' (m, l, O) of a CTA; called by all 128 threads after every warp's
+// loop.  Scratch: mlw [2*4*RP] floats, rowv [6*RP] floats, ow [4][RP][D] floats (the
+// warps' stage area may be reused: the call starts with a barrier).  Leaves rowM = rowv[0,
+// RP) (the CTA's row maxima), rowL = rowv[RP, 2RP) (sums of l rescaled to them) and ow[w][r]
+// = warp w's O row r rescaled to rowM[r]; the CTA's unnormalised O row is the sum over w.
+template <int D, int RP>
+SD_DEVINL void mma_combine_warps(const WarpAcc<D, RP>& acc, float* mlw, float* rowv, float* ow) {
+    constexpr int MT = RP / 16, NT = D / 8;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t4 = lane & 3;
+    if (t4 == 0) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int r = mt * 16 + g + 8 * hf;
+                mlw[warp * RP + r] = acc.m[mt][hf];
+                mlw[kMmaWarps * RP + warp * RP + r] = acc.l[mt][hf];
+            }
+    }
+    __syncthreads();  // every warp is done with its stages: they may hold the warps' O now
+    float* rowM = rowv;
+    float* rowL = rowv + RP;
+    float* fac = rowv + 2 * RP;  // [4][RP]
+    if (tid < RP) {
+        const int r = tid;
+        float M = mlw[r];
+#pragma unroll
+        for (int w = 1; w < kMmaWarps; ++w) M = fmaxf(M, mlw[w * RP + r]);
+        float Ls = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMmaWarps; ++w) {
+            const float mw = mlw[w * RP + r];
+            const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+            fac[w * RP + r] = f;
+            Ls = fmaf(mlw[kMmaWarps * RP + w * RP + r], f, Ls);
+        }
+        rowM[r] = M;
+        rowL[r] = Ls;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int r = mt * 16 + g + 8 * hf;
+            const float f = fac[warp * RP + r];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float2 o2 = make_float2(acc.o[mt][nt][2 * hf] * f, acc.o[mt][nt][2 * hf + 1] * f);
+                *reinterpret_cast<float2*>(ow + ((size_t)warp * RP + r) * D + nt * 8 + 2 * t4) = o2;
+            }
+        }
+    __syncthreads();
+}
+
+// The CTA's unnormalised O columns [col, col + 4) of row r: the sum of the 4 warps' parts.
+template <int D, int RP>
+SD_DEVINL float4 mma_cta_row4(const float* ow, int r, int col) {
+    float4 o = *reinterpret_cast<const float4*>(ow + (size_t)r * D + col);
+#pragma unroll
+    for (int w = 1; w < kMmaWarps; ++w) {
+        const float4 x = *reinterpret_cast<const float4*>(ow + ((size_t)w * RP + r) * D + col);
+        o.x += x.x;
+        o.y += x.y;
+        o.z += x.z;
+        o.w += x.w;
+    }
+    return o;
+}
+
+}  // namespace sd

@@ -18,6 +18,7 @@
 // merge kernel combines them in split order (deterministic).
 #include <algorithm>
 
+#include "attend_mma.cuh"
 #include "sd_common.cuh"
 #include "sd_host.h"
 
@@ -29,7 +30,6 @@ constexpr int kCH = 64;             // rows per staged chunk
 constexpr int kMaxSplitRows = 448;  // rows whose sources a CTA resolves up front
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
-constexpr int32_t kNoRow = INT32_MIN;  // source code of a skipped (invalid) row
 
 struct AttendParams {
     const void* q;
@@ -443,37 +443,26 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
 
 // ------------------------------------------------------------------ bf16 path (warp MMA)
 
-constexpr int kSub = 16;     // keys per warp sub-chunk
-constexpr int kWStages = 2;  // sub-chunks in flight per warp
-
 template <int D, int RP>
 struct MmaLayout {
-    static constexpr int kRowB = D * 2 + 16;  // padded bf16 row: conflict-free ldmatrix
-    static constexpr int kStage = 2 * kSub * kRowB;  // K rows then V rows
+    using Rows = MmaRows<D>;
     static constexpr int oQ = 0;
-    static constexpr int oStage = ((RP * kRowB + 127) / 128) * 128;
-    static constexpr int oSrc = oStage + 4 * kWStages * kStage;
-    static constexpr int oML = oSrc + kMaxSplitRows * 4;  // [4 warps][RP] m, then l
-    static constexpr int oRow = oML + 2 * 4 * RP * 4;      // [RP] row max, sum; [4][RP] factors
+    static constexpr int oStage = ((RP * Rows::kRowB + 127) / 128) * 128;
+    static constexpr int oSrc = oStage + Rows::kStagesBytes;
+    static constexpr int oML = oSrc + kMaxSplitRows * 4;   // [4 warps][RP] m, then l
+    static constexpr int oRow = oML + 2 * kMmaWarps * RP * 4;  // [RP] row max, sum; [4][RP] factors
     static constexpr int oFlag = oRow + 6 * RP * 4;
     static constexpr int kBytes = oFlag + 16;
-    static_assert(4 * RP * D * 4 <= 4 * kWStages * kStage, "warp outputs must fit in the stages");
+    static_assert(kMmaWarps * RP * D * 4 <= Rows::kStagesBytes, "warp outputs must fit in the stages");
 };
 
-// Grid (split, kvh, b), 4 warps.  The split's rows are cut into 16-key sub-chunks dealt
-// round-robin to the warps; each warp runs its own 2-deep cp.async pipeline (16-byte
-// pieces, one warp instruction moves two 256-byte rows, from the HBM pool or from host
-// memory; zero rows for skipped entries) and its own online softmax, with QK^T and PV on
-// the tensor cores: S[16q x 8k] tiles from Q and K (ldmatrix), P split into bf16 hi + lo
-// parts so the PV product keeps ~16 significant bits, V fragments through ldmatrix.trans.
-// At the end the 4 warps' (m, l, O) are combined through shared memory into the CTA's
-// split partial, and the last CTA of each (b, kvh) merges the splits.
+// Grid (split, kvh, b), 4 warps.  The split's rows are resolved to their sources up front,
+// then attend_mma.cuh's per-warp loop runs over them; the 4 warps' (m, l, O) are combined
+// into the CTA's split partial, and the last CTA of each (b, kvh) merges the splits.
 template <int D, int RP>
 __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendParams p) {
     using L = MmaLayout<D, RP>;
-    constexpr int MT = RP / 16;      // 16-row M tiles of query rows
-    constexpr int KS = D / 16;       // k-steps of QK
-    constexpr int NT = D / 8;        // 8-column n-tiles of PV
+    using Rows = MmaRows<D>;
     constexpr int PPR = D * 2 / 16;  // 16-byte pieces per row
     extern __shared__ __align__(128) uint8_t sm[];
     int32_t* src = reinterpret_cast<int32_t*>(sm + L::oSrc);
@@ -481,18 +470,16 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     float* rowv = reinterpret_cast<float*>(sm + L::oRow);
     int* flag_s = reinterpret_cast<int*>(sm + L::oFlag);
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, t4 = lane & 3;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int bk = b * p.Hkv + kvh;
-    uint8_t* stages = sm + L::oStage + warp * kWStages * L::kStage;
 
     pdl_wait();
 
     // ---- prologue: query rows (cp.async, zero beyond R) and the rows' sources, together
     for (int e = tid; e < RP * PPR; e += kAttThreads) {
         const int r = e / PPR, part = e % PPR;
-        uint8_t* dst = sm + L::oQ + r * L::kRowB + part * 16;
+        uint8_t* dst = sm + L::oQ + r * Rows::kRowB + part * 16;
         if (r < p.R) {
             const int v = r / p.G, gg = r % p.G;
             const uint8_t* qrow = static_cast<const uint8_t*>(p.q) +
@@ -540,235 +527,34 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     }
     cp_async_wait<0>();
     __syncthreads();
-    auto row_code = [&](int j) -> int32_t {
-        if (j >= nrows) return kNoRow;
-        return p.resolve ? src[j] : (int32_t)(j0 + j);
+
+    RowSource rs;
+    rs.k_pool = p.kc + (size_t)bk * p.pool_rows * (D * 2);
+    rs.v_pool = p.vc + (size_t)bk * p.pool_rows * (D * 2);
+    rs.k_host = p.kh + (size_t)bk * p.T * (D * 2);
+    rs.v_host = p.vh + (size_t)bk * p.T * (D * 2);
+    auto row_code = [&](int j) -> int32_t { return p.resolve ? src[j] : (int32_t)(j0 + j); };
+    float* lbase = nullptr;  // logits of query row 0 of this group, at list row j0
+    if (p.logits != nullptr) lbase = p.logits + ((size_t)b * p.V * p.Hq + kvh * p.G) * p.n_rows + j0;
+    auto logit = [&](int r, int j, float x) {
+        if (lbase != nullptr && r < p.R) {
+            const int v = r / p.G, gg = r % p.G;
+            lbase[((size_t)v * p.Hq + gg) * p.n_rows + j] = x * kLn2;
+        }
     };
+    WarpAcc<D, RP> acc;
+    acc.init();
+    mma_attend_warp<D, RP>(acc, sm + L::oStage + warp * Rows::kWarpBytes, smem_addr(sm + L::oQ), warp, nrows, rs,
+                           p.scale_log2, row_code, logit);
 
-    const int nsub = (nrows + kSub - 1) / kSub;
-    const int my_n = warp < nsub ? (nsub - warp + 3) / 4 : 0;
-
-    // ---- fill stage `st` with sub-chunk ci of this warp: lanes 2j and 2j+1 move row j of K
-    // and of V, alternating 16-byte pieces, so each lane pair reads whole 32-byte sectors;
-    // the row's source is resolved once per lane
-    auto issue = [&](int ci, int st) {
-        const int c = warp + 4 * ci;
-        uint8_t* kst = stages + st * L::kStage;
-        const int row = lane >> 1, half = lane & 1;
-        const int32_t code = row_code(c * kSub + row);
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-            uint8_t* dst = kst + which * kSub * L::kRowB + row * L::kRowB + half * 16;
-            if (code == kNoRow) {
-#pragma unroll
-                for (int i = 0; i < PPR / 2; ++i) *reinterpret_cast<uint4*>(dst + i * 32) = make_uint4(0u, 0u, 0u, 0u);
-            } else {
-                const uint8_t* srow = code >= 0
-                    ? (which ? p.vc : p.kc) + ((size_t)bk * p.pool_rows + code) * (D * 2)
-                    : (which ? p.vh : p.kh) + ((size_t)bk * p.T + (size_t)(-1 - (long)code)) * (D * 2);
-                srow += half * 16;
-#pragma unroll
-                for (int i = 0; i < PPR / 2; ++i) cp_async16(dst + i * 32, srow + i * 32);
-            }
-        }
-        cp_async_commit();
-    };
-
-    float m_r[MT][2], l_r[MT][2];
-    float oacc[MT][NT][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-        m_r[mt][0] = m_r[mt][1] = -INFINITY;
-        l_r[mt][0] = l_r[mt][1] = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) oacc[mt][nt][e] = 0.f;
-    }
-
-    const uint32_t q_base = smem_addr(sm + L::oQ);
-    int issued = 0;
-    for (; issued < min(kWStages, my_n); ++issued) issue(issued, issued);
-    for (int ci = 0; ci < my_n; ++ci) {
-        const int st = ci % kWStages;
-        if (ci + 1 < issued)
-            cp_async_wait<1>();
-        else
-            cp_async_wait<0>();
-        __syncwarp();
-        const uint32_t k_base = smem_addr(stages + st * L::kStage);
-        const uint32_t v_base = k_base + kSub * L::kRowB;
-        const int c = warp + 4 * ci;
-
-        // ---- S = Q K^T for this warp's 16 keys: [MT][2 n-tiles][4]
-        float sacc[MT][2][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < KS; ks += 2) {
-            uint32_t bk0[4], bk1[4];  // n-tile 0 / 1: (b0, b1) of k-step ks, then of ks + 1
-            ldsm_x4(k_base + (0 * 8 + (lane & 7)) * L::kRowB + (ks * 16 + (lane >> 3) * 8) * 2, bk0[0], bk0[1], bk0[2], bk0[3]);
-            ldsm_x4(k_base + (1 * 8 + (lane & 7)) * L::kRowB + (ks * 16 + (lane >> 3) * 8) * 2, bk1[0], bk1[1], bk1[2], bk1[3]);
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(q_base + (mt * 16 + (lane & 15)) * L::kRowB + ((ks + kk) * 16 + (lane >> 4) * 8) * 2, a0, a1, a2, a3);
-                    mma_bf16_16816(sacc[mt][0], a0, a1, a2, a3, bk0[2 * kk], bk0[2 * kk + 1]);
-                    mma_bf16_16816(sacc[mt][1], a0, a1, a2, a3, bk1[2 * kk], bk1[2 * kk + 1]);
-                }
-            }
-        }
-
-        // ---- online softmax (base 2); this lane holds keys 8*nt + 2*t4 + e of rows g, g + 8
-        bool kval[2][2];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) kval[nt][e] = row_code(c * kSub + nt * 8 + 2 * t4 + e) != kNoRow;
-        uint32_t ph[MT][4], pl[MT][4];  // P as A fragments (hi, lo)
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                float x[2][2];
-                float tmax = -INFINITY;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        x[nt][e] = kval[nt][e] ? sacc[mt][nt][2 * hf + e] * p.scale_log2 : -INFINITY;
-                        tmax = fmaxf(tmax, x[nt][e]);
-                    }
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-                const float mo = m_r[mt][hf];
-                const float mn = fmaxf(mo, tmax);
-                const float alpha = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
-                float rs = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float pv = (x[nt][e] == -INFINITY) ? 0.f : fast_exp2(x[nt][e] - mn);
-                        sacc[mt][nt][2 * hf + e] = pv;
-                        rs += pv;
-                    }
-                rs += __shfl_xor_sync(0xffffffffu, rs, 1);
-                rs += __shfl_xor_sync(0xffffffffu, rs, 2);
-                l_r[mt][hf] = l_r[mt][hf] * alpha + rs;
-                m_r[mt][hf] = mn;
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {  // only when a row's maximum moved
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        oacc[mt][nt][2 * hf] *= alpha;
-                        oacc[mt][nt][2 * hf + 1] *= alpha;
-                    }
-                }
-                const int r = mt * 16 + g + 8 * hf;
-                if (p.logits != nullptr && r < p.R) {
-                    const int v = r / p.G, gg = r % p.G;
-                    float* lrow = p.logits + (((size_t)b * p.V + v) * p.Hq + kvh * p.G + gg) * p.n_rows;
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int j = c * kSub + nt * 8 + 2 * t4 + e;
-                            if (j < nrows) lrow[j0 + j] = x[nt][e] * kLn2;
-                        }
-                }
-            }
-            // A fragments: a0 = (g, keys 2t..), a1 = (g+8, 2t..), a2 = (g, 2t+8..), a3 = (g+8, 2t+8..)
-            split_bf16x2(sacc[mt][0][0], sacc[mt][0][1], ph[mt][0], pl[mt][0]);
-            split_bf16x2(sacc[mt][0][2], sacc[mt][0][3], ph[mt][1], pl[mt][1]);
-            split_bf16x2(sacc[mt][1][0], sacc[mt][1][1], ph[mt][2], pl[mt][2]);
-            split_bf16x2(sacc[mt][1][2], sacc[mt][1][3], ph[mt][3], pl[mt][3]);
-        }
-
-        // ---- O += P V: V fragments by ldmatrix.trans, 2 n-tiles per load
-#pragma unroll
-        for (int nt = 0; nt < NT; nt += 2) {
-            uint32_t v0, v1, v2, v3;
-            ldsm_x4_t(v_base + (lane & 15) * L::kRowB + (nt * 8 + (lane >> 4) * 8) * 2, v0, v1, v2, v3);
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                mma_bf16_16816(oacc[mt][nt], ph[mt][0], ph[mt][1], ph[mt][2], ph[mt][3], v0, v1);
-                mma_bf16_16816(oacc[mt][nt], pl[mt][0], pl[mt][1], pl[mt][2], pl[mt][3], v0, v1);
-                mma_bf16_16816(oacc[mt][nt + 1], ph[mt][0], ph[mt][1], ph[mt][2], ph[mt][3], v2, v3);
-                mma_bf16_16816(oacc[mt][nt + 1], pl[mt][0], pl[mt][1], pl[mt][2], pl[mt][3], v2, v3);
-            }
-        }
-        __syncwarp();
-        if (ci + kWStages < my_n) {
-            issue(ci + kWStages, st);
-            ++issued;
-        }
-    }
-
-    // ---- combine the 4 warps: m, l per row, then O rows scaled to the CTA maximum
-    if (t4 == 0) {
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int r = mt * 16 + g + 8 * hf;
-                mlw[warp * RP + r] = m_r[mt][hf];
-                mlw[4 * RP + warp * RP + r] = l_r[mt][hf];
-            }
-    }
-    __syncthreads();  // every warp is done with its stages: they hold the warps' O now
-    // per row: the CTA maximum, the sum of the warps' l rescaled to it, each warp's factor
-    float* rowM = rowv;            // [RP]
-    float* rowL = rowv + RP;       // [RP]
-    float* fac = rowv + 2 * RP;    // [4][RP]
-    if (tid < RP) {
-        const int r = tid;
-        float M = mlw[r];
-#pragma unroll
-        for (int w = 1; w < 4; ++w) M = fmaxf(M, mlw[w * RP + r]);
-        float Ls = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float mw = mlw[w * RP + r];
-            const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-            fac[w * RP + r] = f;
-            Ls = fmaf(mlw[4 * RP + w * RP + r], f, Ls);
-        }
-        rowM[r] = M;
-        rowL[r] = Ls;
-    }
-    __syncthreads();
     float* ow = reinterpret_cast<float*>(sm + L::oStage);  // [4][RP][D]
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            const int r = mt * 16 + g + 8 * hf;
-            const float f = fac[warp * RP + r];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                float2 o2 = make_float2(oacc[mt][nt][2 * hf] * f, oacc[mt][nt][2 * hf + 1] * f);
-                *reinterpret_cast<float2*>(ow + ((size_t)warp * RP + r) * D + nt * 8 + 2 * t4) = o2;
-            }
-        }
-    __syncthreads();
+    mma_combine_warps<D, RP>(acc, mlw, rowv, ow);
+    const float* rowM = rowv;
+    const float* rowL = rowv + RP;
     for (int e = tid; e < p.R * (D / 4); e += kAttThreads) {
         const int r = e / (D / 4), col = (e % (D / 4)) * 4;
         const float Ls = rowL[r];
-        float4 o = *reinterpret_cast<const float4*>(ow + (0 * RP + r) * D + col);
-#pragma unroll
-        for (int w = 1; w < 4; ++w) {
-            const float4 x = *reinterpret_cast<const float4*>(ow + (w * RP + r) * D + col);
-            o.x += x.x;
-            o.y += x.y;
-            o.z += x.z;
-            o.w += x.w;
-        }
+        const float4 o = mma_cta_row4<D, RP>(ow, r, col);
         if (p.splits == 1) {
             const int v = r / p.G, gg = r % p.G;
             const size_t qrow = ((size_t)b * p.V + v) * p.Hq + kvh * p.G + gg;
@@ -786,7 +572,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     }
     if (p.splits == 1) return;
     __syncthreads();  // the stage area is scratch for the merge
-    merge_if_last<D>(p, b, kvh, RP, reinterpret_cast<float*>(sm + L::oStage), 4 * kWStages * L::kStage / 4, flag_s);
+    merge_if_last<D>(p, b, kvh, RP, reinterpret_cast<float*>(sm + L::oStage), Rows::kStagesBytes / 4, flag_s);
 }
 
 int padded_rows(int R) { return R <= 4 ? 4 : R <= 8 ? 8 : R <= 16 ? 16 : R <= 32 ? 32 : -1; }
