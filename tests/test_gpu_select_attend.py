@@ -55,6 +55,14 @@ def make_scores(kind, B, Hkv, N, seed):
         s = (rng.standard_normal((B, Hkv, N)) * 3).astype(np.float32)
         s[..., ::3] = 0.0
         s[..., 1::3] = -0.0
+    elif kind == "denorm":    # boundary among negative denormals, just below the zeros' bin
+        s = np.empty((B, Hkv, N), dtype=np.float32)
+        for r in np.ndindex(B, Hkv):
+            q4 = N // 4
+            vals = np.concatenate([rng.uniform(1, 2, q4).astype(np.float32),            # positives
+                                   np.where(rng.random(q4) < 0.5, 0.0, -0.0).astype(np.float32),
+                                   -(rng.permutation(N - 2 * q4) + 1).astype(np.float32) * np.float32(1e-42)])
+            s[r] = vals[rng.permutation(N)]
     else:
         raise ValueError(kind)
     return torch.from_numpy(s).cuda(), s.astype(np.float64), None
@@ -94,6 +102,7 @@ def run_case(B, V, Hq, Hkv, d, N, block, k, kind, splits, seed, want_logits=True
     (1, 1, 8, 2, 128, 20000, 1, 100, "few", 0),       # candidate overflow -> key passes
     (1, 1, 8, 2, 128, 20000, 1, 100, "flat", 0),      # every score equal, histogram given
     (1, 1, 8, 2, 128, 3001, 1, 1500, "zeros", 0),     # signed zeros in the boundary
+    (1, 1, 8, 2, 128, 4000, 1, 2300, "denorm", 0),    # boundary bin just below zero
     (1, 1, 8, 8, 128, 5000, 1, 333, "normal", 0),     # MHA (G = 1)
     (1, 1, 8, 2, 128, 64, 64, 7, "normal", 0),        # 7 blocks of 64 tokens
     (1, 1, 8, 2, 128, 2048, 64, 64, "index", 0),      # block-selection shape: 2048 blocks

@@ -8,7 +8,7 @@
 //
 // A CTA of 4 warps owns a list of `nrows` K/V rows.  The list is cut into 16-row
 // sub-chunks dealt round-robin to the warps; each warp runs its own 2-deep cp.async
-// pipeline (lanes 2j and 2j+1 move row j of K and of V in alternating 16-byte pieces) and
+// pipeline (8 lanes move one 128-byte line of a row, 4 rows per instruction) and
 // its own online softmax in base 2 over all RP query rows: S[16q x 8k] tiles from Q and K
 // through ldmatrix, P split into bf16 hi + lo parts so the PV product keeps ~16
 // significant bits, V fragments through ldmatrix.trans.  mma_combine_warps then merges
@@ -81,25 +81,32 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
     const int nsub = (nrows + kSub - 1) / kSub;
     const int my_n = warp < nsub ? (nsub - warp + kMmaWarps - 1) / kMmaWarps : 0;
 
+    // Lanes 8q..8q+7 move one 128-byte line of a row per instruction (4 rows at a time), so
+    // every request is a whole line, in HBM and over the host link alike.
     auto issue = [&](int ci, int st) {
         const int c = warp + kMmaWarps * ci;
         uint8_t* kst = stages + st * L::kStage;
-        const int row = lane >> 1, half = lane & 1;
-        const int32_t code = code_of(c * kSub + row);
+        const int sub = lane >> 3, piece = lane & 7;
+        int32_t code[kSub / 4];
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-            uint8_t* dst = kst + which * kSub * L::kRowB + row * L::kRowB + half * 16;
-            if (code == kNoRow) {
+        for (int q = 0; q < kSub / 4; ++q) code[q] = code_of(c * kSub + q * 4 + sub);
 #pragma unroll
-                for (int i = 0; i < PPR / 2; ++i) *reinterpret_cast<uint4*>(dst + i * 32) = make_uint4(0u, 0u, 0u, 0u);
-            } else {
-                const uint8_t* srow = code >= 0 ? (which ? rs.v_pool : rs.k_pool) + (size_t)code * (D * 2)
-                                                : (which ? rs.v_host : rs.k_host) + (size_t)(-1 - (long)code) * (D * 2);
-                srow += half * 16;
+        for (int which = 0; which < 2; ++which)
 #pragma unroll
-                for (int i = 0; i < PPR / 2; ++i) cp_async16(dst + i * 32, srow + i * 32);
+            for (int q = 0; q < kSub / 4; ++q) {
+                uint8_t* dst = kst + which * kSub * L::kRowB + (q * 4 + sub) * L::kRowB + piece * 16;
+                if (code[q] == kNoRow) {
+#pragma unroll
+                    for (int h = 0; h < PPR / 8; ++h) *reinterpret_cast<uint4*>(dst + h * 128) = make_uint4(0u, 0u, 0u, 0u);
+                } else {
+                    const uint8_t* srow = code[q] >= 0
+                        ? (which ? rs.v_pool : rs.k_pool) + (size_t)code[q] * (D * 2)
+                        : (which ? rs.v_host : rs.k_host) + (size_t)(-1 - (long)code[q]) * (D * 2);
+                    srow += piece * 16;
+#pragma unroll
+                    for (int h = 0; h < PPR / 8; ++h) cp_async16(dst + h * 128, srow + h * 128);
+                }
             }
-        }
         cp_async_commit();
     };
 

@@ -16,26 +16,29 @@ namespace {
 
 // ------------------------------------------------------------------ score accumulate
 
-// Dense selection: one thread per (b, position), no atomics, fixed summation order.
+// Dense selection: one thread per (b, position), no atomics, fixed summation order (query
+// rows ascending).  Grid (position blocks, b); the logits were just written by the
+// attention and sit in L2, so all of a thread's rows (up to 32) are loaded before any is
+// used; streaming loads, as nothing reads them again.
 __global__ void score_accumulate_dense_kernel(const float* __restrict__ logits,
-                                              const float* __restrict__ lse, int B, int V, int Hq,
-                                              int T, double weight, double* __restrict__ s) {
-    const long n = (long)B * T;
-    for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n; e += (long)gridDim.x * blockDim.x) {
-        const int b = (int)(e / T), i = (int)(e % T);
-        const int rows = V * Hq;
-        const size_t q0 = (size_t)b * rows;
-        float acc = 0.f;
-        for (int r0 = 0; r0 < rows; r0 += 8) {  // eight loads in flight before any use
-            float z[8];
+                                              const float* __restrict__ lse, int rows, int T,
+                                              double weight, double* __restrict__ s) {
+    constexpr int kBatch = 32;
+    pdl_wait();
+    const int b = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= T) return;
+    const size_t q0 = (size_t)b * rows;
+    float acc = 0.f;
+    for (int r0 = 0; r0 < rows; r0 += kBatch) {
+        float z[kBatch];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) z[u] = r0 + u < rows ? logits[(q0 + r0 + u) * T + i] : 0.f;
+        for (int u = 0; u < kBatch; ++u) z[u] = r0 + u < rows ? __ldcs(logits + (q0 + r0 + u) * T + i) : 0.f;
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (r0 + u < rows) acc += expf(z[u] - lse[q0 + r0 + u]);
-        }
-        s[e] += weight * (double)acc;
+        for (int u = 0; u < kBatch; ++u)
+            if (r0 + u < rows) acc += expf(z[u] - lse[q0 + r0 + u]);
     }
+    s[(size_t)b * T + i] += weight * (double)acc;
 }
 
 // Sparse selection: one thread per (b, kvh, selected row); several KV groups may select
@@ -309,10 +312,11 @@ extern "C" sd_status sd_score_accumulate(const float* logits, const float* lse, 
     cudaStream_t st = as_stream(stream);
     const int threads = 256;
     if (idx == nullptr) {
-        const long n = (long)B * T;
-        const long blocks = std::min<long>((n + threads - 1) / threads, (long)num_sms() * 16);
-        score_accumulate_dense_kernel<<<(unsigned)blocks, threads, 0, st>>>(logits, lse, B, V, Hq, T,
-                                                                           weight, s);
+        SD_REQUIRE(B <= 65535, "sd_score_accumulate: B must be <= 65535");
+        const dim3 grid((unsigned)((T + threads - 1) / threads), (unsigned)B);
+        SD_CUDA_CHECK(launch_pdl(score_accumulate_dense_kernel, grid, dim3(threads), 0, st, logits, lse, V * Hq, T,
+                                 weight, s),
+                      "sd_score_accumulate: launch");
     } else {
         const long n = (long)B * Hkv * n_rows;
         const long blocks = std::min<long>((n + threads - 1) / threads, (long)num_sms() * 16);

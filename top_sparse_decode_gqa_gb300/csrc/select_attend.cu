@@ -10,24 +10,31 @@
 //
 // Computes exactly what sd_topk followed by sd_gather_attend computes, in one launch and
 // without leaving the SMs between the two steps.  CTA c of a cluster owns the contiguous
-// part [c*part, (c+1)*part) of the row's N scores:
-//   1. the row's top digit (11 bits of the order key) comes from the indexer's histogram;
-//      one pass over the part marks every entry above it in a bitmap, keeps the entries of
-//      that digit as candidates and counts their next digit;
-//   2. the next two digits are resolved over the candidates, each CTA summing the P
-//      histograms through distributed shared memory (DSMEM), so every CTA finds the same
-//      threshold key and the same number of ties still needed;
-//   3. the P (above, equal) counts give each CTA its ties (lowest indices first) and its
-//      offset in the row's ascending output; it writes its selected indices there;
-//   4. the CTA then attends over its own selected rows with the warp-MMA loop of
+// part [c*part, (c+1)*part) of the row's N scores.  Exchanges between the CTAs go through
+// distributed shared memory (DSMEM) as pushes (remote adds and stores) followed by one
+// cluster barrier, never as remote reads:
+//   1. the row's top digit d0 (11 bits of the order key) comes from the indexer's
+//      histogram; one pass over the part marks every score above d0's bin in a bitmap
+//      (float compares against the bin's bounds) and keeps the bin's scores as candidates;
+//      their next digit is added into every CTA's histogram (barrier B1);
+//   2. every CTA picks the same digit d1; candidates above it join the bitmap, and those in
+//      the final 21-bit bin are pushed with their positions to every CTA, together with the
+//      part's count of scores above that bin (barrier B2);
+//   3. locally, every CTA finds the threshold key among the final-bin entries, every
+//      part's counts above / equal to it, its own ties (lowest indices first) and its
+//      offset in the row's ascending output, and writes its selected indices there;
+//   4. the CTA attends over its own selected rows with the warp-MMA loop of
 //      attend_mma.cuh (all G*V query rows of the group per fetched row);
-//   5. the P partial (m, l, O) are merged through DSMEM, each CTA finishing every P-th
-//      output column group.
-// When a CTA's candidates overflow its buffer, the cluster resolves the digits and the
-// ordered emit over the keys themselves instead (same result, more passes).
+//   5. the partial (m, l, O) of each query row is pushed to the CTA that owns the row
+//      (barrier B4), which merges the P partials.
+// When the candidates or the final bin overflow their buffers (heavy ties), every CTA
+// resolves the threshold over the whole row from global memory instead (same result).
 #include <cooperative_groups.h>
 
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "attend_mma.cuh"
 #include "sd_common.cuh"
@@ -41,7 +48,6 @@ namespace {
 constexpr int kSaThreads = kMmaWarps * 32;
 constexpr int kSaWarps = kMmaWarps;
 constexpr int kSaHist = 2048;      // bins of the 11-bit digits
-constexpr int kSaCand = 1024;      // candidates a CTA keeps
 constexpr int kSaMaxCluster = 8;   // portable cluster size
 constexpr int kSaWin = 512;        // selected rows whose sources are resolved at a time
 constexpr int kSaPartAlign = 128;  // part sizes are multiples of this many scores
@@ -63,15 +69,29 @@ struct SelAttParams {
     float* lse;
     float* logits;
     int32_t* err;
+    int inbox_own;  // 1: the merge inbox has its own shared memory after the layout's end
 };
 
-// Shared-memory layout.  Phase-A buffers (histograms, bitmaps, candidates) and phase-B
-// buffers (row sources, warp and row statistics, merge weights) share one region: phase B
-// starts after the last barrier at which another CTA reads a phase-A buffer.
+// Shared-memory layout (byte offsets), in order:
+//   Q    the RP query rows (bf16, padded rows)
+//   U    the warps' K/V stages; before them, the part's scores when they are staged
+//   H    hist0 (top digit; after B1 the row's final-bin entries pushed by the cluster),
+//        hist1 (the cluster's sum of digit 1), hist2 (digit 2 of the final bin); the merge
+//        inbox when it has no memory of its own (after barrier B3)
+//   S    sel and tie bitmaps of the part
+//   C    phase A: the candidates' keys and indices; phase B: row sources, warp and
+//        row statistics
+//   Lst  this CTA's final-bin candidates, then its selected entries in ascending order
+//   Misc SaMisc
 struct SaLayout {
-    int oQ, oU, oA, oHist0, oHist1, oHist2, oSel, oTie, oCandK, oCandI;
-    int oSrc, oML, oRow, oW, oMisc, bytes;
+    int oQ, oU, oH, oHist0, oHist1, oHist2, oSel, oTie, oCandK, oCandI, oSrc, oML, oRow, oLst, oMisc, bytes;
 };
+
+constexpr int kSaCand = 1024;  // candidates a CTA keeps
+constexpr int kSaList = 512;   // selected entries a CTA keeps in shared memory
+constexpr int kSaFb = 1024;    // final-bin entries of a row (keys + positions in hist0's 8 KB)
+constexpr int kSaHBytes = (2 * kSaHist + kSaHist / 2) * 4;
+constexpr int kSaTwoPerSm = 233472 / 2 - 1024;  // dynamic shared memory of one of two CTAs per SM
 
 __host__ __device__ constexpr int sa_align(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -81,38 +101,46 @@ __host__ __device__ inline SaLayout sa_layout(int D, int RP, int part, int stage
     const int stages = kMmaWarps * kWStages * 2 * kSub * row_b;
     L.oQ = 0;
     L.oU = sa_align(RP * row_b, 128);
-    const int u = sa_align(staged && part * 4 > stages ? part * 4 : stages, 128);
-    L.oA = L.oU + u;
-    // phase A
-    L.oHist0 = L.oA;
+    L.oH = L.oU + sa_align(staged && part * 4 > stages ? part * 4 : stages, 128);
+    L.oHist0 = L.oH;
     L.oHist1 = L.oHist0 + kSaHist * 4;
     L.oHist2 = L.oHist1 + kSaHist * 4;
-    L.oSel = L.oHist2 + (kSaHist / 2) * 4;
+    L.oSel = L.oH + kSaHBytes;
     L.oTie = L.oSel + part / 8;
     L.oCandK = L.oTie + part / 8;
     L.oCandI = L.oCandK + kSaCand * 4;
-    const int end_a = L.oCandI + kSaCand * 4;
-    // phase B
-    L.oSrc = L.oA;
+    L.oSrc = L.oCandK;
     L.oML = L.oSrc + kSaWin * 4;
     L.oRow = L.oML + 2 * kMmaWarps * RP * 4;
-    L.oW = L.oRow + 6 * RP * 4;
-    const int end_b = L.oW + (kSaMaxCluster + 1) * RP * 4;
-    L.oMisc = sa_align(end_a > end_b ? end_a : end_b, 16);
-    L.bytes = L.oMisc + 128;
+    L.oLst = L.oCandI + kSaCand * 4;
+    L.oMisc = L.oLst + kSaList * 4;
+    L.bytes = L.oMisc + 256;
     return L;
 }
 
-// Values a CTA publishes to its cluster (at the start of the misc area).
+// Merge inbox inside H: for each of this CTA's query rows (r = lr * P + rank) and each
+// source CTA s, O[lr][s][D], then m[lr][s], l[lr][s].
+__host__ __device__ inline int sa_inbox_bytes(int D, int R, int P) {
+    const int slots = (R + P - 1) / P * P;
+    return slots * (D + 2) * 4;
+}
+
+// Values the CTAs of a cluster exchange (ovf, cnt_gt and cnt_eq are written by the other
+// CTAs) and the CTA's own scratch.
 struct SaMisc {
-    uint32_t n_cand;   // candidates seen (may exceed kSaCand)
-    uint32_t gt, eq;   // entries above / equal to the threshold key
-    uint32_t pad0;
-    uint32_t wgt[kSaWarps], weq[kSaWarps];  // per-warp counts of the ordered emit
+    uint32_t ovf;                     // some CTA's candidate list overflowed
+    uint32_t dsure[kSaMaxCluster];    // per CTA of the cluster: entries above the final bin
+    uint32_t fb_n;                    // final-bin entries pushed into this CTA so far
+    uint32_t fb_off[kSaMaxCluster];   // where this CTA's entries go in each CTA's buffer
+    uint32_t cgt[kSaMaxCluster], ceq[kSaMaxCluster];  // per part: above / equal to the threshold
+    uint32_t nfb;                     // this CTA's final-bin entries
+    uint32_t ncand;                   // candidates of this part (may exceed kSaCand)
+    uint32_t wgt[kSaWarps], weq[kSaWarps];
     uint32_t wsum[kSaWarps];
-    uint32_t sel_digit, sel_above;
+    uint32_t sel_digit, sel_above, tot;
     uint64_t bar;
 };
+static_assert(sizeof(SaMisc) <= 256, "misc area");
 
 // Inclusive prefix sum over the CTA's 128 threads (one value each).
 SD_DEVINL uint32_t cta_inclusive_scan(uint32_t v, uint32_t* wsum) {
@@ -130,6 +158,16 @@ SD_DEVINL uint32_t cta_inclusive_scan(uint32_t v, uint32_t* wsum) {
         if (w < warp) off += wsum[w];
     __syncthreads();
     return v + off;
+}
+
+// Block-wide exclusive prefix sum; also returns the total.
+SD_DEVINL uint32_t cta_exclusive_scan(uint32_t v, SaMisc* ms, uint32_t& total) {
+    const uint32_t incl = cta_inclusive_scan(v, ms->wsum);
+    if ((int)threadIdx.x == kSaThreads - 1) ms->tot = incl;
+    __syncthreads();
+    total = ms->tot;
+    __syncthreads();
+    return incl - v;
 }
 
 // Given the histogram of one digit (nb bins, higher bins = larger keys) of the entries
@@ -166,18 +204,13 @@ SD_DEVINL void cta_select_digit(const uint32_t* hist, int nb, uint32_t krem, SaM
     __syncthreads();
 }
 
-// dst[i] = sum over the cluster's P CTAs of their copy of src[i], i < n (n a multiple of
-// 4 * kSaThreads is not required; n is a multiple of 4).
+// dst[i] = sum over the cluster's P CTAs of their copy of src[i], i < n (n a multiple of 4).
 SD_DEVINL void cluster_sum_hist(cg::cluster_group& cl, const uint32_t* src, uint32_t* dst, int n, int P) {
-    const uint4* rem[kSaMaxCluster];
-#pragma unroll
-    for (int c = 0; c < kSaMaxCluster; ++c)
-        rem[c] = reinterpret_cast<const uint4*>(cl.map_shared_rank(const_cast<uint32_t*>(src), c < P ? c : 0));
     for (int i = threadIdx.x; i < n / 4; i += kSaThreads) {
         uint4 x[kSaMaxCluster];
 #pragma unroll
         for (int c = 0; c < kSaMaxCluster; ++c)
-            if (c < P) x[c] = rem[c][i];
+            if (c < P) x[c] = reinterpret_cast<const uint4*>(cl.map_shared_rank(const_cast<uint32_t*>(src), c))[i];
         uint4 s = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int c = 0; c < kSaMaxCluster; ++c)
@@ -191,15 +224,17 @@ SD_DEVINL void cluster_sum_hist(cg::cluster_group& cl, const uint32_t* src, uint
     }
 }
 
-// Block-wide exclusive prefix sum; also returns the total.
-SD_DEVINL uint32_t cta_exclusive_scan(uint32_t v, uint32_t* wsum, uint32_t& total) {
-    const uint32_t incl = cta_inclusive_scan(v, wsum);
-    __shared__ uint32_t tot;
-    if ((int)threadIdx.x == kSaThreads - 1) tot = incl;
-    __syncthreads();
-    total = tot;
-    __syncthreads();
-    return incl - v;
+// Adds `v` to bin `bin` of the array `h` (same shared-memory offset) of every CTA of the
+// cluster, this one included.
+SD_DEVINL void cluster_add(cg::cluster_group& cl, uint32_t* h, uint32_t bin, uint32_t v, int P) {
+    for (int c = 0; c < P; ++c) atomicAdd(cl.map_shared_rank(h, c) + bin, v);
+}
+
+// The float whose order key is k (the inverse of float_key); k = 0x7FFFFFFF, the key no
+// float maps to (-0 takes the key of +0), gives the largest float below it, -denorm_min.
+SD_DEVINL float key_float(uint32_t k) {
+    if (k == 0x7FFFFFFFu) return __uint_as_float(0x80000001u);
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 template <int D, int RP>
@@ -219,6 +254,7 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
     uint32_t* tie = reinterpret_cast<uint32_t*>(sm + L.oTie);
     uint32_t* cand_k = reinterpret_cast<uint32_t*>(sm + L.oCandK);
     uint32_t* cand_i = reinterpret_cast<uint32_t*>(sm + L.oCandI);
+    int32_t* lst = reinterpret_cast<int32_t*>(sm + L.oLst);
     SaMisc* ms = reinterpret_cast<SaMisc*>(sm + L.oMisc);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -230,15 +266,19 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
     const float* srow = p.scores + (size_t)bk * N;
     int32_t* orow = p.idx + (size_t)bk * k;
     uint32_t* hrow = p.key_hist != nullptr ? p.key_hist + (size_t)bk * kSaHist : nullptr;
+    const bool trivial = (k == 0 || k == N);  // no select needed (every CTA agrees)
 
+    // ---- zero what the cluster adds into; B0: nobody adds before everyone has zeroed
     if (tid == 0) {
-        ms->n_cand = 0;
+        ms->ovf = 0;
+        ms->fb_n = 0;
+        ms->nfb = 0;
         mbar_init(&ms->bar, 1);
         fence_mbarrier_init();
     }
-    for (int i = tid; i < kSaHist; i += kSaThreads) hist1[i] = 0u;
-    for (int i = tid; i < kSaHist / 2; i += kSaThreads) hist2[i] = 0u;
-    __syncthreads();
+    if (tid == 0) ms->ncand = 0;
+    for (int i = tid; i < 2 * kSaHist + kSaHist / 2; i += kSaThreads) hist0[i] = 0u;  // hist0, hist1, hist2
+    cl.sync();  // B0
 
     pdl_wait();  // scores, key_hist and q may come from the preceding kernels
 
@@ -264,14 +304,9 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
         }
     }
     cp_async_commit();
-
-    // ---- the top digit's histogram: from the indexer, or counted here and summed
-    uint32_t d0 = 0, above0 = 0;
-    const bool trivial = (k == 0 || k == N);  // no select needed (every CTA agrees)
-    if (hrow != nullptr) {
+    if (hrow != nullptr && !trivial)
         for (int i = tid; i < kSaHist / 4; i += kSaThreads)
             reinterpret_cast<uint4*>(hist0)[i] = __ldcg(reinterpret_cast<const uint4*>(hrow) + i);
-    }
     if (staged) {
         const bool ok = mbar_wait(&ms->bar, 0);
         if (__syncthreads_or(!ok)) {  // keep going on the global copy; the result is flagged
@@ -282,131 +317,321 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
     auto key_at = [&](int i) -> uint32_t {  // i in [p0, p1)
         return float_key(staged ? __uint_as_float(keys_s[i - p0]) : __ldcg(srow + i));
     };
-    if (hrow == nullptr && !trivial) {
-        // count the top digit of the part into hist1, then sum the cluster's into hist0
-        for (int base = p0 + warp * 32; base < p1; base += kSaThreads) {
-            const int i = base + lane;
-            const bool valid = i < p1;
-            const uint32_t dg = valid ? key_at(i) >> 21 : 0xffffffffu;
-            const uint32_t peers = __match_any_sync(0xffffffffu, dg);
-            if (valid && lane == __ffs(peers) - 1) atomicAdd(&hist1[dg], (uint32_t)__popc(peers));
-        }
-        cl.sync();
-        cluster_sum_hist(cl, hist1, hist0, kSaHist, P);
-        cl.sync();  // every CTA has read the others' hist1
-        for (int i = tid; i < kSaHist; i += kSaThreads) hist1[i] = 0u;
-    }
-    __syncthreads();
-    if (!trivial) cta_select_digit(hist0, kSaHist, (uint32_t)k, ms, d0, above0);
-    d0 &= kSaHist - 1;
-    uint32_t krem = (uint32_t)k - above0;
 
-    // ---- one pass over the part: bitmap of entries above d0, candidates of digit d0 and
-    // the histogram of their next digit
+    // ---- the top digit: from the indexer's histogram, or counted here and summed
+    uint32_t d0 = 0, above0 = 0;
     if (!trivial) {
-        const uint32_t lt = lanemask_lt();
-        constexpr int U = 8;
-        for (int g0 = warp; g0 < nw; g0 += U * kSaWarps) {
-            uint32_t kk[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int i = p0 + (g0 + u * kSaWarps) * 32 + lane;
-                kk[u] = (g0 + u * kSaWarps < nw && i < p1) ? key_at(i) : 0u;
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int gw = g0 + u * kSaWarps;
-                if (gw >= nw) break;
-                const int li = gw * 32 + lane;
-                const bool valid = p0 + li < p1;
-                const uint32_t dg = kk[u] >> 21;
-                const uint32_t sure = __ballot_sync(0xffffffffu, valid && dg > d0);
-                if (lane == 0) {
-                    sel[gw] = sure;
-                    tie[gw] = 0u;
-                }
-                const bool in = valid && dg == d0;
-                if (in) atomicAdd(&hist1[(kk[u] >> 10) & (kSaHist - 1)], 1u);
-                const uint32_t m = __ballot_sync(0xffffffffu, in);
-                if (m != 0u) {
-                    const int leader = __ffs(m) - 1;
-                    uint32_t at = 0;
-                    if (lane == leader) at = atomicAdd(&ms->n_cand, (uint32_t)__popc(m));
-                    at = __shfl_sync(0xffffffffu, at, leader);
-                    const uint32_t slot = at + __popc(m & lt);
-                    if (in && slot < (uint32_t)kSaCand) {
-                        cand_k[slot] = kk[u];
-                        cand_i[slot] = (uint32_t)li;
-                    }
-                }
-            }
-        }
-    }
-    cl.sync();  // B1: hist1, n_cand published; every CTA has read key_hist
-    if (hrow != nullptr && rank == 0)
-        for (int i = tid; i < kSaHist / 4; i += kSaThreads) reinterpret_cast<uint4*>(hrow)[i] = make_uint4(0u, 0u, 0u, 0u);
-    bool overflow = false;
-#pragma unroll
-    for (int c = 0; c < kSaMaxCluster; ++c)
-        if (c < P) overflow |= cl.map_shared_rank(&ms->n_cand, c)[0] > (uint32_t)kSaCand;
-    const uint32_t n_cand = min(ms->n_cand, (uint32_t)kSaCand);
-
-    uint32_t thr = 0;
-    uint32_t my_gt = 0, my_eq = 0;
-    if (!trivial) {
-        // ---- digit 1 (bits 20..10): sum of the cluster's hist1 into hist0
-        cluster_sum_hist(cl, hist1, hist0, kSaHist, P);
-        __syncthreads();
-        uint32_t d1, ab1;
-        cta_select_digit(hist0, kSaHist, krem, ms, d1, ab1);
-        d1 &= kSaHist - 1;
-        krem -= ab1;
-        const uint32_t pre21 = (d0 << 11) | d1;
-        // ---- digit 2 (bits 9..0) over the entries with those 21 top bits
-        if (!overflow) {
-            for (uint32_t c = tid; c < n_cand; c += kSaThreads) {
-                const uint32_t ck = cand_k[c];
-                if ((ck >> 10) == pre21) atomicAdd(&hist2[ck & 1023u], 1u);
-            }
-        } else {
+        const uint32_t* top = hist0;
+        if (hrow == nullptr) {
             for (int base = p0 + warp * 32; base < p1; base += kSaThreads) {
                 const int i = base + lane;
                 const bool valid = i < p1;
-                const uint32_t kk = valid ? key_at(i) : 0u;
-                const bool in = valid && (kk >> 10) == pre21;
-                const uint32_t peers = __match_any_sync(0xffffffffu, in ? (kk & 1023u) : 0xffffffffu);
-                if (in && lane == __ffs(peers) - 1) atomicAdd(&hist2[kk & 1023u], (uint32_t)__popc(peers));
+                const uint32_t dg = valid ? key_at(i) >> 21 : 0xffffffffu;
+                const uint32_t peers = __match_any_sync(0xffffffffu, dg);
+                if (valid && lane == __ffs(peers) - 1) atomicAdd(&hist0[dg], (uint32_t)__popc(peers));
+            }
+            cl.sync();  // every CTA's top-digit counts are complete (and are not changed again)
+            cluster_sum_hist(cl, hist0, cand_k, kSaHist, P);  // the candidate area is free until the pass
+            top = cand_k;
+        }
+        __syncthreads();
+        cta_select_digit(top, kSaHist, (uint32_t)k, ms, d0, above0);
+        d0 &= kSaHist - 1;
+    }
+    uint32_t krem = (uint32_t)k - above0;
+    const uint32_t krem0 = krem;  // still needed from the d0 bin (the fallback restarts there)
+
+    // ---- one pass over the part: bitmaps of the entries above d0's bin (sel) and in it (the
+    // candidates, in tie for now), written by lanes 0..U-1 without divergence; then the
+    // candidates are listed with one scan and their next digit is added to every CTA's hist1
+    if (!trivial) {
+        constexpr int U = 8;
+        // the d0 bin as the closed float interval [f_lo, f_hi]: a score lies above the bin iff
+        // f > f_hi and in it iff f_lo <= f <= f_hi (-0 and +0 compare equal, as their order
+        // keys do); the bins next to the infinities and NaN keys compare keys instead
+        const uint32_t k_lo = d0 << 21, k_hi = k_lo | 0x1FFFFFu;
+        const bool fcmp = d0 > 0x003u && d0 < 0x7FCu;
+        const float f_lo = key_float(k_lo), f_hi = key_float(k_hi);
+        for (int g0 = warp; g0 < nw; g0 += U * kSaWarps) {
+            float f[U];
+            uint32_t sure[U], cm[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = p0 + (g0 + u * kSaWarps) * 32 + lane;
+                f[u] = i < p1 ? (staged ? __uint_as_float(keys_s[i - p0]) : __ldcg(srow + i)) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const bool valid = p0 + (g0 + u * kSaWarps) * 32 + lane < p1;  // also false past nw
+                bool above, in;
+                if (fcmp) {
+                    above = f[u] > f_hi;
+                    in = f[u] >= f_lo && f[u] <= f_hi;
+                } else {
+                    const uint32_t kk = float_key(f[u]);
+                    above = kk > k_hi;
+                    in = (kk >> 21) == d0;
+                }
+                sure[u] = __ballot_sync(0xffffffffu, valid && above);
+                cm[u] = __ballot_sync(0xffffffffu, valid && in);
+            }
+            uint32_t my_s = 0, my_c = 0;  // lane u keeps group u's words
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                my_s = lane == u ? sure[u] : my_s;
+                my_c = lane == u ? cm[u] : my_c;
+            }
+            const int gw = g0 + lane * kSaWarps;
+            if (lane < U && gw < nw) {
+                sel[gw] = my_s;
+                tie[gw] = my_c;
             }
         }
-        cl.sync();  // B2: hist2 published; nobody reads hist1 any more
-        cluster_sum_hist(cl, hist2, hist1, kSaHist / 2, P);
+        __syncthreads();
+        // list the candidates: thread t owns words [t*W, t*W + W)
+        const int W = (nw + kSaThreads - 1) / kSaThreads;
+        const int w0 = tid * W, w1 = min(nw, w0 + W);
+        uint32_t cnt = 0, n_cand;
+        for (int w = w0; w < w1; ++w) cnt += __popc(tie[w]);
+        uint32_t slot = cta_exclusive_scan(cnt, ms, n_cand);
+        for (int w = w0; w < w1; ++w) {
+            uint32_t bits = tie[w];
+            tie[w] = 0u;  // the tie bitmap proper starts empty
+            while (bits != 0u) {
+                const int li = w * 32 + __ffs(bits) - 1;
+                bits &= bits - 1u;
+                if (slot < (uint32_t)kSaCand) {
+                    cand_k[slot] = float_key(staged ? __uint_as_float(keys_s[li]) : __ldcg(srow + p0 + li));
+                    cand_i[slot] = (uint32_t)li;
+                }
+                ++slot;
+            }
+        }
+        if (tid == 0) ms->ncand = n_cand;
+        __syncthreads();
+        if (n_cand <= (uint32_t)kSaCand) {
+            for (uint32_t c = tid; c < n_cand; c += kSaThreads)
+                cluster_add(cl, hist1, (cand_k[c] >> 10) & (kSaHist - 1), 1u, P);
+        } else {
+            // more candidates than the list holds: count their next digit over the keys
+            for (int base0 = p0 + warp * 32; base0 < p1; base0 += kSaThreads) {
+                const int i = base0 + lane;
+                const bool valid = i < p1;
+                const uint32_t kk = valid ? key_at(i) : 0u;
+                const bool in = valid && (kk >> 21) == d0;
+                const uint32_t bin = (kk >> 10) & (kSaHist - 1);
+                const uint32_t peers = __match_any_sync(0xffffffffu, in ? bin : 0xffffffffu);
+                if (in && lane == __ffs(peers) - 1) cluster_add(cl, hist1, bin, (uint32_t)__popc(peers), P);
+            }
+            if (tid == 0)
+                for (int c = 0; c < P; ++c) atomicOr(cl.map_shared_rank(&ms->ovf, c), 1u);
+        }
+    }
+    cl.sync();  // B1: hist1 and ovf complete in every CTA; every CTA has read key_hist
+    if (hrow != nullptr && rank == 0)
+        for (int i = tid; i < kSaHist / 4; i += kSaThreads) reinterpret_cast<uint4*>(hrow)[i] = make_uint4(0u, 0u, 0u, 0u);
+    // candidate c of the per-warp lists, or false past a warp's count
+    const uint32_t n_cand = min(ms->ncand, (uint32_t)kSaCand);
+    uint32_t* fbk = hist0;             // final-bin keys pushed by the cluster (hist0 is done with)
+    uint32_t* fbp = hist0 + kSaFb;     // and their positions in the row
+    bool fallback = !trivial && ms->ovf != 0u;
+
+    // ---- digit 1 (bits 20..10) from the cluster's sum; candidates above its bin join the
+    // selection, those in it (the final bin) are pushed to every CTA with this part's count
+    // of entries above the final bin
+    uint32_t pre21 = 0;
+    if (!trivial && !fallback) {
+        uint32_t d1, ab1;
+        cta_select_digit(hist1, kSaHist, krem, ms, d1, ab1);
+        d1 &= kSaHist - 1;
+        krem -= ab1;
+        pre21 = (d0 << 11) | d1;
+        for (uint32_t c = tid; c < n_cand; c += kSaThreads) {
+            const uint32_t ck = cand_k[c], ci = cand_i[c], dg = (ck >> 10) & (kSaHist - 1);
+            if (dg > d1) {
+                atomicOr(&sel[ci >> 5], 1u << (ci & 31));
+            } else if (dg == d1) {
+                const uint32_t q = atomicAdd(&ms->nfb, 1u);
+                if (q < (uint32_t)kSaList) lst[q] = c;
+            }
+        }
+        __syncthreads();
+        uint32_t cnt = 0;
+        for (int w = tid; w < nw; w += kSaThreads) cnt += __popc(sel[w]);
+        uint32_t total;
+        cta_exclusive_scan(cnt, ms, total);
+        const uint32_t nfb = min(ms->nfb, (uint32_t)kSaList);
+        if (tid < P) {
+            SaMisc* rm = cl.map_shared_rank(ms, tid);
+            // a list longer than this CTA keeps pushes the cluster's total past the buffer
+            ms->fb_off[tid] = atomicAdd(&rm->fb_n, ms->nfb > (uint32_t)kSaList ? (uint32_t)kSaFb + 1u : ms->nfb);
+            rm->dsure[rank] = total;
+        }
+        __syncthreads();
+        for (uint32_t q = tid; q < nfb; q += kSaThreads) {
+            const int c = lst[q];
+            const uint32_t key = cand_k[c], pos = (uint32_t)p0 + cand_i[c];
+            for (int t = 0; t < P; ++t) {
+                const uint32_t slot = ms->fb_off[t] + q;
+                if (slot < (uint32_t)kSaFb) {
+                    cl.map_shared_rank(fbk, t)[slot] = key;
+                    cl.map_shared_rank(fbp, t)[slot] = pos;
+                }
+            }
+        }
+    }
+    cl.sync();  // B2: every CTA holds the row's final-bin entries and the parts' counts above it
+    if (!trivial && !fallback && ms->fb_n > (uint32_t)kSaFb) fallback = true;  // same in every CTA
+
+    uint32_t thr = 0, base = 0, take = 0, my_gt = 0, my_eq = 0;
+    if (!trivial && !fallback) {
+        // ---- digit 2 (bits 9..0) among the final-bin entries: the threshold key
+        const uint32_t n_fb = ms->fb_n;
+        for (int i = tid; i < kSaHist / 2; i += kSaThreads) hist2[i] = 0u;
+        if (tid < kSaMaxCluster) {
+            ms->cgt[tid] = tid < P ? ms->dsure[tid] : 0u;
+            ms->ceq[tid] = 0u;
+        }
+        __syncthreads();
+        for (uint32_t e = tid; e < n_fb; e += kSaThreads) atomicAdd(&hist2[fbk[e] & 1023u], 1u);
         __syncthreads();
         uint32_t d2, ab2;
-        cta_select_digit(hist1, kSaHist / 2, krem, ms, d2, ab2);
+        cta_select_digit(hist2, kSaHist / 2, krem, ms, d2, ab2);
         d2 &= 1023u;
         krem -= ab2;
         thr = (pre21 << 10) | d2;
-        // ---- this part's counts above / equal to the threshold
-        if (!overflow) {
-            uint32_t gt = 0, eq = 0;
-            for (int w = tid; w < nw; w += kSaThreads) gt += __popc(sel[w]);
-            for (uint32_t c = tid; c < n_cand; c += kSaThreads) {
-                gt += cand_k[c] > thr;
-                eq += cand_k[c] == thr;
+        // ---- every part's counts above / equal to the threshold, from the final bin
+        for (uint32_t e = tid; e < n_fb; e += kSaThreads) {
+            const uint32_t key = fbk[e], r = min(fbp[e] / (uint32_t)p.part, (uint32_t)(P - 1));
+            if (key > thr) atomicAdd(&ms->cgt[r], 1u);
+            else if (key == thr) atomicAdd(&ms->ceq[r], 1u);
+        }
+        __syncthreads();
+        // ---- the final-bin entries of this part above the threshold join the selection, those
+        // equal to it are ties
+        for (uint32_t e = tid; e < n_fb; e += kSaThreads) {
+            const uint32_t pos = fbp[e];
+            if (pos < (uint32_t)p0 || pos >= (uint32_t)p1) continue;
+            const uint32_t li = pos - (uint32_t)p0;
+            if (fbk[e] > thr) atomicOr(&sel[li >> 5], 1u << (li & 31));
+            else if (fbk[e] == thr) atomicOr(&tie[li >> 5], 1u << (li & 31));
+        }
+        my_gt = ms->cgt[rank];
+        my_eq = ms->ceq[rank];
+    } else if (fallback) {
+        // ---- heavy ties: every CTA resolves the threshold over the whole row from global
+        // memory (no more exchanges), then counts every part
+        uint32_t prefix = d0 << 21, pmask = 0x7FFu << 21;
+        const int nall = N;
+        krem = krem0;
+#pragma unroll 1
+        for (int pass = 1; pass < 3; ++pass) {
+            const int shift = pass == 1 ? 10 : 0;
+            const uint32_t nb = pass == 1 ? 2048u : 1024u;
+            for (int i = tid; i < kSaHist; i += kSaThreads) hist0[i] = 0u;
+            __syncthreads();
+            for (int base0 = warp * 32; base0 < nall; base0 += kSaThreads) {
+                const int i = base0 + lane;
+                const bool valid = i < nall;
+                const uint32_t kk = valid ? float_key(__ldcg(srow + i)) : 0u;
+                const bool in = valid && (kk & pmask) == prefix;
+                const uint32_t dg = (kk >> shift) & (nb - 1);
+                const uint32_t peers = __match_any_sync(0xffffffffu, in ? dg : 0xffffffffu);
+                if (in && lane == __ffs(peers) - 1) atomicAdd(&hist0[dg], (uint32_t)__popc(peers));
             }
-            gt = __reduce_add_sync(0xffffffffu, gt);
-            eq = __reduce_add_sync(0xffffffffu, eq);
-            if (lane == 0) {
-                ms->wgt[warp] = gt;
-                ms->weq[warp] = eq;
+            __syncthreads();
+            uint32_t dg, ab;
+            cta_select_digit(hist0, (int)nb, krem, ms, dg, ab);
+            prefix |= (dg & (nb - 1)) << shift;
+            pmask |= (nb - 1) << shift;
+            krem -= ab;
+        }
+        thr = prefix;
+        if (tid < kSaMaxCluster) ms->cgt[tid] = ms->ceq[tid] = 0u;
+        __syncthreads();
+        for (int base0 = warp * 32; base0 < nall; base0 += kSaThreads) {  // groups never straddle parts
+            const int i = base0 + lane;
+            const bool valid = i < nall;
+            const uint32_t kk = valid ? float_key(__ldcg(srow + i)) : 0u;
+            const uint32_t gt = __popc(__ballot_sync(0xffffffffu, valid && kk > thr));
+            const uint32_t eq = __popc(__ballot_sync(0xffffffffu, valid && kk == thr));
+            if (lane == 0 && (gt | eq)) {
+                const int r = min(base0 / p.part, P - 1);
+                atomicAdd(&ms->cgt[r], gt);
+                atomicAdd(&ms->ceq[r], eq);
             }
-        } else {
-            // warp w scans the contiguous segment [p0 + w*seg, p0 + (w+1)*seg)
-            const int seg = ((np + kSaWarps - 1) / kSaWarps + 31) / 32 * 32;
-            const int s0 = p0 + warp * seg, s1 = min(p1, s0 + seg);
+        }
+        __syncthreads();
+        my_gt = ms->cgt[rank];
+        my_eq = ms->ceq[rank];
+    } else if (k == N) {
+        my_gt = (uint32_t)np;
+        for (int c = tid; c < P; c += kSaThreads) ms->cgt[c] = (uint32_t)min(p.part, N - c * p.part);
+        if (tid < kSaMaxCluster) ms->ceq[tid] = 0u;
+        __syncthreads();
+    } else if (tid < kSaMaxCluster) {  // k == 0
+        ms->cgt[tid] = ms->ceq[tid] = 0u;
+    }
+    __syncthreads();
+
+    // ---- this CTA's ties and its offset in the row's ascending output
+    {
+        uint32_t eq_before = 0;
+        for (int c = 0; c < rank; ++c) {
+            const uint32_t ec = ms->ceq[c];
+            const uint32_t tc = krem > eq_before ? min(ec, krem - eq_before) : 0u;
+            base += ms->cgt[c] + tc;
+            eq_before += ec;
+        }
+        take = krem > eq_before ? min(my_eq, krem - eq_before) : 0u;
+    }
+    const uint32_t n_mine = base >= (uint32_t)k ? 0u : min(my_gt + take, (uint32_t)k - base);
+    auto put = [&](uint32_t at, int pos) {  // at < n_mine
+        orow[base + at] = pos;
+        if (at < (uint32_t)kSaList) lst[at] = pos;
+    };
+    __syncthreads();  // lst is rewritten below
+
+    // ---- ordered emit of this part's selection into idx[base, base + n_mine)
+    if (k == N) {
+        for (int i = tid; i < np; i += kSaThreads) put((uint32_t)i, p0 + i);
+    } else if (!trivial && !fallback) {
+        // one scan gives each thread the selected and tied entries before its words
+        const int W = (nw + kSaThreads - 1) / kSaThreads;  // words per thread
+        const int w0 = tid * W, w1 = min(nw, w0 + W);
+        uint32_t cs = 0, ct = 0;
+        for (int w = w0; w < w1; ++w) {
+            cs += __popc(sel[w]);
+            ct += __popc(tie[w]);
+        }
+        uint32_t tot_s, tot_t;
+        const uint32_t sel_before = cta_exclusive_scan(cs, ms, tot_s);
+        const uint32_t tie_before = cta_exclusive_scan(ct, ms, tot_t);
+        uint32_t ties_left = take > tie_before ? take - tie_before : 0u;
+        uint32_t at = sel_before + min(tie_before, take);
+        for (int w = w0; w < w1; ++w) {
+            uint32_t bits = sel[w], tb = tie[w];
+            while (tb != 0u && ties_left > 0u) {  // the lowest-index ties still needed
+                const uint32_t low = tb & (0u - tb);
+                bits |= low;
+                tb ^= low;
+                --ties_left;
+            }
+            while (bits != 0u) {
+                const int bpos = __ffs(bits) - 1;
+                bits &= bits - 1u;
+                if (at < n_mine) put(at, p0 + w * 32 + bpos);
+                ++at;
+            }
+        }
+    } else if (!trivial) {
+        // ordered ballot emit over the keys: warp w scans [p0 + w*seg, p0 + (w+1)*seg)
+        const int seg = ((np + kSaWarps - 1) / kSaWarps + 31) / 32 * 32;
+        const int s0 = p0 + warp * seg, s1 = min(p1, s0 + seg);
+        {
             uint32_t gt = 0, eq = 0;
-            for (int base = s0; base < s1; base += 32) {
-                const int i = base + lane;
+            for (int i0 = s0; i0 < s1; i0 += 32) {
+                const int i = i0 + lane;
                 const bool valid = i < s1;
                 const uint32_t kk = valid ? key_at(i) : 0u;
                 gt += __popc(__ballot_sync(0xffffffffu, valid && kk > thr));
@@ -418,75 +643,6 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
             }
         }
         __syncthreads();
-#pragma unroll
-        for (int w = 0; w < kSaWarps; ++w) {
-            my_gt += ms->wgt[w];
-            my_eq += ms->weq[w];
-        }
-    } else if (k == N) {
-        my_gt = (uint32_t)np;
-    }
-    if (tid == 0) {
-        ms->gt = my_gt;
-        ms->eq = my_eq;
-    }
-    cl.sync();  // B3: counts published; nobody reads a histogram any more
-
-    // ---- this CTA's ties and its offset in the row's ascending output
-    uint32_t base = 0, take = 0;
-    {
-        uint32_t eq_before = 0;
-        for (int c = 0; c < rank; ++c) {
-            const SaMisc* rm = cl.map_shared_rank(ms, c);
-            const uint32_t gc = rm->gt, ec = rm->eq;
-            const uint32_t tc = krem > eq_before ? min(ec, krem - eq_before) : 0u;
-            base += gc + tc;
-            eq_before += ec;
-        }
-        take = krem > eq_before ? min(my_eq, krem - eq_before) : 0u;
-    }
-    const uint32_t n_mine = base >= (uint32_t)k ? 0u : min(my_gt + take, (uint32_t)k - base);
-
-    // ---- ordered emit of this part's selection into idx[base, base + n_mine)
-    if (k == N) {
-        for (int i = tid; i < np; i += kSaThreads) orow[p0 + i] = p0 + i;
-    } else if (!trivial && !overflow) {
-        for (uint32_t c = tid; c < n_cand; c += kSaThreads) {
-            const uint32_t ck = cand_k[c], ci = cand_i[c];
-            if (ck > thr) atomicOr(&sel[ci >> 5], 1u << (ci & 31));
-            else if (ck == thr) atomicOr(&tie[ci >> 5], 1u << (ci & 31));
-        }
-        __syncthreads();
-        const int W = (nw + kSaThreads - 1) / kSaThreads;  // words per thread
-        const int w0 = tid * W, w1 = min(nw, w0 + W);
-        uint32_t cnt = 0, total;
-        for (int w = w0; w < w1; ++w) cnt += __popc(tie[w]);
-        uint32_t before = cta_exclusive_scan(cnt, ms->wsum, total);
-        for (int w = w0; w < w1; ++w) {
-            uint32_t bits = tie[w];
-            while (bits != 0u && before < take) {
-                const uint32_t low = bits & (0u - bits);
-                sel[w] |= low;
-                bits ^= low;
-                ++before;
-            }
-        }
-        __syncthreads();
-        cnt = 0;
-        for (int w = w0; w < w1; ++w) cnt += __popc(sel[w]);
-        uint32_t at = cta_exclusive_scan(cnt, ms->wsum, total);
-        for (int w = w0; w < w1; ++w) {
-            uint32_t bits = sel[w];
-            while (bits != 0u) {
-                const int bpos = __ffs(bits) - 1;
-                bits &= bits - 1u;
-                if (at < n_mine) orow[base + at] = p0 + w * 32 + bpos;
-                ++at;
-            }
-        }
-    } else if (!trivial) {
-        const int seg = ((np + kSaWarps - 1) / kSaWarps + 31) / 32 * 32;
-        const int s0 = p0 + warp * seg, s1 = min(p1, s0 + seg);
         uint32_t eq_seen = 0, pos = 0;
         for (int w = 0; w < warp; ++w) {
             const uint32_t tw = take > eq_seen ? min(ms->weq[w], take - eq_seen) : 0u;
@@ -504,13 +660,13 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
             const bool pick = is_gt || (is_eq && eq_seen + __popc(eqm & lt) < take);
             const uint32_t pm = __ballot_sync(0xffffffffu, pick);
             const uint32_t at = pos + __popc(pm & lt);
-            if (pick && at < n_mine) orow[base + at] = i;
+            if (pick && at < n_mine) put(at, i);
             pos += __popc(pm);
             eq_seen += __popc(eqm);
         }
     }
     cp_async_wait<0>();  // query rows
-    __syncthreads();     // this CTA's idx entries are visible to all its threads
+    __syncthreads();     // the selection list is complete (shared memory and idx)
 
     // ---- attention over this CTA's selected rows, kSaWin list rows at a time
     int32_t* src = reinterpret_cast<int32_t*>(sm + L.oSrc);
@@ -528,8 +684,8 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
     for (int w0 = 0; w0 < n_list; w0 += kSaWin) {
         const int nwin = min(kSaWin, n_list - w0);
         for (int j = tid; j < nwin; j += kSaThreads) {
-            const int jl = w0 + j;
-            const int selv = orow[base + jl / p.block];
+            const int jl = w0 + j, e = jl / p.block;
+            const int selv = e < kSaList ? lst[e] : orow[base + e];
             const int pos = selv * p.block + jl % p.block;
             int32_t code = pos;
             if (selv < 0 || selv >= N) {  // only with a histogram that does not match the scores
@@ -561,110 +717,150 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
         __syncthreads();  // src is rewritten by the next window
     }
 
-    // ---- this CTA's partial (m, l, O): O summed over the warps into ow[0]
+    // ---- this CTA's partial (m, l, O), pushed into the inbox of each query row's owner
     float* mlw = reinterpret_cast<float*>(sm + L.oML);
     float* rowv = reinterpret_cast<float*>(sm + L.oRow);
     float* ow = reinterpret_cast<float*>(sm + L.oU);
     mma_combine_warps<D, RP>(acc, mlw, rowv, ow);
-    for (int e = tid; e < p.R * (D / 4); e += kSaThreads) {
+    const int R = p.R;
+    const int own = (R + P - 1) / P;  // query rows per owner
+    // the inbox either has its own memory, or reuses H once every CTA is past its selection
+    if (!p.inbox_own) cl.sync();  // B3: every CTA has finished its selection and attention
+    float* inO = reinterpret_cast<float*>(sm + (p.inbox_own ? L.bytes : L.oH));  // [own][P][D]
+    float* inM = inO + own * P * D;                      // [own][P]
+    float* inL = inM + own * P;                          // [own][P]
+    for (int e = tid; e < R * (D / 4); e += kSaThreads) {
         const int r = e / (D / 4), col = (e % (D / 4)) * 4;
+        const int owner = r % P, lr = r / P;
         const float4 o = mma_cta_row4<D, RP>(ow, r, col);
-        *reinterpret_cast<float4*>(ow + (size_t)r * D + col) = o;
-    }
-    cl.sync();  // B4: every CTA's partial is published
-
-    // ---- merge: weights of the P partials per query row, then every P-th column group
-    float* wts = reinterpret_cast<float*>(sm + L.oW);  // [P][RP] weight / L, then [RP] lse
-    if (tid < p.R) {
-        const int r = tid;
-        float mc[kSaMaxCluster], lc[kSaMaxCluster];
-        float M = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kSaMaxCluster; ++c)
-            if (c < P) {
-                const float* rv = cl.map_shared_rank(rowv, c);
-                mc[c] = rv[r];
-                lc[c] = rv[RP + r];
-                M = fmaxf(M, mc[c]);
-            }
-        float Ls = 0.f;
-#pragma unroll
-        for (int c = 0; c < kSaMaxCluster; ++c)
-            if (c < P && M != -INFINITY && mc[c] != -INFINITY) Ls = fmaf(lc[c], exp2f(mc[c] - M), Ls);
-#pragma unroll
-        for (int c = 0; c < kSaMaxCluster; ++c)
-            if (c < P) wts[c * RP + r] = (Ls > 0.f && mc[c] != -INFINITY) ? exp2f(mc[c] - M) / Ls : 0.f;
-        if (r % P == rank) {
-            const int v = r / p.G, gg = r % p.G;
-            p.lse[((size_t)b * p.V + v) * p.Hq + kvh * p.G + gg] = Ls > 0.f ? (M + log2f(Ls)) * kLn2f : -INFINITY;
+        float* dO = cl.map_shared_rank(inO, owner);
+        *reinterpret_cast<float4*>(dO + ((size_t)lr * P + rank) * D + col) = o;
+        if (col == 0) {
+            cl.map_shared_rank(inM, owner)[lr * P + rank] = rowv[r];
+            cl.map_shared_rank(inL, owner)[lr * P + rank] = rowv[RP + r];
         }
     }
-    __syncthreads();
-    const float* rem_o[kSaMaxCluster];
-#pragma unroll
-    for (int c = 0; c < kSaMaxCluster; ++c) rem_o[c] = cl.map_shared_rank(ow, c < P ? c : 0);
-    const int items = p.R * (D / 4);
-    for (int e = rank + P * tid; e < items; e += P * kSaThreads) {
-        const int r = e / (D / 4), col = (e % (D / 4)) * 4;
-        float4 x[kSaMaxCluster];
-#pragma unroll
-        for (int c = 0; c < kSaMaxCluster; ++c)
-            if (c < P) x[c] = *reinterpret_cast<const float4*>(rem_o[c] + (size_t)r * D + col);
+    cl.sync();  // B4: every inbox is complete; no shared memory is read across CTAs after this
+
+    // ---- merge this CTA's query rows r = lr * P + rank over the P partials
+    for (int e = tid; e < own * (D / 4); e += kSaThreads) {
+        const int lr = e / (D / 4), col = (e % (D / 4)) * 4;
+        const int r = lr * P + rank;
+        if (r >= R) continue;
+        float M = -INFINITY;
+        for (int s = 0; s < P; ++s) M = fmaxf(M, inM[lr * P + s]);
+        float Ls = 0.f;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < kSaMaxCluster; ++c)
-            if (c < P) {
-                const float wgt = wts[c * RP + r];
-                o.x = fmaf(wgt, x[c].x, o.x);
-                o.y = fmaf(wgt, x[c].y, o.y);
-                o.z = fmaf(wgt, x[c].z, o.z);
-                o.w = fmaf(wgt, x[c].w, o.w);
-            }
+        for (int s = 0; s < P; ++s) {
+            const float ms_ = inM[lr * P + s];
+            if (M == -INFINITY || ms_ == -INFINITY) continue;
+            const float wgt = exp2f(ms_ - M);
+            Ls = fmaf(inL[lr * P + s], wgt, Ls);
+            const float4 x = *reinterpret_cast<const float4*>(inO + ((size_t)lr * P + s) * D + col);
+            o.x = fmaf(wgt, x.x, o.x);
+            o.y = fmaf(wgt, x.y, o.y);
+            o.z = fmaf(wgt, x.z, o.z);
+            o.w = fmaf(wgt, x.w, o.w);
+        }
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
         const int v = r / p.G, gg = r % p.G;
         const size_t qrow = ((size_t)b * p.V + v) * p.Hq + kvh * p.G + gg;
-        *reinterpret_cast<float4*>(p.out + qrow * D + col) = o;
+        *reinterpret_cast<float4*>(p.out + qrow * D + col) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+        if (col == 0) p.lse[qrow] = Ls > 0.f ? (M + log2f(Ls)) * kLn2f : -INFINITY;
     }
-    cl.sync();  // B5: no CTA leaves while another may still read its shared memory
 }
 
 struct SaPlan {
     int P, part, staged, RP, smem;
 };
 
-// Cluster size and part length: enough CTAs to fill the GPU (two per SM at these shared
-// memory sizes), at most 8 per cluster, at least 256 scores per part.
-SaPlan plan_select_attend(int rows, int N, int D, int R, int requested, bool scores_aligned) {
+SaPlan plan_for(int N, int D, int RP, int P, bool scores_aligned) {
     SaPlan pl{};
-    pl.RP = R <= 16 ? 16 : 32;
-    int P;
-    if (requested > 0) {
-        P = requested;
-    } else {
-        const int slots = num_sms() * 2;
-        P = rows > 0 ? slots / rows : 1;
-    }
+    pl.RP = RP;
     P = std::max(1, std::min(P, kSaMaxCluster));
     P = std::min(P, std::max(1, (N + 255) / 256));
     int part = (N + P - 1) / P;
     part = std::max(kSaPartAlign, (part + kSaPartAlign - 1) / kSaPartAlign * kSaPartAlign);
     pl.P = std::max(1, (N + part - 1) / part);
     pl.part = part;
-    const int row_b = D * 2 + 16;
-    const int stages = kMmaWarps * kWStages * 2 * kSub * row_b;
+    const int stages = kMmaWarps * kWStages * 2 * kSub * (D * 2 + 16);
     pl.staged = (scores_aligned && N % 4 == 0 && part * 4 <= stages) ? 1 : 0;
-    pl.smem = sa_layout(D, pl.RP, part, pl.staged).bytes;
+    pl.smem = sa_layout(D, RP, part, pl.staged).bytes;
     return pl;
 }
 
+// Clusters of `P` CTAs with `smem` bytes each that the current device runs at once
+// (queried once per device and shape, then cached).
 template <int D, int RP>
-sd_status launch_select_attend(const SelAttParams& p, const SaPlan& pl, cudaStream_t st) {
+int max_active_clusters(int P, int smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, P, smem);
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
     auto kern = select_attend_kernel<D, RP>;
-    SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem),
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(P, 1, 1);
+        cfg.blockDim = dim3(kSaThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = P;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    std::lock_guard<std::mutex> g(mu);
+    cache[key] = n;
+    return n;
+}
+
+// Cluster size: the caller's, or the largest P <= 8 (parts of at least 256 scores) whose
+// rows * P CTAs all run at once on this GPU with room to spare; P = 1 when even single
+// CTAs need several waves.
+template <int D, int RP>
+SaPlan plan_select_attend(int rows, int N, int requested, bool scores_aligned) {
+    if (requested > 0) return plan_for(N, D, RP, requested, scores_aligned);
+    for (int P = kSaMaxCluster; P > 1; --P) {
+        const SaPlan pl = plan_for(N, D, RP, P, scores_aligned);
+        if (pl.P != P) continue;  // N too short for P parts
+        // keep a tenth of the clusters' room free: a programmatic launch places clusters while
+        // the preceding kernel still holds SMs, and a full GPU would leave one for a second wave
+        if (rows * 10 <= max_active_clusters<D, RP>(P, pl.smem) * 9) return pl;
+    }
+    return plan_for(N, D, RP, 1, scores_aligned);
+}
+
+template <int D, int RP>
+sd_status launch_select_attend(SelAttParams p, int rows, int requested, bool scores_aligned, cudaStream_t st) {
+    const SaPlan pl = plan_select_attend<D, RP>(rows, p.N, requested, scores_aligned);
+    if (sa_inbox_bytes(D, p.R, pl.P) > kSaHBytes) {
+        set_error("sd_select_attend: merge inbox does not fit (R=%d, P=%d)", p.R, pl.P);
+        return SD_ERR_UNSUPPORTED;
+    }
+    p.part = pl.part;
+    p.staged = pl.staged;
+    // a separate inbox saves a cluster barrier when two CTAs per SM still fit
+    const int inbox = sa_inbox_bytes(D, p.R, pl.P);
+    p.inbox_own = pl.smem + inbox <= kSaTwoPerSm ? 1 : 0;
+    const int smem = pl.smem + (p.inbox_own ? inbox : 0);
+    auto kern = select_attend_kernel<D, RP>;
+    SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                   "sd_select_attend: cudaFuncSetAttribute");
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(pl.P, p.Hkv, p.B);
     cfg.blockDim = dim3(kSaThreads);
-    cfg.dynamicSmemBytes = pl.smem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -759,11 +955,12 @@ extern "C" sd_status sd_select_attend(const float* scores, int N, uint32_t* key_
         SD_REQUIRE(aligned16(a->k_cache) && aligned16(a->v_cache),
                    "sd_select_attend: k_cache/v_cache must be 16-byte aligned");
     }
-    const SaPlan pl = plan_select_attend(a->B * a->Hkv, N, a->d, R, a->splits, aligned16(scores));
-    p.part = pl.part;
-    p.staged = pl.staged;
+    const int rows = a->B * a->Hkv;
+    const bool al = aligned16(scores);
     cudaStream_t st = as_stream(stream);
     if (a->d == 128)
-        return pl.RP == 16 ? launch_select_attend<128, 16>(p, pl, st) : launch_select_attend<128, 32>(p, pl, st);
-    return pl.RP == 16 ? launch_select_attend<64, 16>(p, pl, st) : launch_select_attend<64, 32>(p, pl, st);
+        return R <= 16 ? launch_select_attend<128, 16>(p, rows, a->splits, al, st)
+                       : launch_select_attend<128, 32>(p, rows, a->splits, al, st);
+    return R <= 16 ? launch_select_attend<64, 16>(p, rows, a->splits, al, st)
+                   : launch_select_attend<64, 32>(p, rows, a->splits, al, st);
 }
