@@ -6,13 +6,13 @@
 // decode attention over an irregular per-token selection; Adaptive DHiSparse (news page),
 // "Metodologia": every query row of a group shares each fetched row.
 //
-// A CTA of 4 warps owns a list of `nrows` K/V rows.  The list is cut into 16-row
-// sub-chunks dealt round-robin to the warps; each warp runs its own 2-deep cp.async
+// A CTA of NW warps owns a list of `nrows` K/V rows.  The list is cut into 16-row
+// sub-chunks dealt round-robin to the warps; each warp runs its own NS-deep cp.async
 // pipeline (8 lanes move one 128-byte line of a row, 4 rows per instruction) and
 // its own online softmax in base 2 over all RP query rows: S[16q x 8k] tiles from Q and K
 // through ldmatrix, P split into bf16 hi + lo parts so the PV product keeps ~16
 // significant bits, V fragments through ldmatrix.trans.  mma_combine_warps then merges
-// the 4 warps' (m, l, O) in shared memory.
+// the NW warps' (m, l, O) in shared memory.
 #pragma once
 
 #include <stdint.h>
@@ -21,19 +21,32 @@
 
 namespace sd {
 
-constexpr int kMmaWarps = 4;          // warps of a CTA that run the attention loop
+constexpr int kMmaWarps = 4;          // warps of a CTA that run the attention loop (default)
 constexpr int kSub = 16;              // rows per warp sub-chunk
-constexpr int kWStages = 2;           // sub-chunks in flight per warp
+constexpr int kWStages = 2;           // sub-chunks in flight per warp (default)
 constexpr int32_t kNoRow = INT32_MIN;  // source code of a skipped row (contributes nothing)
 constexpr float kLn2f = 0.69314718055994530942f;
 
-template <int D>
+template <int D, int NW = kMmaWarps, int NS = kWStages>
 struct MmaRows {
     static constexpr int kRowB = D * 2 + 16;         // padded bf16 row: conflict-free ldmatrix
     static constexpr int kStage = 2 * kSub * kRowB;  // K rows then V rows
-    static constexpr int kWarpBytes = kWStages * kStage;
-    static constexpr int kStagesBytes = kMmaWarps * kWarpBytes;
+    static constexpr int kWarpBytes = NS * kStage;
+    static constexpr int kStagesBytes = NW * kWarpBytes;
 };
+
+// cp.async.wait_group with a run-time count below NS (the instruction takes an immediate).
+template <int NS>
+SD_DEVINL void cp_async_wait_dyn(int n) {
+    if constexpr (NS > 3) {
+        if (n >= 3) { cp_async_wait<3>(); return; }
+    }
+    if constexpr (NS > 2) {
+        if (n == 2) { cp_async_wait<2>(); return; }
+    }
+    if (n >= 1) cp_async_wait<1>();
+    else cp_async_wait<0>();
+}
 
 // Where a row's bytes are: code >= 0 is row `code` of the device pool (k_pool + code * row
 // bytes, already offset to this (b, kvh)); code < 0 is host row -1 - code of the mapped
@@ -69,22 +82,23 @@ struct WarpAcc {
 // beyond the real ones zero).  row_code(j) returns the source of list row j (kNoRow for a
 // skipped row; called only for j < nrows).  logit(r, j, x) receives every (query row,
 // list row) score in base-2 units (x * ln 2 is the natural logit) of valid rows.
-template <int D, int RP, class RowCode, class Logit>
+template <int D, int RP, int NW = kMmaWarps, int NS = kWStages, class RowCode, class Logit>
 SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_base, int warp, int nrows,
                                const RowSource& rs, float scale_log2, RowCode row_code, Logit logit) {
-    using L = MmaRows<D>;
+    static_assert(NS >= 2 && NS <= 4, "2 to 4 stages per warp");
+    using L = MmaRows<D, NW, NS>;
     constexpr int MT = RP / 16, KS = D / 16, NT = D / 8;
     constexpr int PPR = D * 2 / 16;  // 16-byte pieces per row
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
     auto code_of = [&](int j) -> int32_t { return j < nrows ? row_code(j) : kNoRow; };
     const int nsub = (nrows + kSub - 1) / kSub;
-    const int my_n = warp < nsub ? (nsub - warp + kMmaWarps - 1) / kMmaWarps : 0;
+    const int my_n = warp < nsub ? (nsub - warp + NW - 1) / NW : 0;
 
     // Lanes 8q..8q+7 move one 128-byte line of a row per instruction (4 rows at a time), so
     // every request is a whole line, in HBM and over the host link alike.
     auto issue = [&](int ci, int st) {
-        const int c = warp + kMmaWarps * ci;
+        const int c = warp + NW * ci;
         uint8_t* kst = stages + st * L::kStage;
         const int sub = lane >> 3, piece = lane & 7;
         int32_t code[kSub / 4];
@@ -111,17 +125,14 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
     };
 
     int issued = 0;
-    for (; issued < min(kWStages, my_n); ++issued) issue(issued, issued);
+    for (; issued < min(NS, my_n); ++issued) issue(issued, issued);
     for (int ci = 0; ci < my_n; ++ci) {
-        const int st = ci % kWStages;
-        if (ci + 1 < issued)
-            cp_async_wait<1>();
-        else
-            cp_async_wait<0>();
+        const int st = ci % NS;
+        cp_async_wait_dyn<NS>(issued - ci - 1);  // chunk ci has landed; later ones may still fly
         __syncwarp();
         const uint32_t k_base = smem_addr(stages + st * L::kStage);
         const uint32_t v_base = k_base + kSub * L::kRowB;
-        const int c = warp + kMmaWarps * ci;
+        const int c = warp + NW * ci;
 
         // ---- S = Q K^T for this warp's 16 rows: [MT][2 n-tiles][4]
         float sacc[MT][2][4];
@@ -223,19 +234,20 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
             }
         }
         __syncwarp();
-        if (ci + kWStages < my_n) {
-            issue(ci + kWStages, st);
+        if (ci + NS < my_n) {
+            issue(ci + NS, st);
             ++issued;
         }
     }
 }
 
-// Combines the 4 warps' (m, l, O) of a CTA; called by all 128 threads after every warp's
-// loop.  Scratch: mlw [2*4*RP] floats, rowv [6*RP] floats, ow [4][RP][D] floats (the
-// warps' stage area may be reused: the call starts with a barrier).  Leaves rowM = rowv[0,
-// RP) (the CTA's row maxima), rowL = rowv[RP, 2RP) (sums of l rescaled to them) and ow[w][r]
-// = warp w's O row r rescaled to rowM[r]; the CTA's unnormalised O row is the sum over w.
-template <int D, int RP>
+// Combines the NW warps' (m, l, O) of a CTA; called by all NW*32 threads after every
+// warp's loop.  Scratch: mlw [2*NW*RP] floats, rowv [(2+NW)*RP] floats, ow [NW][RP][D]
+// floats (the warps' stage area may be reused: the call starts with a barrier).  Leaves
+// rowM = rowv[0, RP) (the CTA's row maxima), rowL = rowv[RP, 2RP) (sums of l rescaled to
+// them) and ow[w][r] = warp w's O row r rescaled to rowM[r]; the CTA's unnormalised O row is
+// the sum over w.
+template <int D, int RP, int NW = kMmaWarps>
 SD_DEVINL void mma_combine_warps(const WarpAcc<D, RP>& acc, float* mlw, float* rowv, float* ow) {
     constexpr int MT = RP / 16, NT = D / 8;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -247,25 +259,25 @@ SD_DEVINL void mma_combine_warps(const WarpAcc<D, RP>& acc, float* mlw, float* r
             for (int hf = 0; hf < 2; ++hf) {
                 const int r = mt * 16 + g + 8 * hf;
                 mlw[warp * RP + r] = acc.m[mt][hf];
-                mlw[kMmaWarps * RP + warp * RP + r] = acc.l[mt][hf];
+                mlw[NW * RP + warp * RP + r] = acc.l[mt][hf];
             }
     }
     __syncthreads();  // every warp is done with its stages: they may hold the warps' O now
     float* rowM = rowv;
     float* rowL = rowv + RP;
-    float* fac = rowv + 2 * RP;  // [4][RP]
+    float* fac = rowv + 2 * RP;  // [NW][RP]
     if (tid < RP) {
         const int r = tid;
         float M = mlw[r];
 #pragma unroll
-        for (int w = 1; w < kMmaWarps; ++w) M = fmaxf(M, mlw[w * RP + r]);
+        for (int w = 1; w < NW; ++w) M = fmaxf(M, mlw[w * RP + r]);
         float Ls = 0.f;
 #pragma unroll
-        for (int w = 0; w < kMmaWarps; ++w) {
+        for (int w = 0; w < NW; ++w) {
             const float mw = mlw[w * RP + r];
             const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
             fac[w * RP + r] = f;
-            Ls = fmaf(mlw[kMmaWarps * RP + w * RP + r], f, Ls);
+            Ls = fmaf(mlw[NW * RP + w * RP + r], f, Ls);
         }
         rowM[r] = M;
         rowL[r] = Ls;
@@ -286,12 +298,12 @@ SD_DEVINL void mma_combine_warps(const WarpAcc<D, RP>& acc, float* mlw, float* r
     __syncthreads();
 }
 
-// The CTA's unnormalised O columns [col, col + 4) of row r: the sum of the 4 warps' parts.
-template <int D, int RP>
+// The CTA's unnormalised O columns [col, col + 4) of row r: the sum of the NW warps' parts.
+template <int D, int RP, int NW = kMmaWarps>
 SD_DEVINL float4 mma_cta_row4(const float* ow, int r, int col) {
     float4 o = *reinterpret_cast<const float4*>(ow + (size_t)r * D + col);
 #pragma unroll
-    for (int w = 1; w < kMmaWarps; ++w) {
+    for (int w = 1; w < NW; ++w) {
         const float4 x = *reinterpret_cast<const float4*>(ow + ((size_t)w * RP + r) * D + col);
         o.x += x.x;
         o.y += x.y;

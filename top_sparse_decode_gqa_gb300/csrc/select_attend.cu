@@ -16,10 +16,12 @@
 //   1. the row's top digit d0 (11 bits of the order key) comes from the indexer's
 //      histogram; one pass over the part marks every score above d0's bin in a bitmap
 //      (float compares against the bin's bounds) and keeps the bin's scores as candidates;
-//      their next digit is added into every CTA's histogram (barrier B1);
-//   2. every CTA picks the same digit d1; candidates above it join the bitmap, and those in
-//      the final 21-bit bin are pushed with their positions to every CTA, together with the
-//      part's count of scores above that bin (barrier B2);
+//      each CTA histograms their next digit and pushes 64 coarse sums of it to every CTA
+//      (barrier B1);
+//   2. every CTA picks the same coarse group, then reads that group's 32 fine bins from
+//      the cluster and picks the same digit d1; candidates above it join the bitmap, and
+//      those in the final 21-bit bin are pushed with their positions to every CTA,
+//      together with the part's count of scores above that bin (barrier B2);
 //   3. locally, every CTA finds the threshold key among the final-bin entries, every
 //      part's counts above / equal to it, its own ties (lowest indices first) and its
 //      offset in the row's ascending output, and writes its selected indices there;
@@ -76,8 +78,8 @@ struct SelAttParams {
 //   Q    the RP query rows (bf16, padded rows)
 //   U    the warps' K/V stages; before them, the part's scores when they are staged
 //   H    hist0 (top digit; after B1 the row's final-bin entries pushed by the cluster),
-//        hist1 (the cluster's sum of digit 1), hist2 (digit 2 of the final bin); the merge
-//        inbox when it has no memory of its own (after barrier B3)
+//        hist1 (this part's digit 1), hist2 (the cluster's coarse digit-1 sums, then digit 2
+//        of the final bin); the merge inbox when it has no memory of its own (after B3)
 //   S    sel and tie bitmaps of the part
 //   C    phase A: the candidates' keys and indices; phase B: row sources, warp and
 //        row statistics
@@ -91,6 +93,7 @@ constexpr int kSaCand = 1024;  // candidates a CTA keeps
 constexpr int kSaList = 512;   // selected entries a CTA keeps in shared memory
 constexpr int kSaFb = 1024;    // final-bin entries of a row (keys + positions in hist0's 8 KB)
 constexpr int kSaHBytes = (2 * kSaHist + kSaHist / 2) * 4;
+constexpr int kSaCoarse = 64;  // coarse groups of the digit-1 histogram exchanged by pushes
 constexpr int kSaTwoPerSm = 233472 / 2 - 1024;  // dynamic shared memory of one of two CTAs per SM
 
 __host__ __device__ constexpr int sa_align(int x, int a) { return (x + a - 1) / a * a; }
@@ -160,6 +163,16 @@ SD_DEVINL uint32_t cta_inclusive_scan(uint32_t v, uint32_t* wsum) {
     return v + off;
 }
 
+SD_DEVINL uint32_t warp_inclusive_scan(uint32_t v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
 // Block-wide exclusive prefix sum; also returns the total.
 SD_DEVINL uint32_t cta_exclusive_scan(uint32_t v, SaMisc* ms, uint32_t& total) {
     const uint32_t incl = cta_inclusive_scan(v, ms->wsum);
@@ -224,17 +237,60 @@ SD_DEVINL void cluster_sum_hist(cg::cluster_group& cl, const uint32_t* src, uint
     }
 }
 
-// Adds `v` to bin `bin` of the array `h` (same shared-memory offset) of every CTA of the
-// cluster, this one included.
-SD_DEVINL void cluster_add(cg::cluster_group& cl, uint32_t* h, uint32_t bin, uint32_t v, int P) {
-    for (int c = 0; c < P; ++c) atomicAdd(cl.map_shared_rank(h, c) + bin, v);
-}
-
 // The float whose order key is k (the inverse of float_key); k = 0x7FFFFFFF, the key no
 // float maps to (-0 takes the key of +0), gives the largest float below it, -denorm_min.
 SD_DEVINL float key_float(uint32_t k) {
     if (k == 0x7FFFFFFFu) return __uint_as_float(0x80000001u);
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// One pass over the part [p0, p1): sel word w = the entries of 32-score group w above the
+// d0 bin, tie word w = those in it.  Lanes 0..U-1 store the U groups a warp just scanned, so
+// nothing diverges; the staging and compare modes are compile-time, so the U loads and
+// compares of a round interleave.
+template <bool STAGED, bool FCMP>
+SD_DEVINL void sa_scan(const uint32_t* keys_s, const float* srow, int p0, int p1, int nw, uint32_t d0, float f_lo,
+                       float f_hi, uint32_t k_hi, uint32_t* sel, uint32_t* tie) {
+    constexpr int U = 8;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int g0 = warp; g0 < nw; g0 += U * kSaWarps) {
+        float f[U];
+        uint32_t sure[U], cm[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = p0 + (g0 + u * kSaWarps) * 32 + lane;
+            if constexpr (STAGED)
+                f[u] = i < p1 ? __uint_as_float(keys_s[i - p0]) : 0.f;
+            else
+                f[u] = i < p1 ? __ldcg(srow + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const bool valid = p0 + (g0 + u * kSaWarps) * 32 + lane < p1;  // also false past nw
+            bool above, in;
+            if constexpr (FCMP) {
+                above = f[u] > f_hi;
+                in = f[u] >= f_lo && f[u] <= f_hi;
+            } else {
+                const uint32_t kk = float_key(f[u]);
+                above = kk > k_hi;
+                in = (kk >> 21) == d0;
+            }
+            sure[u] = __ballot_sync(0xffffffffu, valid && above);
+            cm[u] = __ballot_sync(0xffffffffu, valid && in);
+        }
+        uint32_t my_s = 0, my_c = 0;  // lane u keeps group u's words
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            my_s = lane == u ? sure[u] : my_s;
+            my_c = lane == u ? cm[u] : my_c;
+        }
+        const int gw = g0 + lane * kSaWarps;
+        if (lane < U && gw < nw) {
+            sel[gw] = my_s;
+            tie[gw] = my_c;
+        }
+    }
 }
 
 template <int D, int RP>
@@ -250,6 +306,7 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
     uint32_t* hist0 = reinterpret_cast<uint32_t*>(sm + L.oHist0);
     uint32_t* hist1 = reinterpret_cast<uint32_t*>(sm + L.oHist1);
     uint32_t* hist2 = reinterpret_cast<uint32_t*>(sm + L.oHist2);
+    uint32_t* coarse = hist2;  // [P][kSaCoarse] coarse digit-1 sums pushed by the cluster, until B2
     uint32_t* sel = reinterpret_cast<uint32_t*>(sm + L.oSel);
     uint32_t* tie = reinterpret_cast<uint32_t*>(sm + L.oTie);
     uint32_t* cand_k = reinterpret_cast<uint32_t*>(sm + L.oCandK);
@@ -307,6 +364,13 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
     if (hrow != nullptr && !trivial)
         for (int i = tid; i < kSaHist / 4; i += kSaThreads)
             reinterpret_cast<uint4*>(hist0)[i] = __ldcg(reinterpret_cast<const uint4*>(hrow) + i);
+    // the top digit first when the indexer's histogram is given: it overlaps the staging
+    uint32_t d0 = 0, above0 = 0;
+    if (!trivial && hrow != nullptr) {
+        __syncthreads();
+        cta_select_digit(hist0, kSaHist, (uint32_t)k, ms, d0, above0);
+        d0 &= kSaHist - 1;
+    }
     if (staged) {
         const bool ok = mbar_wait(&ms->bar, 0);
         if (__syncthreads_or(!ok)) {  // keep going on the global copy; the result is flagged
@@ -318,24 +382,19 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
         return float_key(staged ? __uint_as_float(keys_s[i - p0]) : __ldcg(srow + i));
     };
 
-    // ---- the top digit: from the indexer's histogram, or counted here and summed
-    uint32_t d0 = 0, above0 = 0;
-    if (!trivial) {
-        const uint32_t* top = hist0;
-        if (hrow == nullptr) {
-            for (int base = p0 + warp * 32; base < p1; base += kSaThreads) {
-                const int i = base + lane;
-                const bool valid = i < p1;
-                const uint32_t dg = valid ? key_at(i) >> 21 : 0xffffffffu;
-                const uint32_t peers = __match_any_sync(0xffffffffu, dg);
-                if (valid && lane == __ffs(peers) - 1) atomicAdd(&hist0[dg], (uint32_t)__popc(peers));
-            }
-            cl.sync();  // every CTA's top-digit counts are complete (and are not changed again)
-            cluster_sum_hist(cl, hist0, cand_k, kSaHist, P);  // the candidate area is free until the pass
-            top = cand_k;
+    // ---- otherwise the top digit is counted here and summed over the cluster
+    if (!trivial && hrow == nullptr) {
+        for (int base = p0 + warp * 32; base < p1; base += kSaThreads) {
+            const int i = base + lane;
+            const bool valid = i < p1;
+            const uint32_t dg = valid ? key_at(i) >> 21 : 0xffffffffu;
+            const uint32_t peers = __match_any_sync(0xffffffffu, dg);
+            if (valid && lane == __ffs(peers) - 1) atomicAdd(&hist0[dg], (uint32_t)__popc(peers));
         }
+        cl.sync();  // every CTA's top-digit counts are complete (and are not changed again)
+        cluster_sum_hist(cl, hist0, cand_k, kSaHist, P);  // the candidate area is free until the pass
         __syncthreads();
-        cta_select_digit(top, kSaHist, (uint32_t)k, ms, d0, above0);
+        cta_select_digit(cand_k, kSaHist, (uint32_t)k, ms, d0, above0);
         d0 &= kSaHist - 1;
     }
     uint32_t krem = (uint32_t)k - above0;
@@ -345,47 +404,18 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
     // candidates, in tie for now), written by lanes 0..U-1 without divergence; then the
     // candidates are listed with one scan and their next digit is added to every CTA's hist1
     if (!trivial) {
-        constexpr int U = 8;
         // the d0 bin as the closed float interval [f_lo, f_hi]: a score lies above the bin iff
         // f > f_hi and in it iff f_lo <= f <= f_hi (-0 and +0 compare equal, as their order
         // keys do); the bins next to the infinities and NaN keys compare keys instead
         const uint32_t k_lo = d0 << 21, k_hi = k_lo | 0x1FFFFFu;
         const bool fcmp = d0 > 0x003u && d0 < 0x7FCu;
         const float f_lo = key_float(k_lo), f_hi = key_float(k_hi);
-        for (int g0 = warp; g0 < nw; g0 += U * kSaWarps) {
-            float f[U];
-            uint32_t sure[U], cm[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int i = p0 + (g0 + u * kSaWarps) * 32 + lane;
-                f[u] = i < p1 ? (staged ? __uint_as_float(keys_s[i - p0]) : __ldcg(srow + i)) : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const bool valid = p0 + (g0 + u * kSaWarps) * 32 + lane < p1;  // also false past nw
-                bool above, in;
-                if (fcmp) {
-                    above = f[u] > f_hi;
-                    in = f[u] >= f_lo && f[u] <= f_hi;
-                } else {
-                    const uint32_t kk = float_key(f[u]);
-                    above = kk > k_hi;
-                    in = (kk >> 21) == d0;
-                }
-                sure[u] = __ballot_sync(0xffffffffu, valid && above);
-                cm[u] = __ballot_sync(0xffffffffu, valid && in);
-            }
-            uint32_t my_s = 0, my_c = 0;  // lane u keeps group u's words
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                my_s = lane == u ? sure[u] : my_s;
-                my_c = lane == u ? cm[u] : my_c;
-            }
-            const int gw = g0 + lane * kSaWarps;
-            if (lane < U && gw < nw) {
-                sel[gw] = my_s;
-                tie[gw] = my_c;
-            }
+        if (staged) {
+            if (fcmp) sa_scan<true, true>(keys_s, srow, p0, p1, nw, d0, f_lo, f_hi, k_hi, sel, tie);
+            else sa_scan<true, false>(keys_s, srow, p0, p1, nw, d0, f_lo, f_hi, k_hi, sel, tie);
+        } else {
+            if (fcmp) sa_scan<false, true>(keys_s, srow, p0, p1, nw, d0, f_lo, f_hi, k_hi, sel, tie);
+            else sa_scan<false, false>(keys_s, srow, p0, p1, nw, d0, f_lo, f_hi, k_hi, sel, tie);
         }
         __syncthreads();
         // list the candidates: thread t owns words [t*W, t*W + W)
@@ -409,9 +439,9 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
         }
         if (tid == 0) ms->ncand = n_cand;
         __syncthreads();
+        // the next digit of the candidates into this CTA's hist1
         if (n_cand <= (uint32_t)kSaCand) {
-            for (uint32_t c = tid; c < n_cand; c += kSaThreads)
-                cluster_add(cl, hist1, (cand_k[c] >> 10) & (kSaHist - 1), 1u, P);
+            for (uint32_t c = tid; c < n_cand; c += kSaThreads) atomicAdd(&hist1[(cand_k[c] >> 10) & (kSaHist - 1)], 1u);
         } else {
             // more candidates than the list holds: count their next digit over the keys
             for (int base0 = p0 + warp * 32; base0 < p1; base0 += kSaThreads) {
@@ -421,13 +451,21 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
                 const bool in = valid && (kk >> 21) == d0;
                 const uint32_t bin = (kk >> 10) & (kSaHist - 1);
                 const uint32_t peers = __match_any_sync(0xffffffffu, in ? bin : 0xffffffffu);
-                if (in && lane == __ffs(peers) - 1) cluster_add(cl, hist1, bin, (uint32_t)__popc(peers), P);
+                if (in && lane == __ffs(peers) - 1) atomicAdd(&hist1[bin], (uint32_t)__popc(peers));
             }
             if (tid == 0)
                 for (int c = 0; c < P; ++c) atomicOr(cl.map_shared_rank(&ms->ovf, c), 1u);
         }
+        // 64 coarse sums of 32 bins each, pushed to every CTA (the fine bins stay here)
+        __syncthreads();
+        for (int g = tid; g < kSaCoarse; g += kSaThreads) {
+            uint32_t sum = 0;
+#pragma unroll 8
+            for (int j = 0; j < kSaHist / kSaCoarse; ++j) sum += hist1[g * (kSaHist / kSaCoarse) + j];
+            for (int c = 0; c < P; ++c) cl.map_shared_rank(coarse, c)[rank * kSaCoarse + g] = sum;
+        }
     }
-    cl.sync();  // B1: hist1 and ovf complete in every CTA; every CTA has read key_hist
+    cl.sync();  // B1: coarse sums and ovf pushed, every hist1 complete; every CTA has read key_hist
     if (hrow != nullptr && rank == 0)
         for (int i = tid; i < kSaHist / 4; i += kSaThreads) reinterpret_cast<uint4*>(hrow)[i] = make_uint4(0u, 0u, 0u, 0u);
     // candidate c of the per-warp lists, or false past a warp's count
@@ -441,9 +479,46 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
     // of entries above the final bin
     uint32_t pre21 = 0;
     if (!trivial && !fallback) {
-        uint32_t d1, ab1;
-        cta_select_digit(hist1, kSaHist, krem, ms, d1, ab1);
-        d1 &= kSaHist - 1;
+        // the coarse group holding the krem-th largest, then its 32 fine bins summed over the
+        // cluster (one round of remote reads)
+        uint32_t* ctot = reinterpret_cast<uint32_t*>(lst);  // lst is free until the final-bin list
+        if (tid < kSaCoarse) {
+            uint32_t t = 0;
+            for (int c = 0; c < P; ++c) t += coarse[c * kSaCoarse + tid];
+            ctot[tid] = t;
+        }
+        if (tid == 0) {
+            ms->sel_digit = 0;
+            ms->sel_above = 0;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const uint32_t ga = ctot[kSaCoarse - 1 - 2 * lane], gb = ctot[kSaCoarse - 2 - 2 * lane];
+            const uint32_t incl = warp_inclusive_scan(ga + gb), excl = incl - ga - gb;
+            const uint32_t cross = __ballot_sync(0xffffffffu, excl < krem && krem <= incl);
+            if (cross != 0u) {
+                const int src = __ffs(cross) - 1;
+                uint32_t G = 0, aboveG = 0;
+                if (lane == src) {
+                    const bool first = excl + ga >= krem;
+                    G = (uint32_t)(kSaCoarse - 1 - 2 * lane - (first ? 0 : 1));
+                    aboveG = first ? excl : excl + ga;
+                }
+                G = __shfl_sync(0xffffffffu, G, src);
+                aboveG = __shfl_sync(0xffffffffu, aboveG, src);
+                const uint32_t bin = G * (kSaHist / kSaCoarse) + 31u - (uint32_t)lane;  // from the top
+                uint32_t f = 0;
+                for (int c = 0; c < P; ++c) f += cl.map_shared_rank(hist1, c)[bin];
+                const uint32_t fi = warp_inclusive_scan(f) + aboveG, fe = fi - f;
+                const uint32_t fc = __ballot_sync(0xffffffffu, fe < krem && krem <= fi);
+                if (fc != 0u && lane == __ffs(fc) - 1) {
+                    ms->sel_digit = bin;
+                    ms->sel_above = fe;
+                }
+            }
+        }
+        __syncthreads();
+        const uint32_t d1 = ms->sel_digit & (kSaHist - 1), ab1 = ms->sel_above;
         krem -= ab1;
         pre21 = (d0 << 11) | d1;
         for (uint32_t c = tid; c < n_cand; c += kSaThreads) {
