@@ -44,6 +44,11 @@
 
 namespace cg = cooperative_groups;
 
+// Most of this kernel's code runs once per launch, so its time goes to fetching instructions
+// into a cold cache.  Helpers called more than once, and paths that normally do not run, are
+// kept out of line: repeated calls then hit a warm cache and the common path stays compact.
+#define SD_DEVNOINL __device__ __noinline__
+
 namespace sd {
 namespace {
 
@@ -174,7 +179,7 @@ SD_DEVINL uint32_t warp_inclusive_scan(uint32_t v) {
 }
 
 // Block-wide exclusive prefix sum; also returns the total.
-SD_DEVINL uint32_t cta_exclusive_scan(uint32_t v, SaMisc* ms, uint32_t& total) {
+SD_DEVNOINL uint32_t cta_exclusive_scan(uint32_t v, SaMisc* ms, uint32_t& total) {
     const uint32_t incl = cta_inclusive_scan(v, ms->wsum);
     if ((int)threadIdx.x == kSaThreads - 1) ms->tot = incl;
     __syncthreads();
@@ -187,7 +192,7 @@ SD_DEVINL uint32_t cta_exclusive_scan(uint32_t v, SaMisc* ms, uint32_t& total) {
 // still in the running, the digit holding the krem-th largest and how many entries lie in
 // higher bins.  Thread t owns bins [nb - per*(t+1), nb - per*t).  If no bin crosses (a
 // histogram that does not match the scores) the answer is digit 0, 0 above.
-SD_DEVINL void cta_select_digit(const uint32_t* hist, int nb, uint32_t krem, SaMisc* ms, uint32_t& digit,
+SD_DEVNOINL void cta_select_digit(const uint32_t* hist, int nb, uint32_t krem, SaMisc* ms, uint32_t& digit,
                                 uint32_t& above) {
     const int tid = threadIdx.x;
     if (tid == 0) {
@@ -218,7 +223,7 @@ SD_DEVINL void cta_select_digit(const uint32_t* hist, int nb, uint32_t krem, SaM
 }
 
 // dst[i] = sum over the cluster's P CTAs of their copy of src[i], i < n (n a multiple of 4).
-SD_DEVINL void cluster_sum_hist(cg::cluster_group& cl, const uint32_t* src, uint32_t* dst, int n, int P) {
+SD_DEVNOINL void cluster_sum_hist(cg::cluster_group& cl, const uint32_t* src, uint32_t* dst, int n, int P) {
     for (int i = threadIdx.x; i < n / 4; i += kSaThreads) {
         uint4 x[kSaMaxCluster];
 #pragma unroll
@@ -249,7 +254,7 @@ SD_DEVINL float key_float(uint32_t k) {
 // nothing diverges; the staging and compare modes are compile-time, so the U loads and
 // compares of a round interleave.
 template <bool STAGED, bool FCMP>
-SD_DEVINL void sa_scan(const uint32_t* keys_s, const float* srow, int p0, int p1, int nw, uint32_t d0, float f_lo,
+SD_DEVNOINL void sa_scan(const uint32_t* keys_s, const float* srow, int p0, int p1, int nw, uint32_t d0, float f_lo,
                        float f_hi, uint32_t k_hi, uint32_t* sel, uint32_t* tie) {
     constexpr int U = 8;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -290,6 +295,110 @@ SD_DEVINL void sa_scan(const uint32_t* keys_s, const float* srow, int p0, int p1
             sel[gw] = my_s;
             tie[gw] = my_c;
         }
+    }
+}
+
+// Heavy ties (a candidate list or the final bin overflowed): the threshold key over the
+// whole row from global memory, starting from the top digit d0 with krem0 entries still
+// needed, and every part's counts above / equal to it (ms->cgt, ms->ceq).  No exchange with
+// the other CTAs.  Returns the threshold; *krem_out = entries equal to it still needed.
+SD_DEVNOINL uint32_t sa_fallback_threshold(const float* srow, int N, int part, int P, uint32_t d0, uint32_t krem0,
+                                           uint32_t* hist, SaMisc* ms, uint32_t& krem_out) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t prefix = d0 << 21, pmask = 0x7FFu << 21, krem = krem0;
+#pragma unroll 1
+    for (int pass = 1; pass < 3; ++pass) {
+        const int shift = pass == 1 ? 10 : 0;
+        const uint32_t nb = pass == 1 ? 2048u : 1024u;
+        for (int i = tid; i < kSaHist; i += kSaThreads) hist[i] = 0u;
+        __syncthreads();
+        for (int base0 = warp * 32; base0 < N; base0 += kSaThreads) {
+            const int i = base0 + lane;
+            const bool valid = i < N;
+            const uint32_t kk = valid ? float_key(__ldcg(srow + i)) : 0u;
+            const bool in = valid && (kk & pmask) == prefix;
+            const uint32_t dg = (kk >> shift) & (nb - 1);
+            const uint32_t peers = __match_any_sync(0xffffffffu, in ? dg : 0xffffffffu);
+            if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], (uint32_t)__popc(peers));
+        }
+        __syncthreads();
+        uint32_t dg, ab;
+        cta_select_digit(hist, (int)nb, krem, ms, dg, ab);
+        prefix |= (dg & (nb - 1)) << shift;
+        pmask |= (nb - 1) << shift;
+        krem -= ab;
+    }
+    const uint32_t thr = prefix;
+    if (tid < kSaMaxCluster) ms->cgt[tid] = ms->ceq[tid] = 0u;
+    __syncthreads();
+    for (int base0 = warp * 32; base0 < N; base0 += kSaThreads) {  // groups never straddle parts
+        const int i = base0 + lane;
+        const bool valid = i < N;
+        const uint32_t kk = valid ? float_key(__ldcg(srow + i)) : 0u;
+        const uint32_t gt = __popc(__ballot_sync(0xffffffffu, valid && kk > thr));
+        const uint32_t eq = __popc(__ballot_sync(0xffffffffu, valid && kk == thr));
+        if (lane == 0 && (gt | eq)) {
+            const int r = min(base0 / part, P - 1);
+            atomicAdd(&ms->cgt[r], gt);
+            atomicAdd(&ms->ceq[r], eq);
+        }
+    }
+    __syncthreads();
+    krem_out = krem;
+    return thr;
+}
+
+// Ordered emit over the keys of the part [p0, p1) (staged in keys_s, or read from global
+// memory when keys_s is null): every key above thr and the first `take` keys equal to it, in
+// ascending index order, to out[0, n_mine) and the first kSaList of them to lst as well.
+// Warp w scans the contiguous segment [p0 + w*seg, p0 + (w+1)*seg).
+SD_DEVNOINL void sa_emit_ordered(const uint32_t* keys_s, const float* srow, int p0, int p1, uint32_t thr,
+                                 uint32_t take, uint32_t n_mine, SaMisc* ms, int32_t* out, int32_t* lst) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    auto key_at = [&](int i) -> uint32_t {
+        return float_key(keys_s != nullptr ? __uint_as_float(keys_s[i - p0]) : __ldcg(srow + i));
+    };
+    const int np = p1 - p0;
+    const int seg = ((np + kSaWarps - 1) / kSaWarps + 31) / 32 * 32;
+    const int s0 = p0 + warp * seg, s1 = min(p1, s0 + seg);
+    {
+        uint32_t gt = 0, eq = 0;
+        for (int i0 = s0; i0 < s1; i0 += 32) {
+            const int i = i0 + lane;
+            const bool valid = i < s1;
+            const uint32_t kk = valid ? key_at(i) : 0u;
+            gt += __popc(__ballot_sync(0xffffffffu, valid && kk > thr));
+            eq += __popc(__ballot_sync(0xffffffffu, valid && kk == thr));
+        }
+        if (lane == 0) {
+            ms->wgt[warp] = gt;
+            ms->weq[warp] = eq;
+        }
+    }
+    __syncthreads();
+    uint32_t eq_seen = 0, pos = 0;
+    for (int w = 0; w < warp; ++w) {
+        const uint32_t tw = take > eq_seen ? min(ms->weq[w], take - eq_seen) : 0u;
+        pos += ms->wgt[w] + tw;
+        eq_seen += ms->weq[w];
+    }
+    const uint32_t lt = lanemask_lt();
+    for (int i0 = s0; i0 < s1; i0 += 32) {
+        const int i = i0 + lane;
+        const bool valid = i < s1;
+        const uint32_t kk = valid ? key_at(i) : 0u;
+        const bool is_gt = valid && kk > thr;
+        const bool is_eq = valid && kk == thr;
+        const uint32_t eqm = __ballot_sync(0xffffffffu, is_eq);
+        const bool pick = is_gt || (is_eq && eq_seen + __popc(eqm & lt) < take);
+        const uint32_t pm = __ballot_sync(0xffffffffu, pick);
+        const uint32_t at = pos + __popc(pm & lt);
+        if (pick && at < n_mine) {
+            out[at] = i;
+            if (at < (uint32_t)kSaList) lst[at] = i;
+        }
+        pos += __popc(pm);
+        eq_seen += __popc(eqm);
     }
 }
 
@@ -594,49 +703,7 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
         my_gt = ms->cgt[rank];
         my_eq = ms->ceq[rank];
     } else if (fallback) {
-        // ---- heavy ties: every CTA resolves the threshold over the whole row from global
-        // memory (no more exchanges), then counts every part
-        uint32_t prefix = d0 << 21, pmask = 0x7FFu << 21;
-        const int nall = N;
-        krem = krem0;
-#pragma unroll 1
-        for (int pass = 1; pass < 3; ++pass) {
-            const int shift = pass == 1 ? 10 : 0;
-            const uint32_t nb = pass == 1 ? 2048u : 1024u;
-            for (int i = tid; i < kSaHist; i += kSaThreads) hist0[i] = 0u;
-            __syncthreads();
-            for (int base0 = warp * 32; base0 < nall; base0 += kSaThreads) {
-                const int i = base0 + lane;
-                const bool valid = i < nall;
-                const uint32_t kk = valid ? float_key(__ldcg(srow + i)) : 0u;
-                const bool in = valid && (kk & pmask) == prefix;
-                const uint32_t dg = (kk >> shift) & (nb - 1);
-                const uint32_t peers = __match_any_sync(0xffffffffu, in ? dg : 0xffffffffu);
-                if (in && lane == __ffs(peers) - 1) atomicAdd(&hist0[dg], (uint32_t)__popc(peers));
-            }
-            __syncthreads();
-            uint32_t dg, ab;
-            cta_select_digit(hist0, (int)nb, krem, ms, dg, ab);
-            prefix |= (dg & (nb - 1)) << shift;
-            pmask |= (nb - 1) << shift;
-            krem -= ab;
-        }
-        thr = prefix;
-        if (tid < kSaMaxCluster) ms->cgt[tid] = ms->ceq[tid] = 0u;
-        __syncthreads();
-        for (int base0 = warp * 32; base0 < nall; base0 += kSaThreads) {  // groups never straddle parts
-            const int i = base0 + lane;
-            const bool valid = i < nall;
-            const uint32_t kk = valid ? float_key(__ldcg(srow + i)) : 0u;
-            const uint32_t gt = __popc(__ballot_sync(0xffffffffu, valid && kk > thr));
-            const uint32_t eq = __popc(__ballot_sync(0xffffffffu, valid && kk == thr));
-            if (lane == 0 && (gt | eq)) {
-                const int r = min(base0 / p.part, P - 1);
-                atomicAdd(&ms->cgt[r], gt);
-                atomicAdd(&ms->ceq[r], eq);
-            }
-        }
-        __syncthreads();
+        thr = sa_fallback_threshold(srow, N, p.part, P, d0, krem0, hist0, ms, krem);
         my_gt = ms->cgt[rank];
         my_eq = ms->ceq[rank];
     } else if (k == N) {
@@ -700,45 +767,7 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
             }
         }
     } else if (!trivial) {
-        // ordered ballot emit over the keys: warp w scans [p0 + w*seg, p0 + (w+1)*seg)
-        const int seg = ((np + kSaWarps - 1) / kSaWarps + 31) / 32 * 32;
-        const int s0 = p0 + warp * seg, s1 = min(p1, s0 + seg);
-        {
-            uint32_t gt = 0, eq = 0;
-            for (int i0 = s0; i0 < s1; i0 += 32) {
-                const int i = i0 + lane;
-                const bool valid = i < s1;
-                const uint32_t kk = valid ? key_at(i) : 0u;
-                gt += __popc(__ballot_sync(0xffffffffu, valid && kk > thr));
-                eq += __popc(__ballot_sync(0xffffffffu, valid && kk == thr));
-            }
-            if (lane == 0) {
-                ms->wgt[warp] = gt;
-                ms->weq[warp] = eq;
-            }
-        }
-        __syncthreads();
-        uint32_t eq_seen = 0, pos = 0;
-        for (int w = 0; w < warp; ++w) {
-            const uint32_t tw = take > eq_seen ? min(ms->weq[w], take - eq_seen) : 0u;
-            pos += ms->wgt[w] + tw;
-            eq_seen += ms->weq[w];
-        }
-        const uint32_t lt = lanemask_lt();
-        for (int i0 = s0; i0 < s1; i0 += 32) {
-            const int i = i0 + lane;
-            const bool valid = i < s1;
-            const uint32_t kk = valid ? key_at(i) : 0u;
-            const bool is_gt = valid && kk > thr;
-            const bool is_eq = valid && kk == thr;
-            const uint32_t eqm = __ballot_sync(0xffffffffu, is_eq);
-            const bool pick = is_gt || (is_eq && eq_seen + __popc(eqm & lt) < take);
-            const uint32_t pm = __ballot_sync(0xffffffffu, pick);
-            const uint32_t at = pos + __popc(pm & lt);
-            if (pick && at < n_mine) put(at, i);
-            pos += __popc(pm);
-            eq_seen += __popc(eqm);
-        }
+        sa_emit_ordered(staged ? keys_s : nullptr, srow, p0, p1, thr, take, n_mine, ms, orow + base, lst);
     }
     cp_async_wait<0>();  // query rows
     __syncthreads();     // the selection list is complete (shared memory and idx)
