@@ -37,9 +37,13 @@ def _load():
         lib.oracle_score_accumulate.argtypes = [P, P, P, I, I, I, I, I, I, I, D, P]
         lib.oracle_tier_classify.argtypes = [P, I, I, P, I, I, P, P]
         lib.oracle_quantize_rows_int8.argtypes = [P, I, P, I, I, I, I, P, P]
+        lib.oracle_window_count.argtypes = [I, I, I]
+        lib.oracle_window_max.argtypes = [P, I, I, I, I, P]
+        lib.oracle_window_union.argtypes = [P, I, I, I, I, I, P, I]
         for name in ("oracle_index_score", "oracle_block_pool", "oracle_topk",
                      "oracle_gather_attend", "oracle_score_accumulate", "oracle_tier_classify",
-                     "oracle_quantize_rows_int8"):
+                     "oracle_quantize_rows_int8", "oracle_window_count", "oracle_window_max",
+                     "oracle_window_union"):
             getattr(lib, name).restype = I
         _lib = lib
     return _lib
@@ -118,6 +122,38 @@ def topk(scores, k):
     rows = s.size // N if N > 0 else int(np.prod(s.shape[:-1]))
     out = np.empty(s.shape[:-1] + (k,), dtype=np.int32)
     _check(_load().oracle_topk(_ptr(s), rows, N, k, _ptr(out)), "topk")
+    return out
+
+
+def window_count(N, kernel, stride):
+    """Compression windows of `kernel` scores every `stride` over N scores (SparDA,
+    "Estrategia de Treinamento": the (32, 16) inference grid)."""
+    return _load().oracle_window_count(N, kernel, stride)
+
+
+def window_max(scores, kernel, stride):
+    """Window score = max of the token scores the window covers.  scores [..., N] (compared
+    as fp64) -> fp64 [..., NW]."""
+    s = np.ascontiguousarray(scores, dtype=np.float64)
+    N = s.shape[-1]
+    rows = s.size // N if N > 0 else int(np.prod(s.shape[:-1]))
+    NW = window_count(N, kernel, stride)
+    out = np.empty(s.shape[:-1] + (NW,), dtype=np.float64)
+    _check(_load().oracle_window_max(_ptr(s), rows, N, kernel, stride, _ptr(out)), "window_max")
+    return out
+
+
+def window_union(widx, N, kernel, stride, max_segs=None):
+    """Union of the selected windows' segments of `stride` tokens, ascending, padded with -1
+    (empty slots).  widx [..., k] int -> int32 [..., max_segs] (default k * kernel/stride)."""
+    w = np.ascontiguousarray(widx, dtype=np.int32)
+    k = w.shape[-1]
+    rows = w.size // k if k > 0 else int(np.prod(w.shape[:-1]))
+    if max_segs is None:
+        max_segs = k * (kernel // stride)
+    out = np.empty(w.shape[:-1] + (max_segs,), dtype=np.int32)
+    _check(_load().oracle_window_union(_ptr(w), rows, k, N, kernel, stride, _ptr(out), max_segs),
+           "window_union")
     return out
 
 

@@ -186,7 +186,9 @@ int oracle_topk(const double* scores, int rows, int N, int k, int32_t* idx) {
  *   m      = max_j z_j,  w_j = exp(z_j - m),  l = sum_j w_j
  *   out    = sum_j w_j * Vv[b,kvh,rows_j,:] / l,   lse = m + log(l)
  *   logits[b,v,h,j] = z_j  (if logits != NULL)
- * An empty selection gives out = 0 and lse = -infinity.
+ * An idx entry of -1 is an empty slot: its rows take no part (z_j = -infinity, weight 0);
+ * reading taken for selections of varying size padded to a fixed length (the union of
+ * overlapping windows).  An empty selection gives out = 0 and lse = -infinity.
  * Layouts: q [B,V,Hq,d]; K, Vv [B,Hkv,T,d]; idx [B,Hkv,n_idx]; out [B,V,Hq,d];
  * lse [B,V,Hq]; logits [B,V,Hq,n_idx*block].  Returns ORC_BAD_INDEX if a row is
  * outside [0, T).
@@ -214,16 +216,24 @@ int oracle_gather_attend(const void* q, const void* K, const void* Vv, int dtype
                 orc_load_row(q, dtype, qrow * d, d, qv);
                 for (long j = 0; j < n_rows; ++j) {
                     long row = j;
-                    if (idx != NULL)
-                        row = (long)idx[((size_t)b * Hkv + kvh) * n_idx + j / block] * block + j % block;
-                    if (row < 0 || row >= T) {
-                        bad = 1;
-                        row = 0;
+                    if (idx != NULL) {
+                        const long sel = idx[((size_t)b * Hkv + kvh) * n_idx + j / block];
+                        row = sel == -1 ? -1 : sel * block + j % block;
+                        if (sel != -1 && (sel < 0 || row >= T)) {
+                            bad = 1;
+                            row = -1;
+                        }
                     }
                     rows[j] = row;
                 }
                 double m = -INFINITY;
+                long n_valid = 0;
                 for (long j = 0; j < n_rows; ++j) {
+                    if (rows[j] < 0) {
+                        z[j] = -INFINITY;
+                        continue;
+                    }
+                    ++n_valid;
                     orc_load_row(K, dtype, (((size_t)b * Hkv + kvh) * T + rows[j]) * d, d, kr);
                     double dot = 0.0;
                     for (int c = 0; c < d; ++c) dot += qv[c] * kr[c];
@@ -235,13 +245,14 @@ int oracle_gather_attend(const void* q, const void* K, const void* Vv, int dtype
                 double l = 0.0;
                 for (int c = 0; c < d; ++c) acc[c] = 0.0;
                 for (long j = 0; j < n_rows; ++j) {
+                    if (rows[j] < 0) continue;
                     const double wj = exp(z[j] - m);
                     l += wj;
                     orc_load_row(Vv, dtype, (((size_t)b * Hkv + kvh) * T + rows[j]) * d, d, kr);
                     for (int c = 0; c < d; ++c) acc[c] += wj * kr[c];
                 }
-                for (int c = 0; c < d; ++c) out[qrow * d + c] = (n_rows > 0) ? acc[c] / l : 0.0;
-                lse[qrow] = (n_rows > 0) ? m + log(l) : -INFINITY;
+                for (int c = 0; c < d; ++c) out[qrow * d + c] = (n_valid > 0) ? acc[c] / l : 0.0;
+                lse[qrow] = (n_valid > 0) ? m + log(l) : -INFINITY;
                 if (logits != NULL)
                     for (long j = 0; j < n_rows; ++j) logits[qrow * n_rows + j] = z[j];
                 free(qv);
@@ -259,7 +270,8 @@ int oracle_gather_attend(const void* q, const void* K, const void* Vv, int dtype
  * One call adds one layer's term with weight = 1/(|L| * H):
  *   alpha_{v,h}[j] = exp(logits[b,v,h,j] - lse[b,v,h])   (softmax weight of selected row j)
  *   s[b, rows_j] += weight * alpha_{v,h}[j]   for every v, h and selected row j
- * where rows_j expands idx exactly as in step 3 (rows not selected receive nothing).
+ * where rows_j expands idx exactly as in step 3 (rows not selected, and the rows of empty
+ * slots -1, receive nothing).
  * With V > 1 verify tokens, every query token's weights are summed (reading: each
  * query token is one decode step's worth of attention).
  * Layouts: logits [B,V,Hq,n_idx*block], lse [B,V,Hq], idx [B,Hkv,n_idx] (NULL: dense),
@@ -281,8 +293,11 @@ int oracle_score_accumulate(const double* logits, const double* lse, const int32
                 const size_t qrow = (((size_t)b * V + v) * Hq + h);
                 for (long j = 0; j < n_rows; ++j) {
                     long row = j;
-                    if (idx != NULL)
-                        row = (long)idx[((size_t)b * Hkv + kvh) * n_idx + j / block] * block + j % block;
+                    if (idx != NULL) {
+                        const long sel = idx[((size_t)b * Hkv + kvh) * n_idx + j / block];
+                        if (sel == -1) continue;
+                        row = sel * block + j % block;
+                    }
                     if (row < 0 || row >= T) {
                         bad = 1;
                         continue;
@@ -291,6 +306,72 @@ int oracle_score_accumulate(const double* logits, const double* lse, const int32
                     s[(size_t)b * T + row] += weight * alpha;
                 }
             }
+    return bad ? ORC_BAD_INDEX : ORC_OK;
+}
+
+/*
+ * Step 2' -- block scores on overlapping compression windows.  [SparDA] "Estrategia de
+ * Treinamento": the inference block grid is a compression window of `kernel` tokens moved by
+ * `stride` (32, 16), and finer scores are max-pooled onto that grid.  Reading taken: the
+ * score of window n is the maximum of the token scores it covers,
+ *   w[r, n] = max over t in [n*stride, min(n*stride + kernel, N)) of scores[r, t],
+ * for n = 0 .. NW-1 with NW = 1 + ceil((N - kernel) / stride) windows (one clipped window
+ * when N < kernel; none when N = 0).  scores [rows, N] -> w [rows, NW].
+ */
+int oracle_window_count(int N, int kernel, int stride) {
+    if (N <= 0) return 0;
+    if (N <= kernel) return 1;
+    return 1 + (N - kernel + stride - 1) / stride;
+}
+
+int oracle_window_max(const double* scores, int rows, int N, int kernel, int stride, double* w) {
+    if (rows < 0 || N < 0 || kernel < 1 || stride < 1) return ORC_BAD_ARG;
+    const int NW = oracle_window_count(N, kernel, stride);
+    for (int r = 0; r < rows; ++r)
+        for (int n = 0; n < NW; ++n) {
+            const long t0 = (long)n * stride;
+            const long t1 = t0 + kernel < N ? t0 + kernel : N;
+            double m = -INFINITY;
+            for (long t = t0; t < t1; ++t)
+                if (scores[(size_t)r * N + t] > m) m = scores[(size_t)r * N + t];
+            w[(size_t)r * NW + n] = m;
+        }
+    return ORC_OK;
+}
+
+/*
+ * Step 2'' -- the tokens of the selected windows.  Windows overlap, so a token may lie in
+ * two selected windows; attention must see it once.  With kernel a multiple of stride and
+ * N a multiple of stride, the tokens are whole segments of `stride` tokens: window n covers
+ * segments n .. n + kernel/stride - 1 (those below N/stride).  Per row the union of the
+ * selected windows' segments, ascending, padded to max_segs entries with -1 (empty slots).
+ * widx [rows, k] window indices -> segs [rows, max_segs]; max_segs >= k * kernel/stride.
+ */
+int oracle_window_union(const int32_t* widx, int rows, int k, int N, int kernel, int stride, int32_t* segs,
+                        int max_segs) {
+    if (rows < 0 || k < 0 || N < 0 || kernel < 1 || stride < 1) return ORC_BAD_ARG;
+    if (kernel % stride != 0 || N % stride != 0) return ORC_BAD_ARG;
+    const int per = kernel / stride, NS = N / stride, NW = oracle_window_count(N, kernel, stride);
+    if ((long)max_segs < (long)k * per) return ORC_BAD_ARG;
+    unsigned char* in = (unsigned char*)malloc((size_t)(NS > 0 ? NS : 1));
+    int bad = 0;
+    for (int r = 0; r < rows; ++r) {
+        memset(in, 0, (size_t)(NS > 0 ? NS : 1));
+        for (int j = 0; j < k; ++j) {
+            const int n = widx[(size_t)r * k + j];
+            if (n < 0 || n >= NW) {
+                bad = 1;
+                continue;
+            }
+            for (int q = 0; q < per; ++q)
+                if (n + q < NS) in[n + q] = 1;
+        }
+        int at = 0;
+        for (int g = 0; g < NS; ++g)
+            if (in[g]) segs[(size_t)r * max_segs + at++] = g;
+        for (; at < max_segs; ++at) segs[(size_t)r * max_segs + at] = -1;
+    }
+    free(in);
     return bad ? ORC_BAD_INDEX : ORC_OK;
 }
 

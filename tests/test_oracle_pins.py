@@ -451,3 +451,108 @@ def test_int8_error_bound_and_untouched_rows():
     # the largest-magnitude element of each row maps to +-127
     assert np.all(np.abs(codes).max(-1)[t2] == 127)
     np.testing.assert_allclose(scales[t2], (amax / np.float32(127))[t2], rtol=1e-7)
+
+
+# ----------------------------------------------------------------------------- windows
+
+
+@pytest.mark.parametrize("N,kernel,stride", [(64, 32, 16), (70, 32, 16), (20, 32, 16), (48, 16, 16),
+                                             (33, 2, 1), (1, 32, 16), (0, 32, 16)])
+def test_window_max_brute_force(N, kernel, stride):
+    # every window's score is the maximum of the scores it covers (numpy over explicit slices)
+    rng = np.random.default_rng(N + kernel)
+    s = rng.integers(-50, 50, size=(3, N)).astype(np.float64)
+    w = oracle.window_max(s, kernel, stride)
+    starts = list(range(0, max(N - kernel, 0) + stride, stride)) if N > 0 else []
+    starts = [t for t in starts if t < N and (t == 0 or t + kernel - stride < N)]
+    assert w.shape == (3, len(starts)) == (3, oracle.window_count(N, kernel, stride))
+    for r in range(3):
+        for n, t0 in enumerate(starts):
+            assert w[r, n] == s[r, t0:min(t0 + kernel, N)].max()
+
+
+def test_window_count_closed_form():
+    assert oracle.window_count(32768, 32, 16) == 2047        # (32768 - 32) / 16 + 1
+    assert oracle.window_count(32769, 32, 16) == 2048        # one clipped window more
+    assert oracle.window_count(32, 32, 16) == 1
+    assert oracle.window_count(10, 32, 16) == 1
+    assert oracle.window_count(0, 32, 16) == 0
+    assert oracle.window_count(100, 1, 1) == 100             # token grid
+
+
+def test_window_max_of_a_ramp():
+    # increasing scores: window n's maximum is its last score
+    s = np.arange(160, dtype=np.float64)[None]
+    w = oracle.window_max(s, 32, 16)
+    np.testing.assert_array_equal(w[0], [min(16 * n + 31, 159) for n in range(w.shape[1])])
+
+
+@pytest.mark.parametrize("N,kernel,stride,k", [(64, 32, 16, 2), (512, 32, 16, 7), (512, 32, 16, 31),
+                                               (96, 48, 16, 3), (64, 16, 16, 4)])
+def test_window_union_is_the_set_of_covered_tokens(N, kernel, stride, k):
+    # brute force: the union of the selected windows' token ranges, as segments of `stride`
+    rng = np.random.default_rng(N + k)
+    NW = oracle.window_count(N, kernel, stride)
+    widx = np.stack([np.sort(rng.permutation(NW)[:k]) for _ in range(4)]).astype(np.int32)
+    segs = oracle.window_union(widx, N, kernel, stride)
+    assert segs.shape == (4, k * (kernel // stride))
+    for r in range(4):
+        tokens = set()
+        for n in widx[r]:
+            tokens |= set(range(n * stride, min(n * stride + kernel, N)))
+        want = sorted({t // stride for t in tokens})
+        got = segs[r]
+        np.testing.assert_array_equal(got[:len(want)], want)
+        assert np.all(got[len(want):] == -1)
+        # segments cover exactly the tokens
+        covered = {g * stride + i for g in got[got >= 0] for i in range(stride)}
+        assert covered == tokens
+
+
+def test_window_union_padding_and_bad_window():
+    segs = oracle.window_union(np.array([[0, 1]], np.int32), 64, 32, 16, max_segs=8)
+    np.testing.assert_array_equal(segs[0], [0, 1, 2, -1, -1, -1, -1, -1])  # windows 0, 1 share segment 1
+    with pytest.raises(oracle.OracleError):
+        oracle.window_union(np.array([[3]], np.int32), 64, 32, 16)          # only windows 0..2 exist
+    with pytest.raises(oracle.OracleError):
+        oracle.window_union(np.array([[0]], np.int32), 64, 24, 16)          # kernel not a multiple
+
+
+def test_attend_empty_slots_take_no_part():
+    # a selection padded with -1 equals SDPA over the non-empty rows only
+    g = torch.Generator().manual_seed(15)
+    B, Vq, Hq, Hkv, d, T, blk = 1, 2, 4, 2, 16, 128, 16
+    q = torch.randn(B, Vq, Hq, d, generator=g)
+    K, V = torch.randn(B, Hkv, T, d, generator=g), torch.randn(B, Hkv, T, d, generator=g)
+    sidx = np.array([[[1, 2, 5, -1, -1], [0, 7, -1, -1, -1]]], np.int32)
+    out, lse, logits = oracle.gather_attend(q, K, V, sidx, B, Vq, Hq, Hkv, d, T, 5, blk, 0.25, True)
+    for kvh, segs in enumerate(([1, 2, 5], [0, 7])):
+        rows = torch.tensor([g_ * blk + i for g_ in segs for i in range(blk)])
+        ro, rl = _sdpa_reference(q[:, :, kvh * 2:kvh * 2 + 2], K[:, kvh:kvh + 1, rows], V[:, kvh:kvh + 1, rows], 0.25)
+        np.testing.assert_allclose(out[:, :, kvh * 2:kvh * 2 + 2], ro, atol=1e-12)
+        np.testing.assert_allclose(lse[:, :, kvh * 2:kvh * 2 + 2], rl, atol=1e-12)
+    # the empty slots' logits are -inf; the rest of each query row's weights sum to one
+    assert np.all(np.isneginf(logits[0, :, 0:2, 3 * blk:]))
+    np.testing.assert_allclose(np.exp(logits - lse[..., None]).sum(-1), 1.0, atol=1e-12)
+    # all slots empty: nothing is attended
+    out0, lse0, _ = oracle.gather_attend(q, K, V, np.full((1, 2, 3), -1, np.int32), B, Vq, Hq, Hkv, d, T, 3, blk, 0.25)
+    assert np.all(out0 == 0) and np.all(np.isneginf(lse0))
+    # any other negative entry is still an error
+    with pytest.raises(oracle.OracleError):
+        oracle.gather_attend(q, K, V, np.array([[[-2], [0]]], np.int32), B, Vq, Hq, Hkv, d, T, 1, blk, 0.25)
+
+
+def test_score_accumulate_skips_empty_slots():
+    g = torch.Generator().manual_seed(16)
+    B, Vq, Hq, Hkv, d, T, blk = 1, 1, 4, 2, 8, 64, 16
+    q = torch.randn(B, Vq, Hq, d, generator=g)
+    K, V = torch.randn(B, Hkv, T, d, generator=g), torch.randn(B, Hkv, T, d, generator=g)
+    sidx = np.array([[[1, -1], [3, 0]]], np.int32)
+    _, lse, logits = oracle.gather_attend(q, K, V, sidx, B, Vq, Hq, Hkv, d, T, 2, blk, 0.5, True)
+    s = np.zeros((B, T))
+    oracle.score_accumulate(logits, lse, sidx, s, B, Vq, Hq, Hkv, 2, blk, T, 1.0)
+    # KV head 0's two query heads put all their mass on segment 1 (its other slot is empty);
+    # KV head 1's on segments 3 and 0
+    assert np.all(s[0, 32:48] == 0)                              # segment 2: never selected
+    np.testing.assert_allclose(s.sum(), Vq * Hq, atol=1e-12)       # every head's weights sum to 1
+    np.testing.assert_allclose(s[0, 16:32].sum(), 2.0, atol=1e-12)  # heads 0, 1 -> segment 1 only
