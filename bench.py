@@ -283,6 +283,71 @@ class SparseDecodeStep:
                 "host": host_rows * row_bytes}
 
 
+class WindowStep:
+    """One sparse decode step on the overlapping compression-window grid: the indexer, the
+    windows' max-pooled scores (with the key histogram), the top-k windows, the union of
+    their segments, and the attention over it (segments of `stride` tokens, empty slots
+    skipped)."""
+
+    dominant = "sd_index_score"
+    phases = ()
+    launches_per_step = 5
+    dominant_per_step = 1
+
+    def __init__(self, w, x, device):
+        import torch
+        from top_sparse_decode_gqa_gb300 import binding as sd
+        self.sd, self.w, self.dev = sd, w, device
+        self.q_idx, self.k_idx, self.q = (x[k].to(device) for k in ("q_idx", "k_idx", "q"))
+        self.k_cache, self.v_cache = x["k"].to(device), x["v"].to(device)
+        self.kern, self.strd = w.window_kernel, w.window_stride
+        self.NW = sd.sd_window_count(w.T, self.kern, self.strd)
+        self.max_segs = w.k * (self.kern // self.strd)
+        self.scores = torch.empty(w.B, w.Hkv, w.T, dtype=torch.float32, device=device)
+        self.wscores = torch.empty(w.B, w.Hkv, self.NW, dtype=torch.float32, device=device)
+        self.widx = torch.empty(w.B, w.Hkv, w.k, dtype=torch.int32, device=device)
+        self.segs = torch.empty(w.B, w.Hkv, self.max_segs, dtype=torch.int32, device=device)
+        self.key_hist = sd.key_hist_buffer(w.B * w.Hkv, device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.args, self.out, self.lse, _ = sd.make_attend_args(
+            self.q, self.k_cache, self.v_cache, self.segs, block=self.strd, T=w.T, err_word=self.err)
+        need = sd.sd_gather_attend_workspace_bytes(self.args)
+        self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=device)
+        self.idx = self.segs
+        self.rows_used = None
+
+    def run(self, m: "StepMarks" = None):
+        sd = self.sd
+        if m is not None:
+            m.start.record()
+            m.before(0)
+        sd.sd_index_score(self.q_idx, self.k_idx, self.scores, self.err)
+        if m is not None:
+            m.after(0)
+        sd.sd_window_max(self.scores, self.kern, self.strd, self.wscores, key_hist=self.key_hist)
+        sd.sd_topk(self.wscores, self.w.k, self.widx, key_hist=self.key_hist)
+        sd.sd_window_union(self.widx, self.w.T, self.kern, self.strd, self.segs, err_word=self.err)
+        sd.sd_gather_attend(self.args, self.ws)
+        if m is not None:
+            m.end.record()
+
+    def after_warmup(self):
+        """Counts the K/V rows the union selects (fixed by the inputs)."""
+        self.rows_used = int((self.segs >= 0).sum().item()) * self.strd
+
+    def bytes(self):
+        w = self.w
+        e = w.elem_bytes
+        key_bytes = w.B * w.Hkv * w.T * w.dI * e
+        q_idx_bytes = w.B * w.Hkv * w.V * w.dI * e
+        score_bytes = w.B * w.Hkv * w.T * 4
+        kv = (self.rows_used or 0) * w.d * e * 2
+        q_bytes = w.B * w.V * w.Hq * w.d * e
+        out_bytes = w.B * w.V * w.Hq * (w.d + 1) * 4 + w.B * w.Hkv * self.max_segs * 4
+        return {"dominant": key_bytes + q_idx_bytes + score_bytes,
+                "hbm": key_bytes + q_idx_bytes + kv + q_bytes + out_bytes, "host": 0}
+
+
 class DenseScoringStep:
     """One decode step of the importance-scoring workload: for every layer, dense attention
     over all cached rows (logits kept) and that layer's term of the importance score."""
@@ -353,7 +418,11 @@ class DenseScoringStep:
 
 
 def make_step(w, x, device, separate=False):
-    return DenseScoringStep(w, x, device) if w.layers > 1 else SparseDecodeStep(w, x, device, separate)
+    if w.layers > 1:
+        return DenseScoringStep(w, x, device)
+    if w.window_kernel > 0:
+        return WindowStep(w, x, device)
+    return SparseDecodeStep(w, x, device, separate)
 
 
 def host_link_gbs(device, nbytes=512 << 20):
@@ -450,7 +519,7 @@ def run_ours(args):
     by = step.bytes()
     dom_s = statistics.mean(dom_ms) / 1e3
     achieved = by["dominant"] / dom_s / 1e9
-    if isinstance(step, SparseDecodeStep):
+    if isinstance(step, (SparseDecodeStep, WindowStep)):
         kernel_file, kernel_tag = ("index_score.cu", "index_score_tc.cu", "tc_common.cuh", "sd_common.cuh"), "index_score"
     else:
         kernel_file, kernel_tag = ("gather_attend.cu", "sd_common.cuh"), "gather_attend"
@@ -470,6 +539,11 @@ def run_ours(args):
         tail = [m.dom[0][1].elapsed_time(m.end) for m in kmarks]
         step_roof["kernel_us"] = {"index_score": round(statistics.mean(dom_ms) * 1e3, 2),
                                   "select_attend": round(statistics.mean(tail) * 1e3, 2)}
+    elif isinstance(step, WindowStep):
+        tail = [m.dom[0][1].elapsed_time(m.end) for m in kmarks]
+        step_roof["kernel_us"] = {"index_score": round(statistics.mean(dom_ms) * 1e3, 2),
+                                  "window_max+topk+union+gather_attend": round(statistics.mean(tail) * 1e3, 2)}
+        step_roof["kv_rows_selected"] = step.rows_used
     elif isinstance(step, SparseDecodeStep):
         after_topk = [m.dom[0][1].elapsed_time(m.phase["after_topk"]) for m in kmarks]
         tail = [m.phase["after_topk"].elapsed_time(m.end) for m in kmarks]
@@ -497,6 +571,8 @@ def run_ours(args):
                    "queries_per_step": w.queries_per_step,
                    "path": ("indexer + fused select/attend" if getattr(step, "fused", False)
                             else "indexer + top-k + gather-attend" if isinstance(step, SparseDecodeStep)
+                            else "indexer + window max + top-k windows + union + gather-attend"
+                            if isinstance(step, WindowStep)
                             else "dense attention + score accumulate per layer"),
                    "l2": "flushed between timed steps: 2x L2 written then read, outside the events",
                    "parallelism": f"replica x{world} (each rank its own batch)"},
@@ -525,10 +601,11 @@ def measure_e2e(step, w, x, clean_l2, K):
     host memory; host wall clock per step, including the copies and the final sync."""
     import torch
     ins = [(step.q, x["q"][0, 0] if w.layers > 1 else x["q"])]
-    if isinstance(step, SparseDecodeStep):
+    if isinstance(step, (SparseDecodeStep, WindowStep)):
         ins.append((step.q_idx, x["q_idx"]))
     ins = [(dst, src.contiguous().pin_memory()) for dst, src in ins]
-    outs = [step.out, step.lse] + ([step.idx] if isinstance(step, SparseDecodeStep) else [step.s])
+    sparse = isinstance(step, (SparseDecodeStep, WindowStep))
+    outs = [step.out, step.lse] + ([step.idx] if sparse else [step.s])
     outs = [(src, torch.empty(src.shape, dtype=src.dtype).pin_memory()) for src in outs]
     times = []
     for i in range(K + 3):
@@ -571,6 +648,12 @@ def oracle_step(w, x, b0, b1):
     if w.block > 1:
         keys = oracle.block_pool(keys, nb, w.Hkv, w.T, w.dI, w.block).astype("float32")
     sc = oracle.index_score(q_idx, keys, nb, w.Hkv, w.V, w.N, w.dI)
+    if w.window_kernel > 0:  # windows: max-pooled scores, top-k windows, their union
+        widx = oracle.topk(oracle.window_max(sc, w.window_kernel, w.window_stride), w.k)
+        segs = oracle.window_union(widx, w.T, w.window_kernel, w.window_stride)
+        return oracle.gather_attend(x["q"][b0:b1].contiguous(), x["k"][b0:b1].contiguous(),
+                                    x["v"][b0:b1].contiguous(), segs, nb, w.V, w.Hq, w.Hkv, w.d, w.T,
+                                    segs.shape[-1], w.window_stride, scale)
     idx = oracle.topk(sc, w.k)
     return oracle.gather_attend(x["q"][b0:b1].contiguous(), x["k"][b0:b1].contiguous(),
                                 x["v"][b0:b1].contiguous(), idx, nb, w.V, w.Hq, w.Hkv, w.d, w.T,

@@ -132,7 +132,8 @@ sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx, uin
  * For query row (b, v, h) with kvh = h / (Hq/Hkv):
  *   rows_j = idx[b,kvh, j / block] * block + j % block, j < n_idx*block  (idx == NULL:
  *            dense, rows_j = j and n_idx*block must equal T; n_idx == 0 is an empty
- *            selection whatever idx is)
+ *            selection whatever idx is; an idx entry of -1 is an empty slot whose rows
+ *            take no part, z_j = -inf, e.g. the padding of sd_window_union)
  *   z_j    = scale * q[b,v,h,:] . K[b,kvh,rows_j,:]
  *   out[b,v,h,:] = sum_j softmax(z)_j V[b,kvh,rows_j,:],  lse[b,v,h] = log sum_j exp(z_j)
  *   logits[b,v,h,j] = z_j (optional).  No rows: out = 0, lse = -inf.
@@ -223,6 +224,37 @@ sd_status sd_select_attend(const float* scores, int N, uint32_t* key_hist, int32
                            const sd_attend_args* args, void* stream);
 
 /*
+ * sd_window_max -- block scores on overlapping compression windows.
+ * [SparDA] "Estrategia de Treinamento": the inference block grid is a compression window of
+ * `kernel` tokens moved by `stride` (32, 16), and finer scores are max-pooled onto it.
+ * Reading taken: window n's score is the maximum of the token scores it covers,
+ *     wscores[r, n] = max over t in [n*stride, min(n*stride + kernel, N)) of scores[r, t],
+ * n < NW = sd_window_count(N, kernel, stride) = 1 + ceil((N - kernel) / stride) (1 when
+ * N <= kernel, 0 when N == 0).  scores [rows, N] fp32 (as written by sd_index_score);
+ * wscores [rows, NW] fp32 (written).  key_hist: nullable [rows, SD_KEY_HIST_BINS] uint32,
+ * zero-filled by the caller; the call adds the histogram sd_topk takes for these window
+ * scores.  Limits: 1 <= stride <= kernel <= 1024.
+ */
+int sd_window_count(int N, int kernel, int stride);
+sd_status sd_window_max(const float* scores, int rows, int N, int kernel, int stride, float* wscores,
+                        uint32_t* key_hist, void* stream);
+
+/*
+ * sd_window_union -- the tokens of the selected windows, each once.
+ * Windows overlap, so a token can lie in two selected windows; attention must see it once.
+ * With kernel a multiple of stride and N a multiple of stride, the tokens are whole segments
+ * of `stride` tokens: window n covers segments n .. n + kernel/stride - 1 (those below
+ * N/stride).  Per row r: the union of the segments of the windows in widx[r, 0..k),
+ * ascending, written to segs[r, 0..), padded with -1 (empty slots) to max_segs entries;
+ * segs feeds sd_gather_attend with block = stride and n_idx = max_segs.
+ * widx [rows, k] int32 window indices in [0, NW) (others are skipped and set
+ * SD_DEVERR_INDEX in *err_word); segs [rows, max_segs] int32 (written);
+ * max_segs >= k * kernel/stride.  Limit: N/stride <= 65536 segments per row.
+ */
+sd_status sd_window_union(const int32_t* widx, int rows, int k, int N, int kernel, int stride, int32_t* segs,
+                          int max_segs, int32_t* err_word, void* stream);
+
+/*
  * sd_score_accumulate -- one layer's term of the cumulative attention-importance score.
  * [HBM] Metodologia 2:  s_i(t) = s_i(t-1) + (1/|L|) sum_l (1/H) sum_h alpha_{l,h}(t)[i].
  * Adds, for every query row (b, v, h) and selected row j (expanded as in
@@ -231,7 +263,8 @@ sd_status sd_select_attend(const float* scores, int N, uint32_t* key_hist, int32
  * so calling it once per layer with weight = 1/(|L| * Hq) applies the equation.
  * logits [B,V,Hq,n_idx*block] and lse [B,V,Hq] fp32 as written by sd_gather_attend;
  * idx [B,Hkv,n_idx] or NULL (dense); s [B,T] fp64, updated in place.
- * Rows not selected receive nothing.  Order of additions into one s entry is not fixed
+ * Rows not selected, and the rows of empty slots (-1), receive nothing.  Order of
+ * additions into one s entry is not fixed
  * when several KV groups select it (fp64 atomics); the result varies only by rounding.
  */
 sd_status sd_score_accumulate(const float* logits, const float* lse, const int32_t* idx, int B,

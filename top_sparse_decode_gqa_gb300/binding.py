@@ -26,7 +26,8 @@ EXPORTS = (
     "sd_version", "sd_status_string", "sd_last_error_message", "sd_index_score", "sd_block_pool",
     "sd_topk_workspace_bytes", "sd_topk", "sd_gather_attend_workspace_bytes", "sd_gather_attend",
     "sd_score_accumulate", "sd_tier_classify_workspace_bytes", "sd_tier_classify",
-    "sd_quantize_rows_int8", "sd_gather_attend_noalloc", "sd_select_attend",
+    "sd_quantize_rows_int8", "sd_gather_attend_noalloc", "sd_select_attend", "sd_window_count",
+    "sd_window_max", "sd_window_union",
 )
 
 
@@ -75,6 +76,10 @@ def lib() -> ctypes.CDLL:
         L.sd_gather_attend.argtypes = [ctypes.POINTER(sd_attend_args), P]
         L.sd_gather_attend_noalloc.argtypes = [ctypes.POINTER(sd_attend_args), P]
         L.sd_select_attend.argtypes = [P, I, P, P, ctypes.POINTER(sd_attend_args), P]
+        L.sd_window_count.argtypes = [I, I, I]
+        L.sd_window_count.restype = I
+        L.sd_window_max.argtypes = [P, I, I, I, I, P, P, P]
+        L.sd_window_union.argtypes = [P, I, I, I, I, I, P, I, P, P]
         L.sd_score_accumulate.argtypes = [P, P, P, I, I, I, I, I, I, I, D, P, P, P]
         L.sd_tier_classify_workspace_bytes.argtypes = [I, I]
         L.sd_tier_classify_workspace_bytes.restype = Z
@@ -263,6 +268,41 @@ def sd_select_attend(scores: torch.Tensor, args: sd_attend_args, idx: torch.Tens
     _check(lib().sd_select_attend(_ptr(scores), scores.shape[-1], _ptr(key_hist), _ptr(idx),
                                   ctypes.byref(args), _stream(stream)), "sd_select_attend")
     return idx
+
+
+def sd_window_count(N: int, kernel: int, stride: int) -> int:
+    return lib().sd_window_count(N, kernel, stride)
+
+
+def sd_window_max(scores: torch.Tensor, kernel: int, stride: int, wscores: Optional[torch.Tensor] = None,
+                  key_hist: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Max-pooled scores of overlapping windows (kernel, stride) of each row of scores [..., N];
+    key_hist (zero-filled) receives the histogram sd_topk takes for the window scores."""
+    _dev(scores, "scores")
+    N = scores.shape[-1]
+    rows = scores.numel() // N if N > 0 else math.prod(scores.shape[:-1])
+    NW = sd_window_count(N, kernel, stride)
+    if wscores is None:
+        wscores = torch.empty(scores.shape[:-1] + (NW,), dtype=torch.float32, device=scores.device)
+    _check(lib().sd_window_max(_ptr(scores), rows, N, kernel, stride, _ptr(wscores), _ptr(key_hist),
+                               _stream(stream)), "sd_window_max")
+    return wscores
+
+
+def sd_window_union(widx: torch.Tensor, N: int, kernel: int, stride: int, segs: Optional[torch.Tensor] = None,
+                    max_segs: Optional[int] = None, err_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Segments of `stride` tokens covered by the selected windows widx [..., k], ascending,
+    padded with -1 to max_segs (default k * kernel/stride)."""
+    _dev(widx, "widx")
+    k = widx.shape[-1]
+    rows = widx.numel() // k if k > 0 else math.prod(widx.shape[:-1])
+    if max_segs is None:
+        max_segs = k * (kernel // stride)
+    if segs is None:
+        segs = torch.empty(widx.shape[:-1] + (max_segs,), dtype=torch.int32, device=widx.device)
+    _check(lib().sd_window_union(_ptr(widx), rows, k, N, kernel, stride, _ptr(segs), max_segs, _ptr(err_word),
+                                 _stream(stream)), "sd_window_union")
+    return segs
 
 
 def select_attend(scores, k, q, k_cache, v_cache, key_hist=None, stream=None, **kw):

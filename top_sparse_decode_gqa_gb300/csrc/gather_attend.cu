@@ -235,6 +235,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
         long pos = jg;
         if (p.idx != nullptr) {
             const long sel = p.idx[(size_t)bk * p.n_idx + jg / p.block];
+            if (sel == -1) return kNoRow;  // empty slot
             pos = sel * p.block + jg % p.block;
             if (sel < 0 || pos >= p.T) {
                 report(p.err, SD_DEVERR_INDEX);
@@ -502,7 +503,9 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
             if (p.idx != nullptr) {
                 const long sel = p.idx[(size_t)bk * p.n_idx + jg / p.block];
                 pos = sel * p.block + jg % p.block;
-                if (sel < 0 || pos >= p.T) {
+                if (sel == -1) {  // empty slot
+                    ok = false;
+                } else if (sel < 0 || pos >= p.T) {
                     report(p.err, SD_DEVERR_INDEX);
                     ok = false;
                 }

@@ -56,6 +56,7 @@ __global__ void score_accumulate_sparse_kernel(const float* __restrict__ logits,
         const long bk = e / n_rows;
         const int b = (int)(bk / Hkv), kvh = (int)(bk % Hkv);
         const long sel = idx[bk * n_idx + j / block];
+        if (sel == -1) continue;  // empty slot
         const long pos = sel * block + j % block;
         if (sel < 0 || pos >= T) {
             report(err, SD_DEVERR_INDEX);

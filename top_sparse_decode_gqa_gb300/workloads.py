@@ -22,6 +22,10 @@ available here):
 * ``c5_importance_tiering``: Qwen2.5-7B-shaped, 28 layers of 28/4 heads, d = 128, bf16,
   T = 65536, batch 2, dense decode for 64 steps accumulating the importance score, then
   a 20/40/30/10 % four-tier split.
+* ``c6_window_blocks``: the Llama-3-8B-shaped layer of ``c2`` on the overlapping
+  compression-window grid (windows of 32 tokens every 16): token scores max-pooled onto
+  2047 windows, top-64 windows per KV head, attention over their union (at most 2048
+  tokens, as 16-token segments).
 
 Value recipe: indexer query and keys are integers drawn uniformly from [-8, 8] (exact in
 bf16 and fp32); attention q, K, V are standard normal, rounded to bf16 (nearest even)
@@ -59,6 +63,8 @@ class Workload:
     resident_frac: float = 1.0    # fraction of positions resident in the HBM pool
     layers: int = 1
     steps: int = 1
+    window_kernel: int = 0  # > 0: select compression windows of this many tokens ...
+    window_stride: int = 0  # ... moved by this many (k counts windows)
     cum_frac: tuple = (0.2, 0.6, 0.9)
     n_sink: int = 0
     n_recent: int = 0
@@ -73,7 +79,10 @@ class Workload:
 
     @property
     def n_rows(self) -> int:
-        """Selected K/V rows per (b, kvh) after block expansion."""
+        """Selected K/V row slots per (b, kvh) after block expansion (windows: the segment
+        slots of their union, some of them empty)."""
+        if self.window_kernel > 0:
+            return self.k * self.window_kernel
         return self.k * self.block
 
     @property
@@ -117,6 +126,9 @@ WORKLOADS: Dict[str, Workload] = {
                  dI=128, k=2048, resident_frac=0.1),
         Workload("c5_importance_tiering", 4, B=2, V=1, Hq=28, Hkv=4, d=128, T=65536,
                  dtype="bf16", dI=128, k=65536, layers=28, steps=64),
+        Workload("c6_window_blocks", 5, B=8, V=1, Hq=32, Hkv=8, d=128, T=32768, dtype="bf16",
+                 dI=128, k=64, planted=655, planted_values="five_to_eight", planted_attn_boost=0.5,
+                 window_kernel=32, window_stride=16),
     )
 }
 
