@@ -348,6 +348,63 @@ class WindowStep:
                 "hbm": key_bytes + q_idx_bytes + kv + q_bytes + out_bytes, "host": 0}
 
 
+class HeadsStep:
+    """One sparse decode step with selection per query head: every head's unscaled
+    attention logits against its KV head's keys (with the key histogram, one row per head),
+    each head's top-k, and the attention of each head over its own selected rows."""
+
+    dominant = "sd_index_score_heads"
+    phases = ("after_topk",)
+    launches_per_step = 3
+    dominant_per_step = 1
+
+    def __init__(self, w, x, device):
+        import torch
+        from top_sparse_decode_gqa_gb300 import binding as sd
+        assert w.V == 1, "per-head selection scores the decode query of every head"
+        self.sd, self.w, self.dev = sd, w, device
+        self.q = x["q"].to(device)                              # [B,1,Hq,d]
+        self.q_heads = self.q.view(w.B, w.Hkv, w.G, w.d)        # the same bytes, [B,Hkv,G,d]
+        self.k_cache, self.v_cache = x["k"].to(device), x["v"].to(device)
+        self.scores = torch.empty(w.B, w.Hkv, w.G, w.T, dtype=torch.float32, device=device)
+        self.idx = torch.empty(w.B, w.Hq, w.k, dtype=torch.int32, device=device)
+        self.key_hist = sd.key_hist_buffer(w.B * w.Hq, device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.args, self.out, self.lse, _ = sd.make_attend_args(
+            self.q, self.k_cache, self.v_cache, self.idx, T=w.T, err_word=self.err, per_head=True)
+        need = sd.sd_gather_attend_workspace_bytes(self.args)
+        self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=device)
+
+    def run(self, m: "StepMarks" = None):
+        sd = self.sd
+        if m is not None:
+            m.start.record()
+            m.before(0)
+        sd.sd_index_score_heads(self.q_heads, self.k_cache, self.scores, self.err, key_hist=self.key_hist)
+        if m is not None:
+            m.after(0)
+        sd.sd_topk(self.scores, self.w.k, self.idx, key_hist=self.key_hist)
+        if m is not None:
+            m.at("after_topk")
+        sd.sd_gather_attend(self.args, self.ws)
+        if m is not None:
+            m.end.record()
+
+    def after_warmup(self):
+        pass
+
+    def bytes(self):
+        w = self.w
+        e = w.elem_bytes
+        key_bytes = w.B * w.Hkv * w.T * w.d * e
+        q_bytes = w.B * w.Hq * w.d * e
+        score_bytes = w.B * w.Hq * w.T * 4
+        kv = w.B * w.Hq * w.k * w.d * e * 2
+        out_bytes = w.B * w.Hq * (w.d + 1) * 4 + w.B * w.Hq * w.k * 4
+        return {"dominant": key_bytes + q_bytes + score_bytes,
+                "hbm": key_bytes + q_bytes + kv + out_bytes, "host": 0}
+
+
 class DenseScoringStep:
     """One decode step of the importance-scoring workload: for every layer, dense attention
     over all cached rows (logits kept) and that layer's term of the importance score."""
@@ -422,6 +479,8 @@ def make_step(w, x, device, separate=False):
         return DenseScoringStep(w, x, device)
     if w.window_kernel > 0:
         return WindowStep(w, x, device)
+    if w.per_head:
+        return HeadsStep(w, x, device)
     return SparseDecodeStep(w, x, device, separate)
 
 
@@ -519,7 +578,7 @@ def run_ours(args):
     by = step.bytes()
     dom_s = statistics.mean(dom_ms) / 1e3
     achieved = by["dominant"] / dom_s / 1e9
-    if isinstance(step, (SparseDecodeStep, WindowStep)):
+    if isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep)):
         kernel_file, kernel_tag = ("index_score.cu", "index_score_tc.cu", "tc_common.cuh", "sd_common.cuh"), "index_score"
     else:
         kernel_file, kernel_tag = ("gather_attend.cu", "sd_common.cuh"), "gather_attend"
@@ -544,7 +603,7 @@ def run_ours(args):
         step_roof["kernel_us"] = {"index_score": round(statistics.mean(dom_ms) * 1e3, 2),
                                   "window_max+topk+union+gather_attend": round(statistics.mean(tail) * 1e3, 2)}
         step_roof["kv_rows_selected"] = step.rows_used
-    elif isinstance(step, SparseDecodeStep):
+    elif isinstance(step, (SparseDecodeStep, HeadsStep)):
         after_topk = [m.dom[0][1].elapsed_time(m.phase["after_topk"]) for m in kmarks]
         tail = [m.phase["after_topk"].elapsed_time(m.end) for m in kmarks]
         step_roof["kernel_us"] = {"index_score": round(statistics.mean(dom_ms) * 1e3, 2),
@@ -573,6 +632,8 @@ def run_ours(args):
                             else "indexer + top-k + gather-attend" if isinstance(step, SparseDecodeStep)
                             else "indexer + window max + top-k windows + union + gather-attend"
                             if isinstance(step, WindowStep)
+                            else "per-head logits + per-head top-k + per-head gather-attend"
+                            if isinstance(step, HeadsStep)
                             else "dense attention + score accumulate per layer"),
                    "l2": "flushed between timed steps: 2x L2 written then read, outside the events",
                    "parallelism": f"replica x{world} (each rank its own batch)"},
@@ -604,7 +665,7 @@ def measure_e2e(step, w, x, clean_l2, K):
     if isinstance(step, (SparseDecodeStep, WindowStep)):
         ins.append((step.q_idx, x["q_idx"]))
     ins = [(dst, src.contiguous().pin_memory()) for dst, src in ins]
-    sparse = isinstance(step, (SparseDecodeStep, WindowStep))
+    sparse = isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep))
     outs = [step.out, step.lse] + ([step.idx] if sparse else [step.s])
     outs = [(src, torch.empty(src.shape, dtype=src.dtype).pin_memory()) for src in outs]
     times = []
@@ -643,6 +704,13 @@ def oracle_step(w, x, b0, b1):
             oracle.score_accumulate(z, lse, None, s, nb, w.V, w.Hq, w.Hkv, w.T, 1, w.T,
                                     1.0 / (w.layers * w.Hq))
         return s
+    if w.per_head:  # every head's own logits, its own top-k, attention over its own rows
+        q = x["q"][b0:b1].contiguous()
+        sc = oracle.index_score_heads(q.view(nb, w.Hkv, w.G, w.d), x["k"][b0:b1].contiguous(), nb, w.Hkv, w.G,
+                                      w.T, w.d)
+        idx = oracle.topk(sc.reshape(nb, w.Hq, w.T), w.k)
+        return oracle.gather_attend(q, x["k"][b0:b1].contiguous(), x["v"][b0:b1].contiguous(), idx, nb, w.V,
+                                    w.Hq, w.Hkv, w.d, w.T, w.k, 1, scale, per_head=True)
     q_idx = x["q_idx"][b0:b1].contiguous()
     keys = x["k_idx"][b0:b1].contiguous()
     if w.block > 1:

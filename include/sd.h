@@ -93,6 +93,23 @@ sd_status sd_index_score(const void* q_idx, sd_dtype q_dtype, const void* k_idx,
                          float* scores, uint32_t* key_hist, int32_t* err_word, void* stream);
 
 /*
+ * sd_index_score_heads -- one score row per query row (no max over the V queries).
+ * [Illusion] sec. 2 "Mecanismos de Esparsidade": Oracle Top-K selects per query head with the
+ * attention query itself.  For every (b, kvh), query row v and token t:
+ *     scores[b, kvh, v, t] = sum_j q[b, kvh, v, j] * k[b, kvh, t, j]
+ * With the attention query [B, 1, Hq, d] seen as q [B, Hkv, G, d] (V = G) and the attention
+ * keys k [B, Hkv, T, d], scores [B, Hkv, G, T] = [B, Hq, T] are every query head's unscaled
+ * logits, the input of a per-head sd_topk (B*Hq rows).  Same dtypes and limits as
+ * sd_index_score, except V <= 16 for bf16 q and k (tensor cores) and V <= 8 otherwise; the
+ * sums are fp32 (exact for integer inputs; otherwise fp32 rounding in an order of the
+ * kernel's choosing).  key_hist: nullable [B*Hkv*V, SD_KEY_HIST_BINS], one histogram per
+ * score row, zero-filled by the caller.
+ */
+sd_status sd_index_score_heads(const void* q, sd_dtype q_dtype, const void* k, sd_dtype k_dtype, int B, int Hkv,
+                               int V, int N, int d, float* scores, uint32_t* key_hist, int32_t* err_word,
+                               void* stream);
+
+/*
  * sd_block_pool -- block keys for block-granular selection (cache-build helper).
  * [SparDA] sec. 2 item 1 (top-k blocks) and "Estrategia de Treinamento" (pooling onto the
  * block grid).  Disjoint blocks of `block` tokens; the key of block n is the mean of its
@@ -154,6 +171,10 @@ sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx, uin
  * workspace must not overlap on the GPU.  splits = 0 picks one wave of CTAs for this GPU;
  * a requested split count is adjusted to at least one 64-row chunk per split and at most
  * 448 rows per split when rows are selected through idx or slot_map.
+ * per_head = 1 ([Illusion] sec. 2: Oracle Top-K per query head): idx is [B,Hq,n_idx] and
+ * query head h attends to its own selection idx[b,h,:], rows read from KV head
+ * h / (Hq/Hkv) (all V query tokens of the head share it); the split plan and workspace then
+ * count B*Hq groups of V query rows.  Needs idx.
  * The kernel is launched as a programmatic dependent of the preceding kernel in the
  * stream (it waits for that kernel's results before reading anything).
  */
@@ -175,6 +196,7 @@ typedef struct {
     void* workspace;          /* device scratch of workspace_bytes */
     size_t workspace_bytes;
     int splits;               /* 0 = automatic */
+    int per_head;             /* 1: idx is [B,Hq,n_idx], one selection per query head */
 } sd_attend_args;
 
 size_t sd_gather_attend_workspace_bytes(const sd_attend_args* args);

@@ -33,7 +33,8 @@ def _load():
         lib.oracle_index_score.argtypes = [P, I, P, I, I, I, I, I, I, P]
         lib.oracle_block_pool.argtypes = [P, I, I, I, I, I, I, P]
         lib.oracle_topk.argtypes = [P, I, I, I, P]
-        lib.oracle_gather_attend.argtypes = [P, P, P, I, P, I, I, I, I, I, I, I, I, D, P, P, P]
+        lib.oracle_gather_attend.argtypes = [P, P, P, I, P, I, I, I, I, I, I, I, I, D, P, P, P, I]
+        lib.oracle_index_score_heads.argtypes = [P, I, P, I, I, I, I, I, I, P]
         lib.oracle_score_accumulate.argtypes = [P, P, P, I, I, I, I, I, I, I, D, P]
         lib.oracle_tier_classify.argtypes = [P, I, I, P, I, I, P, P]
         lib.oracle_quantize_rows_int8.argtypes = [P, I, P, I, I, I, I, P, P]
@@ -43,7 +44,7 @@ def _load():
         for name in ("oracle_index_score", "oracle_block_pool", "oracle_topk",
                      "oracle_gather_attend", "oracle_score_accumulate", "oracle_tier_classify",
                      "oracle_quantize_rows_int8", "oracle_window_count", "oracle_window_max",
-                     "oracle_window_union"):
+                     "oracle_window_union", "oracle_index_score_heads"):
             getattr(lib, name).restype = I
         _lib = lib
     return _lib
@@ -104,6 +105,18 @@ def index_score(q_idx, k_idx, B, Hkv, V, N, dI):
     return out
 
 
+def index_score_heads(q, k, B, Hkv, V, N, dI):
+    """Per-query scores (Illusion sec. 2, Oracle Top-K per query head): fp64 [B,Hkv,V,N],
+    scores[b,h,v,t] = sum_j q[b,h,v,j] k[b,h,t,j] (no max over v)."""
+    qa, qd = _as_data(q)
+    ka, kd = _as_data(k)
+    assert qa.size == B * Hkv * V * dI and ka.size == B * Hkv * N * dI
+    out = np.empty((B, Hkv, V, N), dtype=np.float64)
+    _check(_load().oracle_index_score_heads(_ptr(qa), qd, _ptr(ka), kd, B, Hkv, V, N, dI, _ptr(out)),
+           "index_score_heads")
+    return out
+
+
 def block_pool(k_idx, B, Hkv, T, dI, block):
     """Mean of each disjoint block of `block` indexer keys (SparDA, block grid).
     Returns fp64 [B,Hkv,T/block,dI]."""
@@ -157,7 +170,7 @@ def window_union(widx, N, kernel, stride, max_segs=None):
     return out
 
 
-def gather_attend(q, K, Vv, idx, B, V, Hq, Hkv, d, T, n_idx, block, scale, want_logits=False):
+def gather_attend(q, K, Vv, idx, B, V, Hq, Hkv, d, T, n_idx, block, scale, want_logits=False, per_head=False):
     """Exact softmax attention of every query row over the selected rows only
     (Illusion sec. 2 / 3C).  idx None means dense (all T rows).
     Returns (out fp64 [B,V,Hq,d], lse fp64 [B,V,Hq], logits fp64 [B,V,Hq,n_idx*block] or None)."""
@@ -169,13 +182,13 @@ def gather_attend(q, K, Vv, idx, B, V, Hq, Hkv, d, T, n_idx, block, scale, want_
     ia = None
     if idx is not None:
         ia = np.ascontiguousarray(idx, dtype=np.int32)
-        assert ia.size == B * Hkv * n_idx
+        assert ia.size == B * (Hq if per_head else Hkv) * n_idx
     out = np.empty((B, V, Hq, d), dtype=np.float64)
     lse = np.empty((B, V, Hq), dtype=np.float64)
     logits = np.empty((B, V, Hq, n_idx * block), dtype=np.float64) if want_logits else None
     _check(_load().oracle_gather_attend(_ptr(qa), _ptr(ka), _ptr(va), qd, _ptr(ia), B, V, Hq, Hkv,
                                         d, T, n_idx, block, float(scale), _ptr(out), _ptr(lse),
-                                        _ptr(logits)), "gather_attend")
+                                        _ptr(logits), 1 if per_head else 0), "gather_attend")
     return out, lse, logits
 
 

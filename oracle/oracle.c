@@ -102,6 +102,40 @@ int oracle_index_score(const void* q_idx, int q_dtype, const void* k_idx, int k_
 }
 
 /*
+ * Step 1, per query -- [Illusion] sec. 2 "Mecanismos de Esparsidade": Oracle Top-K selects
+ * per query head with the attention query itself, so every query row keeps its own scores:
+ *
+ *   scores[b,h,v,t] = sum_j  q[b,h,v,j] * k[b,h,t,j]      (no max over v)
+ *
+ * With the attention query [B,1,Hq,d] read as [B,Hkv,G,d] (V = G) these are every query
+ * head's unscaled logits.  Layouts: q [B,Hkv,V,dI], k [B,Hkv,N,dI], scores [B,Hkv,V,N].
+ */
+int oracle_index_score_heads(const void* q_in, int q_dtype, const void* k_in, int k_dtype, int B, int Hkv, int V,
+                             int N, int dI, double* scores) {
+    if (B < 0 || Hkv < 0 || V < 1 || N < 0 || dI < 1) return ORC_BAD_ARG;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < Hkv; ++h) {
+            double* q = (double*)malloc(sizeof(double) * (size_t)V * dI);
+            double* k = (double*)malloc(sizeof(double) * (size_t)dI);
+            for (int v = 0; v < V; ++v)
+                orc_load_row(q_in, q_dtype, (((size_t)b * Hkv + h) * V + v) * dI, dI, q + (size_t)v * dI);
+            for (int t = 0; t < N; ++t) {
+                orc_load_row(k_in, k_dtype, (((size_t)b * Hkv + h) * N + t) * dI, dI, k);
+                for (int v = 0; v < V; ++v) {
+                    double dot = 0.0;
+                    for (int j = 0; j < dI; ++j) dot += q[(size_t)v * dI + j] * k[j];
+                    scores[(((size_t)b * Hkv + h) * V + v) * N + t] = dot;
+                }
+            }
+            free(q);
+            free(k);
+        }
+    }
+    return ORC_OK;
+}
+
+/*
  * Step 1' -- block key for block-granular selection.  [SparDA] sec. 2 item 1 selects
  * top-k *blocks*, and "Estrategia de Treinamento" pools finer scores onto a block grid.
  * Reading taken: disjoint blocks of `block` tokens; the block key is the mean of the
@@ -186,6 +220,8 @@ int oracle_topk(const double* scores, int rows, int N, int k, int32_t* idx) {
  *   m      = max_j z_j,  w_j = exp(z_j - m),  l = sum_j w_j
  *   out    = sum_j w_j * Vv[b,kvh,rows_j,:] / l,   lse = m + log(l)
  *   logits[b,v,h,j] = z_j  (if logits != NULL)
+ * per_head = 1 ([Illusion] sec. 2, Oracle Top-K per query head): idx is [B,Hq,n_idx] and
+ * query head h takes its rows from idx[b,h,:] (still from KV head kvh = h / G).
  * An idx entry of -1 is an empty slot: its rows take no part (z_j = -infinity, weight 0);
  * reading taken for selections of varying size padded to a fixed length (the union of
  * overlapping windows).  An empty selection gives out = 0 and lse = -infinity.
@@ -196,7 +232,7 @@ int oracle_topk(const double* scores, int rows, int N, int k, int32_t* idx) {
 int oracle_gather_attend(const void* q, const void* K, const void* Vv, int dtype,
                          const int32_t* idx, int B, int V, int Hq, int Hkv, int d, int T,
                          int n_idx, int block, double scale, double* out, double* lse,
-                         double* logits) {
+                         double* logits, int per_head) {
     if (Hkv < 1 || Hq % Hkv != 0 || d < 1 || block < 1 || n_idx < 0) return ORC_BAD_ARG;
     if (idx == NULL && n_idx * block != T) return ORC_BAD_ARG;
     const int G = Hq / Hkv;
@@ -217,7 +253,8 @@ int oracle_gather_attend(const void* q, const void* K, const void* Vv, int dtype
                 for (long j = 0; j < n_rows; ++j) {
                     long row = j;
                     if (idx != NULL) {
-                        const long sel = idx[((size_t)b * Hkv + kvh) * n_idx + j / block];
+                        const size_t irow = per_head ? (size_t)b * Hq + h : (size_t)b * Hkv + kvh;
+                        const long sel = idx[irow * n_idx + j / block];
                         row = sel == -1 ? -1 : sel * block + j % block;
                         if (sel != -1 && (sel < 0 || row >= T)) {
                             bad = 1;

@@ -556,3 +556,49 @@ def test_score_accumulate_skips_empty_slots():
     assert np.all(s[0, 32:48] == 0)                              # segment 2: never selected
     np.testing.assert_allclose(s.sum(), Vq * Hq, atol=1e-12)       # every head's weights sum to 1
     np.testing.assert_allclose(s[0, 16:32].sum(), 2.0, atol=1e-12)  # heads 0, 1 -> segment 1 only
+
+
+# ----------------------------------------------------------------------------- per-head selection
+
+
+def test_index_score_heads_are_each_heads_logits():
+    # with the attention query viewed as [B,Hkv,G,d], the per-query scores are every query
+    # head's unscaled logits against its KV head's keys (fp64 einsum)
+    g = torch.Generator().manual_seed(31)
+    B, Hkv, G, N, d = 2, 3, 4, 50, 16
+    q = torch.randn(B, 1, Hkv * G, d, generator=g)
+    K = torch.randn(B, Hkv, N, d, generator=g)
+    s = oracle.index_score_heads(q.reshape(B, Hkv, G, d), K, B, Hkv, G, N, d)
+    ref = torch.einsum("bhd,bhtd->bht", q[:, 0].double(), K.double().repeat_interleave(G, dim=1))
+    np.testing.assert_allclose(s.reshape(B, Hkv * G, N), ref.numpy(), atol=1e-12)
+    # the union score of the shared indexer is their max over the group
+    u = oracle.index_score(q.reshape(B, Hkv, G, d), K, B, Hkv, G, N, d)
+    np.testing.assert_array_equal(u, s.max(axis=2))
+
+
+def test_attend_per_head_uses_each_heads_own_rows():
+    g = torch.Generator().manual_seed(32)
+    B, Vq, Hq, Hkv, d, T, k = 2, 2, 8, 2, 16, 120, 11
+    G = Hq // Hkv
+    q = torch.randn(B, Vq, Hq, d, generator=g)
+    K, V = torch.randn(B, Hkv, T, d, generator=g), torch.randn(B, Hkv, T, d, generator=g)
+    idx = torch.stack([torch.stack([torch.sort(torch.randperm(T, generator=g)[:k]).values
+                                    for _ in range(Hq)]) for _ in range(B)]).to(torch.int32)  # [B,Hq,k]
+    out, lse, logits = oracle.gather_attend(q, K, V, idx.numpy(), B, Vq, Hq, Hkv, d, T, k, 1, 0.3, True,
+                                            per_head=True)
+    for h in range(Hq):
+        kvh = h // G
+        rows = idx[:, h].long()  # [B,k]
+        Kg = torch.gather(K[:, kvh], 1, rows[..., None].expand(B, k, d))[:, None]
+        Vg = torch.gather(V[:, kvh], 1, rows[..., None].expand(B, k, d))[:, None]
+        ro, rl = _sdpa_reference(q[:, :, h:h + 1], Kg, Vg, 0.3)
+        np.testing.assert_allclose(out[:, :, h:h + 1], ro, atol=1e-12)
+        np.testing.assert_allclose(lse[:, :, h:h + 1], rl, atol=1e-12)
+    np.testing.assert_allclose(np.exp(logits - lse[..., None]).sum(-1), 1.0, atol=1e-12)
+    # when every head of a group picks the group's rows, per-head equals the shared selection
+    shared = idx[:, ::G].contiguous()                        # [B,Hkv,k]
+    per = shared.repeat_interleave(G, dim=1).contiguous()    # [B,Hq,k]
+    o1, l1, _ = oracle.gather_attend(q, K, V, shared.numpy(), B, Vq, Hq, Hkv, d, T, k, 1, 0.3)
+    o2, l2, _ = oracle.gather_attend(q, K, V, per.numpy(), B, Vq, Hq, Hkv, d, T, k, 1, 0.3, per_head=True)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)

@@ -27,7 +27,7 @@ EXPORTS = (
     "sd_topk_workspace_bytes", "sd_topk", "sd_gather_attend_workspace_bytes", "sd_gather_attend",
     "sd_score_accumulate", "sd_tier_classify_workspace_bytes", "sd_tier_classify",
     "sd_quantize_rows_int8", "sd_gather_attend_noalloc", "sd_select_attend", "sd_window_count",
-    "sd_window_max", "sd_window_union",
+    "sd_window_max", "sd_window_union", "sd_index_score_heads",
 )
 
 
@@ -47,7 +47,7 @@ class sd_attend_args(ctypes.Structure):
         ("n_idx", ctypes.c_int), ("block", ctypes.c_int), ("scale", ctypes.c_float),
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("logits", ctypes.c_void_p),
         ("err_word", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
-        ("workspace_bytes", ctypes.c_size_t), ("splits", ctypes.c_int),
+        ("workspace_bytes", ctypes.c_size_t), ("splits", ctypes.c_int), ("per_head", ctypes.c_int),
     ]
 
 
@@ -76,6 +76,7 @@ def lib() -> ctypes.CDLL:
         L.sd_gather_attend.argtypes = [ctypes.POINTER(sd_attend_args), P]
         L.sd_gather_attend_noalloc.argtypes = [ctypes.POINTER(sd_attend_args), P]
         L.sd_select_attend.argtypes = [P, I, P, P, ctypes.POINTER(sd_attend_args), P]
+        L.sd_index_score_heads.argtypes = [P, I, P, I, I, I, I, I, I, P, P, P, P]
         L.sd_window_count.argtypes = [I, I, I]
         L.sd_window_count.restype = I
         L.sd_window_max.argtypes = [P, I, I, I, I, P, P, P]
@@ -155,6 +156,26 @@ def sd_index_score(q_idx: torch.Tensor, k_idx: torch.Tensor, scores: Optional[to
     return scores
 
 
+def sd_index_score_heads(q: torch.Tensor, k: torch.Tensor, scores: Optional[torch.Tensor] = None,
+                         err_word: Optional[torch.Tensor] = None, stream=None,
+                         key_hist: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One score row per query row: scores [B,Hkv,V,N] from q [B,Hkv,V,d] and k [B,Hkv,N,d],
+    no max over V.  With the attention query [B,1,Hq,d] viewed as [B,Hkv,G,d] and the
+    attention keys, every query head's unscaled logits ([B,Hq,N] in memory)."""
+    _dev(q, "q")
+    _dev(k, "k")
+    B, Hkv, V, d = q.shape
+    N = k.shape[2]
+    if tuple(k.shape) != (B, Hkv, N, d):
+        raise ValueError("k shape must be [B,Hkv,N,d] matching q")
+    if scores is None:
+        scores = torch.empty((B, Hkv, V, N), dtype=torch.float32, device=k.device)
+    _check(lib().sd_index_score_heads(_ptr(q), _dtype_code(q), _ptr(k), _dtype_code(k), B, Hkv, V, N, d,
+                                      _ptr(scores), _ptr(key_hist), _ptr(err_word), _stream(stream)),
+           "sd_index_score_heads")
+    return scores
+
+
 def sd_block_pool(k_idx: torch.Tensor, block: int, pooled: Optional[torch.Tensor] = None,
                   stream=None) -> torch.Tensor:
     """Mean-pooled block keys [B,Hkv,T/block,dI] fp32 of k_idx [B,Hkv,T,dI]."""
@@ -189,7 +210,7 @@ def sd_topk(scores: torch.Tensor, k: int, idx: Optional[torch.Tensor] = None,
 
 def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=None, scale=None,
                      k_host=None, v_host=None, slot_map=None, out=None, lse=None, logits=None,
-                     want_logits=False, err_word=None, splits=0) -> tuple:
+                     want_logits=False, err_word=None, splits=0, per_head=False) -> tuple:
     """Fill an sd_attend_args from tensors; returns (args, out, lse, logits)."""
     _dev(q, "q")
     B, V, Hq, d = q.shape
@@ -228,6 +249,7 @@ def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=No
     a.logits = logits.data_ptr() if logits is not None else None
     a.err_word = err_word.data_ptr() if err_word is not None else None
     a.splits = splits
+    a.per_head = 1 if per_head else 0
     return a, out, lse, logits
 
 

@@ -40,6 +40,7 @@ struct AttendParams {
     const int32_t* slot_map;
     const int32_t* idx;
     int B, V, Hq, Hkv, G, R, T, pool_rows, n_idx, block, n_rows, rows_per_split, splits;
+    int kv_heads, heads_per_kv;  // KV heads of the cache; groups per KV head (per-head mode: G)
     int dtype;
     int resolve;  // 1: sources resolved up front (idx or slot_map given)
     float scale_log2;
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int bk = b * p.Hkv + kvh;
+    const int kvsrc = b * p.kv_heads + kvh / p.heads_per_kv;  // the (b, KV head) slab the rows come from
     const size_t esz = sizeof(ST);
 
     pdl_wait();  // everything below may read what the preceding kernel wrote
@@ -272,10 +274,10 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
             size_t row;
             if (code >= 0) {
                 base = which ? p.vc : p.kc;
-                row = (size_t)bk * p.pool_rows + code;
+                row = (size_t)kvsrc * p.pool_rows + code;
             } else {
                 base = which ? p.vh : p.kh;
-                row = (size_t)bk * p.T + (size_t)(-1 - (long)code);
+                row = (size_t)kvsrc * p.T + (size_t)(-1 - (long)code);
             }
             cp_async16(dst, base + row * L::kVRow + part * 16);
         }
@@ -531,11 +533,12 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     cp_async_wait<0>();
     __syncthreads();
 
+    const int kvsrc = b * p.kv_heads + kvh / p.heads_per_kv;  // the (b, KV head) slab the rows come from
     RowSource rs;
-    rs.k_pool = p.kc + (size_t)bk * p.pool_rows * (D * 2);
-    rs.v_pool = p.vc + (size_t)bk * p.pool_rows * (D * 2);
-    rs.k_host = p.kh + (size_t)bk * p.T * (D * 2);
-    rs.v_host = p.vh + (size_t)bk * p.T * (D * 2);
+    rs.k_pool = p.kc + (size_t)kvsrc * p.pool_rows * (D * 2);
+    rs.v_pool = p.vc + (size_t)kvsrc * p.pool_rows * (D * 2);
+    rs.k_host = p.kh + (size_t)kvsrc * p.T * (D * 2);
+    rs.v_host = p.vh + (size_t)kvsrc * p.T * (D * 2);
     auto row_code = [&](int j) -> int32_t { return p.resolve ? src[j] : (int32_t)(j0 + j); };
     float* lbase = nullptr;  // logits of query row 0 of this group, at list row j0
     if (p.logits != nullptr) lbase = p.logits + ((size_t)b * p.V * p.Hq + kvh * p.G) * p.n_rows + j0;
@@ -618,8 +621,8 @@ size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 SplitPlan plan_splits(const sd_attend_args* a) {
     SplitPlan sp{};
     const long n_rows = (long)a->n_idx * a->block;
-    const long bk = (long)a->B * a->Hkv;
-    sp.RP = kernel_rows(a->dtype, a->Hkv > 0 ? (a->Hq / a->Hkv) * a->V : 0);
+    const long bk = (long)a->B * (a->per_head ? a->Hq : a->Hkv);
+    sp.RP = kernel_rows(a->dtype, a->per_head ? a->V : (a->Hkv > 0 ? (a->Hq / a->Hkv) * a->V : 0));
     const long chunks = (n_rows + kCH - 1) / kCH;
     const bool resolve = a->idx != nullptr || a->slot_map != nullptr;
     long splits;
@@ -706,11 +709,14 @@ static sd_status validate_attend(const sd_attend_args* a) {
         set_error("sd_gather_attend: d must be 64 or 128 (got %d)", a->d);
         return SD_ERR_UNSUPPORTED;
     }
-    if (kernel_rows(a->dtype, (a->Hq / a->Hkv) * a->V) < 0) {
-        set_error("sd_gather_attend: G*V = %d exceeds 32", (a->Hq / a->Hkv) * a->V);
+    const int rows_per_group = a->per_head ? a->V : (a->Hq / a->Hkv) * a->V;
+    if (kernel_rows(a->dtype, rows_per_group) < 0) {
+        set_error("sd_gather_attend: %d query rows per group exceed 32", rows_per_group);
         return SD_ERR_UNSUPPORTED;
     }
-    SD_REQUIRE(a->B <= 65535 && a->Hkv <= 65535, "sd_gather_attend: B and Hkv must be <= 65535");
+    SD_REQUIRE(a->B <= 65535 && a->Hq <= 65535, "sd_gather_attend: B and Hq must be <= 65535");
+    SD_REQUIRE(a->per_head == 0 || a->per_head == 1, "sd_gather_attend: per_head must be 0 or 1");
+    SD_REQUIRE(!a->per_head || a->idx != nullptr || a->n_idx == 0, "sd_gather_attend: per_head needs idx");
     return SD_OK;
 }
 
@@ -736,8 +742,16 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
     p.B = a->B;
     p.V = a->V;
     p.Hq = a->Hq;
-    p.Hkv = a->Hkv;
-    p.G = a->Hq / a->Hkv;
+    p.kv_heads = a->Hkv;
+    if (a->per_head) {  // one group per query head: G = 1, rows from KV head h / (Hq/Hkv)
+        p.Hkv = a->Hq;
+        p.G = 1;
+        p.heads_per_kv = a->Hq / a->Hkv;
+    } else {
+        p.Hkv = a->Hkv;
+        p.G = a->Hq / a->Hkv;
+        p.heads_per_kv = 1;
+    }
     p.R = p.G * a->V;
     p.T = a->T;
     p.n_idx = a->n_idx;
@@ -772,7 +786,7 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
                    "sd_gather_attend: workspace of %zu bytes needed (got %zu)", sp.ws_bytes,
                    a->workspace_bytes);
         SD_REQUIRE(aligned16(a->workspace), "sd_gather_attend: workspace must be 16-byte aligned");
-        const size_t np = (size_t)a->B * a->Hkv * sp.splits * sp.RP;
+        const size_t np = (size_t)a->B * p.Hkv * sp.splits * sp.RP;
         p.ws_o = static_cast<float*>(a->workspace);
         p.ws_m = p.ws_o + np * a->d;
         p.ws_l = p.ws_m + np;

@@ -58,7 +58,7 @@ SD_DEVINL int reduce_scatter(float (&acc)[kR], int lane) {
 template <typename KT, int DI, int VT>
 __global__ void __launch_bounds__(kIdxThreads, 1) index_score_kernel(
     const void* __restrict__ q_idx, int q_dtype, const KT* __restrict__ k_idx, int rows, int V,
-    int N, float* __restrict__ scores, uint32_t* __restrict__ key_hist, int32_t* err_word) {
+    int N, float* __restrict__ scores, uint32_t* __restrict__ key_hist, int32_t* err_word, int per_query) {
     using U = Unpack16<KT>;
     constexpr int ROWB = DI * (int)sizeof(KT);  // bytes per key row: 128, 256 or 512
     constexpr int LPR = ROWB / 16;              // lanes sharing a row
@@ -140,20 +140,29 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_score_kernel(
         int ridx = 0;
 #pragma unroll
         for (int v = 0; v < VT; ++v) ridx = reduce_scatter<LPR>(acc[v], lane);
-        float best = acc[0][0];
-#pragma unroll
-        for (int v = 1; v < VT; ++v)
-            if (v < V) best = fmaxf(best, acc[v][0]);
         // lanes holding a duplicate of the same row (bits below LPR/8) do not store
         const int row = g + GROUPS * ridx;
         const uint32_t n = min((uint32_t)TR, (uint32_t)N - ct0);
         const bool store = (lane & (LPR / 8 - 1)) == 0 && (uint32_t)row < n;
-        if (store) scores[(size_t)cr * N + ct0 + row] = best;
-        if (key_hist != nullptr) {
-            const uint32_t dg = float_key(best) >> 21;
-            const uint32_t peers = __match_any_sync(0xffffffffu, store ? dg : 0xffffffffu);
-            if (store && lane == __ffs(peers) - 1)
-                atomicAdd(&key_hist[(size_t)cr * 2048 + dg], (uint32_t)__popc(peers));
+        auto put = [&](uint32_t srow, float x) {  // score row srow: store, histogram
+            if (store) scores[(size_t)srow * N + ct0 + row] = x;
+            if (key_hist != nullptr) {
+                const uint32_t dg = float_key(x) >> 21;
+                const uint32_t peers = __match_any_sync(0xffffffffu, store ? dg : 0xffffffffu);
+                if (store && lane == __ffs(peers) - 1)
+                    atomicAdd(&key_hist[(size_t)srow * 2048 + dg], (uint32_t)__popc(peers));
+            }
+        };
+        if (per_query) {
+#pragma unroll
+            for (int v = 0; v < VT; ++v)
+                if (v < V) put(cr * (uint32_t)V + (uint32_t)v, acc[v][0]);
+        } else {
+            float best = acc[0][0];
+#pragma unroll
+            for (int v = 1; v < VT; ++v)
+                if (v < V) best = fmaxf(best, acc[v][0]);
+            put(cr, best);
         }
         __syncwarp();
         if (lane == 0 && i + kWarpStages < ntiles) {
@@ -171,7 +180,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_score_kernel(
 
 template <typename KT, int DI, int VT>
 sd_status launch_index_score(const void* q_idx, int q_dtype, const void* k_idx, int rows, int V,
-                             int N, float* scores, uint32_t* key_hist, int32_t* err_word,
+                             int N, float* scores, uint32_t* key_hist, int32_t* err_word, int per_query,
                              cudaStream_t st) {
     auto kern = index_score_kernel<KT, DI, VT>;
     SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kIdxSmem),
@@ -180,7 +189,7 @@ sd_status launch_index_score(const void* q_idx, int q_dtype, const void* k_idx, 
     const long tiles = (long)rows * ((N + TR - 1) / TR);
     const long grid = std::min<long>((tiles + kIdxWarps - 1) / kIdxWarps, (long)num_sms());
     kern<<<(unsigned)grid, kIdxThreads, kIdxSmem, st>>>(q_idx, q_dtype, reinterpret_cast<const KT*>(k_idx),
-                                                       rows, V, N, scores, key_hist, err_word);
+                                                       rows, V, N, scores, key_hist, err_word, per_query);
     return launch_status("sd_index_score");
 }
 
@@ -200,44 +209,66 @@ __global__ void block_pool_kernel(const KT* __restrict__ k_idx, int dtype, int T
 
 using namespace sd;
 
-extern "C" sd_status sd_index_score(const void* q_idx, sd_dtype q_dtype, const void* k_idx,
-                                    sd_dtype k_dtype, int B, int Hkv, int V, int N, int d_idx,
-                                    float* scores, uint32_t* key_hist, int32_t* err_word,
-                                    void* stream) {
+namespace {
+
+sd_status index_score_common(const char* who, const void* q_idx, sd_dtype q_dtype, const void* k_idx,
+                             sd_dtype k_dtype, int B, int Hkv, int V, int N, int d_idx, float* scores,
+                             uint32_t* key_hist, int32_t* err_word, int per_query, void* stream) {
     clear_error();
-    SD_REQUIRE(B >= 0 && Hkv >= 0 && N >= 0, "sd_index_score: negative size");
-    SD_REQUIRE(valid_dtype(q_dtype) && valid_dtype(k_dtype), "sd_index_score: bad dtype");
-    SD_REQUIRE(V >= 1 && V <= 8, "sd_index_score: V must be in [1, 8] (got %d)", V);
+    SD_REQUIRE(B >= 0 && Hkv >= 0 && N >= 0, "%s: negative size", who);
+    SD_REQUIRE(valid_dtype(q_dtype) && valid_dtype(k_dtype), "%s: bad dtype", who);
+    const bool tc = k_dtype == SD_BF16 && q_dtype == SD_BF16;
+    const int vmax = per_query && tc ? 16 : 8;
+    SD_REQUIRE(V >= 1 && V <= vmax, "%s: V must be in [1, %d] (got %d)", who, vmax, V);
     if (d_idx != 64 && d_idx != 128) {
-        set_error("sd_index_score: d_idx must be 64 or 128 (got %d)", d_idx);
+        set_error("%s: d_idx must be 64 or 128 (got %d)", who, d_idx);
         return SD_ERR_UNSUPPORTED;
     }
     const long rows = (long)B * Hkv;
     if (rows == 0 || N == 0) return SD_OK;
-    SD_REQUIRE(q_idx && k_idx && scores, "sd_index_score: null pointer");
-    SD_REQUIRE(aligned16(k_idx) && aligned16(scores), "sd_index_score: pointers must be 16-byte aligned");
-    SD_REQUIRE(rows <= (1L << 30) && rows * (long)N < (1L << 36), "sd_index_score: too many rows");
+    SD_REQUIRE(q_idx && k_idx && scores, "%s: null pointer", who);
+    SD_REQUIRE(aligned16(k_idx) && aligned16(scores), "%s: pointers must be 16-byte aligned", who);
+    SD_REQUIRE(rows <= (1L << 30) && rows * (per_query ? V : 1) * (long)N < (1L << 36), "%s: too many rows", who);
     cudaStream_t st = as_stream(stream);
     const int r = (int)rows;
     // bf16 keys and queries: the contraction runs on the tensor cores (exact for the
     // integer-valued indexer: products exact, fp32 sums of integers below 2^24 exact)
-    if (k_dtype == SD_BF16 && q_dtype == SD_BF16) {
-        SD_REQUIRE(aligned16(q_idx), "sd_index_score: q_idx must be 16-byte aligned");
-        SD_REQUIRE((long)rows * N < (1L << 31) && (long)rows * V < (1L << 31), "sd_index_score: too many rows");
-        return index_score_tc_launch(q_idx, k_idx, r, V, N, d_idx, scores, key_hist, err_word, st);
+    if (tc) {
+        SD_REQUIRE(aligned16(q_idx), "%s: q must be 16-byte aligned", who);
+        SD_REQUIRE((long)rows * N * (per_query ? V : 1) < (1L << 31) && (long)rows * V < (1L << 31),
+                   "%s: too many rows", who);
+        return index_score_tc_launch(q_idx, k_idx, r, V, N, d_idx, scores, key_hist, err_word, per_query, st);
     }
+    const int pq = per_query;
     if (k_dtype == SD_BF16) {
         if (d_idx == 128)
-            return V == 1 ? launch_index_score<bf16_t, 128, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st)
-                          : launch_index_score<bf16_t, 128, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st);
-        return V == 1 ? launch_index_score<bf16_t, 64, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st)
-                      : launch_index_score<bf16_t, 64, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st);
+            return V == 1 ? launch_index_score<bf16_t, 128, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, pq, st)
+                          : launch_index_score<bf16_t, 128, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, pq, st);
+        return V == 1 ? launch_index_score<bf16_t, 64, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, pq, st)
+                      : launch_index_score<bf16_t, 64, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, pq, st);
     }
     if (d_idx == 128)
-        return V == 1 ? launch_index_score<float, 128, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st)
-                      : launch_index_score<float, 128, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st);
-    return V == 1 ? launch_index_score<float, 64, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st)
-                  : launch_index_score<float, 64, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, st);
+        return V == 1 ? launch_index_score<float, 128, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, pq, st)
+                      : launch_index_score<float, 128, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, pq, st);
+    return V == 1 ? launch_index_score<float, 64, 1>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, pq, st)
+                  : launch_index_score<float, 64, 8>(q_idx, q_dtype, k_idx, r, V, N, scores, key_hist, err_word, pq, st);
+}
+
+}  // namespace
+
+extern "C" sd_status sd_index_score(const void* q_idx, sd_dtype q_dtype, const void* k_idx,
+                                    sd_dtype k_dtype, int B, int Hkv, int V, int N, int d_idx,
+                                    float* scores, uint32_t* key_hist, int32_t* err_word,
+                                    void* stream) {
+    return index_score_common("sd_index_score", q_idx, q_dtype, k_idx, k_dtype, B, Hkv, V, N, d_idx, scores,
+                              key_hist, err_word, 0, stream);
+}
+
+extern "C" sd_status sd_index_score_heads(const void* q, sd_dtype q_dtype, const void* k, sd_dtype k_dtype, int B,
+                                          int Hkv, int V, int N, int d, float* scores, uint32_t* key_hist,
+                                          int32_t* err_word, void* stream) {
+    return index_score_common("sd_index_score_heads", q, q_dtype, k, k_dtype, B, Hkv, V, N, d, scores, key_hist,
+                              err_word, 1, stream);
 }
 
 extern "C" sd_status sd_block_pool(const void* k_idx, sd_dtype k_dtype, int B, int Hkv, int T,

@@ -14,8 +14,9 @@
 //               tile, then commits to the stage's "empty" barrier and the accumulator's
 //               "full" barrier;
 //   warps 0-3   epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 tokens x 16 columns),
-//               max over the V real query columns, coalesced score store, optional fused
-//               histogram of the score's top 11 order-key bits; then free the accumulator.
+//               max over the V real query columns (or, per query, every column to its own
+//               score row), coalesced score store, optional fused histogram of the score's
+//               top 11 order-key bits; then free the accumulator.
 // Query rows past V (the next group's queries, or zero fill past the end) only produce
 // accumulator columns that are never read.  Tokens past N in a tile are never stored.
 // Every wait is bounded; a wait that runs out raises an abort flag that the other roles
@@ -51,7 +52,7 @@ struct TcLayout {
 template <int DI>
 __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, int rows,
-    int V, int N, float* __restrict__ scores, uint32_t* __restrict__ key_hist, int32_t* err_word) {
+    int V, int N, float* __restrict__ scores, uint32_t* __restrict__ key_hist, int32_t* err_word, int per_query) {
     using L = TcLayout<DI>;
     extern __shared__ uint8_t smem_raw[];
     // the 128-byte swizzle layout needs 1024-byte aligned tiles
@@ -161,18 +162,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(
             tc_fence_after_sync();
             float v[16];
             tmem_ld16(tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)buf * kQN, v);
-            float best = v[0];
-#pragma unroll
-            for (int j = 1; j < 16; ++j)
-                if (j < V) best = fmaxf(best, v[j]);
             const uint32_t tok = t0 + (uint32_t)(warp * 32 + lane);
             const bool store = tok < (uint32_t)N;
-            if (store) scores[(size_t)r * N + tok] = best;
-            if (key_hist != nullptr) {
-                const uint32_t dg = float_key(best) >> 21;
-                const uint32_t peers = __match_any_sync(0xffffffffu, store ? dg : 0xffffffffu);
-                if (store && lane == __ffs(peers) - 1)
-                    atomicAdd(&key_hist[(size_t)r * 2048 + dg], (uint32_t)__popc(peers));
+            auto put = [&](uint32_t srow, float x) {  // score row srow: store, histogram
+                if (store) scores[(size_t)srow * N + tok] = x;
+                if (key_hist != nullptr) {
+                    const uint32_t dg = float_key(x) >> 21;
+                    const uint32_t peers = __match_any_sync(0xffffffffu, store ? dg : 0xffffffffu);
+                    if (store && lane == __ffs(peers) - 1)
+                        atomicAdd(&key_hist[(size_t)srow * 2048 + dg], (uint32_t)__popc(peers));
+                }
+            };
+            if (per_query) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (j < V) put(r * (uint32_t)V + (uint32_t)j, v[j]);
+            } else {
+                float best = v[0];
+#pragma unroll
+                for (int j = 1; j < 16; ++j)
+                    if (j < V) best = fmaxf(best, v[j]);
+                put(r, best);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -222,9 +232,10 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t nrows, int d, int box_r
 
 }  // namespace
 
-// bf16 keys and bf16 queries on the tensor cores; d_idx in {64, 128}, V <= 8.
+// bf16 keys and bf16 queries on the tensor cores; d_idx in {64, 128}, V <= 16.  per_query:
+// every query row gets its own score row (rows*V of them) instead of the max over V.
 sd_status index_score_tc_launch(const void* q_idx, const void* k_idx, int rows, int V, int N, int d_idx,
-                                float* scores, uint32_t* key_hist, int32_t* err_word, cudaStream_t st) {
+                                float* scores, uint32_t* key_hist, int32_t* err_word, int per_query, cudaStream_t st) {
     CUtensorMap kmap, qmap;
     if (!make_map(&kmap, k_idx, (uint64_t)rows * N, d_idx, kTileM) ||
         !make_map(&qmap, q_idx, (uint64_t)rows * V, d_idx, kQN)) {
@@ -239,13 +250,13 @@ sd_status index_score_tc_launch(const void* q_idx, const void* k_idx, int rows, 
         SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcLayout<128>::kBytes),
                       "sd_index_score: cudaFuncSetAttribute");
         kern<<<(unsigned)grid, kTcThreads, TcLayout<128>::kBytes, st>>>(kmap, qmap, rows, V, N, scores, key_hist,
-                                                                       err_word);
+                                                                       err_word, per_query);
     } else {
         auto kern = index_score_tc_kernel<64>;
         SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcLayout<64>::kBytes),
                       "sd_index_score: cudaFuncSetAttribute");
         kern<<<(unsigned)grid, kTcThreads, TcLayout<64>::kBytes, st>>>(kmap, qmap, rows, V, N, scores, key_hist,
-                                                                      err_word);
+                                                                      err_word, per_query);
     }
     return launch_status("sd_index_score (tensor cores)");
 }

@@ -41,7 +41,7 @@ inline sd_status launch_status(const char* what) {
 
 // The indexer on the tensor cores (index_score_tc.cu): bf16 keys and queries.
 sd_status index_score_tc_launch(const void* q_idx, const void* k_idx, int rows, int V, int N, int d_idx,
-                                float* scores, uint32_t* key_hist, int32_t* err_word, cudaStream_t st);
+                                float* scores, uint32_t* key_hist, int32_t* err_word, int per_query, cudaStream_t st);
 
 // Launches `kern` as a programmatic dependent of the preceding kernel in the stream: it
 // may be scheduled before that kernel finishes and must call pdl_wait() before reading

@@ -1016,6 +1016,10 @@ extern "C" sd_status sd_select_attend(const float* scores, int N, uint32_t* key_
         return SD_ERR_UNSUPPORTED;
     }
     SD_REQUIRE(a->splits >= 0 && a->splits <= kSaMaxCluster, "sd_select_attend: splits must be in [0, 8]");
+    if (a->per_head) {
+        set_error("sd_select_attend: per-head selections go through sd_topk + sd_gather_attend");
+        return SD_ERR_UNSUPPORTED;
+    }
     if (a->B == 0) return SD_OK;
     SD_REQUIRE(scores && a->q && a->out && a->lse && (k == 0 || idx), "sd_select_attend: null pointer");
     SD_REQUIRE(aligned16(a->q) && aligned16(a->out), "sd_select_attend: q and out must be 16-byte aligned");

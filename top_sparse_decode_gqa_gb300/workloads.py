@@ -6,7 +6,7 @@ it.  Every tensor is drawn on the host from one CPU ``torch.Generator`` seeded w
 ``1000 + cfg_id``, in a fixed order (indexer query, indexer keys, attention query, K, V,
 planted positions and values, residency), so any two consumers see the same bytes.
 
-The five workloads are the shapes the source pages benchmark on, with synthetic values in
+The workloads are the shapes the source pages benchmark on, with synthetic values in
 place of trained models and datasets (which the pages evaluate on and which are not
 available here):
 
@@ -26,6 +26,10 @@ available here):
   compression-window grid (windows of 32 tokens every 16): token scores max-pooled onto
   2047 windows, top-64 windows per KV head, attention over their union (at most 2048
   tokens, as 16-token segments).
+* ``c7_head_topk``: the layer of ``c2`` with selection per query head: each head's own
+  unscaled attention logits against its KV head's keys score the tokens, each head keeps
+  its own top-1024 and attends over those rows only (the indexer tensors are drawn, to keep
+  the draw order, but not used).
 
 Value recipe: indexer query and keys are integers drawn uniformly from [-8, 8] (exact in
 bf16 and fp32); attention q, K, V are standard normal, rounded to bf16 (nearest even)
@@ -65,6 +69,7 @@ class Workload:
     steps: int = 1
     window_kernel: int = 0  # > 0: select compression windows of this many tokens ...
     window_stride: int = 0  # ... moved by this many (k counts windows)
+    per_head: bool = False  # select per query head from the attention logits (k per head)
     cum_frac: tuple = (0.2, 0.6, 0.9)
     n_sink: int = 0
     n_recent: int = 0
@@ -129,6 +134,9 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("c6_window_blocks", 5, B=8, V=1, Hq=32, Hkv=8, d=128, T=32768, dtype="bf16",
                  dI=128, k=64, planted=655, planted_values="five_to_eight", planted_attn_boost=0.5,
                  window_kernel=32, window_stride=16),
+        Workload("c7_head_topk", 6, B=8, V=1, Hq=32, Hkv=8, d=128, T=32768, dtype="bf16",
+                 dI=128, k=1024, planted=655, planted_values="five_to_eight", planted_attn_boost=0.5,
+                 per_head=True),
     )
 }
 
