@@ -115,6 +115,9 @@ def test_topk_float_scores_and_signed_zero():
     (3, 1, 3, 777, 13, False),
     (2, 3, 1, 2048, 64, False),       # block-selection shape: static + dynamic smem > 48 KB
     (1, 2, 1, 12000, 50, False),      # N between the cached and uncached sizes
+    (8, 32, 1, 4096 + 5, 300, False),  # more rows than SMs: the 512-thread variant
+    (10, 16, 1, 3000, 100, True),     # ... and its full-pass fallback
+    (4, 40, 2, 2048, 2047, False),
 ])
 def test_index_topk_with_key_histogram(B, Hkv, V, N, k, flat):
     g = torch.Generator().manual_seed(N + k)

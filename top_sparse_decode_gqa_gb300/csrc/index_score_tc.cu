@@ -5,18 +5,21 @@
 // verify queries sharing the selection the scores of a tile of 128 tokens are a small
 // dense contraction, S[128 x V] = K_tile[128 x d] . Q[V x d]^T, followed by a max over V.
 //
-// Warp roles in a persistent CTA (one per SM), over 128-token tiles dealt round-robin:
-//   warp 4      TMA producer: per tile one mbarrier-completed stage of the 4-stage ring
+// Warp roles in a persistent CTA (one per SM), over 128-token tiles dealt round-robin,
+// with E epilogue warpgroups (E = 1, or more when every query column is a score row of its
+// own and the epilogue has V times the stores and histogram updates per tile):
+//   warp 4E     TMA producer: per tile one mbarrier-completed stage of the 4-stage ring
 //               holding the key tile (d/64 boxes of 128 rows x 64 bf16, 128-byte swizzle)
 //               and the 16 query rows starting at the tile's first query (same layout);
-//   warp 5      MMA issuer: allocates 32 TMEM columns (two 16-column fp32 accumulators),
+//   warp 4E+1   MMA issuer: allocates 32E TMEM columns (2E 16-column fp32 accumulators),
 //               issues d/16 tcgen05.mma (M = 128 tokens, N = 16 query rows, K = 16) per
 //               tile, then commits to the stage's "empty" barrier and the accumulator's
 //               "full" barrier;
-//   warps 0-3   epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 tokens x 16 columns),
-//               max over the V real query columns (or, per query, every column to its own
-//               score row), coalesced score store, optional fused histogram of the score's
-//               top 11 order-key bits; then free the accumulator.
+//   warps 0..4E-1  epilogue, warpgroup e taking tiles i = e mod E: tcgen05.ld of the
+//               warp's 32 TMEM lanes (= 32 tokens x 16 columns), which frees the
+//               accumulator, then the max over the V real query columns (or, per query,
+//               every column to its own score row), coalesced score store and optional
+//               fused histogram of the score's top 11 order-key bits.
 // Query rows past V (the next group's queries, or zero fill past the end) only produce
 // accumulator columns that are never read.  Tokens past N in a tile are never stored.
 // Every wait is bounded; a wait that runs out raises an abort flag that the other roles
@@ -29,13 +32,15 @@
 namespace sd {
 namespace {
 
-constexpr int kTcThreads = 192;
 constexpr int kTileM = 128;   // tokens per tile
 constexpr int kQN = 16;       // query rows per MMA (N)
 constexpr int kTcStages = 4;
 constexpr int kAtomA = kTileM * 128;  // one 64-element K slice of the key tile: 16 KB
 constexpr int kAtomB = kQN * 128;     // one 64-element K slice of the query tile: 2 KB
-constexpr uint32_t kTmemCols = 32;
+
+// Epilogue warpgroups: the shared score (max over V) needs one; per-query scores have V
+// stores and histogram updates per token.
+int tc_epilogue_groups(int V, int per_query) { return !per_query || V == 1 ? 1 : V == 2 ? 2 : 4; }
 
 template <int DI>
 struct TcLayout {
@@ -44,16 +49,19 @@ struct TcLayout {
     static constexpr int kStageB = kAtoms * kAtomB;
     static constexpr int kStage = kStageA + kStageB;
     static constexpr int oBars = kTcStages * kStage;              // 1024-aligned stages first
-    static constexpr int kBars = 2 * kTcStages + 4;                // full, empty, tfull[2], tempty[2]
+    static constexpr int kBars = 2 * kTcStages + 8;                // full, empty, tfull[<=4], tempty[<=4]
     static constexpr int oMisc = oBars + kBars * 8;                // tmem slot, abort flag, consumed
     static constexpr int kBytes = oMisc + 16 + 1024;               // + alignment slack
 };
 
-template <int DI>
-__global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(
+template <int DI, int E>
+__global__ void __launch_bounds__(32 * (4 * E + 2), 1) index_score_tc_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, int rows,
     int V, int N, float* __restrict__ scores, uint32_t* __restrict__ key_hist, int32_t* err_word, int per_query) {
     using L = TcLayout<DI>;
+    constexpr int NB = 2 * E;                   // accumulators (16 TMEM columns each)
+    constexpr uint32_t kTmemCols = 32u * E;     // a power of two >= 32
+    constexpr int kProducer = 4 * E, kIssuer = 4 * E + 1;
     extern __shared__ uint8_t smem_raw[];
     // the 128-byte swizzle layout needs 1024-byte aligned tiles
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -61,7 +69,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::oBars);
     uint64_t* empty = full + kTcStages;
     uint64_t* tfull = empty + kTcStages;
-    uint64_t* tempty = tfull + 2;
+    uint64_t* tempty = tfull + NB;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::oMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::oMisc + 4);
     volatile uint32_t* consumed = reinterpret_cast<volatile uint32_t*>(smem + L::oMisc + 8);
@@ -83,7 +91,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NB; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], 4);  // one arrive per epilogue warp
         }
@@ -91,7 +99,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(
         *consumed = 0;
         fence_mbarrier_init();
     }
-    if (warp == 5) tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == kIssuer) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -99,7 +107,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(
     pdl_launch_dependents();
 
     uint32_t issued = 0;
-    if (warp == 4) {
+    if (warp == kProducer) {
         if (lane == 0) {
             // keys are read once: evict them first, so the scores written meanwhile stay in L2
             const uint64_t stream_policy = l2_evict_first_policy();
@@ -122,14 +130,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(
                 ++issued;
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kIssuer) {
         if (lane == 0) {
             constexpr uint32_t idesc = umma_idesc_bf16_f32(kTileM, kQN);
             for (uint32_t i = 0; i < ntiles; ++i) {
                 const int s = (int)(i % kTcStages);
-                const int buf = (int)(i & 1u);
+                const int buf = (int)(i % NB);
                 if (!mbar_wait(&full[s], (i / kTcStages) & 1u) ||
-                    !mbar_wait(&tempty[buf], ((i >> 1) & 1u) ^ 1u) || *abort_flag) {
+                    !mbar_wait(&tempty[buf], ((i / NB) & 1u) ^ 1u) || *abort_flag) {
                     *abort_flag = 1;
                     break;
                 }
@@ -149,20 +157,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(
             }
         }
     } else {
-        // epilogue: warp w reads TMEM lanes [32w, 32w + 32) = tokens t0 + 32w + lane
-        for (uint32_t i = 0; i < ntiles; ++i) {
-            const int buf = (int)(i & 1u);
+        // epilogue: warp w reads TMEM lanes [32q, 32q + 32), q = w mod 4 = tokens t0 + 32q + lane
+        const int quarter = warp & 3;
+        for (uint32_t i = (uint32_t)(warp >> 2); i < ntiles; i += E) {
+            const int buf = (int)(i % NB);
             uint32_t r, t0;
             tile_pos(i, r, t0);
-            const bool ok = mbar_wait(&tfull[buf], (i >> 1) & 1u);
+            const bool ok = mbar_wait(&tfull[buf], (i / NB) & 1u);
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
                 *abort_flag = 1;
                 break;
             }
             tc_fence_after_sync();
             float v[16];
-            tmem_ld16(tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)buf * kQN, v);
-            const uint32_t tok = t0 + (uint32_t)(warp * 32 + lane);
+            tmem_ld16(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)buf * kQN, v);
+            // the values are in registers: hand the accumulator back to the MMA issuer
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[buf]);
+            const uint32_t tok = t0 + (uint32_t)(quarter * 32 + lane);
             const bool store = tok < (uint32_t)N;
             auto put = [&](uint32_t srow, float x) {  // score row srow: store, histogram
                 if (store) scores[(size_t)srow * N + tok] = x;
@@ -184,19 +197,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(
                     if (j < V) best = fmaxf(best, v[j]);
                 put(r, best);
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[buf]);
         }
     }
     __syncthreads();
-    if (tid == 128 && *abort_flag) {
+    if (tid == 0 && *abort_flag) {
         report(err_word, SD_DEVERR_TIMEOUT);
         // let the stages the producer filled but no MMA consumed land before exiting
         for (uint32_t j = *consumed; j < issued; ++j) mbar_wait(&full[j % kTcStages], (j / kTcStages) & 1u);
     }
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kIssuer) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, kTmemCols);
     }
@@ -244,20 +254,17 @@ sd_status index_score_tc_launch(const void* q_idx, const void* k_idx, int rows, 
     }
     const uint32_t tpr = (uint32_t)((N + kTileM - 1) / kTileM);
     const long tiles = (long)rows * tpr;
-    const long grid = std::min<long>(tiles, (long)num_sms());
-    if (d_idx == 128) {
-        auto kern = index_score_tc_kernel<128>;
-        SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcLayout<128>::kBytes),
-                      "sd_index_score: cudaFuncSetAttribute");
-        kern<<<(unsigned)grid, kTcThreads, TcLayout<128>::kBytes, st>>>(kmap, qmap, rows, V, N, scores, key_hist,
-                                                                       err_word, per_query);
-    } else {
-        auto kern = index_score_tc_kernel<64>;
-        SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcLayout<64>::kBytes),
-                      "sd_index_score: cudaFuncSetAttribute");
-        kern<<<(unsigned)grid, kTcThreads, TcLayout<64>::kBytes, st>>>(kmap, qmap, rows, V, N, scores, key_hist,
-                                                                      err_word, per_query);
-    }
+    const unsigned grid = (unsigned)std::min<long>(tiles, (long)num_sms());
+    const int E = tc_epilogue_groups(V, per_query);
+    const bool d128 = d_idx == 128;
+    auto kern = d128 ? (E == 1 ? index_score_tc_kernel<128, 1> : E == 2 ? index_score_tc_kernel<128, 2>
+                                                                        : index_score_tc_kernel<128, 4>)
+                     : (E == 1 ? index_score_tc_kernel<64, 1> : E == 2 ? index_score_tc_kernel<64, 2>
+                                                                       : index_score_tc_kernel<64, 4>);
+    const int bytes = d128 ? TcLayout<128>::kBytes : TcLayout<64>::kBytes;
+    SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+                  "sd_index_score: cudaFuncSetAttribute");
+    kern<<<grid, 32 * (4 * E + 2), bytes, st>>>(kmap, qmap, rows, V, N, scores, key_hist, err_word, per_query);
     return launch_status("sd_index_score (tensor cores)");
 }
 

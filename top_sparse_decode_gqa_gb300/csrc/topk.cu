@@ -5,8 +5,9 @@
 // scoring tokens; SparDA (gist.science summary), sec. 2 item 1, selects top-k blocks the
 // same way.  The pages are silent on ties; the lower index wins.
 //
-// One 1024-thread CTA per row.  Scores become order-preserving uint32 keys (kept in
-// shared memory when the row fits).  A radix select with 11/11/10-bit digits finds the
+// One CTA per row (1024 threads; 512 threads, two CTAs per SM, when the rows outnumber
+// the SMs and the first digit's histogram is given).  Scores become order-preserving
+// uint32 keys (kept in shared memory when the row fits and several passes read it).  A radix select with 11/11/10-bit digits finds the
 // k-th largest key `thr` and how many entries equal to it are still needed (`krem`).  A
 // final ordered pass gives each warp a contiguous segment of the row: per-warp counts,
 // a 32-entry scan, and warp ballots emit every key > thr and the first krem keys == thr
@@ -19,11 +20,12 @@
 namespace sd {
 namespace {
 
-constexpr int kTkThreads = 1024;
+constexpr int kTkThreads = 1024;  // threads of the plain kernel, and the most any variant has
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kHistBins = 2048;
 
-// Block-wide inclusive prefix sum of one value per thread (1024 threads).
+// Block-wide inclusive prefix sum of one value per thread (NT threads).
+template <int NT>
 SD_DEVINL uint32_t block_inclusive_scan(uint32_t v, uint32_t* wsum) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -34,7 +36,7 @@ SD_DEVINL uint32_t block_inclusive_scan(uint32_t v, uint32_t* wsum) {
     if (lane == 31) wsum[warp] = v;
     __syncthreads();
     if (warp == 0) {
-        uint32_t w = wsum[lane];
+        uint32_t w = lane < NT / 32 ? wsum[lane] : 0u;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t n = __shfl_up_sync(0xffffffffu, w, o);
@@ -58,17 +60,18 @@ struct TopkShared {
 // Given the histogram of one digit (nb bins, higher bins = larger keys) of the entries
 // still in the running, pick the digit holding the krem-th largest: returns it and how
 // many of those entries lie in higher bins.  Thread t owns bins [nb - per*(t+1), nb - per*t).
+template <int NT>
 SD_DEVINL void select_digit(TopkShared& sh, uint32_t nb, int krem, uint32_t& digit, uint32_t& above) {
     const int tid = threadIdx.x;
     if (tid == 0) {  // defined even if no bin crosses (a histogram that does not match)
         sh.sel_digit = 0;
         sh.sel_above = 0;
     }
-    const int per = (int)nb / kTkThreads;
+    const int per = (int)nb / NT;
     const int hi = (int)nb - per * tid;
     uint32_t local = 0;
     for (int b = hi - per; b < hi; ++b) local += sh.hist[b];
-    const uint32_t incl = block_inclusive_scan(local, sh.wsum);
+    const uint32_t incl = block_inclusive_scan<NT>(local, sh.wsum);
     const uint32_t excl = incl - local;
     if (excl < (uint32_t)krem && (uint32_t)krem <= incl) {
         uint32_t acc = excl;
@@ -89,13 +92,13 @@ SD_DEVINL void select_digit(TopkShared& sh, uint32_t nb, int krem, uint32_t& dig
 
 // Histogram pass over all N keys: counts the digit (kk >> shift) & (nb - 1) of every key
 // whose bits under pmask equal prefix (warp-aggregated shared atomics).
-template <typename KeyAt>
+template <int NT, typename KeyAt>
 SD_DEVINL void hist_pass_all(TopkShared& sh, KeyAt key_at, int N, uint32_t prefix, uint32_t pmask,
                              int shift, uint32_t nb) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int b = tid; b < kHistBins; b += kTkThreads) sh.hist[b] = 0;
+    for (int b = tid; b < kHistBins; b += NT) sh.hist[b] = 0;
     __syncthreads();
-    for (int base = warp * 32; base < N; base += kTkThreads) {
+    for (int base = warp * 32; base < N; base += NT) {
         const int i = base + lane;
         const bool valid = i < N;
         const uint32_t kk = valid ? key_at(i) : 0u;
@@ -109,11 +112,12 @@ SD_DEVINL void hist_pass_all(TopkShared& sh, KeyAt key_at, int N, uint32_t prefi
 
 // Ordered emit: every key > thr and the first krem keys == thr (lowest indices), written
 // in ascending index order.  Warp w scans the contiguous segment [w*seg, (w+1)*seg).
-template <typename KeyAt>
+template <int NT, typename KeyAt>
 SD_DEVINL void emit_selected(TopkShared& sh, KeyAt key_at, int N, int k, uint32_t thr, int krem,
                              int32_t* orow) {
+    constexpr int NWP = NT / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int seg = ((N + kTkWarps - 1) / kTkWarps + 31) / 32 * 32;
+    const int seg = ((N + NWP - 1) / NWP + 31) / 32 * 32;
     const int s0 = warp * seg, s1 = min(N, s0 + seg);
     uint32_t gt = 0, eq = 0;
     for (int base = s0; base < s1; base += 32) {
@@ -130,7 +134,7 @@ SD_DEVINL void emit_selected(TopkShared& sh, KeyAt key_at, int N, int k, uint32_
     __syncthreads();
     if (tid == 0) {
         uint32_t eqb = 0, ob = 0;
-        for (int w = 0; w < kTkWarps; ++w) {
+        for (int w = 0; w < NWP; ++w) {
             sh.eq_before[w] = eqb;
             const int take = max(0, min((int)sh.cnt_eq[w], krem - (int)eqb));
             sh.base_out[w] = ob;
@@ -223,22 +227,30 @@ __global__ void __launch_bounds__(kTkThreads, 1)
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
         const uint32_t nb = pass == 2 ? 1024u : 2048u;
-        hist_pass_all(sh, key_at, N, prefix, pmask, kShift[pass], nb);
+        hist_pass_all<kTkThreads>(sh, key_at, N, prefix, pmask, kShift[pass], nb);
         uint32_t dg, above;
-        select_digit(sh, nb, krem, dg, above);
+        select_digit<kTkThreads>(sh, nb, krem, dg, above);
         prefix |= dg << kShift[pass];
         pmask |= (nb - 1) << kShift[pass];
         krem -= (int)above;
     }
-    emit_selected(sh, key_at, N, k, prefix, krem, orow);
+    emit_selected<kTkThreads>(sh, key_at, N, k, prefix, krem, orow);
 }
 
 constexpr int kCandCap = 4096;
 
+// Bits 0..7 of x moved to bits 0, 4, ..., 28 (the others cleared).
+SD_DEVINL uint32_t spread8(uint32_t x) {
+    x = (x | (x << 12)) & 0x000F000Fu;
+    x = (x | (x << 6)) & 0x03030303u;
+    return (x | (x << 3)) & 0x11111111u;
+}
+
 // Block-wide exclusive prefix sum of one value per thread; also returns the total.
+template <int NT>
 SD_DEVINL uint32_t block_exclusive_scan(uint32_t v, uint32_t* wsum, uint32_t& total) {
-    const uint32_t incl = block_inclusive_scan(v, wsum);
-    if ((int)threadIdx.x == kTkThreads - 1) wsum[0] = incl;
+    const uint32_t incl = block_inclusive_scan<NT>(v, wsum);
+    if ((int)threadIdx.x == NT - 1) wsum[0] = incl;
     __syncthreads();
     total = wsum[0];
     __syncthreads();
@@ -246,23 +258,24 @@ SD_DEVINL uint32_t block_exclusive_scan(uint32_t v, uint32_t* wsum, uint32_t& to
 }
 
 // Histogram-seeded variant, bitmap emit.  The first digit's histogram comes from
-// sd_index_score and picks the top digit d0.  One pass over the row (staged in shared
-// memory when it fits) marks every entry whose digit is above d0 in a selection bitmap
-// (a warp's 32 consecutive entries = one bitmap word, written from a ballot) and collects
-// the entries of digit d0 (candidates, with their indices).  The last 21 bits are resolved
+// sd_index_score and picks the top digit d0.  One pass over the row, read straight from
+// global memory (the scores were just written, so mostly from L2), marks every entry whose
+// digit is above d0 in a selection bitmap (a warp's 32 consecutive entries = one bitmap
+// word, written from a ballot) and collects the entries of digit d0 (candidates, with their
+// indices; a warp reserves the slots of 8 words with one shared atomic).  The last 21 bits are resolved
 // among the candidates; candidates above the threshold join the bitmap, those equal to it
 // go to a tie bitmap of which a prefix scan keeps the lowest-index ones still needed; a
 // prefix scan over the selection bitmap writes the indices in ascending order.  Falls back
 // to full passes when the candidates exceed their buffer.  Leaves the histogram zeroed.
-__global__ void __launch_bounds__(kTkThreads, 1)
+template <int NT>
+__global__ void __launch_bounds__(NT, kTkThreads / NT)
     topk_hist_kernel(const float* __restrict__ scores, int N, int k, int32_t* __restrict__ idx_out,
-                     uint32_t* __restrict__ key_hist, int cache_keys, int32_t* err_word) {
+                     uint32_t* __restrict__ key_hist) {
+    constexpr int NWP = NT / 32;
     extern __shared__ __align__(16) uint32_t dyn[];
     __shared__ TopkShared sh;
-    __shared__ __align__(8) uint64_t stage_bar;
     const int NW = (N + 31) / 32;  // bitmap words
-    uint32_t* keys_s = dyn;
-    uint32_t* cand_key = dyn + (cache_keys ? N : 0);
+    uint32_t* cand_key = dyn;
     uint32_t* cand_idx = cand_key + kCandCap;
     uint32_t* sel = cand_idx + kCandCap;
     uint32_t* tie = sel + NW;
@@ -272,11 +285,11 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     uint32_t* hrow = key_hist + (size_t)blockIdx.x * kHistBins;
     pdl_wait();
     pdl_launch_dependents();
-    for (int b = tid; b < kHistBins; b += kTkThreads) {
+    for (int b = tid; b < kHistBins; b += NT) {
         sh.hist[b] = hrow[b];
         hrow[b] = 0u;
     }
-    for (int w = tid; w < NW; w += kTkThreads) {
+    for (int w = tid; w < NW; w += NT) {
         sel[w] = 0u;
         tie[w] = 0u;
     }
@@ -284,16 +297,12 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     __syncthreads();
     if (k == 0) return;
     if (k == N) {
-        for (int i = tid; i < N; i += kTkThreads) orow[i] = i;
+        for (int i = tid; i < N; i += NT) orow[i] = i;
         return;
     }
-    if (cache_keys && !stage_keys(srow, N, keys_s, &stage_bar)) {
-        if (tid == 0) report(err_word, SD_DEVERR_TIMEOUT);
-        return;
-    }
-    auto key_at = [&](int i) -> uint32_t { return float_key(cache_keys ? __uint_as_float(keys_s[i]) : srow[i]); };
+    auto key_at = [&](int i) -> uint32_t { return float_key(__ldcg(srow + i)); };
     uint32_t d0, above;
-    select_digit(sh, 2048u, k, d0, above);
+    select_digit<NT>(sh, 2048u, k, d0, above);
     d0 &= (kHistBins - 1);
     int krem = k - (int)above;
     if (sh.hist[d0] > (uint32_t)kCandCap) {
@@ -302,48 +311,100 @@ __global__ void __launch_bounds__(kTkThreads, 1)
 #pragma unroll 1
         for (int pass = 1; pass < 3; ++pass) {
             const uint32_t nb = pass == 2 ? 1024u : 2048u;
-            hist_pass_all(sh, key_at, N, prefix, pmask, kShift[pass], nb);
+            hist_pass_all<NT>(sh, key_at, N, prefix, pmask, kShift[pass], nb);
             uint32_t dg, ab;
-            select_digit(sh, nb, krem, dg, ab);
+            select_digit<NT>(sh, nb, krem, dg, ab);
             prefix |= dg << kShift[pass];
             pmask |= (nb - 1) << kShift[pass];
             krem -= (int)ab;
         }
-        emit_selected(sh, key_at, N, k, prefix, krem, orow);
+        emit_selected<NT>(sh, key_at, N, k, prefix, krem, orow);
         return;
     }
     // ---- one pass: bitmap of entries above d0, candidates of digit d0
-    {
-        const uint32_t lt = lanemask_lt();
-        constexpr int U = 8;  // 32-entry groups a warp loads before using any
-        for (int g0 = warp; g0 < NW; g0 += U * kTkWarps) {
-            uint32_t kk[U];
+    const uint32_t lt = lanemask_lt();
+    if (((reinterpret_cast<uintptr_t>(srow) | (uintptr_t)N) & 3u) == 0 &&
+        (reinterpret_cast<uintptr_t>(srow) & 15u) == 0) {
+        // 16-byte loads: lane l holds entries 4l..4l+3 of a 128-entry chunk (4 bitmap words)
+        const float4* srow4 = reinterpret_cast<const float4*>(srow);
+        const int NCH = (N + 127) / 128;
+        constexpr int U = 4;  // chunks a warp loads before using any
+        for (int c0 = warp; c0 < NCH; c0 += U * NWP) {
+            float4 f[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int i = (g0 + u * kTkWarps) * 32 + lane;
-                kk[u] = (g0 + u * kTkWarps < NW && i < N) ? key_at(i) : 0u;
+                const int c = c0 + u * NWP;
+                const int e = c * 128 + lane * 4;
+                f[u] = (c < NCH && e < N) ? __ldcg(srow4 + e / 4) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int gw = g0 + u * kTkWarps;
-                if (gw >= NW) break;
+                const int c = c0 + u * NWP;
+                if (c >= NCH) break;
+                const bool valid = c * 128 + lane * 4 < N;
+                const uint32_t kk[4] = {float_key(f[u].x), float_key(f[u].y), float_key(f[u].z), float_key(f[u].w)};
+                uint32_t m[4], word = 0, n_in = 0, before = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t dg = kk[j] >> 21;
+                    const uint32_t sure = __ballot_sync(0xffffffffu, valid && dg > d0);
+                    m[j] = __ballot_sync(0xffffffffu, valid && dg == d0);
+                    // bitmap word w holds lanes 8w..8w+7: entry 4(l-8w)+j is bit l of ballot j
+                    word |= spread8((sure >> (8 * (lane & 3))) & 0xffu) << j;
+                    n_in += __popc(m[j]);
+                    before += __popc(m[j] & lt);
+                }
+                if (lane < 4 && 4 * c + lane < NW) sel[4 * c + lane] = word;
+                if (n_in != 0u) {  // one reservation for the chunk's candidates
+                    uint32_t at = 0;
+                    if (lane == 0) at = atomicAdd(&sh.cand_n, n_in);
+                    uint32_t slot = __shfl_sync(0xffffffffu, at, 0) + before;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if ((m[j] >> lane) & 1u) {
+                            if (slot < (uint32_t)kCandCap) {
+                                cand_key[slot] = kk[j];
+                                cand_idx[slot] = (uint32_t)(c * 128 + lane * 4 + j);
+                            }
+                            ++slot;
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        constexpr int U = 8;  // 32-entry groups a warp loads before using any
+        for (int g0 = warp; g0 < NW; g0 += U * NWP) {
+            uint32_t kk[U], m[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = (g0 + u * NWP) * 32 + lane;
+                kk[u] = (g0 + u * NWP < NW && i < N) ? key_at(i) : 0u;
+            }
+            uint32_t n_in = 0;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int gw = g0 + u * NWP;
                 const int i = gw * 32 + lane;
-                const bool valid = i < N;
+                const bool valid = gw < NW && i < N;
                 const uint32_t dg = kk[u] >> 21;
                 const uint32_t sure = __ballot_sync(0xffffffffu, valid && dg > d0);
-                if (lane == 0) sel[gw] = sure;
-                const bool in = valid && dg == d0;
-                const uint32_t m = __ballot_sync(0xffffffffu, in);
-                if (m != 0u) {
-                    const int leader = __ffs(m) - 1;
-                    uint32_t at = 0;
-                    if (lane == leader) at = atomicAdd(&sh.cand_n, (uint32_t)__popc(m));
-                    at = __shfl_sync(0xffffffffu, at, leader);
-                    const uint32_t slot = at + __popc(m & lt);
-                    if (in && slot < (uint32_t)kCandCap) {
+                if (lane == 0 && gw < NW) sel[gw] = sure;
+                m[u] = __ballot_sync(0xffffffffu, valid && dg == d0);
+                n_in += __popc(m[u]);
+            }
+            if (n_in != 0u) {  // one reservation for the batch's candidates
+                uint32_t at = 0;
+                if (lane == 0) at = atomicAdd(&sh.cand_n, n_in);
+                at = __shfl_sync(0xffffffffu, at, 0);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t slot = at + __popc(m[u] & lt);
+                    if (((m[u] >> lane) & 1u) && slot < (uint32_t)kCandCap) {
                         cand_key[slot] = kk[u];
-                        cand_idx[slot] = (uint32_t)i;
+                        cand_idx[slot] = (uint32_t)((g0 + u * NWP) * 32 + lane);
                     }
+                    at += __popc(m[u]);
                 }
             }
         }
@@ -356,34 +417,34 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     for (int pass = 1; pass < 3; ++pass) {
         const uint32_t nb = pass == 2 ? 1024u : 2048u;
         const int shift = kShift[pass];
-        for (int b = tid; b < kHistBins; b += kTkThreads) sh.hist[b] = 0;
+        for (int b = tid; b < kHistBins; b += NT) sh.hist[b] = 0;
         __syncthreads();
-        for (uint32_t c = tid; c < n_cand; c += kTkThreads) {
+        for (uint32_t c = tid; c < n_cand; c += NT) {
             const uint32_t ck = cand_key[c];
             if ((ck & pmask) == prefix) atomicAdd(&sh.hist[(ck >> shift) & (nb - 1)], 1u);
         }
         __syncthreads();
         uint32_t dg, ab;
-        select_digit(sh, nb, krem, dg, ab);
+        select_digit<NT>(sh, nb, krem, dg, ab);
         prefix |= dg << shift;
         pmask |= (nb - 1) << shift;
         krem -= (int)ab;
     }
     const uint32_t thr = prefix;
-    for (uint32_t c = tid; c < n_cand; c += kTkThreads) {
+    for (uint32_t c = tid; c < n_cand; c += NT) {
         const uint32_t ck = cand_key[c], ci = cand_idx[c];
         if (ck > thr) atomicOr(&sel[ci >> 5], 1u << (ci & 31));
         else if (ck == thr) atomicOr(&tie[ci >> 5], 1u << (ci & 31));
     }
     __syncthreads();
     // ---- keep the krem lowest-index ties; thread t owns words [t*W, t*W + W)
-    const int W = (NW + kTkThreads - 1) / kTkThreads;
+    const int W = (NW + NT - 1) / NT;
     const int w0 = tid * W, w1 = min(NW, w0 + W);
     {
         uint32_t cnt = 0;
         for (int w = w0; w < w1; ++w) cnt += __popc(tie[w]);
         uint32_t total;
-        uint32_t before = block_exclusive_scan(cnt, sh.wsum, total);
+        uint32_t before = block_exclusive_scan<NT>(cnt, sh.wsum, total);
         for (int w = w0; w < w1; ++w) {
             uint32_t bits = tie[w];
             while (bits != 0u && (int)before < krem) {
@@ -400,7 +461,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         uint32_t cnt = 0;
         for (int w = w0; w < w1; ++w) cnt += __popc(sel[w]);
         uint32_t total;
-        uint32_t at = block_exclusive_scan(cnt, sh.wsum, total);
+        uint32_t at = block_exclusive_scan<NT>(cnt, sh.wsum, total);
         for (int w = w0; w < w1; ++w) {
             uint32_t bits = sel[w];
             while (bits != 0u) {
@@ -449,14 +510,22 @@ extern "C" sd_status sd_topk(const float* scores, int rows, int N, int k, int32_
         if (k == 0) return SD_OK;
     }
     if (key_hist != nullptr) {
-        const int cache = key_bytes + aux_bytes + static_bytes <= limit ? 1 : 0;
-        const size_t dyn = (cache ? key_bytes : 0) + aux_bytes;
-        // static + dynamic may exceed the 48 KB default even when dyn alone does not
-        SD_CUDA_CHECK(cudaFuncSetAttribute(topk_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn),
-                      "sd_topk: cudaFuncSetAttribute");
-        SD_CUDA_CHECK(launch_pdl(topk_hist_kernel, rows, kTkThreads, dyn, st, scores, N, k, idx, key_hist, cache,
-                                 (int32_t*)nullptr),
-                      "sd_topk: launch");
+        // more rows than SMs: 512-thread CTAs, two per SM, so the rows run in one wave
+        const size_t dyn = aux_bytes;
+        if (rows > num_sms()) {
+            SD_CUDA_CHECK(cudaFuncSetAttribute(topk_hist_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)dyn),
+                          "sd_topk: cudaFuncSetAttribute");
+            SD_CUDA_CHECK(launch_pdl(topk_hist_kernel<512>, rows, 512, dyn, st, scores, N, k, idx, key_hist),
+                          "sd_topk: launch");
+        } else {
+            SD_CUDA_CHECK(cudaFuncSetAttribute(topk_hist_kernel<kTkThreads>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn),
+                          "sd_topk: cudaFuncSetAttribute");
+            SD_CUDA_CHECK(launch_pdl(topk_hist_kernel<kTkThreads>, rows, kTkThreads, dyn, st, scores, N, k, idx,
+                                     key_hist),
+                          "sd_topk: launch");
+        }
     } else {
         const int cache = key_bytes + static_bytes <= limit ? 1 : 0;
         const size_t dyn = cache ? key_bytes : 0;
