@@ -202,18 +202,21 @@ class SparseDecodeStep:
     """One sparse decode step, inputs resident: the indexer, then either the fused select +
     attend launch (bf16 workloads) or the separate top-k and gather-attend launches.  For a
     tiered workload the full K/V cache stays in pinned host memory and only the resident
-    share sits in the HBM pool."""
+    share sits in the HBM pool; there the default path copies the selected host rows into
+    an HBM stage with one copy kernel spread over every SM (sd_stage_host_rows) between the
+    top-k and the attention."""
 
     dominant = "sd_index_score"
 
-    def __init__(self, w, x, device, separate=False):
+    def __init__(self, w, x, device, separate=False, tiered_path="staged"):
         import torch
         from top_sparse_decode_gqa_gb300 import binding as sd
         self.sd, self.w, self.dev = sd, w, device
-        self.fused = w.dtype == "bf16" and not separate
-        self.phases = () if self.fused else ("after_topk",)
-        self.launches_per_step = 2 if self.fused else 3
         self.tiered = w.resident_frac < 1.0
+        self.staged = self.tiered and tiered_path == "staged" and not separate
+        self.fused = w.dtype == "bf16" and not separate and not self.staged
+        self.phases = () if self.fused else ("after_topk", "after_stage") if self.staged else ("after_topk",)
+        self.launches_per_step = 2 if self.fused else 4 if self.staged else 3
         self.q_idx, self.k_idx, self.q = (x[k].to(device) for k in ("q_idx", "k_idx", "q"))
         self.scores = torch.empty(w.B, w.Hkv, w.N, dtype=torch.float32, device=device)
         self.idx = torch.empty(w.B, w.Hkv, w.k, dtype=torch.int32, device=device)
@@ -232,6 +235,9 @@ class SparseDecodeStep:
             block=w.block, T=w.T, err_word=self.err, **kw)
         need = 0 if self.fused else sd.sd_gather_attend_workspace_bytes(self.args)
         self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=device)
+        if self.staged:
+            self.stage = sd.stage_buffers(self.args, self.q.dtype, device)
+            self.counter = sd.stage_counter(device)
         self.keys = self.k_idx
         if w.block > 1:
             self.keys = sd.sd_block_pool(self.k_idx, w.block)
@@ -253,6 +259,10 @@ class SparseDecodeStep:
             sd.sd_topk(self.scores, self.w.k, self.idx, key_hist=self.key_hist)
             if m is not None:
                 m.at("after_topk")
+            if self.staged:
+                sd.sd_stage_host_rows(self.args, self.counter)
+                if m is not None:
+                    m.at("after_stage")
             sd.sd_gather_attend(self.args, self.ws)
         if m is not None:
             m.end.record()
@@ -474,14 +484,14 @@ class DenseScoringStep:
                 "host": 0}
 
 
-def make_step(w, x, device, separate=False):
+def make_step(w, x, device, separate=False, tiered_path="staged"):
     if w.layers > 1:
         return DenseScoringStep(w, x, device)
     if w.window_kernel > 0:
         return WindowStep(w, x, device)
     if w.per_head:
         return HeadsStep(w, x, device)
-    return SparseDecodeStep(w, x, device, separate)
+    return SparseDecodeStep(w, x, device, separate, tiered_path)
 
 
 def host_link_gbs(device, nbytes=512 << 20):
@@ -520,7 +530,7 @@ def run_ours(args):
         dist.barrier()
     w = WORKLOADS[args.workload]
     x = generate(w)
-    step = make_step(w, x, device, args.separate)
+    step = make_step(w, x, device, args.separate, args.tiered_path)
     props = torch.cuda.get_device_properties(device)
     flush = torch.empty(2 * max(int(getattr(props, "L2_cache_size", 0)), 128 << 20), dtype=torch.uint8,
                         device=device)
@@ -603,6 +613,13 @@ def run_ours(args):
         step_roof["kernel_us"] = {"index_score": round(statistics.mean(dom_ms) * 1e3, 2),
                                   "window_max+topk+union+gather_attend": round(statistics.mean(tail) * 1e3, 2)}
         step_roof["kv_rows_selected"] = step.rows_used
+    elif isinstance(step, SparseDecodeStep) and step.staged:
+        k_us = lambda a, b: round(statistics.mean(a(m).elapsed_time(b(m)) for m in kmarks) * 1e3, 2)
+        step_roof["kernel_us"] = {
+            "index_score": round(statistics.mean(dom_ms) * 1e3, 2),
+            "topk": k_us(lambda m: m.dom[0][1], lambda m: m.phase["after_topk"]),
+            "stage_host_rows": k_us(lambda m: m.phase["after_topk"], lambda m: m.phase["after_stage"]),
+            "gather_attend": k_us(lambda m: m.phase["after_stage"], lambda m: m.end)}
     elif isinstance(step, (SparseDecodeStep, HeadsStep)):
         after_topk = [m.dom[0][1].elapsed_time(m.phase["after_topk"]) for m in kmarks]
         tail = [m.phase["after_topk"].elapsed_time(m.end) for m in kmarks]
@@ -629,6 +646,8 @@ def run_ours(args):
                    "k": w.k, "block": w.block, "V": w.V, "layers": w.layers,
                    "queries_per_step": w.queries_per_step,
                    "path": ("indexer + fused select/attend" if getattr(step, "fused", False)
+                            else "indexer + top-k + host-row staging + gather-attend"
+                            if getattr(step, "staged", False)
                             else "indexer + top-k + gather-attend" if isinstance(step, SparseDecodeStep)
                             else "indexer + window max + top-k windows + union + gather-attend"
                             if isinstance(step, WindowStep)
@@ -791,6 +810,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--separate", action="store_true",
                     help="run top-k and gather-attend as two launches instead of the fused one")
+    ap.add_argument("--tiered-path", choices=("staged", "fused"), default="staged",
+                    help="tiered workloads: stage the selected host rows into HBM with one copy kernel "
+                         "before the attention (staged), or read them inside the fused select/attend")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

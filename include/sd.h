@@ -171,6 +171,10 @@ sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx, uin
  * workspace must not overlap on the GPU.  splits = 0 picks one wave of CTAs for this GPU;
  * a requested split count is adjusted to at least one 64-row chunk per split and at most
  * 448 rows per split when rows are selected through idx or slot_map.
+ * Staged host rows: with slot_map and k_stage/v_stage set, a row whose slot is -1 is read
+ * from the stage at [group, j] (j = its position in the group's selection list, group =
+ * b*Hkv + kvh, or b*Hq + h with per_head) instead of host memory; the stage must hold what
+ * sd_stage_host_rows copied there for the same args.  Same values, so the same bits.
  * per_head = 1 ([Illusion] sec. 2: Oracle Top-K per query head): idx is [B,Hq,n_idx] and
  * query head h attends to its own selection idx[b,h,:], rows read from KV head
  * h / (Hq/Hkv) (all V query tokens of the head share it); the split plan and workspace then
@@ -197,6 +201,8 @@ typedef struct {
     size_t workspace_bytes;
     int splits;               /* 0 = automatic */
     int per_head;             /* 1: idx is [B,Hq,n_idx], one selection per query head */
+    const void* k_stage;      /* nullable HBM stage [groups, n_idx*block, d] (sd_stage_host_rows) */
+    const void* v_stage;      /* same layout as k_stage; both set or both NULL */
 } sd_attend_args;
 
 size_t sd_gather_attend_workspace_bytes(const sd_attend_args* args);
@@ -223,6 +229,27 @@ sd_status sd_gather_attend(const sd_attend_args* args, void* stream);
 sd_status sd_gather_attend_noalloc(const sd_attend_args* args, void* stream);
 
 /*
+ * sd_stage_host_rows -- copy the selected rows that live in host memory into an HBM stage.
+ * [DHiSparse] "A Inovacao" (the history stays in host memory and only the selected rows
+ * are fetched) and "Metodologia" (the query rows of a group share the fetch of a missing
+ * row); [SparDA] sec. 2 item 3 (a kernel moves the needed rows from host memory through
+ * unified addressing ahead of the attention).
+ * With the same args as the sd_gather_attend call that follows (slot_map, k_host/v_host,
+ * idx, n_idx, block, per_head and k_stage/v_stage must be set): for every group g (b*Hkv +
+ * kvh, or b*Hq + h with per_head) and list row j < n_idx*block whose token
+ * t = idx[g, j/block]*block + j%block has slot_map[b,t] == -1, copies K/V host row
+ * [b, kvh, t, :] (kvh = h / (Hq/Hkv) with per_head) to k_stage/v_stage[g, j, :].  Other
+ * stage rows are left as they are; empty slots (-1), pool rows and rows that
+ * sd_gather_attend would reject (reported through err_word) are skipped.  The copy is
+ * spread over every SM: warps take chunks of rows from counter[0], a caller-owned device
+ * uint32[2] that must be zero-filled before the first call and is left at zero by every
+ * call (calls sharing one counter must not overlap on the GPU).  The result does not depend
+ * on which warp copied which row.  Launched as a programmatic dependent of the preceding
+ * kernel; sd_gather_attend launched after it waits for it.  Limits as sd_gather_attend.
+ */
+sd_status sd_stage_host_rows(const sd_attend_args* args, uint32_t* counter, void* stream);
+
+/*
  * sd_select_attend -- sd_topk and sd_gather_attend fused in one launch.
  * [Illusion] sec. 2 "Mecanismos de Esparsidade" (Oracle Top-K feeding a sparse decode
  * kernel) and sec. 3C; [SparDA] sec. 2 item 1 (top-k blocks); [DHiSparse] "Metodologia"
@@ -230,8 +257,8 @@ sd_status sd_gather_attend_noalloc(const sd_attend_args* args, void* stream);
  * Computes what sd_topk(scores, B*Hkv, N, n_idx, idx, key_hist) followed by
  * sd_gather_attend(args with idx) computes: idx [B,Hkv,n_idx] int32 (written, ascending,
  * bit-identical to sd_topk), out, lse and optional logits as sd_gather_attend defines
- * them, with the selection list of every (b, kvh) taken from idx.  args->idx, workspace
- * and workspace_bytes are ignored; k = args->n_idx.  scores [B*Hkv, N] fp32 with
+ * them, with the selection list of every (b, kvh) taken from idx.  args->idx, workspace,
+ * workspace_bytes, k_stage and v_stage are ignored; k = args->n_idx.  scores [B*Hkv, N] fp32 with
  * N * args->block == args->T (one score per token, or per block of `block` tokens).
  * key_hist: nullable, as in sd_topk (the indexer's histogram of exactly these scores;
  * zero-filled again by the call).  args->splits: CTAs per (b, kvh), 0 = automatic, at most

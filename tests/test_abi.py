@@ -103,3 +103,38 @@ def test_select_attend_validation(lib):
     a.V, a.block, a.n_idx = 1, 64, 8
     a.B = 0  # nothing to do: accepted without touching the pointers
     assert lib.sd_select_attend(None, 64, None, None, ctypes.byref(a), None) == 0
+
+
+def test_stage_host_rows_validation(lib):
+    from top_sparse_decode_gqa_gb300.binding import sd_attend_args
+    dummy = ctypes.c_void_p(16)
+    a = sd_attend_args()
+    a.q = a.k_cache = a.v_cache = a.out = a.lse = a.idx = 16
+    a.dtype, a.B, a.V, a.Hq, a.Hkv, a.d, a.T = 1, 2, 1, 32, 8, 128, 4096
+    a.pool_rows, a.n_idx, a.block, a.scale = 409, 64, 1, 0.1
+    # the staged copy needs a slot map, host K/V, both stage buffers and a counter
+    assert lib.sd_stage_host_rows(ctypes.byref(a), dummy, None) == 1
+    assert b"slot_map" in lib.sd_last_error_message()
+    a.slot_map = 16
+    assert lib.sd_stage_host_rows(ctypes.byref(a), dummy, None) == 1
+    assert b"k_host" in lib.sd_last_error_message()
+    a.k_host = a.v_host = 16
+    assert lib.sd_stage_host_rows(ctypes.byref(a), dummy, None) == 1
+    assert b"k_stage" in lib.sd_last_error_message()
+    a.k_stage = 16
+    assert lib.sd_stage_host_rows(ctypes.byref(a), dummy, None) == 1
+    a.v_stage = 24  # misaligned
+    assert lib.sd_stage_host_rows(ctypes.byref(a), dummy, None) == 1
+    assert b"aligned" in lib.sd_last_error_message()
+    a.v_stage = 32
+    assert lib.sd_stage_host_rows(ctypes.byref(a), None, None) == 1
+    assert b"counter" in lib.sd_last_error_message()
+    # the shared attention checks apply, named for this call
+    a.d = 96
+    assert lib.sd_stage_host_rows(ctypes.byref(a), dummy, None) == 2
+    assert lib.sd_last_error_message().startswith(b"sd_stage_host_rows:")
+    # sd_gather_attend: a stage needs both buffers
+    a.d, a.v_stage = 128, None
+    a.workspace, a.workspace_bytes = 16, 1 << 30
+    assert lib.sd_gather_attend(ctypes.byref(a), None) == 1
+    assert b"go together" in lib.sd_last_error_message()

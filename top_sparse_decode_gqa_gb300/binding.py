@@ -27,7 +27,7 @@ EXPORTS = (
     "sd_topk_workspace_bytes", "sd_topk", "sd_gather_attend_workspace_bytes", "sd_gather_attend",
     "sd_score_accumulate", "sd_tier_classify_workspace_bytes", "sd_tier_classify",
     "sd_quantize_rows_int8", "sd_gather_attend_noalloc", "sd_select_attend", "sd_window_count",
-    "sd_window_max", "sd_window_union", "sd_index_score_heads",
+    "sd_window_max", "sd_window_union", "sd_index_score_heads", "sd_stage_host_rows",
 )
 
 
@@ -48,6 +48,7 @@ class sd_attend_args(ctypes.Structure):
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("logits", ctypes.c_void_p),
         ("err_word", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t), ("splits", ctypes.c_int), ("per_head", ctypes.c_int),
+        ("k_stage", ctypes.c_void_p), ("v_stage", ctypes.c_void_p),
     ]
 
 
@@ -77,6 +78,7 @@ def lib() -> ctypes.CDLL:
         L.sd_gather_attend_noalloc.argtypes = [ctypes.POINTER(sd_attend_args), P]
         L.sd_select_attend.argtypes = [P, I, P, P, ctypes.POINTER(sd_attend_args), P]
         L.sd_index_score_heads.argtypes = [P, I, P, I, I, I, I, I, I, P, P, P, P]
+        L.sd_stage_host_rows.argtypes = [ctypes.POINTER(sd_attend_args), P, P]
         L.sd_window_count.argtypes = [I, I, I]
         L.sd_window_count.restype = I
         L.sd_window_max.argtypes = [P, I, I, I, I, P, P, P]
@@ -210,7 +212,8 @@ def sd_topk(scores: torch.Tensor, k: int, idx: Optional[torch.Tensor] = None,
 
 def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=None, scale=None,
                      k_host=None, v_host=None, slot_map=None, out=None, lse=None, logits=None,
-                     want_logits=False, err_word=None, splits=0, per_head=False) -> tuple:
+                     want_logits=False, err_word=None, splits=0, per_head=False, k_stage=None,
+                     v_stage=None) -> tuple:
     """Fill an sd_attend_args from tensors; returns (args, out, lse, logits)."""
     _dev(q, "q")
     B, V, Hq, d = q.shape
@@ -250,6 +253,10 @@ def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=No
     a.err_word = err_word.data_ptr() if err_word is not None else None
     a.splits = splits
     a.per_head = 1 if per_head else 0
+    for name, t in (("k_stage", k_stage), ("v_stage", v_stage)):
+        if t is not None:
+            _dev(t, name)
+            setattr(a, name, t.data_ptr())
     return a, out, lse, logits
 
 
@@ -276,6 +283,29 @@ def sd_gather_attend_noalloc(args: sd_attend_args, stream=None) -> None:
     that cannot allocate); args.workspace is ignored."""
     _check(lib().sd_gather_attend_noalloc(ctypes.byref(args), _stream(stream)),
            "sd_gather_attend_noalloc")
+
+
+def stage_buffers(args: sd_attend_args, dtype: torch.dtype, device="cuda") -> tuple:
+    """HBM stage tensors (k_stage, v_stage) [groups, n_idx*block, d] for `args` (groups =
+    B*Hkv, or B*Hq per head), set into args; returns them."""
+    groups = args.B * (args.Hq if args.per_head else args.Hkv)
+    shape = (groups, args.n_idx * args.block, args.d)
+    ks = torch.empty(shape, dtype=dtype, device=device)
+    vs = torch.empty(shape, dtype=dtype, device=device)
+    args.k_stage, args.v_stage = ks.data_ptr(), vs.data_ptr()
+    return ks, vs
+
+
+def stage_counter(device="cuda") -> torch.Tensor:
+    """A zero-filled device uint32[2] (held as int32) for sd_stage_host_rows."""
+    return torch.zeros(2, dtype=torch.int32, device=device)
+
+
+def sd_stage_host_rows(args: sd_attend_args, counter: torch.Tensor, stream=None) -> None:
+    """Copies the selected host-resident rows `args` describes into args.k_stage/v_stage
+    (see stage_buffers); counter from stage_counter, left at zero."""
+    _dev(counter, "counter")
+    _check(lib().sd_stage_host_rows(ctypes.byref(args), _ptr(counter), _stream(stream)), "sd_stage_host_rows")
 
 
 def sd_select_attend(scores: torch.Tensor, args: sd_attend_args, idx: torch.Tensor,

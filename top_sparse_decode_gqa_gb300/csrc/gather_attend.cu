@@ -43,6 +43,7 @@ struct AttendParams {
     int kv_heads, heads_per_kv;  // KV heads of the cache; groups per KV head (per-head mode: G)
     int dtype;
     int resolve;  // 1: sources resolved up front (idx or slot_map given)
+    int staged;   // 1: kh/vh are the HBM stage [groups, n_rows, d], host rows by list position
     float scale_log2;
     float* out;
     float* lse;
@@ -210,6 +211,8 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int bk = b * p.Hkv + kvh;
     const int kvsrc = b * p.kv_heads + kvh / p.heads_per_kv;  // the (b, KV head) slab the rows come from
+    // host rows: the (b, KV head) slab of the host cache, or this group's rows of the stage
+    const size_t host_row0 = p.staged ? (size_t)bk * p.n_rows : (size_t)kvsrc * p.T;
     const size_t esz = sizeof(ST);
 
     pdl_wait();  // everything below may read what the preceding kernel wrote
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
         if (p.slot_map == nullptr) return (int32_t)pos;
         const int slot = p.slot_map[(size_t)b * p.T + pos];
         if (slot >= 0 && slot < p.pool_rows) return slot;
-        if (slot == -1) return (int32_t)(-1 - pos);
+        if (slot == -1) return (int32_t)(-1 - (p.staged ? (long)jg : pos));
         report(p.err, SD_DEVERR_SLOT);
         return kNoRow;
     };
@@ -277,7 +280,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
                 row = (size_t)kvsrc * p.pool_rows + code;
             } else {
                 base = which ? p.vh : p.kh;
-                row = (size_t)kvsrc * p.T + (size_t)(-1 - (long)code);
+                row = host_row0 + (size_t)(-1 - (long)code);
             }
             cp_async16(dst, base + row * L::kVRow + part * 16);
         }
@@ -521,7 +524,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
                 if (slot >= 0 && slot < p.pool_rows) {
                     code = slot;
                 } else if (slot == -1) {
-                    code = (int32_t)(-1 - pos);
+                    code = (int32_t)(-1 - (p.staged ? (long)jg : pos));
                 } else {
                     report(p.err, SD_DEVERR_SLOT);
                     code = kNoRow;
@@ -537,8 +540,9 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     RowSource rs;
     rs.k_pool = p.kc + (size_t)kvsrc * p.pool_rows * (D * 2);
     rs.v_pool = p.vc + (size_t)kvsrc * p.pool_rows * (D * 2);
-    rs.k_host = p.kh + (size_t)kvsrc * p.T * (D * 2);
-    rs.v_host = p.vh + (size_t)kvsrc * p.T * (D * 2);
+    const size_t host_row0 = p.staged ? (size_t)bk * p.n_rows : (size_t)kvsrc * p.T;
+    rs.k_host = p.kh + host_row0 * (D * 2);
+    rs.v_host = p.vh + host_row0 * (D * 2);
     auto row_code = [&](int j) -> int32_t { return p.resolve ? src[j] : (int32_t)(j0 + j); };
     float* lbase = nullptr;  // logits of query row 0 of this group, at list row j0
     if (p.logits != nullptr) lbase = p.logits + ((size_t)b * p.V * p.Hq + kvh * p.G) * p.n_rows + j0;
@@ -679,55 +683,44 @@ sd_status dispatch_rp(const AttendParams& p, int dtype, int RP, cudaStream_t st)
     }
 }
 
-// Device address of pinned host memory (NULL if it is not mapped pinned memory).
-const uint8_t* host_dev_ptr(const void* h) {
-    cudaPointerAttributes at{};
-    if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
-        cudaGetLastError();
-        return nullptr;
-    }
-    if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
-    return static_cast<const uint8_t*>(at.devicePointer);
-}
-
 }  // namespace
 }  // namespace sd
 
 using namespace sd;
 
-static sd_status validate_attend(const sd_attend_args* a) {
-    SD_REQUIRE(a != nullptr, "sd_gather_attend: null args");
+sd_status sd::validate_attend_args(const sd_attend_args* a, const char* who) {
+    SD_REQUIRE(a != nullptr, "%s: null args", who);
     SD_REQUIRE(a->B >= 0 && a->V >= 1 && a->Hq >= 1 && a->Hkv >= 1 && a->T >= 0,
-               "sd_gather_attend: bad sizes (B=%d V=%d Hq=%d Hkv=%d T=%d)", a->B, a->V, a->Hq, a->Hkv, a->T);
-    SD_REQUIRE(a->Hq % a->Hkv == 0, "sd_gather_attend: Hq must be a multiple of Hkv");
-    SD_REQUIRE(valid_dtype(a->dtype), "sd_gather_attend: bad dtype");
-    SD_REQUIRE(a->block >= 1 && a->n_idx >= 0, "sd_gather_attend: bad block / n_idx");
-    SD_REQUIRE((long)a->n_idx * a->block <= (1L << 30), "sd_gather_attend: selection too large");
+               "%s: bad sizes (B=%d V=%d Hq=%d Hkv=%d T=%d)", who, a->B, a->V, a->Hq, a->Hkv, a->T);
+    SD_REQUIRE(a->Hq % a->Hkv == 0, "%s: Hq must be a multiple of Hkv", who);
+    SD_REQUIRE(valid_dtype(a->dtype), "%s: bad dtype", who);
+    SD_REQUIRE(a->block >= 1 && a->n_idx >= 0, "%s: bad block / n_idx", who);
+    SD_REQUIRE((long)a->n_idx * a->block <= (1L << 30), "%s: selection too large", who);
     if (a->idx == nullptr && a->n_idx > 0)
-        SD_REQUIRE((long)a->n_idx * a->block == a->T, "sd_gather_attend: dense mode needs n_idx*block == T");
+        SD_REQUIRE((long)a->n_idx * a->block == a->T, "%s: dense mode needs n_idx*block == T", who);
     if (a->d != 64 && a->d != 128) {
-        set_error("sd_gather_attend: d must be 64 or 128 (got %d)", a->d);
+        set_error("%s: d must be 64 or 128 (got %d)", who, a->d);
         return SD_ERR_UNSUPPORTED;
     }
     const int rows_per_group = a->per_head ? a->V : (a->Hq / a->Hkv) * a->V;
     if (kernel_rows(a->dtype, rows_per_group) < 0) {
-        set_error("sd_gather_attend: %d query rows per group exceed 32", rows_per_group);
+        set_error("%s: %d query rows per group exceed 32", who, rows_per_group);
         return SD_ERR_UNSUPPORTED;
     }
-    SD_REQUIRE(a->B <= 65535 && a->Hq <= 65535, "sd_gather_attend: B and Hq must be <= 65535");
-    SD_REQUIRE(a->per_head == 0 || a->per_head == 1, "sd_gather_attend: per_head must be 0 or 1");
-    SD_REQUIRE(!a->per_head || a->idx != nullptr || a->n_idx == 0, "sd_gather_attend: per_head needs idx");
+    SD_REQUIRE(a->B <= 65535 && a->Hq <= 65535, "%s: B and Hq must be <= 65535", who);
+    SD_REQUIRE(a->per_head == 0 || a->per_head == 1, "%s: per_head must be 0 or 1", who);
+    SD_REQUIRE(!a->per_head || a->idx != nullptr || a->n_idx == 0, "%s: per_head needs idx", who);
     return SD_OK;
 }
 
 extern "C" size_t sd_gather_attend_workspace_bytes(const sd_attend_args* a) {
-    if (validate_attend(a) != SD_OK) return 0;
+    if (validate_attend_args(a, "sd_gather_attend") != SD_OK) return 0;
     return plan_splits(a).ws_bytes;
 }
 
 extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
     clear_error();
-    sd_status vs = validate_attend(a);
+    sd_status vs = validate_attend_args(a, "sd_gather_attend");
     if (vs != SD_OK) return vs;
     if (a->B == 0) return SD_OK;
     SD_REQUIRE(a->q && a->out && a->lse, "sd_gather_attend: null q/out/lse");
@@ -768,11 +761,20 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
     if (a->slot_map != nullptr) {
         SD_REQUIRE(a->pool_rows >= 0, "sd_gather_attend: pool_rows must be >= 0");
         SD_REQUIRE(a->k_host && a->v_host, "sd_gather_attend: slot_map needs k_host and v_host");
-        p.kh = host_dev_ptr(a->k_host);
-        p.vh = host_dev_ptr(a->v_host);
+        SD_REQUIRE((a->k_stage == nullptr) == (a->v_stage == nullptr),
+                   "sd_gather_attend: k_stage and v_stage go together");
+        p.kh = mapped_host_ptr(a->k_host);
+        p.vh = mapped_host_ptr(a->v_host);
         SD_REQUIRE(p.kh && p.vh, "sd_gather_attend: k_host/v_host must be pinned, mapped host memory");
         SD_REQUIRE(aligned16(a->k_host) && aligned16(a->v_host), "sd_gather_attend: host K/V must be 16-byte aligned");
         p.pool_rows = a->pool_rows;
+        if (a->k_stage != nullptr) {  // host rows come from the HBM stage
+            SD_REQUIRE(aligned16(a->k_stage) && aligned16(a->v_stage),
+                       "sd_gather_attend: k_stage/v_stage must be 16-byte aligned");
+            p.kh = static_cast<const uint8_t*>(a->k_stage);
+            p.vh = static_cast<const uint8_t*>(a->v_stage);
+            p.staged = 1;
+        }
     } else {
         p.pool_rows = a->T;
     }

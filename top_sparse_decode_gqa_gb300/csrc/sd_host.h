@@ -22,9 +22,30 @@ int num_sms();
 // Maximum opt-in dynamic shared memory per block of the current device (cached).
 int max_smem_optin();
 
+// Host-side checks of an sd_attend_args shared by the calls that take one; `who` names the
+// call in the error message.
+sd_status validate_attend_args(const sd_attend_args* a, const char* who);
+
+// Top-k of few long rows by thread-block clusters (the selection of sd_select_attend alone):
+// false when the rows need clusters of one CTA (nothing launched), else launches and sets
+// *status.
+bool topk_by_clusters(const float* scores, int rows, int N, int k, int32_t* idx, uint32_t* key_hist,
+                      cudaStream_t st, sd_status* status);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Device address of pinned, mapped host memory (NULL if h is not such memory).
+inline const uint8_t* mapped_host_ptr(const void* h) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
+    return static_cast<const uint8_t*>(at.devicePointer);
+}
 
 inline bool valid_dtype(int dt) { return dt == SD_F32 || dt == SD_BF16; }
 inline int dtype_bytes(int dt) { return dt == SD_F32 ? 4 : 2; }

@@ -77,6 +77,7 @@ struct SelAttParams {
     float* logits;
     int32_t* err;
     int inbox_own;  // 1: the merge inbox has its own shared memory after the layout's end
+    int attend;     // 0: selection only (idx written; q, K/V and the outputs untouched)
 };
 
 // Shared-memory layout (byte offsets), in order:
@@ -457,7 +458,7 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
             bulk_g2s(reinterpret_cast<uint8_t*>(keys_s) + off, reinterpret_cast<const uint8_t*>(srow + p0) + off,
                      (uint32_t)min(kChunk, np * 4 - off), &ms->bar);
     }
-    for (int e = tid; e < RP * PPR; e += kSaThreads) {
+    for (int e = tid; p.attend && e < RP * PPR; e += kSaThreads) {
         const int r = e / PPR, part = e % PPR;
         uint8_t* dst = sm + L.oQ + r * Rows::kRowB + part * 16;
         if (r < p.R) {
@@ -769,6 +770,10 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
     } else if (!trivial) {
         sa_emit_ordered(staged ? keys_s : nullptr, srow, p0, p1, thr, take, n_mine, ms, orow + base, lst);
     }
+    if (!p.attend) {  // selection only: no CTA leaves while the cluster may still read it
+        cl.sync();
+        return;
+    }
     cp_async_wait<0>();  // query rows
     __syncthreads();     // the selection list is complete (shared memory and idx)
 
@@ -979,17 +984,36 @@ sd_status launch_select_attend(SelAttParams p, int rows, int requested, bool sco
     return launch_status("sd_select_attend");
 }
 
-const uint8_t* mapped_host_ptr(const void* h) {
-    cudaPointerAttributes at{};
-    if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
-        cudaGetLastError();
-        return nullptr;
-    }
-    if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
-    return static_cast<const uint8_t*>(at.devicePointer);
+}  // namespace
+
+// sd_topk's path for few long rows: the cluster kernel's selection alone, one cluster of
+// P >= 2 CTAs per row.  Returns false (nothing launched) when the rows are too many for
+// clusters of two or more CTAs to run in one wave; the caller then uses its own kernel.
+bool topk_by_clusters(const float* scores, int rows, int N, int k, int32_t* idx, uint32_t* key_hist,
+                      cudaStream_t st, sd_status* status) {
+    if (rows <= 0 || rows > 65535 || k <= 0 || k >= N) return false;
+    const bool al = aligned16(scores);
+    const SaPlan pl = plan_select_attend<128, 16>(rows, N, 0, al);
+    if (pl.P < 2) return false;
+    SelAttParams p{};
+    p.scores = scores;
+    p.key_hist = key_hist;
+    p.idx = idx;
+    p.N = N;
+    p.k = k;
+    p.B = 1;
+    p.Hkv = rows;
+    p.V = 1;
+    p.Hq = rows;
+    p.G = 1;
+    p.R = 1;
+    p.T = N;
+    p.block = 1;
+    p.attend = 0;
+    *status = launch_select_attend<128, 16>(p, rows, 0, al, st);
+    return true;
 }
 
-}  // namespace
 }  // namespace sd
 
 using namespace sd;
@@ -1047,6 +1071,7 @@ extern "C" sd_status sd_select_attend(const float* scores, int N, uint32_t* key_
     p.lse = a->lse;
     p.logits = a->logits;
     p.err = a->err_word;
+    p.attend = 1;
     if (a->slot_map != nullptr) {
         SD_REQUIRE(a->pool_rows >= 0, "sd_select_attend: pool_rows must be >= 0");
         SD_REQUIRE(a->k_host && a->v_host, "sd_select_attend: slot_map needs k_host and v_host");

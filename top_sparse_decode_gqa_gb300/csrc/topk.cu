@@ -5,8 +5,11 @@
 // scoring tokens; SparDA (gist.science summary), sec. 2 item 1, selects top-k blocks the
 // same way.  The pages are silent on ties; the lower index wins.
 //
-// One CTA per row (1024 threads; 512 threads, two CTAs per SM, when the rows outnumber
-// the SMs and the first digit's histogram is given).  Scores become order-preserving
+// Rows of 16384 entries or more, when clusters of two or more CTAs per row fit in one wave,
+// go to the cluster selection of select_attend.cu (each CTA owns a part of the row; the
+// digits are summed over distributed shared memory).  Otherwise one CTA per row (1024
+// threads; 512 threads, two CTAs per SM, when the rows outnumber the SMs and the first
+// digit's histogram is given).  Scores become order-preserving
 // uint32 keys (kept in shared memory when the row fits and several passes read it).  A radix select with 11/11/10-bit digits finds the
 // k-th largest key `thr` and how many entries equal to it are still needed (`krem`).  A
 // final ordered pass gives each warp a contiguous segment of the row: per-warp counts,
@@ -238,6 +241,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
 }
 
 constexpr int kCandCap = 4096;
+constexpr int kClusterMinN = 16384;  // rows at least this long go to the cluster selection
 
 // Bits 0..7 of x moved to bits 0, 4, ..., 28 (the others cleared).
 SD_DEVINL uint32_t spread8(uint32_t x) {
@@ -498,6 +502,11 @@ extern "C" sd_status sd_topk(const float* scores, int rows, int N, int k, int32_
     if (key_hist == nullptr && k == 0) return SD_OK;
     SD_REQUIRE(scores && (k == 0 || idx), "sd_topk: null pointer");
     cudaStream_t st = as_stream(stream);
+    // few long rows: several CTAs per row in a thread-block cluster
+    if (N >= kClusterMinN) {
+        sd_status cs = SD_OK;
+        if (topk_by_clusters(scores, rows, N, k, idx, key_hist, st, &cs)) return cs;
+    }
     const size_t limit = (size_t)max_smem_optin();
     const size_t static_bytes = sizeof(TopkShared) + 1024;
     const size_t key_bytes = (size_t)N * sizeof(uint32_t);
