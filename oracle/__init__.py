@@ -41,8 +41,10 @@ def _load():
         lib.oracle_window_count.argtypes = [I, I, I]
         lib.oracle_window_max.argtypes = [P, I, I, I, I, P]
         lib.oracle_window_union.argtypes = [P, I, I, I, I, I, P, I]
+        lib.oracle_gather_attend_ring.argtypes = [P, P, P, I, P, I, I, I, I, I, I, I, I, D, P, P, P, P, I, P, P,
+                                                  P]
         for name in ("oracle_index_score", "oracle_block_pool", "oracle_topk",
-                     "oracle_gather_attend", "oracle_score_accumulate", "oracle_tier_classify",
+                     "oracle_gather_attend", "oracle_gather_attend_ring", "oracle_score_accumulate", "oracle_tier_classify",
                      "oracle_quantize_rows_int8", "oracle_window_count", "oracle_window_max",
                      "oracle_window_union", "oracle_index_score_heads"):
             getattr(lib, name).restype = I
@@ -190,6 +192,55 @@ def gather_attend(q, K, Vv, idx, B, V, Hq, Hkv, d, T, n_idx, block, scale, want_
                                         d, T, n_idx, block, float(scale), _ptr(out), _ptr(lse),
                                         _ptr(logits), 1 if per_head else 0), "gather_attend")
     return out, lse, logits
+
+
+def gather_attend_ring(q, K, Vv, idx, B, V, Hq, Hkv, d, T, n_idx, block, scale, ring_k, ring_v, ring_pos, qpos,
+                       want_logits=False):
+    """Verify attention with the draft tokens' window-bounded ring (Adaptive DHiSparse,
+    "Metodologia"): the selected history rows as gather_attend, plus every ring slot s of
+    the KV head with 0 <= ring_pos[b,s] <= qpos[b,v].  ring_k/ring_v [B,Hkv,W,d] (dtype of
+    q), ring_pos int [B,W] (-1 = empty), qpos int [B,V].  Returns (out, lse, logits
+    [B,V,Hq,n_idx*block + W] or None), fp64."""
+    qa, qd = _as_data(q)
+    ka, kd = _as_data(K)
+    va, vd = _as_data(Vv)
+    rka, rkd = _as_data(ring_k)
+    rva, rvd = _as_data(ring_v)
+    assert qd == kd == vd == rkd == rvd, "q, K, V and the ring must share one dtype"
+    W = ring_pos.shape[-1]
+    assert qa.size == B * V * Hq * d and ka.size == B * Hkv * T * d and va.size == ka.size
+    assert rka.size == B * Hkv * W * d and rva.size == rka.size
+    rp = np.ascontiguousarray(ring_pos, dtype=np.int32)
+    qp = np.ascontiguousarray(qpos, dtype=np.int32)
+    assert rp.size == B * W and qp.size == B * V
+    ia = None
+    if idx is not None:
+        ia = np.ascontiguousarray(idx, dtype=np.int32)
+        assert ia.size == B * Hkv * n_idx
+    out = np.empty((B, V, Hq, d), dtype=np.float64)
+    lse = np.empty((B, V, Hq), dtype=np.float64)
+    logits = np.empty((B, V, Hq, n_idx * block + W), dtype=np.float64) if want_logits else None
+    _check(_load().oracle_gather_attend_ring(_ptr(qa), _ptr(ka), _ptr(va), qd, _ptr(ia), B, V, Hq, Hkv, d, T, n_idx,
+                                             block, float(scale), _ptr(rka), _ptr(rva), _ptr(rp), _ptr(qp), W,
+                                             _ptr(out), _ptr(lse), _ptr(logits)), "gather_attend_ring")
+    return out, lse, logits
+
+
+def ring_append(k_new, v_new, ring_k, ring_v, ring_pos, pos0):
+    """Appends n new tokens to the window-bounded ring (Adaptive DHiSparse, "Metodologia"):
+    token i of sequence b (position pos0[b] + i) goes to slot (pos0[b] + i) mod W.
+    k_new/v_new [B,Hkv,n,d]; ring_k/ring_v [B,Hkv,W,d] and ring_pos [B,W] (numpy arrays or
+    CPU tensors) are updated in place, token by token in order."""
+    B, Hkv, n, _ = k_new.shape
+    W = ring_pos.shape[-1]
+    for b in range(B):
+        for i in range(n):
+            pos = int(pos0[b]) + i
+            slot = pos % W
+            for h in range(Hkv):
+                ring_k[b, h, slot] = k_new[b, h, i]
+                ring_v[b, h, slot] = v_new[b, h, i]
+            ring_pos[b, slot] = pos
 
 
 def score_accumulate(logits, lse, idx, s, B, V, Hq, Hkv, n_idx, block, T, weight):

@@ -302,6 +302,94 @@ int oracle_gather_attend(const void* q, const void* K, const void* Vv, int dtype
 }
 
 /*
+ * Verify attention with the draft tokens' window-bounded ring.  Adaptive DHiSparse (news
+ * page), "Metodologia e Eficiencia de Carga": the verify queries share the fetch of the
+ * selected history rows, and the draft tokens' K/V live in a ring bounded by a window.
+ * Reading taken: the ring holds W slots per (b, kvh); ring_pos[b,s] is the token position
+ * slot s holds (-1 = empty); query token v of sequence b sits at position qpos[b,v].  Query
+ * row (b,v,h) attends the selected history rows (as oracle_gather_attend) and every ring
+ * slot s with 0 <= ring_pos[b,s] <= qpos[b,v] (causal among the drafts; the window bound
+ * is the ring's size).  List order: the n_idx*block history rows, then the W slots;
+ * logits [B,V,Hq,n_idx*block + W] with -inf where a row takes no part.
+ */
+int oracle_gather_attend_ring(const void* q, const void* K, const void* Vv, int dtype, const int32_t* idx, int B,
+                              int V, int Hq, int Hkv, int d, int T, int n_idx, int block, double scale,
+                              const void* ring_k, const void* ring_v, const int32_t* ring_pos,
+                              const int32_t* qpos, int W, double* out, double* lse, double* logits) {
+    if (Hkv < 1 || Hq % Hkv != 0 || d < 1 || block < 1 || n_idx < 0 || W < 0) return ORC_BAD_ARG;
+    if (idx == NULL && n_idx * block != T) return ORC_BAD_ARG;
+    const int G = Hq / Hkv;
+    const long n_rows = (long)n_idx * block, n_all = n_rows + W;
+    int bad = 0;
+#pragma omp parallel for collapse(3) schedule(dynamic) reduction(| : bad)
+    for (int b = 0; b < B; ++b)
+        for (int v = 0; v < V; ++v)
+            for (int h = 0; h < Hq; ++h) {
+                const int kvh = h / G;
+                const size_t qrow = (((size_t)b * V + v) * Hq + h);
+                double* qv = (double*)malloc(sizeof(double) * (size_t)d);
+                double* kr = (double*)malloc(sizeof(double) * (size_t)d);
+                double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+                double* z = (double*)malloc(sizeof(double) * (size_t)(n_all > 0 ? n_all : 1));
+                orc_load_row(q, dtype, qrow * d, d, qv);
+                /* z_j for every list row: history row, or ring slot j - n_rows */
+                double m = -INFINITY;
+                long n_valid = 0;
+                for (long j = 0; j < n_all; ++j) {
+                    z[j] = -INFINITY;
+                    if (j < n_rows) {
+                        long row = j;
+                        if (idx != NULL) {
+                            const long sel = idx[((size_t)b * Hkv + kvh) * n_idx + j / block];
+                            if (sel == -1) continue;
+                            row = sel * block + j % block;
+                            if (sel < 0 || row >= T) {
+                                bad = 1;
+                                continue;
+                            }
+                        }
+                        orc_load_row(K, dtype, (((size_t)b * Hkv + kvh) * T + row) * d, d, kr);
+                    } else {
+                        const long slot = j - n_rows;
+                        const long tpos = ring_pos[(size_t)b * W + slot];
+                        if (tpos < 0 || tpos > qpos[(size_t)b * V + v]) continue;
+                        orc_load_row(ring_k, dtype, (((size_t)b * Hkv + kvh) * W + slot) * d, d, kr);
+                    }
+                    double dot = 0.0;
+                    for (int c = 0; c < d; ++c) dot += qv[c] * kr[c];
+                    z[j] = scale * dot;
+                    if (z[j] > m) m = z[j];
+                    ++n_valid;
+                }
+                double l = 0.0;
+                for (int c = 0; c < d; ++c) acc[c] = 0.0;
+                for (long j = 0; j < n_all; ++j) {
+                    if (z[j] == -INFINITY) continue;
+                    const double wj = exp(z[j] - m);
+                    l += wj;
+                    if (j < n_rows) {
+                        const long row = idx != NULL ? (long)idx[((size_t)b * Hkv + kvh) * n_idx + j / block] * block +
+                                                           j % block
+                                                     : j;
+                        orc_load_row(Vv, dtype, (((size_t)b * Hkv + kvh) * T + row) * d, d, kr);
+                    } else {
+                        orc_load_row(ring_v, dtype, (((size_t)b * Hkv + kvh) * W + (j - n_rows)) * d, d, kr);
+                    }
+                    for (int c = 0; c < d; ++c) acc[c] += wj * kr[c];
+                }
+                for (int c = 0; c < d; ++c) out[qrow * d + c] = (n_valid > 0) ? acc[c] / l : 0.0;
+                lse[qrow] = (n_valid > 0) ? m + log(l) : -INFINITY;
+                if (logits != NULL)
+                    for (long j = 0; j < n_all; ++j) logits[qrow * n_all + j] = z[j];
+                free(qv);
+                free(kr);
+                free(acc);
+                free(z);
+            }
+    return bad ? ORC_BAD_INDEX : ORC_OK;
+}
+
+/*
  * Step 4 -- cumulative attention-importance score.  [HBM] Metodologia 2, the equation
  *   s_i(t) = s_i(t-1) + (1/|L|) sum over layers l of (1/H) sum over heads h of alpha_{l,h}(t)[i].
  * One call adds one layer's term with weight = 1/(|L| * H):

@@ -602,3 +602,110 @@ def test_attend_per_head_uses_each_heads_own_rows():
     o2, l2, _ = oracle.gather_attend(q, K, V, per.numpy(), B, Vq, Hq, Hkv, d, T, k, 1, 0.3, per_head=True)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(l1, l2)
+
+
+# ----------------------------------------------------------------------------- draft ring (verify)
+
+
+def _ring_case(seed, B=2, Vq=3, Hq=8, Hkv=2, d=16, T=90, k=7, W=6):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, Vq, Hq, d, generator=g)
+    K, V = torch.randn(B, Hkv, T, d, generator=g), torch.randn(B, Hkv, T, d, generator=g)
+    idx = torch.stack([torch.stack([torch.sort(torch.randperm(T, generator=g)[:k]).values
+                                    for _ in range(Hkv)]) for _ in range(B)]).to(torch.int32)
+    rk, rv = torch.randn(B, Hkv, W, d, generator=g), torch.randn(B, Hkv, W, d, generator=g)
+    # ring positions: some empty, the rest a window of recent positions in ring order
+    rpos = torch.full((B, W), -1, dtype=torch.int32)
+    for b in range(B):
+        n = W - b  # sequence 1 has one empty slot
+        first = T - 2
+        for i in range(n):
+            rpos[b, (first + i) % W] = first + i
+    qpos = torch.stack([torch.arange(T - 1, T - 1 + Vq) for _ in range(B)]).to(torch.int32)
+    return q, K, V, idx, rk, rv, rpos, qpos
+
+
+def test_ring_attend_equals_sdpa_over_each_querys_visible_rows():
+    q, K, V, idx, rk, rv, rpos, qpos = _ring_case(41)
+    B, Vq, Hq, d = q.shape
+    Hkv, T, W = K.shape[1], K.shape[2], rpos.shape[1]
+    G, k = Hq // Hkv, idx.shape[-1]
+    out, lse, z = oracle.gather_attend_ring(q, K, V, idx.numpy(), B, Vq, Hq, Hkv, d, T, k, 1, 0.4, rk, rv,
+                                            rpos.numpy(), qpos.numpy(), want_logits=True)
+    for b in range(B):
+        for v in range(Vq):
+            vis = [s for s in range(W) if 0 <= int(rpos[b, s]) <= int(qpos[b, v])]
+            for h in range(Hq):
+                kvh = h // G
+                Kr = torch.cat([K[b, kvh, idx[b, kvh].long()], rk[b, kvh, vis]])[None, None]
+                Vr = torch.cat([V[b, kvh, idx[b, kvh].long()], rv[b, kvh, vis]])[None, None]
+                ro, rl = _sdpa_reference(q[b:b + 1, v:v + 1, h:h + 1], Kr, Vr, 0.4)
+                np.testing.assert_allclose(out[b, v, h], ro[0, 0, 0], atol=1e-12)
+                np.testing.assert_allclose(lse[b, v, h], rl[0, 0, 0], atol=1e-12)
+                hidden = [s for s in range(W) if s not in vis]
+                assert np.all(np.isneginf(z[b, v, h, k + np.array(hidden, dtype=int)]))
+                assert np.all(np.isfinite(z[b, v, h, k + np.array(vis, dtype=int)]))
+
+
+def test_ring_causal_among_drafts_and_reductions():
+    q, K, V, idx, rk, rv, rpos, qpos = _ring_case(42, W=8)
+    B, Vq, Hq, d = q.shape
+    Hkv, T, W = K.shape[1], K.shape[2], rpos.shape[1]
+    k = idx.shape[-1]
+    args = (q, K, V, idx.numpy(), B, Vq, Hq, Hkv, d, T, k, 1, 0.3, rk, rv)
+    # an empty ring is plain gather-attend, bit for bit
+    empty = np.full((B, W), -1, dtype=np.int32)
+    o0, l0, _ = oracle.gather_attend_ring(*args, empty, qpos.numpy())
+    o1, l1, _ = oracle.gather_attend(q, K, V, idx.numpy(), B, Vq, Hq, Hkv, d, T, k, 1, 0.3)
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
+    # a ring entirely in every query's past: plain gather-attend over the history rows
+    # followed by the ring rows as extra cache rows selected after them
+    past = np.tile(np.arange(W, dtype=np.int32), (B, 1))
+    Kx, Vx = torch.cat([K, rk], dim=2), torch.cat([V, rv], dim=2)
+    idx_x = torch.cat([idx, torch.arange(T, T + W, dtype=torch.int32).expand(B, Hkv, W)], dim=2)
+    o2, l2, _ = oracle.gather_attend_ring(*args, past, np.full((B, Vq), T, dtype=np.int32))
+    o3, l3, _ = oracle.gather_attend(q, Kx, Vx, idx_x.numpy(), B, Vq, Hq, Hkv, d, T + W, k + W, 1, 0.3)
+    np.testing.assert_array_equal(o2, o3)
+    np.testing.assert_array_equal(l2, l3)
+    # the V draft tokens in the ring: draft v sees drafts 0..v only; slot order is irrelevant
+    drafts = np.full((B, W), -1, dtype=np.int32)
+    for b in range(B):
+        for v in range(Vq):
+            drafts[b, (5 + v) % W] = 100 + v
+    qp = np.tile(np.arange(100, 100 + Vq, dtype=np.int32), (B, 1))
+    _, _, z = oracle.gather_attend_ring(*args, drafts, qp, want_logits=True)
+    for b in range(B):
+        for v in range(Vq):
+            for u in range(Vq):
+                col = k + (5 + u) % W
+                assert np.isfinite(z[b, v, 0, col]) == (u <= v)
+    perm = np.random.default_rng(0).permutation(W)
+    o4, l4, _ = oracle.gather_attend_ring(*args, drafts, qp)
+    o5, l5, _ = oracle.gather_attend_ring(q, K, V, idx.numpy(), B, Vq, Hq, Hkv, d, T, k, 1, 0.3, rk[:, :, perm],
+                                          rv[:, :, perm], drafts[:, perm], qp)
+    np.testing.assert_allclose(o4, o5, atol=1e-13)
+    np.testing.assert_allclose(l4, l5, atol=1e-13)
+
+
+def test_ring_append_keeps_the_last_window():
+    g = torch.Generator().manual_seed(43)
+    B, Hkv, d, W = 2, 3, 4, 5
+    ring_k, ring_v = np.zeros((B, Hkv, W, d)), np.zeros((B, Hkv, W, d))
+    ring_pos = np.full((B, W), -1, dtype=np.int32)
+    toks_k = torch.randn(B, Hkv, 23, d, generator=g).numpy()
+    toks_v = torch.randn(B, Hkv, 23, d, generator=g).numpy()
+    pos0 = np.array([0, 0])
+    for n in (3, 1, 8, 4, 7):  # appends of varying size, wrapping the ring several times
+        oracle.ring_append(toks_k[:, :, pos0[0]:pos0[0] + n], toks_v[:, :, pos0[0]:pos0[0] + n], ring_k, ring_v,
+                           ring_pos, pos0)
+        pos0 = pos0 + n
+        held = np.sort(ring_pos, axis=1)
+        want = np.arange(max(0, pos0[0] - W), pos0[0])
+        assert np.array_equal(held[0][held[0] >= 0], want)
+        for b in range(B):
+            for s in range(W):
+                if ring_pos[b, s] >= 0:
+                    assert s == ring_pos[b, s] % W
+                    np.testing.assert_array_equal(ring_k[b, :, s], toks_k[b, :, ring_pos[b, s]])
+                    np.testing.assert_array_equal(ring_v[b, :, s], toks_v[b, :, ring_pos[b, s]])
