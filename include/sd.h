@@ -171,6 +171,12 @@ sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx, uin
  * workspace must not overlap on the GPU.  splits = 0 picks one wave of CTAs for this GPU;
  * a requested split count is adjusted to at least one 64-row chunk per split and at most
  * 448 rows per split when rows are selected through idx or slot_map.
+ * Draft ring ([DHiSparse] "Metodologia": the draft tokens' K/V live in a ring bounded by a
+ * window; reading taken: the verify queries attend it causally): with ring_w > 0 the list
+ * of every group is the n_idx*block selected rows followed by the ring_w slots of its KV
+ * head's ring, and query token v of sequence b attends slot s only when
+ * 0 <= ring_pos[b,s] <= qpos[b,v] (z = -inf otherwise); logits then have n_idx*block +
+ * ring_w columns.  sd_ring_append fills the ring.
  * Staged host rows: with slot_map and k_stage/v_stage set, a row whose slot is -1 is read
  * from the stage at [group, j] (j = its position in the group's selection list, group =
  * b*Hkv + kvh, or b*Hq + h with per_head) instead of host memory; the stage must hold what
@@ -203,6 +209,11 @@ typedef struct {
     int per_head;             /* 1: idx is [B,Hq,n_idx], one selection per query head */
     const void* k_stage;      /* nullable HBM stage [groups, n_idx*block, d] (sd_stage_host_rows) */
     const void* v_stage;      /* same layout as k_stage; both set or both NULL */
+    const void* ring_k;       /* draft ring [B,Hkv,ring_w,d] (device, dtype), or NULL */
+    const void* ring_v;       /* same layout as ring_k */
+    const int32_t* ring_pos;  /* [B,ring_w] token position held by each slot, -1 = empty */
+    const int32_t* qpos;      /* [B,V] token position of each query token */
+    int ring_w;               /* ring slots; 0 = no ring */
 } sd_attend_args;
 
 size_t sd_gather_attend_workspace_bytes(const sd_attend_args* args);
@@ -250,6 +261,18 @@ sd_status sd_gather_attend_noalloc(const sd_attend_args* args, void* stream);
 sd_status sd_stage_host_rows(const sd_attend_args* args, uint32_t* counter, void* stream);
 
 /*
+ * sd_ring_append -- write new tokens' K/V into the window-bounded draft ring.
+ * [DHiSparse] "Metodologia" (the draft tokens' K/V live in a ring bounded by a window).
+ * Token i < n of sequence b, at position pos0[b] + i, goes to slot (pos0[b] + i) mod W:
+ * ring_k/ring_v[b, h, slot, :] = k_new/v_new[b, h, i, :] for every KV head h, and
+ * ring_pos[b, slot] = pos0[b] + i.  k_new, v_new [B,Hkv,n,d] and ring_k, ring_v
+ * [B,Hkv,W,d] of `dtype`; ring_pos [B,W] int32; pos0 [B] int32 (device, >= 0).  Limits:
+ * 1 <= n <= W (no slot is written twice in one call), d in {64, 128}.
+ */
+sd_status sd_ring_append(const void* k_new, const void* v_new, sd_dtype dtype, int B, int Hkv, int n, int d,
+                         void* ring_k, void* ring_v, int32_t* ring_pos, const int32_t* pos0, int W, void* stream);
+
+/*
  * sd_select_attend -- sd_topk and sd_gather_attend fused in one launch.
  * [Illusion] sec. 2 "Mecanismos de Esparsidade" (Oracle Top-K feeding a sparse decode
  * kernel) and sec. 3C; [SparDA] sec. 2 item 1 (top-k blocks); [DHiSparse] "Metodologia"
@@ -258,7 +281,8 @@ sd_status sd_stage_host_rows(const sd_attend_args* args, uint32_t* counter, void
  * sd_gather_attend(args with idx) computes: idx [B,Hkv,n_idx] int32 (written, ascending,
  * bit-identical to sd_topk), out, lse and optional logits as sd_gather_attend defines
  * them, with the selection list of every (b, kvh) taken from idx.  args->idx, workspace,
- * workspace_bytes, k_stage and v_stage are ignored; k = args->n_idx.  scores [B*Hkv, N] fp32 with
+ * workspace_bytes, k_stage and v_stage are ignored; k = args->n_idx; a draft ring
+ * (ring_w > 0) is not supported here (SD_ERR_UNSUPPORTED: use the separate calls).  scores [B*Hkv, N] fp32 with
  * N * args->block == args->T (one score per token, or per block of `block` tokens).
  * key_hist: nullable, as in sd_topk (the indexer's histogram of exactly these scores;
  * zero-filled again by the call).  args->splits: CTAs per (b, kvh), 0 = automatic, at most

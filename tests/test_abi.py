@@ -138,3 +138,24 @@ def test_stage_host_rows_validation(lib):
     a.workspace, a.workspace_bytes = 16, 1 << 30
     assert lib.sd_gather_attend(ctypes.byref(a), None) == 1
     assert b"go together" in lib.sd_last_error_message()
+
+
+def test_ring_validation(lib):
+    from top_sparse_decode_gqa_gb300.binding import sd_attend_args
+    dummy = ctypes.c_void_p(16)
+    # sd_ring_append: n must be in [1, W]; d 64 or 128
+    assert lib.sd_ring_append(dummy, dummy, 1, 2, 8, 9, 128, dummy, dummy, dummy, dummy, 8, None) == 1
+    assert lib.sd_ring_append(dummy, dummy, 1, 2, 8, 0, 128, dummy, dummy, dummy, dummy, 8, None) == 1
+    assert lib.sd_ring_append(dummy, dummy, 1, 2, 8, 4, 96, dummy, dummy, dummy, dummy, 8, None) == 2
+    assert lib.sd_ring_append(None, None, 1, 0, 8, 4, 128, None, None, None, None, 8, None) == 0
+    a = sd_attend_args()
+    a.q = a.k_cache = a.v_cache = a.out = a.lse = a.idx = 16
+    a.dtype, a.B, a.V, a.Hq, a.Hkv, a.d, a.T = 1, 2, 8, 32, 8, 128, 4096
+    a.pool_rows, a.n_idx, a.block, a.scale = 4096, 64, 1, 0.1
+    # a ring needs its four arrays
+    a.ring_w = 64
+    assert lib.sd_gather_attend(ctypes.byref(a), None) == 1
+    assert b"ring" in lib.sd_last_error_message()
+    a.ring_k = a.ring_v = a.ring_pos = a.qpos = 16
+    # the fused select/attend has no ring
+    assert lib.sd_select_attend(dummy, 4096, None, dummy, ctypes.byref(a), None) == 2

@@ -27,7 +27,7 @@ EXPORTS = (
     "sd_topk_workspace_bytes", "sd_topk", "sd_gather_attend_workspace_bytes", "sd_gather_attend",
     "sd_score_accumulate", "sd_tier_classify_workspace_bytes", "sd_tier_classify",
     "sd_quantize_rows_int8", "sd_gather_attend_noalloc", "sd_select_attend", "sd_window_count",
-    "sd_window_max", "sd_window_union", "sd_index_score_heads", "sd_stage_host_rows",
+    "sd_window_max", "sd_window_union", "sd_index_score_heads", "sd_stage_host_rows", "sd_ring_append",
 )
 
 
@@ -49,6 +49,8 @@ class sd_attend_args(ctypes.Structure):
         ("err_word", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t), ("splits", ctypes.c_int), ("per_head", ctypes.c_int),
         ("k_stage", ctypes.c_void_p), ("v_stage", ctypes.c_void_p),
+        ("ring_k", ctypes.c_void_p), ("ring_v", ctypes.c_void_p), ("ring_pos", ctypes.c_void_p),
+        ("qpos", ctypes.c_void_p), ("ring_w", ctypes.c_int),
     ]
 
 
@@ -79,6 +81,7 @@ def lib() -> ctypes.CDLL:
         L.sd_select_attend.argtypes = [P, I, P, P, ctypes.POINTER(sd_attend_args), P]
         L.sd_index_score_heads.argtypes = [P, I, P, I, I, I, I, I, I, P, P, P, P]
         L.sd_stage_host_rows.argtypes = [ctypes.POINTER(sd_attend_args), P, P]
+        L.sd_ring_append.argtypes = [P, P, I, I, I, I, I, P, P, P, P, I, P]
         L.sd_window_count.argtypes = [I, I, I]
         L.sd_window_count.restype = I
         L.sd_window_max.argtypes = [P, I, I, I, I, P, P, P]
@@ -213,7 +216,7 @@ def sd_topk(scores: torch.Tensor, k: int, idx: Optional[torch.Tensor] = None,
 def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=None, scale=None,
                      k_host=None, v_host=None, slot_map=None, out=None, lse=None, logits=None,
                      want_logits=False, err_word=None, splits=0, per_head=False, k_stage=None,
-                     v_stage=None) -> tuple:
+                     v_stage=None, ring_k=None, ring_v=None, ring_pos=None, qpos=None) -> tuple:
     """Fill an sd_attend_args from tensors; returns (args, out, lse, logits)."""
     _dev(q, "q")
     B, V, Hq, d = q.shape
@@ -233,8 +236,9 @@ def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=No
         out = torch.empty((B, V, Hq, d), dtype=torch.float32, device=dev)
     if lse is None:
         lse = torch.empty((B, V, Hq), dtype=torch.float32, device=dev)
+    ring_w = ring_pos.shape[-1] if ring_pos is not None else 0
     if logits is None and want_logits:
-        logits = torch.empty((B, V, Hq, n_idx * block), dtype=torch.float32, device=dev)
+        logits = torch.empty((B, V, Hq, n_idx * block + ring_w), dtype=torch.float32, device=dev)
     for name, t in (("k_host", k_host), ("v_host", v_host)):
         if t is not None and (t.is_cuda or not t.is_pinned() or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous pinned host tensor")
@@ -253,10 +257,12 @@ def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=No
     a.err_word = err_word.data_ptr() if err_word is not None else None
     a.splits = splits
     a.per_head = 1 if per_head else 0
-    for name, t in (("k_stage", k_stage), ("v_stage", v_stage)):
+    for name, t in (("k_stage", k_stage), ("v_stage", v_stage), ("ring_k", ring_k), ("ring_v", ring_v),
+                    ("ring_pos", ring_pos), ("qpos", qpos)):
         if t is not None:
             _dev(t, name)
             setattr(a, name, t.data_ptr())
+    a.ring_w = ring_w
     return a, out, lse, logits
 
 
@@ -306,6 +312,25 @@ def sd_stage_host_rows(args: sd_attend_args, counter: torch.Tensor, stream=None)
     (see stage_buffers); counter from stage_counter, left at zero."""
     _dev(counter, "counter")
     _check(lib().sd_stage_host_rows(ctypes.byref(args), _ptr(counter), _stream(stream)), "sd_stage_host_rows")
+
+
+def ring_buffers(B: int, Hkv: int, W: int, d: int, dtype: torch.dtype, device="cuda") -> tuple:
+    """An empty draft ring: (ring_k, ring_v) [B,Hkv,W,d] zeros and ring_pos [B,W] = -1."""
+    rk = torch.zeros((B, Hkv, W, d), dtype=dtype, device=device)
+    return rk, torch.zeros_like(rk), torch.full((B, W), -1, dtype=torch.int32, device=device)
+
+
+def sd_ring_append(k_new: torch.Tensor, v_new: torch.Tensor, ring_k: torch.Tensor, ring_v: torch.Tensor,
+                   ring_pos: torch.Tensor, pos0: torch.Tensor, stream=None) -> None:
+    """Writes k_new/v_new [B,Hkv,n,d] into the ring at slots (pos0[b] + i) mod W and records
+    the positions in ring_pos [B,W]."""
+    for name, t in (("k_new", k_new), ("v_new", v_new), ("ring_k", ring_k), ("ring_v", ring_v),
+                    ("ring_pos", ring_pos), ("pos0", pos0)):
+        _dev(t, name)
+    B, Hkv, n, d = k_new.shape
+    W = ring_k.shape[2]
+    _check(lib().sd_ring_append(_ptr(k_new), _ptr(v_new), _dtype_code(k_new), B, Hkv, n, d, _ptr(ring_k),
+                                _ptr(ring_v), _ptr(ring_pos), _ptr(pos0), W, _stream(stream)), "sd_ring_append")
 
 
 def sd_select_attend(scores: torch.Tensor, args: sd_attend_args, idx: torch.Tensor,

@@ -25,6 +25,7 @@ constexpr int kMmaWarps = 4;          // warps of a CTA that run the attention l
 constexpr int kSub = 16;              // rows per warp sub-chunk
 constexpr int kWStages = 2;           // sub-chunks in flight per warp (default)
 constexpr int32_t kNoRow = INT32_MIN;  // source code of a skipped row (contributes nothing)
+constexpr int32_t kRingBase = 1 << 30;  // codes >= this: slot code - kRingBase of the draft ring
 constexpr float kLn2f = 0.69314718055994530942f;
 
 template <int D, int NW = kMmaWarps, int NS = kWStages>
@@ -48,14 +49,22 @@ SD_DEVINL void cp_async_wait_dyn(int n) {
     else cp_async_wait<0>();
 }
 
-// Where a row's bytes are: code >= 0 is row `code` of the device pool (k_pool + code * row
-// bytes, already offset to this (b, kvh)); code < 0 is host row -1 - code of the mapped
-// host cache (k_host likewise offset); kNoRow is skipped.
+// Where a row's bytes are: code >= kRingBase is slot code - kRingBase of the draft ring
+// (k_ring + slot * row bytes, offset to this (b, kvh)); other code >= 0 is row `code` of the
+// device pool (k_pool + code * row bytes, likewise offset); code < 0 is host row -1 - code
+// of the mapped host cache (k_host likewise offset); kNoRow is skipped.
 struct RowSource {
     const uint8_t* k_pool;
     const uint8_t* v_pool;
     const uint8_t* k_host;
     const uint8_t* v_host;
+    const uint8_t* k_ring = nullptr;
+    const uint8_t* v_ring = nullptr;
+};
+
+// Visibility of list row j to query row r when every row is visible to every query.
+struct AllVisible {
+    SD_DEVINL bool operator()(int, int) const { return true; }
 };
 
 template <int D, int RP>
@@ -81,10 +90,12 @@ struct WarpAcc {
 // memory, `q_base` the shared address of the RP query rows (kRowB apart, pre-loaded, rows
 // beyond the real ones zero).  row_code(j) returns the source of list row j (kNoRow for a
 // skipped row; called only for j < nrows).  logit(r, j, x) receives every (query row,
-// list row) score in base-2 units (x * ln 2 is the natural logit) of valid rows.
-template <int D, int RP, int NW = kMmaWarps, int NS = kWStages, class RowCode, class Logit>
+// list row) score in base-2 units (x * ln 2 is the natural logit) of valid rows, -inf where
+// vis(r, j) hides the row from the query row (the causal mask of the draft ring).
+template <int D, int RP, int NW = kMmaWarps, int NS = kWStages, class RowCode, class Logit, class Vis = AllVisible>
 SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_base, int warp, int nrows,
-                               const RowSource& rs, float scale_log2, RowCode row_code, Logit logit) {
+                               const RowSource& rs, float scale_log2, RowCode row_code, Logit logit,
+                               Vis vis = Vis()) {
     static_assert(NS >= 2 && NS <= 4, "2 to 4 stages per warp");
     using L = MmaRows<D, NW, NS>;
     constexpr int MT = RP / 16, KS = D / 16, NT = D / 8;
@@ -113,7 +124,9 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
 #pragma unroll
                     for (int h = 0; h < PPR / 8; ++h) *reinterpret_cast<uint4*>(dst + h * 128) = make_uint4(0u, 0u, 0u, 0u);
                 } else {
-                    const uint8_t* srow = code[q] >= 0
+                    const uint8_t* srow = code[q] >= kRingBase
+                        ? (which ? rs.v_ring : rs.k_ring) + (size_t)(code[q] - kRingBase) * (D * 2)
+                        : code[q] >= 0
                         ? (which ? rs.v_pool : rs.k_pool) + (size_t)code[q] * (D * 2)
                         : (which ? rs.v_host : rs.k_host) + (size_t)(-1 - (long)code[q]) * (D * 2);
                     srow += piece * 16;
@@ -170,13 +183,15 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
         for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
+                const int r = mt * 16 + g + 8 * hf;
                 float x[2][2];
                 float tmax = -INFINITY;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        x[nt][e] = kval[nt][e] ? sacc[mt][nt][2 * hf + e] * scale_log2 : -INFINITY;
+                        const bool on = kval[nt][e] && vis(r, c * kSub + nt * 8 + 2 * t4 + e);
+                        x[nt][e] = on ? sacc[mt][nt][2 * hf + e] * scale_log2 : -INFINITY;
                         tmax = fmaxf(tmax, x[nt][e]);
                     }
                 tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
@@ -204,7 +219,6 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
                         acc.o[mt][nt][2 * hf + 1] *= alpha;
                     }
                 }
-                const int r = mt * 16 + g + 8 * hf;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll

@@ -43,7 +43,13 @@ struct AttendParams {
     int kv_heads, heads_per_kv;  // KV heads of the cache; groups per KV head (per-head mode: G)
     int dtype;
     int resolve;  // 1: sources resolved up front (idx or slot_map given)
-    int staged;   // 1: kh/vh are the HBM stage [groups, n_rows, d], host rows by list position
+    int staged;   // 1: kh/vh are the HBM stage [groups, n_hist, d], host rows by list position
+    int n_hist;   // selected (history) list rows; list rows [n_hist, n_rows) are the draft ring's slots
+    int ring_w;   // draft ring slots (0: none)
+    const uint8_t* rk;        // draft ring [B, kv_heads, ring_w, d]
+    const uint8_t* rv;
+    const int32_t* ring_pos;  // [B, ring_w] token position per slot, -1 empty
+    const int32_t* qpos;      // [B, V] position of each query token
     float scale_log2;
     float* out;
     float* lse;
@@ -212,7 +218,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
     const int bk = b * p.Hkv + kvh;
     const int kvsrc = b * p.kv_heads + kvh / p.heads_per_kv;  // the (b, KV head) slab the rows come from
     // host rows: the (b, KV head) slab of the host cache, or this group's rows of the stage
-    const size_t host_row0 = p.staged ? (size_t)bk * p.n_rows : (size_t)kvsrc * p.T;
+    const size_t host_row0 = p.staged ? (size_t)bk * p.n_hist : (size_t)kvsrc * p.T;
     const size_t esz = sizeof(ST);
 
     pdl_wait();  // everything below may read what the preceding kernel wrote
@@ -237,6 +243,10 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
     // ---- resolve every row's source once: >= 0 device row (pool slot, or cache
     // position without a slot map), < 0 host row -1 - position, kNoRow skipped
     auto resolve_row = [&](int jg) -> int32_t {
+        if (jg >= p.n_hist) {  // draft ring slot: skipped when empty
+            const int slot = jg - p.n_hist;
+            return p.ring_pos[(size_t)b * p.ring_w + slot] < 0 ? kNoRow : kRingBase + slot;
+        }
         long pos = jg;
         if (p.idx != nullptr) {
             const long sel = p.idx[(size_t)bk * p.n_idx + jg / p.block];
@@ -258,6 +268,12 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
         for (int j = tid; j < nrows; j += kAttThreads) src[j] = resolve_row(j0 + j);
     __syncthreads();
     auto row_code = [&](int j) -> int32_t { return p.resolve ? src[j] : (int32_t)(j0 + j); };
+    // a draft-ring row is visible to query row r (token v = r / G) up to its own position
+    auto visible = [&](int r, int j) -> bool {
+        const int32_t code = row_code(j);
+        if (code < kRingBase || r >= p.R) return true;
+        return p.ring_pos[(size_t)b * p.ring_w + (code - kRingBase)] <= p.qpos[(size_t)b * p.V + r / p.G];
+    };
 
     auto issue = [&](int c, int bf) {
         uint8_t* kdst = sm + L::oK + bf * kCH * L::kKRow;
@@ -275,7 +291,10 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
             }
             const uint8_t* base;
             size_t row;
-            if (code >= 0) {
+            if (code >= kRingBase) {
+                base = which ? p.rv : p.rk;
+                row = (size_t)kvsrc * p.ring_w + (code - kRingBase);
+            } else if (code >= 0) {
                 base = which ? p.vc : p.kc;
                 row = (size_t)kvsrc * p.pool_rows + code;
             } else {
@@ -329,7 +348,8 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
                 }
             }
 #pragma unroll
-            for (int r = 0; r < RP / 2; ++r) ss[(hf * (RP / 2) + r) * L::kSRow + j] = valid ? s[r] : -INFINITY;
+            for (int r = 0; r < RP / 2; ++r)
+                ss[(hf * (RP / 2) + r) * L::kSRow + j] = valid && visible(hf * (RP / 2) + r, c * kCH + j) ? s[r] : -INFINITY;
         }
         __syncthreads();
 
@@ -502,6 +522,11 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     if (p.resolve) {
         for (int j = tid; j < nrows; j += kAttThreads) {
             const int jg = j0 + j;
+            if (jg >= p.n_hist) {  // draft ring slot: skipped when empty
+                const int slot = jg - p.n_hist;
+                src[j] = p.ring_pos[(size_t)b * p.ring_w + slot] < 0 ? kNoRow : kRingBase + slot;
+                continue;
+            }
             long pos = jg;
             int32_t code;
             bool ok = true;
@@ -540,9 +565,13 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     RowSource rs;
     rs.k_pool = p.kc + (size_t)kvsrc * p.pool_rows * (D * 2);
     rs.v_pool = p.vc + (size_t)kvsrc * p.pool_rows * (D * 2);
-    const size_t host_row0 = p.staged ? (size_t)bk * p.n_rows : (size_t)kvsrc * p.T;
+    const size_t host_row0 = p.staged ? (size_t)bk * p.n_hist : (size_t)kvsrc * p.T;
     rs.k_host = p.kh + host_row0 * (D * 2);
     rs.v_host = p.vh + host_row0 * (D * 2);
+    if (p.ring_w > 0) {
+        rs.k_ring = p.rk + (size_t)kvsrc * p.ring_w * (D * 2);
+        rs.v_ring = p.rv + (size_t)kvsrc * p.ring_w * (D * 2);
+    }
     auto row_code = [&](int j) -> int32_t { return p.resolve ? src[j] : (int32_t)(j0 + j); };
     float* lbase = nullptr;  // logits of query row 0 of this group, at list row j0
     if (p.logits != nullptr) lbase = p.logits + ((size_t)b * p.V * p.Hq + kvh * p.G) * p.n_rows + j0;
@@ -552,10 +581,16 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
             lbase[((size_t)v * p.Hq + gg) * p.n_rows + j] = x * kLn2;
         }
     };
+    // a draft-ring row is visible to query row r (token v = r / G) up to its own position
+    auto visible = [&](int r, int j) -> bool {
+        const int32_t code = row_code(j);
+        if (code < kRingBase || r >= p.R) return true;
+        return p.ring_pos[(size_t)b * p.ring_w + (code - kRingBase)] <= p.qpos[(size_t)b * p.V + r / p.G];
+    };
     WarpAcc<D, RP> acc;
     acc.init();
     mma_attend_warp<D, RP>(acc, sm + L::oStage + warp * Rows::kWarpBytes, smem_addr(sm + L::oQ), warp, nrows, rs,
-                           p.scale_log2, row_code, logit);
+                           p.scale_log2, row_code, logit, visible);
 
     float* ow = reinterpret_cast<float*>(sm + L::oStage);  // [4][RP][D]
     mma_combine_warps<D, RP>(acc, mlw, rowv, ow);
@@ -624,11 +659,11 @@ size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 // sources are resolved up front.  Partials [bk][split][RP][d] + m, l, then counters.
 SplitPlan plan_splits(const sd_attend_args* a) {
     SplitPlan sp{};
-    const long n_rows = (long)a->n_idx * a->block;
+    const long n_rows = (long)a->n_idx * a->block + a->ring_w;
     const long bk = (long)a->B * (a->per_head ? a->Hq : a->Hkv);
     sp.RP = kernel_rows(a->dtype, a->per_head ? a->V : (a->Hkv > 0 ? (a->Hq / a->Hkv) * a->V : 0));
     const long chunks = (n_rows + kCH - 1) / kCH;
-    const bool resolve = a->idx != nullptr || a->slot_map != nullptr;
+    const bool resolve = a->idx != nullptr || a->slot_map != nullptr || a->ring_w > 0;
     long splits;
     if (a->splits > 0) {
         splits = a->splits;
@@ -710,6 +745,13 @@ sd_status sd::validate_attend_args(const sd_attend_args* a, const char* who) {
     SD_REQUIRE(a->B <= 65535 && a->Hq <= 65535, "%s: B and Hq must be <= 65535", who);
     SD_REQUIRE(a->per_head == 0 || a->per_head == 1, "%s: per_head must be 0 or 1", who);
     SD_REQUIRE(!a->per_head || a->idx != nullptr || a->n_idx == 0, "%s: per_head needs idx", who);
+    SD_REQUIRE(a->ring_w >= 0 && a->ring_w <= (1 << 20), "%s: ring_w must be in [0, 2^20]", who);
+    if (a->ring_w > 0) {
+        SD_REQUIRE(a->ring_k && a->ring_v && a->ring_pos && a->qpos, "%s: a ring needs ring_k, ring_v, ring_pos and qpos",
+                   who);
+        SD_REQUIRE(aligned16(a->ring_k) && aligned16(a->ring_v), "%s: ring_k/ring_v must be 16-byte aligned", who);
+    }
+    SD_REQUIRE(a->T < kRingBase && a->pool_rows < kRingBase, "%s: T and pool_rows must be < 2^30", who);
     return SD_OK;
 }
 
@@ -749,7 +791,15 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
     p.T = a->T;
     p.n_idx = a->n_idx;
     p.block = a->block;
-    p.n_rows = a->n_idx * a->block;
+    p.n_hist = a->n_idx * a->block;
+    p.n_rows = p.n_hist + a->ring_w;
+    p.ring_w = a->ring_w;
+    if (a->ring_w > 0) {
+        p.rk = static_cast<const uint8_t*>(a->ring_k);
+        p.rv = static_cast<const uint8_t*>(a->ring_v);
+        p.ring_pos = a->ring_pos;
+        p.qpos = a->qpos;
+    }
     p.dtype = a->dtype;
     p.scale_log2 = a->scale * kLog2e;
     p.out = a->out;
@@ -794,7 +844,7 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
         p.ws_l = p.ws_m + np;
         p.counters = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a->workspace) + sp.counters_offset);
     }
-    p.resolve = (a->idx != nullptr || a->slot_map != nullptr) ? 1 : 0;
+    p.resolve = (a->idx != nullptr || a->slot_map != nullptr || a->ring_w > 0) ? 1 : 0;
     cudaStream_t st = as_stream(stream);
     return a->d == 128 ? dispatch_rp<128>(p, a->dtype, sp.RP, st) : dispatch_rp<64>(p, a->dtype, sp.RP, st);
 }
