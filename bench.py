@@ -415,6 +415,81 @@ class HeadsStep:
                 "hbm": key_bytes + q_bytes + kv + out_bytes, "host": 0}
 
 
+class VerifyGroupStep:
+    """One speculative-verify step over a group of layers that share one selection: the
+    indexer and the top-k once, then for every layer the V draft tokens' K/V appended to the
+    layer's window-bounded ring and the attention over the selected rows plus the ring
+    (causal among the drafts)."""
+
+    dominant = "sd_index_score"
+    phases = ("after_topk",)
+    dominant_per_step = 1
+
+    def __init__(self, w, x, device):
+        import torch
+        from top_sparse_decode_gqa_gb300 import binding as sd
+        self.sd, self.w, self.dev = sd, w, device
+        self.launches_per_step = 2 + 2 * w.layers
+        self.q_idx, self.k_idx = x["q_idx"].to(device), x["k_idx"].to(device)
+        self.q = x["q"][0].to(device)                       # [layers,B,V,Hq,d]
+        self.ks = [k.to(device) for k in x["k"]]
+        self.vs = [v.to(device) for v in x["v"]]
+        self.ring_k, self.ring_v = x["ring_k"].to(device), x["ring_v"].to(device)
+        self.ring_pos = [x["ring_pos"].to(device) for _ in range(w.layers)]
+        self.draft_k, self.draft_v = x["draft_k"].to(device), x["draft_v"].to(device)
+        self.qpos = x["qpos"].to(device)
+        self.pos0 = torch.full((w.B,), w.T, dtype=torch.int32, device=device)
+        self.scores = torch.empty(w.B, w.Hkv, w.N, dtype=torch.float32, device=device)
+        self.idx = torch.empty(w.B, w.Hkv, w.k, dtype=torch.int32, device=device)
+        self.key_hist = sd.key_hist_buffer(w.B * w.Hkv, device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.args = []
+        for layer in range(w.layers):
+            a, out, lse, _ = sd.make_attend_args(self.q[layer], self.ks[layer], self.vs[layer], self.idx, T=w.T,
+                                                 err_word=self.err, ring_k=self.ring_k[layer],
+                                                 ring_v=self.ring_v[layer], ring_pos=self.ring_pos[layer],
+                                                 qpos=self.qpos)
+            self.args.append((a, out, lse))
+        need = sd.sd_gather_attend_workspace_bytes(self.args[0][0])
+        self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=device)
+        self.out, self.lse = self.args[-1][1], self.args[-1][2]
+
+    def run(self, m: "StepMarks" = None):
+        sd, w = self.sd, self.w
+        if m is not None:
+            m.start.record()
+            m.before(0)
+        sd.sd_index_score(self.q_idx, self.k_idx, self.scores, self.err, key_hist=self.key_hist)
+        if m is not None:
+            m.after(0)
+        sd.sd_topk(self.scores, w.k, self.idx, key_hist=self.key_hist)
+        if m is not None:
+            m.at("after_topk")
+        for layer in range(w.layers):
+            sd.sd_ring_append(self.draft_k[layer], self.draft_v[layer], self.ring_k[layer], self.ring_v[layer],
+                              self.ring_pos[layer], self.pos0)
+            sd.sd_gather_attend(self.args[layer][0], self.ws)
+        if m is not None:
+            m.end.record()
+
+    def after_warmup(self):
+        pass
+
+    def bytes(self):
+        w = self.w
+        e = w.elem_bytes
+        key_bytes = w.B * w.Hkv * w.T * w.dI * e
+        q_idx_bytes = w.B * w.Hkv * w.V * w.dI * e
+        score_bytes = w.B * w.Hkv * w.T * 4
+        row = w.d * e * 2
+        per_layer = (w.B * w.Hkv * (w.k + w.ring_w) * row            # selected rows + ring read
+                     + w.B * w.Hkv * w.V * row * 2                     # drafts read and written into the ring
+                     + w.B * w.V * w.Hq * w.d * e                      # queries
+                     + w.B * w.V * w.Hq * (w.d + 1) * 4)               # out, lse
+        return {"dominant": key_bytes + q_idx_bytes + score_bytes,
+                "hbm": key_bytes + q_idx_bytes + w.B * w.Hkv * w.k * 4 + w.layers * per_layer, "host": 0}
+
+
 class DenseScoringStep:
     """One decode step of the importance-scoring workload: for every layer, dense attention
     over all cached rows (logits kept) and that layer's term of the importance score."""
@@ -485,6 +560,8 @@ class DenseScoringStep:
 
 
 def make_step(w, x, device, separate=False, tiered_path="staged"):
+    if w.ring_w > 0:
+        return VerifyGroupStep(w, x, device)
     if w.layers > 1:
         return DenseScoringStep(w, x, device)
     if w.window_kernel > 0:
@@ -588,7 +665,7 @@ def run_ours(args):
     by = step.bytes()
     dom_s = statistics.mean(dom_ms) / 1e3
     achieved = by["dominant"] / dom_s / 1e9
-    if isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep)):
+    if isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep)):
         kernel_file, kernel_tag = ("index_score.cu", "index_score_tc.cu", "tc_common.cuh", "sd_common.cuh"), "index_score"
     else:
         kernel_file, kernel_tag = ("gather_attend.cu", "sd_common.cuh"), "gather_attend"
@@ -620,6 +697,13 @@ def run_ours(args):
             "topk": k_us(lambda m: m.dom[0][1], lambda m: m.phase["after_topk"]),
             "stage_host_rows": k_us(lambda m: m.phase["after_topk"], lambda m: m.phase["after_stage"]),
             "gather_attend": k_us(lambda m: m.phase["after_stage"], lambda m: m.end)}
+    elif isinstance(step, VerifyGroupStep):
+        after_topk = [m.dom[0][1].elapsed_time(m.phase["after_topk"]) for m in kmarks]
+        tail = [m.phase["after_topk"].elapsed_time(m.end) for m in kmarks]
+        step_roof["kernel_us"] = {"index_score": round(statistics.mean(dom_ms) * 1e3, 2),
+                                  "topk": round(statistics.mean(after_topk) * 1e3, 2),
+                                  "ring_append+gather_attend_all_layers": round(statistics.mean(tail) * 1e3, 2),
+                                  "layers": w.layers}
     elif isinstance(step, (SparseDecodeStep, HeadsStep)):
         after_topk = [m.dom[0][1].elapsed_time(m.phase["after_topk"]) for m in kmarks]
         tail = [m.phase["after_topk"].elapsed_time(m.end) for m in kmarks]
@@ -653,6 +737,9 @@ def run_ours(args):
                             if isinstance(step, WindowStep)
                             else "per-head logits + per-head top-k + per-head gather-attend"
                             if isinstance(step, HeadsStep)
+                            else f"indexer + top-k once, then per layer ({w.layers}) ring append + gather-attend "
+                                 "over the selected rows and the draft ring"
+                            if isinstance(step, VerifyGroupStep)
                             else "dense attention + score accumulate per layer"),
                    "l2": "flushed between timed steps: 2x L2 written then read, outside the events",
                    "parallelism": f"replica x{world} (each rank its own batch)"},
@@ -680,11 +767,14 @@ def measure_e2e(step, w, x, clean_l2, K):
     (attention output, lse and, for sparse steps, the selected indices) back into pinned
     host memory; host wall clock per step, including the copies and the final sync."""
     import torch
-    ins = [(step.q, x["q"][0, 0] if w.layers > 1 else x["q"])]
-    if isinstance(step, (SparseDecodeStep, WindowStep)):
+    verify = isinstance(step, VerifyGroupStep)
+    ins = [(step.q, x["q"][0] if verify else x["q"][0, 0] if w.layers > 1 else x["q"])]
+    if isinstance(step, (SparseDecodeStep, WindowStep, VerifyGroupStep)):
         ins.append((step.q_idx, x["q_idx"]))
+    if verify:  # the drafts' K/V come from the host with the queries
+        ins += [(step.draft_k, x["draft_k"]), (step.draft_v, x["draft_v"])]
     ins = [(dst, src.contiguous().pin_memory()) for dst, src in ins]
-    sparse = isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep))
+    sparse = isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep))
     outs = [step.out, step.lse] + ([step.idx] if sparse else [step.s])
     outs = [(src, torch.empty(src.shape, dtype=src.dtype).pin_memory()) for src in outs]
     times = []
@@ -713,6 +803,22 @@ def oracle_step(w, x, b0, b1):
     import oracle
     nb = b1 - b0
     scale = 1.0 / math.sqrt(w.d)
+    if w.ring_w > 0:  # one selection for the layer group, then per layer: ring append + attention
+        sc = oracle.index_score(x["q_idx"][b0:b1].contiguous(), x["k_idx"][b0:b1].contiguous(), nb, w.Hkv, w.V,
+                                w.N, w.dI)
+        idx = oracle.topk(sc, w.k)
+        res = []
+        for layer in range(w.layers):
+            rk = x["ring_k"][layer, b0:b1].float().numpy().copy()
+            rv = x["ring_v"][layer, b0:b1].float().numpy().copy()
+            rp = x["ring_pos"][b0:b1].numpy().copy()
+            oracle.ring_append(x["draft_k"][layer, b0:b1].float().numpy(), x["draft_v"][layer, b0:b1].float().numpy(),
+                               rk, rv, rp, [w.T] * nb)
+            res.append(oracle.gather_attend_ring(x["q"][0, layer, b0:b1].contiguous(), x["k"][layer][b0:b1].contiguous(),
+                                                 x["v"][layer][b0:b1].contiguous(), idx, nb, w.V, w.Hq, w.Hkv, w.d, w.T,
+                                                 w.k, 1, scale, torch_bf16(rk), torch_bf16(rv), rp,
+                                                 x["qpos"][b0:b1].numpy()))
+        return idx, res
     if w.layers > 1:  # dense attention per layer and the layer's importance-score term
         s = np.zeros((nb, w.T))
         for layer in range(w.layers):
@@ -745,6 +851,12 @@ def oracle_step(w, x, b0, b1):
     return oracle.gather_attend(x["q"][b0:b1].contiguous(), x["k"][b0:b1].contiguous(),
                                 x["v"][b0:b1].contiguous(), idx, nb, w.V, w.Hq, w.Hkv, w.d, w.T,
                                 w.k, w.block, scale)
+
+
+def torch_bf16(a):
+    """A float array of bf16-representable values back as a bf16 tensor (exact)."""
+    import torch
+    return torch.from_numpy(a).to(torch.bfloat16)
 
 
 def cpu_baseline(w, x, budget_s: float = 10.0, nseq: int = 1):

@@ -159,3 +159,42 @@ def test_empty_ring_is_plain_attention():
     ro, rl, _ = oracle.gather_attend(q, K, Vv, idx.numpy(), B, V, Hq, Hkv, d, T, n, 1, 1 / math.sqrt(d))
     assert_attend_close(o1, ro)
     assert_attend_close(l1, rl, "lse")
+
+
+def test_c8_verify_layer_group_full():
+    # the benchmark's verify workload at full size, in its launch sequence: one indexer pass
+    # and one top-k for the layer group, then per layer the drafts appended to the layer's
+    # ring and the attention over the selected rows plus the ring
+    from top_sparse_decode_gqa_gb300.workloads import WORKLOADS, generate
+    w = WORKLOADS["c8_verify_layer_group"]
+    x = generate(w)
+    e = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hist = sd().key_hist_buffer(w.B * w.Hkv)
+    s = sd().sd_index_score(x["q_idx"].cuda(), x["k_idx"].cuda(), err_word=e, key_hist=hist)
+    idx = sd().sd_topk(s, w.k, key_hist=hist)
+    qpos, pos0 = x["qpos"].cuda(), torch.full((w.B,), w.T, dtype=torch.int32, device="cuda")
+    outs = []
+    for layer in range(w.layers):
+        rk, rv = x["ring_k"][layer].cuda(), x["ring_v"][layer].cuda()
+        rp = x["ring_pos"].cuda()
+        sd().sd_ring_append(x["draft_k"][layer].cuda(), x["draft_v"][layer].cuda(), rk, rv, rp, pos0)
+        out, lse, _ = sd().gather_attend(x["q"][0, layer].cuda(), x["k"][layer].cuda(), x["v"][layer].cuda(), idx,
+                                         T=w.T, err_word=e, ring_k=rk, ring_v=rv, ring_pos=rp, qpos=qpos)
+        outs.append((out.cpu(), lse.cpu(), rp.cpu()))
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    ri = oracle.topk(oracle.index_score(x["q_idx"], x["k_idx"], w.B, w.Hkv, w.V, w.T, w.dI), w.k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ri)
+    for layer in range(w.layers):
+        rk = x["ring_k"][layer].float().numpy().copy()
+        rv = x["ring_v"][layer].float().numpy().copy()
+        rp = x["ring_pos"].numpy().copy()
+        oracle.ring_append(x["draft_k"][layer].float().numpy(), x["draft_v"][layer].float().numpy(), rk, rv, rp,
+                           [w.T] * w.B)
+        np.testing.assert_array_equal(outs[layer][2].numpy(), rp)
+        ro, rl, _ = oracle.gather_attend_ring(x["q"][0, layer], x["k"][layer], x["v"][layer], ri, w.B, w.V, w.Hq,
+                                              w.Hkv, w.d, w.T, w.k, 1, 1 / math.sqrt(w.d),
+                                              torch.from_numpy(rk).to(torch.bfloat16),
+                                              torch.from_numpy(rv).to(torch.bfloat16), rp, x["qpos"].numpy())
+        assert_attend_close(outs[layer][0], ro)
+        assert_attend_close(outs[layer][1], rl, "lse")

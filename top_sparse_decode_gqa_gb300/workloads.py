@@ -30,6 +30,12 @@ available here):
   unscaled attention logits against its KV head's keys score the tokens, each head keeps
   its own top-1024 and attends over those rows only (the indexer tensors are drawn, to keep
   the draw order, but not used).
+* ``c8_verify_layer_group``: a speculative-verify step over a group of 4 Llama-shaped layers
+  that share one selection: batch 2, 8 draft tokens, 32/8 heads, d = 128, bf16, T = 32768;
+  one indexer pass and one union top-1024 per KV head serve all 4 layers; every layer
+  appends the 8 drafts' K/V to its own 64-slot window-bounded ring (which already holds the
+  56 most recent accepted tokens) and attends the selected rows plus the ring, causally
+  among the drafts.
 
 Value recipe: indexer query and keys are integers drawn uniformly from [-8, 8] (exact in
 bf16 and fp32); attention q, K, V are standard normal, rounded to bf16 (nearest even)
@@ -70,6 +76,7 @@ class Workload:
     window_kernel: int = 0  # > 0: select compression windows of this many tokens ...
     window_stride: int = 0  # ... moved by this many (k counts windows)
     per_head: bool = False  # select per query head from the attention logits (k per head)
+    ring_w: int = 0         # > 0: draft-token ring of this many slots per layer (verify loop)
     cum_frac: tuple = (0.2, 0.6, 0.9)
     n_sink: int = 0
     n_recent: int = 0
@@ -137,6 +144,8 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("c7_head_topk", 6, B=8, V=1, Hq=32, Hkv=8, d=128, T=32768, dtype="bf16",
                  dI=128, k=1024, planted=655, planted_values="five_to_eight", planted_attn_boost=0.5,
                  per_head=True),
+        Workload("c8_verify_layer_group", 7, B=2, V=8, Hq=32, Hkv=8, d=128, T=32768, dtype="bf16",
+                 dI=128, k=1024, layers=4, ring_w=64),
     )
 }
 
@@ -166,7 +175,11 @@ def generate(w: Workload, seed: Optional[int] = None) -> Dict[str, torch.Tensor]
     [steps,layers,B,V,Hq,d] when layers*steps > 1); ``k``, ``v`` [B,Hkv,T,d] (or a list of
     per-layer tensors); ``planted`` int64 [B,Hkv,planted] positions (sorted); and, when
     resident_frac < 1, ``resident`` int64 [B,P] sorted resident positions, ``slot_map``
-    int32 [B,T] (slot or -1) and ``k_pool``, ``v_pool`` [B,Hkv,P,d].
+    int32 [B,T] (slot or -1) and ``k_pool``, ``v_pool`` [B,Hkv,P,d].  With a draft ring
+    (ring_w > 0): ``ring_k``, ``ring_v`` [layers,B,Hkv,W,d] (slots of the recent accepted
+    tokens T-(W-V) .. T-1 filled, at slot position mod W), ``ring_pos`` int32 [B,W] (-1 where
+    empty), ``draft_k``, ``draft_v`` [layers,B,Hkv,V,d] (the V draft tokens, positions
+    T .. T+V-1, appended by the step) and ``qpos`` int32 [B,V] = T + v.
     """
     g = torch.Generator().manual_seed(1000 + w.cfg_id if seed is None else seed)
     B, Hkv, V, T = w.B, w.Hkv, w.V, w.T
@@ -223,6 +236,18 @@ def generate(w: Workload, seed: Optional[int] = None) -> Dict[str, torch.Tensor]
         idx = res[:, None, :, None].expand(B, Hkv, P, w.d)
         out["k_pool"] = torch.gather(out["k"], 2, idx).contiguous()
         out["v_pool"] = torch.gather(out["v"], 2, idx).contiguous()
+    # 8. draft ring: its K/V, then the drafts' K/V
+    if w.ring_w > 0:
+        W, L = w.ring_w, max(1, w.layers)
+        out["ring_k"] = _randn(g, (L, B, Hkv, W, w.d), w.dtype)
+        out["ring_v"] = _randn(g, (L, B, Hkv, W, w.d), w.dtype)
+        out["draft_k"] = _randn(g, (L, B, Hkv, V, w.d), w.dtype)
+        out["draft_v"] = _randn(g, (L, B, Hkv, V, w.d), w.dtype)
+        ring_pos = torch.full((B, W), -1, dtype=torch.int32)
+        for t in range(max(0, T - (W - V)), T):
+            ring_pos[:, t % W] = t
+        out["ring_pos"] = ring_pos
+        out["qpos"] = (T + torch.arange(V, dtype=torch.int32)).expand(B, V).contiguous()
     return out
 
 
