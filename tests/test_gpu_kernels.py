@@ -273,10 +273,11 @@ def test_host_pointer_must_be_pinned():
 # --------------------------------------------------------------------------- importance
 
 
-@pytest.mark.parametrize("dense,block", [(True, 1), (False, 1), (False, 16)])
-def test_score_accumulate_matches_oracle(dense, block):
-    g = torch.Generator().manual_seed(51 + block)
-    B, V, Hq, Hkv, d, T = 2, 2, 8, 2, 64, 1024
+@pytest.mark.parametrize("dense,block,V,Hq,T", [(True, 1, 2, 8, 1024), (False, 1, 2, 8, 1024), (False, 16, 2, 8, 1024),
+                                                 (True, 1, 1, 28, 2048), (True, 1, 3, 12, 1022)])
+def test_score_accumulate_matches_oracle(dense, block, V, Hq, T):
+    g = torch.Generator().manual_seed(51 + block + T)
+    B, Hkv, d = 2, 2 if Hq % 2 == 0 else 1, 64
     n_idx = T // block if dense else (40 if block > 1 else 300)
     q, K, Vv, idx = _attend_case(g, B, V, Hq, Hkv, d, T, None if dense else n_idx, block, torch.float32)
     _, lse, logits = oracle.gather_attend(q, K, Vv, None if dense else idx.numpy(), B, V, Hq, Hkv, d, T,

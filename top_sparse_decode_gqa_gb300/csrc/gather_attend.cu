@@ -270,6 +270,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
     auto row_code = [&](int j) -> int32_t { return p.resolve ? src[j] : (int32_t)(j0 + j); };
     // a draft-ring row is visible to query row r (token v = r / G) up to its own position
     auto visible = [&](int r, int j) -> bool {
+        if (p.ring_w == 0) return true;
         const int32_t code = row_code(j);
         if (code < kRingBase || r >= p.R) return true;
         return p.ring_pos[(size_t)b * p.ring_w + (code - kRingBase)] <= p.qpos[(size_t)b * p.V + r / p.G];
@@ -485,7 +486,7 @@ struct MmaLayout {
 // Grid (split, kvh, b), 4 warps.  The split's rows are resolved to their sources up front,
 // then attend_mma.cuh's per-warp loop runs over them; the 4 warps' (m, l, O) are combined
 // into the CTA's split partial, and the last CTA of each (b, kvh) merges the splits.
-template <int D, int RP>
+template <int D, int RP, bool RING>
 __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendParams p) {
     using L = MmaLayout<D, RP>;
     using Rows = MmaRows<D>;
@@ -583,9 +584,13 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     };
     // a draft-ring row is visible to query row r (token v = r / G) up to its own position
     auto visible = [&](int r, int j) -> bool {
-        const int32_t code = row_code(j);
-        if (code < kRingBase || r >= p.R) return true;
-        return p.ring_pos[(size_t)b * p.ring_w + (code - kRingBase)] <= p.qpos[(size_t)b * p.V + r / p.G];
+        if constexpr (!RING) {
+            return true;
+        } else {
+            const int32_t code = row_code(j);
+            if (code < kRingBase || r >= p.R) return true;
+            return p.ring_pos[(size_t)b * p.ring_w + (code - kRingBase)] <= p.qpos[(size_t)b * p.V + r / p.G];
+        }
     };
     WarpAcc<D, RP> acc;
     acc.init();
@@ -699,7 +704,7 @@ sd_status launch_attend(const AttendParams& p, cudaStream_t st) {
 template <int D, int RP>
 sd_status launch_attend_mma(const AttendParams& p, cudaStream_t st) {
     using L = MmaLayout<D, RP>;
-    auto kern = attend_mma_kernel<D, RP>;
+    auto kern = p.ring_w > 0 ? attend_mma_kernel<D, RP, true> : attend_mma_kernel<D, RP, false>;
     SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes),
                   "sd_gather_attend: cudaFuncSetAttribute");
     SD_CUDA_CHECK(launch_pdl(kern, dim3(p.splits, p.Hkv, p.B), dim3(kAttThreads), L::kBytes, st, p),

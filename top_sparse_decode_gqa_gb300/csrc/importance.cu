@@ -16,27 +16,70 @@ namespace {
 
 // ------------------------------------------------------------------ score accumulate
 
-// Dense selection: one thread per (b, position), no atomics, fixed summation order (query
-// rows ascending).  Grid (position blocks, b); the logits were just written by the
-// attention and sit in L2, so all of a thread's rows (up to 32) are loaded before any is
-// used; streaming loads, as nothing reads them again.
-__global__ void score_accumulate_dense_kernel(const float* __restrict__ logits,
-                                              const float* __restrict__ lse, int rows, int T,
-                                              double weight, double* __restrict__ s) {
-    constexpr int kBatch = 32;
+// Dense selection (every position is a list row): thread -> 4 consecutive positions of one
+// sequence (16-byte loads along T).  The rows' lse values are staged in shared memory, the
+// logits of kRowBatch rows are all loaded before any is used, the rows are summed in a
+// fixed order, and the fp64 running score takes one add per position.
+constexpr int kAccThreads = 128;
+constexpr int kRowBatch = 16;
+
+__global__ void __launch_bounds__(kAccThreads)
+    score_accumulate_dense_kernel(const float* __restrict__ logits, const float* __restrict__ lse, int rows, int T,
+                                  double weight, double* __restrict__ s) {
+    extern __shared__ float lse_s[];  // [rows]
     pdl_wait();
     const int b = blockIdx.y;
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= T) return;
     const size_t q0 = (size_t)b * rows;
+    for (int r = threadIdx.x; r < rows; r += kAccThreads) lse_s[r] = lse[q0 + r];
+    __syncthreads();
+    const int i = (blockIdx.x * kAccThreads + threadIdx.x) * 4;
+    if (i >= T) return;
+    const float* lrow = logits + q0 * T + i;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r0 = 0; r0 < rows; r0 += kRowBatch) {
+        float4 z[kRowBatch];
+#pragma unroll
+        for (int u = 0; u < kRowBatch; ++u)
+            z[u] = r0 + u < rows ? __ldcs(reinterpret_cast<const float4*>(lrow + (size_t)(r0 + u) * T))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < kRowBatch; ++u) {
+            if (r0 + u < rows) {
+                const float m = lse_s[r0 + u];
+                acc.x += expf(z[u].x - m);
+                acc.y += expf(z[u].y - m);
+                acc.z += expf(z[u].z - m);
+                acc.w += expf(z[u].w - m);
+            }
+        }
+    }
+    double* srow = s + (size_t)b * T + i;
+    srow[0] += weight * (double)acc.x;
+    srow[1] += weight * (double)acc.y;
+    srow[2] += weight * (double)acc.z;
+    srow[3] += weight * (double)acc.w;
+}
+
+// Dense selection with T not a multiple of 4 (or unaligned logits): thread per position.
+__global__ void __launch_bounds__(kAccThreads)
+    score_accumulate_dense_scalar_kernel(const float* __restrict__ logits, const float* __restrict__ lse, int rows,
+                                         int T, double weight, double* __restrict__ s) {
+    extern __shared__ float lse_s[];  // [rows]
+    pdl_wait();
+    const int b = blockIdx.y;
+    const size_t q0 = (size_t)b * rows;
+    for (int r = threadIdx.x; r < rows; r += kAccThreads) lse_s[r] = lse[q0 + r];
+    __syncthreads();
+    const int i = blockIdx.x * kAccThreads + threadIdx.x;
+    if (i >= T) return;
     float acc = 0.f;
-    for (int r0 = 0; r0 < rows; r0 += kBatch) {
-        float z[kBatch];
+    for (int r0 = 0; r0 < rows; r0 += kRowBatch) {
+        float z[kRowBatch];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) z[u] = r0 + u < rows ? __ldcs(logits + (q0 + r0 + u) * T + i) : 0.f;
+        for (int u = 0; u < kRowBatch; ++u) z[u] = r0 + u < rows ? __ldcs(logits + (q0 + r0 + u) * T + i) : 0.f;
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u)
-            if (r0 + u < rows) acc += expf(z[u] - lse[q0 + r0 + u]);
+        for (int u = 0; u < kRowBatch; ++u)
+            if (r0 + u < rows) acc += expf(z[u] - lse_s[r0 + u]);
     }
     s[(size_t)b * T + i] += weight * (double)acc;
 }
@@ -314,9 +357,14 @@ extern "C" sd_status sd_score_accumulate(const float* logits, const float* lse, 
     const int threads = 256;
     if (idx == nullptr) {
         SD_REQUIRE(B <= 65535, "sd_score_accumulate: B must be <= 65535");
-        const dim3 grid((unsigned)((T + threads - 1) / threads), (unsigned)B);
-        SD_CUDA_CHECK(launch_pdl(score_accumulate_dense_kernel, grid, dim3(threads), 0, st, logits, lse, V * Hq, T,
-                                 weight, s),
+        const int rows = V * Hq;
+        SD_REQUIRE(rows <= 12288, "sd_score_accumulate: V*Hq must be <= 12288");
+        const size_t smem = (size_t)rows * sizeof(float);
+        const bool vec = T % 4 == 0 && aligned16(logits);
+        auto kern = vec ? score_accumulate_dense_kernel : score_accumulate_dense_scalar_kernel;
+        const int per_cta = vec ? 4 * kAccThreads : kAccThreads;
+        const dim3 grid((unsigned)((T + per_cta - 1) / per_cta), (unsigned)B);
+        SD_CUDA_CHECK(launch_pdl(kern, grid, dim3(kAccThreads), smem, st, logits, lse, rows, T, weight, s),
                       "sd_score_accumulate: launch");
     } else {
         const long n = (long)B * Hkv * n_rows;
