@@ -200,7 +200,8 @@ class StepMarks:
 
 class SparseDecodeStep:
     """One sparse decode step, inputs resident: the indexer, then either the fused select +
-    attend launch (bf16 workloads) or the separate top-k and gather-attend launches.  For a
+    attend launch (bf16 token-level workloads) or the separate top-k and gather-attend
+    launches (block-level selection, fp32, or on request).  For a
     tiered workload the full K/V cache stays in pinned host memory and only the resident
     share sits in the HBM pool; there the default path copies the selected host rows into
     an HBM stage with one copy kernel spread over every SM (sd_stage_host_rows) between the
@@ -214,7 +215,9 @@ class SparseDecodeStep:
         self.sd, self.w, self.dev = sd, w, device
         self.tiered = w.resident_frac < 1.0
         self.staged = self.tiered and tiered_path == "staged" and not separate
-        self.fused = w.dtype == "bf16" and not separate and not self.staged
+        # block selection picks few entries but many rows per group: the separate top-k and
+        # gather-attend spread the rows over the whole GPU, the fused kernel over one cluster
+        self.fused = w.dtype == "bf16" and not separate and not self.staged and w.block == 1
         self.phases = () if self.fused else ("after_topk", "after_stage") if self.staged else ("after_topk",)
         self.launches_per_step = 2 if self.fused else 4 if self.staged else 3
         self.q_idx, self.k_idx, self.q = (x[k].to(device) for k in ("q_idx", "k_idx", "q"))
