@@ -20,8 +20,10 @@
  * NULL means such errors are not reported).  Every wait inside a kernel is bounded; a
  * wait that runs out sets SD_DEVERR_TIMEOUT and the kernel returns.  No kernel traps.
  *
- * Element types: SD_F32 = IEEE binary32, SD_BF16 = bfloat16 (upper half of a binary32).
- * Arithmetic is fp32 (fp64 for the importance score) whatever the storage type.
+ * Element types: SD_F32 = IEEE binary32, SD_BF16 = bfloat16 (upper half of a binary32),
+ * SD_F16 = IEEE binary16 (only where a call says so: sd_block_pool's output and the
+ * indexer's q and k together).  Arithmetic is fp32 (fp64 for the importance score)
+ * whatever the storage type.
  *
  * Sources the operations follow (web pages, cited by title and section):
  *   [SparDA]    "SparDA: Atencao Esparsa Desacoplada para Inferencia Eficiente de LLMs de
@@ -52,7 +54,7 @@ typedef enum {
     SD_ERR_TIMEOUT = 5        /* reserved: reported through *err_word, see below */
 } sd_status;
 
-typedef enum { SD_F32 = 0, SD_BF16 = 1 } sd_dtype;
+typedef enum { SD_F32 = 0, SD_BF16 = 1, SD_F16 = 2 } sd_dtype;
 
 /* Bits a kernel ORs into *err_word. */
 #define SD_DEVERR_INDEX 0x1   /* a selected index outside [0, N) or [0, T) was skipped */
@@ -79,7 +81,9 @@ const char* sd_last_error_message(void);
  * q_idx  [B,Hkv,V,d_idx] of q_dtype; k_idx [B,Hkv,N,d_idx] of k_dtype (token keys, or
  * the pooled block keys of sd_block_pool for block-granular selection, then N = blocks);
  * scores [B,Hkv,N] fp32 (written).  fp32 products and sums: integer-valued inputs with
- * |sum| < 2^24 give exact scores.  Limits: d_idx in {64, 128}, 1 <= V <= 8, N >= 0.
+ * |sum| < 2^24 give exact scores (likewise multiples of 2^-6, e.g. pooled block keys, with
+ * |sum| < 2^18).  q_dtype and k_dtype are each F32 or BF16, or both F16 (q and k of one
+ * 16-bit type run on the tensor cores).  Limits: d_idx in {64, 128}, 1 <= V <= 8, N >= 0.
  * key_hist: nullable [B*Hkv, SD_KEY_HIST_BINS] uint32 in/out.  When given, every score
  * written adds 1 to the bin of its top 11 order-key bits (the order key maps fp32 to
  * uint32 preserving order, -0.0 like +0.0).  Pass the same array to sd_topk for these
@@ -115,11 +119,15 @@ sd_status sd_index_score_heads(const void* q, sd_dtype q_dtype, const void* k, s
  * block grid).  Disjoint blocks of `block` tokens; the key of block n is the mean of its
  * tokens' indexer keys, computed in fp32 (exact for integer keys and power-of-two block):
  *     pooled[b,h,n,j] = (1/block) * sum_{t in [n*block, (n+1)*block)} k_idx[b,h,t,j]
- * k_idx [B,Hkv,T,d_idx] of k_dtype; pooled [B,Hkv,T/block,d_idx] fp32 (written).
+ * k_idx [B,Hkv,T,d_idx] of k_dtype (F32 or BF16); pooled [B,Hkv,T/block,d_idx] of
+ * pooled_dtype (written): F32, or F16 rounded to nearest even -- exact when the means are
+ * multiples of 2^-14 below 2048 in magnitude with at most 11 significant bits, as for
+ * integer keys in [-8, 8] and block <= 64 (half the key bytes, and with an F16 indexer
+ * query the block scores run on the tensor cores).
  * T must be a multiple of block.  Limits: d_idx in {64, 128}, 1 <= block <= 4096.
  */
 sd_status sd_block_pool(const void* k_idx, sd_dtype k_dtype, int B, int Hkv, int T, int d_idx,
-                        int block, float* pooled, void* stream);
+                        int block, void* pooled, sd_dtype pooled_dtype, void* stream);
 
 /*
  * sd_topk -- exact top-k per row.
@@ -164,11 +172,10 @@ sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx, uin
  * Accumulation order depends only on (n_idx, block, splits), never on the data source.
  * Limits: d in {64, 128}; G*V <= 32; dtype F32 or BF16 for q, K and V alike.
  * The split-K partition over selected rows needs workspace (sd_gather_attend_workspace_bytes;
- * 0 when one split suffices): the splits' (m, l, o) partials and one completion counter
- * per (b, kvh); the last split of a group to finish merges the partials in split order.
- * The workspace must be zero-filled before its first use; every call leaves the counters
- * at zero again, so a workspace can be reused without clearing.  Calls sharing one
- * workspace must not overlap on the GPU.  splits = 0 picks one wave of CTAs for this GPU;
+ * 0 when one split suffices): the splits' (m, l, o) partials, which a second kernel of the
+ * call merges per (group, query row) in a fixed order.  The workspace needs no
+ * initialisation and can be reused; calls sharing one workspace must not overlap on the
+ * GPU.  splits = 0 picks one wave of CTAs for this GPU;
  * a requested split count is adjusted to at least one 64-row chunk per split and at most
  * 448 rows per split when rows are selected through idx or slot_map.
  * Draft ring ([DHiSparse] "Metodologia": the draft tokens' K/V live in a ring bounded by a
@@ -231,9 +238,8 @@ sd_status sd_gather_attend(const sd_attend_args* args, void* stream);
  * It allocates nothing.  On the first call made on each device (with that device
  * current) the array's device address is looked up and the array is cleared once: make
  * that first call before any stream capture.  All calls share the array and it keeps the
- * last call's contents; the part that must start at zero (the per-group completion
- * counters) is left at zero by every call, but calls whose kernels overlap on the GPU race
- * on the array.  A request
+ * last call's contents (nothing in it needs to start at zero), so calls whose kernels
+ * overlap on the GPU race on the array.  A request
  * whose split-K partials need more than 16 MiB returns SD_ERR_INVALID_ARG without
  * launching (pass a smaller `splits`, or use sd_gather_attend with a workspace).
  */

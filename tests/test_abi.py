@@ -50,7 +50,10 @@ def test_host_validation_rejects_before_launch(lib):
     # V out of range
     assert lib.sd_index_score(dummy, 1, dummy, 1, 1, 1, 9, 10, 128, dummy, None, None, None) == 1
     # ragged block pooling
-    assert lib.sd_block_pool(dummy, 1, 1, 1, 100, 128, 64, dummy, None) == 1
+    assert lib.sd_block_pool(dummy, 1, 1, 1, 100, 128, 64, dummy, 0, None) == 1
+    # pooled keys are F32 or F16 only; F16 indexer operands go together
+    assert lib.sd_block_pool(dummy, 1, 1, 1, 128, 128, 64, dummy, 1, None) == 1
+    assert lib.sd_index_score(dummy, 2, dummy, 1, 1, 1, 1, 10, 128, dummy, None, None, None) == 1
     # non-monotone tier fractions
     fr = (ctypes.c_double * 3)(0.5, 0.2, 0.9)
     assert lib.sd_tier_classify(dummy, 1, 10, fr, 0, 0, dummy, dummy, None, 0, None) == 1

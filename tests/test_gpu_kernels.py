@@ -76,6 +76,30 @@ def test_block_pool_bit_exact(T, dI, block, dt):
     np.testing.assert_array_equal(p.cpu().numpy().astype(np.float64), ref)
 
 
+@pytest.mark.parametrize("T,dI,block,V", [(2048 * 64, 128, 64, 1), (64 * 300 + 0, 64, 64, 4), (16 * 777, 128, 16, 8),
+                                          (64 * 5, 128, 64, 2)])
+def test_fp16_pooled_keys_on_the_tensor_cores(T, dI, block, V):
+    # fp16 pooled keys of integer keys are exact (multiples of 1/block below 8); with an fp16
+    # query of the same integers the block scores run on the tensor cores, bit-exact
+    g = torch.Generator().manual_seed(T + V)
+    B, Hkv = 2, 2
+    k = rint(g, (B, Hkv, T, dI), torch.bfloat16)
+    q = rint(g, (B, Hkv, V, dI), torch.float16)
+    p = sd().sd_block_pool(k.cuda(), block, dtype=torch.float16)
+    ref = oracle.block_pool(k, B, Hkv, T, dI, block)
+    np.testing.assert_array_equal(p.cpu().numpy().astype(np.float64), ref)
+    hist = sd().key_hist_buffer(B * Hkv)
+    s = sd().sd_index_score(q.cuda(), p, key_hist=hist)
+    rs = oracle.index_score(q, ref.astype(np.float32), B, Hkv, V, T // block, dI)
+    np.testing.assert_array_equal(s.cpu().numpy().astype(np.float64), rs)
+    kk = min(64, T // block)
+    idx = sd().sd_topk(s, kk, key_hist=hist)
+    np.testing.assert_array_equal(idx.cpu().numpy(), oracle.topk(rs, kk))
+    # mixed 16-bit types are rejected
+    with pytest.raises(sd().SdError):
+        sd().sd_index_score(q.to(torch.bfloat16).cuda(), p)
+
+
 # --------------------------------------------------------------------------- top-k
 
 

@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsdgqa.so")
 
 SD_OK, SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED, SD_ERR_CUDA = 0, 1, 2, 3
-SD_F32, SD_BF16 = 0, 1
+SD_F32, SD_BF16, SD_F16 = 0, 1, 2
 SD_DEVERR_INDEX, SD_DEVERR_SLOT, SD_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 
 # Every symbol include/sd.h declares (checked by the tests against the built library).
@@ -70,7 +70,7 @@ def lib() -> ctypes.CDLL:
         L.sd_status_string.argtypes = [I]
         L.sd_last_error_message.restype = ctypes.c_char_p
         L.sd_index_score.argtypes = [P, I, P, I, I, I, I, I, I, P, P, P, P]
-        L.sd_block_pool.argtypes = [P, I, I, I, I, I, I, P, P]
+        L.sd_block_pool.argtypes = [P, I, I, I, I, I, I, P, I, P]
         L.sd_topk_workspace_bytes.argtypes = [I, I, I]
         L.sd_topk_workspace_bytes.restype = Z
         L.sd_topk.argtypes = [P, I, I, I, P, P, P, Z, P]
@@ -110,7 +110,9 @@ def _dtype_code(t: torch.Tensor) -> int:
         return SD_F32
     if t.dtype == torch.bfloat16:
         return SD_BF16
-    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+    if t.dtype == torch.float16:
+        return SD_F16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32, bfloat16 or float16)")
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -182,14 +184,15 @@ def sd_index_score_heads(q: torch.Tensor, k: torch.Tensor, scores: Optional[torc
 
 
 def sd_block_pool(k_idx: torch.Tensor, block: int, pooled: Optional[torch.Tensor] = None,
-                  stream=None) -> torch.Tensor:
-    """Mean-pooled block keys [B,Hkv,T/block,dI] fp32 of k_idx [B,Hkv,T,dI]."""
+                  stream=None, dtype: torch.dtype = torch.float32) -> torch.Tensor:
+    """Mean-pooled block keys [B,Hkv,T/block,dI] of k_idx [B,Hkv,T,dI], as float32 or
+    float16 (`dtype`, or the dtype of a given `pooled`)."""
     _dev(k_idx, "k_idx")
     B, Hkv, T, dI = k_idx.shape
     if pooled is None:
-        pooled = torch.empty((B, Hkv, T // block, dI), dtype=torch.float32, device=k_idx.device)
+        pooled = torch.empty((B, Hkv, T // block, dI), dtype=dtype, device=k_idx.device)
     _check(lib().sd_block_pool(_ptr(k_idx), _dtype_code(k_idx), B, Hkv, T, dI, block, _ptr(pooled),
-                               _stream(stream)), "sd_block_pool")
+                               _dtype_code(pooled), _stream(stream)), "sd_block_pool")
     return pooled
 
 

@@ -92,8 +92,10 @@ struct WarpAcc {
 // skipped row; called only for j < nrows).  logit(r, j, x) receives every (query row,
 // list row) score in base-2 units (x * ln 2 is the natural logit) of valid rows, -inf where
 // vis(r, j) hides the row from the query row (the causal mask of the draft ring).
+// nq = the real query rows (<= RP): an upper half tile (rows 8..15 of an M tile) holding
+// none of them skips its softmax, and its P fragments are zero.
 template <int D, int RP, int NW = kMmaWarps, int NS = kWStages, class RowCode, class Logit, class Vis = AllVisible>
-SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_base, int warp, int nrows,
+SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_base, int warp, int nrows, int nq,
                                const RowSource& rs, float scale_log2, RowCode row_code, Logit logit,
                                Vis vis = Vis()) {
     static_assert(NS >= 2 && NS <= 4, "2 to 4 stages per warp");
@@ -147,14 +149,15 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
         const uint32_t v_base = k_base + kSub * L::kRowB;
         const int c = warp + NW * ci;
 
-        // ---- S = Q K^T for this warp's 16 rows: [MT][2 n-tiles][4]
-        float sacc[MT][2][4];
+        // ---- S = Q K^T for this warp's 16 rows: [MT][2 n-tiles][4].  Even and odd k-steps
+        // accumulate separately (4 independent MMA chains per M tile), then add.
+        float sacc[MT][2][4], sodd[MT][2][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
+                for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = sodd[mt][nt][e] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KS; ks += 2) {
             uint32_t bk0[4], bk1[4];  // n-tile 0 / 1: (b0, b1) of k-step ks, then of ks + 1
@@ -162,15 +165,23 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
             ldsm_x4(k_base + (1 * 8 + (lane & 7)) * L::kRowB + (ks * 16 + (lane >> 3) * 8) * 2, bk1[0], bk1[1], bk1[2], bk1[3]);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
+                uint32_t a[2][4];
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(q_base + (mt * 16 + (lane & 15)) * L::kRowB + ((ks + kk) * 16 + (lane >> 4) * 8) * 2, a0, a1, a2, a3);
-                    mma_bf16_16816(sacc[mt][0], a0, a1, a2, a3, bk0[2 * kk], bk0[2 * kk + 1]);
-                    mma_bf16_16816(sacc[mt][1], a0, a1, a2, a3, bk1[2 * kk], bk1[2 * kk + 1]);
-                }
+                for (int kk = 0; kk < 2; ++kk)
+                    ldsm_x4(q_base + (mt * 16 + (lane & 15)) * L::kRowB + ((ks + kk) * 16 + (lane >> 4) * 8) * 2,
+                            a[kk][0], a[kk][1], a[kk][2], a[kk][3]);
+                mma_bf16_16816(sacc[mt][0], a[0][0], a[0][1], a[0][2], a[0][3], bk0[0], bk0[1]);
+                mma_bf16_16816(sacc[mt][1], a[0][0], a[0][1], a[0][2], a[0][3], bk1[0], bk1[1]);
+                mma_bf16_16816(sodd[mt][0], a[1][0], a[1][1], a[1][2], a[1][3], bk0[2], bk0[3]);
+                mma_bf16_16816(sodd[mt][1], a[1][0], a[1][1], a[1][2], a[1][3], bk1[2], bk1[3]);
             }
         }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[mt][nt][e] += sodd[mt][nt][e];
 
         // ---- online softmax (base 2); this lane holds rows 8*nt + 2*t4 + e of query rows g, g + 8
         bool kval[2][2];
@@ -181,8 +192,13 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
         uint32_t ph[MT][4], pl[MT][4];  // P as A fragments (hi, lo)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
+            const int nhf = mt * 16 + 8 < nq ? 2 : 1;  // warp-uniform
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
+                if (hf >= nhf) {  // rows mt*16 + 8.. are padding: P = 0 there
+                    sacc[mt][0][2] = sacc[mt][0][3] = sacc[mt][1][2] = sacc[mt][1][3] = 0.f;
+                    break;
+                }
                 const int r = mt * 16 + g + 8 * hf;
                 float x[2][2];
                 float tmax = -INFINITY;
@@ -234,17 +250,21 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
             split_bf16x2(sacc[mt][1][2], sacc[mt][1][3], ph[mt][3], pl[mt][3]);
         }
 
-        // ---- O += P V: V fragments by ldmatrix.trans, 2 n-tiles per load
+        // ---- O += P V: V fragments by ldmatrix.trans, 4 n-tiles per round: the hi parts of
+        // the 4 accumulators, then the lo parts (4 MMAs between dependent ones)
 #pragma unroll
-        for (int nt = 0; nt < NT; nt += 2) {
-            uint32_t v0, v1, v2, v3;
-            ldsm_x4_t(v_base + (lane & 15) * L::kRowB + (nt * 8 + (lane >> 4) * 8) * 2, v0, v1, v2, v3);
+        for (int nt = 0; nt < NT; nt += 4) {
+            uint32_t v[8];
+            ldsm_x4_t(v_base + (lane & 15) * L::kRowB + (nt * 8 + (lane >> 4) * 8) * 2, v[0], v[1], v[2], v[3]);
+            ldsm_x4_t(v_base + (lane & 15) * L::kRowB + ((nt + 2) * 8 + (lane >> 4) * 8) * 2, v[4], v[5], v[6], v[7]);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-                mma_bf16_16816(acc.o[mt][nt], ph[mt][0], ph[mt][1], ph[mt][2], ph[mt][3], v0, v1);
-                mma_bf16_16816(acc.o[mt][nt], pl[mt][0], pl[mt][1], pl[mt][2], pl[mt][3], v0, v1);
-                mma_bf16_16816(acc.o[mt][nt + 1], ph[mt][0], ph[mt][1], ph[mt][2], ph[mt][3], v2, v3);
-                mma_bf16_16816(acc.o[mt][nt + 1], pl[mt][0], pl[mt][1], pl[mt][2], pl[mt][3], v2, v3);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    mma_bf16_16816(acc.o[mt][nt + u], ph[mt][0], ph[mt][1], ph[mt][2], ph[mt][3], v[2 * u], v[2 * u + 1]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    mma_bf16_16816(acc.o[mt][nt + u], pl[mt][0], pl[mt][1], pl[mt][2], pl[mt][3], v[2 * u], v[2 * u + 1]);
             }
         }
         __syncwarp();

@@ -14,8 +14,8 @@
 // current, its device address is looked up with cudaGetSymbolAddress and the array is
 // cleared once with cudaMemset (so make that first call before any stream capture).  All
 // calls share the one array and it keeps whatever the last call left there.  The split
-// partials are rewritten by every call before they are read; the per-group completion
-// counters must start at zero, which the one-time clear ensures and every call restores.
+// partials are rewritten by every call before they are read, so nothing in the array needs
+// to start at zero.
 // Two calls whose kernels overlap on the GPU (different streams, no ordering between
 // them) race on the array and give wrong results.  Requests whose split-K scratch needs
 // more than the array holds are rejected with SD_ERR_INVALID_ARG before anything is
@@ -56,7 +56,7 @@ sd_status scratch_address(void** out) {
             sd::set_error("sd_gather_attend_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
             return SD_ERR_CUDA;
         }
-        e = cudaMemset(p, 0, kNoAllocScratchBytes);  // the completion counters start at zero
+        e = cudaMemset(p, 0, kNoAllocScratchBytes);  // a defined start (nothing needs it)
         if (e != cudaSuccess) {
             sd::set_error("sd_gather_attend_noalloc: clearing the scratch: %s", cudaGetErrorString(e));
             return SD_ERR_CUDA;

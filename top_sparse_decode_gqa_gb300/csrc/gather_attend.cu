@@ -58,7 +58,6 @@ struct AttendParams {
     float* ws_o;
     float* ws_m;
     float* ws_l;
-    uint32_t* counters;  // [B*Hkv], zero between calls
 };
 
 template <typename ST, int D, int RP>
@@ -89,108 +88,88 @@ int att_ctas_per_sm(int bytes) {
     return per < 1 ? 1 : (per > 3 ? 3 : per);
 }
 
-// Called by every CTA after it wrote its split's partial: the last CTA of the (b, kvh) to
-// arrive combines all splits' (m, l, o) partials in split order (deterministic) into out
-// and lse, then resets the group's counter for the next call.  `scratch` holds at least
-// `scratch_floats` floats of shared memory no longer in use.
+constexpr int kMergeThreads = 128;
+constexpr int kMergeWarps = kMergeThreads / 32;
+
+// Block-wide max / sum of one value per thread (kMergeThreads), the same in every thread.
+SD_DEVINL float merge_block_max(float v, float* red) {
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = red[0];
+    for (int w = 1; w < kMergeWarps; ++w) r = fmaxf(r, red[w]);
+    return r;
+}
+SD_DEVINL float merge_block_sum(float v, float* red) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = red[0];
+    for (int w = 1; w < kMergeWarps; ++w) r += red[w];
+    return r;
+}
+
+// The split-K merge, after every split wrote its (m, l, o) partial: grid (groups, R), one
+// CTA per (group, query row).  M = max over the splits of m, L = sum of l * 2^(m - M), and
+// o = sum over the splits of o_s * 2^(m_s - M) / L, each split's terms in a fixed order
+// (warp w takes splits w, w + 4, ...; the warps' sums are added in warp order), so the
+// result is the same on every run.  lse = (M + log2 L) ln 2.
 template <int D>
-SD_DEVINL void merge_if_last(const AttendParams& p, int b, int kvh, int RP, float* scratch,
-                             int scratch_floats, int* flag_s) {
-    const int tid = threadIdx.x, nthr = blockDim.x;
-    const int bk = b * p.Hkv + kvh;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) flag_s[0] = atomicAdd(&p.counters[bk], 1u) == (uint32_t)(p.splits - 1) ? 1 : 0;
-    __syncthreads();
-    if (!flag_s[0]) return;
-    __threadfence();
-    const int S = p.splits, R = p.R;
-    // scratch: m[S][R], then w[S][R] (weights), then lse-ready row maxima; all loads of the
-    // splits' m and l go out at once (one per thread), not as per-row loops
-    const int cap = scratch_floats / (2 * R) - 1;
-    for (int s0 = 0; s0 < S; s0 += cap) {
-        const int s1 = min(S, s0 + cap), ns = s1 - s0;
-        float* mm = scratch;            // [ns][R]
-        float* ww = scratch + ns * R;   // [ns][R]
-        __syncthreads();
-        for (int e = tid; e < ns * R; e += nthr) {
-            const int s = s0 + e / R, r = e % R;
-            const size_t prow = ((size_t)bk * S + s) * RP + r;
-            mm[e] = __ldcg(p.ws_m + prow);
-            ww[e] = __ldcg(p.ws_l + prow);
+__global__ void __launch_bounds__(kMergeThreads) attend_merge_kernel(const AttendParams p, int RP) {
+    __shared__ float red[kMergeWarps];
+    __shared__ __align__(16) float part[kMergeWarps][D];
+    pdl_wait();  // every split's partial is written
+    pdl_launch_dependents();
+    constexpr int CPL = D / 32;  // columns per lane
+    const int bk = blockIdx.x, r = blockIdx.y;
+    const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int S = p.splits;
+    const size_t base = (size_t)bk * S * RP + r;  // partial row of split s: base + s * RP
+    float m = -INFINITY;
+    for (int s = tid; s < S; s += kMergeThreads) m = fmaxf(m, __ldcg(p.ws_m + base + (size_t)s * RP));
+    const float M = merge_block_max(m, red);
+    float l = 0.f;
+    if (M != -INFINITY)
+        for (int s = tid; s < S; s += kMergeThreads) {
+            const float ms = __ldcg(p.ws_m + base + (size_t)s * RP);
+            if (ms != -INFINITY) l = fmaf(__ldcg(p.ws_l + base + (size_t)s * RP), exp2f(ms - M), l);
         }
-        __syncthreads();
-        if (tid < R) {
-            // global maximum and sum over all splits (the other chunks re-read m, l)
-            const int r = tid;
-            float M = -INFINITY, Ls = 0.f;
-            for (int s = 0; s < S; ++s) {
-                const size_t prow = ((size_t)bk * S + s) * RP + r;
-                const float m = (s >= s0 && s < s1) ? mm[(s - s0) * R + r] : __ldcg(p.ws_m + prow);
-                M = fmaxf(M, m);
-            }
-            if (M != -INFINITY)
-                for (int s = 0; s < S; ++s) {
-                    const size_t prow = ((size_t)bk * S + s) * RP + r;
-                    const bool here = s >= s0 && s < s1;
-                    const float m = here ? mm[(s - s0) * R + r] : __ldcg(p.ws_m + prow);
-                    const float l = here ? ww[(s - s0) * R + r] : __ldcg(p.ws_l + prow);
-                    if (m != -INFINITY) Ls = fmaf(l, exp2f(m - M), Ls);
-                }
-            for (int s = s0; s < s1; ++s) {
-                const float m = mm[(s - s0) * R + r];
-                ww[(s - s0) * R + r] = (Ls > 0.f && m != -INFINITY) ? exp2f(m - M) / Ls : 0.f;
-            }
-            if (s0 == 0) {
-                const int v = r / p.G, g = r % p.G;
-                const size_t qrow = ((size_t)b * p.V + v) * p.Hq + kvh * p.G + g;
-                p.lse[qrow] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
-            }
+    const float L = merge_block_sum(l, red);
+    float o[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) o[c] = 0.f;
+    constexpr int U = 4;  // splits a warp loads before using any
+    for (int s0 = warp; s0 < S; s0 += U * kMergeWarps) {
+        float ms[U], x[U][CPL];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int s = s0 + u * kMergeWarps;
+            ms[u] = s < S ? __ldcg(p.ws_m + base + (size_t)s * RP) : -INFINITY;
+            const float* orow = p.ws_o + (base + (size_t)(s < S ? s : 0) * RP) * D + lane * CPL;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) x[u][c] = s < S ? __ldcg(orow + c) : 0.f;
         }
-        __syncthreads();
-        const int items = R * (D / 4);  // (row, 4 columns)
-        for (int e0 = tid; e0 < items; e0 += 2 * nthr) {
-            float4 o[2];
-            int rr[2], cc[2];
-            size_t qrow[2];
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int e = e0 + t * nthr;
-                rr[t] = e < items ? e / (D / 4) : 0;
-                cc[t] = e < items ? (e % (D / 4)) * 4 : 0;
-                const int v = rr[t] / p.G, g = rr[t] % p.G;
-                qrow[t] = ((size_t)b * p.V + v) * p.Hq + kvh * p.G + g;
-                o[t] = (s0 == 0 || e >= items) ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                               : *reinterpret_cast<const float4*>(p.out + qrow[t] * D + cc[t]);
-            }
-            for (int s = s0; s < s1; s += 8) {  // 2 items x 8 splits of loads in flight
-                float4 x[2][8];
+        for (int u = 0; u < U; ++u) {
+            const float w = (L > 0.f && ms[u] != -INFINITY) ? exp2f(ms[u] - M) / L : 0.f;
 #pragma unroll
-                for (int t = 0; t < 2; ++t)
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        x[t][u] = (s + u < s1 && e0 + t * nthr < items)
-                                      ? __ldcg(reinterpret_cast<const float4*>(
-                                            p.ws_o + (((size_t)bk * S + s + u) * RP + rr[t]) * D + cc[t]))
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int t = 0; t < 2; ++t)
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        if (s + u < s1) {
-                            const float wgt = ww[(s + u - s0) * R + rr[t]];
-                            o[t].x = fmaf(wgt, x[t][u].x, o[t].x);
-                            o[t].y = fmaf(wgt, x[t][u].y, o[t].y);
-                            o[t].z = fmaf(wgt, x[t][u].z, o[t].z);
-                            o[t].w = fmaf(wgt, x[t][u].w, o[t].w);
-                        }
-            }
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-                if (e0 + t * nthr < items) *reinterpret_cast<float4*>(p.out + qrow[t] * D + cc[t]) = o[t];
+            for (int c = 0; c < CPL; ++c) o[c] = fmaf(w, x[u][c], o[c]);
         }
     }
-    if (tid == 0) p.counters[bk] = 0u;  // ready for the next call
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) part[warp][lane * CPL + c] = o[c];
+    __syncthreads();
+    const int v = r / p.G, g = r % p.G;
+    const size_t qrow = ((size_t)b * p.V + v) * p.Hq + kvh * p.G + g;
+    for (int col = tid; col < D; col += kMergeThreads) {
+        float x = part[0][col];
+        for (int w = 1; w < kMergeWarps; ++w) x += part[w][col];
+        p.out[qrow * D + col] = x;
+    }
+    if (tid == 0) p.lse[qrow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
 
 template <typename ST, int D, int RP>
@@ -211,7 +190,6 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
     float* alpha_s = reinterpret_cast<float*>(sm + L::oAlpha);
     float* m_s = reinterpret_cast<float*>(sm + L::oM);
     float* l_s = reinterpret_cast<float*>(sm + L::oL);
-    int* flag_s = reinterpret_cast<int*>(sm + L::oFlag);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -462,10 +440,6 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
             }
         }
     }
-    if (p.splits == 1) return;
-
-    // ---- the last CTA of this (b, kvh) to finish merges the partials in split order
-    merge_if_last<D>(p, b, kvh, RP, reinterpret_cast<float*>(sm + L::oK), (2 * kCH * L::kKRow) / 4, flag_s);
 }
 
 // ------------------------------------------------------------------ bf16 path (warp MMA)
@@ -495,7 +469,6 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     int32_t* src = reinterpret_cast<int32_t*>(sm + L::oSrc);
     float* mlw = reinterpret_cast<float*>(sm + L::oML);
     float* rowv = reinterpret_cast<float*>(sm + L::oRow);
-    int* flag_s = reinterpret_cast<int*>(sm + L::oFlag);
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -594,8 +567,8 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     };
     WarpAcc<D, RP> acc;
     acc.init();
-    mma_attend_warp<D, RP>(acc, sm + L::oStage + warp * Rows::kWarpBytes, smem_addr(sm + L::oQ), warp, nrows, rs,
-                           p.scale_log2, row_code, logit, visible);
+    mma_attend_warp<D, RP>(acc, sm + L::oStage + warp * Rows::kWarpBytes, smem_addr(sm + L::oQ), warp, nrows, p.R,
+                           rs, p.scale_log2, row_code, logit, visible);
 
     float* ow = reinterpret_cast<float*>(sm + L::oStage);  // [4][RP][D]
     mma_combine_warps<D, RP>(acc, mlw, rowv, ow);
@@ -620,9 +593,6 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
             }
         }
     }
-    if (p.splits == 1) return;
-    __syncthreads();  // the stage area is scratch for the merge
-    merge_if_last<D>(p, b, kvh, RP, reinterpret_cast<float*>(sm + L::oStage), Rows::kStagesBytes / 4, flag_s);
 }
 
 int padded_rows(int R) { return R <= 4 ? 4 : R <= 8 ? 8 : R <= 16 ? 16 : R <= 32 ? 32 : -1; }
@@ -654,14 +624,14 @@ int layout_bytes(int dtype, int d, int RP) {
 
 struct SplitPlan {
     int splits, rows_per_split, RP;
-    size_t ws_bytes, counters_offset;
+    size_t ws_bytes;
 };
 
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 // Split-K plan: one wave of CTAs over the GPU (unless the caller asks for a split count),
 // at least one chunk per split, and at most kMaxSplitRows rows per split when the rows'
-// sources are resolved up front.  Partials [bk][split][RP][d] + m, l, then counters.
+// sources are resolved up front.  Workspace: partials o [bk][split][RP][d], then m, l.
 SplitPlan plan_splits(const sd_attend_args* a) {
     SplitPlan sp{};
     const long n_rows = (long)a->n_idx * a->block + a->ring_w;
@@ -684,8 +654,7 @@ SplitPlan plan_splits(const sd_attend_args* a) {
     sp.rows_per_split = (int)rps;
     if (splits > 1) {
         const size_t np = (size_t)bk * splits * sp.RP;
-        sp.counters_offset = align16(np * (a->d + 2) * sizeof(float));
-        sp.ws_bytes = sp.counters_offset + align16((size_t)bk * sizeof(uint32_t));
+        sp.ws_bytes = align16(np * (a->d + 2) * sizeof(float));
     }
     return sp;
 }
@@ -847,9 +816,18 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
         p.ws_o = static_cast<float*>(a->workspace);
         p.ws_m = p.ws_o + np * a->d;
         p.ws_l = p.ws_m + np;
-        p.counters = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a->workspace) + sp.counters_offset);
     }
     p.resolve = (a->idx != nullptr || a->slot_map != nullptr || a->ring_w > 0) ? 1 : 0;
     cudaStream_t st = as_stream(stream);
-    return a->d == 128 ? dispatch_rp<128>(p, a->dtype, sp.RP, st) : dispatch_rp<64>(p, a->dtype, sp.RP, st);
+    const sd_status s1 = a->d == 128 ? dispatch_rp<128>(p, a->dtype, sp.RP, st) : dispatch_rp<64>(p, a->dtype, sp.RP, st);
+    if (s1 != SD_OK || sp.splits == 1) return s1;
+    // the splits' partials merged by (group, query row), all in parallel
+    const dim3 mgrid((unsigned)((long)a->B * p.Hkv), (unsigned)p.R);
+    if (a->d == 128)
+        SD_CUDA_CHECK(launch_pdl(attend_merge_kernel<128>, mgrid, dim3(kMergeThreads), 0, st, p, sp.RP),
+                      "sd_gather_attend: merge launch");
+    else
+        SD_CUDA_CHECK(launch_pdl(attend_merge_kernel<64>, mgrid, dim3(kMergeThreads), 0, st, p, sp.RP),
+                      "sd_gather_attend: merge launch");
+    return launch_status("sd_gather_attend (merge)");
 }

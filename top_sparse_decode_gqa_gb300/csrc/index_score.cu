@@ -8,6 +8,8 @@
 // one 1-D bulk copy (TMA) into a 4-stage shared-memory ring completed on mbarriers, and
 // the CUDA cores take the dot products straight from shared memory.  Each token row is
 // read by LPR lanes with one 16-byte load each; LPR-lane shuffles finish the sum.
+#include <cuda_fp16.h>
+
 #include "sd_common.cuh"
 #include "sd_host.h"
 
@@ -193,15 +195,19 @@ sd_status launch_index_score(const void* q_idx, int q_dtype, const void* k_idx, 
     return launch_status("sd_index_score");
 }
 
-template <typename KT>
+template <typename KT, typename OT>
 __global__ void block_pool_kernel(const KT* __restrict__ k_idx, int dtype, int T, int dI,
-                                  int block, float* __restrict__ pooled) {
+                                  int block, OT* __restrict__ pooled) {
     const int n = blockIdx.x, r = blockIdx.y, j = threadIdx.x;
     const int NB = T / block;
     float sum = 0.f;
     for (int t = 0; t < block; ++t)
         sum += load_elem(k_idx, dtype, ((size_t)r * T + (size_t)n * block + t) * dI + j);
-    pooled[((size_t)r * NB + n) * dI + j] = __fdiv_rn(sum, (float)block);
+    const float mean = __fdiv_rn(sum, (float)block);
+    if constexpr (sizeof(OT) == 2)
+        pooled[((size_t)r * NB + n) * dI + j] = __float2half_rn(mean);
+    else
+        pooled[((size_t)r * NB + n) * dI + j] = mean;
 }
 
 }  // namespace
@@ -216,8 +222,10 @@ sd_status index_score_common(const char* who, const void* q_idx, sd_dtype q_dtyp
                              uint32_t* key_hist, int32_t* err_word, int per_query, void* stream) {
     clear_error();
     SD_REQUIRE(B >= 0 && Hkv >= 0 && N >= 0, "%s: negative size", who);
-    SD_REQUIRE(valid_dtype(q_dtype) && valid_dtype(k_dtype), "%s: bad dtype", who);
-    const bool tc = k_dtype == SD_BF16 && q_dtype == SD_BF16;
+    const bool f16 = q_dtype == SD_F16 && k_dtype == SD_F16;
+    SD_REQUIRE(f16 || (valid_dtype(q_dtype) && valid_dtype(k_dtype)),
+               "%s: q and k must be F32 or BF16 each, or both F16", who);
+    const bool tc = f16 || (k_dtype == SD_BF16 && q_dtype == SD_BF16);
     const int vmax = per_query && tc ? 16 : 8;
     SD_REQUIRE(V >= 1 && V <= vmax, "%s: V must be in [1, %d] (got %d)", who, vmax, V);
     if (d_idx != 64 && d_idx != 128) {
@@ -237,7 +245,7 @@ sd_status index_score_common(const char* who, const void* q_idx, sd_dtype q_dtyp
         SD_REQUIRE(aligned16(q_idx), "%s: q must be 16-byte aligned", who);
         SD_REQUIRE((long)rows * N * (per_query ? V : 1) < (1L << 31) && (long)rows * V < (1L << 31),
                    "%s: too many rows", who);
-        return index_score_tc_launch(q_idx, k_idx, r, V, N, d_idx, scores, key_hist, err_word, per_query, st);
+        return index_score_tc_launch(q_idx, k_idx, r, V, N, d_idx, scores, key_hist, err_word, per_query, f16, st);
     }
     const int pq = per_query;
     if (k_dtype == SD_BF16) {
@@ -272,10 +280,11 @@ extern "C" sd_status sd_index_score_heads(const void* q, sd_dtype q_dtype, const
 }
 
 extern "C" sd_status sd_block_pool(const void* k_idx, sd_dtype k_dtype, int B, int Hkv, int T,
-                                   int d_idx, int block, float* pooled, void* stream) {
+                                   int d_idx, int block, void* pooled, sd_dtype pooled_dtype, void* stream) {
     clear_error();
     SD_REQUIRE(B >= 0 && Hkv >= 0 && T >= 0, "sd_block_pool: negative size");
     SD_REQUIRE(valid_dtype(k_dtype), "sd_block_pool: bad dtype");
+    SD_REQUIRE(pooled_dtype == SD_F32 || pooled_dtype == SD_F16, "sd_block_pool: pooled_dtype must be F32 or F16");
     SD_REQUIRE(block >= 1 && block <= 4096, "sd_block_pool: block must be in [1, 4096]");
     SD_REQUIRE(T % block == 0, "sd_block_pool: T (%d) must be a multiple of block (%d)", T, block);
     if (d_idx != 64 && d_idx != 128) {
@@ -287,11 +296,20 @@ extern "C" sd_status sd_block_pool(const void* k_idx, sd_dtype k_dtype, int B, i
     SD_REQUIRE(k_idx && pooled, "sd_block_pool: null pointer");
     SD_REQUIRE(rows <= 65535, "sd_block_pool: B*Hkv must be <= 65535");
     dim3 grid(T / block, (unsigned)rows);
-    if (k_dtype == SD_BF16)
-        block_pool_kernel<bf16_t><<<grid, d_idx, 0, as_stream(stream)>>>(
-            reinterpret_cast<const bf16_t*>(k_idx), k_dtype, T, d_idx, block, pooled);
-    else
-        block_pool_kernel<float><<<grid, d_idx, 0, as_stream(stream)>>>(
-            reinterpret_cast<const float*>(k_idx), k_dtype, T, d_idx, block, pooled);
+    cudaStream_t st = as_stream(stream);
+    const bool half_out = pooled_dtype == SD_F16;
+    if (k_dtype == SD_BF16) {
+        auto k = reinterpret_cast<const bf16_t*>(k_idx);
+        if (half_out)
+            block_pool_kernel<bf16_t, __half><<<grid, d_idx, 0, st>>>(k, k_dtype, T, d_idx, block, static_cast<__half*>(pooled));
+        else
+            block_pool_kernel<bf16_t, float><<<grid, d_idx, 0, st>>>(k, k_dtype, T, d_idx, block, static_cast<float*>(pooled));
+    } else {
+        auto k = reinterpret_cast<const float*>(k_idx);
+        if (half_out)
+            block_pool_kernel<float, __half><<<grid, d_idx, 0, st>>>(k, k_dtype, T, d_idx, block, static_cast<__half*>(pooled));
+        else
+            block_pool_kernel<float, float><<<grid, d_idx, 0, st>>>(k, k_dtype, T, d_idx, block, static_cast<float*>(pooled));
+    }
     return launch_status("sd_block_pool");
 }

@@ -57,7 +57,8 @@ struct TcLayout {
 template <int DI, int E>
 __global__ void __launch_bounds__(32 * (4 * E + 2), 1) index_score_tc_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, int rows,
-    int V, int N, float* __restrict__ scores, uint32_t* __restrict__ key_hist, int32_t* err_word, int per_query) {
+    int V, int N, float* __restrict__ scores, uint32_t* __restrict__ key_hist, int32_t* err_word, int per_query,
+    uint32_t idesc) {
     using L = TcLayout<DI>;
     constexpr int NB = 2 * E;                   // accumulators (16 TMEM columns each)
     constexpr uint32_t kTmemCols = 32u * E;     // a power of two >= 32
@@ -132,7 +133,6 @@ __global__ void __launch_bounds__(32 * (4 * E + 2), 1) index_score_tc_kernel(
         }
     } else if (warp == kIssuer) {
         if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_bf16_f32(kTileM, kQN);
             for (uint32_t i = 0; i < ntiles; ++i) {
                 const int s = (int)(i % kTcStages);
                 const int buf = (int)(i % NB);
@@ -225,16 +225,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D bf16 tensor map over [nrows, d] (row-major), box = 64 columns x box_rows rows,
-// 128-byte swizzle, zero fill outside the tensor.
-bool make_map(CUtensorMap* m, const void* base, uint64_t nrows, int d, int box_rows) {
+// 2-D tensor map of 16-bit elements (bf16 or fp16) over [nrows, d] (row-major), box = 64
+// columns x box_rows rows, 128-byte swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* m, const void* base, uint64_t nrows, int d, int box_rows, bool f16) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)nrows};
     cuuint64_t strides[1] = {(cuuint64_t)d * 2};
     cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -242,13 +243,14 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t nrows, int d, int box_r
 
 }  // namespace
 
-// bf16 keys and bf16 queries on the tensor cores; d_idx in {64, 128}, V <= 16.  per_query:
-// every query row gets its own score row (rows*V of them) instead of the max over V.
+// bf16 (or fp16) keys and queries of the same type on the tensor cores; d_idx in {64, 128},
+// V <= 16.  per_query: every query row gets its own score row (rows*V of them) instead of
+// the max over V.
 sd_status index_score_tc_launch(const void* q_idx, const void* k_idx, int rows, int V, int N, int d_idx,
-                                float* scores, uint32_t* key_hist, int32_t* err_word, int per_query, cudaStream_t st) {
+                                float* scores, uint32_t* key_hist, int32_t* err_word, int per_query, bool f16, cudaStream_t st) {
     CUtensorMap kmap, qmap;
-    if (!make_map(&kmap, k_idx, (uint64_t)rows * N, d_idx, kTileM) ||
-        !make_map(&qmap, q_idx, (uint64_t)rows * V, d_idx, kQN)) {
+    if (!make_map(&kmap, k_idx, (uint64_t)rows * N, d_idx, kTileM, f16) ||
+        !make_map(&qmap, q_idx, (uint64_t)rows * V, d_idx, kQN, f16)) {
         set_error("sd_index_score: cuTensorMapEncodeTiled failed");
         return SD_ERR_CUDA;
     }
@@ -264,7 +266,8 @@ sd_status index_score_tc_launch(const void* q_idx, const void* k_idx, int rows, 
     const int bytes = d128 ? TcLayout<128>::kBytes : TcLayout<64>::kBytes;
     SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
                   "sd_index_score: cudaFuncSetAttribute");
-    kern<<<grid, 32 * (4 * E + 2), bytes, st>>>(kmap, qmap, rows, V, N, scores, key_hist, err_word, per_query);
+    const uint32_t idesc = f16 ? umma_idesc_f16_f32(kTileM, kQN) : umma_idesc_bf16_f32(kTileM, kQN);
+    kern<<<grid, 32 * (4 * E + 2), bytes, st>>>(kmap, qmap, rows, V, N, scores, key_hist, err_word, per_query, idesc);
     return launch_status("sd_index_score (tensor cores)");
 }
 

@@ -48,7 +48,7 @@ inline const uint8_t* mapped_host_ptr(const void* h) {
 }
 
 inline bool valid_dtype(int dt) { return dt == SD_F32 || dt == SD_BF16; }
-inline int dtype_bytes(int dt) { return dt == SD_F32 ? 4 : 2; }
+inline int dtype_bytes(int dt) { return dt == SD_F32 ? 4 : 2; }  // F32 4, BF16 and F16 2
 
 // Maps the last launch error to a status (and records it).
 inline sd_status launch_status(const char* what) {
@@ -60,9 +60,10 @@ inline sd_status launch_status(const char* what) {
     return SD_OK;
 }
 
-// The indexer on the tensor cores (index_score_tc.cu): bf16 keys and queries.
+// The indexer on the tensor cores (index_score_tc.cu): bf16 keys and queries, or fp16 ones
+// (f16).
 sd_status index_score_tc_launch(const void* q_idx, const void* k_idx, int rows, int V, int N, int d_idx,
-                                float* scores, uint32_t* key_hist, int32_t* err_word, int per_query, cudaStream_t st);
+                                float* scores, uint32_t* key_hist, int32_t* err_word, int per_query, bool f16, cudaStream_t st);
 
 // Launches `kern` as a programmatic dependent of the preceding kernel in the stream: it
 // may be scheduled before that kernel finishes and must call pdl_wait() before reading

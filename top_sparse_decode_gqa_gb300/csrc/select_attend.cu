@@ -821,7 +821,7 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
                 lbase[((size_t)v * p.Hq + gg) * n_all + w0 + j] = x * kLn2f;
             }
         };
-        mma_attend_warp<D, RP>(acc, sm + L.oU + warp * Rows::kWarpBytes, smem_addr(sm + L.oQ), warp, nwin, rs,
+        mma_attend_warp<D, RP>(acc, sm + L.oU + warp * Rows::kWarpBytes, smem_addr(sm + L.oQ), warp, nwin, p.R, rs,
                                p.scale_log2, row_code, logit);
         __syncthreads();  // src is rewritten by the next window
     }

@@ -15,7 +15,8 @@ available here):
 * ``c2_llama3_8b_gqa``: Llama-3-8B-shaped GQA layer, batch 8, 32/8 heads, d = 128, bf16,
   T = 32768, top-1024 tokens, 2 % planted heavy hitters.
 * ``c3_block_sparse``: batch 4, 32/8 heads, d = 128, bf16, T = 131072 in 64-token blocks,
-  top-64 blocks by the mean-pooled block key, exact attention over the 4096 rows.
+  top-64 blocks by the mean-pooled block key, exact attention over the 4096 rows.  Its
+  indexer query is stored in fp16 (the same integers), to meet the fp16 pooled keys.
 * ``c4_tiered_verify``: batch 4, 8 speculative-verify query tokens, 32/8 heads, d = 128,
   bf16, T = 131072, one top-2048 union per KV head, 10 % of positions resident in an HBM
   pool and the full cache in pinned host memory.
@@ -77,6 +78,7 @@ class Workload:
     window_stride: int = 0  # ... moved by this many (k counts windows)
     per_head: bool = False  # select per query head from the attention logits (k per head)
     ring_w: int = 0         # > 0: draft-token ring of this many slots per layer (verify loop)
+    q_idx_dtype: str = ""   # storage type of the indexer query if not `dtype` ("f16": with fp16 pooled keys)
     cum_frac: tuple = (0.2, 0.6, 0.9)
     n_sink: int = 0
     n_recent: int = 0
@@ -133,7 +135,7 @@ WORKLOADS: Dict[str, Workload] = {
                  dI=128, k=1024, planted=655, planted_values="five_to_eight",
                  planted_attn_boost=0.5),
         Workload("c3_block_sparse", 2, B=4, V=1, Hq=32, Hkv=8, d=128, T=131072, dtype="bf16",
-                 dI=128, k=64, block=64),
+                 dI=128, k=64, block=64, q_idx_dtype="f16"),
         Workload("c4_tiered_verify", 3, B=4, V=8, Hq=32, Hkv=8, d=128, T=131072, dtype="bf16",
                  dI=128, k=2048, resident_frac=0.1),
         Workload("c5_importance_tiering", 4, B=2, V=1, Hq=28, Hkv=4, d=128, T=65536,
@@ -151,7 +153,7 @@ WORKLOADS: Dict[str, Workload] = {
 
 
 def _store(x: torch.Tensor, dtype: str) -> torch.Tensor:
-    return x.to(torch.float32 if dtype == "f32" else torch.bfloat16)
+    return x.to({"f32": torch.float32, "f16": torch.float16}.get(dtype, torch.bfloat16))
 
 
 def _randint(g, shape, dtype):
@@ -185,7 +187,7 @@ def generate(w: Workload, seed: Optional[int] = None) -> Dict[str, torch.Tensor]
     B, Hkv, V, T = w.B, w.Hkv, w.V, w.T
     out: Dict[str, torch.Tensor] = {}
     # 1. indexer query, 2. indexer keys
-    out["q_idx"] = _randint(g, (B, Hkv, V, w.dI), w.dtype)
+    out["q_idx"] = _randint(g, (B, Hkv, V, w.dI), w.q_idx_dtype or w.dtype)
     out["k_idx"] = _randint(g, (B, Hkv, T, w.dI), w.dtype)
     # 3. attention query
     if w.layers * w.steps > 1:
