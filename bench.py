@@ -242,8 +242,9 @@ class SparseDecodeStep:
             self.stage = sd.stage_buffers(self.args, self.q.dtype, device)
             self.counter = sd.stage_counter(device)
         self.keys = self.k_idx
-        if w.block > 1:
-            self.keys = sd.sd_block_pool(self.k_idx, w.block)
+        if w.block > 1:  # pooled block keys, built once (cache fill): fp16 to meet an fp16 query
+            self.keys = sd.sd_block_pool(self.k_idx, w.block, dtype=self.q_idx.dtype
+                                         if self.q_idx.dtype == torch.float16 else torch.float32)
         self.host_rows = None
 
     dominant_per_step = 1
@@ -283,8 +284,8 @@ class SparseDecodeStep:
         host memory (what the method must move: keys, selected K/V rows, queries, outputs)."""
         w = self.w
         e = w.elem_bytes
-        key_bytes = w.B * w.Hkv * w.N * w.dI * (4 if w.block > 1 else e)
-        q_idx_bytes = w.B * w.Hkv * w.V * w.dI * e
+        key_bytes = w.B * w.Hkv * w.N * w.dI * (self.keys.element_size() if w.block > 1 else e)
+        q_idx_bytes = w.B * w.Hkv * w.V * w.dI * self.q_idx.element_size()
         score_bytes = w.B * w.Hkv * w.N * 4
         row_bytes = w.d * e * 2
         kv_rows = w.B * w.Hkv * w.n_rows
@@ -493,6 +494,127 @@ class VerifyGroupStep:
                 "hbm": key_bytes + q_idx_bytes + w.B * w.Hkv * w.k * 4 + w.layers * per_layer, "host": 0}
 
 
+class LookaheadStep:
+    """One decode step over L tiered layers, each with its own selection: per layer the
+    indexer, the top-k, the copy of the selected host-resident rows into an HBM stage, and
+    the attention.  With lookahead (default) the selection and staging run on their own
+    streams ahead of the attention: layer l+1's indexer and top-k start once layer l has
+    started (its attention input is ready once layer l-1's attention is done), and its
+    staging copy (host link) runs beside layer l's attention and layer l+2's indexer (HBM).
+    Two stage buffers alternate between layers.  Without lookahead every call runs in
+    order on one stream."""
+
+    dominant = "sd_index_score"
+    phases = ()
+
+    def __init__(self, w, x, device, lookahead=True):
+        import torch
+        from top_sparse_decode_gqa_gb300 import binding as sd
+        self.sd, self.w, self.dev, self.lookahead = sd, w, device, lookahead
+        L = w.layers
+        self.launches_per_step = 5 * L  # indexer, top-k, staging, attention, merge
+        self.dominant_per_step = L
+        self.q_idx = x["q_idx"].to(device)                          # [L,B,Hkv,V,dI]
+        self.k_idx = [k.to(device) for k in x["k_idx"]]
+        self.q = x["q"][0].to(device)                               # [L,B,V,Hq,d]
+        self.k_pool = [k.to(device) for k in x["k_pool"]]
+        self.v_pool = [v.to(device) for v in x["v_pool"]]
+        self.k_host = [k.pin_memory() for k in x["k"]]
+        self.v_host = [v.pin_memory() for v in x["v"]]
+        self.slot_map = x["slot_map"].to(device)
+        self.scores = [torch.empty(w.B, w.Hkv, w.T, dtype=torch.float32, device=device) for _ in range(L)]
+        self.idx = [torch.empty(w.B, w.Hkv, w.k, dtype=torch.int32, device=device) for _ in range(L)]
+        self.key_hist = [sd.key_hist_buffer(w.B * w.Hkv, device) for _ in range(L)]
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.args = []
+        for layer in range(L):
+            a, out, lse, _ = sd.make_attend_args(self.q[layer], self.k_pool[layer], self.v_pool[layer],
+                                                 self.idx[layer], T=w.T, k_host=self.k_host[layer],
+                                                 v_host=self.v_host[layer], slot_map=self.slot_map, err_word=self.err)
+            self.args.append((a, out, lse))
+        self.stages = [sd.stage_buffers(self.args[0][0], self.q.dtype, device) for _ in range(2)]
+        self.counters = [sd.stage_counter(device) for _ in range(2)]
+        for layer in range(L):
+            ks, vs = self.stages[layer % 2]
+            self.args[layer][0].k_stage, self.args[layer][0].v_stage = ks.data_ptr(), vs.data_ptr()
+        need = sd.sd_gather_attend_workspace_bytes(self.args[0][0])
+        self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=device)
+        self.out, self.lse = self.args[-1][1], self.args[-1][2]
+        self.s_sel, self.s_stage = torch.cuda.Stream(device), torch.cuda.Stream(device)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        self.ev_sel = [ev() for _ in range(L)]
+        self.ev_stage = [ev() for _ in range(L)]
+        self.ev_att = [ev() for _ in range(L)]
+        self.ev_start = ev()
+        self.host_rows = None
+
+    def _select(self, layer, m):
+        sd, w = self.sd, self.w
+        if m is not None:
+            m.before(layer)
+        sd.sd_index_score(self.q_idx[layer], self.k_idx[layer], self.scores[layer], self.err,
+                          key_hist=self.key_hist[layer])
+        if m is not None:
+            m.after(layer)
+        sd.sd_topk(self.scores[layer], w.k, self.idx[layer], key_hist=self.key_hist[layer])
+
+    def run(self, m: "StepMarks" = None):
+        import torch
+        sd, L = self.sd, self.w.layers
+        main = torch.cuda.current_stream()
+        if m is not None:
+            m.start.record()
+        if not self.lookahead:
+            for layer in range(L):
+                self._select(layer, m)
+                sd.sd_stage_host_rows(self.args[layer][0], self.counters[layer % 2])
+                sd.sd_gather_attend(self.args[layer][0], self.ws)
+            if m is not None:
+                m.end.record()
+            return
+        self.ev_start.record(main)
+        self.s_sel.wait_event(self.ev_start)
+        self.s_stage.wait_event(self.ev_start)
+        for layer in range(L):
+            with torch.cuda.stream(self.s_sel):
+                if layer >= 2:  # layer - 1 has started: layer - 2's attention is done
+                    self.s_sel.wait_event(self.ev_att[layer - 2])
+                self._select(layer, m)
+                self.ev_sel[layer].record(self.s_sel)
+            with torch.cuda.stream(self.s_stage):
+                self.s_stage.wait_event(self.ev_sel[layer])
+                sd.sd_stage_host_rows(self.args[layer][0], self.counters[layer % 2], stream=self.s_stage)
+                self.ev_stage[layer].record(self.s_stage)
+            main.wait_event(self.ev_stage[layer])
+            sd.sd_gather_attend(self.args[layer][0], self.ws, stream=main)
+            self.ev_att[layer].record(main)
+        if m is not None:
+            m.end.record()
+
+    def after_warmup(self):
+        """Counts the selected rows that live in host memory (fixed by the inputs)."""
+        import torch
+        rows = 0
+        b = torch.arange(self.w.B, device=self.dev)[:, None, None]
+        for layer in range(self.w.layers):
+            rows += int((self.slot_map[b, self.idx[layer].long()] < 0).sum().item())
+        self.host_rows = rows
+
+    def bytes(self):
+        w = self.w
+        e = w.elem_bytes
+        key_bytes = w.B * w.Hkv * w.T * w.dI * e
+        q_idx_bytes = w.B * w.Hkv * w.V * w.dI * e
+        score_bytes = w.B * w.Hkv * w.T * 4
+        row = w.d * e * 2
+        host_rows = self.host_rows or 0
+        dev_rows = w.layers * w.B * w.Hkv * w.k - host_rows
+        q_bytes = w.B * w.V * w.Hq * w.d * e
+        out_bytes = w.B * w.V * w.Hq * (w.d + 1) * 4 + w.B * w.Hkv * w.k * 4
+        hbm = w.layers * (key_bytes + q_idx_bytes + q_bytes + out_bytes) + dev_rows * row
+        return {"dominant": key_bytes + q_idx_bytes + score_bytes, "hbm": hbm, "host": host_rows * row}
+
+
 class DenseScoringStep:
     """One decode step of the importance-scoring workload: for every layer, dense attention
     over all cached rows (logits kept) and that layer's term of the importance score."""
@@ -562,7 +684,9 @@ class DenseScoringStep:
                 "host": 0}
 
 
-def make_step(w, x, device, separate=False, tiered_path="staged"):
+def make_step(w, x, device, separate=False, tiered_path="staged", lookahead=True):
+    if w.layer_indexers:
+        return LookaheadStep(w, x, device, lookahead)
     if w.ring_w > 0:
         return VerifyGroupStep(w, x, device)
     if w.layers > 1:
@@ -610,7 +734,7 @@ def run_ours(args):
         dist.barrier()
     w = WORKLOADS[args.workload]
     x = generate(w)
-    step = make_step(w, x, device, args.separate, args.tiered_path)
+    step = make_step(w, x, device, args.separate, args.tiered_path, not args.no_lookahead)
     props = torch.cuda.get_device_properties(device)
     flush = torch.empty(2 * max(int(getattr(props, "L2_cache_size", 0)), 128 << 20), dtype=torch.uint8,
                         device=device)
@@ -668,7 +792,7 @@ def run_ours(args):
     by = step.bytes()
     dom_s = statistics.mean(dom_ms) / 1e3
     achieved = by["dominant"] / dom_s / 1e9
-    if isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep)):
+    if isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep, LookaheadStep)):
         kernel_file, kernel_tag = ("index_score.cu", "index_score_tc.cu", "tc_common.cuh", "sd_common.cuh"), "index_score"
     else:
         kernel_file, kernel_tag = ("gather_attend.cu", "sd_common.cuh"), "gather_attend"
@@ -679,9 +803,16 @@ def run_ours(args):
     t_roof = by["hbm"] / (peak * 1e9)
     if by["host"]:
         host_gbs = host_link_gbs(device)
-        t_roof += by["host"] / (host_gbs * 1e9)
+        t_host = by["host"] / (host_gbs * 1e9)
         step_roof.update({"host_bytes": by["host"], "host_link_gbs_measured": round(host_gbs, 1),
                           "bound": "hbm+host"})
+        if isinstance(step, LookaheadStep) and step.lookahead:
+            # the host copies of one layer run beside another layer's HBM work: the bound is
+            # the larger of the two streams of bytes, not their sum
+            step_roof.update({"bound": "max(hbm, host)", "t_roof_serial_us": round((t_roof + t_host) * 1e6, 2)})
+            t_roof = max(t_roof, t_host)
+        else:
+            t_roof += t_host
     step_roof["t_roof_us"] = round(t_roof * 1e6, 2)
     step_roof["frac"] = round(t_roof / step_s, 4)
     if isinstance(step, SparseDecodeStep) and step.fused:
@@ -700,6 +831,19 @@ def run_ours(args):
             "topk": k_us(lambda m: m.dom[0][1], lambda m: m.phase["after_topk"]),
             "stage_host_rows": k_us(lambda m: m.phase["after_topk"], lambda m: m.phase["after_stage"]),
             "gather_attend": k_us(lambda m: m.phase["after_stage"], lambda m: m.end)}
+    elif isinstance(step, LookaheadStep):
+        step_roof["kernel_us"] = {"index_score": round(statistics.mean(dom_ms) * 1e3, 2), "layers": w.layers}
+        if step.lookahead:  # the same steps with every call in order on one stream, for comparison
+            step.lookahead = False
+            serial = []
+            for _ in range(min(K, 20)):
+                clean_l2()
+                sm_ = StepMarks(0)
+                step.run(sm_)
+                torch.cuda.synchronize()
+                serial.append(sm_.step_ms())
+            step.lookahead = True
+            step_roof["serial_ms_per_step"] = round(statistics.mean(serial), 5)
     elif isinstance(step, VerifyGroupStep):
         after_topk = [m.dom[0][1].elapsed_time(m.phase["after_topk"]) for m in kmarks]
         tail = [m.phase["after_topk"].elapsed_time(m.end) for m in kmarks]
@@ -743,6 +887,10 @@ def run_ours(args):
                             else f"indexer + top-k once, then per layer ({w.layers}) ring append + gather-attend "
                                  "over the selected rows and the draft ring"
                             if isinstance(step, VerifyGroupStep)
+                            else f"per layer ({w.layers}): indexer + top-k + host-row staging + gather-attend, "
+                                 + ("selection and staging on their own streams ahead of the attention"
+                                    if step.lookahead else "in order on one stream")
+                            if isinstance(step, LookaheadStep)
                             else "dense attention + score accumulate per layer"),
                    "l2": "flushed between timed steps: 2x L2 written then read, outside the events",
                    "parallelism": f"replica x{world} (each rank its own batch)"},
@@ -771,14 +919,15 @@ def measure_e2e(step, w, x, clean_l2, K):
     host memory; host wall clock per step, including the copies and the final sync."""
     import torch
     verify = isinstance(step, VerifyGroupStep)
-    ins = [(step.q, x["q"][0] if verify else x["q"][0, 0] if w.layers > 1 else x["q"])]
-    if isinstance(step, (SparseDecodeStep, WindowStep, VerifyGroupStep)):
+    multi = isinstance(step, (VerifyGroupStep, LookaheadStep))
+    ins = [(step.q, x["q"][0] if multi else x["q"][0, 0] if w.layers > 1 else x["q"])]
+    if isinstance(step, (SparseDecodeStep, WindowStep, VerifyGroupStep, LookaheadStep)):
         ins.append((step.q_idx, x["q_idx"]))
     if verify:  # the drafts' K/V come from the host with the queries
         ins += [(step.draft_k, x["draft_k"]), (step.draft_v, x["draft_v"])]
     ins = [(dst, src.contiguous().pin_memory()) for dst, src in ins]
-    sparse = isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep))
-    outs = [step.out, step.lse] + ([step.idx] if sparse else [step.s])
+    sparse = isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep, LookaheadStep))
+    outs = [step.out, step.lse] + ([step.idx[-1] if isinstance(step.idx, list) else step.idx] if sparse else [step.s])
     outs = [(src, torch.empty(src.shape, dtype=src.dtype).pin_memory()) for src in outs]
     times = []
     for i in range(K + 3):
@@ -806,6 +955,17 @@ def oracle_step(w, x, b0, b1):
     import oracle
     nb = b1 - b0
     scale = 1.0 / math.sqrt(w.d)
+    if w.layer_indexers:  # every layer: its own selection, then attention over its rows
+        res = []
+        for layer in range(w.layers):
+            sc = oracle.index_score(x["q_idx"][layer, b0:b1].contiguous(), x["k_idx"][layer][b0:b1].contiguous(), nb,
+                                    w.Hkv, w.V, w.N, w.dI)
+            idx = oracle.topk(sc, w.k)
+            res.append((idx, oracle.gather_attend(x["q"][0, layer, b0:b1].contiguous(),
+                                                  x["k"][layer][b0:b1].contiguous(),
+                                                  x["v"][layer][b0:b1].contiguous(), idx, nb, w.V, w.Hq, w.Hkv, w.d,
+                                                  w.T, w.k, 1, scale)))
+        return res
     if w.ring_w > 0:  # one selection for the layer group, then per layer: ring append + attention
         sc = oracle.index_score(x["q_idx"][b0:b1].contiguous(), x["k_idx"][b0:b1].contiguous(), nb, w.Hkv, w.V,
                                 w.N, w.dI)
@@ -925,6 +1085,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--separate", action="store_true",
                     help="run top-k and gather-attend as two launches instead of the fused one")
+    ap.add_argument("--no-lookahead", action="store_true",
+                    help="multi-layer tiered workloads: run every layer's calls in order on one stream")
     ap.add_argument("--tiered-path", choices=("staged", "fused"), default="staged",
                     help="tiered workloads: stage the selected host rows into HBM with one copy kernel "
                          "before the attention (staged), or read them inside the fused select/attend")

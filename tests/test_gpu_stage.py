@@ -175,3 +175,29 @@ def test_c4_staged_pipeline_full():
         assert_attend_close(out[b:b + 1, :, h * w.G:(h + 1) * w.G], ro)
         assert_attend_close(lse[b:b + 1, :, h * w.G:(h + 1) * w.G], rl, "lse")
     del stage
+
+
+def test_c9_lookahead_full():
+    # the benchmark's multi-layer tiered workload in its launch configuration: every layer's
+    # selection and staging run on their own streams ahead of the attention, and the results
+    # are the same bits as the same calls in order on one stream, and the oracle's values
+    import bench
+    from top_sparse_decode_gqa_gb300.workloads import WORKLOADS, generate
+    w = WORKLOADS["c9_lookahead_tiered"]
+    x = generate(w)
+    step = bench.make_step(w, x, torch.device("cuda"), lookahead=True)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.err.item()) == 0
+    got = [(step.idx[l].clone(), step.args[l][1].clone(), step.args[l][2].clone()) for l in range(w.layers)]
+    step.lookahead = False
+    step.run()
+    torch.cuda.synchronize()
+    for l in range(w.layers):
+        assert torch.equal(step.idx[l], got[l][0])
+        assert torch.equal(step.args[l][1], got[l][1]) and torch.equal(step.args[l][2], got[l][2])
+    ref = bench.oracle_step(w, x, 0, 1)  # sequence 0, every layer
+    for l, (ri, (ro, rl, _)) in enumerate(ref):
+        np.testing.assert_array_equal(got[l][0][:1].cpu().numpy(), ri)
+        assert_attend_close(got[l][1][:1], ro)
+        assert_attend_close(got[l][2][:1], rl, "lse")

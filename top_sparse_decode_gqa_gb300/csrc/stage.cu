@@ -36,7 +36,7 @@ struct StageParams {
     int32_t* err;
 };
 
-__global__ void __launch_bounds__(kStThreads, 4) stage_host_rows_kernel(const StageParams p) {
+__global__ void __launch_bounds__(kStThreads, 1) stage_host_rows_kernel(const StageParams p) {
     pdl_wait();  // idx (and the slot map) may come from the preceding kernel
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
@@ -151,8 +151,10 @@ extern "C" sd_status sd_stage_host_rows(const sd_attend_args* a, uint32_t* count
     p.counter = counter;
     p.err = a->err_word;
     if (p.total_rows == 0) return SD_OK;
-    // one wave of 4 CTAs (32 warps) per SM: 128 KB of host reads in flight per SM
-    const int grid = num_sms() * 4;
+    // one CTA (8 warps, 32 KB of host reads in flight) per SM is several times what the host
+    // link can serve, and leaves each SM room for other kernels running beside the copy
+    // (the next layer's indexer, the current layer's attention)
+    const int grid = num_sms();
     SD_CUDA_CHECK(launch_pdl(stage_host_rows_kernel, dim3((unsigned)grid), dim3(kStThreads), 0, as_stream(stream), p),
                   "sd_stage_host_rows: launch");
     return launch_status("sd_stage_host_rows");

@@ -37,6 +37,10 @@ available here):
   appends the 8 drafts' K/V to its own 64-slot window-bounded ring (which already holds the
   56 most recent accepted tokens) and attends the selected rows plus the ring, causally
   among the drafts.
+* ``c9_lookahead_tiered``: 4 layers of the tiered verify layer of ``c4`` at batch 2, each
+  with its own indexer query and keys (a selection per layer), its own K/V cache in pinned
+  host memory and its own HBM pool of the same resident 10 % of positions; the step runs
+  layer l+1's indexer, top-k and host-row staging ahead, beside layer l's attention.
 
 Value recipe: indexer query and keys are integers drawn uniformly from [-8, 8] (exact in
 bf16 and fp32); attention q, K, V are standard normal, rounded to bf16 (nearest even)
@@ -79,6 +83,7 @@ class Workload:
     per_head: bool = False  # select per query head from the attention logits (k per head)
     ring_w: int = 0         # > 0: draft-token ring of this many slots per layer (verify loop)
     q_idx_dtype: str = ""   # storage type of the indexer query if not `dtype` ("f16": with fp16 pooled keys)
+    layer_indexers: bool = False  # one indexer query and key set per layer (selection per layer)
     cum_frac: tuple = (0.2, 0.6, 0.9)
     n_sink: int = 0
     n_recent: int = 0
@@ -148,6 +153,8 @@ WORKLOADS: Dict[str, Workload] = {
                  per_head=True),
         Workload("c8_verify_layer_group", 7, B=2, V=8, Hq=32, Hkv=8, d=128, T=32768, dtype="bf16",
                  dI=128, k=1024, layers=4, ring_w=64),
+        Workload("c9_lookahead_tiered", 8, B=2, V=8, Hq=32, Hkv=8, d=128, T=131072, dtype="bf16",
+                 dI=128, k=2048, resident_frac=0.1, layers=4, layer_indexers=True),
     )
 }
 
@@ -186,9 +193,13 @@ def generate(w: Workload, seed: Optional[int] = None) -> Dict[str, torch.Tensor]
     g = torch.Generator().manual_seed(1000 + w.cfg_id if seed is None else seed)
     B, Hkv, V, T = w.B, w.Hkv, w.V, w.T
     out: Dict[str, torch.Tensor] = {}
-    # 1. indexer query, 2. indexer keys
-    out["q_idx"] = _randint(g, (B, Hkv, V, w.dI), w.q_idx_dtype or w.dtype)
-    out["k_idx"] = _randint(g, (B, Hkv, T, w.dI), w.dtype)
+    # 1. indexer query, 2. indexer keys (per layer: all layers' queries, then all layers' keys)
+    if w.layer_indexers:
+        out["q_idx"] = _randint(g, (w.layers, B, Hkv, V, w.dI), w.q_idx_dtype or w.dtype)
+        out["k_idx"] = [_randint(g, (B, Hkv, T, w.dI), w.dtype) for _ in range(w.layers)]
+    else:
+        out["q_idx"] = _randint(g, (B, Hkv, V, w.dI), w.q_idx_dtype or w.dtype)
+        out["k_idx"] = _randint(g, (B, Hkv, T, w.dI), w.dtype)
     # 3. attention query
     if w.layers * w.steps > 1:
         out["q"] = _randn(g, (w.steps, w.layers, B, V, w.Hq, w.d), w.dtype)
@@ -236,8 +247,12 @@ def generate(w: Workload, seed: Optional[int] = None) -> Dict[str, torch.Tensor]
         out["resident"] = res
         out["slot_map"] = slot_map
         idx = res[:, None, :, None].expand(B, Hkv, P, w.d)
-        out["k_pool"] = torch.gather(out["k"], 2, idx).contiguous()
-        out["v_pool"] = torch.gather(out["v"], 2, idx).contiguous()
+        if isinstance(out["k"], list):  # every layer's pool holds the same resident positions
+            out["k_pool"] = [torch.gather(k, 2, idx).contiguous() for k in out["k"]]
+            out["v_pool"] = [torch.gather(v, 2, idx).contiguous() for v in out["v"]]
+        else:
+            out["k_pool"] = torch.gather(out["k"], 2, idx).contiguous()
+            out["v_pool"] = torch.gather(out["v"], 2, idx).contiguous()
     # 8. draft ring: its K/V, then the drafts' K/V
     if w.ring_w > 0:
         W, L = w.ring_w, max(1, w.layers)
