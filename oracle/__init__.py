@@ -66,7 +66,8 @@ def _check(rc, what):
 
 
 def _as_data(x):
-    """Return (contiguous numpy array, dtype code) for fp32 or bfloat16 data."""
+    """Return (contiguous numpy array, dtype code) for fp32, bfloat16 or float16 data (float16
+    passed on as the equal fp32 values)."""
     try:
         import torch
         if isinstance(x, torch.Tensor):
@@ -75,6 +76,8 @@ def _as_data(x):
                 return x.view(torch.int16).numpy().view(np.uint16), BF16
             if x.dtype == torch.float32:
                 return x.numpy(), F32
+            if x.dtype == torch.float16:  # every binary16 value is a binary32 value: exact
+                return x.to(torch.float32).numpy(), F32
             raise TypeError(f"unsupported tensor dtype {x.dtype}")
     except ImportError:
         pass
@@ -283,3 +286,51 @@ def quantize_rows_int8(x, tier, B, Hkv, T, d, codes=None, scales=None):
     _check(_load().oracle_quantize_rows_int8(_ptr(xa), xd, _ptr(ta), B, Hkv, T, d, _ptr(codes),
                                              _ptr(scales)), "quantize_rows_int8")
     return codes, scales
+
+
+def promote_rows(idx, block, slot_map, pool_pos, hand, k_host, v_host, k_pool, v_pool):
+    """Keeps the HBM pool as a cache of host rows (Adaptive DHiSparse "Metodologia": the
+    pool holds extra history while memory allows; SparDA sec. 2 item 3: needed rows are
+    fetched ahead).  Reading taken, per sequence b:
+      1. the step's selected positions are the union over the KV heads of the rows of
+         idx[b, h, :] (block-expanded; -1 entries empty);
+      2. the misses are the selected positions whose slot_map is -1, in ascending order;
+      3. a slot is pinned when it holds a selected position; the victims are the first
+         unpinned slots in ring order starting at hand[b], one per miss while they last;
+      4. miss m goes to victim m: the victim's old position (if any) leaves the pool
+         (slot_map = -1), the miss's host K/V rows of every KV head are copied into the
+         slot, slot_map[b, miss] = slot, pool_pos[b, slot] = miss;
+      5. hand[b] moves past the last victim taken (unchanged when there is none).
+    All arrays are numpy (modified in place): idx [B,Hkv,n_idx], slot_map [B,T],
+    pool_pos [B,P], hand [B], k/v_host [B,Hkv,T,d], k/v_pool [B,Hkv,P,d].
+    Returns the number of rows promoted per sequence."""
+    B, Hkv, n_idx = idx.shape
+    T, P = slot_map.shape[1], pool_pos.shape[1]
+    promoted = []
+    for b in range(B):
+        sel = set()
+        for h in range(Hkv):
+            for e in idx[b, h]:
+                if e >= 0:
+                    sel.update(range(int(e) * block, int(e) * block + block))
+        misses = sorted(t for t in sel if slot_map[b, t] == -1)
+        victims = []
+        for i in range(P):
+            if len(victims) == len(misses):
+                break
+            s = (int(hand[b]) + i) % P
+            if pool_pos[b, s] < 0 or int(pool_pos[b, s]) not in sel:
+                victims.append(s)
+        for t, s in zip(misses, victims):
+            old = int(pool_pos[b, s])
+            if old >= 0:
+                slot_map[b, old] = -1
+            k_pool[b, :, s] = k_host[b, :, t]
+            v_pool[b, :, s] = v_host[b, :, t]
+            slot_map[b, t] = s
+            pool_pos[b, s] = t
+        taken = min(len(misses), len(victims))
+        if taken:
+            hand[b] = (victims[taken - 1] + 1) % P
+        promoted.append(taken)
+    return promoted

@@ -709,3 +709,75 @@ def test_ring_append_keeps_the_last_window():
                     assert s == ring_pos[b, s] % W
                     np.testing.assert_array_equal(ring_k[b, :, s], toks_k[b, :, ring_pos[b, s]])
                     np.testing.assert_array_equal(ring_v[b, :, s], toks_v[b, :, ring_pos[b, s]])
+
+
+# ----------------------------------------------------------------------------- pool as a cache
+
+
+def _pool_state(pool_pos, T):
+    slot_map = np.full((pool_pos.shape[0], T), -1, dtype=np.int32)
+    for b in range(pool_pos.shape[0]):
+        for s, t in enumerate(pool_pos[b]):
+            if t >= 0:
+                slot_map[b, t] = s
+    return slot_map
+
+
+def test_promote_hand_worked_example():
+    gd = load_golden("promote_small.json")
+    T, P = gd["T"], gd["P"]
+    idx = np.array(gd["idx"], dtype=np.int32)
+    pool_pos = np.array(gd["pool_pos_before"], dtype=np.int32)
+    slot_map = _pool_state(pool_pos, T)
+    hand = np.array(gd["hand_before"], dtype=np.int32)
+    kh = np.arange(1 * 2 * T * 4, dtype=np.float64).reshape(1, 2, T, 4)
+    vh = -kh
+    kp, vp = np.zeros((1, 2, P, 4)), np.zeros((1, 2, P, 4))
+    n = oracle.promote_rows(idx, gd["block"], slot_map, pool_pos, hand, kh, vh, kp, vp)
+    assert n == gd["promoted"]
+    np.testing.assert_array_equal(pool_pos, gd["pool_pos_after"])
+    np.testing.assert_array_equal(slot_map, gd["slot_map_after"])
+    np.testing.assert_array_equal(hand, gd["hand_after"])
+    for s, t in enumerate(pool_pos[0]):
+        if t in (1, 5, 10):
+            np.testing.assert_array_equal(kp[0, :, s], kh[0, :, t])
+            np.testing.assert_array_equal(vp[0, :, s], vh[0, :, t])
+    assert oracle.promote_rows(idx, gd["block"], slot_map, pool_pos, hand, kh, vh, kp, vp) == [0]
+
+
+def test_promote_invariants_under_random_drifting_selections():
+    rng = np.random.default_rng(7)
+    B, Hkv, T, P, n, blk, d = 3, 2, 400, 60, 9, 4, 2
+    kh = rng.standard_normal((B, Hkv, T, d))
+    vh = rng.standard_normal((B, Hkv, T, d))
+    kp, vp = np.zeros((B, Hkv, P, d)), np.zeros((B, Hkv, P, d))
+    pool_pos = np.full((B, P), -1, dtype=np.int32)
+    slot_map = np.full((B, T), -1, dtype=np.int32)
+    hand = np.zeros(B, dtype=np.int32)
+    base = rng.permutation(T // blk)[:n]
+    for step in range(12):
+        idx = np.empty((B, Hkv, n), dtype=np.int32)
+        for b in range(B):
+            for h in range(Hkv):
+                cur = base.copy()
+                cur[rng.integers(0, n, 2)] = rng.integers(0, T // blk, 2)  # drift
+                idx[b, h] = np.sort(cur)
+        before = slot_map.copy()
+        oracle.promote_rows(idx, blk, slot_map, pool_pos, hand, kh, vh, kp, vp)
+        for b in range(B):
+            sel = {int(e) * blk + o for h in range(Hkv) for e in idx[b, h] for o in range(blk)}
+            # slot_map and pool_pos are inverse maps of the occupied slots
+            assert all(slot_map[b, t] == s for s, t in enumerate(pool_pos[b]) if t >= 0)
+            assert all(pool_pos[b, s] == t for t, s in enumerate(slot_map[b]) if s >= 0)
+            # pool rows hold the host rows of their positions
+            for s, t in enumerate(pool_pos[b]):
+                if t >= 0:
+                    np.testing.assert_array_equal(kp[b, :, s], kh[b, :, t])
+                    np.testing.assert_array_equal(vp[b, :, s], vh[b, :, t])
+            # a selected row resident before the step stays resident
+            assert all(slot_map[b, t] >= 0 for t in sel if before[b, t] >= 0)
+            # every selected row is resident unless every slot holds a selected row
+            if len(sel) <= P:
+                assert all(slot_map[b, t] >= 0 for t in sel)
+            else:
+                assert sum(slot_map[b, t] >= 0 for t in sel) == P
