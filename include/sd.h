@@ -267,6 +267,30 @@ sd_status sd_gather_attend_noalloc(const sd_attend_args* args, void* stream);
 sd_status sd_stage_host_rows(const sd_attend_args* args, uint32_t* counter, void* stream);
 
 /*
+ * sd_promote_rows -- keep the HBM pool as a cache of host rows.
+ * [DHiSparse] "Metodologia" (the GPU keeps extra history while memory allows and fetches
+ * the rest); [SparDA] sec. 2 item 3 (the needed rows are fetched ahead).  Reading taken,
+ * per sequence b: the step's selected positions (the union over the groups of args->idx,
+ * block-expanded, -1 entries empty) whose slot_map is -1 are the misses; in ascending
+ * position order they go to the first slots of a ring of pool_rows slots, taken in order
+ * from hand[b], that do not hold a position selected in this step.  A slot's old position
+ * leaves the pool (slot_map = -1); the miss's K and V rows of every KV head are copied from
+ * k_host/v_host into the pool (args->k_cache/v_cache, which this call writes), slot_map[b,
+ * miss] = slot, pool_pos[b, slot] = miss, and hand[b] moves past the last slot taken.
+ * Misses beyond the free slots stay in host memory.  A following sd_gather_attend reads the
+ * promoted rows from HBM, with the same bits (the values are the same).
+ * pool_pos [B, pool_rows] int32 (slot -> position, -1 empty) and hand [B] int32 are the
+ * caller's device state, kept consistent with slot_map between calls.  The workspace
+ * (sd_promote_rows_workspace_bytes) must be zero-filled before the first call; every call
+ * leaves it ready for the next.  Three launches (mark, plan, copy), each a programmatic
+ * dependent of the one before.  Limits as sd_gather_attend; needs idx, slot_map, the pool
+ * and the host cache.
+ */
+size_t sd_promote_rows_workspace_bytes(const sd_attend_args* args);
+sd_status sd_promote_rows(const sd_attend_args* args, int32_t* pool_pos, int32_t* hand, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/*
  * sd_ring_append -- write new tokens' K/V into the window-bounded draft ring.
  * [DHiSparse] "Metodologia" (the draft tokens' K/V live in a ring bounded by a window).
  * Token i < n of sequence b, at position pos0[b] + i, goes to slot (pos0[b] + i) mod W:

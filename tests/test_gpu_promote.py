@@ -1,0 +1,159 @@
+"""The HBM pool kept as a cache (sd_promote_rows): over several steps of drifting
+selections the device's slot map, reverse map, hand and pool rows equal the oracle's
+after every step, bit for bit; the attention over promoted rows gives the same bits as over
+the same rows read from host memory; and the full-size tiered verify workload promotes
+its selection.  All calls go through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from top_sparse_decode_gqa_gb300 import build
+    build.build()
+
+
+def sd():
+    from top_sparse_decode_gqa_gb300 import binding
+    return binding
+
+
+def _drift(rng, base, n, n_blocks, groups, B):
+    idx = np.empty((B, groups, n), dtype=np.int32)
+    for b in range(B):
+        for h in range(groups):
+            cur = base.copy()
+            k = rng.integers(1, 4)
+            cur[rng.integers(0, n, k)] = rng.integers(0, n_blocks, k)
+            cur = np.unique(cur)
+            row = np.full(n, -1, dtype=np.int32)  # duplicates removed: the tail stays empty
+            row[:len(cur)] = cur
+            idx[b, h] = row
+    return idx
+
+
+@pytest.mark.parametrize("T,P,n,block,per_head", [(2000, 60, 9, 4, False), (4096, 300, 64, 1, False),
+                                                  (1000, 50, 12, 1, True), (640, 8, 5, 2, False)])
+def test_promotion_matches_the_oracle_over_drifting_steps(T, P, n, block, per_head):
+    rng = np.random.default_rng(T + P)
+    B, Hq, Hkv, d = 3, 8, 2, 128
+    groups = Hq if per_head else Hkv
+    kh = torch.randn(B, Hkv, T, d, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    vh = torch.randn(B, Hkv, T, d, generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
+    k_host, v_host = kh.pin_memory(), vh.pin_memory()
+    k_pool = torch.zeros(B, Hkv, P, d, dtype=torch.bfloat16, device="cuda")
+    v_pool = torch.zeros_like(k_pool)
+    slot_map = torch.full((B, T), -1, dtype=torch.int32, device="cuda")
+    pool_pos, hand = sd().pool_state(slot_map, P)
+    q = torch.zeros(B, 1, Hq, d, dtype=torch.bfloat16, device="cuda")
+    # the oracle's copy of the state
+    o_slot = np.full((B, T), -1, dtype=np.int32)
+    o_pos = np.full((B, P), -1, dtype=np.int32)
+    o_hand = np.zeros(B, dtype=np.int32)
+    o_kp = np.zeros((B, Hkv, P, d), dtype=np.float32)
+    o_vp = np.zeros((B, Hkv, P, d), dtype=np.float32)
+    khf, vhf = kh.float().numpy(), vh.float().numpy()
+    base = rng.permutation(T // block)[:n].astype(np.int32)
+    ws = None
+    for step in range(6):
+        idx_np = _drift(rng, base, n, T // block, groups, B)
+        idx = torch.from_numpy(idx_np).cuda()
+        a, _, _, _ = sd().make_attend_args(q, k_pool, v_pool, idx, block=block, T=T, k_host=k_host, v_host=v_host,
+                                           slot_map=slot_map, per_head=per_head)
+        ws = sd().sd_promote_rows(a, pool_pos, hand, ws)
+        torch.cuda.synchronize()
+        # (with per-head selections the union over the query heads is what is promoted)
+        oracle.promote_rows(idx_np, block, o_slot, o_pos, o_hand, khf, vhf, o_kp, o_vp)
+        np.testing.assert_array_equal(slot_map.cpu().numpy(), o_slot, err_msg=f"step {step}")
+        np.testing.assert_array_equal(pool_pos.cpu().numpy(), o_pos)
+        np.testing.assert_array_equal(hand.cpu().numpy(), o_hand)
+        occ = o_pos >= 0
+        kp, vp = k_pool.float().cpu().numpy(), v_pool.float().cpu().numpy()
+        for b in range(B):
+            np.testing.assert_array_equal(kp[b][:, occ[b]], o_kp[b][:, occ[b]])
+            np.testing.assert_array_equal(vp[b][:, occ[b]], o_vp[b][:, occ[b]])
+
+
+def test_attention_over_promoted_rows_is_the_same():
+    from top_sparse_decode_gqa_gb300.workloads import residency_map
+    g = torch.Generator().manual_seed(5)
+    B, Hq, Hkv, d, T, n, V = 2, 16, 4, 128, 4096, 200, 2
+    q = torch.randn(B, V, Hq, d, generator=g).to(torch.bfloat16).cuda()
+    K = torch.randn(B, Hkv, T, d, generator=g).to(torch.bfloat16)
+    Vv = torch.randn(B, Hkv, T, d, generator=g).to(torch.bfloat16)
+    idx = torch.stack([torch.stack([torch.sort(torch.randperm(T, generator=g)[:n]).values for _ in range(Hkv)])
+                       for _ in range(B)]).int().cuda()
+    P = T // 4
+    res, slot_map = residency_map(B, T, P, 7)
+    gi = res[:, None, :, None].expand(B, Hkv, P, d)
+    k_pool = torch.gather(K, 2, gi).contiguous().cuda()
+    v_pool = torch.gather(Vv, 2, gi).contiguous().cuda()
+    slot_map = slot_map.cuda()
+    k_host, v_host = K.pin_memory(), Vv.pin_memory()
+    e = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a, out, lse, _ = sd().make_attend_args(q, k_pool, v_pool, idx, T=T, k_host=k_host, v_host=v_host,
+                                           slot_map=slot_map, err_word=e)
+    ws = torch.zeros(max(16, sd().sd_gather_attend_workspace_bytes(a)), dtype=torch.uint8, device="cuda")
+    sd().sd_gather_attend(a, ws)
+    torch.cuda.synchronize()
+    o0, l0 = out.clone(), lse.clone()
+    host_before = int((slot_map.gather(1, idx.view(B, -1).long()) < 0).sum().item())
+    pool_pos, hand = sd().pool_state(slot_map, P)
+    sd().sd_promote_rows(a, pool_pos, hand)
+    sd().sd_gather_attend(a, ws)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    assert torch.equal(out, o0) and torch.equal(lse, l0)
+    host_after = int((slot_map.gather(1, idx.view(B, -1).long()) < 0).sum().item())
+    assert host_before > 0 and host_after == 0  # the pool had room for the whole selection
+
+
+def test_c4_promotion_full():
+    # the tiered verify workload: its selection promoted into the 10 % pool (more misses
+    # than free slots), then the attention over pool and host rows; the same bits as before
+    from top_sparse_decode_gqa_gb300.workloads import WORKLOADS, generate
+    w = WORKLOADS["c4_tiered_verify"]
+    x = generate(w)
+    dev = {k: x[k].cuda() for k in ("q_idx", "k_idx", "q", "slot_map", "k_pool", "v_pool")}
+    k_host, v_host = x["k"].pin_memory(), x["v"].pin_memory()
+    e = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hist = sd().key_hist_buffer(w.B * w.Hkv)
+    scores = sd().sd_index_score(dev["q_idx"], dev["k_idx"], key_hist=hist)
+    idx = sd().sd_topk(scores, w.k, key_hist=hist)
+    a, out, lse, _ = sd().make_attend_args(dev["q"], dev["k_pool"], dev["v_pool"], idx, T=w.T, k_host=k_host,
+                                           v_host=v_host, slot_map=dev["slot_map"], err_word=e)
+    ws = torch.zeros(max(16, sd().sd_gather_attend_workspace_bytes(a)), dtype=torch.uint8, device="cuda")
+    sd().sd_gather_attend(a, ws)
+    torch.cuda.synchronize()
+    o0, l0 = out.clone(), lse.clone()
+    sm0 = dev["slot_map"].cpu().numpy().copy()
+    pool_pos, hand = sd().pool_state(dev["slot_map"], w.pool_rows)
+    pp0, h0 = pool_pos.cpu().numpy().copy(), hand.cpu().numpy().copy()
+    sd().sd_promote_rows(a, pool_pos, hand)
+    sd().sd_gather_attend(a, ws)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    assert torch.equal(out, o0) and torch.equal(lse, l0)
+    # the device state equals the oracle's promotion of the same selection
+    o_slot, o_pos, o_hand = sm0.copy(), pp0.copy(), h0.copy()
+    P = w.pool_rows
+    dummy = np.zeros((w.B, 1, w.T, 1)), np.zeros((w.B, 1, w.T, 1))
+    oracle.promote_rows(idx.cpu().numpy(), 1, o_slot, o_pos, o_hand, dummy[0], dummy[1],
+                        np.zeros((w.B, 1, P, 1)), np.zeros((w.B, 1, P, 1)))
+    np.testing.assert_array_equal(dev["slot_map"].cpu().numpy(), o_slot)
+    np.testing.assert_array_equal(pool_pos.cpu().numpy(), o_pos)
+    np.testing.assert_array_equal(hand.cpu().numpy(), o_hand)
+    # the promoted rows are the host rows of their positions (a sample of slots)
+    kp = dev["k_pool"].cpu()
+    for b in range(w.B):
+        for s in range(0, P, 997):
+            t = int(o_pos[b, s])
+            if t >= 0:
+                assert torch.equal(kp[b, :, s], x["k"][b, :, t])

@@ -28,6 +28,7 @@ EXPORTS = (
     "sd_score_accumulate", "sd_tier_classify_workspace_bytes", "sd_tier_classify",
     "sd_quantize_rows_int8", "sd_gather_attend_noalloc", "sd_select_attend", "sd_window_count",
     "sd_window_max", "sd_window_union", "sd_index_score_heads", "sd_stage_host_rows", "sd_ring_append",
+    "sd_promote_rows_workspace_bytes", "sd_promote_rows",
 )
 
 
@@ -82,6 +83,9 @@ def lib() -> ctypes.CDLL:
         L.sd_index_score_heads.argtypes = [P, I, P, I, I, I, I, I, I, P, P, P, P]
         L.sd_stage_host_rows.argtypes = [ctypes.POINTER(sd_attend_args), P, P]
         L.sd_ring_append.argtypes = [P, P, I, I, I, I, I, P, P, P, P, I, P]
+        L.sd_promote_rows_workspace_bytes.argtypes = [ctypes.POINTER(sd_attend_args)]
+        L.sd_promote_rows_workspace_bytes.restype = Z
+        L.sd_promote_rows.argtypes = [ctypes.POINTER(sd_attend_args), P, P, P, Z, P]
         L.sd_window_count.argtypes = [I, I, I]
         L.sd_window_count.restype = I
         L.sd_window_max.argtypes = [P, I, I, I, I, P, P, P]
@@ -315,6 +319,30 @@ def sd_stage_host_rows(args: sd_attend_args, counter: torch.Tensor, stream=None)
     (see stage_buffers); counter from stage_counter, left at zero."""
     _dev(counter, "counter")
     _check(lib().sd_stage_host_rows(ctypes.byref(args), _ptr(counter), _stream(stream)), "sd_stage_host_rows")
+
+
+def pool_state(slot_map: torch.Tensor, pool_rows: int) -> tuple:
+    """(pool_pos [B, pool_rows], hand [B]) consistent with slot_map [B, T] (device int32)."""
+    B, T = slot_map.shape
+    pool_pos = torch.full((B, pool_rows), -1, dtype=torch.int32, device=slot_map.device)
+    res = slot_map >= 0
+    b, t = res.nonzero(as_tuple=True)
+    pool_pos[b, slot_map[b, t].long()] = t.to(torch.int32)
+    return pool_pos, torch.zeros(B, dtype=torch.int32, device=slot_map.device)
+
+
+def sd_promote_rows(args: sd_attend_args, pool_pos: torch.Tensor, hand: torch.Tensor,
+                    workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Promotes the selected host rows `args` describes into its pool (see include/sd.h);
+    returns the workspace (zero-filled when created here), to pass to the next call."""
+    _dev(pool_pos, "pool_pos")
+    _dev(hand, "hand")
+    need = lib().sd_promote_rows_workspace_bytes(ctypes.byref(args))
+    if workspace is None:
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=pool_pos.device)
+    _check(lib().sd_promote_rows(ctypes.byref(args), _ptr(pool_pos), _ptr(hand), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)), "sd_promote_rows")
+    return workspace
 
 
 def ring_buffers(B: int, Hkv: int, W: int, d: int, dtype: torch.dtype, device="cuda") -> tuple:
