@@ -494,6 +494,115 @@ class VerifyGroupStep:
                 "hbm": key_bytes + q_idx_bytes + w.B * w.Hkv * w.k * 4 + w.layers * per_layer, "host": 0}
 
 
+class CachedTieredStep:
+    """One decode step of a tiered layer whose pool is kept as a cache: the indexer (this
+    step's window of the sliding verify queries), the top-k, the promotion of the selected
+    host rows into the pool (evicting rows not selected), the staging of the host rows the
+    pool had no room for, and the attention.  Steps cycle over the query windows; the pool
+    carries over from step to step."""
+
+    dominant = "sd_index_score"
+    phases = ("after_topk", "after_promote")
+    launches_per_step = 8  # indexer, top-k, promotion (3), staging, attention, merge
+    dominant_per_step = 1
+
+    def __init__(self, w, x, device):
+        import torch
+        from top_sparse_decode_gqa_gb300 import binding as sd
+        self.sd, self.w, self.dev = sd, w, device
+        seq = x["q_idx_seq"]
+        self.q_idx_win = [seq[:, :, s:s + w.V].contiguous().to(device) for s in range(w.drift_steps)]
+        self.q_idx = self.q_idx_win[0]
+        self.k_idx = x["k_idx"].to(device)
+        self.q = x["q"].to(device)
+        self.k_cache, self.v_cache = x["k_pool"].to(device), x["v_pool"].to(device)  # the pool, written
+        self.slot_map = x["slot_map"].to(device)
+        self.k_host, self.v_host = x["k"].pin_memory(), x["v"].pin_memory()
+        self.static_map = x["slot_map"].to(device)  # the residency as generated (for comparison)
+        self.pool_pos, self.hand = sd.pool_state(self.slot_map, w.pool_rows)
+        self.scores = torch.empty(w.B, w.Hkv, w.T, dtype=torch.float32, device=device)
+        self.idx = torch.empty(w.B, w.Hkv, w.k, dtype=torch.int32, device=device)
+        self.key_hist = sd.key_hist_buffer(w.B * w.Hkv, device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.args, self.out, self.lse, _ = sd.make_attend_args(
+            self.q, self.k_cache, self.v_cache, self.idx, T=w.T, k_host=self.k_host, v_host=self.v_host,
+            slot_map=self.slot_map, err_word=self.err)
+        self.stage = sd.stage_buffers(self.args, self.q.dtype, device)
+        self.counter = sd.stage_counter(device)
+        self.ws_promote = torch.zeros(max(16, sd.sd_promote_rows_workspace_bytes(self.args)), dtype=torch.uint8,
+                                      device=device)
+        need = sd.sd_gather_attend_workspace_bytes(self.args)
+        self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=device)
+        self.step_no = 0
+        self.host_bytes = None
+
+    def run(self, m: "StepMarks" = None):
+        sd, w = self.sd, self.w
+        q_idx = self.q_idx_win[self.step_no % w.drift_steps]
+        self.step_no += 1
+        if m is not None:
+            m.start.record()
+            m.before(0)
+        sd.sd_index_score(q_idx, self.k_idx, self.scores, self.err, key_hist=self.key_hist)
+        if m is not None:
+            m.after(0)
+        sd.sd_topk(self.scores, w.k, self.idx, key_hist=self.key_hist)
+        if m is not None:
+            m.at("after_topk")
+        sd.sd_promote_rows(self.args, self.pool_pos, self.hand, self.ws_promote)
+        if m is not None:
+            m.at("after_promote")
+        sd.sd_stage_host_rows(self.args, self.counter)
+        sd.sd_gather_attend(self.args, self.ws)
+        if m is not None:
+            m.end.record()
+
+    def host_misses(self, slot_map):
+        """(distinct host positions, host rows over the KV heads) of the current selection."""
+        import torch
+        B, T = self.w.B, self.w.T
+        sel = self.idx.view(B, -1).long()
+        b = torch.arange(B, device=sel.device)[:, None].expand_as(sel)
+        miss = slot_map[b, sel] < 0
+        return int(torch.unique((b * T + sel)[miss]).numel()), int(miss.sum().item())
+
+    def after_warmup(self):
+        """Host bytes per step in the steady state, averaged over one cycle of the query
+        windows: the promoted positions (K and V of every KV head) plus the selected rows
+        left in host memory (staged); and, for comparison, the host rows the same
+        selections would read with the pool kept as it was generated."""
+        import torch
+        w, row = self.w, self.w.d * self.w.elem_bytes * 2
+        with_cache = without = 0
+        for _ in range(w.drift_steps):
+            q_idx = self.q_idx_win[self.step_no % w.drift_steps]
+            self.step_no += 1
+            self.sd.sd_index_score(q_idx, self.k_idx, self.scores, self.err, key_hist=self.key_hist)
+            self.sd.sd_topk(self.scores, w.k, self.idx, key_hist=self.key_hist)
+            without += self.host_misses(self.static_map)[1] * row
+            before, _ = self.host_misses(self.slot_map)
+            self.sd.sd_promote_rows(self.args, self.pool_pos, self.hand, self.ws_promote)
+            left_pos, left_rows = self.host_misses(self.slot_map)
+            with_cache += (before - left_pos) * w.Hkv * row + left_rows * row
+            self.sd.sd_stage_host_rows(self.args, self.counter)
+            self.sd.sd_gather_attend(self.args, self.ws)
+        torch.cuda.synchronize()
+        self.host_bytes = with_cache // w.drift_steps
+        self.host_bytes_static = without // w.drift_steps
+
+    def bytes(self):
+        w = self.w
+        e = w.elem_bytes
+        key_bytes = w.B * w.Hkv * w.T * w.dI * e
+        q_idx_bytes = w.B * w.Hkv * w.V * w.dI * e
+        score_bytes = w.B * w.Hkv * w.T * 4
+        q_bytes = w.B * w.V * w.Hq * w.d * e
+        out_bytes = w.B * w.V * w.Hq * (w.d + 1) * 4 + w.B * w.Hkv * w.k * 4
+        rows = w.B * w.Hkv * w.k * w.d * e * 2
+        return {"dominant": key_bytes + q_idx_bytes + score_bytes,
+                "hbm": key_bytes + q_idx_bytes + rows + q_bytes + out_bytes, "host": self.host_bytes or 0}
+
+
 class LookaheadStep:
     """One decode step over L tiered layers, each with its own selection: per layer the
     indexer, the top-k, the copy of the selected host-resident rows into an HBM stage, and
@@ -685,6 +794,8 @@ class DenseScoringStep:
 
 
 def make_step(w, x, device, separate=False, tiered_path="staged", lookahead=True):
+    if w.drift_steps > 0:
+        return CachedTieredStep(w, x, device)
     if w.layer_indexers:
         return LookaheadStep(w, x, device, lookahead)
     if w.ring_w > 0:
@@ -698,20 +809,24 @@ def make_step(w, x, device, separate=False, tiered_path="staged", lookahead=True
     return SparseDecodeStep(w, x, device, separate, tiered_path)
 
 
-def host_link_gbs(device, nbytes=512 << 20):
-    """Host->device bandwidth of one pinned copy (CUDA events), the host-row roofline term."""
+def host_link_gbs(device, nbytes=256 << 20, reps=5):
+    """Host->device bandwidth of a pinned copy (CUDA events): the best of `reps` copies after
+    two untimed ones, the host-row roofline term."""
     import torch
-    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h = torch.ones(nbytes, dtype=torch.uint8).pin_memory()
     d = torch.empty(nbytes, dtype=torch.uint8, device=device)
     for _ in range(2):
         d.copy_(h, non_blocking=True)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(3):
-        d.copy_(h, non_blocking=True)
-    b.record()
     torch.cuda.synchronize()
-    return 3 * nbytes / (a.elapsed_time(b) / 1e3) / 1e9
+    best = 0.0
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        d.copy_(h, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (a.elapsed_time(b) / 1e3) / 1e9)
+    return best
 
 
 # ----------------------------------------------------------------------------- arms
@@ -792,7 +907,7 @@ def run_ours(args):
     by = step.bytes()
     dom_s = statistics.mean(dom_ms) / 1e3
     achieved = by["dominant"] / dom_s / 1e9
-    if isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep, LookaheadStep)):
+    if isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep, LookaheadStep, CachedTieredStep)):
         kernel_file, kernel_tag = ("index_score.cu", "index_score_tc.cu", "tc_common.cuh", "sd_common.cuh"), "index_score"
     else:
         kernel_file, kernel_tag = ("gather_attend.cu", "sd_common.cuh"), "gather_attend"
@@ -831,6 +946,14 @@ def run_ours(args):
             "topk": k_us(lambda m: m.dom[0][1], lambda m: m.phase["after_topk"]),
             "stage_host_rows": k_us(lambda m: m.phase["after_topk"], lambda m: m.phase["after_stage"]),
             "gather_attend": k_us(lambda m: m.phase["after_stage"], lambda m: m.end)}
+    elif isinstance(step, CachedTieredStep):
+        k_us = lambda a, b: round(statistics.mean(a(m).elapsed_time(b(m)) for m in kmarks) * 1e3, 2)  # noqa: E731
+        step_roof["kernel_us"] = {
+            "index_score": round(statistics.mean(dom_ms) * 1e3, 2),
+            "topk": k_us(lambda m: m.dom[0][1], lambda m: m.phase["after_topk"]),
+            "promote": k_us(lambda m: m.phase["after_topk"], lambda m: m.phase["after_promote"]),
+            "stage_host_rows+gather_attend": k_us(lambda m: m.phase["after_promote"], lambda m: m.end)}
+        step_roof["host_bytes_per_step_without_cache"] = step.host_bytes_static
     elif isinstance(step, LookaheadStep):
         step_roof["kernel_us"] = {"index_score": round(statistics.mean(dom_ms) * 1e3, 2), "layers": w.layers}
         if step.lookahead:  # the same steps with every call in order on one stream, for comparison
@@ -887,6 +1010,9 @@ def run_ours(args):
                             else f"indexer + top-k once, then per layer ({w.layers}) ring append + gather-attend "
                                  "over the selected rows and the draft ring"
                             if isinstance(step, VerifyGroupStep)
+                            else "indexer + top-k + promotion into the pool (cache) + staging of the rest + "
+                                 "gather-attend, the query window sliding step by step"
+                            if isinstance(step, CachedTieredStep)
                             else f"per layer ({w.layers}): indexer + top-k + host-row staging + gather-attend, "
                                  + ("selection and staging on their own streams ahead of the attention"
                                     if step.lookahead else "in order on one stream")
@@ -923,10 +1049,13 @@ def measure_e2e(step, w, x, clean_l2, K):
     ins = [(step.q, x["q"][0] if multi else x["q"][0, 0] if w.layers > 1 else x["q"])]
     if isinstance(step, (SparseDecodeStep, WindowStep, VerifyGroupStep, LookaheadStep)):
         ins.append((step.q_idx, x["q_idx"]))
+    if isinstance(step, CachedTieredStep):  # every window of indexer queries comes from the host
+        ins += [(dst, x["q_idx_seq"][:, :, s:s + w.V]) for s, dst in enumerate(step.q_idx_win)]
     if verify:  # the drafts' K/V come from the host with the queries
         ins += [(step.draft_k, x["draft_k"]), (step.draft_v, x["draft_v"])]
     ins = [(dst, src.contiguous().pin_memory()) for dst, src in ins]
-    sparse = isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep, LookaheadStep))
+    sparse = isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep, LookaheadStep,
+                               CachedTieredStep))
     outs = [step.out, step.lse] + ([step.idx[-1] if isinstance(step.idx, list) else step.idx] if sparse else [step.s])
     outs = [(src, torch.empty(src.shape, dtype=src.dtype).pin_memory()) for src in outs]
     times = []
@@ -1000,6 +1129,8 @@ def oracle_step(w, x, b0, b1):
         return oracle.gather_attend(q, x["k"][b0:b1].contiguous(), x["v"][b0:b1].contiguous(), idx, nb, w.V,
                                     w.Hq, w.Hkv, w.d, w.T, w.k, 1, scale, per_head=True)
     q_idx = x["q_idx"][b0:b1].contiguous()
+    if w.drift_steps > 0:  # the first query window
+        q_idx = x["q_idx_seq"][b0:b1, :, :w.V].contiguous()
     keys = x["k_idx"][b0:b1].contiguous()
     if w.block > 1:
         keys = oracle.block_pool(keys, nb, w.Hkv, w.T, w.dI, w.block).astype("float32")

@@ -157,3 +157,45 @@ def test_c4_promotion_full():
             t = int(o_pos[b, s])
             if t >= 0:
                 assert torch.equal(kp[b, :, s], x["k"][b, :, t])
+
+
+def test_c10_cached_tiered_steps():
+    # the benchmark's cached workload over a whole cycle of query windows: every step's
+    # attention equals (bit for bit) the same selection read with the pool as generated, and
+    # the oracle on a sampled group; the cache ends up serving most of the selected rows
+    import math
+    import bench
+    from gpu_util import assert_attend_close
+    from top_sparse_decode_gqa_gb300.workloads import WORKLOADS, generate
+    w = WORKLOADS["c10_cached_tiered"]
+    x = generate(w)
+    step = bench.make_step(w, x, torch.device("cuda"))
+    static_pool = (x["k_pool"].cuda(), x["v_pool"].cuda(), x["slot_map"].cuda())
+    e = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a0, out0, lse0, _ = sd().make_attend_args(step.q, static_pool[0], static_pool[1], step.idx, T=w.T,
+                                              k_host=step.k_host, v_host=step.v_host, slot_map=static_pool[2],
+                                              err_word=e)
+    ws0 = torch.zeros(max(16, sd().sd_gather_attend_workspace_bytes(a0)), dtype=torch.uint8, device="cuda")
+    host_rows = []
+    for s in range(w.drift_steps):
+        step.run()
+        sd().sd_gather_attend(a0, ws0)
+        torch.cuda.synchronize()
+        assert int(step.err.item()) == 0 and int(e.item()) == 0
+        assert torch.equal(step.out, out0) and torch.equal(step.lse, lse0)
+        host_rows.append(step.host_misses(step.slot_map)[1])
+        if s in (0, w.drift_steps - 1):
+            b, h = s % w.B, 3
+            qw = x["q_idx_seq"][b:b + 1, h:h + 1, s:s + w.V]
+            rs = oracle.index_score(qw, x["k_idx"][b:b + 1, h:h + 1], 1, 1, w.V, w.T, w.dI)
+            ri = oracle.topk(rs, w.k)
+            np.testing.assert_array_equal(step.idx[b:b + 1, h:h + 1].cpu().numpy(), ri)
+            qh = x["q"][b:b + 1, :, h * w.G:(h + 1) * w.G].contiguous()
+            ro, rl, _ = oracle.gather_attend(qh, x["k"][b:b + 1, h:h + 1].contiguous(),
+                                             x["v"][b:b + 1, h:h + 1].contiguous(), ri, 1, w.V, w.G, 1, w.d, w.T,
+                                             w.k, 1, 1 / math.sqrt(w.d))
+            assert_attend_close(step.out[b:b + 1, :, h * w.G:(h + 1) * w.G], ro)
+            assert_attend_close(step.lse[b:b + 1, :, h * w.G:(h + 1) * w.G], rl, "lse")
+    # after the first steps most selected rows are in the pool
+    total_rows = w.B * w.Hkv * w.k
+    assert host_rows[-1] < 0.5 * total_rows

@@ -331,6 +331,10 @@ def pool_state(slot_map: torch.Tensor, pool_rows: int) -> tuple:
     return pool_pos, torch.zeros(B, dtype=torch.int32, device=slot_map.device)
 
 
+def sd_promote_rows_workspace_bytes(args: sd_attend_args) -> int:
+    return lib().sd_promote_rows_workspace_bytes(ctypes.byref(args))
+
+
 def sd_promote_rows(args: sd_attend_args, pool_pos: torch.Tensor, hand: torch.Tensor,
                     workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Promotes the selected host rows `args` describes into its pool (see include/sd.h);

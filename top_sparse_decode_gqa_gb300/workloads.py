@@ -41,6 +41,10 @@ available here):
   with its own indexer query and keys (a selection per layer), its own K/V cache in pinned
   host memory and its own HBM pool of the same resident 10 % of positions; the step runs
   layer l+1's indexer, top-k and host-row staging ahead, beside layer l's attention.
+* ``c10_cached_tiered``: the tiered verify layer of ``c4`` with a 25 % pool, over 16
+  decode steps whose 8 verify queries slide along a sequence of 23 indexer queries (each
+  step drops the oldest and adds one), so consecutive selections overlap; the pool is kept
+  as a cache: each step promotes its selected host rows into it before the attention.
 
 Value recipe: indexer query and keys are integers drawn uniformly from [-8, 8] (exact in
 bf16 and fp32); attention q, K, V are standard normal, rounded to bf16 (nearest even)
@@ -84,6 +88,7 @@ class Workload:
     ring_w: int = 0         # > 0: draft-token ring of this many slots per layer (verify loop)
     q_idx_dtype: str = ""   # storage type of the indexer query if not `dtype` ("f16": with fp16 pooled keys)
     layer_indexers: bool = False  # one indexer query and key set per layer (selection per layer)
+    drift_steps: int = 0    # > 0: decode steps whose V verify queries slide along a query sequence
     cum_frac: tuple = (0.2, 0.6, 0.9)
     n_sink: int = 0
     n_recent: int = 0
@@ -155,6 +160,8 @@ WORKLOADS: Dict[str, Workload] = {
                  dI=128, k=1024, layers=4, ring_w=64),
         Workload("c9_lookahead_tiered", 8, B=2, V=8, Hq=32, Hkv=8, d=128, T=131072, dtype="bf16",
                  dI=128, k=2048, resident_frac=0.1, layers=4, layer_indexers=True),
+        Workload("c10_cached_tiered", 9, B=4, V=8, Hq=32, Hkv=8, d=128, T=131072, dtype="bf16",
+                 dI=128, k=2048, resident_frac=0.25, drift_steps=16),
     )
 }
 
@@ -253,7 +260,11 @@ def generate(w: Workload, seed: Optional[int] = None) -> Dict[str, torch.Tensor]
         else:
             out["k_pool"] = torch.gather(out["k"], 2, idx).contiguous()
             out["v_pool"] = torch.gather(out["v"], 2, idx).contiguous()
-    # 8. draft ring: its K/V, then the drafts' K/V
+    # 8. sliding indexer queries: a sequence of V + drift_steps - 1 queries per (b, kvh);
+    # step s uses queries s .. s + V - 1
+    if w.drift_steps > 0:
+        out["q_idx_seq"] = _randint(g, (B, Hkv, V + w.drift_steps - 1, w.dI), w.q_idx_dtype or w.dtype)
+    # 9. draft ring: its K/V, then the drafts' K/V
     if w.ring_w > 0:
         W, L = w.ring_w, max(1, w.layers)
         out["ring_k"] = _randn(g, (L, B, Hkv, W, w.d), w.dtype)
