@@ -57,3 +57,29 @@ def test_residency_pool_holds_copies_of_resident_rows():
         assert torch.equal(x["v_pool"][b, :, sm[pos].long()], x["v"][b, :, pos])
     res, sm = residency_map(3, 50, 0, seed=1)
     assert res.shape == (3, 0) and torch.all(sm == -1)
+
+
+def test_later_workloads_match_their_descriptions():
+    c3, c6, c7, c8, c9, c10 = (WORKLOADS[n] for n in ("c3_block_sparse", "c6_window_blocks", "c7_head_topk",
+                                                      "c8_verify_layer_group", "c9_lookahead_tiered",
+                                                      "c10_cached_tiered"))
+    assert c3.q_idx_dtype == "f16"
+    assert (c6.window_kernel, c6.window_stride, c6.k, c6.n_rows) == (32, 16, 64, 2048)
+    assert (c7.per_head, c7.k, c7.Hq, c7.Hkv, c7.T) == (True, 1024, 32, 8, 32768)
+    assert (c8.layers, c8.ring_w, c8.V, c8.k, c8.B) == (4, 64, 8, 1024, 2)
+    assert (c9.layers, c9.layer_indexers, c9.resident_frac, c9.B, c9.T) == (4, True, 0.1, 2, 131072)
+    assert (c10.drift_steps, c10.resident_frac, c10.pool_rows) == (16, 0.25, 32768)
+
+
+def test_sliding_query_windows_and_rings_are_drawn():
+    w = WORKLOADS["c10_cached_tiered"].scaled(B=1, T=2048, k=64)
+    x = generate(w)
+    assert x["q_idx_seq"].shape == (1, w.Hkv, w.V + w.drift_steps - 1, w.dI)
+    w8 = WORKLOADS["c8_verify_layer_group"].scaled(T=1024, k=32)
+    x8 = generate(w8)
+    W, T, V = w8.ring_w, w8.T, w8.V
+    held = x8["ring_pos"][0]
+    # the ring holds the W - V tokens before T at slot position mod W; the drafts' slots are empty
+    assert sorted(int(t) for t in held if t >= 0) == list(range(T - (W - V), T))
+    assert all(int(held[t % W]) == t for t in range(T - (W - V), T))
+    assert x8["qpos"].tolist() == [[T + v for v in range(V)]] * w8.B
