@@ -162,3 +162,29 @@ def test_ring_validation(lib):
     a.ring_k = a.ring_v = a.ring_pos = a.qpos = 16
     # the fused select/attend has no ring
     assert lib.sd_select_attend(dummy, 4096, None, dummy, ctypes.byref(a), None) == 2
+
+
+def test_promote_validation(lib):
+    from top_sparse_decode_gqa_gb300.binding import sd_attend_args
+    dummy = ctypes.c_void_p(16)
+    a = sd_attend_args()
+    a.q = a.k_cache = a.v_cache = a.out = a.lse = 16
+    a.dtype, a.B, a.V, a.Hq, a.Hkv, a.d, a.T = 1, 2, 8, 32, 8, 128, 4096
+    a.pool_rows, a.n_idx, a.block, a.scale = 409, 64, 1, 0.1
+    # needs a selection and a slot map
+    a.idx = 16
+    assert lib.sd_promote_rows(ctypes.byref(a), dummy, dummy, dummy, 1 << 20, None) == 1
+    assert b"idx and slot_map" in lib.sd_last_error_message()
+    a.slot_map = 16
+    # needs the host cache and the caller's pool state
+    assert lib.sd_promote_rows(ctypes.byref(a), dummy, dummy, dummy, 1 << 20, None) == 1
+    assert b"k_host" in lib.sd_last_error_message()
+    a.k_host = a.v_host = 16
+    assert lib.sd_promote_rows(ctypes.byref(a), None, dummy, dummy, 1 << 20, None) == 1
+    # and a workspace of the queried size
+    need = lib.sd_promote_rows_workspace_bytes(ctypes.byref(a))
+    assert need > 4096 * 2 // 8  # at least the bitmap of 2 x 4096 positions
+    assert lib.sd_promote_rows(ctypes.byref(a), dummy, dummy, dummy, need - 16, None) == 1
+    assert b"workspace" in lib.sd_last_error_message()
+    a.pool_rows = 0
+    assert lib.sd_promote_rows_workspace_bytes(ctypes.byref(a)) == 0
