@@ -117,7 +117,7 @@ SD_DEVINL float merge_block_sum(float v, float* red) {
 // (warp w takes splits w, w + 4, ...; the warps' sums are added in warp order), so the
 // result is the same on every run.  lse = (M + log2 L) ln 2.
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) attend_merge_kernel(const AttendParams p, int RP) {
+__global__ void __launch_bounds__(kMergeThreads, 8) attend_merge_kernel(const AttendParams p, int RP) {
     __shared__ float red[kMergeWarps];
     __shared__ __align__(16) float part[kMergeWarps][D];
     pdl_wait();  // every split's partial is written
@@ -128,20 +128,26 @@ __global__ void __launch_bounds__(kMergeThreads) attend_merge_kernel(const Atten
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int S = p.splits;
     const size_t base = (size_t)bk * S * RP + r;  // partial row of split s: base + s * RP
-    float m = -INFINITY;
-    for (int s = tid; s < S; s += kMergeThreads) m = fmaxf(m, __ldcg(p.ws_m + base + (size_t)s * RP));
-    const float M = merge_block_max(m, red);
-    float l = 0.f;
-    if (M != -INFINITY)
-        for (int s = tid; s < S; s += kMergeThreads) {
-            const float ms = __ldcg(p.ws_m + base + (size_t)s * RP);
-            if (ms != -INFINITY) l = fmaf(__ldcg(p.ws_l + base + (size_t)s * RP), exp2f(ms - M), l);
+    // (m, l) of every split in one pass: this thread's running maximum and sum, then the
+    // block's maximum and the sums rescaled to it
+    float m = -INFINITY, l = 0.f;
+    for (int s = tid; s < S; s += kMergeThreads) {
+        const float ms = __ldcg(p.ws_m + base + (size_t)s * RP);
+        const float ls = __ldcg(p.ws_l + base + (size_t)s * RP);
+        if (ms == -INFINITY) continue;
+        if (ms > m) {
+            l = (m == -INFINITY) ? ls : fmaf(l, exp2f(m - ms), ls);
+            m = ms;
+        } else {
+            l = fmaf(ls, exp2f(ms - m), l);
         }
-    const float L = merge_block_sum(l, red);
+    }
+    const float M = merge_block_max(m, red);
+    const float L = merge_block_sum(m == -INFINITY ? 0.f : l * exp2f(m - M), red);
     float o[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) o[c] = 0.f;
-    constexpr int U = 4;  // splits a warp loads before using any
+    constexpr int U = 8;  // splits a warp requests before using any (8 CTAs per SM fit: one wave)
     for (int s0 = warp; s0 < S; s0 += U * kMergeWarps) {
         float ms[U], x[U][CPL];
 #pragma unroll
