@@ -465,7 +465,8 @@ struct MmaLayout {
 
 // Grid (split, kvh, b), 4 warps.  The split's rows are resolved to their sources up front,
 // then attend_mma.cuh's per-warp loop runs over them; the 4 warps' (m, l, O) are combined
-// into the CTA's split partial, and the last CTA of each (b, kvh) merges the splits.
+// into the CTA's split partial (or, with one split, into out and lse); attend_merge_kernel
+// then merges the splits.  RING: the list ends with draft-ring slots, masked per query row.
 template <int D, int RP, bool RING>
 __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendParams p) {
     using L = MmaLayout<D, RP>;
