@@ -516,9 +516,12 @@ class CachedTieredStep:
         self.k_idx = x["k_idx"].to(device)
         self.q = x["q"].to(device)
         self.k_cache, self.v_cache = x["k_pool"].to(device), x["v_pool"].to(device)  # the pool, written
-        self.slot_map = x["slot_map"].to(device)
+        sm = x["slot_map"]
+        if w.slot_per_head:  # every KV head starts from the generated residency
+            sm = sm[:, None, :].expand(w.B, w.Hkv, w.T).contiguous()
+        self.slot_map = sm.to(device)
         self.k_host, self.v_host = x["k"].pin_memory(), x["v"].pin_memory()
-        self.static_map = x["slot_map"].to(device)  # the residency as generated (for comparison)
+        self.static_map = sm.to(device)  # the residency as generated (for comparison)
         self.pool_pos, self.hand = sd.pool_state(self.slot_map, w.pool_rows)
         self.scores = torch.empty(w.B, w.Hkv, w.T, dtype=torch.float32, device=device)
         self.idx = torch.empty(w.B, w.Hkv, w.k, dtype=torch.int32, device=device)
@@ -558,9 +561,15 @@ class CachedTieredStep:
             m.end.record()
 
     def host_misses(self, slot_map):
-        """(distinct host positions, host rows over the KV heads) of the current selection."""
+        """(distinct host units, host rows over the KV heads) of the current selection: a
+        unit is a (sequence, position), or a (sequence, KV head, position) with residency
+        per KV head."""
         import torch
         B, T = self.w.B, self.w.T
+        if slot_map.dim() == 3:
+            miss = slot_map.gather(2, self.idx.long()) < 0
+            n = int(miss.sum().item())
+            return n, n
         sel = self.idx.view(B, -1).long()
         b = torch.arange(B, device=sel.device)[:, None].expand_as(sel)
         miss = slot_map[b, sel] < 0
@@ -583,7 +592,8 @@ class CachedTieredStep:
             before, _ = self.host_misses(self.slot_map)
             self.sd.sd_promote_rows(self.args, self.pool_pos, self.hand, self.ws_promote)
             left_pos, left_rows = self.host_misses(self.slot_map)
-            with_cache += (before - left_pos) * w.Hkv * row + left_rows * row
+            heads = 1 if w.slot_per_head else w.Hkv  # rows a promoted unit brings
+            with_cache += (before - left_pos) * heads * row + left_rows * row
             self.sd.sd_stage_host_rows(self.args, self.counter)
             self.sd.sd_gather_attend(self.args, self.ws)
         torch.cuda.synchronize()

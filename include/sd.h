@@ -184,6 +184,9 @@ sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx, uin
  * head's ring, and query token v of sequence b attends slot s only when
  * 0 <= ring_pos[b,s] <= qpos[b,v] (z = -inf otherwise); logits then have n_idx*block +
  * ring_w columns.  sd_ring_append fills the ring.
+ * Residency per KV head: with slot_per_head = 1, slot_map is [B,Hkv,T] and the row of KV
+ * head kvh at position t is in pool slot slot_map[b,kvh,t] (or host memory at -1), so the
+ * KV heads of a sequence may keep different positions in the pool.
  * Staged host rows: with slot_map and k_stage/v_stage set, a row whose slot is -1 is read
  * from the stage at [group, j] (j = its position in the group's selection list, group =
  * b*Hkv + kvh, or b*Hq + h with per_head) instead of host memory; the stage must hold what
@@ -221,6 +224,7 @@ typedef struct {
     const int32_t* ring_pos;  /* [B,ring_w] token position held by each slot, -1 = empty */
     const int32_t* qpos;      /* [B,V] token position of each query token */
     int ring_w;               /* ring slots; 0 = no ring */
+    int slot_per_head;        /* 1: slot_map is [B,Hkv,T], one residency map per KV head */
 } sd_attend_args;
 
 size_t sd_gather_attend_workspace_bytes(const sd_attend_args* args);
@@ -278,7 +282,10 @@ sd_status sd_stage_host_rows(const sd_attend_args* args, uint32_t* counter, void
  * k_host/v_host into the pool (args->k_cache/v_cache, which this call writes), slot_map[b,
  * miss] = slot, pool_pos[b, slot] = miss, and hand[b] moves past the last slot taken.
  * Misses beyond the free slots stay in host memory.  A following sd_gather_attend reads the
- * promoted rows from HBM, with the same bits (the values are the same).
+ * promoted rows from HBM, with the same bits (the values are the same).  With
+ * slot_per_head = 1 every (b, KV head) is such a unit of its own (its selection, its slot
+ * map row, its pool slots; one row per miss): pool_pos is then [B*Hkv, pool_rows] and hand
+ * [B*Hkv].
  * pool_pos [B, pool_rows] int32 (slot -> position, -1 empty) and hand [B] int32 are the
  * caller's device state, kept consistent with slot_map between calls.  The workspace
  * (sd_promote_rows_workspace_bytes) must be zero-filled before the first call; every call

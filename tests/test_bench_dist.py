@@ -33,17 +33,30 @@ def _worker(rank, world, port, out):
     out.put((r, w, local, t, v))
 
 
-def test_two_gloo_ranks_take_the_max_time_and_sum_the_work():
+def _run_two_ranks():
     ctx = mp.get_context("spawn")
     out = ctx.Queue()
     port = _free_port()
     procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
     for p in procs:
         p.start()
-    res = sorted(out.get(timeout=120) for _ in procs)
+    try:
+        res = sorted(out.get(timeout=120) for _ in procs)
+    except Exception:
+        res = None
     for p in procs:
         p.join(timeout=60)
-        assert p.exitcode == 0
+        if p.exitcode is None:
+            p.kill()
+    ok = res is not None and all(p.exitcode == 0 for p in procs)
+    return res if ok else None
+
+
+def test_two_gloo_ranks_take_the_max_time_and_sum_the_work():
+    # the free port can be taken by another process between the probe and the rendezvous:
+    # a second attempt gets a new one
+    res = _run_two_ranks() or _run_two_ranks()
+    assert res is not None, "two gloo ranks did not complete"
     for rank, (r, w, local, t, v) in enumerate(res):
         assert (r, w, local) == (rank, 2, rank)
         assert t == 1.5                    # max over ranks

@@ -199,3 +199,62 @@ def test_c10_cached_tiered_steps():
     # after the first steps most selected rows are in the pool
     total_rows = w.B * w.Hkv * w.k
     assert host_rows[-1] < 0.5 * total_rows
+
+
+def test_residency_per_kv_head():
+    # per-head slot maps: the same residency copied to every head gives the same bits as the
+    # shared map; promoting per head moves one row per miss and matches the oracle run on
+    # the (b, KV head) units; the attention bits do not change
+    from top_sparse_decode_gqa_gb300.workloads import residency_map
+    g = torch.Generator().manual_seed(11)
+    B, Hq, Hkv, d, T, n, V, P = 2, 16, 4, 128, 4096, 300, 2, 512
+    q = torch.randn(B, V, Hq, d, generator=g).to(torch.bfloat16).cuda()
+    K = torch.randn(B, Hkv, T, d, generator=g).to(torch.bfloat16)
+    Vv = torch.randn(B, Hkv, T, d, generator=g).to(torch.bfloat16)
+    idx = torch.stack([torch.stack([torch.sort(torch.randperm(T, generator=g)[:n]).values for _ in range(Hkv)])
+                       for _ in range(B)]).int().cuda()
+    res, slot_map = residency_map(B, T, P, 3)
+    gi = res[:, None, :, None].expand(B, Hkv, P, d)
+    k_pool = torch.gather(K, 2, gi).contiguous().cuda()
+    v_pool = torch.gather(Vv, 2, gi).contiguous().cuda()
+    k_host, v_host = K.pin_memory(), Vv.pin_memory()
+    o_shared, l_shared, _ = sd().gather_attend(q, k_pool, v_pool, idx, T=T, k_host=k_host, v_host=v_host,
+                                               slot_map=slot_map.cuda())
+    per_head = slot_map[:, None, :].expand(B, Hkv, T).contiguous().cuda()
+    e = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a, out, lse, _ = sd().make_attend_args(q, k_pool, v_pool, idx, T=T, k_host=k_host, v_host=v_host,
+                                           slot_map=per_head, err_word=e)
+    assert a.slot_per_head == 1
+    ws = torch.zeros(max(16, sd().sd_gather_attend_workspace_bytes(a)), dtype=torch.uint8, device="cuda")
+    sd().sd_gather_attend(a, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, o_shared) and torch.equal(lse, l_shared)
+    # promotion per (b, KV head)
+    pool_pos, hand = sd().pool_state(per_head, P)
+    assert pool_pos.shape == (B * Hkv, P)
+    o_slot = per_head.cpu().numpy().reshape(B * Hkv, T).copy()
+    o_pos, o_hand = pool_pos.cpu().numpy().copy(), hand.cpu().numpy().copy()
+    sd().sd_promote_rows(a, pool_pos, hand)
+    sd().sd_gather_attend(a, ws)
+    # the staged path over per-head maps as well
+    stage = sd().stage_buffers(a, torch.bfloat16)
+    sd().sd_stage_host_rows(a, sd().stage_counter())
+    sd().sd_gather_attend(a, ws)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    assert torch.equal(out, o_shared) and torch.equal(lse, l_shared)
+    kh = K.float().numpy().reshape(B * Hkv, 1, T, d)
+    vh = Vv.float().numpy().reshape(B * Hkv, 1, T, d)
+    kp = np.zeros((B * Hkv, 1, P, d), dtype=np.float32)
+    vp = np.zeros_like(kp)
+    for u in range(B * Hkv):  # the oracle's pool starts with the generated rows
+        for s_, t in enumerate(o_pos[u]):
+            if t >= 0:
+                kp[u, 0, s_], vp[u, 0, s_] = kh[u, 0, t], vh[u, 0, t]
+    oracle.promote_rows(idx.cpu().numpy().reshape(B * Hkv, 1, n), 1, o_slot, o_pos, o_hand, kh, vh, kp, vp)
+    np.testing.assert_array_equal(per_head.cpu().numpy().reshape(B * Hkv, T), o_slot)
+    np.testing.assert_array_equal(pool_pos.cpu().numpy(), o_pos)
+    np.testing.assert_array_equal(hand.cpu().numpy(), o_hand)
+    got = k_pool.float().cpu().numpy().reshape(B * Hkv, 1, P, d)
+    np.testing.assert_array_equal(got, kp)
+    del stage

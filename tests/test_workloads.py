@@ -68,7 +68,7 @@ def test_later_workloads_match_their_descriptions():
     assert (c7.per_head, c7.k, c7.Hq, c7.Hkv, c7.T) == (True, 1024, 32, 8, 32768)
     assert (c8.layers, c8.ring_w, c8.V, c8.k, c8.B) == (4, 64, 8, 1024, 2)
     assert (c9.layers, c9.layer_indexers, c9.resident_frac, c9.B, c9.T) == (4, True, 0.1, 2, 131072)
-    assert (c10.drift_steps, c10.resident_frac, c10.pool_rows) == (16, 0.25, 32768)
+    assert (c10.drift_steps, c10.resident_frac, c10.pool_rows, c10.slot_per_head) == (16, 0.1, 13107, True)
 
 
 def test_sliding_query_windows_and_rings_are_drawn():

@@ -51,7 +51,7 @@ class sd_attend_args(ctypes.Structure):
         ("workspace_bytes", ctypes.c_size_t), ("splits", ctypes.c_int), ("per_head", ctypes.c_int),
         ("k_stage", ctypes.c_void_p), ("v_stage", ctypes.c_void_p),
         ("ring_k", ctypes.c_void_p), ("ring_v", ctypes.c_void_p), ("ring_pos", ctypes.c_void_p),
-        ("qpos", ctypes.c_void_p), ("ring_w", ctypes.c_int),
+        ("qpos", ctypes.c_void_p), ("ring_w", ctypes.c_int), ("slot_per_head", ctypes.c_int),
     ]
 
 
@@ -224,7 +224,8 @@ def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=No
                      k_host=None, v_host=None, slot_map=None, out=None, lse=None, logits=None,
                      want_logits=False, err_word=None, splits=0, per_head=False, k_stage=None,
                      v_stage=None, ring_k=None, ring_v=None, ring_pos=None, qpos=None) -> tuple:
-    """Fill an sd_attend_args from tensors; returns (args, out, lse, logits)."""
+    """Fill an sd_attend_args from tensors; returns (args, out, lse, logits).  slot_map is
+    [B,T] (residency per sequence) or [B,Hkv,T] (per KV head)."""
     _dev(q, "q")
     B, V, Hq, d = q.shape
     Hkv = k_cache.shape[1]
@@ -270,6 +271,7 @@ def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=No
             _dev(t, name)
             setattr(a, name, t.data_ptr())
     a.ring_w = ring_w
+    a.slot_per_head = 1 if slot_map is not None and slot_map.dim() == 3 else 0
     return a, out, lse, logits
 
 
@@ -322,7 +324,9 @@ def sd_stage_host_rows(args: sd_attend_args, counter: torch.Tensor, stream=None)
 
 
 def pool_state(slot_map: torch.Tensor, pool_rows: int) -> tuple:
-    """(pool_pos [B, pool_rows], hand [B]) consistent with slot_map [B, T] (device int32)."""
+    """(pool_pos [U, pool_rows], hand [U]) consistent with slot_map [B, T] (U = B) or
+    [B, Hkv, T] (U = B*Hkv), device int32."""
+    slot_map = slot_map.reshape(-1, slot_map.shape[-1])
     B, T = slot_map.shape
     pool_pos = torch.full((B, pool_rows), -1, dtype=torch.int32, device=slot_map.device)
     res = slot_map >= 0

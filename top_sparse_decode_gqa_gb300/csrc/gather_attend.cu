@@ -44,6 +44,7 @@ struct AttendParams {
     int dtype;
     int resolve;  // 1: sources resolved up front (idx or slot_map given)
     int staged;   // 1: kh/vh are the HBM stage [groups, n_hist, d], host rows by list position
+    int slot_per_head;  // 1: slot_map is [B, kv_heads, T] (residency per (b, KV head))
     int n_hist;   // selected (history) list rows; list rows [n_hist, n_rows) are the draft ring's slots
     int ring_w;   // draft ring slots (0: none)
     const uint8_t* rk;        // draft ring [B, kv_heads, ring_w, d]
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
             }
         }
         if (p.slot_map == nullptr) return (int32_t)pos;
-        const int slot = p.slot_map[(size_t)b * p.T + pos];
+        const int slot = p.slot_map[(size_t)(p.slot_per_head ? kvsrc : b) * p.T + pos];
         if (slot >= 0 && slot < p.pool_rows) return slot;
         if (slot == -1) return (int32_t)(-1 - (p.staged ? (long)jg : pos));
         report(p.err, SD_DEVERR_SLOT);
@@ -500,6 +501,8 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     const int j0 = split * p.rows_per_split;
     const int j1 = min(p.n_rows, j0 + p.rows_per_split);
     const int nrows = max(0, j1 - j0);
+    const int kvsrc = b * p.kv_heads + kvh / p.heads_per_kv;  // the (b, KV head) slab the rows come from
+    const int32_t* srow_map = p.slot_map != nullptr ? p.slot_map + (size_t)(p.slot_per_head ? kvsrc : b) * p.T : nullptr;
     if (p.resolve) {
         for (int j = tid; j < nrows; j += kAttThreads) {
             const int jg = j0 + j;
@@ -526,7 +529,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
             } else if (p.slot_map == nullptr) {
                 code = (int32_t)pos;
             } else {
-                const int slot = p.slot_map[(size_t)b * p.T + pos];
+                const int slot = srow_map[pos];
                 if (slot >= 0 && slot < p.pool_rows) {
                     code = slot;
                 } else if (slot == -1) {
@@ -542,7 +545,6 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     cp_async_wait<0>();
     __syncthreads();
 
-    const int kvsrc = b * p.kv_heads + kvh / p.heads_per_kv;  // the (b, KV head) slab the rows come from
     RowSource rs;
     rs.k_pool = p.kc + (size_t)kvsrc * p.pool_rows * (D * 2);
     rs.v_pool = p.vc + (size_t)kvsrc * p.pool_rows * (D * 2);
@@ -733,6 +735,7 @@ sd_status sd::validate_attend_args(const sd_attend_args* a, const char* who) {
         SD_REQUIRE(aligned16(a->ring_k) && aligned16(a->ring_v), "%s: ring_k/ring_v must be 16-byte aligned", who);
     }
     SD_REQUIRE(a->T < kRingBase && a->pool_rows < kRingBase, "%s: T and pool_rows must be < 2^30", who);
+    SD_REQUIRE(a->slot_per_head == 0 || a->slot_per_head == 1, "%s: slot_per_head must be 0 or 1", who);
     return SD_OK;
 }
 
@@ -806,6 +809,7 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
             p.vh = static_cast<const uint8_t*>(a->v_stage);
             p.staged = 1;
         }
+        p.slot_per_head = a->slot_per_head;
     } else {
         p.pool_rows = a->T;
     }

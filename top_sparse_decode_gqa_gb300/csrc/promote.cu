@@ -7,7 +7,8 @@
 // positions (union over the KV heads) that are not in the pool are promoted, in ascending
 // position order, into the first slots of a FIFO ring (starting at the sequence's hand)
 // that do not hold a position selected in the same step; a slot's old position leaves the
-// pool.  A later step that selects the same rows reads them from HBM.
+// pool.  A later step that selects the same rows reads them from HBM.  With a slot map per
+// (sequence, KV head) every (b, KV head) is such a unit, holding only its own head's rows.
 //
 // Three launches:
 //   mark   every selected position sets its bit in a per-sequence bitmap;
@@ -230,16 +231,30 @@ struct PromoteLayout {
 
 size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// The promotion's units.  With one slot map per sequence the unit is the sequence (its KV
+// heads share a slot); with one per (sequence, KV head) every (b, KV head) is a unit of its
+// own with a single KV head -- the same memory read as [B*Hkv, 1, ...] -- whose selection
+// is its own row of idx (or the G query heads' rows with per-head selections).
+struct PromoteUnits {
+    int units, heads, groups;
+};
+
+PromoteUnits promote_units(const sd_attend_args* a) {
+    const int G = a->Hq / a->Hkv;
+    if (a->slot_per_head) return {a->B * a->Hkv, 1, a->per_head ? G : 1};
+    return {a->B, a->Hkv, a->per_head ? a->Hq : a->Hkv};
+}
+
 PromoteLayout promote_layout(const sd_attend_args* a) {
     PromoteLayout l{};
-    const int groups = a->per_head ? a->Hq : a->Hkv;
+    const PromoteUnits u = promote_units(a);
     l.W32 = (a->T + 31) / 32;
-    const long sel = (long)groups * a->n_idx * a->block;
+    const long sel = (long)u.groups * a->n_idx * a->block;
     l.max_tasks = (int)std::min<long>((long)a->pool_rows, std::max<long>(1, sel));
     l.mark = 0;
-    l.tasks = al256((size_t)a->B * l.W32 * 4);
-    l.ntask = l.tasks + al256((size_t)a->B * l.max_tasks * sizeof(int2));
-    l.counter = l.ntask + al256((size_t)a->B * 4);
+    l.tasks = al256((size_t)u.units * l.W32 * 4);
+    l.ntask = l.tasks + al256((size_t)u.units * l.max_tasks * sizeof(int2));
+    l.counter = l.ntask + al256((size_t)u.units * 4);
     l.bytes = l.counter + 256;
     return l;
 }
@@ -286,23 +301,25 @@ extern "C" sd_status sd_promote_rows(const sd_attend_args* a, int32_t* pool_pos,
     p.tasks = reinterpret_cast<int2*>(ws + l.tasks);
     p.ntask = reinterpret_cast<int32_t*>(ws + l.ntask);
     p.counter = reinterpret_cast<uint32_t*>(ws + l.counter);
-    p.B = a->B;
-    p.groups = a->per_head ? a->Hq : a->Hkv;
+    const PromoteUnits u = promote_units(a);
+    SD_REQUIRE(u.units <= 65535, "sd_promote_rows: %d units (sequences, or sequence x KV head) exceed 65535", u.units);
+    p.B = u.units;
+    p.groups = u.groups;
     p.n_idx = a->n_idx;
     p.block = a->block;
     p.T = a->T;
     p.P = a->pool_rows;
-    p.Hkv = a->Hkv;
+    p.Hkv = u.heads;
     p.row_bytes = a->d * dtype_bytes(a->dtype);
     p.W32 = l.W32;
     p.max_tasks = l.max_tasks;
     p.err = a->err_word;
     cudaStream_t st = as_stream(stream);
-    const long marks = (long)a->B * p.groups * a->n_idx * a->block;
+    const long marks = (long)p.B * p.groups * a->n_idx * a->block;
     const int mgrid = (int)std::min<long>((marks + 255) / 256, (long)num_sms() * 8);
     SD_CUDA_CHECK(launch_pdl(promote_mark_kernel, dim3((unsigned)mgrid), dim3(256), 0, st, p),
                   "sd_promote_rows: mark launch");
-    SD_CUDA_CHECK(launch_pdl(promote_plan_kernel, dim3((unsigned)a->B), dim3(kPlanThreads), 0, st, p),
+    SD_CUDA_CHECK(launch_pdl(promote_plan_kernel, dim3((unsigned)p.B), dim3(kPlanThreads), 0, st, p),
                   "sd_promote_rows: plan launch");
     SD_CUDA_CHECK(launch_pdl(promote_copy_kernel, dim3((unsigned)num_sms()), dim3(kCopyThreads), 0, st, p),
                   "sd_promote_rows: copy launch");

@@ -78,6 +78,7 @@ struct SelAttParams {
     int32_t* err;
     int inbox_own;  // 1: the merge inbox has its own shared memory after the layout's end
     int attend;     // 0: selection only (idx written; q, K/V and the outputs untouched)
+    int slot_per_head;  // 1: slot_map is [B, Hkv, T]
 };
 
 // Shared-memory layout (byte offsets), in order:
@@ -801,7 +802,7 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
                 report(p.err, SD_DEVERR_INDEX);
                 code = kNoRow;
             } else if (p.slot_map != nullptr) {
-                const int slot = p.slot_map[(size_t)b * p.T + pos];
+                const int slot = p.slot_map[(size_t)(p.slot_per_head ? bk : b) * p.T + pos];
                 if (slot >= 0 && slot < p.pool_rows) {
                     code = slot;
                 } else if (slot == -1) {
@@ -1077,6 +1078,8 @@ extern "C" sd_status sd_select_attend(const float* scores, int N, uint32_t* key_
     p.logits = a->logits;
     p.err = a->err_word;
     p.attend = 1;
+    p.slot_per_head = a->slot_per_head;
+    SD_REQUIRE(a->slot_per_head == 0 || a->slot_per_head == 1, "sd_select_attend: slot_per_head must be 0 or 1");
     if (a->slot_map != nullptr) {
         SD_REQUIRE(a->pool_rows >= 0, "sd_select_attend: pool_rows must be >= 0");
         SD_REQUIRE(a->k_host && a->v_host, "sd_select_attend: slot_map needs k_host and v_host");

@@ -34,6 +34,7 @@ struct StageParams {
     int total_rows;
     uint32_t* counter;  // [0] next chunk, [1] CTAs done; zero between calls
     int32_t* err;
+    int slot_per_head;  // 1: slot_map is [B, kv_heads, T]
 };
 
 __global__ void __launch_bounds__(kStThreads, 1) stage_host_rows_kernel(const StageParams p) {
@@ -68,7 +69,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stage_host_rows_kernel(const St
                 }
             }
             if (ok) {
-                const int slot = p.slot_map[(size_t)b * p.T + pos];
+                const int slot = p.slot_map[(size_t)(p.slot_per_head ? kvsrc : b) * p.T + pos];
                 if (slot == -1)
                     host_row = kvsrc * p.T + (int)pos;
                 else if (slot < -1 || slot >= p.pool_rows)
@@ -150,6 +151,7 @@ extern "C" sd_status sd_stage_host_rows(const sd_attend_args* a, uint32_t* count
     p.total_rows = (int)total;
     p.counter = counter;
     p.err = a->err_word;
+    p.slot_per_head = a->slot_per_head;
     if (p.total_rows == 0) return SD_OK;
     // one CTA (8 warps, 32 KB of host reads in flight) per SM is several times what the host
     // link can serve, and leaves each SM room for other kernels running beside the copy

@@ -41,10 +41,11 @@ available here):
   with its own indexer query and keys (a selection per layer), its own K/V cache in pinned
   host memory and its own HBM pool of the same resident 10 % of positions; the step runs
   layer l+1's indexer, top-k and host-row staging ahead, beside layer l's attention.
-* ``c10_cached_tiered``: the tiered verify layer of ``c4`` with a 25 % pool, over 16
-  decode steps whose 8 verify queries slide along a sequence of 23 indexer queries (each
-  step drops the oldest and adds one), so consecutive selections overlap; the pool is kept
-  as a cache: each step promotes its selected host rows into it before the attention.
+* ``c10_cached_tiered``: the tiered verify layer of ``c4`` (10 % pool), over 16 decode
+  steps whose 8 verify queries slide along a sequence of 23 indexer queries (each step
+  drops the oldest and adds one), so consecutive selections overlap; residency is kept per
+  (sequence, KV head) -- every head starts from the generated resident positions -- and the
+  pool is a cache: each step promotes its selected host rows into it before the attention.
 
 Value recipe: indexer query and keys are integers drawn uniformly from [-8, 8] (exact in
 bf16 and fp32); attention q, K, V are standard normal, rounded to bf16 (nearest even)
@@ -89,6 +90,7 @@ class Workload:
     q_idx_dtype: str = ""   # storage type of the indexer query if not `dtype` ("f16": with fp16 pooled keys)
     layer_indexers: bool = False  # one indexer query and key set per layer (selection per layer)
     drift_steps: int = 0    # > 0: decode steps whose V verify queries slide along a query sequence
+    slot_per_head: bool = False  # residency (slot map) per (sequence, KV head) instead of per sequence
     cum_frac: tuple = (0.2, 0.6, 0.9)
     n_sink: int = 0
     n_recent: int = 0
@@ -161,7 +163,7 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("c9_lookahead_tiered", 8, B=2, V=8, Hq=32, Hkv=8, d=128, T=131072, dtype="bf16",
                  dI=128, k=2048, resident_frac=0.1, layers=4, layer_indexers=True),
         Workload("c10_cached_tiered", 9, B=4, V=8, Hq=32, Hkv=8, d=128, T=131072, dtype="bf16",
-                 dI=128, k=2048, resident_frac=0.25, drift_steps=16),
+                 dI=128, k=2048, resident_frac=0.1, drift_steps=16, slot_per_head=True),
     )
 }
 
