@@ -170,22 +170,27 @@ __global__ void __launch_bounds__(kPlanThreads) promote_plan_kernel(const Promot
     for (int w = tid; w < p.W32; w += kPlanThreads) p.mark[(size_t)b * p.W32 + w] = 0u;
 }
 
-// Warps take tasks (one promoted position of one sequence) from the counter and copy its K
+// Warps take chunks of kTaskChunk tasks (a task: one promoted position of one unit) from the
+// counter -- chunks past a unit's task count are skipped at once -- and copy each task's K
 // and V rows of every KV head as 16-byte pieces, loads before stores.
+constexpr int kTaskChunk = 32;
+
 __global__ void __launch_bounds__(kCopyThreads) promote_copy_kernel(const PromoteParams p) {
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int pieces = p.row_bytes / 16;       // per row
     const int per_task = 2 * p.Hkv * pieces;    // K and V of every head
-    const long total = (long)p.B * p.max_tasks;
+    const int chunks_per_unit = (p.max_tasks + kTaskChunk - 1) / kTaskChunk;
+    const long total = (long)p.B * chunks_per_unit;
     for (;;) {
         uint32_t c = 0;
         if (lane == 0) c = atomicAdd(&p.counter[0], 1u);
         c = __shfl_sync(0xffffffffu, c, 0);
         if ((long)c >= total) break;
-        const int b = (int)(c / p.max_tasks), m = (int)(c % p.max_tasks);
-        if (m >= p.ntask[b]) continue;
+        const int b = (int)(c / chunks_per_unit), m0 = (int)(c % chunks_per_unit) * kTaskChunk;
+        const int m1 = min(p.ntask[b], m0 + kTaskChunk);
+        for (int m = m0; m < m1; ++m) {
         const int2 t = p.tasks[(size_t)b * p.max_tasks + m];
         if (t.x < 0 || t.x >= p.T || t.y < 0 || t.y >= p.P) {  // never for a consistent plan
             if (lane == 0) report(p.err, SD_DEVERR_SLOT);
@@ -212,6 +217,7 @@ __global__ void __launch_bounds__(kCopyThreads) promote_copy_kernel(const Promot
                 const size_t dst = (((size_t)b * p.Hkv + h) * p.P + t.y) * p.row_bytes + off;
                 *reinterpret_cast<uint4*>((which ? p.vp : p.kp) + dst) = v[u];
             }
+        }
         }
     }
     __syncthreads();
