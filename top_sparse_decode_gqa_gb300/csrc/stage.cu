@@ -30,29 +30,34 @@ struct StageParams {
     const int32_t* idx;
     int T, pool_rows, n_idx, block, n_rows;
     int groups_per_seq, kv_heads, heads_per_kv;
-    int row_bytes, rows_per_chunk;
+    int row_bytes, rows_per_chunk;  // rows_per_chunk: rows one copy batch moves
     int total_rows;
     uint32_t* counter;  // [0] next chunk, [1] CTAs done; zero between calls
     int32_t* err;
     int slot_per_head;  // 1: slot_map is [B, kv_heads, T]
 };
 
+// A warp takes the next 32 list rows from the counter (one per lane), resolves each to its
+// host row or to nothing (pooled or empty), and copies only the misses, rows_per_chunk rows
+// (kStPieces 16-byte pieces per lane, all loads before any store) at a time.
 __global__ void __launch_bounds__(kStThreads, 1) stage_host_rows_kernel(const StageParams p) {
+    __shared__ int s_hr[kStThreads / 32][32];  // per warp: the misses' host rows, in lane order
+    __shared__ int s_f[kStThreads / 32][32];   // and their list rows
     pdl_wait();  // idx (and the slot map) may come from the preceding kernel
     pdl_launch_dependents();
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ppr = p.row_bytes / 16;  // pieces per K (or V) row
     const int C = p.rows_per_chunk;    // C * 2 * ppr == 32 * kStPieces
-    const int nchunks = (p.total_rows + C - 1) / C;
+    const int nchunks = (p.total_rows + 31) / 32;
     for (;;) {
         uint32_t c = 0;
         if (lane == 0) c = atomicAdd(&p.counter[0], 1u);
         c = __shfl_sync(0xffffffffu, c, 0);
         if (c >= (uint32_t)nchunks) break;
-        // lane r < C resolves list row f = c*C + r to its host row, or -1 (nothing to copy)
+        // lane r resolves list row f = 32c + r to its host row, or -1 (nothing to copy)
         int host_row = -1;  // < 2^31 (checked on the host)
-        const int f = (int)c * C + lane;
-        if (lane < C && f < p.total_rows) {
+        const int f = (int)c * 32 + lane;
+        if (f < p.total_rows) {
             const int g = f / p.n_rows, j = f % p.n_rows;
             const int b = g / p.groups_per_seq;
             const int kvsrc = b * p.kv_heads + (g % p.groups_per_seq) / p.heads_per_kv;
@@ -76,27 +81,38 @@ __global__ void __launch_bounds__(kStThreads, 1) stage_host_rows_kernel(const St
                     report(p.err, SD_DEVERR_SLOT);
             }
         }
-        // piece q = lane + 32 i of the chunk: row q / (2 ppr), K for the first ppr pieces of a
-        // row and V for the rest, 16 bytes at (q mod ppr) * 16
-        uint4 v[kStPieces];
-        int hr[kStPieces];
+        const uint32_t miss = __ballot_sync(0xffffffffu, host_row >= 0);
+        if (miss == 0u) continue;
+        if (host_row >= 0) {
+            const int rank = __popc(miss & ((1u << lane) - 1u));
+            s_hr[warp][rank] = host_row;
+            s_f[warp][rank] = f;
+        }
+        __syncwarp();
+        const int n_miss = __popc(miss);
+        for (int m0 = 0; m0 < n_miss; m0 += C) {
+            // piece q = lane + 32 i of the batch: miss m0 + q / (2 ppr), K for the first ppr
+            // pieces of a row and V for the rest, 16 bytes at (q mod ppr) * 16
+            uint4 v[kStPieces];
 #pragma unroll
-        for (int i = 0; i < kStPieces; ++i) {
-            const int q = lane + 32 * i, r = q / (2 * ppr), w = q % (2 * ppr);
-            hr[i] = __shfl_sync(0xffffffffu, host_row, r);
-            if (hr[i] >= 0) {
-                const uint8_t* src = (w < ppr ? p.kh : p.vh) + (size_t)hr[i] * p.row_bytes + (w % ppr) * 16;
-                v[i] = __ldcs(reinterpret_cast<const uint4*>(src));
+            for (int i = 0; i < kStPieces; ++i) {
+                const int q = lane + 32 * i, m = m0 + q / (2 * ppr), w = q % (2 * ppr);
+                if (m < n_miss) {
+                    const uint8_t* src =
+                        (w < ppr ? p.kh : p.vh) + (size_t)s_hr[warp][m] * p.row_bytes + (w % ppr) * 16;
+                    v[i] = __ldcs(reinterpret_cast<const uint4*>(src));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kStPieces; ++i) {
+                const int q = lane + 32 * i, m = m0 + q / (2 * ppr), w = q % (2 * ppr);
+                if (m < n_miss) {
+                    uint8_t* dst = (w < ppr ? p.ks : p.vs) + (size_t)s_f[warp][m] * p.row_bytes + (w % ppr) * 16;
+                    *reinterpret_cast<uint4*>(dst) = v[i];
+                }
             }
         }
-#pragma unroll
-        for (int i = 0; i < kStPieces; ++i) {
-            if (hr[i] >= 0) {
-                const int q = lane + 32 * i, r = q / (2 * ppr), w = q % (2 * ppr);
-                uint8_t* dst = (w < ppr ? p.ks : p.vs) + (size_t)((int)c * C + r) * p.row_bytes + (w % ppr) * 16;
-                *reinterpret_cast<uint4*>(dst) = v[i];
-            }
-        }
+        __syncwarp();  // the lists are rewritten by the next chunk
     }
     // the last CTA to finish leaves the counter at zero for the next call
     __syncthreads();
