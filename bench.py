@@ -496,20 +496,30 @@ class VerifyGroupStep:
 
 class CachedTieredStep:
     """One decode step of a tiered layer whose pool is kept as a cache: the indexer (this
-    step's window of the sliding verify queries), the top-k, the promotion of the selected
-    host rows into the pool (evicting rows not selected), the staging of the host rows the
-    pool had no room for, and the attention.  Steps cycle over the query windows; the pool
-    carries over from step to step."""
+    step's window of the sliding verify queries), the top-k, the staging of the selected
+    rows the pool does not hold, the attention, and the promotion of the staged rows into
+    the pool (evicting rows not selected).  Steps cycle over the query windows; the pool
+    carries over from step to step.
+
+    With residency per (sequence, KV head) the promotion copies the rows from the stage
+    (sd_promote_staged_rows) after the attention, and step s+1 runs step s's promotion on a
+    side stream beside its own indexer and top-k (two selection buffers alternate), joining
+    it before its staging; `concurrent = False` runs the same calls in order on one stream.
+    With one slot map per sequence the promotion reads the host cache before the staging
+    (sd_promote_rows)."""
 
     dominant = "sd_index_score"
-    phases = ("after_topk", "after_promote")
     launches_per_step = 8  # indexer, top-k, promotion (3), staging, attention, merge
     dominant_per_step = 1
 
-    def __init__(self, w, x, device):
+    def __init__(self, w, x, device, concurrent=True):
         import torch
         from top_sparse_decode_gqa_gb300 import binding as sd
         self.sd, self.w, self.dev = sd, w, device
+        self.staged_promotion = bool(w.slot_per_head)
+        self.concurrent = concurrent
+        self.phases = (("after_topk", "promote_start", "promote_end") if self.staged_promotion
+                       else ("after_topk", "after_promote"))
         seq = x["q_idx_seq"]
         self.q_idx_win = [seq[:, :, s:s + w.V].contiguous().to(device) for s in range(w.drift_steps)]
         self.q_idx = self.q_idx_win[0]
@@ -524,39 +534,68 @@ class CachedTieredStep:
         self.static_map = sm.to(device)  # the residency as generated (for comparison)
         self.pool_pos, self.hand = sd.pool_state(self.slot_map, w.pool_rows)
         self.scores = torch.empty(w.B, w.Hkv, w.T, dtype=torch.float32, device=device)
-        self.idx = torch.empty(w.B, w.Hkv, w.k, dtype=torch.int32, device=device)
+        self.idx_buf = [torch.empty(w.B, w.Hkv, w.k, dtype=torch.int32, device=device) for _ in range(2)]
+        self.idx = self.idx_buf[0]
         self.key_hist = sd.key_hist_buffer(w.B * w.Hkv, device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self.args, self.out, self.lse, _ = sd.make_attend_args(
             self.q, self.k_cache, self.v_cache, self.idx, T=w.T, k_host=self.k_host, v_host=self.v_host,
             slot_map=self.slot_map, err_word=self.err)
         self.stage = sd.stage_buffers(self.args, self.q.dtype, device)
+        args1 = type(self.args).from_buffer_copy(self.args)  # the same call on the other selection buffer
+        args1.idx = self.idx_buf[1].data_ptr()
+        self.args_buf = [self.args, args1]
         self.counter = sd.stage_counter(device)
-        self.ws_promote = torch.zeros(max(16, sd.sd_promote_rows_workspace_bytes(self.args)), dtype=torch.uint8,
-                                      device=device)
+        ws_bytes = (sd.sd_promote_staged_rows_workspace_bytes(self.args) if self.staged_promotion
+                    else sd.sd_promote_rows_workspace_bytes(self.args))
+        self.ws_promote = torch.zeros(max(16, ws_bytes), dtype=torch.uint8, device=device)
         need = sd.sd_gather_attend_workspace_bytes(self.args)
         self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=device)
+        self.side = torch.cuda.Stream(device=device)
+        self.pending = None  # the args of the step whose staged rows are still to be promoted
         self.step_no = 0
         self.host_bytes = None
 
     def run(self, m: "StepMarks" = None):
+        import contextlib
+        import torch
         sd, w = self.sd, self.w
         q_idx = self.q_idx_win[self.step_no % w.drift_steps]
+        args = self.args_buf[self.step_no % 2]
         self.step_no += 1
         if m is not None:
             m.start.record()
+        if self.pending is not None:  # the previous step's promotion, beside this step's selection
+            main = torch.cuda.current_stream()
+            if self.concurrent:
+                self.side.wait_stream(main)
+            with torch.cuda.stream(self.side) if self.concurrent else contextlib.nullcontext():
+                if m is not None:
+                    m.at("promote_start")
+                sd.sd_promote_staged_rows(self.pending, self.pool_pos, self.hand, self.ws_promote)
+                if m is not None:
+                    m.at("promote_end")
+        if m is not None:
             m.before(0)
         sd.sd_index_score(q_idx, self.k_idx, self.scores, self.err, key_hist=self.key_hist)
         if m is not None:
             m.after(0)
+        self.idx = self.idx_buf[(self.step_no - 1) % 2]
         sd.sd_topk(self.scores, w.k, self.idx, key_hist=self.key_hist)
         if m is not None:
             m.at("after_topk")
-        sd.sd_promote_rows(self.args, self.pool_pos, self.hand, self.ws_promote)
-        if m is not None:
-            m.at("after_promote")
-        sd.sd_stage_host_rows(self.args, self.counter)
-        sd.sd_gather_attend(self.args, self.ws)
+        if self.staged_promotion:
+            if self.pending is not None and self.concurrent:
+                torch.cuda.current_stream().wait_stream(self.side)
+            sd.sd_stage_host_rows(args, self.counter)
+            sd.sd_gather_attend(args, self.ws)
+            self.pending = args
+        else:
+            sd.sd_promote_rows(args, self.pool_pos, self.hand, self.ws_promote)
+            if m is not None:
+                m.at("after_promote")
+            sd.sd_stage_host_rows(args, self.counter)
+            sd.sd_gather_attend(args, self.ws)
         if m is not None:
             m.end.record()
 
@@ -577,25 +616,34 @@ class CachedTieredStep:
 
     def after_warmup(self):
         """Host bytes per step in the steady state, averaged over one cycle of the query
-        windows: the promoted positions (K and V of every KV head) plus the selected rows
-        left in host memory (staged); and, for comparison, the host rows the same
-        selections would read with the pool kept as it was generated."""
+        windows: the rows promoted from host memory (K and V of every KV head of a promoted
+        position; none with staged promotion) plus the selected rows left in host memory
+        (staged); and, for comparison, the host rows the same selections would read with
+        the pool kept as it was generated."""
         import torch
         w, row = self.w, self.w.d * self.w.elem_bytes * 2
         with_cache = without = 0
         for _ in range(w.drift_steps):
+            if self.staged_promotion:
+                # after the step, the slot map is the one its staging saw (its own promotion
+                # runs with the next step)
+                self.run()
+                torch.cuda.synchronize()
+                without += self.host_misses(self.static_map)[1] * row
+                with_cache += self.host_misses(self.slot_map)[1] * row
+                continue
             q_idx = self.q_idx_win[self.step_no % w.drift_steps]
+            args, self.idx = self.args_buf[self.step_no % 2], self.idx_buf[self.step_no % 2]
             self.step_no += 1
             self.sd.sd_index_score(q_idx, self.k_idx, self.scores, self.err, key_hist=self.key_hist)
             self.sd.sd_topk(self.scores, w.k, self.idx, key_hist=self.key_hist)
             without += self.host_misses(self.static_map)[1] * row
             before, _ = self.host_misses(self.slot_map)
-            self.sd.sd_promote_rows(self.args, self.pool_pos, self.hand, self.ws_promote)
+            self.sd.sd_promote_rows(args, self.pool_pos, self.hand, self.ws_promote)
             left_pos, left_rows = self.host_misses(self.slot_map)
-            heads = 1 if w.slot_per_head else w.Hkv  # rows a promoted unit brings
-            with_cache += (before - left_pos) * heads * row + left_rows * row
-            self.sd.sd_stage_host_rows(self.args, self.counter)
-            self.sd.sd_gather_attend(self.args, self.ws)
+            with_cache += (before - left_pos) * w.Hkv * row + left_rows * row
+            self.sd.sd_stage_host_rows(args, self.counter)
+            self.sd.sd_gather_attend(args, self.ws)
         torch.cuda.synchronize()
         self.host_bytes = with_cache // w.drift_steps
         self.host_bytes_static = without // w.drift_steps
@@ -811,7 +859,7 @@ class DenseScoringStep:
 
 def make_step(w, x, device, separate=False, tiered_path="staged", lookahead=True):
     if w.drift_steps > 0:
-        return CachedTieredStep(w, x, device)
+        return CachedTieredStep(w, x, device, concurrent=lookahead)
     if w.layer_indexers:
         return LookaheadStep(w, x, device, lookahead)
     if w.ring_w > 0:
@@ -964,11 +1012,33 @@ def run_ours(args):
             "gather_attend": k_us(lambda m: m.phase["after_stage"], lambda m: m.end)}
     elif isinstance(step, CachedTieredStep):
         k_us = lambda a, b: round(statistics.mean(a(m).elapsed_time(b(m)) for m in kmarks) * 1e3, 2)  # noqa: E731
-        step_roof["kernel_us"] = {
-            "index_score": round(statistics.mean(dom_ms) * 1e3, 2),
-            "topk": k_us(lambda m: m.dom[0][1], lambda m: m.phase["after_topk"]),
-            "promote": k_us(lambda m: m.phase["after_topk"], lambda m: m.phase["after_promote"]),
-            "stage_host_rows+gather_attend": k_us(lambda m: m.phase["after_promote"], lambda m: m.end)}
+        if step.staged_promotion:
+            # the promotion (of the previous step's staged rows) runs on the side stream beside
+            # the indexer and top-k; the staging waits for it
+            step_roof["kernel_us"] = {
+                "index_score": round(statistics.mean(dom_ms) * 1e3, 2),
+                "topk": k_us(lambda m: m.dom[0][1], lambda m: m.phase["after_topk"]),
+                "promote_staged_rows (side stream)": k_us(lambda m: m.phase["promote_start"],
+                                                          lambda m: m.phase["promote_end"]),
+                "stage_host_rows+gather_attend": k_us(lambda m: m.phase["after_topk"], lambda m: m.end)}
+            if step.concurrent:  # the same steps with every call in order on one stream
+                step.concurrent = False
+                serial = []
+                for i in range(3 + min(K, 20)):  # 3 untimed, then the median
+                    clean_l2()
+                    sm_ = StepMarks(0)
+                    step.run(sm_)
+                    torch.cuda.synchronize()
+                    if i >= 3:
+                        serial.append(sm_.step_ms())
+                step.concurrent = True
+                step_roof["serial_ms_per_step_median"] = round(statistics.median(serial), 5)
+        else:
+            step_roof["kernel_us"] = {
+                "index_score": round(statistics.mean(dom_ms) * 1e3, 2),
+                "topk": k_us(lambda m: m.dom[0][1], lambda m: m.phase["after_topk"]),
+                "promote": k_us(lambda m: m.phase["after_topk"], lambda m: m.phase["after_promote"]),
+                "stage_host_rows+gather_attend": k_us(lambda m: m.phase["after_promote"], lambda m: m.end)}
         step_roof["host_bytes_per_step_without_cache"] = step.host_bytes_static
     elif isinstance(step, LookaheadStep):
         step_roof["kernel_us"] = {"index_score": round(statistics.mean(dom_ms) * 1e3, 2), "layers": w.layers}
@@ -1027,8 +1097,13 @@ def run_ours(args):
                             else f"indexer + top-k once, then per layer ({w.layers}) ring append + gather-attend "
                                  "over the selected rows and the draft ring"
                             if isinstance(step, VerifyGroupStep)
-                            else "indexer + top-k + promotion into the pool (cache) + staging of the rest + "
-                                 "gather-attend, the query window sliding step by step"
+                            else ("indexer + top-k + staging of the rows the pool lacks + gather-attend, then "
+                                  "their promotion from the stage into the pool (cache) "
+                                  + ("beside the next step's indexer and top-k"
+                                     if step.concurrent else "in order on one stream")
+                                  if step.staged_promotion else
+                                  "indexer + top-k + promotion into the pool (cache) + staging of the rest + "
+                                  "gather-attend") + ", the query window sliding step by step"
                             if isinstance(step, CachedTieredStep)
                             else f"per layer ({w.layers}): indexer + top-k + host-row staging + gather-attend, "
                                  + ("next layer's selection before this layer's attention, staging on its own stream"
@@ -1073,8 +1148,10 @@ def measure_e2e(step, w, x, clean_l2, K):
     ins = [(dst, src.contiguous().pin_memory()) for dst, src in ins]
     sparse = isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep, LookaheadStep,
                                CachedTieredStep))
-    outs = [step.out, step.lse] + ([step.idx[-1] if isinstance(step.idx, list) else step.idx] if sparse else [step.s])
-    outs = [(src, torch.empty(src.shape, dtype=src.dtype).pin_memory()) for src in outs]
+    # the result tensors, looked up after every step (a step may alternate its buffers)
+    results = lambda: [step.out, step.lse] + (  # noqa: E731
+        [step.idx[-1] if isinstance(step.idx, list) else step.idx] if sparse else [step.s])
+    outs = [torch.empty(src.shape, dtype=src.dtype).pin_memory() for src in results()]
     times = []
     for i in range(K + 3):
         clean_l2()
@@ -1083,13 +1160,13 @@ def measure_e2e(step, w, x, clean_l2, K):
         for dst, src in ins:
             dst.copy_(src, non_blocking=True)
         step.run()
-        for src, dst in outs:
+        for src, dst in zip(results(), outs):
             dst.copy_(src, non_blocking=True)
         torch.cuda.current_stream().synchronize()
         if i >= 3:
             times.append(time.perf_counter() - t0)
     bi = sum(src.numel() * src.element_size() for _, src in ins)
-    bo = sum(dst.numel() * dst.element_size() for _, dst in outs)
+    bo = sum(dst.numel() * dst.element_size() for dst in outs)
     return {"value": round(w.queries_per_step * len(times) / sum(times), 1), "unit": "queries/s",
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "timing": "host wall clock per step incl. copies and sync"}

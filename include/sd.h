@@ -298,6 +298,26 @@ sd_status sd_promote_rows(const sd_attend_args* args, int32_t* pool_pos, int32_t
                           size_t workspace_bytes, void* stream);
 
 /*
+ * sd_promote_staged_rows -- sd_promote_rows with the promoted rows taken from the HBM stage.
+ * [DHiSparse] "Metodologia" and [SparDA] sec. 2 item 3, as sd_promote_rows; the order of the
+ * calls is a reading: the step's misses cross the host link once, into the stage
+ * (sd_stage_host_rows), the attention reads them there, and only then are they promoted, so
+ * the promotion can run beside the next step's selection.
+ * Leaves slot_map, pool_pos, hand and the pool exactly as sd_promote_rows would with the same
+ * arguments and state.  Contract: slot_per_head = 1 (a unit is one (b, KV head), so each
+ * promoted row is the one its own head staged), and args->k_stage/v_stage hold what
+ * sd_stage_host_rows copied for these args with slot_map as it is now (no promotion in
+ * between); the host cache is not read.  A stage not filled that way gives wrong pool rows
+ * but no out-of-bounds access.  The workspace (sd_promote_staged_rows_workspace_bytes, a
+ * [B*Hkv, T] int32 map beyond sd_promote_rows' layout) is zero-filled before the first call
+ * and left ready for the next.  Errors as sd_promote_rows; SD_ERR_INVALID_ARG without
+ * slot_per_head or the stage, or with B*Hkv*groups*n_idx*block >= 2^31.
+ */
+size_t sd_promote_staged_rows_workspace_bytes(const sd_attend_args* args);
+sd_status sd_promote_staged_rows(const sd_attend_args* args, int32_t* pool_pos, int32_t* hand, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
  * sd_ring_append -- write new tokens' K/V into the window-bounded draft ring.
  * [DHiSparse] "Metodologia" (the draft tokens' K/V live in a ring bounded by a window).
  * Token i < n of sequence b, at position pos0[b] + i, goes to slot (pos0[b] + i) mod W:

@@ -188,3 +188,29 @@ def test_promote_validation(lib):
     assert b"workspace" in lib.sd_last_error_message()
     a.pool_rows = 0
     assert lib.sd_promote_rows_workspace_bytes(ctypes.byref(a)) == 0
+
+
+def test_promote_staged_validation(lib):
+    from top_sparse_decode_gqa_gb300.binding import sd_attend_args
+    dummy = ctypes.c_void_p(16)
+    a = sd_attend_args()
+    a.q = a.k_cache = a.v_cache = a.out = a.lse = a.idx = a.slot_map = 16
+    a.dtype, a.B, a.V, a.Hq, a.Hkv, a.d, a.T = 1, 2, 8, 32, 8, 128, 4096
+    a.pool_rows, a.n_idx, a.block, a.scale = 409, 64, 1, 0.1
+    # the staged promotion works on (sequence, KV head) units only
+    assert lib.sd_promote_staged_rows(ctypes.byref(a), dummy, dummy, dummy, 1 << 24, None) == 1
+    assert b"(sequence, KV head)" in lib.sd_last_error_message()
+    a.slot_per_head = 1
+    # it reads the stage, not the host cache
+    assert lib.sd_promote_staged_rows(ctypes.byref(a), dummy, dummy, dummy, 1 << 24, None) == 1
+    assert b"k_stage" in lib.sd_last_error_message()
+    a.k_stage = a.v_stage = 24  # not 16-byte aligned
+    assert lib.sd_promote_staged_rows(ctypes.byref(a), dummy, dummy, dummy, 1 << 24, None) == 1
+    a.k_stage = a.v_stage = 32
+    # its workspace adds a [B*Hkv, T] int32 map to the host-mode layout
+    need = lib.sd_promote_staged_rows_workspace_bytes(ctypes.byref(a))
+    assert need >= lib.sd_promote_rows_workspace_bytes(ctypes.byref(a)) + 2 * 8 * 4096 * 4
+    assert lib.sd_promote_staged_rows(ctypes.byref(a), dummy, dummy, dummy, need - 16, None) == 1
+    assert b"workspace" in lib.sd_last_error_message()
+    a.pool_rows = 0
+    assert lib.sd_promote_staged_rows_workspace_bytes(ctypes.byref(a)) == 0

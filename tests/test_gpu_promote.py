@@ -81,6 +81,68 @@ def test_promotion_matches_the_oracle_over_drifting_steps(T, P, n, block, per_he
             np.testing.assert_array_equal(vp[b][:, occ[b]], o_vp[b][:, occ[b]])
 
 
+@pytest.mark.parametrize("T,P,n,block,per_head", [(2000, 60, 9, 4, False), (4096, 300, 64, 1, False),
+                                                  (1000, 50, 12, 1, True)])
+def test_staged_promotion_matches_the_oracle(T, P, n, block, per_head):
+    # per (b, KV head) units: each step stages the misses, attends, then promotes them from
+    # the stage; the state and the pool rows equal the oracle's promotion of the same
+    # selections, and the attention equals the one over the host rows
+    import math
+    rng = np.random.default_rng(T + P + 1)
+    B, Hq, Hkv, d, V = 3, 8, 2, 128, 1
+    G = Hq // Hkv
+    groups = Hq if per_head else Hkv
+    kh = torch.randn(B, Hkv, T, d, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    vh = torch.randn(B, Hkv, T, d, generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
+    k_host, v_host = kh.pin_memory(), vh.pin_memory()
+    k_pool = torch.zeros(B, Hkv, P, d, dtype=torch.bfloat16, device="cuda")
+    v_pool = torch.zeros_like(k_pool)
+    slot_map = torch.full((B, Hkv, T), -1, dtype=torch.int32, device="cuda")
+    pool_pos, hand = sd().pool_state(slot_map, P)
+    q = torch.randn(B, V, Hq, d, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).cuda()
+    U = B * Hkv
+    o_slot = np.full((U, T), -1, dtype=np.int32)
+    o_pos = np.full((U, P), -1, dtype=np.int32)
+    o_hand = np.zeros(U, dtype=np.int32)
+    o_kp = np.zeros((U, 1, P, d), dtype=np.float32)
+    o_vp = np.zeros((U, 1, P, d), dtype=np.float32)
+    khf, vhf = kh.float().numpy().reshape(U, 1, T, d), vh.float().numpy().reshape(U, 1, T, d)
+    base = rng.permutation(T // block)[:n].astype(np.int32)
+    ws = None
+    counter = sd().stage_counter()
+    e = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for step in range(6):
+        idx_np = _drift(rng, base, n, T // block, groups, B)
+        idx = torch.from_numpy(idx_np).cuda()
+        a, out, lse, _ = sd().make_attend_args(q, k_pool, v_pool, idx, block=block, T=T, k_host=k_host,
+                                               v_host=v_host, slot_map=slot_map, per_head=per_head, err_word=e)
+        assert a.slot_per_head == 1
+        stage = sd().stage_buffers(a, torch.bfloat16)
+        sd().sd_stage_host_rows(a, counter)
+        gws = torch.zeros(max(16, sd().sd_gather_attend_workspace_bytes(a)), dtype=torch.uint8, device="cuda")
+        sd().sd_gather_attend(a, gws)
+        ws = sd().sd_promote_staged_rows(a, pool_pos, hand, ws)
+        torch.cuda.synchronize()
+        assert int(e.item()) == 0
+        oracle.promote_rows(idx_np.reshape(U, groups // Hkv, n), block, o_slot, o_pos, o_hand, khf, vhf, o_kp, o_vp)
+        np.testing.assert_array_equal(slot_map.cpu().numpy().reshape(U, T), o_slot, err_msg=f"step {step}")
+        np.testing.assert_array_equal(pool_pos.cpu().numpy(), o_pos)
+        np.testing.assert_array_equal(hand.cpu().numpy(), o_hand)
+        occ = o_pos >= 0
+        kp = k_pool.float().cpu().numpy().reshape(U, 1, P, d)
+        vp = v_pool.float().cpu().numpy().reshape(U, 1, P, d)
+        for u in range(U):
+            np.testing.assert_array_equal(kp[u][:, occ[u]], o_kp[u][:, occ[u]])
+            np.testing.assert_array_equal(vp[u][:, occ[u]], o_vp[u][:, occ[u]])
+        if step == 5 and not per_head:  # the attention of the last step against the oracle
+            from gpu_util import assert_attend_close
+            ro, rl, _ = oracle.gather_attend(q.cpu(), kh, vh, idx_np, B, V, Hq, Hkv, d, T, n, block,
+                                             1 / math.sqrt(d))
+            assert_attend_close(out, ro)
+            assert_attend_close(lse, rl, "lse")
+        del stage
+
+
 def test_attention_over_promoted_rows_is_the_same():
     from top_sparse_decode_gqa_gb300.workloads import residency_map
     g = torch.Generator().manual_seed(5)
@@ -176,14 +238,28 @@ def test_c10_cached_tiered_steps():
                                               k_host=step.k_host, v_host=step.v_host, slot_map=static_pool[2],
                                               err_word=e)
     ws0 = torch.zeros(max(16, sd().sd_gather_attend_workspace_bytes(a0)), dtype=torch.uint8, device="cuda")
-    host_rows = []
+    assert step.staged_promotion and step.concurrent
+    # the oracle's promotion state, from the generated residency (one unit per (b, KV head))
+    U = w.B * w.Hkv
+    sm0 = x["slot_map"].numpy()
+    o_slot = np.repeat(sm0, w.Hkv, axis=0).astype(np.int32)
+    o_pos = np.full((U, w.pool_rows), -1, dtype=np.int32)
+    for u in range(U):
+        t = np.nonzero(sm0[u // w.Hkv] >= 0)[0]
+        o_pos[u, sm0[u // w.Hkv, t]] = t
+    o_hand = np.zeros(U, dtype=np.int32)
+    dummy_h = np.zeros((U, 1, w.T, 1), dtype=np.float32)  # rows checked below, against the host cache
+    dummy_p = np.zeros((U, 1, w.pool_rows, 1), dtype=np.float32)
+    host_rows, sel = [], []
     for s in range(w.drift_steps):
         step.run()
+        a0.idx = step.idx.data_ptr()  # the step alternates two selection buffers
         sd().sd_gather_attend(a0, ws0)
         torch.cuda.synchronize()
         assert int(step.err.item()) == 0 and int(e.item()) == 0
         assert torch.equal(step.out, out0) and torch.equal(step.lse, lse0)
         host_rows.append(step.host_misses(step.slot_map)[1])
+        sel.append(step.idx.cpu().numpy().reshape(U, 1, w.k))
         if s in (0, w.drift_steps - 1):
             b, h = s % w.B, 3
             qw = x["q_idx_seq"][b:b + 1, h:h + 1, s:s + w.V]
@@ -199,6 +275,27 @@ def test_c10_cached_tiered_steps():
     # after the first steps most selected rows are in the pool
     total_rows = w.B * w.Hkv * w.k
     assert host_rows[-1] < 0.5 * total_rows
+    # every step's promotion ran with the next step, beside its selection: the state equals
+    # the oracle's promotions of the same selections in order; then the last one
+    for s in range(w.drift_steps - 1):
+        oracle.promote_rows(sel[s], 1, o_slot, o_pos, o_hand, dummy_h, dummy_h, dummy_p, dummy_p)
+    np.testing.assert_array_equal(step.slot_map.cpu().numpy().reshape(U, w.T), o_slot)
+    np.testing.assert_array_equal(step.pool_pos.cpu().numpy(), o_pos)
+    np.testing.assert_array_equal(step.hand.cpu().numpy(), o_hand)
+    sd().sd_promote_staged_rows(step.pending, step.pool_pos, step.hand, step.ws_promote)
+    torch.cuda.synchronize()
+    oracle.promote_rows(sel[-1], 1, o_slot, o_pos, o_hand, dummy_h, dummy_h, dummy_p, dummy_p)
+    np.testing.assert_array_equal(step.slot_map.cpu().numpy().reshape(U, w.T), o_slot)
+    np.testing.assert_array_equal(step.pool_pos.cpu().numpy(), o_pos)
+    np.testing.assert_array_equal(step.hand.cpu().numpy(), o_hand)
+    # every occupied slot holds its position's K and V rows of its own KV head
+    pos = torch.from_numpy(o_pos.astype(np.int64))
+    occ = pos >= 0
+    unit = torch.arange(U)[:, None].expand_as(pos)
+    for pool, host in ((step.k_cache, x["k"]), (step.v_cache, x["v"])):
+        got = pool.view(U, w.pool_rows, w.d).cpu()[occ]
+        want = host.view(U, w.T, w.d)[unit[occ], pos[occ]]
+        assert torch.equal(got, want)
 
 
 def test_residency_per_kv_head():

@@ -28,7 +28,8 @@ EXPORTS = (
     "sd_score_accumulate", "sd_tier_classify_workspace_bytes", "sd_tier_classify",
     "sd_quantize_rows_int8", "sd_gather_attend_noalloc", "sd_select_attend", "sd_window_count",
     "sd_window_max", "sd_window_union", "sd_index_score_heads", "sd_stage_host_rows", "sd_ring_append",
-    "sd_promote_rows_workspace_bytes", "sd_promote_rows",
+    "sd_promote_rows_workspace_bytes", "sd_promote_rows", "sd_promote_staged_rows_workspace_bytes",
+    "sd_promote_staged_rows",
 )
 
 
@@ -86,6 +87,9 @@ def lib() -> ctypes.CDLL:
         L.sd_promote_rows_workspace_bytes.argtypes = [ctypes.POINTER(sd_attend_args)]
         L.sd_promote_rows_workspace_bytes.restype = Z
         L.sd_promote_rows.argtypes = [ctypes.POINTER(sd_attend_args), P, P, P, Z, P]
+        L.sd_promote_staged_rows_workspace_bytes.argtypes = [ctypes.POINTER(sd_attend_args)]
+        L.sd_promote_staged_rows_workspace_bytes.restype = Z
+        L.sd_promote_staged_rows.argtypes = [ctypes.POINTER(sd_attend_args), P, P, P, Z, P]
         L.sd_window_count.argtypes = [I, I, I]
         L.sd_window_count.restype = I
         L.sd_window_max.argtypes = [P, I, I, I, I, P, P, P]
@@ -350,6 +354,26 @@ def sd_promote_rows(args: sd_attend_args, pool_pos: torch.Tensor, hand: torch.Te
         workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=pool_pos.device)
     _check(lib().sd_promote_rows(ctypes.byref(args), _ptr(pool_pos), _ptr(hand), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream)), "sd_promote_rows")
+    return workspace
+
+
+def sd_promote_staged_rows_workspace_bytes(args: sd_attend_args) -> int:
+    return lib().sd_promote_staged_rows_workspace_bytes(ctypes.byref(args))
+
+
+def sd_promote_staged_rows(args: sd_attend_args, pool_pos: torch.Tensor, hand: torch.Tensor,
+                           workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Promotes the step's misses from the stage `args` names into its pool, after the
+    staging and the attention (see include/sd.h); returns the workspace (zero-filled when
+    created here), to pass to the next call."""
+    _dev(pool_pos, "pool_pos")
+    _dev(hand, "hand")
+    need = lib().sd_promote_staged_rows_workspace_bytes(ctypes.byref(args))
+    if workspace is None:
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=pool_pos.device)
+    _check(lib().sd_promote_staged_rows(ctypes.byref(args), _ptr(pool_pos), _ptr(hand), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream)),
+           "sd_promote_staged_rows")
     return workspace
 
 

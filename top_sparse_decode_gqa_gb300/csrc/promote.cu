@@ -18,6 +18,12 @@
 //   copy   a persistent grid copies each promoted position's K and V rows of every KV head
 //          from the host cache (device mapping) into its pool slot; warps take tasks from a
 //          counter that the last CTA resets.
+//
+// Staged mode (sd_promote_staged_rows, units of one KV head): the step's misses were already
+// copied into the HBM stage by sd_stage_host_rows and read from there by the attention, so
+// the promotion runs after the attention and copies each promoted row from the stage (the
+// list row that selected it, recorded by the mark kernel) instead of crossing the host link
+// a second time.  The pool state after the call is the same as in the host mode.
 #include <algorithm>
 
 #include "sd_common.cuh"
@@ -34,8 +40,11 @@ struct PromoteParams {
     int32_t* slot_map;       // [B, T]
     int32_t* pool_pos;       // [B, P]
     int32_t* hand;           // [B]
-    const uint8_t* kh;       // mapped host cache [B, Hkv, T, d]
+    const uint8_t* kh;       // mapped host cache [B, Hkv, T, d] (host mode)
     const uint8_t* vh;
+    const uint8_t* ks;       // stage [units * groups * n_idx * block, d] (staged mode)
+    const uint8_t* vs;
+    int32_t* row_of;         // [B, T] staged mode: a list row that selected the position
     uint8_t* kp;             // pool [B, Hkv, P, d]
     uint8_t* vp;
     uint32_t* mark;          // [B, W32], zero between calls
@@ -63,6 +72,9 @@ __global__ void __launch_bounds__(256) promote_mark_kernel(const PromoteParams p
             continue;
         }
         atomicOr(&p.mark[(size_t)b * p.W32 + (pos >> 5)], 1u << (pos & 31));
+        // several groups of a unit may select the same position: any one of their list rows
+        // holds the row (one KV head per unit), so whichever store lands last is right
+        if (p.row_of != nullptr) p.row_of[(size_t)b * p.T + pos] = (int)e;
     }
 }
 
@@ -205,8 +217,13 @@ __global__ void __launch_bounds__(kCopyThreads) promote_copy_kernel(const Promot
                 if (q >= per_task) continue;
                 const int which = q / (p.Hkv * pieces), rem = q % (p.Hkv * pieces);
                 const int h = rem / pieces, off = (rem % pieces) * 16;
-                const size_t src = (((size_t)b * p.Hkv + h) * p.T + t.x) * p.row_bytes + off;
-                v[u] = __ldcs(reinterpret_cast<const uint4*>((which ? p.vh : p.kh) + src));
+                if (p.ks != nullptr) {  // staged mode: one KV head per unit
+                    const size_t src = (size_t)p.row_of[(size_t)b * p.T + t.x] * p.row_bytes + off;
+                    v[u] = __ldcs(reinterpret_cast<const uint4*>((which ? p.vs : p.ks) + src));
+                } else {
+                    const size_t src = (((size_t)b * p.Hkv + h) * p.T + t.x) * p.row_bytes + off;
+                    v[u] = __ldcs(reinterpret_cast<const uint4*>((which ? p.vh : p.kh) + src));
+                }
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -231,7 +248,7 @@ __global__ void __launch_bounds__(kCopyThreads) promote_copy_kernel(const Promot
 }
 
 struct PromoteLayout {
-    size_t mark, tasks, ntask, counter, bytes;
+    size_t mark, tasks, ntask, counter, row_of, bytes;
     int W32, max_tasks;
 };
 
@@ -251,7 +268,7 @@ PromoteUnits promote_units(const sd_attend_args* a) {
     return {a->B, a->Hkv, a->per_head ? a->Hq : a->Hkv};
 }
 
-PromoteLayout promote_layout(const sd_attend_args* a) {
+PromoteLayout promote_layout(const sd_attend_args* a, bool staged) {
     PromoteLayout l{};
     const PromoteUnits u = promote_units(a);
     l.W32 = (a->T + 31) / 32;
@@ -261,7 +278,8 @@ PromoteLayout promote_layout(const sd_attend_args* a) {
     l.tasks = al256((size_t)u.units * l.W32 * 4);
     l.ntask = l.tasks + al256((size_t)u.units * l.max_tasks * sizeof(int2));
     l.counter = l.ntask + al256((size_t)u.units * 4);
-    l.bytes = l.counter + 256;
+    l.row_of = l.counter + 256;
+    l.bytes = l.row_of + (staged ? al256((size_t)u.units * a->T * 4) : 0);
     return l;
 }
 
@@ -270,45 +288,54 @@ PromoteLayout promote_layout(const sd_attend_args* a) {
 
 using namespace sd;
 
-extern "C" size_t sd_promote_rows_workspace_bytes(const sd_attend_args* a) {
-    if (validate_attend_args(a, "sd_promote_rows") != SD_OK || a->pool_rows < 1) return 0;
-    return promote_layout(a).bytes;
-}
+namespace {
 
-extern "C" sd_status sd_promote_rows(const sd_attend_args* a, int32_t* pool_pos, int32_t* hand, void* workspace,
-                                     size_t workspace_bytes, void* stream) {
+sd_status promote_impl(const sd_attend_args* a, int32_t* pool_pos, int32_t* hand, void* workspace,
+                       size_t workspace_bytes, void* stream, bool staged, const char* who) {
     clear_error();
-    sd_status vs = validate_attend_args(a, "sd_promote_rows");
+    sd_status vs = validate_attend_args(a, who);
     if (vs != SD_OK) return vs;
-    SD_REQUIRE(a->idx != nullptr && a->slot_map != nullptr, "sd_promote_rows: needs idx and slot_map");
-    SD_REQUIRE(a->pool_rows >= 1, "sd_promote_rows: needs a pool (pool_rows >= 1)");
-    SD_REQUIRE(a->k_host && a->v_host && a->k_cache && a->v_cache && pool_pos && hand,
-               "sd_promote_rows: needs k_host, v_host, the pool (k_cache, v_cache), pool_pos and hand");
-    SD_REQUIRE(aligned16(a->k_host) && aligned16(a->v_host) && aligned16(a->k_cache) && aligned16(a->v_cache),
-               "sd_promote_rows: K/V pointers must be 16-byte aligned");
-    SD_REQUIRE(a->B <= 65535, "sd_promote_rows: B must be <= 65535");
+    SD_REQUIRE(a->idx != nullptr && a->slot_map != nullptr, "%s: needs idx and slot_map", who);
+    SD_REQUIRE(a->pool_rows >= 1, "%s: needs a pool (pool_rows >= 1)", who);
+    SD_REQUIRE(a->k_cache && a->v_cache && pool_pos && hand, "%s: needs the pool (k_cache, v_cache), pool_pos and hand",
+               who);
+    SD_REQUIRE(aligned16(a->k_cache) && aligned16(a->v_cache), "%s: pool pointers must be 16-byte aligned", who);
+    if (staged) {
+        SD_REQUIRE(a->slot_per_head == 1, "%s: needs a slot map per (sequence, KV head)", who);
+        SD_REQUIRE(a->k_stage && a->v_stage && aligned16(a->k_stage) && aligned16(a->v_stage),
+                   "%s: needs k_stage and v_stage (16-byte aligned)", who);
+    } else {
+        SD_REQUIRE(a->k_host && a->v_host, "%s: needs k_host and v_host", who);
+        SD_REQUIRE(aligned16(a->k_host) && aligned16(a->v_host), "%s: host K/V must be 16-byte aligned", who);
+    }
+    SD_REQUIRE(a->B <= 65535, "%s: B must be <= 65535", who);
     if (a->B == 0 || a->n_idx == 0) return SD_OK;
-    const PromoteLayout l = promote_layout(a);
+    const PromoteLayout l = promote_layout(a, staged);
     SD_REQUIRE(workspace != nullptr && workspace_bytes >= l.bytes && aligned16(workspace),
-               "sd_promote_rows: a 16-byte aligned workspace of %zu bytes is needed (got %zu)", l.bytes,
-               workspace_bytes);
+               "%s: a 16-byte aligned workspace of %zu bytes is needed (got %zu)", who, l.bytes, workspace_bytes);
     PromoteParams p{};
     p.idx = a->idx;
     p.slot_map = const_cast<int32_t*>(a->slot_map);
     p.pool_pos = pool_pos;
     p.hand = hand;
-    p.kh = mapped_host_ptr(a->k_host);
-    p.vh = mapped_host_ptr(a->v_host);
-    SD_REQUIRE(p.kh && p.vh, "sd_promote_rows: k_host/v_host must be pinned, mapped host memory");
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (staged) {
+        p.ks = static_cast<const uint8_t*>(a->k_stage);
+        p.vs = static_cast<const uint8_t*>(a->v_stage);
+        p.row_of = reinterpret_cast<int32_t*>(ws + l.row_of);
+    } else {
+        p.kh = mapped_host_ptr(a->k_host);
+        p.vh = mapped_host_ptr(a->v_host);
+        SD_REQUIRE(p.kh && p.vh, "%s: k_host/v_host must be pinned, mapped host memory", who);
+    }
     p.kp = static_cast<uint8_t*>(const_cast<void*>(a->k_cache));
     p.vp = static_cast<uint8_t*>(const_cast<void*>(a->v_cache));
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.mark = reinterpret_cast<uint32_t*>(ws + l.mark);
     p.tasks = reinterpret_cast<int2*>(ws + l.tasks);
     p.ntask = reinterpret_cast<int32_t*>(ws + l.ntask);
     p.counter = reinterpret_cast<uint32_t*>(ws + l.counter);
     const PromoteUnits u = promote_units(a);
-    SD_REQUIRE(u.units <= 65535, "sd_promote_rows: %d units (sequences, or sequence x KV head) exceed 65535", u.units);
+    SD_REQUIRE(u.units <= 65535, "%s: %d units (sequences, or sequence x KV head) exceed 65535", who, u.units);
     p.B = u.units;
     p.groups = u.groups;
     p.n_idx = a->n_idx;
@@ -320,14 +347,34 @@ extern "C" sd_status sd_promote_rows(const sd_attend_args* a, int32_t* pool_pos,
     p.W32 = l.W32;
     p.max_tasks = l.max_tasks;
     p.err = a->err_word;
-    cudaStream_t st = as_stream(stream);
     const long marks = (long)p.B * p.groups * a->n_idx * a->block;
+    SD_REQUIRE(!staged || marks < (1L << 31), "%s: selected rows must be < 2^31", who);
+    cudaStream_t st = as_stream(stream);
     const int mgrid = (int)std::min<long>((marks + 255) / 256, (long)num_sms() * 8);
-    SD_CUDA_CHECK(launch_pdl(promote_mark_kernel, dim3((unsigned)mgrid), dim3(256), 0, st, p),
-                  "sd_promote_rows: mark launch");
-    SD_CUDA_CHECK(launch_pdl(promote_plan_kernel, dim3((unsigned)p.B), dim3(kPlanThreads), 0, st, p),
-                  "sd_promote_rows: plan launch");
-    SD_CUDA_CHECK(launch_pdl(promote_copy_kernel, dim3((unsigned)num_sms()), dim3(kCopyThreads), 0, st, p),
-                  "sd_promote_rows: copy launch");
-    return launch_status("sd_promote_rows");
+    SD_CUDA_CHECK(launch_pdl(promote_mark_kernel, dim3((unsigned)mgrid), dim3(256), 0, st, p), who);
+    SD_CUDA_CHECK(launch_pdl(promote_plan_kernel, dim3((unsigned)p.B), dim3(kPlanThreads), 0, st, p), who);
+    SD_CUDA_CHECK(launch_pdl(promote_copy_kernel, dim3((unsigned)num_sms()), dim3(kCopyThreads), 0, st, p), who);
+    return launch_status(who);
+}
+
+}  // namespace
+
+extern "C" size_t sd_promote_rows_workspace_bytes(const sd_attend_args* a) {
+    if (validate_attend_args(a, "sd_promote_rows") != SD_OK || a->pool_rows < 1) return 0;
+    return promote_layout(a, false).bytes;
+}
+
+extern "C" sd_status sd_promote_rows(const sd_attend_args* a, int32_t* pool_pos, int32_t* hand, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+    return promote_impl(a, pool_pos, hand, workspace, workspace_bytes, stream, false, "sd_promote_rows");
+}
+
+extern "C" size_t sd_promote_staged_rows_workspace_bytes(const sd_attend_args* a) {
+    if (validate_attend_args(a, "sd_promote_staged_rows") != SD_OK || a->pool_rows < 1) return 0;
+    return promote_layout(a, true).bytes;
+}
+
+extern "C" sd_status sd_promote_staged_rows(const sd_attend_args* a, int32_t* pool_pos, int32_t* hand,
+                                            void* workspace, size_t workspace_bytes, void* stream) {
+    return promote_impl(a, pool_pos, hand, workspace, workspace_bytes, stream, true, "sd_promote_staged_rows");
 }
