@@ -37,15 +37,27 @@ struct StageParams {
     int slot_per_head;  // 1: slot_map is [B, kv_heads, T]
 };
 
+// Position of the n-th (from 0) set bit of `mask`, for n < popc(mask): the largest x with
+// popc(mask & (2^x - 1)) <= n, by binary search over x.
+SD_DEVINL int nth_set_bit(uint32_t mask, int n) {
+    int x = 0;
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1)
+        if (__popc(mask & ((1u << (x + step)) - 1u)) <= n) x += step;
+    return x;
+}
+
 // A warp takes the next 32 list rows from the counter (one per lane), resolves each to its
 // host row or to nothing (pooled or empty), and copies only the misses, rows_per_chunk rows
-// (kStPieces 16-byte pieces per lane, all loads before any store) at a time.
-__global__ void __launch_bounds__(kStThreads, 1) stage_host_rows_kernel(const StageParams p) {
-    __shared__ int s_hr[kStThreads / 32][32];  // per warp: the misses' host rows, in lane order
-    __shared__ int s_f[kStThreads / 32][32];   // and their list rows
+// (kStPieces 16-byte pieces per lane, all loads before any store) at a time; a piece's miss
+// is found in the ballot of misses and its rows are shuffled from the lane that resolved it.
+// No shared memory, and registers capped at 80 (the bound's 3 CTAs; the grid has one per SM):
+// the kernel runs beside the indexer, whose CTAs need most of an SM's shared memory, and
+// beside the attention.
+__global__ void __launch_bounds__(kStThreads, 3) stage_host_rows_kernel(const StageParams p) {
     pdl_wait();  // idx (and the slot map) may come from the preceding kernel
     pdl_launch_dependents();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int ppr = p.row_bytes / 16;  // pieces per K (or V) row
     const int C = p.rows_per_chunk;    // C * 2 * ppr == 32 * kStPieces
     const int nchunks = (p.total_rows + 31) / 32;
@@ -83,36 +95,31 @@ __global__ void __launch_bounds__(kStThreads, 1) stage_host_rows_kernel(const St
         }
         const uint32_t miss = __ballot_sync(0xffffffffu, host_row >= 0);
         if (miss == 0u) continue;
-        if (host_row >= 0) {
-            const int rank = __popc(miss & ((1u << lane) - 1u));
-            s_hr[warp][rank] = host_row;
-            s_f[warp][rank] = f;
-        }
-        __syncwarp();
         const int n_miss = __popc(miss);
         for (int m0 = 0; m0 < n_miss; m0 += C) {
-            // piece q = lane + 32 i of the batch: miss m0 + q / (2 ppr), K for the first ppr
-            // pieces of a row and V for the rest, 16 bytes at (q mod ppr) * 16
+            // piece q = lane + 32 i of the batch: miss m0 + q / (2 ppr) (resolved by the lane
+            // holding the miss's bit), K for the first ppr pieces of a row and V for the rest,
+            // 16 bytes at (q mod ppr) * 16
             uint4 v[kStPieces];
 #pragma unroll
             for (int i = 0; i < kStPieces; ++i) {
                 const int q = lane + 32 * i, m = m0 + q / (2 * ppr), w = q % (2 * ppr);
+                const int hr = __shfl_sync(0xffffffffu, host_row, nth_set_bit(miss, m < n_miss ? m : 0));
                 if (m < n_miss) {
-                    const uint8_t* src =
-                        (w < ppr ? p.kh : p.vh) + (size_t)s_hr[warp][m] * p.row_bytes + (w % ppr) * 16;
-                    v[i] = __ldcs(reinterpret_cast<const uint4*>(src));
+                    const uint8_t* s_ = (w < ppr ? p.kh : p.vh) + (size_t)hr * p.row_bytes + (w % ppr) * 16;
+                    v[i] = __ldcs(reinterpret_cast<const uint4*>(s_));
                 }
             }
 #pragma unroll
             for (int i = 0; i < kStPieces; ++i) {
                 const int q = lane + 32 * i, m = m0 + q / (2 * ppr), w = q % (2 * ppr);
+                const int fr = __shfl_sync(0xffffffffu, f, nth_set_bit(miss, m < n_miss ? m : 0));
                 if (m < n_miss) {
-                    uint8_t* dst = (w < ppr ? p.ks : p.vs) + (size_t)s_f[warp][m] * p.row_bytes + (w % ppr) * 16;
+                    uint8_t* dst = (w < ppr ? p.ks : p.vs) + (size_t)fr * p.row_bytes + (w % ppr) * 16;
                     *reinterpret_cast<uint4*>(dst) = v[i];
                 }
             }
         }
-        __syncwarp();  // the lists are rewritten by the next chunk
     }
     // the last CTA to finish leaves the counter at zero for the next call
     __syncthreads();
