@@ -1311,7 +1311,8 @@ def main(argv=None):
     ap.add_argument("--separate", action="store_true",
                     help="run top-k and gather-attend as two launches instead of the fused one")
     ap.add_argument("--no-lookahead", action="store_true",
-                    help="multi-layer tiered workloads: run every layer's calls in order on one stream")
+                    help="lookahead and cached tiered workloads: run every call in order on one stream "
+                         "(no selection of the next layer, or promotion of the previous step, beside others)")
     ap.add_argument("--tiered-path", choices=("staged", "fused"), default="staged",
                     help="tiered workloads: stage the selected host rows into HBM with one copy kernel "
                          "before the attention (staged), or read them inside the fused select/attend")
