@@ -214,3 +214,71 @@ def test_promote_staged_validation(lib):
     assert b"workspace" in lib.sd_last_error_message()
     a.pool_rows = 0
     assert lib.sd_promote_staged_rows_workspace_bytes(ctypes.byref(a)) == 0
+
+
+def test_index_score_heads_validation(lib):
+    dummy = ctypes.c_void_p(16)
+    # negative sizes, mixed f16/bf16 operands, too many query columns, unsupported d
+    assert lib.sd_index_score_heads(dummy, 1, dummy, 1, -1, 8, 4, 4096, 128, dummy, None, None, None) == 1
+    assert lib.sd_index_score_heads(dummy, 2, dummy, 1, 2, 8, 4, 4096, 128, dummy, None, None, None) == 1
+    assert b"F16" in lib.sd_last_error_message()
+    assert lib.sd_index_score_heads(dummy, 1, dummy, 1, 2, 8, 17, 4096, 128, dummy, None, None, None) == 1
+    assert lib.sd_index_score_heads(dummy, 1, dummy, 1, 2, 8, 4, 4096, 96, dummy, None, None, None) == 2
+    # nothing to do
+    assert lib.sd_index_score_heads(None, 1, None, 1, 0, 8, 4, 4096, 128, None, None, None, None) == 0
+
+
+def test_window_calls_validation(lib):
+    # the window count is host arithmetic: ceil((N - kernel) / stride) + 1 windows, 0 below one
+    assert lib.sd_window_count(32768, 32, 16) == 2047
+    assert lib.sd_window_count(64, 32, 16) == 3
+    assert lib.sd_window_count(-1, 32, 16) == 0
+    dummy = ctypes.c_void_p(16)
+    assert lib.sd_window_max(dummy, 4, 1024, 16, 32, dummy, None, None) == 1  # stride > kernel
+    assert lib.sd_window_max(dummy, 4, 1 << 16, 2048, 16, dummy, None, None) == 1  # kernel > 1024
+    assert lib.sd_window_max(None, 0, 1024, 32, 16, None, None, None) == 0
+    assert lib.sd_window_union(dummy, 4, 8, 1024, 24, 16, dummy, 16, None, None) == 1  # kernel % stride
+    assert lib.sd_window_union(dummy, 4, 8, 1000, 32, 16, dummy, 16, None, None) == 1  # N % stride
+    assert lib.sd_window_union(dummy, 4, 8, 1024, 32, 16, dummy, 15, None, None) == 1  # max_segs < k*2
+    assert b"max_segs" in lib.sd_last_error_message()
+    assert lib.sd_window_union(None, 0, 8, 1024, 32, 16, None, 16, None, None) == 0
+
+
+def test_importance_and_tier_validation(lib):
+    dummy = ctypes.c_void_p(16)
+    f64 = ctypes.c_double
+    # Hq not a multiple of Hkv; dense mode needs n_idx * block == T; null outputs
+    assert lib.sd_score_accumulate(dummy, dummy, None, 2, 1, 28, 3, 64, 1, 64, f64(0.1), dummy, None, None) == 1
+    assert lib.sd_score_accumulate(dummy, dummy, None, 2, 1, 28, 4, 64, 1, 65, f64(0.1), dummy, None, None) == 1
+    assert b"dense" in lib.sd_last_error_message()
+    assert lib.sd_score_accumulate(None, dummy, dummy, 2, 1, 28, 4, 64, 1, 4096, f64(0.1), dummy, None, None) == 1
+    assert lib.sd_score_accumulate(None, None, None, 0, 1, 28, 4, 64, 1, 64, f64(0.1), None, None, None) == 0
+    frac = (f64 * 3)
+    assert lib.sd_tier_classify_workspace_bytes(2, 65536) == 0
+    assert lib.sd_tier_classify(dummy, 2, 64, frac(0.2, 0.6, 1.5), 0, 0, dummy, dummy, None, 0, None) == 1
+    assert lib.sd_tier_classify(dummy, 2, 64, frac(0.6, 0.2, 0.9), 0, 0, dummy, dummy, None, 0, None) == 1
+    assert b"nondecreasing" in lib.sd_last_error_message()
+    assert lib.sd_tier_classify(dummy, 2, 64, None, 0, 0, dummy, dummy, None, 0, None) == 1
+    assert lib.sd_tier_classify(dummy, 2, 64, frac(0.2, 0.6, 0.9), -1, 0, dummy, dummy, None, 0, None) == 1
+    assert lib.sd_tier_classify(None, 0, 64, frac(0.2, 0.6, 0.9), 0, 0, None, None, None, 0, None) == 0
+    # int8 rows: bad dtype, unsupported d, null outputs, nothing to do
+    assert lib.sd_quantize_rows_int8(dummy, 7, dummy, 2, 4, 64, 128, dummy, dummy, None) == 1
+    assert lib.sd_quantize_rows_int8(dummy, 1, dummy, 2, 4, 64, 96, dummy, dummy, None) == 2
+    assert lib.sd_quantize_rows_int8(dummy, 1, dummy, 2, 4, 64, 128, None, dummy, None) == 1
+    assert lib.sd_quantize_rows_int8(None, 1, None, 0, 4, 64, 128, None, None, None) == 0
+
+
+def test_noalloc_validation(lib):
+    from top_sparse_decode_gqa_gb300.binding import sd_attend_args
+    assert lib.sd_gather_attend_noalloc(None, None) == 1
+    a = sd_attend_args()
+    a.q = a.k_cache = a.v_cache = a.out = a.lse = a.idx = 16
+    a.dtype, a.B, a.V, a.Hq, a.Hkv, a.d, a.T = 1, 64, 8, 32, 8, 128, 1 << 16
+    a.pool_rows, a.n_idx, a.block, a.scale, a.splits = 1 << 16, 4096, 1, 0.1, 64
+    # 512 groups x 64 splits x 32 query rows of (d + 2) floats: far beyond the 16 MiB scratch
+    assert lib.sd_gather_attend_workspace_bytes(ctypes.byref(a)) > 16 << 20
+    assert lib.sd_gather_attend_noalloc(ctypes.byref(a), None) == 1
+    assert b"static scratch" in lib.sd_last_error_message()
+    # an invalid request reports the gather-attend's own error
+    a.d = 96
+    assert lib.sd_gather_attend_noalloc(ctypes.byref(a), None) in (1, 2)
