@@ -198,28 +198,41 @@ class StepMarks:
         return [a.elapsed_time(b) for a, b in self.dom]
 
 
+def step_supported(w) -> bool:
+    """Whether sd_decode_step (the whole step in one persistent launch) takes this workload."""
+    return (w.resident_frac >= 1.0 and w.dtype == "bf16" and w.d == 128 and w.dI == 128 and w.V <= 8
+            and w.G * w.V <= 16 and w.N <= 32768 and w.N % 4 == 0)
+
+
 class SparseDecodeStep:
-    """One sparse decode step, inputs resident: the indexer, then either the fused select +
-    attend launch (bf16 token-level workloads) or the separate top-k and gather-attend
-    launches (block-level selection, fp32, or on request).  For a
-    tiered workload the full K/V cache stays in pinned host memory and only the resident
-    share sits in the HBM pool; there the default path copies the selected host rows into
-    an HBM stage with one copy kernel spread over every SM (sd_stage_host_rows) between the
-    top-k and the attention."""
+    """One sparse decode step, inputs resident.  Paths: "step" runs the indexer, the top-k and
+    the gather-attend in one persistent launch (sd_decode_step; the default where it applies:
+    bf16, K/V in HBM); "select_attend" runs the indexer, then the fused select + attend launch
+    (token-level selection); "separate" runs the indexer, the top-k and the gather-attend as
+    three launches.  For a tiered workload the full K/V cache stays in pinned host memory and
+    only the resident share sits in the HBM pool; there the default path copies the selected
+    host rows into an HBM stage with one copy kernel spread over every SM
+    (sd_stage_host_rows) between the top-k and the attention."""
 
-    dominant = "sd_index_score"
-
-    def __init__(self, w, x, device, separate=False, tiered_path="staged"):
+    def __init__(self, w, x, device, path="auto", tiered_path="staged"):
         import torch
         from top_sparse_decode_gqa_gb300 import binding as sd
         self.sd, self.w, self.dev = sd, w, device
         self.tiered = w.resident_frac < 1.0
-        self.staged = self.tiered and tiered_path == "staged" and not separate
+        if path == "auto":
+            path = "select_attend" if w.dtype == "bf16" and w.block == 1 and not self.tiered else "separate"
+        if path == "step" and not step_supported(w):
+            raise ValueError(f"sd_decode_step does not take {w.name}")
+        self.path = path
+        self.step_kernel = path == "step"
+        self.staged = self.tiered and tiered_path == "staged" and path == "separate"
         # block selection picks few entries but many rows per group: the separate top-k and
         # gather-attend spread the rows over the whole GPU, the fused kernel over one cluster
-        self.fused = w.dtype == "bf16" and not separate and not self.staged and w.block == 1
-        self.phases = () if self.fused else ("after_topk", "after_stage") if self.staged else ("after_topk",)
-        self.launches_per_step = 2 if self.fused else 4 if self.staged else 3
+        self.fused = path == "select_attend" or (self.tiered and tiered_path == "fused")
+        self.dominant = "sd_decode_step" if self.step_kernel else "sd_index_score"
+        self.phases = (() if self.fused or self.step_kernel else ("after_topk", "after_stage") if self.staged
+                       else ("after_topk",))
+        self.launches_per_step = 1 if self.step_kernel else 2 if self.fused else 4 if self.staged else 3
         self.q_idx, self.k_idx, self.q = (x[k].to(device) for k in ("q_idx", "k_idx", "q"))
         self.scores = torch.empty(w.B, w.Hkv, w.N, dtype=torch.float32, device=device)
         self.idx = torch.empty(w.B, w.Hkv, w.k, dtype=torch.int32, device=device)
@@ -245,6 +258,11 @@ class SparseDecodeStep:
         if w.block > 1:  # pooled block keys, built once (cache fill): fp16 to meet an fp16 query
             self.keys = sd.sd_block_pool(self.k_idx, w.block, dtype=self.q_idx.dtype
                                          if self.q_idx.dtype == torch.float16 else torch.float32)
+        if self.step_kernel:
+            self.step_args, _, _, self.out, self.lse = sd.make_decode_step_args(
+                self.q_idx, self.keys, self.q, self.k_cache, self.v_cache, w.k, block=w.block, scores=self.scores,
+                idx=self.idx, err_word=self.err)
+            self.step_ws = sd.decode_step_workspace(self.step_args, device)
         self.host_rows = None
 
     dominant_per_step = 1
@@ -254,6 +272,12 @@ class SparseDecodeStep:
         if m is not None:
             m.start.record()
             m.before(0)
+        if self.step_kernel:
+            sd.sd_decode_step(self.step_args)
+            if m is not None:
+                m.after(0)
+                m.end.record()
+            return
         sd.sd_index_score(self.q_idx, self.keys, self.scores, self.err, key_hist=self.key_hist)
         if m is not None:
             m.after(0)
@@ -293,6 +317,8 @@ class SparseDecodeStep:
         q_bytes = w.B * w.V * w.Hq * w.d * e
         out_bytes = w.B * w.V * w.Hq * (w.d + 1) * 4 + w.B * w.Hkv * w.k * 4
         hbm = key_bytes + q_idx_bytes + (kv_rows - host_rows) * row_bytes + q_bytes + out_bytes
+        if self.step_kernel:  # the one launch moves the whole step, the scores written included
+            return {"dominant": hbm + score_bytes, "hbm": hbm, "host": 0}
         return {"dominant": key_bytes + q_idx_bytes + score_bytes, "hbm": hbm,
                 "host": host_rows * row_bytes}
 
@@ -857,7 +883,7 @@ class DenseScoringStep:
                 "host": 0}
 
 
-def make_step(w, x, device, separate=False, tiered_path="staged", lookahead=True):
+def make_step(w, x, device, path="auto", tiered_path="staged", lookahead=True):
     if w.drift_steps > 0:
         return CachedTieredStep(w, x, device, concurrent=lookahead)
     if w.layer_indexers:
@@ -870,7 +896,7 @@ def make_step(w, x, device, separate=False, tiered_path="staged", lookahead=True
         return WindowStep(w, x, device)
     if w.per_head:
         return HeadsStep(w, x, device)
-    return SparseDecodeStep(w, x, device, separate, tiered_path)
+    return SparseDecodeStep(w, x, device, path, tiered_path)
 
 
 def host_link_gbs(device, nbytes=256 << 20, reps=5):
@@ -913,7 +939,8 @@ def run_ours(args):
         dist.barrier()
     w = WORKLOADS[args.workload]
     x = generate(w)
-    step = make_step(w, x, device, args.separate, args.tiered_path, not args.no_lookahead)
+    step = make_step(w, x, device, "separate" if args.separate else args.path, args.tiered_path,
+                     not args.no_lookahead)
     props = torch.cuda.get_device_properties(device)
     flush = torch.empty(2 * max(int(getattr(props, "L2_cache_size", 0)), 128 << 20), dtype=torch.uint8,
                         device=device)
@@ -971,7 +998,9 @@ def run_ours(args):
     by = step.bytes()
     dom_s = statistics.mean(dom_ms) / 1e3
     achieved = by["dominant"] / dom_s / 1e9
-    if isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep, LookaheadStep, CachedTieredStep)):
+    if isinstance(step, SparseDecodeStep) and step.step_kernel:
+        kernel_file, kernel_tag = ("decode_step.cu", "tc_common.cuh", "sd_common.cuh"), "decode_step"
+    elif isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep, LookaheadStep, CachedTieredStep)):
         kernel_file, kernel_tag = ("index_score.cu", "index_score_tc.cu", "tc_common.cuh", "sd_common.cuh"), "index_score"
     else:
         kernel_file, kernel_tag = ("gather_attend.cu", "sd_common.cuh"), "gather_attend"
@@ -994,7 +1023,9 @@ def run_ours(args):
             t_roof += t_host
     step_roof["t_roof_us"] = round(t_roof * 1e6, 2)
     step_roof["frac"] = round(t_roof / step_s, 4)
-    if isinstance(step, SparseDecodeStep) and step.fused:
+    if isinstance(step, SparseDecodeStep) and step.step_kernel:
+        step_roof["kernel_us"] = {"decode_step": round(statistics.mean(dom_ms) * 1e3, 2)}
+    elif isinstance(step, SparseDecodeStep) and step.fused:
         tail = [m.dom[0][1].elapsed_time(m.end) for m in kmarks]
         step_roof["kernel_us"] = {"index_score": round(statistics.mean(dom_ms) * 1e3, 2),
                                   "select_attend": round(statistics.mean(tail) * 1e3, 2)}
@@ -1086,7 +1117,9 @@ def run_ours(args):
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "T": w.T,
                    "k": w.k, "block": w.block, "V": w.V, "layers": w.layers,
                    "queries_per_step": w.queries_per_step,
-                   "path": ("indexer + fused select/attend" if getattr(step, "fused", False)
+                   "path": ("indexer + top-k + gather-attend in one persistent launch (sd_decode_step)"
+                            if getattr(step, "step_kernel", False)
+                            else "indexer + fused select/attend" if getattr(step, "fused", False)
                             else "indexer + top-k + host-row staging + gather-attend"
                             if getattr(step, "staged", False)
                             else "indexer + top-k + gather-attend" if isinstance(step, SparseDecodeStep)
@@ -1309,7 +1342,11 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--separate", action="store_true",
-                    help="run top-k and gather-attend as two launches instead of the fused one")
+                    help="run the indexer, top-k and gather-attend as three launches (same as --path separate)")
+    ap.add_argument("--path", choices=("auto", "step", "select_attend", "separate"), default="auto",
+                    help="sparse decode workloads: one persistent launch (step), indexer + fused select/attend, "
+                         "or three launches; auto takes indexer + fused select/attend for token-level bf16 "
+                         "selection and three launches otherwise")
     ap.add_argument("--no-lookahead", action="store_true",
                     help="lookahead and cached tiered workloads: run every call in order on one stream "
                          "(no selection of the next layer, or promotion of the previous step, beside others)")

@@ -354,6 +354,60 @@ sd_status sd_select_attend(const float* scores, int N, uint32_t* key_hist, int32
                            const sd_attend_args* args, void* stream);
 
 /*
+ * sd_decode_step -- one whole decode step in one launch: sd_index_score, sd_topk and
+ * sd_gather_attend fused in a persistent kernel for K/V resident in HBM.
+ * [SparDA] sec. 2 "Indexador de Previsao Compacto" (one indexer head per KV group, no softmax)
+ * and item 1 (top-k blocks); [Illusion] sec. 2 "Mecanismos de Esparsidade" (exact top-k feeding
+ * a sparse decode kernel) and sec. 3C (traffic O(k*d)); [DHiSparse] "Metodologia" (the query
+ * rows of a group share every fetched row).
+ * Computes, with N = T / block:
+ *   scores [B,Hkv,N] = sd_index_score(q_idx, keys)   (max over the V queries; bit-identical)
+ *   idx [B,Hkv,n_idx] = sd_topk(scores, n_idx)       (ascending, ties to the lower index;
+ *                                                     bit-identical)
+ *   out [B,V,Hq,d], lse [B,V,Hq] = sd_gather_attend over the selected rows of k_cache/v_cache
+ *                                  (entry e covers rows e*block .. e*block + block - 1), with
+ *                                  the same definition; the summation order is the call's own
+ *                                  and depends only on (T, block, n_idx), not on the data.
+ * q_idx [B,Hkv,V,d_idx] and keys [B,Hkv,N,d_idx] both of key_dtype (SD_BF16, or SD_F16 e.g. for
+ * the pooled block keys of sd_block_pool): products and sums are fp32, exact for the
+ * integer-valued (or multiple-of-2^-6) indexer inputs sd_index_score describes.  q [B,V,Hq,d],
+ * k_cache and v_cache [B,Hkv,T,d] bf16; scores, idx, out and lse are written.
+ * Limits: d = d_idx = 128, 1 <= V <= 8, (Hq/Hkv)*V <= 16, N <= 65536, 0 <= n_idx <= N,
+ * B*Hkv*T < 2^31 (SD_ERR_UNSUPPORTED outside the first three; use the separate calls).
+ * Workspace (sd_decode_step_workspace_bytes; 256-byte aligned): task counters, per-group
+ * counters and histograms, and the attention partials.  Zero-fill it once before the first
+ * call; every call leaves it ready for the next (its counters and histograms back at zero).
+ * Calls sharing one workspace must not overlap on the GPU.  After a call that reported
+ * SD_DEVERR_TIMEOUT the workspace must be zero-filled again before the next call.
+ * lag: the scoring of group g + lag is scheduled before the attention of group g (0 =
+ * automatic); wait_limit_ns: the bound of every wait inside the kernel (0 = 1 s).
+ * The launch is a programmatic dependent of the preceding kernel in the stream (it waits for
+ * that kernel's results before reading anything).
+ */
+typedef struct {
+    const void* q_idx;        /* [B,Hkv,V,d_idx] of key_dtype */
+    const void* keys;         /* [B,Hkv,T/block,d_idx] of key_dtype */
+    sd_dtype key_dtype;       /* SD_BF16 or SD_F16 */
+    const void* q;            /* [B,V,Hq,d] bf16 */
+    const void* k_cache;      /* [B,Hkv,T,d] bf16, HBM */
+    const void* v_cache;      /* same layout as k_cache */
+    int B, V, Hq, Hkv, d, d_idx, T, block, n_idx;
+    float scale;              /* softmax scale, e.g. 1/sqrt(d) */
+    float* scores;            /* [B,Hkv,T/block] fp32, written (16-byte aligned) */
+    int32_t* idx;             /* [B,Hkv,n_idx] int32, written (may be NULL when n_idx == 0) */
+    float* out;               /* [B,V,Hq,d] fp32, written */
+    float* lse;               /* [B,V,Hq] fp32, written */
+    int32_t* err_word;        /* nullable device int32 */
+    void* workspace;          /* device scratch of workspace_bytes, zero-filled before first use */
+    size_t workspace_bytes;
+    int lag;                  /* 0 = automatic */
+    long long wait_limit_ns;  /* 0 = 1 s */
+} sd_decode_step_args;
+
+size_t sd_decode_step_workspace_bytes(const sd_decode_step_args* args);
+sd_status sd_decode_step(const sd_decode_step_args* args, void* stream);
+
+/*
  * sd_window_max -- block scores on overlapping compression windows.
  * [SparDA] "Estrategia de Treinamento": the inference block grid is a compression window of
  * `kernel` tokens moved by `stride` (32, 16), and finer scores are max-pooled onto it.

@@ -29,7 +29,7 @@ EXPORTS = (
     "sd_quantize_rows_int8", "sd_gather_attend_noalloc", "sd_select_attend", "sd_window_count",
     "sd_window_max", "sd_window_union", "sd_index_score_heads", "sd_stage_host_rows", "sd_ring_append",
     "sd_promote_rows_workspace_bytes", "sd_promote_rows", "sd_promote_staged_rows_workspace_bytes",
-    "sd_promote_staged_rows",
+    "sd_promote_staged_rows", "sd_decode_step_workspace_bytes", "sd_decode_step",
 )
 
 
@@ -53,6 +53,19 @@ class sd_attend_args(ctypes.Structure):
         ("k_stage", ctypes.c_void_p), ("v_stage", ctypes.c_void_p),
         ("ring_k", ctypes.c_void_p), ("ring_v", ctypes.c_void_p), ("ring_pos", ctypes.c_void_p),
         ("qpos", ctypes.c_void_p), ("ring_w", ctypes.c_int), ("slot_per_head", ctypes.c_int),
+    ]
+
+
+class sd_decode_step_args(ctypes.Structure):
+    _fields_ = [
+        ("q_idx", ctypes.c_void_p), ("keys", ctypes.c_void_p), ("key_dtype", ctypes.c_int),
+        ("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("V", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+        ("d", ctypes.c_int), ("d_idx", ctypes.c_int), ("T", ctypes.c_int), ("block", ctypes.c_int),
+        ("n_idx", ctypes.c_int), ("scale", ctypes.c_float),
+        ("scores", ctypes.c_void_p), ("idx", ctypes.c_void_p), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("err_word", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("lag", ctypes.c_int), ("wait_limit_ns", ctypes.c_longlong),
     ]
 
 
@@ -99,9 +112,12 @@ def lib() -> ctypes.CDLL:
         L.sd_tier_classify_workspace_bytes.restype = Z
         L.sd_tier_classify.argtypes = [P, I, I, P, I, I, P, P, P, Z, P]
         L.sd_quantize_rows_int8.argtypes = [P, I, P, I, I, I, I, P, P, P]
+        L.sd_decode_step_workspace_bytes.argtypes = [ctypes.POINTER(sd_decode_step_args)]
+        L.sd_decode_step_workspace_bytes.restype = Z
+        L.sd_decode_step.argtypes = [ctypes.POINTER(sd_decode_step_args), P]
         for name in ("sd_index_score", "sd_block_pool", "sd_topk", "sd_gather_attend",
                      "sd_score_accumulate", "sd_tier_classify", "sd_quantize_rows_int8",
-                     "sd_gather_attend_noalloc"):
+                     "sd_gather_attend_noalloc", "sd_decode_step"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -514,3 +530,65 @@ def sd_quantize_rows_int8(x: torch.Tensor, tier: torch.Tensor, codes: Optional[t
     _check(lib().sd_quantize_rows_int8(_ptr(x), _dtype_code(x), _ptr(tier), B, Hkv, T, d, _ptr(codes),
                                        _ptr(scales), _stream(stream)), "sd_quantize_rows_int8")
     return codes, scales
+
+
+def make_decode_step_args(q_idx, keys, q, k_cache, v_cache, k, *, block=1, scale=None, scores=None, idx=None,
+                          out=None, lse=None, err_word=None, lag=0, wait_limit_ns=0) -> tuple:
+    """Fill an sd_decode_step_args from tensors: q_idx [B,Hkv,V,dI] and keys [B,Hkv,T/block,dI]
+    (bf16 or fp16 alike), q [B,V,Hq,d], k_cache/v_cache [B,Hkv,T,d] bf16; returns (args, scores,
+    idx, out, lse) with the outputs allocated where not given (the workspace is set separately)."""
+    for name, t in (("q_idx", q_idx), ("keys", keys), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _dev(t, name)
+    B, Hkv, V, dI = q_idx.shape
+    N = keys.shape[2]
+    _, Vq, Hq, d = q.shape
+    T = k_cache.shape[2]
+    if Vq != V or tuple(keys.shape) != (B, Hkv, N, dI) or k_cache.shape[:2] != (B, Hkv):
+        raise ValueError("inconsistent shapes for sd_decode_step")
+    dev = q.device
+    if scores is None:
+        scores = torch.empty((B, Hkv, N), dtype=torch.float32, device=dev)
+    if idx is None:
+        idx = torch.empty((B, Hkv, k), dtype=torch.int32, device=dev)
+    if out is None:
+        out = torch.empty((B, V, Hq, d), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, V, Hq), dtype=torch.float32, device=dev)
+    a = sd_decode_step_args()
+    a.q_idx, a.keys, a.key_dtype = q_idx.data_ptr(), keys.data_ptr(), _dtype_code(keys)
+    a.q, a.k_cache, a.v_cache = q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr()
+    a.B, a.V, a.Hq, a.Hkv, a.d, a.d_idx, a.T, a.block, a.n_idx = B, V, Hq, Hkv, d, dI, T, block, k
+    a.scale = 1.0 / math.sqrt(d) if scale is None else scale
+    a.scores, a.idx, a.out, a.lse = scores.data_ptr(), idx.data_ptr(), out.data_ptr(), lse.data_ptr()
+    a.err_word = err_word.data_ptr() if err_word is not None else None
+    a.lag, a.wait_limit_ns = lag, wait_limit_ns
+    return a, scores, idx, out, lse
+
+
+def sd_decode_step_workspace_bytes(args: sd_decode_step_args) -> int:
+    return lib().sd_decode_step_workspace_bytes(ctypes.byref(args))
+
+
+def decode_step_workspace(args: sd_decode_step_args, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace for sd_decode_step calls shaped like `args`, set into args."""
+    n = max(256, sd_decode_step_workspace_bytes(args))
+    ws = torch.zeros(n, dtype=torch.uint8, device=device)
+    args.workspace, args.workspace_bytes = ws.data_ptr(), n
+    return ws
+
+
+def sd_decode_step(args: sd_decode_step_args, stream=None) -> None:
+    """Runs one sd_decode_step call described by `args` (see make_decode_step_args; the
+    workspace must be set, e.g. by decode_step_workspace)."""
+    _check(lib().sd_decode_step(ctypes.byref(args), _stream(stream)), "sd_decode_step")
+
+
+def decode_step(q_idx, keys, q, k_cache, v_cache, k, workspace=None, stream=None, **kw):
+    """Convenience wrapper: one fused decode step; returns (scores, idx, out, lse)."""
+    a, scores, idx, out, lse = make_decode_step_args(q_idx, keys, q, k_cache, v_cache, k, **kw)
+    need = sd_decode_step_workspace_bytes(a)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=q.device)
+    a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    sd_decode_step(a, stream)
+    return scores, idx, out, lse

@@ -1,0 +1,1346 @@
+// decode_step.cu -- one whole sparse decode step (indexer, top-k, gather-attend) in one
+// persistent launch.
+//
+// SparDA (gist.science summary), sec. 2 "Indexador de Previsao Compacto": one indexer head
+// per KV group scores every cached token (or block, sec. 2 item 1) with a dot product and no
+// softmax.  "Esparsidade de Contexto no Tempo de Inferencia" (gist.science summary), sec. 2:
+// exact (Oracle) top-k feeding a sparse decode kernel; sec. 3C: traffic O(k*d) instead of
+// O(N*d).  Adaptive DHiSparse (news page), "Metodologia": the query rows of a group share
+// every fetched row.  Ties in the selection go to the lower index (the pages are silent).
+//
+// Computes what sd_index_score -> sd_topk -> sd_gather_attend computes (scores and index
+// sets bit for bit; attention in its own summation order), for K/V resident in HBM.
+//
+// The work of a step is a list of tasks taken from one device counter by every CTA (one
+// persistent CTA per SM, a few tasks per claim):
+//   scoring task (g, part)   128 indexer keys of KV group g, as two 16 KB stages of 64 keys
+//                            (tiled TMA, 128-byte swizzle) -> scores (mma.sync m16n8k16;
+//                            products of integer-valued keys and queries are exact, so are the
+//                            fp32 sums) and their 11-bit order-key digits added to the group's
+//                            histogram;
+//   attention task (g, part) up to 256 selected rows of group g, as eight stages of 32 K and V
+//                            rows (tiled TMA for whole 32-row runs of a block, 16-byte cp.async
+//                            for scattered rows): exact online softmax over them for all G*V
+//                            query rows of the group, written as partials (m, l, O).
+// The list puts the scoring tasks of group g + L before the attention tasks of group g, so the
+// attention of early groups overlaps the scoring of later ones (L, the lag, covers the time a
+// group's selection takes).  The CTA that claims a group's last scoring task owns its top-k:
+// it runs it once every scoring stage of the group is counted; the group's attention tasks
+// wait (bounded) for it.  The CTA that claims a group's last attention task likewise merges
+// the group's partials, in a fixed order, once every attention stage is counted.  The owners
+// are whichever CTAs happened to claim those tasks, so the selections spread over the GPU.
+//
+// Warp roles in a CTA: warp 4 produces (claims tasks, fills an 8-slot ring of 16 KB stages);
+// warps 0-3 consume, warp w taking stages w, w+4, w+8, ... alone (so four stages are worked on
+// at once while four more load) and posting a record per stage; warps 5-8 count the records
+// into the device-scope counters (fire-and-forget releases, so no role waits on a device-scope
+// fence) and run the selections and merges this CTA owns.  Every wait is bounded; a wait that
+// runs out sets SD_DEVERR_TIMEOUT, every role leaves at its next wait, and the CTA lets its
+// copies in flight land before it exits.
+#include <algorithm>
+#include <cmath>
+
+#include "sd_host.h"
+#include "tc_common.cuh"
+
+namespace sd {
+namespace {
+
+constexpr int kDsCons = 4;                           // consumer warps
+constexpr int kDsProd = kDsCons;                     // producer warp
+constexpr int kDsSel0 = kDsCons + 1;                 // first bookkeeping / selection warp
+constexpr int kDsSelW = 4;                           // bookkeeping / selection warps
+constexpr int kDsThreads = 32 * (kDsCons + 1 + kDsSelW);
+constexpr int kDsST = 32 * kDsSelW;                  // selection threads
+constexpr int kDsStages = 2 * kDsCons;               // ring slots: two per consumer warp
+constexpr int kDsData = 16384;                       // keys, or K then V rows, of one stage
+constexpr int kDsQSlot = 4096;                       // the stage's query rows (<= 16 of 256 B)
+constexpr int kDsStage = kDsData + kDsQSlot;
+constexpr int kDsKeyRows = 64;                       // indexer keys per scoring stage
+constexpr int kDsScoreStages = 2;                    // stages per scoring task
+constexpr int kDsTaskKeys = kDsKeyRows * kDsScoreStages;
+constexpr int kDsRows = 32;                          // K/V rows per attention stage
+constexpr int kDsTaskStages = 8;                     // stages per attention task
+constexpr int kDsTaskRows = kDsRows * kDsTaskStages;  // selected rows per attention task
+constexpr int kDsSub = 4;                            // partials per attention task (stage index mod 4)
+constexpr int kDsBins = 2048;                        // 11-bit digits of the order key
+constexpr int kDsCand = 1024;                        // candidates kept in shared memory
+constexpr int kDsMaxN = 32768;                       // scores per group the selection handles
+constexpr int kDsMaxR = 16;                          // query rows per group
+constexpr int kDsRec = 64;                           // bookkeeping records in flight
+constexpr int kDsJobs = 64;                          // owned selections / merges in flight
+constexpr int kDsChunk = 4096;                       // scores per chunk of a pass over them
+constexpr int kDsClaim = 4;                          // tasks a producer claims per atomic
+constexpr int kDsSelScratch = (kDsBins * 4 + 2 * (kDsMaxN / 8) + 2 * kDsCand * 4) / 8;  // float2 slots
+constexpr int kDsMaxMerge = kDsSelScratch - kDsMaxR;  // (partial, row) pairs a merge takes
+static_assert(kDsChunk == 32 * kDsST, "a pass gives each selection thread one bitmap word per chunk");
+
+enum : int { kTaskScore = 0, kTaskAttend = 1, kTaskEnd = 2 };
+
+struct StageMeta {
+    int kind, g, task, j0, nrows, sgi, nst, pad;
+    uint32_t valid, pad1, pad2, pad3;
+};
+
+struct DsLayout {
+    static constexpr int oHist = kDsStages * kDsStage;        // u32[2048]
+    static constexpr int oSel = oHist + kDsBins * 4;          // u32[kDsMaxN / 32]
+    static constexpr int oTie = oSel + kDsMaxN / 8;           // u32[kDsMaxN / 32]
+    static constexpr int oCandIdx = oTie + kDsMaxN / 8;       // i32[kDsCand]
+    static constexpr int oCandKey = oCandIdx + kDsCand * 4;   // u32[kDsCand]
+    static constexpr int oChunk = oCandKey + kDsCand * 4;     // f32[2][kDsChunk]
+    static constexpr int oScore = oChunk + 2 * kDsChunk * 4;  // f32[4][64] per consumer warp
+    static constexpr int oMeta = oScore + kDsCons * 64 * 4;   // StageMeta[kDsStages]
+    static constexpr int oBars = oMeta + kDsStages * (int)sizeof(StageMeta);
+    // full[S], empty[S], rec_full[R], rec_free[R], chunk[2]
+    static constexpr int kBars = 2 * kDsStages + 2 * kDsRec + 2;
+    static constexpr int oRec = oBars + kBars * 8;            // int2[kDsRec]
+    static constexpr int oJobs = oRec + kDsRec * 8;           // int[2][kDsJobs]: selections, merges
+    static constexpr int oMisc = oJobs + 2 * kDsJobs * 4;     // flags, ring indices, broadcast
+    static constexpr int kMisc = 256;
+    static constexpr int kBytes = oMisc + kMisc + 1024;       // + slack for 1024-byte alignment
+    static_assert(kDsStage % 1024 == 0, "stages must stay 1024-byte aligned (128-byte swizzle)");
+    static_assert(oChunk - oHist == kDsSelScratch * 8, "the selection scratch is one area");
+    static_assert(kBytes <= 232448, "shared memory per CTA");
+};
+
+struct DsParams {
+    const uint8_t* q_idx;  // [NG, V, 128] 16-bit
+    const uint8_t* q;      // [B, V, Hq, 128] bf16
+    const uint8_t* kc;     // [NG * T, 128] bf16
+    const uint8_t* vc;
+    float* scores;         // [NG, N]
+    int32_t* idx;          // [NG, k]
+    float* out;            // [B, V, Hq, 128]
+    float* lse;            // [B, V, Hq]
+    int32_t* err;
+    uint32_t* ctrl;        // [0] next task, [1] CTAs finished
+    uint32_t* gstate;      // [NG][4]: scoring stages done, attention stages done, selection ready
+    uint32_t* hist;        // [NG][2048]
+    float* part_o;         // [NG][AG * kDsSub][R][128]
+    float* part_ml;        // [NG][AG * kDsSub][R][2]
+    int B, V, Hq, Hkv, G, R, T, N, k, block, NG, SG, AG, L, n_rows;
+    int SGS, AGS;          // scoring / attention stages per group (the counters' targets)
+    int tma_blocks;        // block % 32 == 0: a stage's 32 rows are one contiguous run
+    float scale_log2;
+    unsigned long long wait_ns;
+    uint32_t total;
+};
+
+struct Task {
+    int kind, g, part;
+};
+
+// Task t of the list: units u = 0 .. NG + L - 1, unit u holding the scoring tasks of group u
+// (u < NG) and then the attention tasks of group u - L (u >= L).
+SD_DEVINL Task decode_task(const DsParams& p, uint32_t t) {
+    const uint32_t a = (uint32_t)p.L * (uint32_t)p.SG;
+    if (t < a) return {kTaskScore, (int)(t / p.SG), (int)(t % p.SG)};
+    t -= a;
+    const uint32_t u = (uint32_t)(p.SG + p.AG);
+    const uint32_t b = (uint32_t)(p.NG - p.L) * u;
+    if (t < b) {
+        const int uu = p.L + (int)(t / u), r = (int)(t % u);
+        if (r < p.SG) return {kTaskScore, uu, r};
+        return {kTaskAttend, uu - p.L, r - p.SG};
+    }
+    t -= b;
+    return {kTaskAttend, p.NG - p.L + (int)(t / p.AG), (int)(t % p.AG)};
+}
+
+// Stages of attention task `part` (at least one, for an empty selection).
+SD_DEVINL int task_stages(const DsParams& p, int part) {
+    const int rows = max(0, min(kDsTaskRows, p.n_rows - part * kDsTaskRows));
+    return rows > 0 ? (rows + kDsRows - 1) / kDsRows : 1;
+}
+
+// A bounded mbarrier wait that also gives up as soon as another role raised the abort flag.
+SD_DEVINL bool ds_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag, uint64_t limit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > limit) return false;
+        }
+    }
+}
+
+// Lane 0 waits (bounded) and the warp follows its result; on success every lane then observes
+// the completed phase itself (acquire), which cannot have moved on: the next phase needs this
+// warp first.
+SD_DEVINL bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint64_t limit) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = ds_wait(bar, parity, abort_flag, limit);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (ok) (void)mbar_try_wait(bar, parity);
+    else *abort_flag = 1;
+    return ok;
+}
+
+// Byte offset of 16-byte chunk c (0..15 over a 128-element bf16 row) of row r in a stage
+// tile of `rows` rows stored as two 64-column halves with the 128-byte swizzle.
+SD_DEVINL uint32_t swz(int rows, int r, int c) {
+    return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// ------------------------------------------------------------------ consumers: scoring
+
+// Scores of the stage's 64 keys against the V query rows of the group (max over V), one warp:
+// written to the warp's 64-float buffer.
+template <bool F16>
+SD_DEVINL void score_tile(const uint8_t* st, int lane, int V, float* sbuf) {
+    const uint32_t kb = smem_addr(st), qb = smem_addr(st + kDsData);
+    float acc[4][4];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ks += 2) {
+        // B = q^T: matrices (query rows 0-7) x (dims 16ks + 0..7, +8..15, 16(ks+1) + 0..7, +8..15)
+        uint32_t b[4];
+        ldsm_x4(qb + (lane & 7) * 256 + (ks * 16 + (lane >> 3) * 8) * 2, b[0], b[1], b[2], b[3]);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                const int row = 16 * mt + (lane & 15);
+                const int chunk = 2 * (ks + kk) + (lane >> 4);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(kb + swz(kDsKeyRows, row, chunk), a0, a1, a2, a3);
+                if constexpr (F16)
+                    mma_f16_16816(acc[mt], a0, a1, a2, a3, b[2 * kk], b[2 * kk + 1]);
+                else
+                    mma_bf16_16816(acc[mt], a0, a1, a2, a3, b[2 * kk], b[2 * kk + 1]);
+            }
+    }
+    const int g8 = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+        float v0 = -INFINITY, v1 = -INFINITY;  // keys g8 and g8 + 8 of this M tile
+        if (2 * t4 < V) {
+            v0 = acc[mt][0];
+            v1 = acc[mt][2];
+        }
+        if (2 * t4 + 1 < V) {
+            v0 = fmaxf(v0, acc[mt][1]);
+            v1 = fmaxf(v1, acc[mt][3]);
+        }
+        v0 = fmaxf(v0, __shfl_xor_sync(0xffffffffu, v0, 1));
+        v0 = fmaxf(v0, __shfl_xor_sync(0xffffffffu, v0, 2));
+        v1 = fmaxf(v1, __shfl_xor_sync(0xffffffffu, v1, 1));
+        v1 = fmaxf(v1, __shfl_xor_sync(0xffffffffu, v1, 2));
+        if (t4 == 0) {
+            sbuf[16 * mt + g8] = v0;
+            sbuf[16 * mt + g8 + 8] = v1;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ consumers: attention
+
+struct AttAcc {
+    float o[16][4];    // the 128 output columns: n-tiles of 8, C fragments
+    float m[2], l[2];  // query rows g8 and g8 + 8 (base-2 units)
+};
+
+// Query A fragments of the 16 (padded) query rows for the 8 k-steps of d = 128; rows >= R zero.
+SD_DEVINL void load_q_frags(const uint8_t* st, int lane, int R, uint32_t (&qf)[8][4]) {
+    const uint32_t qb = smem_addr(st + kDsData);
+    const int g8 = lane >> 2;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        ldsm_x4(qb + (lane & 15) * 256 + (2 * ks + (lane >> 4)) * 16, qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+        if (g8 >= R) qf[ks][0] = qf[ks][2] = 0u;
+        if (g8 + 8 >= R) qf[ks][1] = qf[ks][3] = 0u;
+    }
+}
+
+// One stage of 32 K/V rows for all query rows, one warp: S = Q K^T (16 x 32), the online
+// softmax (base 2), then O += P V over all 128 columns.
+SD_DEVINL void attend_stage(const uint8_t* st, int lane, const uint32_t (&qf)[8][4], bool two_halves, uint32_t valid,
+                            float scale_log2, AttAcc& acc) {
+    const uint32_t kb = smem_addr(st), vb = kb + kDsData / 2;
+    float s[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[n][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp) {
+            // matrices: keys 16pp + 0..7 (dims 16ks + 0..7, +8..15), keys 16pp + 8..15 (same)
+            const int key = 16 * pp + (lane & 7) + ((lane >> 4) << 3);
+            const int chunk = 2 * ks + ((lane >> 3) & 1);
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(kb + swz(kDsRows, key, chunk), r0, r1, r2, r3);
+            mma_bf16_16816(s[2 * pp], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], r0, r1);
+            mma_bf16_16816(s[2 * pp + 1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], r2, r3);
+        }
+    const int t4 = lane & 3;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        if (hf == 1 && !two_halves) {  // query rows 8..15 are padding: P = 0 there
+#pragma unroll
+            for (int n = 0; n < 4; ++n) s[n][2] = s[n][3] = 0.f;
+            break;
+        }
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int j = 8 * n + 2 * t4 + e;
+                const float x = ((valid >> j) & 1u) ? s[n][2 * hf + e] * scale_log2 : -INFINITY;
+                s[n][2 * hf + e] = x;
+                tmax = fmaxf(tmax, x);
+            }
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+        const float mo = acc.m[hf];
+        const float mn = fmaxf(mo, tmax);
+        const float alpha = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
+        float rsum = 0.f;
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float x = s[n][2 * hf + e];
+                const float pv = (x == -INFINITY) ? 0.f : fast_exp2(x - mn);
+                s[n][2 * hf + e] = pv;
+                rsum += pv;
+            }
+        rsum += __shfl_xor_sync(0xffffffffu, rsum, 1);
+        rsum += __shfl_xor_sync(0xffffffffu, rsum, 2);
+        acc.l[hf] = acc.l[hf] * alpha + rsum;
+        acc.m[hf] = mn;
+        if (alpha != 1.f) {
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt) {
+                acc.o[nt][2 * hf] *= alpha;
+                acc.o[nt][2 * hf + 1] *= alpha;
+            }
+        }
+    }
+    // P as A fragments (bf16 hi + lo, ~16 significant bits), k-step kk = keys 16kk .. 16kk + 15
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+        uint32_t ph[4], pl[4];
+        split_bf16x2(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
+        split_bf16x2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
+        split_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
+        split_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
+#pragma unroll
+        for (int c2 = 0; c2 < 8; ++c2) {
+            // V rows 16kk + 0..15, columns 16 c2 .. 16 c2 + 15, transposed into B fragments
+            const int key = 16 * kk + (lane & 15);
+            const int chunk = 2 * c2 + (lane >> 4);
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_t(vb + swz(kDsRows, key, chunk), v0, v1, v2, v3);
+            mma_bf16_16816(acc.o[2 * c2], ph[0], ph[1], ph[2], ph[3], v0, v1);
+            mma_bf16_16816(acc.o[2 * c2 + 1], ph[0], ph[1], ph[2], ph[3], v2, v3);
+            mma_bf16_16816(acc.o[2 * c2], pl[0], pl[1], pl[2], pl[3], v0, v1);
+            mma_bf16_16816(acc.o[2 * c2 + 1], pl[0], pl[1], pl[2], pl[3], v2, v3);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ selection
+
+// The selection code runs about once per SM and launch, from a cold instruction cache: it is
+// kept small (out-of-line passes, a mode switch instead of a copy per pass kind) rather than
+// unrolled.
+
+struct SelSmem {
+    uint32_t* hist;   // [2048]
+    uint32_t* sel;    // [kDsMaxN / 32]
+    uint32_t* tie;    // [kDsMaxN / 32]
+    int32_t* cidx;    // [kDsCand]
+    uint32_t* ckey;   // [kDsCand]
+    float2* scratch;  // the five arrays above as one [kDsSelScratch] float2 area (merges)
+    float* chunk;     // [2][kDsChunk]
+    uint64_t* cbar;   // [2] chunk barriers
+    volatile uint32_t* cpar;  // [2] their next parities
+    volatile uint32_t* cand_n;
+    int* bc;          // broadcast scalars [16]
+    uint32_t* wt;     // per-warp scan totals [kDsSelW]
+    volatile int* abort_flag;
+    uint64_t lim;
+};
+
+// Barrier of the kDsST selection threads (hardware named barrier 1).  Every selection warp
+// passes the same sequence of these barriers: a selection's or a merge's control flow
+// depends only on values shared through shared memory, and nothing inside either waits on
+// another role (the chunk copies it waits for are its own, with bounded waits), so no
+// selection warp can be left waiting here.
+SD_DEVINL void sel_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kDsST) : "memory"); }
+
+// Sum of v over the selection threads above this one (descending: up = false) or below it
+// (ascending: up = true), in every thread.
+__device__ __noinline__ uint32_t sel_scan_excl(uint32_t v, int sst, SelSmem& S, bool up) {
+    const int lane = sst & 31, w = sst >> 5;
+    uint32_t x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = up ? __shfl_up_sync(0xffffffffu, x, o) : __shfl_down_sync(0xffffffffu, x, o);
+        if (up ? lane >= o : lane + o < 32) x += y;
+    }
+    if (lane == (up ? 31 : 0)) S.wt[w] = x;
+    sel_bar();
+    uint32_t r = x - v;
+    for (int u = 0; u < kDsSelW; ++u)
+        if (up ? u < w : u > w) r += S.wt[u];
+    sel_bar();  // wt may be reused after this
+    return r;
+}
+
+// In the 2048-bin histogram S.hist, the bin d where the count of entries in bins above d is
+// < target <= that count plus hist[d] (1 <= target <= the total): writes d, the count above
+// and hist[d] to S.bc[o .. o+2], visible to every thread on return.
+__device__ __noinline__ void sel_find_bin(uint32_t target, int o, int sst, SelSmem& S) {
+    constexpr int per = kDsBins / kDsST;
+    uint32_t loc = 0;
+    for (int j = 0; j < per; ++j) loc += S.hist[sst * per + ((j + sst) & (per - 1))];
+    const uint32_t above = sel_scan_excl(loc, sst, S, false);
+    if (above < target && target <= above + loc) {
+        uint32_t cum = above;
+        for (int j = per - 1; j >= 0; --j) {
+            const uint32_t c = S.hist[sst * per + j];
+            if (cum + c >= target) {
+                S.bc[o] = sst * per + j;
+                S.bc[o + 1] = (int)cum;
+                S.bc[o + 2] = (int)c;
+                break;
+            }
+            cum += c;
+        }
+    }
+    sel_bar();
+}
+
+enum : int { kPassFirst, kPassSelD, kPassHist2, kPassSelP22, kPassHist3, kPassSelThr, kPassSelTie };
+
+struct PassArg {
+    int mode, D;
+    uint32_t p22, thr;
+};
+
+// The bit an entry with order key `key` sets in the selection (sel) and tie bitmaps, or the
+// histogram bin it adds to (hbin >= 0), for pass modes other than kPassFirst.
+SD_DEVINL void pass_decide(const PassArg& a, uint32_t key, bool& sel, bool& tie, int& hbin) {
+    const int dg = (int)(key >> 21);
+    sel = tie = false;
+    hbin = -1;
+    switch (a.mode) {
+        case kPassSelD: sel = dg == a.D; break;
+        case kPassHist2: hbin = dg == a.D ? (int)((key >> 10) & 2047u) : -1; break;
+        case kPassSelP22: sel = dg == a.D && (key >> 10) >= a.p22; break;
+        case kPassHist3: hbin = (key >> 10) == a.p22 ? (int)(key & 1023u) : -1; break;
+        case kPassSelThr: sel = dg == a.D && key >= a.thr; break;
+        default:  // kPassSelTie
+            sel = dg == a.D && key > a.thr;
+            tie = dg == a.D && key == a.thr;
+            break;
+    }
+}
+
+// One pass over the group's N scores (N a multiple of 4: the scores come in chunks of
+// kDsChunk through two shared-memory buffers filled by 1-D bulk copies, one copy in flight
+// while the other chunk is read).  In a chunk, selection thread t owns bitmap word t (scores
+// 32t .. 32t + 31 of the chunk): it builds the word's bits in a register, so no bitmap
+// update is atomic.  kPassFirst sets the bits above digit D and keeps the digit-D entries as
+// candidates, allocated once per warp and chunk.  Ends with a selection barrier.
+__device__ __noinline__ void score_pass(PassArg a, const float* sc, int N, int sst, SelSmem& S) {
+    const int lane = sst & 31;
+    const int nch = (N + kDsChunk - 1) / kDsChunk;
+    uint32_t par[2] = {S.cpar[0], S.cpar[1]};
+    auto issue = [&](int c, int b) {
+        const uint32_t bytes = (uint32_t)min(kDsChunk, N - c * kDsChunk) * 4u;
+        mbar_arrive_expect_tx(&S.cbar[b], bytes);
+        bulk_g2s(S.chunk + b * kDsChunk, sc + (size_t)c * kDsChunk, bytes, &S.cbar[b]);
+    };
+    if (sst == 0) {
+        // the scores were written by other CTAs (generic stores, acquired through the group's
+        // counter); order that before these async-proxy reads
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        issue(0, 0);
+        if (nch > 1) issue(1, 1);
+    }
+    for (int c = 0; c < nch; ++c) {
+        const int b = c & 1;
+        if (!mbar_wait(&S.cbar[b], par[b], S.lim)) *S.abort_flag = 1;
+        par[b] ^= 1u;
+        const int base = c * kDsChunk + 32 * sst;  // this thread's 32 scores
+        const int nin = max(0, min(32, N - base));
+        const float4* b4 = reinterpret_cast<const float4*>(S.chunk + b * kDsChunk) + 8 * sst;
+        // the thread's 32 keys in read order: key[4j + e] is score 4 * ((j + sst) & 7) + e of its
+        // word (the rotated order makes a quarter warp read 8 distinct bank groups)
+        uint32_t key[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 v = b4[(j + sst) & 7];
+            key[4 * j + 0] = float_key(v.x);
+            key[4 * j + 1] = float_key(v.y);
+            key[4 * j + 2] = float_key(v.z);
+            key[4 * j + 3] = float_key(v.w);
+        }
+        auto bitpos = [&](int e) { return 4 * (((e >> 2) + sst) & 7) + (e & 3); };
+        const int w = base >> 5;
+        if (a.mode == kPassFirst) {
+            uint32_t above = 0, cnt = 0;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int bp = bitpos(e);
+                const int dg = (int)(key[e] >> 21);
+                if (bp < nin && dg > a.D) above |= 1u << bp;
+                if (bp < nin && dg == a.D) ++cnt;
+            }
+            if (nin > 0) S.sel[w] = above;
+            // candidates: one shared atomic per warp, then each thread writes its own
+            uint32_t incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            uint32_t wbase = 0;
+            if (lane == 31 && incl > 0) wbase = atomicAdd(const_cast<uint32_t*>(S.cand_n), incl);
+            wbase = __shfl_sync(0xffffffffu, wbase, 31);
+            uint32_t slot = wbase + incl - cnt;
+            if (cnt > 0) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int bp = bitpos(e);
+                    if (bp < nin && (int)(key[e] >> 21) == a.D) {
+                        if (slot < (uint32_t)kDsCand) {
+                            S.cidx[slot] = base + bp;
+                            S.ckey[slot] = key[e];
+                        }
+                        ++slot;
+                    }
+                }
+            }
+        } else {
+            uint32_t sw = 0, tw = 0;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int bp = bitpos(e);
+                bool sl, tl;
+                int hb;
+                pass_decide(a, key[e], sl, tl, hb);
+                if (bp < nin) {
+                    if (sl) sw |= 1u << bp;
+                    if (tl) tw |= 1u << bp;
+                    if (hb >= 0) atomicAdd(&S.hist[hb], 1u);
+                }
+            }
+            if (nin > 0) {
+                if (sw) S.sel[w] |= sw;
+                if (tw) S.tie[w] |= tw;
+            }
+        }
+        sel_bar();  // every thread is done with buffer b
+        if (sst == 0 && c + 2 < nch) {
+            fence_proxy_async_shared();
+            issue(c + 2, b);
+        }
+    }
+    if (sst == 0) {
+        S.cpar[0] = par[0];
+        S.cpar[1] = par[1];
+    }
+    sel_bar();
+}
+
+// One pass over the candidates (every one has digit D; never kPassFirst).  Ends with a
+// selection barrier.
+__device__ __noinline__ void cand_pass(PassArg a, int n, int sst, SelSmem& S) {
+    for (int c = sst; c < n; c += kDsST) {
+        bool sl, tl;
+        int hb;
+        const int i = S.cidx[c];
+        pass_decide(a, S.ckey[c], sl, tl, hb);
+        if (sl) atomicOr(&S.sel[i >> 5], 1u << (i & 31));
+        if (tl) atomicOr(&S.tie[i >> 5], 1u << (i & 31));
+        if (hb >= 0) atomicAdd(&S.hist[hb], 1u);
+    }
+    sel_bar();
+}
+
+// The group's exact top-k: ascending indices of the k entries first in (score desc, index
+// asc), written to p.idx[g]; the group's histogram is read and zeroed.  All kDsST selection
+// threads call it.
+__device__ __noinline__ void select_group(const DsParams& p, int g, int sst, SelSmem& S) {
+    const int N = p.N, k = p.k;
+    const float* sc = p.scores + (size_t)g * N;
+    uint32_t* gh = p.hist + (size_t)g * kDsBins;
+    int32_t* out = p.idx + (size_t)g * k;
+
+    // 1. the top digit D from the histogram the scoring stages built (then zeroed for next time)
+    for (int j = sst; j < kDsBins / 4; j += kDsST) {
+        uint4* g4 = reinterpret_cast<uint4*>(gh) + j;
+        *reinterpret_cast<uint4*>(S.hist + 4 * j) = __ldcg(g4);
+        __stcg(g4, make_uint4(0u, 0u, 0u, 0u));
+    }
+    const int NW = (N + 31) >> 5;
+    for (int w = sst; w < NW; w += kDsST) S.sel[w] = S.tie[w] = 0u;
+    if (sst == 0) *S.cand_n = 0u;
+    sel_bar();
+    if (k == 0) return;
+    sel_find_bin((uint32_t)k, 0, sst, S);
+    PassArg a{kPassFirst, S.bc[0], 0u, 0u};
+    const uint32_t nD = (uint32_t)S.bc[2];
+    const uint32_t krem = (uint32_t)k - (uint32_t)S.bc[1];
+
+    // 2. one pass over the scores: digits above D are selected, digit D entries become candidates
+    score_pass(a, sc, N, sst, S);
+    const bool overflow = nD > (uint32_t)kDsCand;
+    // 3. the threshold among the digit-D entries: bits 20..10, then 9..0, each a histogram
+    // pass over the candidates (or over the scores again when the candidates overflowed)
+    auto digit_pass = [&](int mode) {
+        a.mode = mode;
+        if (overflow) score_pass(a, sc, N, sst, S);
+        else cand_pass(a, (int)nD, sst, S);
+    };
+    uint32_t ties_take = 0;
+    if (krem == nD) {
+        digit_pass(kPassSelD);
+    } else {
+        for (int j = sst; j < kDsBins; j += kDsST) S.hist[j] = 0u;
+        sel_bar();
+        digit_pass(kPassHist2);
+        sel_find_bin(krem, 3, sst, S);
+        a.p22 = ((uint32_t)a.D << 11) | (uint32_t)S.bc[3];
+        const uint32_t krem2 = krem - (uint32_t)S.bc[4];
+        if (krem2 == (uint32_t)S.bc[5]) {
+            digit_pass(kPassSelP22);
+        } else {
+            for (int j = sst; j < kDsBins; j += kDsST) S.hist[j] = 0u;
+            sel_bar();
+            digit_pass(kPassHist3);
+            sel_find_bin(krem2, 6, sst, S);
+            a.thr = (a.p22 << 10) | (uint32_t)S.bc[6];
+            const uint32_t krem3 = krem2 - (uint32_t)S.bc[7];
+            if (krem3 == (uint32_t)S.bc[8]) {
+                digit_pass(kPassSelThr);
+            } else {
+                ties_take = krem3;
+                digit_pass(kPassSelTie);
+            }
+        }
+    }
+
+    // 4. emit ascending: the selected entries, and the first ties_take ties in index order
+    const int wpt = (NW + kDsST - 1) / kDsST;
+    const int w0 = min(NW, sst * wpt), w1 = min(NW, w0 + wpt);
+    uint32_t cs = 0, ct = 0;
+    for (int w = w0; w < w1; ++w) {
+        cs += (uint32_t)__popc(S.sel[w]);
+        ct += (uint32_t)__popc(S.tie[w]);
+    }
+    const uint32_t tie_before = sel_scan_excl(ct, sst, S, true);
+    const uint32_t take = ties_take > tie_before ? min(ct, ties_take - tie_before) : 0u;
+    uint32_t pos = sel_scan_excl(cs + take, sst, S, true);
+    uint32_t taken = 0;
+    for (int w = w0; w < w1; ++w) {
+        uint32_t sw = S.sel[w], tw = S.tie[w];
+        while (tw != 0u && taken < take) {
+            const uint32_t low = tw & (0u - tw);
+            sw |= low;
+            tw ^= low;
+            ++taken;
+        }
+        while (sw != 0u) {
+            const int bit = __ffs(sw) - 1;
+            if (pos < (uint32_t)k) out[pos] = w * 32 + bit;
+            ++pos;
+            sw &= sw - 1u;
+        }
+    }
+}
+
+// The group's output: the merge of its attention partials in a fixed order (task by task,
+// sub-partial by sub-partial).  All kDsST selection threads call it: the partials' (m, l) go
+// to shared memory, threads r < R turn them into each partial's weight 2^(m - M) / L for
+// their row, then thread c sums column c.
+__device__ __noinline__ void merge_group(const DsParams& p, int g, int sst, SelSmem& S) {
+    const int NP = p.AG * kDsSub, R = p.R;
+    const int b = g / p.Hkv, kvh = g % p.Hkv;
+    const size_t base = (size_t)g * NP * R;
+    float2* ml = S.scratch;              // [NP * R]: (m, l), then (weight, -)
+    float2* rowML = S.scratch + NP * R;  // [R]: (M, L)
+    const float2* gml = reinterpret_cast<const float2*>(p.part_ml) + base;
+    for (int e = sst; e < NP * R; e += kDsST) {
+        // a task of nst stages wrote sub-partials 0 .. min(nst, kDsSub) - 1
+        const int pi = e / R;
+        ml[e] = pi % kDsSub < task_stages(p, pi / kDsSub) ? __ldcg(gml + e) : make_float2(-INFINITY, 0.f);
+    }
+    sel_bar();
+    if (sst < R) {
+        float M = -INFINITY;
+        for (int t = 0; t < NP; ++t) M = fmaxf(M, ml[t * R + sst].x);
+        float L = 0.f;
+        for (int t = 0; t < NP; ++t) {
+            const float2 x = ml[t * R + sst];
+            if (x.x != -INFINITY) L = fmaf(x.y, exp2f(x.x - M), L);
+        }
+        for (int t = 0; t < NP; ++t) {
+            const float mt = ml[t * R + sst].x;
+            ml[t * R + sst].x = (mt == -INFINITY || !(L > 0.f)) ? 0.f : exp2f(mt - M) / L;
+        }
+        rowML[sst] = make_float2(M, L);
+    }
+    sel_bar();
+    for (int r = 0; r < R; ++r) {
+        const float* po = p.part_o + (base + r) * 128 + sst;
+        float o = 0.f;
+        int t = 0;
+        for (; t + 8 <= NP; t += 8) {
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float wgt = ml[(t + u) * R + r].x;
+                x[u] = wgt != 0.f ? __ldcg(po + (size_t)(t + u) * R * 128) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) o = fmaf(ml[(t + u) * R + r].x, x[u], o);
+        }
+        for (; t < NP; ++t) {
+            const float wgt = ml[t * R + r].x;
+            if (wgt != 0.f) o = fmaf(wgt, __ldcg(po + (size_t)t * R * 128), o);
+        }
+        const int v = r / p.G, gi = r % p.G;
+        const size_t qrow = ((size_t)b * p.V + v) * p.Hq + (size_t)kvh * p.G + gi;
+        p.out[qrow * 128 + sst] = o;
+        if (sst == 0) {
+            const float2 x = rowML[r];
+            p.lse[qrow] = x.y > 0.f ? (x.x + log2f(x.y)) * 0.69314718055994530942f : -INFINITY;
+        }
+    }
+    sel_bar();  // the scratch may be reused after this
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <bool F16>
+__global__ void __launch_bounds__(kDsThreads, 1)
+    decode_step_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap kvk,
+                       const __grid_constant__ CUtensorMap kvv, const DsParams p) {
+    using L = DsLayout;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    uint8_t* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::oBars);
+    uint64_t* empty = full + kDsStages;
+    uint64_t* rec_full = empty + kDsStages;
+    uint64_t* rec_free = rec_full + kDsRec;
+    uint64_t* cbar = rec_free + kDsRec;
+    StageMeta* meta = reinterpret_cast<StageMeta*>(sm + L::oMeta);
+    int2* rec = reinterpret_cast<int2*>(sm + L::oRec);
+    volatile int* jobs_sel = reinterpret_cast<volatile int*>(sm + L::oJobs);
+    volatile int* jobs_mer = jobs_sel + kDsJobs;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::oMisc);
+    volatile uint32_t* consumed = reinterpret_cast<volatile uint32_t*>(sm + L::oMisc + 4);  // [4]
+    volatile uint32_t* issued = reinterpret_cast<volatile uint32_t*>(sm + L::oMisc + 20);
+    volatile uint32_t* js = reinterpret_cast<volatile uint32_t*>(sm + L::oMisc + 24);  // sel head, tail, mer head, tail
+    volatile uint32_t* cand_n = reinterpret_cast<volatile uint32_t*>(sm + L::oMisc + 40);
+    volatile int* work = reinterpret_cast<volatile int*>(sm + L::oMisc + 44);  // kind, group, finish
+    volatile uint32_t* cpar = reinterpret_cast<volatile uint32_t*>(sm + L::oMisc + 56);
+    int* bc = reinterpret_cast<int*>(sm + L::oMisc + 64);             // [16]
+    uint32_t* wt = reinterpret_cast<uint32_t*>(sm + L::oMisc + 128);  // [kDsSelW]
+    const uint64_t lim = p.wait_ns;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < kDsStages; ++s) {
+            mbar_init(&full[s], 32);
+            mbar_init(&empty[s], 1);  // the consumer warp that owns the slot
+        }
+        for (int r = 0; r < kDsRec; ++r) {
+            mbar_init(&rec_full[r], 1);
+            mbar_init(&rec_free[r], 1);
+        }
+        mbar_init(&cbar[0], 1);
+        mbar_init(&cbar[1], 1);
+        *abort_flag = 0;
+        for (int j = 0; j < 4; ++j) consumed[j] = 0;
+        *issued = 0;
+        for (int j = 0; j < 4; ++j) js[j] = 0;
+        work[0] = work[1] = work[2] = 0;
+        cpar[0] = cpar[1] = 0;
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    pdl_wait();  // the inputs and the workspace counters are the preceding kernels' results
+
+    if (warp == kDsProd) {
+        // ------------------------------------------------------------ producer
+        const uint64_t pol = l2_evict_first_policy();
+        uint32_t i = 0;  // stages filled
+        bool ok = true;
+        // the next free slot (all lanes); false on an abort
+        auto take_slot = [&](uint32_t n) -> bool {
+            return warp_wait(&empty[n % kDsStages], ((n / kDsStages) & 1u) ^ 1u, abort_flag, lim);
+        };
+        // this CTA owns a selection or merge (lane 0 queues it for the selection warps); false
+        // when the queue stayed full
+        auto own = [&](volatile int* ring, int hi, int g) -> bool {
+            bool got = true;
+            if (lane == 0) {
+                if (js[hi] - js[hi - 1] >= (uint32_t)kDsJobs) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (js[hi] - js[hi - 1] >= (uint32_t)kDsJobs) {
+                        __nanosleep(256);
+                        if (*abort_flag || globaltimer_ns() - t0 > lim) {
+                            got = false;
+                            break;
+                        }
+                    }
+                }
+                if (got) {
+                    ring[js[hi] % kDsJobs] = g;
+                    __threadfence_block();
+                    js[hi] = js[hi] + 1u;
+                }
+            }
+            return __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+        };
+        uint32_t t_next = 0, t_end = 0;  // the claimed tasks not yet started
+        int ready_g = -1;                // the last group seen with its selection published
+        while (ok) {
+            if (t_next == t_end) {  // claim the next kDsClaim tasks of the list in one atomic
+                uint32_t t0 = 0;
+                if (lane == 0) t0 = atomicAdd(&p.ctrl[0], (uint32_t)kDsClaim);
+                t_next = __shfl_sync(0xffffffffu, t0, 0);
+                t_end = t_next + kDsClaim;
+            }
+            const uint32_t t = t_next++;
+            if (t >= p.total) {
+                // one end marker per consumer warp
+                for (int w = 0; w < kDsCons && ok; ++w) {
+                    if (!take_slot(i)) {
+                        ok = false;
+                        break;
+                    }
+                    const int s = (int)(i % kDsStages);
+                    if (lane == 0) meta[s].kind = kTaskEnd;
+                    __syncwarp();
+                    mbar_arrive(&full[s]);
+                    ++i;
+                }
+                break;
+            }
+            const Task tk = decode_task(p, t);
+            if (tk.kind == kTaskScore) {
+                if (tk.part == p.SG - 1 && !own(jobs_sel, 1, tk.g)) {
+                    ok = false;
+                    break;
+                }
+                for (int sgi = 0; sgi < kDsScoreStages; ++sgi) {
+                    const int j0 = tk.part * kDsTaskKeys + sgi * kDsKeyRows;
+                    if (j0 >= p.N && sgi > 0) break;  // past the group's end (only a tail)
+                    if (!take_slot(i)) {
+                        ok = false;
+                        break;
+                    }
+                    const int s = (int)(i % kDsStages);
+                    uint8_t* st = sm + s * kDsStage;
+                    if (lane == 0) {
+                        StageMeta& m = meta[s];
+                        m.kind = kTaskScore;
+                        m.g = tk.g;
+                        m.j0 = j0;
+                        m.nrows = max(0, min(kDsKeyRows, p.N - j0));
+                        const uint32_t qb = (uint32_t)p.V * 256u;
+                        mbar_arrive_expect_tx(&full[s], kDsData + qb);
+                        const int row = tk.g * p.N + j0;
+                        tma_load_2d_hint(st, &kmap, 0, row, &full[s], pol);
+                        tma_load_2d_hint(st + kDsData / 2, &kmap, 64, row, &full[s], pol);
+                        bulk_g2s(st + kDsData, p.q_idx + (size_t)tk.g * qb, qb, &full[s]);
+                    } else {
+                        mbar_arrive(&full[s]);
+                    }
+                    ++i;
+                }
+                continue;
+            }
+            if (tk.part == p.AG - 1 && !own(jobs_mer, 3, tk.g)) {
+                ok = false;
+                break;
+            }
+            // attention task: wait for the group's selection (published once per launch: a group
+            // seen ready stays ready until its last attention task is done)
+            if (tk.g != ready_g) {
+                uint32_t* ready = p.gstate + (size_t)tk.g * 4 + 2;
+                bool got = true;
+                if (lane == 0 && ld_acquire_gpu(ready) == 0u) {
+                    const uint64_t t0 = globaltimer_ns();
+                    for (;;) {
+                        __nanosleep(128);
+                        if (ld_acquire_gpu(ready) != 0u) break;
+                        if (*abort_flag || globaltimer_ns() - t0 > lim) {
+                            got = false;
+                            break;
+                        }
+                    }
+                }
+                if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
+                    ok = false;
+                    break;
+                }
+                (void)ld_acquire_gpu(ready);  // every lane reads the selection after this
+                ready_g = tk.g;
+            }
+            const int g = tk.g, b = g / p.Hkv, kvh = g % p.Hkv;
+            const int r0 = tk.part * kDsTaskRows;
+            const int rows = max(0, min(kDsTaskRows, p.n_rows - r0));
+            const int nst = task_stages(p, tk.part);
+            const uint32_t qbytes = (uint32_t)p.G * 256u;
+            const int32_t* sel_row = p.idx + (size_t)g * p.k;
+            // every selected row of the task at once (one round trip): lane l resolves task row
+            // 32q + l, q < 8, to its K/V row (-1: none, or skipped as out of range)
+            long long src[kDsTaskStages];
+#pragma unroll
+            for (int q = 0; q < kDsTaskStages; ++q) {
+                const int jr = 32 * q + lane;
+                src[q] = -1;
+                if (jr < rows) {
+                    const int j = r0 + jr;
+                    const int e = j / p.block;
+                    const int sel = __ldcg(sel_row + e);
+                    if (sel >= 0 && sel < p.N)
+                        src[q] = (long long)g * p.T + (long long)sel * p.block + (j - e * p.block);
+                    else
+                        report(p.err, SD_DEVERR_INDEX);
+                }
+            }
+#pragma unroll
+            for (int sgi = 0; sgi < kDsTaskStages; ++sgi) {
+                if (sgi >= nst || !ok) break;
+                if (!take_slot(i)) {
+                    ok = false;
+                    break;
+                }
+                const int s = (int)(i % kDsStages);
+                uint8_t* st = sm + s * kDsStage;
+                const int nrows = max(0, min(kDsRows, rows - sgi * kDsRows));
+                const long long ra = src[sgi];
+                // one contiguous run of 32 rows (an aligned part of one block)?
+                long long run0 = -1;
+                if (p.tma_blocks && nrows == kDsRows) run0 = __shfl_sync(0xffffffffu, ra, 0);
+                const uint32_t valid = __ballot_sync(0xffffffffu, ra >= 0);
+                if (lane == 0) {
+                    StageMeta& m = meta[s];
+                    m.kind = kTaskAttend;
+                    m.g = g;
+                    m.task = tk.part;
+                    m.j0 = r0 + sgi * kDsRows;
+                    m.nrows = nrows;
+                    m.sgi = sgi;
+                    m.nst = nst;
+                    m.valid = run0 >= 0 ? 0xffffffffu : valid;
+                }
+                if (run0 >= 0) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&full[s], kDsData + (uint32_t)p.V * qbytes);
+                        tma_load_2d_hint(st, &kvk, 0, (int)run0, &full[s], pol);
+                        tma_load_2d_hint(st + 4096, &kvk, 64, (int)run0, &full[s], pol);
+                        tma_load_2d_hint(st + 8192, &kvv, 0, (int)run0, &full[s], pol);
+                        tma_load_2d_hint(st + 12288, &kvv, 64, (int)run0, &full[s], pol);
+                        for (int v = 0; v < p.V; ++v)
+                            bulk_g2s(st + kDsData + v * qbytes,
+                                     p.q + (((size_t)b * p.V + v) * p.Hq + (size_t)kvh * p.G) * 256, qbytes, &full[s]);
+                    } else {
+                        mbar_arrive(&full[s]);
+                    }
+                } else {
+                    if (lane == 0) {
+                        mbar_expect_tx(&full[s], (uint32_t)p.V * qbytes);
+                        for (int v = 0; v < p.V; ++v)
+                            bulk_g2s(st + kDsData + v * qbytes,
+                                     p.q + (((size_t)b * p.V + v) * p.Hq + (size_t)kvh * p.G) * 256, qbytes, &full[s]);
+                    }
+                    // lanes 8q .. 8q + 7 move one 128-byte line of row 4i + q (zeros for rows skipped)
+                    const int c = lane & 7;
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int row = 4 * it + (lane >> 3);
+                        const long long sr = __shfl_sync(0xffffffffu, ra, row);
+                        const bool on = sr >= 0;
+                        const size_t off = on ? ((size_t)sr * 128 + (size_t)c * 8) * 2 : 0;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t dst = swz(kDsRows, row, 8 * h + c);
+                            cp_async16_zfill(st + dst, p.kc + off + h * 128, on ? 16u : 0u);
+                            cp_async16_zfill(st + kDsData / 2 + dst, p.vc + off + h * 128, on ? 16u : 0u);
+                        }
+                    }
+                    // lanes 1-31 arrive when their copies land; lane 0 holds the phase open until
+                    // its copies land too and arrives itself (release: publishes the metadata)
+                    if (lane == 0) {
+                        cp_async_mbar_arrive(&full[s]);
+                        mbar_arrive(&full[s]);
+                    } else {
+                        cp_async_mbar_arrive_noinc(&full[s]);
+                    }
+                }
+                ++i;
+            }
+        }
+        if (!ok) *abort_flag = 1;
+        if (lane == 0) *issued = i;
+    } else if (warp < kDsCons) {
+        // ------------------------------------------------------------ consumers
+        float* sbuf = reinterpret_cast<float*>(sm + L::oScore) + warp * 64;
+        uint32_t qf[8][4];
+        AttAcc acc;
+        const bool two_halves = p.R > 8;
+        bool ok = true;
+        // stage i = 4n + warp: ring slot i % 8, record slot i % kDsRec
+        for (uint32_t n = 0;; ++n) {
+            const uint32_t i = 4u * n + (uint32_t)warp;
+            const int s = (int)(i % kDsStages);
+            if (!warp_wait(&full[s], (i / kDsStages) & 1u, abort_flag, lim)) {
+                ok = false;
+                break;
+            }
+            const StageMeta m = meta[s];
+            const uint8_t* st = sm + s * kDsStage;
+            if (m.kind == kTaskScore) {
+                score_tile<F16>(st, lane, p.V, sbuf);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int rl = 32 * h + lane;
+                    const bool in = rl < m.nrows;
+                    const float v = sbuf[rl];
+                    if (in) p.scores[(size_t)m.g * p.N + m.j0 + rl] = v;
+                    const uint32_t dg = float_key(v) >> 21;
+                    const uint32_t peers = __match_any_sync(0xffffffffu, in ? dg : 0xffffffffu);
+                    if (in && lane == __ffs(peers) - 1)
+                        atomicAdd(&p.hist[(size_t)m.g * kDsBins + dg], (uint32_t)__popc(peers));
+                }
+            } else if (m.kind == kTaskAttend) {
+                load_q_frags(st, lane, p.R, qf);
+                if (m.sgi < kDsSub) {  // the first of this warp's stages of the task
+#pragma unroll
+                    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc.o[nt][e] = 0.f;
+                    acc.m[0] = acc.m[1] = -INFINITY;
+                    acc.l[0] = acc.l[1] = 0.f;
+                }
+                attend_stage(st, lane, qf, two_halves, m.valid, p.scale_log2, acc);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                if (m.sgi + kDsSub >= m.nst) {  // this warp's last stage of the task: its partial
+                    const int g8 = lane >> 2, t4 = lane & 3;
+                    const size_t pb = (((size_t)m.g * p.AG + m.task) * kDsSub + (m.sgi % kDsSub)) * p.R;
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int r = g8 + 8 * hf;
+                        if (r >= p.R) continue;
+#pragma unroll
+                        for (int nt = 0; nt < 16; ++nt)
+                            *reinterpret_cast<float2*>(p.part_o + (pb + r) * 128 + 8 * nt + 2 * t4) =
+                                make_float2(acc.o[nt][2 * hf], acc.o[nt][2 * hf + 1]);
+                        if (t4 == 0)
+                            *reinterpret_cast<float2*>(p.part_ml + (pb + r) * 2) = make_float2(acc.m[hf], acc.l[hf]);
+                    }
+                }
+            }
+            if (lane == 0) consumed[warp] = n + 1;
+            // the stage's record (its kind and group; an end marker for kTaskEnd)
+            const int slot = (int)(i % kDsRec);
+            if (i >= (uint32_t)kDsRec && !warp_wait(&rec_free[slot], ((i / kDsRec) & 1u) ^ 1u, abort_flag, lim)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) rec[slot] = make_int2(m.kind, m.g);
+            __syncwarp();  // the warp's stores before its arrival (release)
+            if (lane == 0) mbar_arrive(&rec_full[slot]);
+            if (m.kind == kTaskEnd) break;
+        }
+        if (!ok) *abort_flag = 1;
+    } else {
+        // ------------------------------------------------------------ bookkeeping + selection
+        const int sst = tid - 32 * kDsSel0;
+        const int sw = sst >> 5;
+        SelSmem S;
+        S.hist = reinterpret_cast<uint32_t*>(sm + L::oHist);
+        S.sel = reinterpret_cast<uint32_t*>(sm + L::oSel);
+        S.tie = reinterpret_cast<uint32_t*>(sm + L::oTie);
+        S.cidx = reinterpret_cast<int32_t*>(sm + L::oCandIdx);
+        S.ckey = reinterpret_cast<uint32_t*>(sm + L::oCandKey);
+        S.scratch = reinterpret_cast<float2*>(sm + L::oHist);
+        S.chunk = reinterpret_cast<float*>(sm + L::oChunk);
+        S.cbar = cbar;
+        S.cpar = cpar;
+        S.cand_n = cand_n;
+        S.bc = bc;
+        S.wt = wt;
+        S.abort_flag = abort_flag;
+        S.lim = lim;
+        uint32_t a = 0;          // records taken (selection warp 0)
+        int ends = 0;            // consumer warps whose end marker was counted (selection warp 0)
+        uint64_t last_progress = 0;
+        for (;;) {
+            if (sw == 0) {
+                // 1. the records the consumers posted so far move the groups' counters
+                int nb = 0;
+                if (lane == 0)
+                    while (nb < 32 && mbar_try_wait(&rec_full[(a + nb) % kDsRec], ((a + nb) / kDsRec) & 1u)) ++nb;
+                nb = __shfl_sync(0xffffffffu, nb, 0);
+                int kind = -1, gg = 0;
+                if (lane < nb) {
+                    const uint32_t r = (a + (uint32_t)lane) % kDsRec;
+                    (void)mbar_try_wait(&rec_full[r], ((a + lane) / kDsRec) & 1u);  // acquire
+                    const int2 rc = rec[r];
+                    kind = rc.x;
+                    gg = rc.y;
+                    mbar_arrive(&rec_free[r]);
+                    // release: the consumers' stores behind the record
+                    if (kind != kTaskEnd) red_add_release_gpu(&p.gstate[(size_t)gg * 4 + (kind == kTaskScore ? 0 : 1)], 1u);
+                }
+                ends += __popc(__ballot_sync(0xffffffffu, lane < nb && kind == kTaskEnd));
+                a += (uint32_t)nb;
+                // 2. an owned selection or merge whose group is complete (acquire)
+                int wk = -1, wg = 0, fin = 0;
+                if (lane == 0) {
+                    if (js[0] != js[1]) {
+                        const int g = jobs_sel[js[0] % kDsJobs];
+                        if (ld_acquire_gpu(&p.gstate[(size_t)g * 4 + 0]) == (uint32_t)p.SGS) {
+                            wk = kTaskScore;
+                            wg = g;
+                            js[0] = js[0] + 1u;
+                        }
+                    }
+                    if (wk < 0 && js[2] != js[3]) {
+                        const int g = jobs_mer[js[2] % kDsJobs];
+                        if (ld_acquire_gpu(&p.gstate[(size_t)g * 4 + 1]) == (uint32_t)p.AGS) {
+                            wk = kTaskAttend;
+                            wg = g;
+                            js[2] = js[2] + 1u;
+                        }
+                    }
+                    const uint64_t now = globaltimer_ns();
+                    if (wk >= 0 || nb > 0 || last_progress == 0) {
+                        last_progress = now;
+                    } else if (ends == kDsCons && js[0] == js[1] && js[2] == js[3]) {
+                        fin = 1;  // nothing left: no more records, no owned work
+                    } else if (*abort_flag || now - last_progress > lim) {
+                        *abort_flag = 1;
+                        fin = 1;
+                    } else {
+                        __nanosleep(64);
+                    }
+                    work[0] = wk;
+                    work[1] = wg;
+                    work[2] = fin;
+                }
+                __syncwarp();
+            }
+            sel_bar();
+            const int wk = work[0], wg = work[1];
+            const bool fin = work[2] != 0;
+            if (wk == kTaskScore) {
+                select_group(p, wg, sst, S);
+                sel_bar();  // every part of the selection is written: publish it
+                if (sst == 0) {
+                    p.gstate[(size_t)wg * 4 + 0] = 0u;
+                    fence_acq_rel_gpu();
+                    st_release_gpu(p.gstate + (size_t)wg * 4 + 2, 1u);
+                }
+            } else if (wk == kTaskAttend) {
+                merge_group(p, wg, sst, S);
+                if (sst == 0) {
+                    p.gstate[(size_t)wg * 4 + 1] = 0u;
+                    p.gstate[(size_t)wg * 4 + 2] = 0u;
+                }
+            }
+            sel_bar();  // the work word may be rewritten after this
+            if (fin) break;
+        }
+    }
+
+    __syncthreads();
+    if (tid == 0) {
+        if (*abort_flag) {
+            report(p.err, SD_DEVERR_TIMEOUT);
+            // let the stages filled but not consumed land before the CTA exits: stage j belongs
+            // to consumer warp j % 4, which got through its first consumed[j % 4] stages
+            for (uint32_t j = 0; j < *issued; ++j)
+                if (j / kDsCons >= consumed[j % kDsCons]) mbar_wait(&full[j % kDsStages], (j / kDsStages) & 1u, lim);
+        }
+        // the last CTA to finish resets the task counter for the next call
+        __threadfence();
+        if (atomicAdd(&p.ctrl[1], 1u) == gridDim.x - 1u) {
+            p.ctrl[0] = 0u;
+            p.ctrl[1] = 0u;
+        }
+    }
+}
+
+}  // namespace
+
+namespace {
+
+struct StepPlan {
+    int NG, N, SG, AG, SGS, AGS, R, L, n_rows;
+    size_t o_gstate, o_hist, o_part_o, o_part_ml, bytes;
+};
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+StepPlan plan_step(const sd_decode_step_args* a) {
+    StepPlan sp{};
+    sp.NG = a->B * a->Hkv;
+    sp.N = a->block > 0 ? a->T / a->block : 0;
+    sp.SG = std::max(1, (sp.N + kDsTaskKeys - 1) / kDsTaskKeys);
+    sp.SGS = std::max(1, (sp.N + kDsKeyRows - 1) / kDsKeyRows);
+    sp.n_rows = a->n_idx * a->block;
+    sp.AG = std::max(1, (sp.n_rows + kDsTaskRows - 1) / kDsTaskRows);
+    sp.AGS = std::max(1, (sp.n_rows + kDsRows - 1) / kDsRows);
+    sp.R = (a->Hkv > 0 ? a->Hq / a->Hkv : 0) * a->V;
+    if (a->lag > 0) {
+        sp.L = a->lag;
+    } else {
+        // the lag covers ~15 us of the whole GPU's streaming (a group's selection and the
+        // latency of its last scoring stages) at ~6.5 TB/s
+        const double unit_bytes = (double)sp.N * 256.0 + (double)sp.n_rows * 512.0;
+        const double unit_us = unit_bytes / 6.5e6;
+        sp.L = (int)std::ceil(15.0 / std::max(unit_us, 1e-3));
+    }
+    sp.L = std::max(1, std::min(sp.L, std::max(1, sp.NG)));
+    size_t off = 256;  // ctrl
+    sp.o_gstate = off;
+    off += round256((size_t)sp.NG * 16);
+    sp.o_hist = off;
+    off += round256((size_t)sp.NG * kDsBins * 4);
+    sp.o_part_o = off;
+    off += round256((size_t)sp.NG * sp.AG * kDsSub * sp.R * 128 * 4);
+    sp.o_part_ml = off;
+    off += round256((size_t)sp.NG * sp.AG * kDsSub * sp.R * 2 * 4);
+    sp.bytes = off;
+    return sp;
+}
+
+sd_status validate_step(const sd_decode_step_args* a) {
+    const char* who = "sd_decode_step";
+    SD_REQUIRE(a != nullptr, "%s: null args", who);
+    SD_REQUIRE(a->B >= 0 && a->V >= 1 && a->Hq >= 1 && a->Hkv >= 1 && a->T >= 1 && a->block >= 1 && a->n_idx >= 0,
+               "%s: bad sizes (B=%d V=%d Hq=%d Hkv=%d T=%d block=%d n_idx=%d)", who, a->B, a->V, a->Hq, a->Hkv,
+               a->T, a->block, a->n_idx);
+    SD_REQUIRE(a->Hq % a->Hkv == 0, "%s: Hq must be a multiple of Hkv", who);
+    SD_REQUIRE(a->T % a->block == 0, "%s: T must be a multiple of block", who);
+    SD_REQUIRE(a->n_idx <= a->T / a->block, "%s: n_idx must be <= T / block", who);
+    SD_REQUIRE(a->key_dtype == SD_BF16 || a->key_dtype == SD_F16, "%s: key_dtype must be SD_BF16 or SD_F16", who);
+    SD_REQUIRE(a->lag >= 0, "%s: lag must be >= 0", who);
+    if (a->d != 128 || a->d_idx != 128) {
+        set_error("%s: d and d_idx must be 128 (got %d, %d)", who, a->d, a->d_idx);
+        return SD_ERR_UNSUPPORTED;
+    }
+    if (a->V > 8 || (a->Hq / a->Hkv) * a->V > kDsMaxR) {
+        set_error("%s: V <= 8 and (Hq/Hkv)*V <= %d query rows per group are supported", who, kDsMaxR);
+        return SD_ERR_UNSUPPORTED;
+    }
+    const int N = a->T / a->block;
+    if (N > kDsMaxN || (N & 3) != 0) {
+        set_error("%s: T / block must be a multiple of 4 and at most %d (got %d)", who, kDsMaxN, N);
+        return SD_ERR_UNSUPPORTED;
+    }
+    SD_REQUIRE((long long)a->B * a->Hkv * a->T < (1LL << 31), "%s: B*Hkv*T must be < 2^31", who);
+    SD_REQUIRE((long long)a->n_idx * a->block <= (1LL << 30), "%s: selection too large", who);
+    const long long ag = std::max(1LL, ((long long)a->n_idx * a->block + kDsTaskRows - 1) / kDsTaskRows);
+    if (ag * kDsSub * (a->Hq / a->Hkv) * a->V > kDsMaxMerge) {
+        set_error("%s: %lld selected rows per group with %d query rows exceed the merge (at most %d (partial, row) pairs)",
+                  who, (long long)a->n_idx * a->block, (a->Hq / a->Hkv) * a->V, kDsMaxMerge);
+        return SD_ERR_UNSUPPORTED;
+    }
+    return SD_OK;
+}
+
+}  // namespace
+}  // namespace sd
+
+using namespace sd;
+
+extern "C" size_t sd_decode_step_workspace_bytes(const sd_decode_step_args* a) {
+    if (validate_step(a) != SD_OK) return 0;
+    return plan_step(a).bytes;
+}
+
+extern "C" sd_status sd_decode_step(const sd_decode_step_args* a, void* stream) {
+    clear_error();
+    const sd_status vs = validate_step(a);
+    if (vs != SD_OK) return vs;
+    if (a->B == 0) return SD_OK;
+    const char* who = "sd_decode_step";
+    SD_REQUIRE(a->q_idx && a->keys && a->q && a->k_cache && a->v_cache && a->scores && a->out && a->lse &&
+                   (a->idx || a->n_idx == 0),
+               "%s: null pointer argument", who);
+    SD_REQUIRE(aligned16(a->q_idx) && aligned16(a->keys) && aligned16(a->q) && aligned16(a->k_cache) &&
+                   aligned16(a->v_cache) && aligned16(a->out) && aligned16(a->scores),
+               "%s: q_idx, keys, q, k_cache, v_cache, scores and out must be 16-byte aligned", who);
+    const StepPlan sp = plan_step(a);
+    SD_REQUIRE(a->workspace != nullptr && a->workspace_bytes >= sp.bytes,
+               "%s: workspace of %zu bytes needed (got %zu)", who, sp.bytes, a->workspace_bytes);
+    SD_REQUIRE((reinterpret_cast<uintptr_t>(a->workspace) & 255u) == 0, "%s: workspace must be 256-byte aligned", who);
+    const bool f16 = a->key_dtype == SD_F16;
+    CUtensorMap kmap, kvk, kvv;
+    if (!make_tensor_map_2d(&kmap, a->keys, (uint64_t)sp.NG * sp.N, 128, kDsKeyRows, f16) ||
+        !make_tensor_map_2d(&kvk, a->k_cache, (uint64_t)sp.NG * a->T, 128, kDsRows, false) ||
+        !make_tensor_map_2d(&kvv, a->v_cache, (uint64_t)sp.NG * a->T, 128, kDsRows, false)) {
+        set_error("%s: cuTensorMapEncodeTiled failed", who);
+        return SD_ERR_CUDA;
+    }
+    uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+    DsParams p{};
+    p.q_idx = static_cast<const uint8_t*>(a->q_idx);
+    p.q = static_cast<const uint8_t*>(a->q);
+    p.kc = static_cast<const uint8_t*>(a->k_cache);
+    p.vc = static_cast<const uint8_t*>(a->v_cache);
+    p.scores = a->scores;
+    p.idx = a->idx;
+    p.out = a->out;
+    p.lse = a->lse;
+    p.err = a->err_word;
+    p.ctrl = reinterpret_cast<uint32_t*>(ws);
+    p.gstate = reinterpret_cast<uint32_t*>(ws + sp.o_gstate);
+    p.hist = reinterpret_cast<uint32_t*>(ws + sp.o_hist);
+    p.part_o = reinterpret_cast<float*>(ws + sp.o_part_o);
+    p.part_ml = reinterpret_cast<float*>(ws + sp.o_part_ml);
+    p.B = a->B;
+    p.V = a->V;
+    p.Hq = a->Hq;
+    p.Hkv = a->Hkv;
+    p.G = a->Hq / a->Hkv;
+    p.R = sp.R;
+    p.T = a->T;
+    p.N = sp.N;
+    p.k = a->n_idx;
+    p.block = a->block;
+    p.NG = sp.NG;
+    p.SG = sp.SG;
+    p.AG = sp.AG;
+    p.SGS = sp.SGS;
+    p.AGS = sp.AGS;
+    p.L = sp.L;
+    p.n_rows = sp.n_rows;
+    p.tma_blocks = a->block % kDsRows == 0 ? 1 : 0;
+    p.scale_log2 = a->scale * 1.44269504088896340736f;
+    p.wait_ns = a->wait_limit_ns > 0 ? (unsigned long long)a->wait_limit_ns : (unsigned long long)kWaitDeadlineNs;
+    SD_REQUIRE((long long)sp.NG * (sp.SG + sp.AG) < (1LL << 31) - 64, "%s: too many tasks", who);
+    p.total = (uint32_t)((long long)sp.NG * (sp.SG + sp.AG));
+    auto kern = f16 ? decode_step_kernel<true> : decode_step_kernel<false>;
+    SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DsLayout::kBytes),
+                  "sd_decode_step: cudaFuncSetAttribute");
+    const unsigned grid = (unsigned)std::max(1, std::min(num_sms(), (int)std::min<long long>(p.total, 1 << 30)));
+    SD_CUDA_CHECK(launch_pdl(kern, dim3(grid), dim3(kDsThreads), (size_t)DsLayout::kBytes, as_stream(stream), kmap,
+                             kvk, kvv, p),
+                  "sd_decode_step: launch");
+    return launch_status(who);
+}

@@ -212,7 +212,9 @@ __global__ void __launch_bounds__(32 * (4 * E + 2), 1) index_score_tc_kernel(
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (fn == nullptr) {
         void* p = nullptr;
@@ -227,7 +229,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D tensor map of 16-bit elements (bf16 or fp16) over [nrows, d] (row-major), box = 64
 // columns x box_rows rows, 128-byte swizzle, zero fill outside the tensor.
-bool make_map(CUtensorMap* m, const void* base, uint64_t nrows, int d, int box_rows, bool f16) {
+bool make_tensor_map_2d(CUtensorMap* m, const void* base, uint64_t nrows, int d, int box_rows, bool f16) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)nrows};
@@ -241,16 +243,14 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t nrows, int d, int box_r
     return r == CUDA_SUCCESS;
 }
 
-}  // namespace
-
 // bf16 (or fp16) keys and queries of the same type on the tensor cores; d_idx in {64, 128},
 // V <= 16.  per_query: every query row gets its own score row (rows*V of them) instead of
 // the max over V.
 sd_status index_score_tc_launch(const void* q_idx, const void* k_idx, int rows, int V, int N, int d_idx,
                                 float* scores, uint32_t* key_hist, int32_t* err_word, int per_query, bool f16, cudaStream_t st) {
     CUtensorMap kmap, qmap;
-    if (!make_map(&kmap, k_idx, (uint64_t)rows * N, d_idx, kTileM, f16) ||
-        !make_map(&qmap, q_idx, (uint64_t)rows * V, d_idx, kQN, f16)) {
+    if (!make_tensor_map_2d(&kmap, k_idx, (uint64_t)rows * N, d_idx, kTileM, f16) ||
+        !make_tensor_map_2d(&qmap, q_idx, (uint64_t)rows * V, d_idx, kQN, f16)) {
         set_error("sd_index_score: cuTensorMapEncodeTiled failed");
         return SD_ERR_CUDA;
     }

@@ -69,14 +69,20 @@ SD_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns false when the
-// deadline passed first.
-SD_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// deadline (limit_ns of wall-clock time, 1 s by default) passed first.
+SD_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitDeadlineNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitDeadlineNs) return false;
+        if ((i & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// Adds `bytes` to the transaction count the current phase waits for, without arriving.
+SD_DEVINL void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
 }
 
 // 1-D bulk copy (TMA, untiled) of `bytes` (multiple of 16, both addresses 16-byte
@@ -132,6 +138,22 @@ SD_DEVINL void cp_async16(void* dst_smem, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src)
                  : "memory");
 }
+// 16-byte cp.async that copies src_size (0 or 16) bytes and fills the rest with zeros.
+SD_DEVINL void cp_async16_zfill(void* dst_smem, const void* src, uint32_t src_size) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst_smem)), "l"(src),
+                 "r"(src_size)
+                 : "memory");
+}
+// One arrival on `bar` once every cp.async this thread issued before it has landed (the
+// arrival is not added to the barrier's expected count: init the count to include it).
+SD_DEVINL void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+// Like cp_async_mbar_arrive_noinc, but the arrival is counted at issue and taken back when the
+// copies land (no change to the expected count; the phase cannot complete before they land).
+SD_DEVINL void cp_async_mbar_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
 SD_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 SD_DEVINL void cp_async_wait() {
@@ -161,6 +183,38 @@ SD_DEVINL void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t 
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D (16x8 fp32) += A (16x16 fp16, row) * B (16x8 fp16, col).
+SD_DEVINL void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                             uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------- device-scope flags
+
+SD_DEVINL uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+SD_DEVINL void st_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+SD_DEVINL uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+SD_DEVINL void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// Fire-and-forget device-scope add with release semantics (no value comes back, so the issuing
+// thread does not wait for it).
+SD_DEVINL void red_add_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Two fp32 -> packed bf16x2 (round to nearest even), first value in the low half.

@@ -1,6 +1,7 @@
 // sd_host.h -- host-side helpers shared by the libsdgqa entry points (not installed).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -59,6 +60,11 @@ inline sd_status launch_status(const char* what) {
     }
     return SD_OK;
 }
+
+// 2-D tensor map of 16-bit elements (bf16, or fp16 with f16) over [nrows, d] (row-major),
+// box = 64 columns x box_rows rows, 128-byte swizzle, zero fill outside the tensor; false
+// when the driver's encoder is unavailable or rejects the map.
+bool make_tensor_map_2d(CUtensorMap* m, const void* base, uint64_t nrows, int d, int box_rows, bool f16);
 
 // The indexer on the tensor cores (index_score_tc.cu): bf16 keys and queries, or fp16 ones
 // (f16).
