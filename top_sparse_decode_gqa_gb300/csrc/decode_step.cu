@@ -11,32 +11,33 @@
 // Computes what sd_index_score -> sd_topk -> sd_gather_attend computes (scores and index
 // sets bit for bit; attention in its own summation order), for K/V resident in HBM.
 //
-// The work of a step is a list of tasks taken from one device counter by every CTA (one
-// persistent CTA per SM, a few tasks per claim):
+// The work of a step is a list of tasks taken from one device counter (one per claim):
 //   scoring task (g, part)   128 indexer keys of KV group g, as two 16 KB stages of 64 keys
 //                            (tiled TMA, 128-byte swizzle) -> scores (mma.sync m16n8k16;
 //                            products of integer-valued keys and queries are exact, so are the
 //                            fp32 sums) and their 11-bit order-key digits added to the group's
 //                            histogram;
-//   attention task (g, part) up to 256 selected rows of group g, as eight stages of 32 K and V
-//                            rows (tiled TMA for whole 32-row runs of a block, 16-byte cp.async
-//                            for scattered rows): exact online softmax over them for all G*V
-//                            query rows of the group, written as partials (m, l, O).
+//   attention task (g, part) up to 128 selected rows of group g, as up to four stages of 32 K
+//                            and V rows (tiled TMA for whole 32-row runs of a block, 16-byte
+//                            cp.async for scattered rows): exact online softmax over them for
+//                            all G*V query rows of the group, written as one partial (m, l, O).
 // The list puts the scoring tasks of group g + L before the attention tasks of group g, so the
 // attention of early groups overlaps the scoring of later ones (L, the lag, covers the time a
 // group's selection takes).  The CTA that claims a group's last scoring task owns its top-k:
-// it runs it once every scoring stage of the group is counted; the group's attention tasks
+// it runs it once every scoring task of the group is counted; the group's attention tasks
 // wait (bounded) for it.  The CTA that claims a group's last attention task likewise merges
-// the group's partials, in a fixed order, once every attention stage is counted.  The owners
-// are whichever CTAs happened to claim those tasks, so the selections spread over the GPU.
+// the group's partials, in task order, once they are all counted.  The owners are whichever
+// CTAs happened to claim those tasks, so the selections spread over the GPU.
 //
-// Warp roles in a CTA: warp 4 produces (claims tasks, fills an 8-slot ring of 16 KB stages);
-// warps 0-3 consume, warp w taking stages w, w+4, w+8, ... alone (so four stages are worked on
-// at once while four more load) and posting a record per stage; warps 5-8 count the records
-// into the device-scope counters (fire-and-forget releases, so no role waits on a device-scope
-// fence) and run the selections and merges this CTA owns.  Every wait is bounded; a wait that
-// runs out sets SD_DEVERR_TIMEOUT, every role leaves at its next wait, and the CTA lets its
-// copies in flight land before it exits.
+// A CTA (one per SM) runs four independent pipelines: producer warp 4 + w claims tasks and
+// fills the two 16 KB ring slots of consumer warp w, which runs each task alone (so four
+// tasks are worked on at once while the next stages load, and a task waiting for its group's
+// selection holds up only its own pipeline) and posts a record per finished task.  Warp 8
+// keeps the books: it counts the records into the device-scope counters (one fence per batch
+// and fire-and-forget adds) and hands the selections and merges this CTA owns, once their
+// groups are complete, to warps 9-10.  Every wait is bounded; a wait that runs out sets
+// SD_DEVERR_TIMEOUT, every role leaves at its next wait, and the CTA lets its copies in flight
+// land before it exits.
 #include <algorithm>
 #include <cmath>
 
@@ -46,13 +47,14 @@
 namespace sd {
 namespace {
 
-constexpr int kDsCons = 4;                           // consumer warps
-constexpr int kDsProd = kDsCons;                     // producer warp
-constexpr int kDsSel0 = kDsCons + 1;                 // first bookkeeping / selection warp
-constexpr int kDsSelW = 4;                           // bookkeeping / selection warps
-constexpr int kDsThreads = 32 * (kDsCons + 1 + kDsSelW);
+constexpr int kDsCons = 4;                           // pipelines: consumer warps 0-3
+constexpr int kDsProd0 = kDsCons;                    // producer warps 4-7
+constexpr int kDsBook = 2 * kDsCons;                 // bookkeeping warp 8
+constexpr int kDsSel0 = kDsBook + 1;                 // selection warps 9-10
+constexpr int kDsSelW = 2;
+constexpr int kDsThreads = 32 * (kDsSel0 + kDsSelW);
 constexpr int kDsST = 32 * kDsSelW;                  // selection threads
-constexpr int kDsStages = 2 * kDsCons;               // ring slots: two per consumer warp
+constexpr int kDsStages = 2 * kDsCons;               // ring slots: two per pipeline
 constexpr int kDsData = 16384;                       // keys, or K then V rows, of one stage
 constexpr int kDsQSlot = 4096;                       // the stage's query rows (<= 16 of 256 B)
 constexpr int kDsStage = kDsData + kDsQSlot;
@@ -60,22 +62,20 @@ constexpr int kDsKeyRows = 64;                       // indexer keys per scoring
 constexpr int kDsScoreStages = 2;                    // stages per scoring task
 constexpr int kDsTaskKeys = kDsKeyRows * kDsScoreStages;
 constexpr int kDsRows = 32;                          // K/V rows per attention stage
-constexpr int kDsTaskStages = 8;                     // stages per attention task
+constexpr int kDsTaskStages = 4;                     // stages per attention task
 constexpr int kDsTaskRows = kDsRows * kDsTaskStages;  // selected rows per attention task
-constexpr int kDsSub = 4;                            // partials per attention task (stage index mod 4)
 constexpr int kDsBins = 2048;                        // 11-bit digits of the order key
 constexpr int kDsCand = 1024;                        // candidates kept in shared memory
 constexpr int kDsMaxN = 32768;                       // scores per group the selection handles
 constexpr int kDsMaxR = 16;                          // query rows per group
-constexpr int kDsRec = 64;                           // bookkeeping records in flight
-constexpr int kDsJobs = 64;                          // owned selections / merges in flight
-constexpr int kDsChunk = 4096;                       // scores per chunk of a pass over them
-constexpr int kDsClaim = 4;                          // tasks a producer claims per atomic
+constexpr int kDsRecW = 16;                          // records in flight per pipeline
+constexpr int kDsJobsW = 16;                         // owned selections / merges per producer
+constexpr int kDsChunk = 32 * kDsST;                 // scores per chunk of a pass over them
+constexpr int kDsClaim = 1;                          // tasks a producer claims per atomic
 constexpr int kDsSelScratch = (kDsBins * 4 + 2 * (kDsMaxN / 8) + 2 * kDsCand * 4) / 8;  // float2 slots
 constexpr int kDsMaxMerge = kDsSelScratch - kDsMaxR;  // (partial, row) pairs a merge takes
-static_assert(kDsChunk == 32 * kDsST, "a pass gives each selection thread one bitmap word per chunk");
 
-enum : int { kTaskScore = 0, kTaskAttend = 1, kTaskEnd = 2 };
+enum : int { kTaskScore = 0, kTaskAttend = 1, kTaskEnd = 2, kTaskFin = 3 };
 
 struct StageMeta {
     int kind, g, task, j0, nrows, sgi, nst, pad;
@@ -92,17 +92,22 @@ struct DsLayout {
     static constexpr int oScore = oChunk + 2 * kDsChunk * 4;  // f32[4][64] per consumer warp
     static constexpr int oMeta = oScore + kDsCons * 64 * 4;   // StageMeta[kDsStages]
     static constexpr int oBars = oMeta + kDsStages * (int)sizeof(StageMeta);
-    // full[S], empty[S], rec_full[R], rec_free[R], chunk[2]
-    static constexpr int kBars = 2 * kDsStages + 2 * kDsRec + 2;
-    static constexpr int oRec = oBars + kBars * 8;            // int2[kDsRec]
-    static constexpr int oJobs = oRec + kDsRec * 8;           // int[2][kDsJobs]: selections, merges
-    static constexpr int oMisc = oJobs + 2 * kDsJobs * 4;     // flags, ring indices, broadcast
-    static constexpr int kMisc = 256;
+    // full[S], empty[S], rec_full[4][R], rec_free[4][R], chunk[2]
+    static constexpr int kBars = 2 * kDsStages + 2 * kDsCons * kDsRecW + 2;
+    static constexpr int oRec = oBars + kBars * 8;            // int2[4][kDsRecW]
+    static constexpr int oJobs = oRec + kDsCons * kDsRecW * 8;  // int[2][4][kDsJobsW]: selections, merges
+    static constexpr int oMisc = oJobs + 2 * kDsCons * kDsJobsW * 4;  // flags, ring indices, broadcast
+    static constexpr int kMisc = 512;
     static constexpr int kBytes = oMisc + kMisc + 1024;       // + slack for 1024-byte alignment
     static_assert(kDsStage % 1024 == 0, "stages must stay 1024-byte aligned (128-byte swizzle)");
     static_assert(oChunk - oHist == kDsSelScratch * 8, "the selection scratch is one area");
     static_assert(kBytes <= 232448, "shared memory per CTA");
 };
+
+// Offsets in the misc area.
+constexpr int kMiAbort = 0, kMiBusy = 4, kMiWork = 8 /* kind, group */, kMiCandN = 16, kMiCpar = 20 /* [2] */,
+              kMiConsumed = 32 /* [4] */, kMiIssued = 48 /* [4] */, kMiJobIdx = 64 /* [4 producers][4] */,
+              kMiBc = 128 /* [16] */, kMiWt = 192 /* [kDsSelW] */;
 
 struct DsParams {
     const uint8_t* q_idx;  // [NG, V, 128] 16-bit
@@ -115,12 +120,11 @@ struct DsParams {
     float* lse;            // [B, V, Hq]
     int32_t* err;
     uint32_t* ctrl;        // [0] next task, [1] CTAs finished
-    uint32_t* gstate;      // [NG][4]: scoring stages done, attention stages done, selection ready
+    uint32_t* gstate;      // [NG][4]: scoring tasks done, attention tasks done, selection ready
     uint32_t* hist;        // [NG][2048]
-    float* part_o;         // [NG][AG * kDsSub][R][128]
-    float* part_ml;        // [NG][AG * kDsSub][R][2]
+    float* part_o;         // [NG][AG][R][128]
+    float* part_ml;        // [NG][AG][R][2]
     int B, V, Hq, Hkv, G, R, T, N, k, block, NG, SG, AG, L, n_rows;
-    int SGS, AGS;          // scoring / attention stages per group (the counters' targets)
     int tma_blocks;        // block % 32 == 0: a stage's 32 rows are one contiguous run
     float scale_log2;
     unsigned long long wait_ns;
@@ -148,22 +152,16 @@ SD_DEVINL Task decode_task(const DsParams& p, uint32_t t) {
     return {kTaskAttend, p.NG - p.L + (int)(t / p.AG), (int)(t % p.AG)};
 }
 
-// Stages of attention task `part` (at least one, for an empty selection).
-SD_DEVINL int task_stages(const DsParams& p, int part) {
-    const int rows = max(0, min(kDsTaskRows, p.n_rows - part * kDsTaskRows));
-    return rows > 0 ? (rows + kDsRows - 1) / kDsRows : 1;
-}
-
 // A bounded mbarrier wait that also gives up as soon as another role raised the abort flag.
+// Between checks of the deadline and the flag the thread sleeps in the barrier (up to 20 us,
+// woken when the phase completes), so waiting warps leave the issue slots to working ones.
 SD_DEVINL bool ds_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag, uint64_t limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 15u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > limit) return false;
-        }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit) return false;
     }
 }
 
@@ -350,10 +348,6 @@ SD_DEVINL void attend_stage(const uint8_t* st, int lane, const uint32_t (&qf)[8]
 
 // ------------------------------------------------------------------ selection
 
-// The selection code runs about once per SM and launch, from a cold instruction cache: it is
-// kept small (out-of-line passes, a mode switch instead of a copy per pass kind) rather than
-// unrolled.
-
 struct SelSmem {
     uint32_t* hist;   // [2048]
     uint32_t* sel;    // [kDsMaxN / 32]
@@ -380,9 +374,10 @@ SD_DEVINL void sel_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kDsST) : "memory
 
 // Sum of v over the selection threads above this one (descending: up = false) or below it
 // (ascending: up = true), in every thread.
-__device__ __noinline__ uint32_t sel_scan_excl(uint32_t v, int sst, SelSmem& S, bool up) {
+SD_DEVINL uint32_t sel_scan_excl(uint32_t v, int sst, const SelSmem& S, bool up) {
     const int lane = sst & 31, w = sst >> 5;
     uint32_t x = v;
+#pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const uint32_t y = up ? __shfl_up_sync(0xffffffffu, x, o) : __shfl_down_sync(0xffffffffu, x, o);
         if (up ? lane >= o : lane + o < 32) x += y;
@@ -390,6 +385,7 @@ __device__ __noinline__ uint32_t sel_scan_excl(uint32_t v, int sst, SelSmem& S, 
     if (lane == (up ? 31 : 0)) S.wt[w] = x;
     sel_bar();
     uint32_t r = x - v;
+#pragma unroll
     for (int u = 0; u < kDsSelW; ++u)
         if (up ? u < w : u > w) r += S.wt[u];
     sel_bar();  // wt may be reused after this
@@ -399,15 +395,17 @@ __device__ __noinline__ uint32_t sel_scan_excl(uint32_t v, int sst, SelSmem& S, 
 // In the 2048-bin histogram S.hist, the bin d where the count of entries in bins above d is
 // < target <= that count plus hist[d] (1 <= target <= the total): writes d, the count above
 // and hist[d] to S.bc[o .. o+2], visible to every thread on return.
-__device__ __noinline__ void sel_find_bin(uint32_t target, int o, int sst, SelSmem& S) {
+SD_DEVINL void sel_find_bin(uint32_t target, int o, int sst, const SelSmem& S) {
     constexpr int per = kDsBins / kDsST;
+    const uint32_t* h = S.hist + sst * per;
     uint32_t loc = 0;
-    for (int j = 0; j < per; ++j) loc += S.hist[sst * per + ((j + sst) & (per - 1))];
+#pragma unroll 8
+    for (int j = 0; j < per; ++j) loc += h[(j + sst) & (per - 1)];
     const uint32_t above = sel_scan_excl(loc, sst, S, false);
     if (above < target && target <= above + loc) {
         uint32_t cum = above;
         for (int j = per - 1; j >= 0; --j) {
-            const uint32_t c = S.hist[sst * per + j];
+            const uint32_t c = h[j];
             if (cum + c >= target) {
                 S.bc[o] = sst * per + j;
                 S.bc[o + 1] = (int)cum;
@@ -427,39 +425,41 @@ struct PassArg {
     uint32_t p22, thr;
 };
 
-// The bit an entry with order key `key` sets in the selection (sel) and tie bitmaps, or the
-// histogram bin it adds to (hbin >= 0), for pass modes other than kPassFirst.
+// For pass modes other than kPassFirst: whether an entry with order key `key` sets its bit in
+// the selection (sel) and tie bitmaps, and the histogram bin it adds to (hbin >= 0).
 SD_DEVINL void pass_decide(const PassArg& a, uint32_t key, bool& sel, bool& tie, int& hbin) {
-    const int dg = (int)(key >> 21);
+    const bool inD = (int)(key >> 21) == a.D;
     sel = tie = false;
     hbin = -1;
     switch (a.mode) {
-        case kPassSelD: sel = dg == a.D; break;
-        case kPassHist2: hbin = dg == a.D ? (int)((key >> 10) & 2047u) : -1; break;
-        case kPassSelP22: sel = dg == a.D && (key >> 10) >= a.p22; break;
+        case kPassSelD: sel = inD; break;
+        case kPassHist2: hbin = inD ? (int)((key >> 10) & 2047u) : -1; break;
+        case kPassSelP22: sel = inD && (key >> 10) >= a.p22; break;
         case kPassHist3: hbin = (key >> 10) == a.p22 ? (int)(key & 1023u) : -1; break;
-        case kPassSelThr: sel = dg == a.D && key >= a.thr; break;
+        case kPassSelThr: sel = inD && key >= a.thr; break;
         default:  // kPassSelTie
-            sel = dg == a.D && key > a.thr;
-            tie = dg == a.D && key == a.thr;
+            sel = inD && key > a.thr;
+            tie = inD && key == a.thr;
             break;
     }
 }
 
-// One pass over the group's N scores (N a multiple of 4: the scores come in chunks of
-// kDsChunk through two shared-memory buffers filled by 1-D bulk copies, one copy in flight
-// while the other chunk is read).  In a chunk, selection thread t owns bitmap word t (scores
-// 32t .. 32t + 31 of the chunk): it builds the word's bits in a register, so no bitmap
-// update is atomic.  kPassFirst sets the bits above digit D and keeps the digit-D entries as
-// candidates, allocated once per warp and chunk.  Ends with a selection barrier.
-__device__ __noinline__ void score_pass(PassArg a, const float* sc, int N, int sst, SelSmem& S) {
+// One pass over the group's N scores (N a multiple of 4) in chunks of kDsChunk, through two
+// shared-memory buffers filled by 1-D bulk copies (one copy in flight while the other chunk is
+// read).  In a chunk, selection thread t owns bitmap word t (scores 32t .. 32t + 31 of the
+// chunk) and builds its bits in a register, so no bitmap update is atomic.  kPassFirst sets
+// the bits above digit D and keeps the digit-D entries as candidates, allocated once per warp
+// and chunk.  Ends with a selection barrier.
+SD_DEVINL void score_pass(const PassArg& a, const float* sc, int N, int sst, const SelSmem& S) {
     const int lane = sst & 31;
     const int nch = (N + kDsChunk - 1) / kDsChunk;
-    uint32_t par[2] = {S.cpar[0], S.cpar[1]};
+    uint32_t par0 = S.cpar[0], par1 = S.cpar[1];
+    float* chunk = S.chunk;
+    uint64_t* cbar = S.cbar;
     auto issue = [&](int c, int b) {
         const uint32_t bytes = (uint32_t)min(kDsChunk, N - c * kDsChunk) * 4u;
-        mbar_arrive_expect_tx(&S.cbar[b], bytes);
-        bulk_g2s(S.chunk + b * kDsChunk, sc + (size_t)c * kDsChunk, bytes, &S.cbar[b]);
+        mbar_arrive_expect_tx(&cbar[b], bytes);
+        bulk_g2s(chunk + b * kDsChunk, sc + (size_t)c * kDsChunk, bytes, &cbar[b]);
     };
     if (sst == 0) {
         // the scores were written by other CTAs (generic stores, acquired through the group's
@@ -468,13 +468,16 @@ __device__ __noinline__ void score_pass(PassArg a, const float* sc, int N, int s
         issue(0, 0);
         if (nch > 1) issue(1, 1);
     }
+    uint32_t* sel = S.sel;
+    uint32_t* tie = S.tie;
     for (int c = 0; c < nch; ++c) {
         const int b = c & 1;
-        if (!mbar_wait(&S.cbar[b], par[b], S.lim)) *S.abort_flag = 1;
-        par[b] ^= 1u;
+        if (!mbar_wait(&cbar[b], b ? par1 : par0, S.lim)) *S.abort_flag = 1;
+        if (b) par1 ^= 1u;
+        else par0 ^= 1u;
         const int base = c * kDsChunk + 32 * sst;  // this thread's 32 scores
         const int nin = max(0, min(32, N - base));
-        const float4* b4 = reinterpret_cast<const float4*>(S.chunk + b * kDsChunk) + 8 * sst;
+        const float4* b4 = reinterpret_cast<const float4*>(chunk + b * kDsChunk) + 8 * sst;
         // the thread's 32 keys in read order: key[4j + e] is score 4 * ((j + sst) & 7) + e of its
         // word (the rotated order makes a quarter warp read 8 distinct bank groups)
         uint32_t key[32];
@@ -486,18 +489,18 @@ __device__ __noinline__ void score_pass(PassArg a, const float* sc, int N, int s
             key[4 * j + 2] = float_key(v.z);
             key[4 * j + 3] = float_key(v.w);
         }
-        auto bitpos = [&](int e) { return 4 * (((e >> 2) + sst) & 7) + (e & 3); };
         const int w = base >> 5;
         if (a.mode == kPassFirst) {
             uint32_t above = 0, cnt = 0;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                const int bp = bitpos(e);
+                const int bp = 4 * (((e >> 2) + sst) & 7) + (e & 3);
                 const int dg = (int)(key[e] >> 21);
-                if (bp < nin && dg > a.D) above |= 1u << bp;
-                if (bp < nin && dg == a.D) ++cnt;
+                const uint32_t in = bp < nin ? 1u : 0u;
+                above |= (in & (dg > a.D ? 1u : 0u)) << bp;
+                cnt += in & (dg == a.D ? 1u : 0u);
             }
-            if (nin > 0) S.sel[w] = above;
+            if (nin > 0) sel[w] = above;
             // candidates: one shared atomic per warp, then each thread writes its own
             uint32_t incl = cnt;
 #pragma unroll
@@ -512,7 +515,7 @@ __device__ __noinline__ void score_pass(PassArg a, const float* sc, int N, int s
             if (cnt > 0) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const int bp = bitpos(e);
+                    const int bp = 4 * (((e >> 2) + sst) & 7) + (e & 3);
                     if (bp < nin && (int)(key[e] >> 21) == a.D) {
                         if (slot < (uint32_t)kDsCand) {
                             S.cidx[slot] = base + bp;
@@ -526,20 +529,17 @@ __device__ __noinline__ void score_pass(PassArg a, const float* sc, int N, int s
             uint32_t sw = 0, tw = 0;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                const int bp = bitpos(e);
+                const int bp = 4 * (((e >> 2) + sst) & 7) + (e & 3);
                 bool sl, tl;
                 int hb;
                 pass_decide(a, key[e], sl, tl, hb);
-                if (bp < nin) {
-                    if (sl) sw |= 1u << bp;
-                    if (tl) tw |= 1u << bp;
-                    if (hb >= 0) atomicAdd(&S.hist[hb], 1u);
-                }
+                const uint32_t in = bp < nin ? 1u : 0u;
+                sw |= (in & (sl ? 1u : 0u)) << bp;
+                tw |= (in & (tl ? 1u : 0u)) << bp;
+                if (in && hb >= 0) atomicAdd(&S.hist[hb], 1u);
             }
-            if (nin > 0) {
-                if (sw) S.sel[w] |= sw;
-                if (tw) S.tie[w] |= tw;
-            }
+            if (sw) sel[w] |= sw;
+            if (tw) tie[w] |= tw;
         }
         sel_bar();  // every thread is done with buffer b
         if (sst == 0 && c + 2 < nch) {
@@ -548,15 +548,15 @@ __device__ __noinline__ void score_pass(PassArg a, const float* sc, int N, int s
         }
     }
     if (sst == 0) {
-        S.cpar[0] = par[0];
-        S.cpar[1] = par[1];
+        S.cpar[0] = par0;
+        S.cpar[1] = par1;
     }
     sel_bar();
 }
 
 // One pass over the candidates (every one has digit D; never kPassFirst).  Ends with a
 // selection barrier.
-__device__ __noinline__ void cand_pass(PassArg a, int n, int sst, SelSmem& S) {
+SD_DEVINL void cand_pass(const PassArg& a, int n, int sst, const SelSmem& S) {
     for (int c = sst; c < n; c += kDsST) {
         bool sl, tl;
         int hb;
@@ -572,13 +572,14 @@ __device__ __noinline__ void cand_pass(PassArg a, int n, int sst, SelSmem& S) {
 // The group's exact top-k: ascending indices of the k entries first in (score desc, index
 // asc), written to p.idx[g]; the group's histogram is read and zeroed.  All kDsST selection
 // threads call it.
-__device__ __noinline__ void select_group(const DsParams& p, int g, int sst, SelSmem& S) {
+SD_DEVINL void select_group(const DsParams& p, int g, int sst, const SelSmem& S) {
     const int N = p.N, k = p.k;
     const float* sc = p.scores + (size_t)g * N;
     uint32_t* gh = p.hist + (size_t)g * kDsBins;
     int32_t* out = p.idx + (size_t)g * k;
 
-    // 1. the top digit D from the histogram the scoring stages built (then zeroed for next time)
+    // 1. the top digit D from the histogram the scoring tasks built (then zeroed for next time)
+#pragma unroll 4
     for (int j = sst; j < kDsBins / 4; j += kDsST) {
         uint4* g4 = reinterpret_cast<uint4*>(gh) + j;
         *reinterpret_cast<uint4*>(S.hist + 4 * j) = __ldcg(g4);
@@ -661,60 +662,60 @@ __device__ __noinline__ void select_group(const DsParams& p, int g, int sst, Sel
     }
 }
 
-// The group's output: the merge of its attention partials in a fixed order (task by task,
-// sub-partial by sub-partial).  All kDsST selection threads call it: the partials' (m, l) go
-// to shared memory, threads r < R turn them into each partial's weight 2^(m - M) / L for
-// their row, then thread c sums column c.
-__device__ __noinline__ void merge_group(const DsParams& p, int g, int sst, SelSmem& S) {
-    const int NP = p.AG * kDsSub, R = p.R;
+// The group's output: the merge of its AG attention partials in task order.  All kDsST
+// selection threads call it: the partials' (m, l) go to shared memory, warp u reduces rows
+// u, u + kDsSelW, ... (the row maximum M and sum L over the partials) and turns each
+// partial's m into its weight 2^(m - M) / L, then every (row, 4-column) pair sums its
+// partials.
+SD_DEVINL void merge_group(const DsParams& p, int g, int sst, const SelSmem& S) {
+    const int NP = p.AG, R = p.R;
+    const int lane = sst & 31, sw = sst >> 5;
     const int b = g / p.Hkv, kvh = g % p.Hkv;
     const size_t base = (size_t)g * NP * R;
     float2* ml = S.scratch;              // [NP * R]: (m, l), then (weight, -)
     float2* rowML = S.scratch + NP * R;  // [R]: (M, L)
     const float2* gml = reinterpret_cast<const float2*>(p.part_ml) + base;
-    for (int e = sst; e < NP * R; e += kDsST) {
-        // a task of nst stages wrote sub-partials 0 .. min(nst, kDsSub) - 1
-        const int pi = e / R;
-        ml[e] = pi % kDsSub < task_stages(p, pi / kDsSub) ? __ldcg(gml + e) : make_float2(-INFINITY, 0.f);
-    }
+    for (int e = sst; e < NP * R; e += kDsST) ml[e] = __ldcg(gml + e);
     sel_bar();
-    if (sst < R) {
+    for (int r = sw; r < R; r += kDsSelW) {
         float M = -INFINITY;
-        for (int t = 0; t < NP; ++t) M = fmaxf(M, ml[t * R + sst].x);
-        float L = 0.f;
-        for (int t = 0; t < NP; ++t) {
-            const float2 x = ml[t * R + sst];
-            if (x.x != -INFINITY) L = fmaf(x.y, exp2f(x.x - M), L);
+        for (int t = lane; t < NP; t += 32) M = fmaxf(M, ml[t * R + r].x);
+        M = warp_max(M);
+        float Ls = 0.f;
+        for (int t = lane; t < NP; t += 32) {
+            const float2 x = ml[t * R + r];
+            if (x.x != -INFINITY) Ls = fmaf(x.y, exp2f(x.x - M), Ls);
         }
-        for (int t = 0; t < NP; ++t) {
-            const float mt = ml[t * R + sst].x;
-            ml[t * R + sst].x = (mt == -INFINITY || !(L > 0.f)) ? 0.f : exp2f(mt - M) / L;
+        Ls = warp_sum(Ls);
+        for (int t = lane; t < NP; t += 32) {
+            const float mt = ml[t * R + r].x;
+            ml[t * R + r].x = (mt == -INFINITY || !(Ls > 0.f)) ? 0.f : exp2f(mt - M) / Ls;
         }
-        rowML[sst] = make_float2(M, L);
+        if (lane == 0) rowML[r] = make_float2(M, Ls);
     }
     sel_bar();
-    for (int r = 0; r < R; ++r) {
-        const float* po = p.part_o + (base + r) * 128 + sst;
-        float o = 0.f;
-        int t = 0;
-        for (; t + 8 <= NP; t += 8) {
-            float x[8];
+    for (int pr = sst; pr < R * 32; pr += kDsST) {
+        const int r = pr >> 5, c4 = pr & 31;
+        const float4* po = reinterpret_cast<const float4*>(p.part_o + (base + r) * 128) + c4;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int t0 = 0; t0 < NP; t0 += 16) {
+            float4 x[16];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float wgt = ml[(t + u) * R + r].x;
-                x[u] = wgt != 0.f ? __ldcg(po + (size_t)(t + u) * R * 128) : 0.f;
+            for (int u = 0; u < 16; ++u)
+                x[u] = t0 + u < NP ? __ldcg(po + (size_t)(t0 + u) * R * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const float wgt = t0 + u < NP ? ml[(t0 + u) * R + r].x : 0.f;
+                o.x = fmaf(wgt, x[u].x, o.x);
+                o.y = fmaf(wgt, x[u].y, o.y);
+                o.z = fmaf(wgt, x[u].z, o.z);
+                o.w = fmaf(wgt, x[u].w, o.w);
             }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) o = fmaf(ml[(t + u) * R + r].x, x[u], o);
-        }
-        for (; t < NP; ++t) {
-            const float wgt = ml[t * R + r].x;
-            if (wgt != 0.f) o = fmaf(wgt, __ldcg(po + (size_t)t * R * 128), o);
         }
         const int v = r / p.G, gi = r % p.G;
         const size_t qrow = ((size_t)b * p.V + v) * p.Hq + (size_t)kvh * p.G + gi;
-        p.out[qrow * 128 + sst] = o;
-        if (sst == 0) {
+        reinterpret_cast<float4*>(p.out + qrow * 128)[c4] = o;
+        if (c4 == 0) {
             const float2 x = rowML[r];
             p.lse[qrow] = x.y > 0.f ? (x.x + log2f(x.y)) * 0.69314718055994530942f : -INFINITY;
         }
@@ -734,64 +735,58 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     uint8_t* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::oBars);
     uint64_t* empty = full + kDsStages;
-    uint64_t* rec_full = empty + kDsStages;
-    uint64_t* rec_free = rec_full + kDsRec;
-    uint64_t* cbar = rec_free + kDsRec;
+    uint64_t* rec_full = empty + kDsStages;       // [4][kDsRecW]
+    uint64_t* rec_free = rec_full + kDsCons * kDsRecW;
+    uint64_t* cbar = rec_free + kDsCons * kDsRecW;
     StageMeta* meta = reinterpret_cast<StageMeta*>(sm + L::oMeta);
-    int2* rec = reinterpret_cast<int2*>(sm + L::oRec);
-    volatile int* jobs_sel = reinterpret_cast<volatile int*>(sm + L::oJobs);
-    volatile int* jobs_mer = jobs_sel + kDsJobs;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::oMisc);
-    volatile uint32_t* consumed = reinterpret_cast<volatile uint32_t*>(sm + L::oMisc + 4);  // [4]
-    volatile uint32_t* issued = reinterpret_cast<volatile uint32_t*>(sm + L::oMisc + 20);
-    volatile uint32_t* js = reinterpret_cast<volatile uint32_t*>(sm + L::oMisc + 24);  // sel head, tail, mer head, tail
-    volatile uint32_t* cand_n = reinterpret_cast<volatile uint32_t*>(sm + L::oMisc + 40);
-    volatile int* work = reinterpret_cast<volatile int*>(sm + L::oMisc + 44);  // kind, group, finish
-    volatile uint32_t* cpar = reinterpret_cast<volatile uint32_t*>(sm + L::oMisc + 56);
-    int* bc = reinterpret_cast<int*>(sm + L::oMisc + 64);             // [16]
-    uint32_t* wt = reinterpret_cast<uint32_t*>(sm + L::oMisc + 128);  // [kDsSelW]
+    int2* rec = reinterpret_cast<int2*>(sm + L::oRec);  // [4][kDsRecW]
+    volatile int* jobs = reinterpret_cast<volatile int*>(sm + L::oJobs);  // [2][4][kDsJobsW]
+    uint8_t* misc = sm + L::oMisc;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + kMiAbort);
+    volatile int* busy = reinterpret_cast<volatile int*>(misc + kMiBusy);
+    volatile int* work = reinterpret_cast<volatile int*>(misc + kMiWork);
+    volatile uint32_t* consumed = reinterpret_cast<volatile uint32_t*>(misc + kMiConsumed);
+    volatile uint32_t* issued = reinterpret_cast<volatile uint32_t*>(misc + kMiIssued);
+    volatile uint32_t* jidx = reinterpret_cast<volatile uint32_t*>(misc + kMiJobIdx);  // [w][sel head, tail, mer head, tail]
     const uint64_t lim = p.wait_ns;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < kDsStages; ++s) {
             mbar_init(&full[s], 32);
-            mbar_init(&empty[s], 1);  // the consumer warp that owns the slot
+            mbar_init(&empty[s], 1);  // the pipeline's consumer warp
         }
-        for (int r = 0; r < kDsRec; ++r) {
+        for (int r = 0; r < kDsCons * kDsRecW; ++r) {
             mbar_init(&rec_full[r], 1);
             mbar_init(&rec_free[r], 1);
         }
         mbar_init(&cbar[0], 1);
         mbar_init(&cbar[1], 1);
-        *abort_flag = 0;
-        for (int j = 0; j < 4; ++j) consumed[j] = 0;
-        *issued = 0;
-        for (int j = 0; j < 4; ++j) js[j] = 0;
-        work[0] = work[1] = work[2] = 0;
-        cpar[0] = cpar[1] = 0;
+        for (int j = 0; j < L::kMisc / 4; ++j) reinterpret_cast<volatile uint32_t*>(misc)[j] = 0u;
         fence_mbarrier_init();
     }
     __syncthreads();
     pdl_wait();  // the inputs and the workspace counters are the preceding kernels' results
 
-    if (warp == kDsProd) {
-        // ------------------------------------------------------------ producer
+    if (warp >= kDsProd0 && warp < kDsProd0 + kDsCons) {
+        // ------------------------------------------------------------ producer of pipeline w
+        const int w = warp - kDsProd0;
         const uint64_t pol = l2_evict_first_policy();
-        uint32_t i = 0;  // stages filled
+        uint32_t n = 0;  // stages filled into the pipeline: stage n is slot 2w + (n & 1)
         bool ok = true;
-        // the next free slot (all lanes); false on an abort
-        auto take_slot = [&](uint32_t n) -> bool {
-            return warp_wait(&empty[n % kDsStages], ((n / kDsStages) & 1u) ^ 1u, abort_flag, lim);
+        auto take_slot = [&]() -> int {  // the next free slot (all lanes), -1 on an abort
+            const int s = 2 * w + (int)(n & 1u);
+            return warp_wait(&empty[s], ((n >> 1) & 1u) ^ 1u, abort_flag, lim) ? s : -1;
         };
-        // this CTA owns a selection or merge (lane 0 queues it for the selection warps); false
-        // when the queue stayed full
-        auto own = [&](volatile int* ring, int hi, int g) -> bool {
+        // this CTA owns a selection (which 0) or merge (1) of group g: queued for the bookkeeper
+        auto own = [&](int which, int g) -> bool {
             bool got = true;
             if (lane == 0) {
-                if (js[hi] - js[hi - 1] >= (uint32_t)kDsJobs) {
+                volatile uint32_t* hd = jidx + 4 * w + 2 * which;  // head, tail
+                volatile int* ring = jobs + (which * kDsCons + w) * kDsJobsW;
+                if (hd[1] - hd[0] >= (uint32_t)kDsJobsW) {
                     const uint64_t t0 = globaltimer_ns();
-                    while (js[hi] - js[hi - 1] >= (uint32_t)kDsJobs) {
+                    while (hd[1] - hd[0] >= (uint32_t)kDsJobsW) {
                         __nanosleep(256);
                         if (*abort_flag || globaltimer_ns() - t0 > lim) {
                             got = false;
@@ -800,9 +795,9 @@ __global__ void __launch_bounds__(kDsThreads, 1)
                     }
                 }
                 if (got) {
-                    ring[js[hi] % kDsJobs] = g;
+                    ring[hd[1] % kDsJobsW] = g;
                     __threadfence_block();
-                    js[hi] = js[hi] + 1u;
+                    hd[1] = hd[1] + 1u;
                 }
             }
             return __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
@@ -817,42 +812,42 @@ __global__ void __launch_bounds__(kDsThreads, 1)
                 t_end = t_next + kDsClaim;
             }
             const uint32_t t = t_next++;
-            if (t >= p.total) {
-                // one end marker per consumer warp
-                for (int w = 0; w < kDsCons && ok; ++w) {
-                    if (!take_slot(i)) {
-                        ok = false;
-                        break;
-                    }
-                    const int s = (int)(i % kDsStages);
-                    if (lane == 0) meta[s].kind = kTaskEnd;
-                    __syncwarp();
-                    mbar_arrive(&full[s]);
-                    ++i;
+            if (t >= p.total) {  // the pipeline's end marker
+                const int s = take_slot();
+                if (s < 0) {
+                    ok = false;
+                    break;
                 }
+                if (lane == 0) meta[s].kind = kTaskEnd;
+                __syncwarp();
+                mbar_arrive(&full[s]);
+                ++n;
                 break;
             }
             const Task tk = decode_task(p, t);
             if (tk.kind == kTaskScore) {
-                if (tk.part == p.SG - 1 && !own(jobs_sel, 1, tk.g)) {
+                if (tk.part == p.SG - 1 && !own(0, tk.g)) {
                     ok = false;
                     break;
                 }
-                for (int sgi = 0; sgi < kDsScoreStages; ++sgi) {
-                    const int j0 = tk.part * kDsTaskKeys + sgi * kDsKeyRows;
-                    if (j0 >= p.N && sgi > 0) break;  // past the group's end (only a tail)
-                    if (!take_slot(i)) {
+                const int j0t = tk.part * kDsTaskKeys;
+                const int nst = min(kDsScoreStages, (p.N - j0t + kDsKeyRows - 1) / kDsKeyRows);
+                for (int sgi = 0; sgi < nst; ++sgi) {
+                    const int s = take_slot();
+                    if (s < 0) {
                         ok = false;
                         break;
                     }
-                    const int s = (int)(i % kDsStages);
                     uint8_t* st = sm + s * kDsStage;
+                    const int j0 = j0t + sgi * kDsKeyRows;
                     if (lane == 0) {
                         StageMeta& m = meta[s];
                         m.kind = kTaskScore;
                         m.g = tk.g;
                         m.j0 = j0;
-                        m.nrows = max(0, min(kDsKeyRows, p.N - j0));
+                        m.nrows = min(kDsKeyRows, p.N - j0);
+                        m.sgi = sgi;
+                        m.nst = nst;
                         const uint32_t qb = (uint32_t)p.V * 256u;
                         mbar_arrive_expect_tx(&full[s], kDsData + qb);
                         const int row = tk.g * p.N + j0;
@@ -862,11 +857,11 @@ __global__ void __launch_bounds__(kDsThreads, 1)
                     } else {
                         mbar_arrive(&full[s]);
                     }
-                    ++i;
+                    ++n;
                 }
                 continue;
             }
-            if (tk.part == p.AG - 1 && !own(jobs_mer, 3, tk.g)) {
+            if (tk.part == p.AG - 1 && !own(1, tk.g)) {
                 ok = false;
                 break;
             }
@@ -878,7 +873,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
                 if (lane == 0 && ld_acquire_gpu(ready) == 0u) {
                     const uint64_t t0 = globaltimer_ns();
                     for (;;) {
-                        __nanosleep(128);
+                        __nanosleep(256);
                         if (ld_acquire_gpu(ready) != 0u) break;
                         if (*abort_flag || globaltimer_ns() - t0 > lim) {
                             got = false;
@@ -896,11 +891,11 @@ __global__ void __launch_bounds__(kDsThreads, 1)
             const int g = tk.g, b = g / p.Hkv, kvh = g % p.Hkv;
             const int r0 = tk.part * kDsTaskRows;
             const int rows = max(0, min(kDsTaskRows, p.n_rows - r0));
-            const int nst = task_stages(p, tk.part);
+            const int nst = rows > 0 ? (rows + kDsRows - 1) / kDsRows : 1;
             const uint32_t qbytes = (uint32_t)p.G * 256u;
             const int32_t* sel_row = p.idx + (size_t)g * p.k;
             // every selected row of the task at once (one round trip): lane l resolves task row
-            // 32q + l, q < 8, to its K/V row (-1: none, or skipped as out of range)
+            // 32q + l, q < kDsTaskStages, to its K/V row (-1: none, or skipped as out of range)
             long long src[kDsTaskStages];
 #pragma unroll
             for (int q = 0; q < kDsTaskStages; ++q) {
@@ -919,11 +914,11 @@ __global__ void __launch_bounds__(kDsThreads, 1)
 #pragma unroll
             for (int sgi = 0; sgi < kDsTaskStages; ++sgi) {
                 if (sgi >= nst || !ok) break;
-                if (!take_slot(i)) {
+                const int s = take_slot();
+                if (s < 0) {
                     ok = false;
                     break;
                 }
-                const int s = (int)(i % kDsStages);
                 uint8_t* st = sm + s * kDsStage;
                 const int nrows = max(0, min(kDsRows, rows - sgi * kDsRows));
                 const long long ra = src[sgi];
@@ -986,28 +981,29 @@ __global__ void __launch_bounds__(kDsThreads, 1)
                         cp_async_mbar_arrive_noinc(&full[s]);
                     }
                 }
-                ++i;
+                ++n;
             }
         }
         if (!ok) *abort_flag = 1;
-        if (lane == 0) *issued = i;
+        if (lane == 0) issued[w] = n;
     } else if (warp < kDsCons) {
-        // ------------------------------------------------------------ consumers
-        float* sbuf = reinterpret_cast<float*>(sm + L::oScore) + warp * 64;
+        // ------------------------------------------------------------ consumer of pipeline w
+        const int w = warp;
+        float* sbuf = reinterpret_cast<float*>(sm + L::oScore) + w * 64;
         uint32_t qf[8][4];
         AttAcc acc;
         const bool two_halves = p.R > 8;
         bool ok = true;
-        // stage i = 4n + warp: ring slot i % 8, record slot i % kDsRec
+        uint32_t nrec = 0;  // records posted
         for (uint32_t n = 0;; ++n) {
-            const uint32_t i = 4u * n + (uint32_t)warp;
-            const int s = (int)(i % kDsStages);
-            if (!warp_wait(&full[s], (i / kDsStages) & 1u, abort_flag, lim)) {
+            const int s = 2 * w + (int)(n & 1u);
+            if (!warp_wait(&full[s], (n >> 1) & 1u, abort_flag, lim)) {
                 ok = false;
                 break;
             }
             const StageMeta m = meta[s];
             const uint8_t* st = sm + s * kDsStage;
+            bool post = m.kind == kTaskEnd;
             if (m.kind == kTaskScore) {
                 score_tile<F16>(st, lane, p.V, sbuf);
                 __syncwarp();
@@ -1023,9 +1019,10 @@ __global__ void __launch_bounds__(kDsThreads, 1)
                     if (in && lane == __ffs(peers) - 1)
                         atomicAdd(&p.hist[(size_t)m.g * kDsBins + dg], (uint32_t)__popc(peers));
                 }
+                post = m.sgi == m.nst - 1;
             } else if (m.kind == kTaskAttend) {
                 load_q_frags(st, lane, p.R, qf);
-                if (m.sgi < kDsSub) {  // the first of this warp's stages of the task
+                if (m.sgi == 0) {
 #pragma unroll
                     for (int nt = 0; nt < 16; ++nt)
 #pragma unroll
@@ -1036,9 +1033,9 @@ __global__ void __launch_bounds__(kDsThreads, 1)
                 attend_stage(st, lane, qf, two_halves, m.valid, p.scale_log2, acc);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
-                if (m.sgi + kDsSub >= m.nst) {  // this warp's last stage of the task: its partial
+                if (m.sgi == m.nst - 1) {  // the task's partial
                     const int g8 = lane >> 2, t4 = lane & 3;
-                    const size_t pb = (((size_t)m.g * p.AG + m.task) * kDsSub + (m.sgi % kDsSub)) * p.R;
+                    const size_t pb = ((size_t)m.g * p.AG + m.task) * p.R;
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         const int r = g8 + 8 * hf;
@@ -1050,25 +1047,115 @@ __global__ void __launch_bounds__(kDsThreads, 1)
                         if (t4 == 0)
                             *reinterpret_cast<float2*>(p.part_ml + (pb + r) * 2) = make_float2(acc.m[hf], acc.l[hf]);
                     }
+                    post = true;
                 }
             }
-            if (lane == 0) consumed[warp] = n + 1;
-            // the stage's record (its kind and group; an end marker for kTaskEnd)
-            const int slot = (int)(i % kDsRec);
-            if (i >= (uint32_t)kDsRec && !warp_wait(&rec_free[slot], ((i / kDsRec) & 1u) ^ 1u, abort_flag, lim)) {
-                ok = false;
-                break;
+            if (lane == 0) consumed[w] = n + 1;
+            if (post) {  // the task's record: its kind and group (an end marker for kTaskEnd)
+                const int slot = w * kDsRecW + (int)(nrec % kDsRecW);
+                if (nrec >= (uint32_t)kDsRecW &&
+                    !warp_wait(&rec_free[slot], ((nrec / kDsRecW) & 1u) ^ 1u, abort_flag, lim)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) rec[slot] = make_int2(m.kind, m.g);
+                __syncwarp();  // the warp's stores before its arrival (release)
+                if (lane == 0) mbar_arrive(&rec_full[slot]);
+                ++nrec;
             }
-            if (lane == 0) rec[slot] = make_int2(m.kind, m.g);
-            __syncwarp();  // the warp's stores before its arrival (release)
-            if (lane == 0) mbar_arrive(&rec_full[slot]);
             if (m.kind == kTaskEnd) break;
         }
         if (!ok) *abort_flag = 1;
+    } else if (warp == kDsBook) {
+        // ------------------------------------------------------------ bookkeeping
+        uint32_t ra[kDsCons] = {0u, 0u, 0u, 0u};  // records taken per pipeline
+        int ends = 0;
+        uint64_t last_progress = globaltimer_ns();
+        bool fin = false;
+        while (!fin) {
+            bool progress = false;
+            // 1. the records each pipeline posted so far move the groups' counters: one fence for
+            // the batch (release of the consumers' stores behind the records), then plain adds
+#pragma unroll
+            for (int w = 0; w < kDsCons; ++w) {
+                int nb = 0;
+                if (lane == 0)
+                    while (nb < kDsRecW && mbar_try_wait(&rec_full[w * kDsRecW + (ra[w] + nb) % kDsRecW],
+                                                         ((ra[w] + nb) / kDsRecW) & 1u))
+                        ++nb;
+                nb = __shfl_sync(0xffffffffu, nb, 0);
+                if (nb == 0) continue;
+                progress = true;
+                int kind = -1, gg = 0;
+                if (lane < nb) {
+                    const int r = w * kDsRecW + (int)((ra[w] + lane) % kDsRecW);
+                    (void)mbar_try_wait(&rec_full[r], ((ra[w] + lane) / kDsRecW) & 1u);  // acquire
+                    const int2 rc = rec[r];
+                    kind = rc.x;
+                    gg = rc.y;
+                    mbar_arrive(&rec_free[r]);
+                }
+                fence_acq_rel_gpu();
+                if (lane < nb && kind != kTaskEnd)
+                    atomicAdd(&p.gstate[(size_t)gg * 4 + (kind == kTaskScore ? 0 : 1)], 1u);
+                ends += __popc(__ballot_sync(0xffffffffu, lane < nb && kind == kTaskEnd));
+                ra[w] += (uint32_t)nb;
+            }
+            // 2. when the selection warps are idle: an owned selection or merge whose group is
+            // complete (acquire), or the end
+            int post = -1, pg = 0;
+            if (lane == 0 && *busy == 0) {
+                bool pending = false;
+                for (int which = 0; which < 2 && post < 0; ++which)
+                    for (int w = 0; w < kDsCons && post < 0; ++w) {
+                        volatile uint32_t* hd = jidx + 4 * w + 2 * which;
+                        if (hd[0] == hd[1]) continue;
+                        pending = true;
+                        __threadfence_block();
+                        const int g = jobs[(which * kDsCons + w) * kDsJobsW + hd[0] % kDsJobsW];
+                        const uint32_t target = (uint32_t)(which == 0 ? p.SG : p.AG);
+                        if (ld_acquire_gpu(&p.gstate[(size_t)g * 4 + which]) == target) {
+                            post = which == 0 ? kTaskScore : kTaskAttend;
+                            pg = g;
+                            hd[0] = hd[0] + 1u;
+                        }
+                    }
+                const uint64_t now = globaltimer_ns();
+                if (post >= 0 || progress) {
+                    last_progress = now;
+                } else if (ends == kDsCons && !pending) {
+                    post = kTaskFin;  // no more records, no owned work left
+                } else if (*abort_flag || now - last_progress > lim) {
+                    *abort_flag = 1;
+                    post = kTaskFin;
+                }
+            } else if (lane == 0 && (*abort_flag || globaltimer_ns() - last_progress > lim)) {
+                // the selection warps are busy; on an abort, wait for them (bounded) and end
+                const uint64_t t0 = globaltimer_ns();
+                while (*busy != 0 && globaltimer_ns() - t0 < lim) __nanosleep(256);
+                *abort_flag = 1;
+                post = kTaskFin;
+            }
+            post = __shfl_sync(0xffffffffu, post, 0);
+            pg = __shfl_sync(0xffffffffu, pg, 0);
+            if (post >= 0) {
+                if (lane == 0) {
+                    work[0] = post;
+                    work[1] = pg;
+                    *busy = 1;
+                    __threadfence_block();
+                }
+                __syncwarp();
+                // hand it to the selection warps (they wait at barrier 2)
+                asm volatile("bar.arrive 2, %0;" ::"n"(32 + kDsST) : "memory");
+                fin = post == kTaskFin;
+            } else if (!progress) {
+                __nanosleep(64);
+            }
+        }
     } else {
-        // ------------------------------------------------------------ bookkeeping + selection
+        // ------------------------------------------------------------ selection
         const int sst = tid - 32 * kDsSel0;
-        const int sw = sst >> 5;
         SelSmem S;
         S.hist = reinterpret_cast<uint32_t*>(sm + L::oHist);
         S.sel = reinterpret_cast<uint32_t*>(sm + L::oSel);
@@ -1078,74 +1165,16 @@ __global__ void __launch_bounds__(kDsThreads, 1)
         S.scratch = reinterpret_cast<float2*>(sm + L::oHist);
         S.chunk = reinterpret_cast<float*>(sm + L::oChunk);
         S.cbar = cbar;
-        S.cpar = cpar;
-        S.cand_n = cand_n;
-        S.bc = bc;
-        S.wt = wt;
+        S.cpar = reinterpret_cast<volatile uint32_t*>(misc + kMiCpar);
+        S.cand_n = reinterpret_cast<volatile uint32_t*>(misc + kMiCandN);
+        S.bc = reinterpret_cast<int*>(misc + kMiBc);
+        S.wt = reinterpret_cast<uint32_t*>(misc + kMiWt);
         S.abort_flag = abort_flag;
         S.lim = lim;
-        uint32_t a = 0;          // records taken (selection warp 0)
-        int ends = 0;            // consumer warps whose end marker was counted (selection warp 0)
-        uint64_t last_progress = 0;
         for (;;) {
-            if (sw == 0) {
-                // 1. the records the consumers posted so far move the groups' counters
-                int nb = 0;
-                if (lane == 0)
-                    while (nb < 32 && mbar_try_wait(&rec_full[(a + nb) % kDsRec], ((a + nb) / kDsRec) & 1u)) ++nb;
-                nb = __shfl_sync(0xffffffffu, nb, 0);
-                int kind = -1, gg = 0;
-                if (lane < nb) {
-                    const uint32_t r = (a + (uint32_t)lane) % kDsRec;
-                    (void)mbar_try_wait(&rec_full[r], ((a + lane) / kDsRec) & 1u);  // acquire
-                    const int2 rc = rec[r];
-                    kind = rc.x;
-                    gg = rc.y;
-                    mbar_arrive(&rec_free[r]);
-                    // release: the consumers' stores behind the record
-                    if (kind != kTaskEnd) red_add_release_gpu(&p.gstate[(size_t)gg * 4 + (kind == kTaskScore ? 0 : 1)], 1u);
-                }
-                ends += __popc(__ballot_sync(0xffffffffu, lane < nb && kind == kTaskEnd));
-                a += (uint32_t)nb;
-                // 2. an owned selection or merge whose group is complete (acquire)
-                int wk = -1, wg = 0, fin = 0;
-                if (lane == 0) {
-                    if (js[0] != js[1]) {
-                        const int g = jobs_sel[js[0] % kDsJobs];
-                        if (ld_acquire_gpu(&p.gstate[(size_t)g * 4 + 0]) == (uint32_t)p.SGS) {
-                            wk = kTaskScore;
-                            wg = g;
-                            js[0] = js[0] + 1u;
-                        }
-                    }
-                    if (wk < 0 && js[2] != js[3]) {
-                        const int g = jobs_mer[js[2] % kDsJobs];
-                        if (ld_acquire_gpu(&p.gstate[(size_t)g * 4 + 1]) == (uint32_t)p.AGS) {
-                            wk = kTaskAttend;
-                            wg = g;
-                            js[2] = js[2] + 1u;
-                        }
-                    }
-                    const uint64_t now = globaltimer_ns();
-                    if (wk >= 0 || nb > 0 || last_progress == 0) {
-                        last_progress = now;
-                    } else if (ends == kDsCons && js[0] == js[1] && js[2] == js[3]) {
-                        fin = 1;  // nothing left: no more records, no owned work
-                    } else if (*abort_flag || now - last_progress > lim) {
-                        *abort_flag = 1;
-                        fin = 1;
-                    } else {
-                        __nanosleep(64);
-                    }
-                    work[0] = wk;
-                    work[1] = wg;
-                    work[2] = fin;
-                }
-                __syncwarp();
-            }
-            sel_bar();
+            asm volatile("bar.sync 2, %0;" ::"n"(32 + kDsST) : "memory");  // the bookkeeper's hand-off
             const int wk = work[0], wg = work[1];
-            const bool fin = work[2] != 0;
+            if (wk == kTaskFin) break;
             if (wk == kTaskScore) {
                 select_group(p, wg, sst, S);
                 sel_bar();  // every part of the selection is written: publish it
@@ -1154,15 +1183,18 @@ __global__ void __launch_bounds__(kDsThreads, 1)
                     fence_acq_rel_gpu();
                     st_release_gpu(p.gstate + (size_t)wg * 4 + 2, 1u);
                 }
-            } else if (wk == kTaskAttend) {
+            } else {
                 merge_group(p, wg, sst, S);
                 if (sst == 0) {
                     p.gstate[(size_t)wg * 4 + 1] = 0u;
                     p.gstate[(size_t)wg * 4 + 2] = 0u;
                 }
             }
-            sel_bar();  // the work word may be rewritten after this
-            if (fin) break;
+            sel_bar();
+            if (sst == 0) {
+                __threadfence_block();
+                *busy = 0;
+            }
         }
     }
 
@@ -1170,10 +1202,10 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     if (tid == 0) {
         if (*abort_flag) {
             report(p.err, SD_DEVERR_TIMEOUT);
-            // let the stages filled but not consumed land before the CTA exits: stage j belongs
-            // to consumer warp j % 4, which got through its first consumed[j % 4] stages
-            for (uint32_t j = 0; j < *issued; ++j)
-                if (j / kDsCons >= consumed[j % kDsCons]) mbar_wait(&full[j % kDsStages], (j / kDsStages) & 1u, lim);
+            // let the stages filled but not consumed land before the CTA exits
+            for (int w = 0; w < kDsCons; ++w)
+                for (uint32_t j = consumed[w]; j < issued[w]; ++j)
+                    mbar_wait(&full[2 * w + (int)(j & 1u)], (j >> 1) & 1u, lim);
         }
         // the last CTA to finish resets the task counter for the next call
         __threadfence();
@@ -1189,7 +1221,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
 namespace {
 
 struct StepPlan {
-    int NG, N, SG, AG, SGS, AGS, R, L, n_rows;
+    int NG, N, SG, AG, R, L, n_rows;
     size_t o_gstate, o_hist, o_part_o, o_part_ml, bytes;
 };
 
@@ -1200,10 +1232,8 @@ StepPlan plan_step(const sd_decode_step_args* a) {
     sp.NG = a->B * a->Hkv;
     sp.N = a->block > 0 ? a->T / a->block : 0;
     sp.SG = std::max(1, (sp.N + kDsTaskKeys - 1) / kDsTaskKeys);
-    sp.SGS = std::max(1, (sp.N + kDsKeyRows - 1) / kDsKeyRows);
     sp.n_rows = a->n_idx * a->block;
     sp.AG = std::max(1, (sp.n_rows + kDsTaskRows - 1) / kDsTaskRows);
-    sp.AGS = std::max(1, (sp.n_rows + kDsRows - 1) / kDsRows);
     sp.R = (a->Hkv > 0 ? a->Hq / a->Hkv : 0) * a->V;
     if (a->lag > 0) {
         sp.L = a->lag;
@@ -1221,9 +1251,9 @@ StepPlan plan_step(const sd_decode_step_args* a) {
     sp.o_hist = off;
     off += round256((size_t)sp.NG * kDsBins * 4);
     sp.o_part_o = off;
-    off += round256((size_t)sp.NG * sp.AG * kDsSub * sp.R * 128 * 4);
+    off += round256((size_t)sp.NG * sp.AG * sp.R * 128 * 4);
     sp.o_part_ml = off;
-    off += round256((size_t)sp.NG * sp.AG * kDsSub * sp.R * 2 * 4);
+    off += round256((size_t)sp.NG * sp.AG * sp.R * 2 * 4);
     sp.bytes = off;
     return sp;
 }
@@ -1255,7 +1285,7 @@ sd_status validate_step(const sd_decode_step_args* a) {
     SD_REQUIRE((long long)a->B * a->Hkv * a->T < (1LL << 31), "%s: B*Hkv*T must be < 2^31", who);
     SD_REQUIRE((long long)a->n_idx * a->block <= (1LL << 30), "%s: selection too large", who);
     const long long ag = std::max(1LL, ((long long)a->n_idx * a->block + kDsTaskRows - 1) / kDsTaskRows);
-    if (ag * kDsSub * (a->Hq / a->Hkv) * a->V > kDsMaxMerge) {
+    if (ag * (a->Hq / a->Hkv) * a->V > kDsMaxMerge) {
         set_error("%s: %lld selected rows per group with %d query rows exceed the merge (at most %d (partial, row) pairs)",
                   who, (long long)a->n_idx * a->block, (a->Hq / a->Hkv) * a->V, kDsMaxMerge);
         return SD_ERR_UNSUPPORTED;
@@ -1326,8 +1356,6 @@ extern "C" sd_status sd_decode_step(const sd_decode_step_args* a, void* stream) 
     p.NG = sp.NG;
     p.SG = sp.SG;
     p.AG = sp.AG;
-    p.SGS = sp.SGS;
-    p.AGS = sp.AGS;
     p.L = sp.L;
     p.n_rows = sp.n_rows;
     p.tma_blocks = a->block % kDsRows == 0 ? 1 : 0;

@@ -68,6 +68,20 @@ SD_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to `hint_ns` (it resumes as soon as the phase
+// completes): a waiting warp then takes no issue slots from the warps that work.
+SD_DEVINL bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns false when the
 // deadline (limit_ns of wall-clock time, 1 s by default) passed first.
 SD_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitDeadlineNs) {
