@@ -12,7 +12,9 @@ Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and a
 synchronize; each step is timed with CUDA events on the launching stream, and a buffer
 larger than L2 is written between timed steps (outside the events).  Rank 0 prints one
 JSON line; under torchrun every rank runs its own full workload (weak scaling) and the
-time is the maximum over ranks.
+time is the maximum over ranks.  ``--gpus N`` (N > 1) run outside torchrun launches the N
+local ranks itself (torch.distributed.run on 127.0.0.1), or fails when fewer than N GPUs
+are visible.
 
 ``--impl reference`` times the plain CPU oracle (the slow fp64 reference the kernels are
 checked against) on this machine's host cores, on a bounded sample of the same workload.
@@ -1333,7 +1335,36 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def spawn_command(gpus: int, argv, port: int):
+    """The command that runs this benchmark as `gpus` local ranks, one per GPU."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", str(gpus),
+            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + list(argv)
+
+
+def self_spawn(args, argv):
+    """--gpus N > 1 without a torchrun environment: run N local ranks under
+    torch.distributed.run and return their exit status (an error, not a silent one-GPU run,
+    when fewer GPUs are visible).  None when this process is already a rank or N == 1."""
+    if args.gpus <= 1 or "WORLD_SIZE" in os.environ:
+        return None
+    if args.impl == "ours":
+        import torch
+        have = torch.cuda.device_count()
+        if have < args.gpus:
+            print(f"bench.py: --gpus {args.gpus} needs {args.gpus} visible GPUs, found {have}", file=sys.stderr)
+            return 2
+    return subprocess.call(spawn_command(args.gpus, argv, free_port()))
+
+
 def main(argv=None):
+    raw_argv = list(sys.argv[1:] if argv is None else argv)
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -1353,9 +1384,14 @@ def main(argv=None):
     ap.add_argument("--tiered-path", choices=("staged", "fused"), default="staged",
                     help="tiered workloads: stage the selected host rows into HBM with one copy kernel "
                          "before the attention (staged), or read them inside the fused select/attend")
-    args = ap.parse_args(argv)
+    args = ap.parse_args(raw_argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    rc = self_spawn(args, raw_argv)
+    if rc is not None:
+        if rc != 0:
+            raise SystemExit(rc)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -241,7 +241,8 @@ sd_status sd_gather_attend(const sd_attend_args* args, void* stream);
  * compiled into the library, which every GPU that loads the library holds until exit.
  * It allocates nothing.  On the first call made on each device (with that device
  * current) the array's device address is looked up and the array is cleared once: make
- * that first call before any stream capture.  All calls share the array and it keeps the
+ * that first call before any stream capture.  The address is kept for the life of the
+ * process, so do not use this call on a device after cudaDeviceReset.  All calls share the array and it keeps the
  * last call's contents (nothing in it needs to start at zero), so calls whose kernels
  * overlap on the GPU race on the array.  A request
  * whose split-K partials need more than 16 MiB returns SD_ERR_INVALID_ARG without

@@ -90,3 +90,39 @@ def test_reference_arm_prints_its_line(monkeypatch, capsys):
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "queries/s"
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_gpus_n_without_torchrun_spawns_n_ranks_for_the_reference_arm():
+    # the reference arm under N self-spawned ranks: rank 0 alone prints its line
+    import json
+    import subprocess
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "3", "--workload", "c1_tiny"],
+                       capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1 and lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
+
+
+def test_gpus_n_without_enough_gpus_is_an_error():
+    import subprocess
+
+    import torch
+    if torch.cuda.device_count() >= 64:
+        pytest.skip("a machine with 64 GPUs")
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "64", "--steps", "1",
+                        "--warmup", "3"], capture_output=True, text=True, timeout=300, env=env, cwd=ROOT)
+    assert r.returncode != 0 and "visible GPUs" in r.stderr
+    assert not any(x.startswith("{") for x in r.stdout.splitlines())
+
+
+def test_spawn_command_runs_torchrun_on_localhost():
+    sys.path.insert(0, ROOT)
+    import bench
+    cmd = bench.spawn_command(4, ["--steps", "5"], 12345)
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert cmd[cmd.index("--nproc-per-node") + 1] == "4"
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert cmd[-2:] == ["--steps", "5"]

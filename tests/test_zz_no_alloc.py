@@ -33,6 +33,16 @@ def _case(seed, B=2, Hq=32, Hkv=8, d=128, T=8192, k=512):
     return q, K, V, idx
 
 
+def _oracle(q, K, V, idx):
+    import math
+
+    import oracle
+    B, _, Hq, d = q.shape
+    Hkv, T, k = K.shape[1], K.shape[2], idx.shape[-1]
+    return oracle.gather_attend(q.cpu(), K.cpu(), V.cpu(), idx.cpu().numpy(), B, 1, Hq, Hkv, d, T, k, 1,
+                                1 / math.sqrt(d))[:2]
+
+
 def test_noalloc_matches_the_workspace_call_twice_in_a_row(sd):
     for seed in (1, 2):   # two calls in a row share (and reuse) the static scratch
         q, K, V, idx = _case(seed)
@@ -44,8 +54,28 @@ def test_noalloc_matches_the_workspace_call_twice_in_a_row(sd):
         a.workspace, a.workspace_bytes = None, 0      # no caller scratch at all
         sd.sd_gather_attend_noalloc(a)
         torch.cuda.synchronize()
-        assert_attend_close(out, out_ref.double().cpu().numpy())
-        assert_attend_close(lse, lse_ref.double().cpu().numpy(), "lse")
+        # the same split plan and kernels as the workspace call: the same bits
+        assert torch.equal(out, out_ref) and torch.equal(lse, lse_ref)
+        ro, rl = _oracle(q, K, V, idx)
+        assert_attend_close(out, ro)
+        assert_attend_close(lse, rl, "lse")
+
+
+def test_noalloc_partials_of_a_larger_split_do_not_leak_into_a_smaller_one(sd):
+    # more splits first, then fewer, with nothing cleared in between: the second call reads
+    # only the partials it wrote itself
+    q, K, V, idx = _case(4)
+    ro, rl = _oracle(q, K, V, idx)
+    for splits in (16, 3):
+        a_ref, out_ref, lse_ref, _ = sd.make_attend_args(q, K, V, idx, T=K.shape[2], splits=splits)
+        need = sd.sd_gather_attend_workspace_bytes(a_ref)
+        sd.sd_gather_attend(a_ref, torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda"))
+        a, out, lse, _ = sd.make_attend_args(q, K, V, idx, T=K.shape[2], splits=splits)
+        sd.sd_gather_attend_noalloc(a)
+        torch.cuda.synchronize()
+        assert torch.equal(out, out_ref) and torch.equal(lse, lse_ref), splits
+        assert_attend_close(out, ro)
+        assert_attend_close(lse, rl, "lse")
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(sd):

@@ -12,7 +12,9 @@
 // The array is kNoAllocScratchBytes (16 MiB) of device memory that every GPU which loads
 // the library holds until the process exits.  On the first call made while a device is
 // current, its device address is looked up with cudaGetSymbolAddress and the array is
-// cleared once with cudaMemset (so make that first call before any stream capture).  All
+// cleared once with cudaMemset (so make that first call before any stream capture).  The
+// address is kept for the life of the process: after cudaDeviceReset it would be stale, so
+// the call must not be used on a device that was reset.  All
 // calls share the one array and it keeps whatever the last call left there.  The split
 // partials are rewritten by every call before they are read, so nothing in the array needs
 // to start at zero.

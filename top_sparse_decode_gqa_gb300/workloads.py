@@ -45,7 +45,8 @@ available here):
   steps whose 8 verify queries slide along a sequence of 23 indexer queries (each step
   drops the oldest and adds one), so consecutive selections overlap; residency is kept per
   (sequence, KV head) -- every head starts from the generated resident positions -- and the
-  pool is a cache: each step promotes its selected host rows into it before the attention.
+  pool is a cache: each step stages the selected rows the pool lacks, attends, and then
+  promotes those rows from the stage into the pool (beside the next step's selection).
 
 Value recipe: indexer query and keys are integers drawn uniformly from [-8, 8] (exact in
 bf16 and fp32); attention q, K, V are standard normal, rounded to bf16 (nearest even)
