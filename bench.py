@@ -253,6 +253,8 @@ class SparseDecodeStep:
             block=w.block, T=w.T, err_word=self.err, **kw)
         need = 0 if self.fused else sd.sd_gather_attend_workspace_bytes(self.args)
         self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=device)
+        if need > 0 and not self.step_kernel:
+            self.launches_per_step += 1  # the split-K merge kernel
         if self.staged:
             self.stage = sd.stage_buffers(self.args, self.q.dtype, device)
             self.counter = sd.stage_counter(device)
@@ -296,6 +298,46 @@ class SparseDecodeStep:
             sd.sd_gather_attend(self.args, self.ws)
         if m is not None:
             m.end.record()
+
+    def packed_io(self):
+        """Moves the step's per-step inputs (q, q_idx) into one device buffer and its results
+        (out, lse, idx) into another, re-points the calls at them, and returns (d_in, d_out,
+        calls): one copy brings a step's inputs, one copy returns its results, and `calls` are
+        the step's C-ABI calls with their arguments marshalled once (one ctypes call per kernel).
+        K/V resident in HBM only."""
+        import torch
+        sd = self.sd
+        assert not self.tiered
+
+        def pack(tensors):
+            sizes = [t.numel() * t.element_size() for t in tensors]
+            offs = [sum((n + 255) // 256 * 256 for n in sizes[:i]) for i in range(len(sizes))]
+            buf = torch.empty(offs[-1] + (sizes[-1] + 255) // 256 * 256, dtype=torch.uint8, device=self.dev)
+            views = []
+            for t, o, n in zip(tensors, offs, sizes):
+                v = buf[o:o + n].view(t.dtype).view(t.shape)
+                v.copy_(t)
+                views.append(v)
+            return buf, views
+
+        d_in, (self.q, self.q_idx) = pack([self.q, self.q_idx])
+        d_out, (self.out, self.lse, self.idx) = pack([self.out, self.lse, self.idx])
+        if self.step_kernel:
+            a = self.step_args
+            a.q, a.q_idx = self.q.data_ptr(), self.q_idx.data_ptr()
+            a.out, a.lse, a.idx = self.out.data_ptr(), self.lse.data_ptr(), self.idx.data_ptr()
+            calls = [sd.prepare_decode_step(a)]
+        else:
+            a = self.args
+            a.q, a.out, a.lse = self.q.data_ptr(), self.out.data_ptr(), self.lse.data_ptr()
+            calls = [sd.prepare_index_score(self.q_idx, self.keys, self.scores, self.err, key_hist=self.key_hist)]
+            if self.fused:
+                calls.append(sd.prepare_select_attend(self.scores, a, self.idx, key_hist=self.key_hist))
+            else:
+                a.idx = self.idx.data_ptr()
+                calls += [sd.prepare_topk(self.scores, self.w.k, self.idx, key_hist=self.key_hist),
+                          sd.prepare_gather_attend(a, self.ws)]
+        return d_in, d_out, calls
 
     def after_warmup(self):
         """Counts the selected rows that live in host memory (fixed by the inputs)."""
@@ -924,89 +966,18 @@ def host_link_gbs(device, nbytes=256 << 20, reps=5):
 # ----------------------------------------------------------------------------- arms
 
 
-def run_ours(args):
+def step_report(step, w, workload, kmarks, dom_ms, ms_per_step, peak, device, K, clean_l2):
+    """The step's roofline record (bytes, t_roof, fraction, per-kernel times) from its timed
+    steps, and the committed ncu traffic of its dominant kernel (None when stale)."""
     import torch
-    from top_sparse_decode_gqa_gb300 import build as cuda_build
-    from top_sparse_decode_gqa_gb300.workloads import WORKLOADS, generate
-
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=device)
-    if rank == 0:
-        cuda_build.build()
-    if world > 1:
-        dist.barrier()
-    w = WORKLOADS[args.workload]
-    x = generate(w)
-    step = make_step(w, x, device, "separate" if args.separate else args.path, args.tiered_path,
-                     not args.no_lookahead)
-    props = torch.cuda.get_device_properties(device)
-    flush = torch.empty(2 * max(int(getattr(props, "L2_cache_size", 0)), 128 << 20), dtype=torch.uint8,
-                        device=device)
-
-    def clean_l2():
-        # write a buffer of 2x L2, then read it back so the step starts on a cold, clean L2
-        flush.fill_(1)
-        flush.view(torch.int32).sum()
-
-    for _ in range(args.warmup):
-        clean_l2()
-        step.run()
-    torch.cuda.synchronize()
-    if int(step.err.item()) != 0:
-        raise RuntimeError(f"device error word {int(step.err.item())}")
-    step.after_warmup()
-
-    # Timed region 1 (the headline): K steps with one event pair per step, so nothing
-    # between the step's kernels breaks their programmatic overlap.  Timed region 2: the
-    # same steps with events around every kernel, for the per-kernel roofline.
-    K = args.steps
-    K2 = min(K, 500)
-    marks = [StepMarks(0) for _ in range(K)]
-    kmarks = [StepMarks(step.dominant_per_step, step.phases) for _ in range(K2)]
-    clocks = ClockSampler(local)
-    clocks.start()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.mark(True)
-    for i in range(K):
-        clean_l2()
-        step.run(marks[i])
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    for i in range(K2):
-        clean_l2()
-        step.run(kmarks[i])
-    torch.cuda.synchronize()
-    clocks.mark(False)
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop()
-
-    step_ms = [m.step_ms() for m in marks]
-    dom_ms = [t for m in kmarks for t in m.dominant_ms()]
-    total_s = reduce_max(sum(step_ms) / 1e3, world, device)
-    value = aggregate(w.queries_per_step * K, world, total_s)
-    ms_per_step = total_s * 1e3 / K
-
-    e2e = measure_e2e(step, w, x, clean_l2, K=min(K, 200))
-
-    peak, peak_kind = load_peaks()
     by = step.bytes()
-    dom_s = statistics.mean(dom_ms) / 1e3
-    achieved = by["dominant"] / dom_s / 1e9
     if isinstance(step, SparseDecodeStep) and step.step_kernel:
         kernel_file, kernel_tag = ("decode_step.cu", "tc_common.cuh", "sd_common.cuh"), "decode_step"
     elif isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep, LookaheadStep, CachedTieredStep)):
         kernel_file, kernel_tag = ("index_score.cu", "index_score_tc.cu", "tc_common.cuh", "sd_common.cuh"), "index_score"
     else:
         kernel_file, kernel_tag = ("gather_attend.cu", "sd_common.cuh"), "gather_attend"
-    traffic = profiled_traffic(args.workload, kernel_tag, source_digest(*kernel_file))
+    traffic = profiled_traffic(workload, kernel_tag, source_digest(*kernel_file))
     step_s = ms_per_step / 1e3
     step_roof = {"bound": "hbm", "hbm_bytes": by["hbm"], "unit": "GB/s",
                  "achieved": round(by["hbm"] / step_s / 1e9, 1)}
@@ -1103,6 +1074,138 @@ def run_ours(args):
     else:
         step_roof["kernel_us"] = {"gather_attend_per_layer": round(statistics.mean(dom_ms) * 1e3, 2),
                                   "layers": w.layers}
+    return traffic, step_roof
+
+
+def measure_extra(name, args, device, local, clean_l2, peak, steps=20, warmup=3):
+    """A compact measurement of another workload in the same run (the T = 131072 configurations
+    beside the headline): the default path, `warmup` untimed steps, then `steps` steps timed with
+    one event pair each and `steps` more with events around every kernel; L2 flushed before
+    every step, clocks sampled meanwhile.  Returns the record attached to the JSON line."""
+    import torch
+    from top_sparse_decode_gqa_gb300.workloads import WORKLOADS, generate
+    w = WORKLOADS[name]
+    x = generate(w)
+    step = make_step(w, x, device, "auto", "staged", True)
+    for _ in range(warmup):
+        clean_l2()
+        step.run()
+    torch.cuda.synchronize()
+    if int(step.err.item()) != 0:
+        raise RuntimeError(f"{name}: device error word {int(step.err.item())}")
+    step.after_warmup()
+    marks = [StepMarks(0) for _ in range(steps)]
+    kmarks = [StepMarks(step.dominant_per_step, step.phases) for _ in range(steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    torch.cuda.synchronize()
+    clocks.mark(True)
+    for i in range(steps):
+        clean_l2()
+        step.run(marks[i])
+    torch.cuda.synchronize()
+    for i in range(steps):
+        clean_l2()
+        step.run(kmarks[i])
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    clk = clocks.stop()
+    ms_per_step = sum(m.step_ms() for m in marks) / steps
+    dom_ms = [t for m in kmarks for t in m.dominant_ms()]
+    _, step_roof = step_report(step, w, name, kmarks, dom_ms, ms_per_step, peak, device, steps, clean_l2)
+    rec = {"value": round(w.queries_per_step / (ms_per_step / 1e3), 1), "unit": "queries/s",
+           "ms_per_step": round(ms_per_step, 5), "steps": steps, "warmup": warmup,
+           "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "T": w.T, "k": w.k,
+                      "block": w.block, "V": w.V, "resident_frac": w.resident_frac,
+                      "path": ("indexer + top-k + host-row staging + gather-attend" if getattr(step, "staged", False)
+                               else "indexer + top-k + gather-attend")},
+           "step_roofline": step_roof, "clocks": clk,
+           "gpu_launches": step.launches_per_step * steps}
+    del step, x
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_ours(args):
+    import torch
+    from top_sparse_decode_gqa_gb300 import build as cuda_build
+    from top_sparse_decode_gqa_gb300.workloads import WORKLOADS, generate
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    if rank == 0:
+        cuda_build.build()
+    if world > 1:
+        dist.barrier()
+    w = WORKLOADS[args.workload]
+    x = generate(w)
+    step = make_step(w, x, device, "separate" if args.separate else args.path, args.tiered_path,
+                     not args.no_lookahead)
+    props = torch.cuda.get_device_properties(device)
+    flush = torch.empty(2 * max(int(getattr(props, "L2_cache_size", 0)), 128 << 20), dtype=torch.uint8,
+                        device=device)
+
+    def clean_l2():
+        # write a buffer of 2x L2, then read it back so the step starts on a cold, clean L2
+        flush.fill_(1)
+        flush.view(torch.int32).sum()
+
+    for _ in range(args.warmup):
+        clean_l2()
+        step.run()
+    torch.cuda.synchronize()
+    if int(step.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(step.err.item())}")
+    step.after_warmup()
+
+    # Timed region 1 (the headline): K steps with one event pair per step, so nothing
+    # between the step's kernels breaks their programmatic overlap.  Timed region 2: the
+    # same steps with events around every kernel, for the per-kernel roofline.
+    K = args.steps
+    K2 = min(K, 500)
+    marks = [StepMarks(0) for _ in range(K)]
+    kmarks = [StepMarks(step.dominant_per_step, step.phases) for _ in range(K2)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark(True)
+    for i in range(K):
+        clean_l2()
+        step.run(marks[i])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    for i in range(K2):
+        clean_l2()
+        step.run(kmarks[i])
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+
+    step_ms = [m.step_ms() for m in marks]
+    dom_ms = [t for m in kmarks for t in m.dominant_ms()]
+    total_s = reduce_max(sum(step_ms) / 1e3, world, device)
+    value = aggregate(w.queries_per_step * K, world, total_s)
+    ms_per_step = total_s * 1e3 / K
+
+    if isinstance(step, SparseDecodeStep) and not step.tiered:
+        e2e = measure_e2e_packed(step, w, clean_l2, K=min(K, 200))
+    else:
+        e2e = measure_e2e(step, w, x, clean_l2, K=min(K, 200))
+
+    peak, peak_kind = load_peaks()
+    by = step.bytes()
+    dom_s = statistics.mean(dom_ms) / 1e3
+    achieved = by["dominant"] / dom_s / 1e9
+    traffic, step_roof = step_report(step, w, args.workload, kmarks, dom_ms, ms_per_step, peak, device, K, clean_l2)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -1157,12 +1260,67 @@ def run_ours(args):
         "gpu_launches": step.launches_per_step * K,
         "clocks": clk,
     }
+    if not args.no_extra and args.workload == DEFAULT_WORKLOAD:
+        # the T = 131072 configurations (block-sparse; tiered verify) measured in the same run
+        line["t131072"] = {name: measure_extra(name, args, device, local, clean_l2, peak)
+                           for name in ("c3_block_sparse", "c4_tiered_verify")}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, x)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def cuda_runtime():
+    """ctypes handle on the CUDA runtime the library uses (already loaded with it)."""
+    import ctypes
+    for name in ("libcudart.so.13", "libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+        except OSError:
+            continue
+        rt.cudaMemcpyAsync.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+        rt.cudaStreamSynchronize.argtypes = [ctypes.c_void_p]
+        return rt
+    raise RuntimeError("the CUDA runtime library was not found")
+
+
+def measure_e2e_packed(step, w, clean_l2, K):
+    """End to end through the C ABI with host buffers, for a step whose inputs and results
+    are packed (SparseDecodeStep.packed_io): per step one host->device copy of the step's
+    queries from pinned memory, the step's C-ABI calls (one ctypes call per kernel), one
+    device->host copy of out, lse and idx into pinned memory, and a stream synchronize; host
+    wall clock per step."""
+    import ctypes
+    import torch
+    d_in, d_out, calls = step.packed_io()
+    h_in = torch.empty(d_in.numel(), dtype=torch.uint8).pin_memory()
+    h_in.copy_(d_in)  # this step's queries, in the packed layout
+    h_out = torch.empty(d_out.numel(), dtype=torch.uint8).pin_memory()
+    rt = cuda_runtime()
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    cin = (ctypes.c_void_p(d_in.data_ptr()), ctypes.c_void_p(h_in.data_ptr()), d_in.numel(), 1, st)
+    cout = (ctypes.c_void_p(h_out.data_ptr()), ctypes.c_void_p(d_out.data_ptr()), d_out.numel(), 2, st)
+    times = []
+    for i in range(K + 3):
+        clean_l2()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        if rt.cudaMemcpyAsync(*cin) != 0:
+            raise RuntimeError("cudaMemcpyAsync (inputs) failed")
+        for c in calls:
+            c()
+        if rt.cudaMemcpyAsync(*cout) != 0:
+            raise RuntimeError("cudaMemcpyAsync (results) failed")
+        if rt.cudaStreamSynchronize(st) != 0:
+            raise RuntimeError("cudaStreamSynchronize failed")
+        if i >= 3:
+            times.append(time.perf_counter() - t0)
+    return {"value": round(w.queries_per_step * len(times) / sum(times), 1), "unit": "queries/s",
+            "h2d_bytes_per_step": int(d_in.numel()), "d2h_bytes_per_step": int(d_out.numel()),
+            "timing": "host wall clock per step incl. one packed copy each way and the stream sync",
+            "ctypes_calls_per_step": len(calls) + 3}
 
 
 def measure_e2e(step, w, x, clean_l2, K):
@@ -1372,6 +1530,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="with the default workload, skip the T = 131072 configurations measured beside it")
     ap.add_argument("--separate", action="store_true",
                     help="run the indexer, top-k and gather-attend as three launches (same as --path separate)")
     ap.add_argument("--path", choices=("auto", "step", "select_attend", "separate"), default="auto",

@@ -222,13 +222,15 @@ def test_c4_fused_select_attend_full():
                                           err_word=e)
     torch.cuda.synchronize()
     assert int(e.item()) == 0
-    # the index sets are sd_topk's (pinned to the oracle by the separate-call test)
-    np.testing.assert_array_equal(idx.cpu().numpy(), sd().sd_topk(scores, w.k).cpu().numpy())
+    # every row's index set (all 32 (b, kvh) rows) is the oracle's union top-2048 of the
+    # 8-query union scores
     i_gpu = idx.cpu().numpy()
+    rs_all = oracle.index_score(x["q_idx"], x["k_idx"], w.B, w.Hkv, w.V, w.T, w.dI)
+    np.testing.assert_array_equal(scores.cpu().numpy().astype(np.float64), rs_all)
+    ri_all = oracle.topk(rs_all, w.k)
+    np.testing.assert_array_equal(i_gpu, ri_all)
     for b, h in ((0, 0), (w.B - 1, w.Hkv - 1)):
-        rs = oracle.index_score(x["q_idx"][b:b + 1, h:h + 1], x["k_idx"][b:b + 1, h:h + 1], 1, 1, w.V, w.T, w.dI)
-        ri = oracle.topk(rs, w.k)
-        np.testing.assert_array_equal(i_gpu[b:b + 1, h:h + 1], ri)
+        ri = ri_all[b:b + 1, h:h + 1]
         qh = x["q"][b:b + 1, :, h * w.G:(h + 1) * w.G].contiguous()
         ro, rl, _ = oracle.gather_attend(qh, x["k"][b:b + 1, h:h + 1].contiguous(),
                                          x["v"][b:b + 1, h:h + 1].contiguous(), ri, 1, w.V, w.G, 1,
@@ -256,6 +258,7 @@ def test_c5_importance_tiering_full():
     weight = 1.0 / (L * Hq)
     ws = None
     s_after_1 = None
+    out_00 = lse_00 = None
     for step in range(w.steps):
         for layer in range(L):
             a, out, lse, _ = sd().make_attend_args(qd[step, layer], ks[layer], vs[layer], None, T=T,
@@ -265,6 +268,8 @@ def test_c5_importance_tiering_full():
                 ws = torch.zeros(max(need, 1), dtype=torch.uint8, device="cuda")
             sd().sd_gather_attend(a, ws)
             sd().sd_score_accumulate(logits, lse, None, s, Hkv, 1, weight, err_word=e)
+            if step == 0 and layer == 0:
+                out_00, lse_00 = out, lse
         if step == 0:
             s_after_1 = s.cpu().numpy().copy()
     torch.cuda.synchronize()
@@ -272,8 +277,11 @@ def test_c5_importance_tiering_full():
     # oracle: step 1 over all layers
     s_ref = np.zeros((B, T))
     for layer in range(L):
-        _, rl, rz = oracle.gather_attend(x["q"][0, layer], x["k"][layer], x["v"][layer], None, B, 1,
-                                         Hq, Hkv, d, T, T, 1, 1 / math.sqrt(d), True)
+        ro, rl, rz = oracle.gather_attend(x["q"][0, layer], x["k"][layer], x["v"][layer], None, B, 1,
+                                          Hq, Hkv, d, T, T, 1, 1 / math.sqrt(d), True)
+        if layer == 0:   # the dense attention of step 1, layer 0
+            assert_attend_close(out_00, ro)
+            assert_attend_close(lse_00, rl, "lse")
         oracle.score_accumulate(rz, rl, None, s_ref, B, 1, Hq, Hkv, T, 1, T, weight)
     np.testing.assert_allclose(s_after_1, s_ref, rtol=1e-5, atol=1e-12)
     s_np = s.cpu().numpy()
@@ -281,15 +289,23 @@ def test_c5_importance_tiering_full():
     np.testing.assert_allclose(s_np.sum(1), float(w.steps), rtol=1e-5)
     tier, counts = sd().sd_tier_classify(s, w.cum_frac)
     t_np, c_np = tier.cpu().numpy(), counts.cpu().numpy()
+    # the oracle's split of the GPU's own scores: the same tier for every position
+    rt, rc = oracle.tier_classify(s_np, w.cum_frac)
+    np.testing.assert_array_equal(t_np, rt)
+    np.testing.assert_array_equal(c_np, rc)
     for b in range(B):
         assert c_np[b].tolist() == [13107, 26214, 19661, 6554]
         for m in range(3):
             assert s_np[b][t_np[b] == m].min() >= s_np[b][t_np[b] == m + 1].max()
-    # int8 storage of the T2 rows of one layer: reconstruction within half a step
+    # int8 storage of the T2 rows of one layer: the oracle's codes and scales bit for bit,
+    # and reconstruction within half a step
     codes, scales = sd().sd_quantize_rows_int8(ks[0], tier)
+    rcodes, rscales = oracle.quantize_rows_int8(x["k"][0], rt, B, Hkv, T, d)
+    np.testing.assert_array_equal(codes.cpu().numpy(), rcodes)   # rows of other tiers stay zero
+    np.testing.assert_array_equal(scales.cpu().numpy(), rscales)
+    t2 = np.broadcast_to((t_np == 2)[:, None, :], (B, Hkv, T))
     xf = x["k"][0].float().numpy()
     cf = codes.cpu().numpy().astype(np.float64) * scales.cpu().numpy()[..., None]
-    t2 = np.broadcast_to((t_np == 2)[:, None, :], (B, Hkv, T))
     err = np.abs(cf - xf)[t2]
     bound = np.broadcast_to(scales.cpu().numpy()[..., None], xf.shape)[t2] * (0.5 + 1e-5)
     assert np.all(err <= bound)

@@ -115,6 +115,8 @@ def lib() -> ctypes.CDLL:
         L.sd_decode_step_workspace_bytes.argtypes = [ctypes.POINTER(sd_decode_step_args)]
         L.sd_decode_step_workspace_bytes.restype = Z
         L.sd_decode_step.argtypes = [ctypes.POINTER(sd_decode_step_args), P]
+        L.sd_stage_host_rows.restype = I
+        L.sd_select_attend.restype = I
         for name in ("sd_index_score", "sd_block_pool", "sd_topk", "sd_gather_attend",
                      "sd_score_accumulate", "sd_tier_classify", "sd_quantize_rows_int8",
                      "sd_gather_attend_noalloc", "sd_decode_step"):
@@ -592,3 +594,56 @@ def decode_step(q_idx, keys, q, k_cache, v_cache, k, workspace=None, stream=None
     a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     sd_decode_step(a, stream)
     return scores, idx, out, lse
+
+
+class PreparedCall:
+    """One C-ABI call with its arguments marshalled once: calling the object invokes the
+    library function directly, with no per-call shape checks, pointer lookups or Python
+    object creation (a step loop then costs one ctypes call per kernel).  The tensors whose
+    pointers it holds must stay alive and in place."""
+
+    def __init__(self, name: str, *args):
+        self.name = name
+        self.fn = getattr(lib(), name)
+        self.args = args
+
+    def __call__(self) -> None:
+        st = self.fn(*self.args)
+        if st != SD_OK:
+            _check(st, self.name)
+
+
+def prepare_index_score(q_idx, k_idx, scores, err_word=None, key_hist=None, stream=None) -> PreparedCall:
+    B, Hkv, V, dI = q_idx.shape
+    return PreparedCall("sd_index_score", _ptr(q_idx), _dtype_code(q_idx), _ptr(k_idx), _dtype_code(k_idx), B, Hkv,
+                        V, k_idx.shape[2], dI, _ptr(scores), _ptr(key_hist), _ptr(err_word), _stream(stream))
+
+
+def prepare_topk(scores, k, idx, key_hist=None, stream=None) -> PreparedCall:
+    N = scores.shape[-1]
+    rows = scores.numel() // N
+    ws_bytes = lib().sd_topk_workspace_bytes(rows, N, k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=scores.device) if ws_bytes else None
+    call = PreparedCall("sd_topk", _ptr(scores), rows, N, k, _ptr(idx), _ptr(key_hist), _ptr(ws), ws_bytes,
+                        _stream(stream))
+    call.keep = ws   # the workspace lives as long as the call
+    return call
+
+
+def prepare_select_attend(scores, args: sd_attend_args, idx, key_hist=None, stream=None) -> PreparedCall:
+    return PreparedCall("sd_select_attend", _ptr(scores), scores.shape[-1], _ptr(key_hist), _ptr(idx),
+                        ctypes.byref(args), _stream(stream))
+
+
+def prepare_gather_attend(args: sd_attend_args, workspace=None, stream=None) -> PreparedCall:
+    if workspace is not None:
+        args.workspace, args.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    return PreparedCall("sd_gather_attend", ctypes.byref(args), _stream(stream))
+
+
+def prepare_stage_host_rows(args: sd_attend_args, counter, stream=None) -> PreparedCall:
+    return PreparedCall("sd_stage_host_rows", ctypes.byref(args), _ptr(counter), _stream(stream))
+
+
+def prepare_decode_step(args: sd_decode_step_args, stream=None) -> PreparedCall:
+    return PreparedCall("sd_decode_step", ctypes.byref(args), _stream(stream))
