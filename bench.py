@@ -201,9 +201,16 @@ class StepMarks:
 
 
 def step_supported(w) -> bool:
-    """Whether sd_decode_step (the whole step in one persistent launch) takes this workload."""
+    """Whether sd_decode_step (the whole step in one launch) takes this workload."""
     return (w.resident_frac >= 1.0 and w.dtype == "bf16" and w.d == 128 and w.dI == 128 and w.V <= 8
             and w.G * w.V <= 16 and w.N <= 32768 and w.N % 4 == 0)
+
+
+def cluster_step_supported(w) -> bool:
+    """Whether sd_decode_step runs this workload as one thread-block cluster per KV group:
+    block selection (whole 16- or 32-row runs of a block) over at most 8192 blocks."""
+    runs = w.block % 16 == 0 and (32 % w.block == 0 if w.block <= 32 else w.block % 32 == 0)
+    return step_supported(w) and runs and w.N <= 8192
 
 
 class SparseDecodeStep:
@@ -222,7 +229,10 @@ class SparseDecodeStep:
         self.sd, self.w, self.dev = sd, w, device
         self.tiered = w.resident_frac < 1.0
         if path == "auto":
-            path = "select_attend" if w.dtype == "bf16" and w.block == 1 and not self.tiered else "separate"
+            # block selection over short score rows: the whole step in one cluster launch;
+            # token selection: indexer + fused select/attend; tiered: the separate calls
+            path = ("step" if cluster_step_supported(w) else
+                    "select_attend" if w.dtype == "bf16" and w.block == 1 and not self.tiered else "separate")
         if path == "step" and not step_supported(w):
             raise ValueError(f"sd_decode_step does not take {w.name}")
         self.path = path
@@ -298,6 +308,45 @@ class SparseDecodeStep:
             sd.sd_gather_attend(self.args, self.ws)
         if m is not None:
             m.end.record()
+
+    def rotation(self, n):
+        """n input sets in distinct device memory (set 0 is the step's own tensors; the others
+        are copies of q, q_idx, the keys and the K/V cache), each as the list of the step's
+        C-ABI calls with their arguments marshalled once.  Steps run back to back over the sets
+        in turn meet none of their own bytes in L2 when n sets hold a few times L2.  K/V
+        resident in HBM only."""
+        import torch
+        sd = self.sd
+        assert not self.tiered
+        sets = []
+        for i in range(n):
+            if i == 0:
+                q, q_idx, keys, kc, vc = self.q, self.q_idx, self.keys, self.k_cache, self.v_cache
+            else:
+                q, q_idx, keys, kc, vc = (t.clone() for t in (self.q, self.q_idx, self.keys, self.k_cache,
+                                                              self.v_cache))
+            keep = [q, q_idx, keys, kc, vc]
+            if self.step_kernel:
+                a, _, _, _, _ = sd.make_decode_step_args(q_idx, keys, q, kc, vc, self.w.k, block=self.w.block,
+                                                         scores=self.scores, idx=self.idx, out=self.out,
+                                                         lse=self.lse, err_word=self.err)
+                ws = sd.decode_step_workspace(a, self.dev)
+                keep += [a, ws]
+                calls = [sd.prepare_decode_step(a)]
+            else:
+                a, _, _, _ = sd.make_attend_args(q, kc, vc, None if self.fused else self.idx, n_idx=self.w.k,
+                                                 block=self.w.block, T=self.w.T, err_word=self.err, out=self.out,
+                                                 lse=self.lse)
+                keep.append(a)
+                calls = [sd.prepare_index_score(q_idx, keys, self.scores, self.err, key_hist=self.key_hist)]
+                if self.fused:
+                    calls.append(sd.prepare_select_attend(self.scores, a, self.idx, key_hist=self.key_hist))
+                else:
+                    calls += [sd.prepare_topk(self.scores, self.w.k, self.idx, key_hist=self.key_hist),
+                              sd.prepare_gather_attend(a, self.ws)]
+            sets.append((calls, keep))
+        torch.cuda.synchronize()
+        return sets
 
     def packed_io(self):
         """Moves the step's per-step inputs (q, q_idx) into one device buffer and its results
@@ -1077,11 +1126,75 @@ def step_report(step, w, workload, kmarks, dom_ms, ms_per_step, peak, device, K,
     return traffic, step_roof
 
 
-def measure_extra(name, args, device, local, clean_l2, peak, steps=20, warmup=3):
+def path_description(step, w) -> str:
+    """What one timed step of `step` runs, for the JSON line's config."""
+    if isinstance(step, SparseDecodeStep):
+        if step.step_kernel:
+            return ("indexer + top-k + gather-attend in one launch (sd_decode_step, one thread-block cluster "
+                    "per KV group)" if cluster_step_supported(w)
+                    else "indexer + top-k + gather-attend in one persistent launch (sd_decode_step)")
+        if step.fused:
+            return "indexer + fused select/attend"
+        if step.staged:
+            return "indexer + top-k + host-row staging + gather-attend"
+        return "indexer + top-k + gather-attend"
+    if isinstance(step, WindowStep):
+        return "indexer + window max + top-k windows + union + gather-attend"
+    if isinstance(step, HeadsStep):
+        return "per-head logits + per-head top-k + per-head gather-attend"
+    if isinstance(step, VerifyGroupStep):
+        return (f"indexer + top-k once, then per layer ({w.layers}) ring append + gather-attend over the "
+                "selected rows and the draft ring")
+    if isinstance(step, CachedTieredStep):
+        if step.staged_promotion:
+            head = ("indexer + top-k + staging of the rows the pool lacks + gather-attend, then their promotion "
+                    "from the stage into the pool (cache) "
+                    + ("beside the next step's indexer and top-k" if step.concurrent else "in order on one stream"))
+        else:
+            head = "indexer + top-k + promotion into the pool (cache) + staging of the rest + gather-attend"
+        return head + ", the query window sliding step by step"
+    if isinstance(step, LookaheadStep):
+        return (f"per layer ({w.layers}): indexer + top-k + host-row staging + gather-attend, "
+                + ("next layer's selection before this layer's attention, staging on its own stream"
+                   if step.lookahead else "in order on one stream"))
+    return "dense attention + score accumulate per layer"
+
+
+def rotation_count(step, l2_bytes) -> int:
+    """Input sets a back-to-back run rotates through: enough that at least three times L2 of
+    other steps' traffic passes between two uses of one set (at least two sets)."""
+    fp = max(1, step.bytes()["hbm"])
+    return max(2, -(-3 * l2_bytes // fp) + 1)
+
+
+def time_rotated(sets, K) -> float:
+    """ms for K steps run back to back over the input sets in turn (prebound C-ABI calls, the
+    kernels of consecutive launches overlapping programmatically), one event pair around them."""
+    import torch
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = len(sets)
+    start.record()
+    for i in range(K):
+        for c in sets[i % n][0]:
+            c()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def rotated_l2_note(n, step, l2_bytes) -> str:
+    fp = step.bytes()["hbm"]
+    return (f"inputs larger than L2: steps back to back over {n} copies of the step's inputs in distinct "
+            f"memory ({(n - 1) * fp / 1e6:.0f} MB = {(n - 1) * fp / l2_bytes:.1f}x L2 of other steps' traffic "
+            f"between two uses of one copy), no flush; one event pair around the timed steps")
+
+
+def measure_extra(name, args, device, local, clean_l2, peak, steps=100, warmup=3):
     """A compact measurement of another workload in the same run (the T = 131072 configurations
-    beside the headline): the default path, `warmup` untimed steps, then `steps` steps timed with
-    one event pair each and `steps` more with events around every kernel; L2 flushed before
-    every step, clocks sampled meanwhile.  Returns the record attached to the JSON line."""
+    beside the headline): the default path, `warmup` untimed steps, then `steps` steps timed as
+    the headline's are (back to back over copies of the inputs for a sparse step with K/V in
+    HBM, else one event pair per flushed step), and `steps` more, flushed, with events around
+    every kernel; clocks sampled meanwhile.  Returns the record attached to the JSON line."""
     import torch
     from top_sparse_decode_gqa_gb300.workloads import WORKLOADS, generate
     w = WORKLOADS[name]
@@ -1094,15 +1207,26 @@ def measure_extra(name, args, device, local, clean_l2, peak, steps=20, warmup=3)
     if int(step.err.item()) != 0:
         raise RuntimeError(f"{name}: device error word {int(step.err.item())}")
     step.after_warmup()
+    l2_bytes = max(int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0)), 1)
+    rot = None
+    if isinstance(step, SparseDecodeStep) and not step.tiered:
+        rot = step.rotation(rotation_count(step, l2_bytes))
+        for calls, _ in rot:
+            for c in calls:
+                c()
+        torch.cuda.synchronize()
     marks = [StepMarks(0) for _ in range(steps)]
     kmarks = [StepMarks(step.dominant_per_step, step.phases) for _ in range(steps)]
     clocks = ClockSampler(local)
     clocks.start()
     torch.cuda.synchronize()
     clocks.mark(True)
-    for i in range(steps):
-        clean_l2()
-        step.run(marks[i])
+    if rot is not None:
+        rot_ms = time_rotated(rot, steps)
+    else:
+        for i in range(steps):
+            clean_l2()
+            step.run(marks[i])
     torch.cuda.synchronize()
     for i in range(steps):
         clean_l2()
@@ -1110,15 +1234,22 @@ def measure_extra(name, args, device, local, clean_l2, peak, steps=20, warmup=3)
     torch.cuda.synchronize()
     clocks.mark(False)
     clk = clocks.stop()
-    ms_per_step = sum(m.step_ms() for m in marks) / steps
+    if int(step.err.item()) != 0:
+        raise RuntimeError(f"{name}: device error word {int(step.err.item())} after the timed steps")
+    if rot is not None:
+        ms_per_step = rot_ms / steps
+        l2_note = rotated_l2_note(len(rot), step, l2_bytes)
+        del rot
+    else:
+        ms_per_step = sum(m.step_ms() for m in marks) / steps
+        l2_note = "flushed between timed steps: 2x L2 written then read, outside the events"
     dom_ms = [t for m in kmarks for t in m.dominant_ms()]
     _, step_roof = step_report(step, w, name, kmarks, dom_ms, ms_per_step, peak, device, steps, clean_l2)
     rec = {"value": round(w.queries_per_step / (ms_per_step / 1e3), 1), "unit": "queries/s",
            "ms_per_step": round(ms_per_step, 5), "steps": steps, "warmup": warmup,
            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "T": w.T, "k": w.k,
                       "block": w.block, "V": w.V, "resident_frac": w.resident_frac,
-                      "path": ("indexer + top-k + host-row staging + gather-attend" if getattr(step, "staged", False)
-                               else "indexer + top-k + gather-attend")},
+                      "path": path_description(step, w), "l2": l2_note},
            "step_roofline": step_roof, "clocks": clk,
            "gpu_launches": step.launches_per_step * steps}
     del step, x
@@ -1162,11 +1293,22 @@ def run_ours(args):
         raise RuntimeError(f"device error word {int(step.err.item())}")
     step.after_warmup()
 
-    # Timed region 1 (the headline): K steps with one event pair per step, so nothing
-    # between the step's kernels breaks their programmatic overlap.  Timed region 2: the
-    # same steps with events around every kernel, for the per-kernel roofline.
+    # Timed region 1 (the headline).  A sparse step with K/V in HBM runs its K steps back to
+    # back over copies of its inputs that together hold several times L2 (inputs larger than
+    # L2, no flush; one event pair around the K steps).  Other steps: K steps with one event
+    # pair per step and L2 flushed before each, so nothing between the step's kernels breaks
+    # their programmatic overlap.  Timed region 2: the same steps (flushed) with events around
+    # every kernel, for the per-kernel roofline.
     K = args.steps
     K2 = min(K, 500)
+    l2_bytes = max(int(getattr(props, "L2_cache_size", 0)), 1)
+    rot = None
+    if isinstance(step, SparseDecodeStep) and not step.tiered:
+        rot = step.rotation(rotation_count(step, l2_bytes))
+        for calls, _ in rot:  # every copy once, untimed
+            for c in calls:
+                c()
+        torch.cuda.synchronize()
     marks = [StepMarks(0) for _ in range(K)]
     kmarks = [StepMarks(step.dominant_per_step, step.phases) for _ in range(K2)]
     clocks = ClockSampler(local)
@@ -1175,9 +1317,12 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     clocks.mark(True)
-    for i in range(K):
-        clean_l2()
-        step.run(marks[i])
+    if rot is not None:
+        rot_ms = time_rotated(rot, K)
+    else:
+        for i in range(K):
+            clean_l2()
+            step.run(marks[i])
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -1189,10 +1334,19 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
+    if int(step.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(step.err.item())} after the timed steps")
 
-    step_ms = [m.step_ms() for m in marks]
+    if rot is not None:
+        l2_note = rotated_l2_note(len(rot), step, l2_bytes)
+        total_ms = rot_ms
+        del rot
+        torch.cuda.empty_cache()
+    else:
+        l2_note = "flushed between timed steps: 2x L2 written then read, outside the events"
+        total_ms = sum(m.step_ms() for m in marks)
     dom_ms = [t for m in kmarks for t in m.dominant_ms()]
-    total_s = reduce_max(sum(step_ms) / 1e3, world, device)
+    total_s = reduce_max(total_ms / 1e3, world, device)
     value = aggregate(w.queries_per_step * K, world, total_s)
     ms_per_step = total_s * 1e3 / K
 
@@ -1222,33 +1376,8 @@ def run_ours(args):
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "T": w.T,
                    "k": w.k, "block": w.block, "V": w.V, "layers": w.layers,
                    "queries_per_step": w.queries_per_step,
-                   "path": ("indexer + top-k + gather-attend in one persistent launch (sd_decode_step)"
-                            if getattr(step, "step_kernel", False)
-                            else "indexer + fused select/attend" if getattr(step, "fused", False)
-                            else "indexer + top-k + host-row staging + gather-attend"
-                            if getattr(step, "staged", False)
-                            else "indexer + top-k + gather-attend" if isinstance(step, SparseDecodeStep)
-                            else "indexer + window max + top-k windows + union + gather-attend"
-                            if isinstance(step, WindowStep)
-                            else "per-head logits + per-head top-k + per-head gather-attend"
-                            if isinstance(step, HeadsStep)
-                            else f"indexer + top-k once, then per layer ({w.layers}) ring append + gather-attend "
-                                 "over the selected rows and the draft ring"
-                            if isinstance(step, VerifyGroupStep)
-                            else ("indexer + top-k + staging of the rows the pool lacks + gather-attend, then "
-                                  "their promotion from the stage into the pool (cache) "
-                                  + ("beside the next step's indexer and top-k"
-                                     if step.concurrent else "in order on one stream")
-                                  if step.staged_promotion else
-                                  "indexer + top-k + promotion into the pool (cache) + staging of the rest + "
-                                  "gather-attend") + ", the query window sliding step by step"
-                            if isinstance(step, CachedTieredStep)
-                            else f"per layer ({w.layers}): indexer + top-k + host-row staging + gather-attend, "
-                                 + ("next layer's selection before this layer's attention, staging on its own stream"
-                                    if step.lookahead else "in order on one stream")
-                            if isinstance(step, LookaheadStep)
-                            else "dense attention + score accumulate per layer"),
-                   "l2": "flushed between timed steps: 2x L2 written then read, outside the events",
+                   "path": path_description(step, w),
+                   "l2": l2_note,
                    "parallelism": f"replica x{world} (each rank its own batch)"},
         "roofline": {"bound": "hbm", "kernel": step.dominant, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -1317,6 +1446,8 @@ def measure_e2e_packed(step, w, clean_l2, K):
             raise RuntimeError("cudaStreamSynchronize failed")
         if i >= 3:
             times.append(time.perf_counter() - t0)
+    if int(step.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(step.err.item())} after the end-to-end steps")
     return {"value": round(w.queries_per_step * len(times) / sum(times), 1), "unit": "queries/s",
             "h2d_bytes_per_step": int(d_in.numel()), "d2h_bytes_per_step": int(d_out.numel()),
             "timing": "host wall clock per step incl. one packed copy each way and the stream sync",
@@ -1358,6 +1489,9 @@ def measure_e2e(step, w, x, clean_l2, K):
         torch.cuda.current_stream().synchronize()
         if i >= 3:
             times.append(time.perf_counter() - t0)
+    err = getattr(step, "err", None)
+    if err is not None and int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} after the end-to-end steps")
     bi = sum(src.numel() * src.element_size() for _, src in ins)
     bo = sum(dst.numel() * dst.element_size() for dst in outs)
     return {"value": round(w.queries_per_step * len(times) / sum(times), 1), "unit": "queries/s",

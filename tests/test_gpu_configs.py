@@ -209,6 +209,29 @@ def test_c3_fused_select_attend_full():
     assert_attend_close(lse, rl, "lse")
 
 
+def test_c3_decode_step_full():
+    # the whole step in one launch (one thread-block cluster per KV group) on the fp16 pooled
+    # keys: scores and index sets bit-exact, attention within tolerance
+    w = W("c3_block_sparse")
+    x = gen(w)
+    g = to_dev(x)
+    pooled = sd().sd_block_pool(g["k_idx"], w.block, dtype=torch.float16)
+    e = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scores, idx, out, lse = sd().decode_step(g["q_idx"], pooled, g["q"], g["k"], g["v"], w.k, block=w.block,
+                                             err_word=e)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    rp = oracle.block_pool(x["k_idx"], w.B, w.Hkv, w.T, w.dI, w.block)
+    rs = oracle.index_score(x["q_idx"], rp.astype(np.float32), w.B, w.Hkv, w.V, w.N, w.dI)
+    np.testing.assert_array_equal(scores.cpu().numpy().astype(np.float64), rs)
+    ri = oracle.topk(rs, w.k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ri)
+    ro, rl, _ = oracle.gather_attend(x["q"], x["k"], x["v"], ri, w.B, w.V, w.Hq, w.Hkv, w.d, w.T,
+                                     w.k, w.block, 1 / math.sqrt(w.d))
+    assert_attend_close(out, ro)
+    assert_attend_close(lse, rl, "lse")
+
+
 def test_c4_fused_select_attend_full():
     w = W("c4_tiered_verify")
     x = gen(w)

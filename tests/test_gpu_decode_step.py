@@ -70,6 +70,12 @@ def check_against_oracle(inp, B, Hkv, G, V, T, block, kk, scores, idx, out, lse)
     (1, 1, 8, 1, 128 * 40, 128, 9, torch.bfloat16, 0),  # 128-row blocks: two TMA runs each
     (3, 8, 4, 1, 9000, 1, 1024, torch.bfloat16, 0),    # many groups and tasks in flight
     (1, 1, 1, 1, 4, 1, 1, torch.bfloat16, 0),          # four tokens, one selected
+    # block selection over short score rows: one thread-block cluster per KV group
+    (2, 8, 4, 1, 32 * 2048, 32, 64, torch.float16, 0),  # 16 groups: clusters of 8, one CTA per SM
+    (5, 8, 4, 1, 32 * 1000, 32, 40, torch.bfloat16, 0),  # 40 groups: clusters of 4, two CTAs per SM
+    (40, 8, 4, 1, 16 * 64, 16, 12, torch.bfloat16, 0),  # 320 groups: single CTAs, several waves
+    (1, 2, 4, 4, 32 * 516, 32, 33, torch.bfloat16, 0),  # 16 query rows, ragged shares and list
+    (1, 1, 4, 1, 16 * 8196, 16, 50, torch.bfloat16, 0),  # N > 8192: the persistent kernel's block path
 ])
 def test_decode_step_matches_oracle(B, Hkv, G, V, T, block, kk, kdt, lag):
     inp = make_inputs(B, Hkv, G, V, T, block, seed=B * 7919 + T + kk, kdt=kdt)
@@ -95,6 +101,36 @@ def test_decode_step_ties(key_lo, key_hi, T, kk):
     torch.cuda.synchronize()
     assert int(e.item()) == 0
     check_against_oracle(inp, B, Hkv, G, V, T, 1, kk, scores, idx, out, lse)
+
+
+@pytest.mark.parametrize("key_lo,key_hi,N,kk", [
+    (0, 0, 600, 37),     # every block score equal: the lowest 37 indices
+    (-1, 1, 2000, 300),  # few distinct values: heavy ties at the threshold
+])
+def test_decode_step_block_ties(key_lo, key_hi, N, kk):
+    B, Hkv, G, V, block = 2, 4, 4, 1, 32
+    inp = make_inputs(B, Hkv, G, V, N * block, block, seed=N + kk, key_lo=key_lo, key_hi=key_hi)
+    dev = [t.cuda() for t in inp]
+    e = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scores, idx, out, lse = sd().decode_step(*dev, kk, block=block, err_word=e)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    check_against_oracle(inp, B, Hkv, G, V, N * block, block, kk, scores, idx, out, lse)
+
+
+def test_decode_step_block_empty_and_full_selection():
+    B, Hkv, G, V, block, N = 1, 2, 4, 2, 64, 40
+    inp = make_inputs(B, Hkv, G, V, N * block, block, seed=8)
+    dev = [t.cuda() for t in inp]
+    scores, idx, out, lse = sd().decode_step(*dev, 0, block=block)
+    torch.cuda.synchronize()
+    assert idx.numel() == 0
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+    np.testing.assert_array_equal(scores.cpu().numpy().astype(np.float64),
+                                  oracle.index_score(inp[0], inp[1], B, Hkv, V, N, 128))
+    scores, idx, out, lse = sd().decode_step(*dev, N, block=block)
+    torch.cuda.synchronize()
+    check_against_oracle(inp, B, Hkv, G, V, N * block, block, N, scores, idx, out, lse)
 
 
 def test_decode_step_empty_and_full_selection():

@@ -42,6 +42,7 @@
 #include <cmath>
 
 #include "sd_host.h"
+#include "step_tiles.cuh"
 #include "tc_common.cuh"
 
 namespace sd {
@@ -150,200 +151,6 @@ SD_DEVINL Task decode_task(const DsParams& p, uint32_t t) {
     }
     t -= b;
     return {kTaskAttend, p.NG - p.L + (int)(t / p.AG), (int)(t % p.AG)};
-}
-
-// A bounded mbarrier wait that also gives up as soon as another role raised the abort flag.
-// Between checks of the deadline and the flag the thread sleeps in the barrier (up to 20 us,
-// woken when the phase completes), so waiting warps leave the issue slots to working ones.
-SD_DEVINL bool ds_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag, uint64_t limit) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > limit) return false;
-    }
-}
-
-// Lane 0 waits (bounded) and the warp follows its result; on success every lane then observes
-// the completed phase itself (acquire), which cannot have moved on: the next phase needs this
-// warp first.
-SD_DEVINL bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint64_t limit) {
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = ds_wait(bar, parity, abort_flag, limit);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (ok) (void)mbar_try_wait(bar, parity);
-    else *abort_flag = 1;
-    return ok;
-}
-
-// Byte offset of 16-byte chunk c (0..15 over a 128-element bf16 row) of row r in a stage
-// tile of `rows` rows stored as two 64-column halves with the 128-byte swizzle.
-SD_DEVINL uint32_t swz(int rows, int r, int c) {
-    return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
-
-// ------------------------------------------------------------------ consumers: scoring
-
-// Scores of the stage's 64 keys against the V query rows of the group (max over V), one warp:
-// written to the warp's 64-float buffer.
-template <bool F16>
-SD_DEVINL void score_tile(const uint8_t* st, int lane, int V, float* sbuf) {
-    const uint32_t kb = smem_addr(st), qb = smem_addr(st + kDsData);
-    float acc[4][4];
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < 8; ks += 2) {
-        // B = q^T: matrices (query rows 0-7) x (dims 16ks + 0..7, +8..15, 16(ks+1) + 0..7, +8..15)
-        uint32_t b[4];
-        ldsm_x4(qb + (lane & 7) * 256 + (ks * 16 + (lane >> 3) * 8) * 2, b[0], b[1], b[2], b[3]);
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                const int row = 16 * mt + (lane & 15);
-                const int chunk = 2 * (ks + kk) + (lane >> 4);
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(kb + swz(kDsKeyRows, row, chunk), a0, a1, a2, a3);
-                if constexpr (F16)
-                    mma_f16_16816(acc[mt], a0, a1, a2, a3, b[2 * kk], b[2 * kk + 1]);
-                else
-                    mma_bf16_16816(acc[mt], a0, a1, a2, a3, b[2 * kk], b[2 * kk + 1]);
-            }
-    }
-    const int g8 = lane >> 2, t4 = lane & 3;
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-        float v0 = -INFINITY, v1 = -INFINITY;  // keys g8 and g8 + 8 of this M tile
-        if (2 * t4 < V) {
-            v0 = acc[mt][0];
-            v1 = acc[mt][2];
-        }
-        if (2 * t4 + 1 < V) {
-            v0 = fmaxf(v0, acc[mt][1]);
-            v1 = fmaxf(v1, acc[mt][3]);
-        }
-        v0 = fmaxf(v0, __shfl_xor_sync(0xffffffffu, v0, 1));
-        v0 = fmaxf(v0, __shfl_xor_sync(0xffffffffu, v0, 2));
-        v1 = fmaxf(v1, __shfl_xor_sync(0xffffffffu, v1, 1));
-        v1 = fmaxf(v1, __shfl_xor_sync(0xffffffffu, v1, 2));
-        if (t4 == 0) {
-            sbuf[16 * mt + g8] = v0;
-            sbuf[16 * mt + g8 + 8] = v1;
-        }
-    }
-}
-
-// ------------------------------------------------------------------ consumers: attention
-
-struct AttAcc {
-    float o[16][4];    // the 128 output columns: n-tiles of 8, C fragments
-    float m[2], l[2];  // query rows g8 and g8 + 8 (base-2 units)
-};
-
-// Query A fragments of the 16 (padded) query rows for the 8 k-steps of d = 128; rows >= R zero.
-SD_DEVINL void load_q_frags(const uint8_t* st, int lane, int R, uint32_t (&qf)[8][4]) {
-    const uint32_t qb = smem_addr(st + kDsData);
-    const int g8 = lane >> 2;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-        ldsm_x4(qb + (lane & 15) * 256 + (2 * ks + (lane >> 4)) * 16, qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
-        if (g8 >= R) qf[ks][0] = qf[ks][2] = 0u;
-        if (g8 + 8 >= R) qf[ks][1] = qf[ks][3] = 0u;
-    }
-}
-
-// One stage of 32 K/V rows for all query rows, one warp: S = Q K^T (16 x 32), the online
-// softmax (base 2), then O += P V over all 128 columns.
-SD_DEVINL void attend_stage(const uint8_t* st, int lane, const uint32_t (&qf)[8][4], bool two_halves, uint32_t valid,
-                            float scale_log2, AttAcc& acc) {
-    const uint32_t kb = smem_addr(st), vb = kb + kDsData / 2;
-    float s[4][4];
-#pragma unroll
-    for (int n = 0; n < 4; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s[n][e] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-        for (int pp = 0; pp < 2; ++pp) {
-            // matrices: keys 16pp + 0..7 (dims 16ks + 0..7, +8..15), keys 16pp + 8..15 (same)
-            const int key = 16 * pp + (lane & 7) + ((lane >> 4) << 3);
-            const int chunk = 2 * ks + ((lane >> 3) & 1);
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4(kb + swz(kDsRows, key, chunk), r0, r1, r2, r3);
-            mma_bf16_16816(s[2 * pp], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], r0, r1);
-            mma_bf16_16816(s[2 * pp + 1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], r2, r3);
-        }
-    const int t4 = lane & 3;
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-        if (hf == 1 && !two_halves) {  // query rows 8..15 are padding: P = 0 there
-#pragma unroll
-            for (int n = 0; n < 4; ++n) s[n][2] = s[n][3] = 0.f;
-            break;
-        }
-        float tmax = -INFINITY;
-#pragma unroll
-        for (int n = 0; n < 4; ++n)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int j = 8 * n + 2 * t4 + e;
-                const float x = ((valid >> j) & 1u) ? s[n][2 * hf + e] * scale_log2 : -INFINITY;
-                s[n][2 * hf + e] = x;
-                tmax = fmaxf(tmax, x);
-            }
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-        const float mo = acc.m[hf];
-        const float mn = fmaxf(mo, tmax);
-        const float alpha = (mn == -INFINITY || mn == mo) ? 1.f : fast_exp2(mo - mn);
-        float rsum = 0.f;
-#pragma unroll
-        for (int n = 0; n < 4; ++n)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float x = s[n][2 * hf + e];
-                const float pv = (x == -INFINITY) ? 0.f : fast_exp2(x - mn);
-                s[n][2 * hf + e] = pv;
-                rsum += pv;
-            }
-        rsum += __shfl_xor_sync(0xffffffffu, rsum, 1);
-        rsum += __shfl_xor_sync(0xffffffffu, rsum, 2);
-        acc.l[hf] = acc.l[hf] * alpha + rsum;
-        acc.m[hf] = mn;
-        if (alpha != 1.f) {
-#pragma unroll
-            for (int nt = 0; nt < 16; ++nt) {
-                acc.o[nt][2 * hf] *= alpha;
-                acc.o[nt][2 * hf + 1] *= alpha;
-            }
-        }
-    }
-    // P as A fragments (bf16 hi + lo, ~16 significant bits), k-step kk = keys 16kk .. 16kk + 15
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-        uint32_t ph[4], pl[4];
-        split_bf16x2(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
-        split_bf16x2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
-        split_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
-        split_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
-#pragma unroll
-        for (int c2 = 0; c2 < 8; ++c2) {
-            // V rows 16kk + 0..15, columns 16 c2 .. 16 c2 + 15, transposed into B fragments
-            const int key = 16 * kk + (lane & 15);
-            const int chunk = 2 * c2 + (lane >> 4);
-            uint32_t v0, v1, v2, v3;
-            ldsm_x4_t(vb + swz(kDsRows, key, chunk), v0, v1, v2, v3);
-            mma_bf16_16816(acc.o[2 * c2], ph[0], ph[1], ph[2], ph[3], v0, v1);
-            mma_bf16_16816(acc.o[2 * c2 + 1], ph[0], ph[1], ph[2], ph[3], v2, v3);
-            mma_bf16_16816(acc.o[2 * c2], pl[0], pl[1], pl[2], pl[3], v0, v1);
-            mma_bf16_16816(acc.o[2 * c2 + 1], pl[0], pl[1], pl[2], pl[3], v2, v3);
-        }
-    }
 }
 
 // ------------------------------------------------------------------ selection
@@ -1005,7 +812,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
             const uint8_t* st = sm + s * kDsStage;
             bool post = m.kind == kTaskEnd;
             if (m.kind == kTaskScore) {
-                score_tile<F16>(st, lane, p.V, sbuf);
+                score_tile<F16>(smem_addr(st), smem_addr(st + kDsData), lane, p.V, sbuf);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll
@@ -1021,7 +828,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
                 }
                 post = m.sgi == m.nst - 1;
             } else if (m.kind == kTaskAttend) {
-                load_q_frags(st, lane, p.R, qf);
+                load_q_frags(smem_addr(st + kDsData), lane, p.R, qf);
                 if (m.sgi == 0) {
 #pragma unroll
                     for (int nt = 0; nt < 16; ++nt)
@@ -1030,7 +837,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
                     acc.m[0] = acc.m[1] = -INFINITY;
                     acc.l[0] = acc.l[1] = 0.f;
                 }
-                attend_stage(st, lane, qf, two_halves, m.valid, p.scale_log2, acc);
+                attend_stage(smem_addr(st), smem_addr(st) + kDsData / 2, lane, qf, two_halves, m.valid, p.scale_log2, acc);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
                 if (m.sgi == m.nst - 1) {  // the task's partial
@@ -1319,6 +1126,7 @@ extern "C" sd_status sd_decode_step(const sd_decode_step_args* a, void* stream) 
     SD_REQUIRE(a->workspace != nullptr && a->workspace_bytes >= sp.bytes,
                "%s: workspace of %zu bytes needed (got %zu)", who, sp.bytes, a->workspace_bytes);
     SD_REQUIRE((reinterpret_cast<uintptr_t>(a->workspace) & 255u) == 0, "%s: workspace must be 256-byte aligned", who);
+    if (block_step_eligible(a)) return block_step_launch(a, as_stream(stream));
     const bool f16 = a->key_dtype == SD_F16;
     CUtensorMap kmap, kvk, kvv;
     if (!make_tensor_map_2d(&kmap, a->keys, (uint64_t)sp.NG * sp.N, 128, kDsKeyRows, f16) ||

@@ -189,6 +189,14 @@ SD_DEVINL void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2
                  : "r"(addr));
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held one 32-bit pair per lane (lane l: row
+// l / 4, columns 2(l % 4) and 2(l % 4) + 1), returned in the same distribution.
+SD_DEVINL uint32_t movmatrix_t(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 // D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col).
 SD_DEVINL void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                               uint32_t b0, uint32_t b1) {

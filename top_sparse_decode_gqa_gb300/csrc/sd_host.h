@@ -33,6 +33,11 @@ sd_status validate_attend_args(const sd_attend_args* a, const char* who);
 bool topk_by_clusters(const float* scores, int rows, int N, int k, int32_t* idx, uint32_t* key_hist,
                       cudaStream_t st, sd_status* status);
 
+// sd_decode_step's path for block selection over short score rows (one thread-block cluster
+// per KV group): whether a validated request takes it, and its launch.
+bool block_step_eligible(const sd_decode_step_args* a);
+sd_status block_step_launch(const sd_decode_step_args* a, cudaStream_t st);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
