@@ -1068,7 +1068,9 @@ def step_report(step, w, workload, kmarks, dom_ms, ms_per_step, peak, device, K,
     import torch
     by = step.bytes()
     if isinstance(step, SparseDecodeStep) and step.step_kernel:
-        kernel_file, kernel_tag = ("decode_step.cu", "tc_common.cuh", "sd_common.cuh"), "decode_step"
+        kernel_file, kernel_tag = (("block_step.cu", "step_tiles.cuh", "tc_common.cuh", "sd_common.cuh")
+                                   if cluster_step_supported(w) else
+                                   ("decode_step.cu", "step_tiles.cuh", "tc_common.cuh", "sd_common.cuh")), "decode_step"
     elif isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep, LookaheadStep, CachedTieredStep)):
         kernel_file, kernel_tag = ("index_score.cu", "index_score_tc.cu", "tc_common.cuh", "sd_common.cuh"), "index_score"
     else:
@@ -1350,7 +1352,7 @@ def run_ours(args):
     K2 = min(K, 500)
     l2_bytes = max(int(getattr(props, "L2_cache_size", 0)), 1)
     rot = None
-    if isinstance(step, SparseDecodeStep) and not step.tiered:
+    if isinstance(step, SparseDecodeStep) and not step.tiered and not args.no_rotate:
         rot = step.rotation(rotation_count(step, l2_bytes))
         for calls, _ in rot:  # every copy once, untimed
             for c in calls:
@@ -1794,6 +1796,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rotate", action="store_true",
+                    help="time the sparse step like the others (one flushed step per event pair) instead of back "
+                         "to back over copies of its inputs (keeps the device footprint at one copy, e.g. for ncu)")
     ap.add_argument("--no-extra", action="store_true",
                     help="with the default workload, skip the T = 131072 configurations measured beside it")
     ap.add_argument("--separate", action="store_true",
