@@ -20,6 +20,7 @@ namespace {
 
 constexpr int kStThreads = 256;
 constexpr int kStPieces = 8;  // 16-byte pieces a lane moves per chunk (all loads before any store)
+constexpr int kStTailShare = 4;  // the last 1/kStTailShare of the list rows go out as short tickets
 
 struct StageParams {
     const uint8_t* kh;  // mapped host cache [B, kv_heads, T, d]
@@ -32,6 +33,8 @@ struct StageParams {
     int groups_per_seq, kv_heads, heads_per_kv;
     int row_bytes, rows_per_chunk;  // rows_per_chunk: rows one copy batch moves
     int total_rows;
+    int n_long, long_rows;  // tickets of 32 list rows first (n_long of them, long_rows rows), then of
+                            // rows_per_chunk rows
     uint32_t* counter;  // [0] next chunk, [1] CTAs done; zero between calls
     int32_t* err;
     int slot_per_head;  // 1: slot_map is [B, kv_heads, T]
@@ -47,10 +50,14 @@ SD_DEVINL int nth_set_bit(uint32_t mask, int n) {
     return x;
 }
 
-// A warp takes the next 32 list rows from the counter (one per lane), resolves each to its
-// host row or to nothing (pooled or empty), and copies only the misses, rows_per_chunk rows
-// (kStPieces 16-byte pieces per lane, all loads before any store) at a time; a piece's miss
-// is found in the ballot of misses and its rows are shuffled from the lane that resolved it.
+// A warp takes the next ticket of list rows from the counter (one row per lane), resolves
+// each to its host row or to nothing (pooled or empty), and copies only the misses,
+// rows_per_chunk rows (kStPieces 16-byte pieces per lane, all loads before any store) at a
+// time; a piece's miss is found in the ballot of misses and its rows are shuffled from the
+// lane that resolved it.  Tickets hold 32 rows (one resolving lane each: cheap when the pool
+// serves most rows) except over the last 1/kStTailShare of the list, where they hold one copy
+// batch: when most rows are misses a 32-row ticket takes four batches in a row, and the last
+// such tickets would keep a few warps copying after the rest have finished.
 // No shared memory, and registers capped at 80 (the bound's 3 CTAs; the grid has one per SM):
 // the kernel runs beside the indexer, whose CTAs need most of an SM's shared memory, and
 // beside the attention.
@@ -60,16 +67,20 @@ __global__ void __launch_bounds__(kStThreads, 3) stage_host_rows_kernel(const St
     const int lane = threadIdx.x & 31;
     const int ppr = p.row_bytes / 16;  // pieces per K (or V) row
     const int C = p.rows_per_chunk;    // C * 2 * ppr == 32 * kStPieces
-    const int nchunks = (p.total_rows + 31) / 32;
+    const int nchunks = p.n_long + (p.total_rows - p.long_rows + C - 1) / C;
     for (;;) {
         uint32_t c = 0;
         if (lane == 0) c = atomicAdd(&p.counter[0], 1u);
         c = __shfl_sync(0xffffffffu, c, 0);
         if (c >= (uint32_t)nchunks) break;
-        // lane r resolves list row f = 32c + r to its host row, or -1 (nothing to copy)
+        // the ticket's rows [base, base + cnt); lane r resolves list row f = base + r to its
+        // host row, or -1 (nothing to copy)
+        const bool lng = c < (uint32_t)p.n_long;
+        const int base = lng ? (int)c * 32 : p.long_rows + ((int)c - p.n_long) * C;
+        const int cnt = lng ? 32 : C;
         int host_row = -1;  // < 2^31 (checked on the host)
-        const int f = (int)c * 32 + lane;
-        if (f < p.total_rows) {
+        const int f = base + lane;
+        if (lane < cnt && f < p.total_rows) {
             const int g = f / p.n_rows, j = f % p.n_rows;
             const int b = g / p.groups_per_seq;
             const int kvsrc = b * p.kv_heads + (g % p.groups_per_seq) / p.heads_per_kv;
@@ -172,6 +183,8 @@ extern "C" sd_status sd_stage_host_rows(const sd_attend_args* a, uint32_t* count
     SD_REQUIRE(total + 32 < (1L << 31) && (long)a->B * a->Hkv * a->T < (1L << 31),
                "sd_stage_host_rows: selected rows and host cache rows must be < 2^31");
     p.total_rows = (int)total;
+    p.n_long = (int)(total - total / kStTailShare) / 32;
+    p.long_rows = p.n_long * 32;
     p.counter = counter;
     p.err = a->err_word;
     p.slot_per_head = a->slot_per_head;
