@@ -195,6 +195,16 @@ sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx, uin
  * query head h attends to its own selection idx[b,h,:], rows read from KV head
  * h / (Hq/Hkv) (all V query tokens of the head share it); the split plan and workspace then
  * count B*Hq groups of V query rows.  Needs idx.
+ * Tiers ([HBM] Metodologia 1: T0 in HBM, T1 in host memory, T2 at 8 bits, T3 evicted;
+ * Metodologia 3: a row contributes the same terms wherever it is stored): with tier set,
+ * a row at a position whose tier is 3 takes no part (z = -inf, as an empty slot); a row
+ * whose tier is 2 is read as K = k_int8 * k_scale, V = v_int8 * v_scale (its row of codes
+ * and its per-row scale, as sd_quantize_rows_int8 writes them); rows of tiers 0 and 1 are
+ * read as without tiers (from the pool, or host memory at slot -1, or the cache).  The
+ * codes enter the tensor cores unchanged (small integers are exact in bf16) and the
+ * scales multiply the row's logit and its softmax weight in fp32.  A call in which no
+ * selected row has tier 2 or 3 gives the bits of the same call without tiers.  Limits:
+ * bf16, d = 128, not per_head, no ring, no stage; T and pool_rows < 2^29.
  * The kernel is launched as a programmatic dependent of the preceding kernel in the
  * stream (it waits for that kernel's results before reading anything).
  */
@@ -225,6 +235,11 @@ typedef struct {
     const int32_t* qpos;      /* [B,V] token position of each query token */
     int ring_w;               /* ring slots; 0 = no ring */
     int slot_per_head;        /* 1: slot_map is [B,Hkv,T], one residency map per KV head */
+    const uint8_t* tier;      /* nullable [B,T] tier of every position (sd_tier_classify) */
+    const int8_t* k_int8;     /* [B,Hkv,T,d] int8 codes of the T2 rows of K (sd_quantize_rows_int8) */
+    const int8_t* v_int8;     /* same layout, of V */
+    const float* k_scale;     /* [B,Hkv,T] fp32 scales of the T2 rows of K */
+    const float* v_scale;     /* [B,Hkv,T] fp32, of V */
 } sd_attend_args;
 
 size_t sd_gather_attend_workspace_bytes(const sd_attend_args* args);

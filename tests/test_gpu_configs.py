@@ -267,8 +267,9 @@ def test_c4_fused_select_attend_full():
 
 def test_c5_importance_tiering_full():
     """Dense decode over 28 layers for the full 64 steps, the score recurrence, then the
-    four-tier split and the int8 encode of the T2 rows.  The oracle follows step 1 over all
-    28 layers at every position; mass conservation and the tier invariants cover all 64."""
+    four-tier split, the int8 encode of the T2 rows and an attention over the tiered cache.
+    The oracle follows step 1 over all 28 layers at every position; mass conservation and the
+    tier invariants cover all 64; tiers, codes and the tiered attention are the oracle's."""
     w = W("c5_importance_tiering")
     x = gen(w)
     L, B, T, Hq, Hkv, d = w.layers, w.B, w.T, w.Hq, w.Hkv, w.d
@@ -327,6 +328,27 @@ def test_c5_importance_tiering_full():
     np.testing.assert_array_equal(codes.cpu().numpy(), rcodes)   # rows of other tiers stay zero
     np.testing.assert_array_equal(scales.cpu().numpy(), rscales)
     t2 = np.broadcast_to((t_np == 2)[:, None, :], (B, Hkv, T))
+    # the tiers drive the attention: step 1's layer-0 queries over layer 0's cache with the T2
+    # rows as int8 codes and the T3 rows left out, against the oracle over the same rows at
+    # the values the tiers give them
+    vcodes, vscales = sd().sd_quantize_rows_int8(vs[0], tier)
+    a, tout, tlse, _ = sd().make_attend_args(qd[0, 0], ks[0], vs[0], None, T=T, err_word=e, tier=tier, k_int8=codes,
+                                            v_int8=vcodes, k_scale=scales, v_scale=vscales)
+    need = sd().sd_gather_attend_workspace_bytes(a)
+    sd().sd_gather_attend(a, torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    rvc, rvs = oracle.quantize_rows_int8(x["v"][0], rt, B, Hkv, T, d)
+    t2m = np.broadcast_to((rt == 2)[:, None, :, None], (B, Hkv, T, d))
+    kd = torch.from_numpy(np.where(t2m, rcodes.astype(np.float32) * rscales[..., None], x["k"][0].float().numpy()))
+    vd = torch.from_numpy(np.where(t2m, rvc.astype(np.float32) * rvs[..., None], x["v"][0].float().numpy()))
+    ridx = np.broadcast_to(np.arange(T, dtype=np.int32), (B, Hkv, T)).copy()
+    for bb in range(B):
+        ridx[bb][:, rt[bb] == 3] = -1
+    ro2, rl2, _ = oracle.gather_attend(x["q"][0, 0].float(), kd, vd, ridx, B, 1, Hq, Hkv, d, T, T, 1, 1 / math.sqrt(d))
+    assert_attend_close(tout, ro2)
+    assert_attend_close(tlse, rl2, "lse")
+    del kd, vd
     xf = x["k"][0].float().numpy()
     cf = codes.cpu().numpy().astype(np.float64) * scales.cpu().numpy()[..., None]
     err = np.abs(cf - xf)[t2]

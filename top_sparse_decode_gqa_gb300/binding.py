@@ -53,6 +53,8 @@ class sd_attend_args(ctypes.Structure):
         ("k_stage", ctypes.c_void_p), ("v_stage", ctypes.c_void_p),
         ("ring_k", ctypes.c_void_p), ("ring_v", ctypes.c_void_p), ("ring_pos", ctypes.c_void_p),
         ("qpos", ctypes.c_void_p), ("ring_w", ctypes.c_int), ("slot_per_head", ctypes.c_int),
+        ("tier", ctypes.c_void_p), ("k_int8", ctypes.c_void_p), ("v_int8", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
     ]
 
 
@@ -245,9 +247,11 @@ def sd_topk(scores: torch.Tensor, k: int, idx: Optional[torch.Tensor] = None,
 def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=None, scale=None,
                      k_host=None, v_host=None, slot_map=None, out=None, lse=None, logits=None,
                      want_logits=False, err_word=None, splits=0, per_head=False, k_stage=None,
-                     v_stage=None, ring_k=None, ring_v=None, ring_pos=None, qpos=None) -> tuple:
+                     v_stage=None, ring_k=None, ring_v=None, ring_pos=None, qpos=None, tier=None,
+                     k_int8=None, v_int8=None, k_scale=None, v_scale=None) -> tuple:
     """Fill an sd_attend_args from tensors; returns (args, out, lse, logits).  slot_map is
-    [B,T] (residency per sequence) or [B,Hkv,T] (per KV head)."""
+    [B,T] (residency per sequence) or [B,Hkv,T] (per KV head).  tier [B,T] uint8 with
+    k_int8/v_int8 [B,Hkv,T,d] int8 and k_scale/v_scale [B,Hkv,T] fp32: the tiered rows."""
     _dev(q, "q")
     B, V, Hq, d = q.shape
     Hkv = k_cache.shape[1]
@@ -288,7 +292,8 @@ def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=No
     a.splits = splits
     a.per_head = 1 if per_head else 0
     for name, t in (("k_stage", k_stage), ("v_stage", v_stage), ("ring_k", ring_k), ("ring_v", ring_v),
-                    ("ring_pos", ring_pos), ("qpos", qpos)):
+                    ("ring_pos", ring_pos), ("qpos", qpos), ("tier", tier), ("k_int8", k_int8),
+                    ("v_int8", v_int8), ("k_scale", k_scale), ("v_scale", v_scale)):
         if t is not None:
             _dev(t, name)
             setattr(a, name, t.data_ptr())

@@ -26,6 +26,7 @@ constexpr int kSub = 16;              // rows per warp sub-chunk
 constexpr int kWStages = 2;           // sub-chunks in flight per warp (default)
 constexpr int32_t kNoRow = INT32_MIN;  // source code of a skipped row (contributes nothing)
 constexpr int32_t kRingBase = 1 << 30;  // codes >= this: slot code - kRingBase of the draft ring
+constexpr int32_t kI8Base = 1 << 29;    // codes in [kI8Base, kRingBase): int8 row code - kI8Base
 constexpr float kLn2f = 0.69314718055994530942f;
 
 template <int D, int NW = kMmaWarps, int NS = kWStages>
@@ -50,7 +51,8 @@ SD_DEVINL void cp_async_wait_dyn(int n) {
 }
 
 // Where a row's bytes are: code >= kRingBase is slot code - kRingBase of the draft ring
-// (k_ring + slot * row bytes, offset to this (b, kvh)); other code >= 0 is row `code` of the
+// (k_ring + slot * row bytes, offset to this (b, kvh)); with int8 rows (SmemScales), code in
+// [kI8Base, kRingBase) is int8 row code - kI8Base (k_i8 + row * d); other code >= 0 is row `code` of the
 // device pool (k_pool + code * row bytes, likewise offset); code < 0 is host row -1 - code
 // of the mapped host cache (k_host likewise offset); kNoRow is skipped.
 struct RowSource {
@@ -60,6 +62,25 @@ struct RowSource {
     const uint8_t* v_host;
     const uint8_t* k_ring = nullptr;
     const uint8_t* v_ring = nullptr;
+    const int8_t* k_i8 = nullptr;  // int8 rows (codes), offset to this (b, kvh) like the pool
+    const int8_t* v_i8 = nullptr;
+};
+
+// Per-row scales of the rows' K and V: none (every row at full precision) ...
+struct NoScales {
+    static constexpr bool kInt8 = false;
+    SD_DEVINL float ks(int) const { return 1.f; }
+    SD_DEVINL float vs(int) const { return 1.f; }
+};
+
+// ... or read from shared memory for list row j (1 for rows read at full precision, the
+// row's int8 scale for int8 rows, whose codes the loop widens to bf16 in shared memory).
+struct SmemScales {
+    static constexpr bool kInt8 = true;
+    const float* k;
+    const float* v;
+    SD_DEVINL float ks(int j) const { return k[j]; }
+    SD_DEVINL float vs(int j) const { return v[j]; }
 };
 
 // Visibility of list row j to query row r when every row is visible to every query.
@@ -94,10 +115,15 @@ struct WarpAcc {
 // vis(r, j) hides the row from the query row (the causal mask of the draft ring).
 // nq = the real query rows (<= RP): an upper half tile (rows 8..15 of an M tile) holding
 // none of them skips its softmax, and its P fragments are zero.
-template <int D, int RP, int NW = kMmaWarps, int NS = kWStages, class RowCode, class Logit, class Vis = AllVisible>
+// Scl: the rows' per-row scales (NoScales, or SmemScales with int8 rows: a row's codes are
+// copied into the upper half of its bf16 slot and widened in place before use; its K scale
+// multiplies its logits and its V scale its softmax weights in the PV product).
+template <int D, int RP, int NW = kMmaWarps, int NS = kWStages, class RowCode, class Logit, class Vis = AllVisible,
+          class Scl = NoScales>
 SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_base, int warp, int nrows, int nq,
                                const RowSource& rs, float scale_log2, RowCode row_code, Logit logit,
-                               Vis vis = Vis()) {
+                               Vis vis = Vis(), Scl scl = Scl()) {
+    static_assert(!Scl::kInt8 || D == 128, "int8 rows: d = 128 (one 128-byte line per row)");
     static_assert(NS >= 2 && NS <= 4, "2 to 4 stages per warp");
     using L = MmaRows<D, NW, NS>;
     constexpr int MT = RP / 16, KS = D / 16, NT = D / 8;
@@ -122,6 +148,13 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
 #pragma unroll
             for (int q = 0; q < kSub / 4; ++q) {
                 uint8_t* dst = kst + which * kSub * L::kRowB + (q * 4 + sub) * L::kRowB + piece * 16;
+                if constexpr (Scl::kInt8) {
+                    if (code[q] >= kI8Base && code[q] < kRingBase) {  // one 128-byte line of codes
+                        const int8_t* srow = (which ? rs.v_i8 : rs.k_i8) + (size_t)(code[q] - kI8Base) * D;
+                        cp_async16(dst + D, srow + piece * 16);
+                        continue;
+                    }
+                }
                 if (code[q] == kNoRow) {
 #pragma unroll
                     for (int h = 0; h < PPR / 8; ++h) *reinterpret_cast<uint4*>(dst + h * 128) = make_uint4(0u, 0u, 0u, 0u);
@@ -148,6 +181,26 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
         const uint32_t k_base = smem_addr(stages + st * L::kStage);
         const uint32_t v_base = k_base + kSub * L::kRowB;
         const int c = warp + NW * ci;
+        if constexpr (Scl::kInt8) {
+            // widen the chunk's int8 rows in place: lane l reads codes 4l .. 4l + 3 (upper half
+            // of the slot), and after the whole warp has read, writes their bf16 values at
+            // elements 4l .. 4l + 3 (small integers are exact in bf16)
+#pragma unroll 1
+            for (int r = 0; r < kSub; ++r) {
+                const int32_t cd = code_of(c * kSub + r);
+                if (cd < kI8Base || cd >= kRingBase) continue;
+#pragma unroll
+                for (int which = 0; which < 2; ++which) {
+                    uint8_t* row = stages + st * L::kStage + which * kSub * L::kRowB + r * L::kRowB;
+                    const uint32_t w4 = *reinterpret_cast<const uint32_t*>(row + D + 4 * lane);
+                    __syncwarp();
+                    const float f0 = (float)(int8_t)(w4 & 0xffu), f1 = (float)(int8_t)((w4 >> 8) & 0xffu);
+                    const float f2 = (float)(int8_t)((w4 >> 16) & 0xffu), f3 = (float)(int8_t)(w4 >> 24);
+                    *reinterpret_cast<uint2*>(row + 8 * lane) = make_uint2(pack_bf16x2(f0, f1), pack_bf16x2(f2, f3));
+                    __syncwarp();
+                }
+            }
+        }
 
         // ---- S = Q K^T for this warp's 16 rows: [MT][2 n-tiles][4].  Even and odd k-steps
         // accumulate separately (4 independent MMA chains per M tile), then add.
@@ -206,8 +259,11 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const bool on = kval[nt][e] && vis(r, c * kSub + nt * 8 + 2 * t4 + e);
-                        x[nt][e] = on ? sacc[mt][nt][2 * hf + e] * scale_log2 : -INFINITY;
+                        const int jk = c * kSub + nt * 8 + 2 * t4 + e;
+                        const bool on = kval[nt][e] && vis(r, jk);
+                        float xs = sacc[mt][nt][2 * hf + e] * scale_log2;
+                        if constexpr (Scl::kInt8) xs *= scl.ks(jk);
+                        x[nt][e] = on ? xs : -INFINITY;
                         tmax = fmaxf(tmax, x[nt][e]);
                     }
                 tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
@@ -222,6 +278,7 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
                     for (int e = 0; e < 2; ++e) {
                         const float pv = (x[nt][e] == -INFINITY) ? 0.f : fast_exp2(x[nt][e] - mn);
                         sacc[mt][nt][2 * hf + e] = pv;
+                        if constexpr (Scl::kInt8) sacc[mt][nt][2 * hf + e] = pv * scl.vs(c * kSub + nt * 8 + 2 * t4 + e);
                         rsum += pv;
                     }
                 rsum += __shfl_xor_sync(0xffffffffu, rsum, 1);

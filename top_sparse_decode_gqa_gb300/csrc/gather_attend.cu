@@ -59,6 +59,11 @@ struct AttendParams {
     float* ws_o;
     float* ws_m;
     float* ws_l;
+    const uint8_t* tier;  // [B, T] or null: 3 skipped, 2 read from the int8 rows
+    const int8_t* ki8;    // [B, kv_heads, T, d] int8 codes
+    const int8_t* vi8;
+    const float* ksc;     // [B, kv_heads, T] scales
+    const float* vsc;
 };
 
 template <typename ST, int D, int RP>
@@ -451,13 +456,14 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
 
 // ------------------------------------------------------------------ bf16 path (warp MMA)
 
-template <int D, int RP>
+template <int D, int RP, bool I8 = false>
 struct MmaLayout {
     using Rows = MmaRows<D>;
     static constexpr int oQ = 0;
     static constexpr int oStage = ((RP * Rows::kRowB + 127) / 128) * 128;
     static constexpr int oSrc = oStage + Rows::kStagesBytes;
-    static constexpr int oML = oSrc + kMaxSplitRows * 4;   // [4 warps][RP] m, then l
+    static constexpr int oSc = oSrc + kMaxSplitRows * 4;   // with int8 rows: K scales, then V scales
+    static constexpr int oML = oSc + (I8 ? 2 * kMaxSplitRows * 4 : 0);   // [4 warps][RP] m, then l
     static constexpr int oRow = oML + 2 * kMmaWarps * RP * 4;  // [RP] row max, sum; [4][RP] factors
     static constexpr int oFlag = oRow + 6 * RP * 4;
     static constexpr int kBytes = oFlag + 16;
@@ -468,9 +474,11 @@ struct MmaLayout {
 // then attend_mma.cuh's per-warp loop runs over them; the 4 warps' (m, l, O) are combined
 // into the CTA's split partial (or, with one split, into out and lse); attend_merge_kernel
 // then merges the splits.  RING: the list ends with draft-ring slots, masked per query row.
-template <int D, int RP, bool RING>
+// I8: positions of tier 3 are skipped and those of tier 2 read from the int8 rows, their
+// scales kept per list row in shared memory.
+template <int D, int RP, bool RING, bool I8 = false>
 __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendParams p) {
-    using L = MmaLayout<D, RP>;
+    using L = MmaLayout<D, RP, I8>;
     using Rows = MmaRows<D>;
     constexpr int PPR = D * 2 / 16;  // 16-byte pieces per row
     extern __shared__ __align__(128) uint8_t sm[];
@@ -524,8 +532,17 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
                     ok = false;
                 }
             }
-            if (!ok) {
+            float kscl = 1.f, vscl = 1.f;
+            int tr = 0;
+            if constexpr (I8) {
+                if (ok) tr = p.tier[(size_t)b * p.T + pos];
+            }
+            if (!ok || tr == 3) {
                 code = kNoRow;
+            } else if (tr == 2) {
+                code = kI8Base + (int32_t)pos;
+                kscl = p.ksc[(size_t)kvsrc * p.T + pos];
+                vscl = p.vsc[(size_t)kvsrc * p.T + pos];
             } else if (p.slot_map == nullptr) {
                 code = (int32_t)pos;
             } else {
@@ -540,6 +557,10 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
                 }
             }
             src[j] = code;
+            if constexpr (I8) {
+                reinterpret_cast<float*>(sm + L::oSc)[j] = kscl;
+                reinterpret_cast<float*>(sm + L::oSc)[kMaxSplitRows + j] = vscl;
+            }
         }
     }
     cp_async_wait<0>();
@@ -554,6 +575,10 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     if (p.ring_w > 0) {
         rs.k_ring = p.rk + (size_t)kvsrc * p.ring_w * (D * 2);
         rs.v_ring = p.rv + (size_t)kvsrc * p.ring_w * (D * 2);
+    }
+    if constexpr (I8) {
+        rs.k_i8 = p.ki8 + (size_t)kvsrc * p.T * D;
+        rs.v_i8 = p.vi8 + (size_t)kvsrc * p.T * D;
     }
     auto row_code = [&](int j) -> int32_t { return p.resolve ? src[j] : (int32_t)(j0 + j); };
     float* lbase = nullptr;  // logits of query row 0 of this group, at list row j0
@@ -576,8 +601,15 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     };
     WarpAcc<D, RP> acc;
     acc.init();
-    mma_attend_warp<D, RP>(acc, sm + L::oStage + warp * Rows::kWarpBytes, smem_addr(sm + L::oQ), warp, nrows, p.R,
-                           rs, p.scale_log2, row_code, logit, visible);
+    if constexpr (I8) {
+        const SmemScales scl{reinterpret_cast<const float*>(sm + L::oSc),
+                             reinterpret_cast<const float*>(sm + L::oSc) + kMaxSplitRows};
+        mma_attend_warp<D, RP>(acc, sm + L::oStage + warp * Rows::kWarpBytes, smem_addr(sm + L::oQ), warp, nrows,
+                               p.R, rs, p.scale_log2, row_code, logit, visible, scl);
+    } else {
+        mma_attend_warp<D, RP>(acc, sm + L::oStage + warp * Rows::kWarpBytes, smem_addr(sm + L::oQ), warp, nrows,
+                               p.R, rs, p.scale_log2, row_code, logit, visible);
+    }
 
     float* ow = reinterpret_cast<float*>(sm + L::oStage);  // [4][RP][D]
     mma_combine_warps<D, RP>(acc, mlw, rowv, ow);
@@ -647,7 +679,7 @@ SplitPlan plan_splits(const sd_attend_args* a) {
     const long bk = (long)a->B * (a->per_head ? a->Hq : a->Hkv);
     sp.RP = kernel_rows(a->dtype, a->per_head ? a->V : (a->Hkv > 0 ? (a->Hq / a->Hkv) * a->V : 0));
     const long chunks = (n_rows + kCH - 1) / kCH;
-    const bool resolve = a->idx != nullptr || a->slot_map != nullptr || a->ring_w > 0;
+    const bool resolve = a->idx != nullptr || a->slot_map != nullptr || a->ring_w > 0 || a->tier != nullptr;
     long splits;
     if (a->splits > 0) {
         splits = a->splits;
@@ -681,6 +713,17 @@ sd_status launch_attend(const AttendParams& p, cudaStream_t st) {
 
 template <int D, int RP>
 sd_status launch_attend_mma(const AttendParams& p, cudaStream_t st) {
+    if constexpr (D == 128) {
+        if (p.tier != nullptr) {  // int8 rows (validated: no ring)
+            using L = MmaLayout<D, RP, true>;
+            auto kern = attend_mma_kernel<D, RP, false, true>;
+            SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes),
+                          "sd_gather_attend: cudaFuncSetAttribute");
+            SD_CUDA_CHECK(launch_pdl(kern, dim3(p.splits, p.Hkv, p.B), dim3(kAttThreads), L::kBytes, st, p),
+                          "sd_gather_attend: launch");
+            return launch_status("sd_gather_attend");
+        }
+    }
     using L = MmaLayout<D, RP>;
     auto kern = p.ring_w > 0 ? attend_mma_kernel<D, RP, true> : attend_mma_kernel<D, RP, false>;
     SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes),
@@ -736,6 +779,16 @@ sd_status sd::validate_attend_args(const sd_attend_args* a, const char* who) {
     }
     SD_REQUIRE(a->T < kRingBase && a->pool_rows < kRingBase, "%s: T and pool_rows must be < 2^30", who);
     SD_REQUIRE(a->slot_per_head == 0 || a->slot_per_head == 1, "%s: slot_per_head must be 0 or 1", who);
+    if (a->tier != nullptr) {
+        if (a->dtype != SD_BF16 || a->d != 128 || a->per_head || a->ring_w > 0 || a->k_stage != nullptr) {
+            set_error("%s: tiered rows need bf16, d = 128, no per_head, no ring and no stage", who);
+            return SD_ERR_UNSUPPORTED;
+        }
+        SD_REQUIRE(a->k_int8 && a->v_int8 && a->k_scale && a->v_scale,
+                   "%s: tier needs k_int8, v_int8, k_scale and v_scale", who);
+        SD_REQUIRE(aligned16(a->k_int8) && aligned16(a->v_int8), "%s: k_int8/v_int8 must be 16-byte aligned", who);
+        SD_REQUIRE(a->T < kI8Base && a->pool_rows < kI8Base, "%s: with tiers, T and pool_rows must be < 2^29", who);
+    }
     return SD_OK;
 }
 
@@ -828,7 +881,14 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
         p.ws_m = p.ws_o + np * a->d;
         p.ws_l = p.ws_m + np;
     }
-    p.resolve = (a->idx != nullptr || a->slot_map != nullptr || a->ring_w > 0) ? 1 : 0;
+    if (a->tier != nullptr) {
+        p.tier = a->tier;
+        p.ki8 = a->k_int8;
+        p.vi8 = a->v_int8;
+        p.ksc = a->k_scale;
+        p.vsc = a->v_scale;
+    }
+    p.resolve = (a->idx != nullptr || a->slot_map != nullptr || a->ring_w > 0 || a->tier != nullptr) ? 1 : 0;
     cudaStream_t st = as_stream(stream);
     const sd_status s1 = a->d == 128 ? dispatch_rp<128>(p, a->dtype, sp.RP, st) : dispatch_rp<64>(p, a->dtype, sp.RP, st);
     if (s1 != SD_OK || sp.splits == 1) return s1;

@@ -1050,6 +1050,10 @@ extern "C" sd_status sd_select_attend(const float* scores, int N, uint32_t* key_
         set_error("sd_select_attend: a draft ring goes through sd_topk + sd_gather_attend");
         return SD_ERR_UNSUPPORTED;
     }
+    if (a->tier != nullptr) {
+        set_error("sd_select_attend: tiered rows go through sd_topk + sd_gather_attend");
+        return SD_ERR_UNSUPPORTED;
+    }
     if (a->B == 0) return SD_OK;
     SD_REQUIRE(scores && a->q && a->out && a->lse && (k == 0 || idx), "sd_select_attend: null pointer");
     SD_REQUIRE(aligned16(a->q) && aligned16(a->out), "sd_select_attend: q and out must be 16-byte aligned");

@@ -153,6 +153,10 @@ extern "C" sd_status sd_stage_host_rows(const sd_attend_args* a, uint32_t* count
     sd_status vs = validate_attend_args(a, "sd_stage_host_rows");
     if (vs != SD_OK) return vs;
     SD_REQUIRE(a->slot_map != nullptr, "sd_stage_host_rows: needs slot_map");
+    if (a->tier != nullptr) {
+        set_error("sd_stage_host_rows: tiered rows read their host rows in sd_gather_attend");
+        return SD_ERR_UNSUPPORTED;
+    }
     SD_REQUIRE(a->k_host && a->v_host, "sd_stage_host_rows: needs k_host and v_host");
     SD_REQUIRE(a->k_stage && a->v_stage, "sd_stage_host_rows: needs k_stage and v_stage");
     SD_REQUIRE(aligned16(a->k_stage) && aligned16(a->v_stage),
