@@ -1023,7 +1023,80 @@ class DenseScoringStep:
                 "host": 0}
 
 
+class TieredAttendStep:
+    """One decode step over a tiered cache: for every layer, dense attention over all
+    positions with the four tiers of a seeded importance score driving the rows' sources --
+    T0 and T1 at bf16 from HBM, T2 as int8 codes times their per-row scale, T3 left out.
+    The tiers and the int8 codes (of every layer's K and V) are built once, untimed."""
+
+    dominant = "sd_gather_attend"
+    phases = ()
+    tier_seed = 2011
+
+    def __init__(self, w, x, device):
+        import torch
+        from top_sparse_decode_gqa_gb300 import binding as sd
+        from top_sparse_decode_gqa_gb300.workloads import importance_scores
+        self.sd, self.w, self.dev = sd, w, device
+        self.ks = [k.to(device) for k in x["k"]]
+        self.vs = [v.to(device) for v in x["v"]]
+        self.q = x["q"][0].to(device)              # [layers, B, V, Hq, d]
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        s = importance_scores(w.B, w.T, self.tier_seed).to(device)
+        self.tier, counts = sd.sd_tier_classify(s, w.cum_frac)
+        self.counts = counts.cpu()
+        self.codes = [sd.sd_quantize_rows_int8(k, self.tier) + sd.sd_quantize_rows_int8(v, self.tier)
+                      for k, v in zip(self.ks, self.vs)]  # (k codes, k scales, v codes, v scales)
+        self.args = []
+        for layer in range(w.layers):
+            kc, ksc, vc, vsc = self.codes[layer]
+            a, out, lse, _ = sd.make_attend_args(self.q[layer], self.ks[layer], self.vs[layer], None, T=w.T,
+                                                 err_word=self.err, tier=self.tier, k_int8=kc, v_int8=vc,
+                                                 k_scale=ksc, v_scale=vsc)
+            self.args.append((a, out, lse))
+        need = sd.sd_gather_attend_workspace_bytes(self.args[0][0])
+        self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=device)
+        self.out, self.lse = self.args[-1][1], self.args[-1][2]
+
+    @property
+    def launches_per_step(self):
+        return 2 * self.w.layers  # attention + split merge per layer
+
+    @property
+    def dominant_per_step(self):
+        return self.w.layers
+
+    def run(self, m: "StepMarks" = None):
+        sd = self.sd
+        if m is not None:
+            m.start.record()
+        for layer in range(self.w.layers):
+            if m is not None:
+                m.before(layer)
+            sd.sd_gather_attend(self.args[layer][0], self.ws)
+            if m is not None:
+                m.after(layer)
+        if m is not None:
+            m.end.record()
+
+    def after_warmup(self):
+        pass
+
+    def bytes(self):
+        w = self.w
+        c = [int(v) for v in self.counts[0]]  # per sequence (all equal: exact fractions)
+        heads = w.B * w.Hkv
+        rows_bf16 = (c[0] + c[1]) * heads   # T0 + T1 rows, K and V at bf16
+        rows_i8 = c[2] * heads              # T2 rows: K and V codes + scales
+        per_layer = rows_bf16 * 2 * w.d * 2 + rows_i8 * 2 * (w.d + 4) + w.B * w.T  # + the tier map
+        q = w.B * w.V * w.Hq * w.d * 2
+        out = w.B * w.V * w.Hq * (w.d + 1) * 4
+        return {"dominant": per_layer + q + out, "hbm": w.layers * (per_layer + q + out), "host": 0}
+
+
 def make_step(w, x, device, path="auto", tiered_path="staged", lookahead=True):
+    if w.tiered_attention:
+        return TieredAttendStep(w, x, device)
     if w.drift_steps > 0:
         return CachedTieredStep(w, x, device, concurrent=lookahead)
     if w.layer_indexers:
@@ -1202,6 +1275,9 @@ def path_description(step, w) -> str:
         else:
             head = "indexer + top-k + promotion into the pool (cache) + staging of the rest + gather-attend"
         return head + ", the query window sliding step by step"
+    if isinstance(step, TieredAttendStep):
+        return (f"per layer ({w.layers}): dense attention over the tiered cache (T0 and T1 rows at bf16, T2 rows as "
+                "int8 codes and per-row scales, T3 rows left out) + split merge")
     if isinstance(step, LookaheadStep):
         return (f"per layer ({w.layers}): indexer + top-k + host-row staging + gather-attend, "
                 + ("next layer's selection before this layer's attention, staging on its own stream"
@@ -1593,7 +1669,7 @@ def measure_e2e(step, w, x, clean_l2, K):
     host memory; host wall clock per step, including the copies and the final sync."""
     import torch
     verify = isinstance(step, VerifyGroupStep)
-    multi = isinstance(step, (VerifyGroupStep, LookaheadStep))
+    multi = isinstance(step, (VerifyGroupStep, LookaheadStep, TieredAttendStep))
     ins = [(step.q, x["q"][0] if multi else x["q"][0, 0] if w.layers > 1 else x["q"])]
     if isinstance(step, (SparseDecodeStep, WindowStep, VerifyGroupStep, LookaheadStep)):
         ins.append((step.q_idx, x["q_idx"]))
@@ -1606,6 +1682,7 @@ def measure_e2e(step, w, x, clean_l2, K):
                                CachedTieredStep))
     # the result tensors, looked up after every step (a step may alternate its buffers)
     results = lambda: [step.out, step.lse] + (  # noqa: E731
+        [] if isinstance(step, TieredAttendStep) else
         [step.idx[-1] if isinstance(step.idx, list) else step.idx] if sparse else [step.s])
     outs = [torch.empty(src.shape, dtype=src.dtype).pin_memory() for src in results()]
     times = []
@@ -1664,6 +1741,23 @@ def oracle_step(w, x, b0, b1):
                                                  w.k, 1, scale, torch_bf16(rk), torch_bf16(rv), rp,
                                                  x["qpos"][b0:b1].numpy()))
         return idx, res
+    if w.tiered_attention:  # the tiers of the seeded score drive every layer's dense attention
+        from top_sparse_decode_gqa_gb300.workloads import importance_scores
+        tier, _ = oracle.tier_classify(importance_scores(w.B, w.T, TieredAttendStep.tier_seed).numpy()[b0:b1],
+                                       np.array(w.cum_frac))
+        idx = np.broadcast_to(np.arange(w.T, dtype=np.int32), (nb, w.Hkv, w.T)).copy()
+        for b in range(nb):
+            idx[b][:, tier[b] == 3] = -1
+        t2 = np.broadcast_to((tier == 2)[:, None, :, None], (nb, w.Hkv, w.T, w.d))
+        res = []
+        for layer in range(w.layers):
+            kv = []
+            for t in (x["k"][layer][b0:b1].contiguous(), x["v"][layer][b0:b1].contiguous()):
+                codes, scales = oracle.quantize_rows_int8(t, tier, nb, w.Hkv, w.T, w.d)
+                kv.append(np.where(t2, codes.astype(np.float32) * scales[..., None], t.float().numpy()))
+            res.append(oracle.gather_attend(x["q"][0, layer, b0:b1].float(), kv[0], kv[1], idx, nb, w.V, w.Hq,
+                                            w.Hkv, w.d, w.T, w.T, 1, scale)[:2])
+        return res
     if w.layers > 1:  # dense attention per layer and the layer's importance-score term
         s = np.zeros((nb, w.T))
         for layer in range(w.layers):

@@ -64,23 +64,17 @@ struct RowSource {
     const uint8_t* v_ring = nullptr;
     const int8_t* k_i8 = nullptr;  // int8 rows (codes), offset to this (b, kvh) like the pool
     const int8_t* v_i8 = nullptr;
+    const float* k_scl = nullptr;  // their per-row scales, likewise offset
+    const float* v_scl = nullptr;
 };
 
-// Per-row scales of the rows' K and V: none (every row at full precision) ...
+// Whether the list holds int8 rows (the loop then widens their codes to bf16 in shared
+// memory and keeps every row's scale in its slot's pad: 1 for rows at full precision).
 struct NoScales {
     static constexpr bool kInt8 = false;
-    SD_DEVINL float ks(int) const { return 1.f; }
-    SD_DEVINL float vs(int) const { return 1.f; }
 };
-
-// ... or read from shared memory for list row j (1 for rows read at full precision, the
-// row's int8 scale for int8 rows, whose codes the loop widens to bf16 in shared memory).
-struct SmemScales {
+struct Int8Rows {
     static constexpr bool kInt8 = true;
-    const float* k;
-    const float* v;
-    SD_DEVINL float ks(int j) const { return k[j]; }
-    SD_DEVINL float vs(int j) const { return v[j]; }
 };
 
 // Visibility of list row j to query row r when every row is visible to every query.
@@ -115,9 +109,10 @@ struct WarpAcc {
 // vis(r, j) hides the row from the query row (the causal mask of the draft ring).
 // nq = the real query rows (<= RP): an upper half tile (rows 8..15 of an M tile) holding
 // none of them skips its softmax, and its P fragments are zero.
-// Scl: the rows' per-row scales (NoScales, or SmemScales with int8 rows: a row's codes are
-// copied into the upper half of its bf16 slot and widened in place before use; its K scale
-// multiplies its logits and its V scale its softmax weights in the PV product).
+// Scl: NoScales, or Int8Rows with int8 rows: a row's codes are copied into the upper half of
+// its bf16 slot and widened in place before use, and its scale into the slot's 16-byte pad
+// (the pad of full-precision rows holds 1); the K scale multiplies the row's logits and the
+// V scale its softmax weights in the PV product.
 template <int D, int RP, int NW = kMmaWarps, int NS = kWStages, class RowCode, class Logit, class Vis = AllVisible,
           class Scl = NoScales>
 SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_base, int warp, int nrows, int nq,
@@ -149,11 +144,14 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
             for (int q = 0; q < kSub / 4; ++q) {
                 uint8_t* dst = kst + which * kSub * L::kRowB + (q * 4 + sub) * L::kRowB + piece * 16;
                 if constexpr (Scl::kInt8) {
+                    float* pad = reinterpret_cast<float*>(dst - piece * 16 + 2 * D);
                     if (code[q] >= kI8Base && code[q] < kRingBase) {  // one 128-byte line of codes
                         const int8_t* srow = (which ? rs.v_i8 : rs.k_i8) + (size_t)(code[q] - kI8Base) * D;
                         cp_async16(dst + D, srow + piece * 16);
+                        if (piece == 0) cp_async4(pad, (which ? rs.v_scl : rs.k_scl) + (code[q] - kI8Base));
                         continue;
                     }
+                    if (piece == 0) *pad = 1.f;
                 }
                 if (code[q] == kNoRow) {
 #pragma unroll
@@ -262,7 +260,9 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
                         const int jk = c * kSub + nt * 8 + 2 * t4 + e;
                         const bool on = kval[nt][e] && vis(r, jk);
                         float xs = sacc[mt][nt][2 * hf + e] * scale_log2;
-                        if constexpr (Scl::kInt8) xs *= scl.ks(jk);
+                        if constexpr (Scl::kInt8)
+                            xs *= *reinterpret_cast<const float*>(stages + st * L::kStage +
+                                                                  (nt * 8 + 2 * t4 + e) * L::kRowB + 2 * D);
                         x[nt][e] = on ? xs : -INFINITY;
                         tmax = fmaxf(tmax, x[nt][e]);
                     }
@@ -278,7 +278,10 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
                     for (int e = 0; e < 2; ++e) {
                         const float pv = (x[nt][e] == -INFINITY) ? 0.f : fast_exp2(x[nt][e] - mn);
                         sacc[mt][nt][2 * hf + e] = pv;
-                        if constexpr (Scl::kInt8) sacc[mt][nt][2 * hf + e] = pv * scl.vs(c * kSub + nt * 8 + 2 * t4 + e);
+                        if constexpr (Scl::kInt8)
+                            sacc[mt][nt][2 * hf + e] =
+                                pv * *reinterpret_cast<const float*>(stages + st * L::kStage + kSub * L::kRowB +
+                                                                     (nt * 8 + 2 * t4 + e) * L::kRowB + 2 * D);
                         rsum += pv;
                     }
                 rsum += __shfl_xor_sync(0xffffffffu, rsum, 1);

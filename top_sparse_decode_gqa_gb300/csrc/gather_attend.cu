@@ -456,14 +456,13 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(const AttendParams 
 
 // ------------------------------------------------------------------ bf16 path (warp MMA)
 
-template <int D, int RP, bool I8 = false>
+template <int D, int RP>
 struct MmaLayout {
     using Rows = MmaRows<D>;
     static constexpr int oQ = 0;
     static constexpr int oStage = ((RP * Rows::kRowB + 127) / 128) * 128;
     static constexpr int oSrc = oStage + Rows::kStagesBytes;
-    static constexpr int oSc = oSrc + kMaxSplitRows * 4;   // with int8 rows: K scales, then V scales
-    static constexpr int oML = oSc + (I8 ? 2 * kMaxSplitRows * 4 : 0);   // [4 warps][RP] m, then l
+    static constexpr int oML = oSrc + kMaxSplitRows * 4;   // [4 warps][RP] m, then l
     static constexpr int oRow = oML + 2 * kMmaWarps * RP * 4;  // [RP] row max, sum; [4][RP] factors
     static constexpr int oFlag = oRow + 6 * RP * 4;
     static constexpr int kBytes = oFlag + 16;
@@ -474,11 +473,10 @@ struct MmaLayout {
 // then attend_mma.cuh's per-warp loop runs over them; the 4 warps' (m, l, O) are combined
 // into the CTA's split partial (or, with one split, into out and lse); attend_merge_kernel
 // then merges the splits.  RING: the list ends with draft-ring slots, masked per query row.
-// I8: positions of tier 3 are skipped and those of tier 2 read from the int8 rows, their
-// scales kept per list row in shared memory.
+// I8: positions of tier 3 are skipped and those of tier 2 read from the int8 rows.
 template <int D, int RP, bool RING, bool I8 = false>
 __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendParams p) {
-    using L = MmaLayout<D, RP, I8>;
+    using L = MmaLayout<D, RP>;
     using Rows = MmaRows<D>;
     constexpr int PPR = D * 2 / 16;  // 16-byte pieces per row
     extern __shared__ __align__(128) uint8_t sm[];
@@ -532,7 +530,6 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
                     ok = false;
                 }
             }
-            float kscl = 1.f, vscl = 1.f;
             int tr = 0;
             if constexpr (I8) {
                 if (ok) tr = p.tier[(size_t)b * p.T + pos];
@@ -541,8 +538,6 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
                 code = kNoRow;
             } else if (tr == 2) {
                 code = kI8Base + (int32_t)pos;
-                kscl = p.ksc[(size_t)kvsrc * p.T + pos];
-                vscl = p.vsc[(size_t)kvsrc * p.T + pos];
             } else if (p.slot_map == nullptr) {
                 code = (int32_t)pos;
             } else {
@@ -557,10 +552,6 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
                 }
             }
             src[j] = code;
-            if constexpr (I8) {
-                reinterpret_cast<float*>(sm + L::oSc)[j] = kscl;
-                reinterpret_cast<float*>(sm + L::oSc)[kMaxSplitRows + j] = vscl;
-            }
         }
     }
     cp_async_wait<0>();
@@ -579,6 +570,8 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     if constexpr (I8) {
         rs.k_i8 = p.ki8 + (size_t)kvsrc * p.T * D;
         rs.v_i8 = p.vi8 + (size_t)kvsrc * p.T * D;
+        rs.k_scl = p.ksc + (size_t)kvsrc * p.T;
+        rs.v_scl = p.vsc + (size_t)kvsrc * p.T;
     }
     auto row_code = [&](int j) -> int32_t { return p.resolve ? src[j] : (int32_t)(j0 + j); };
     float* lbase = nullptr;  // logits of query row 0 of this group, at list row j0
@@ -602,10 +595,8 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     WarpAcc<D, RP> acc;
     acc.init();
     if constexpr (I8) {
-        const SmemScales scl{reinterpret_cast<const float*>(sm + L::oSc),
-                             reinterpret_cast<const float*>(sm + L::oSc) + kMaxSplitRows};
         mma_attend_warp<D, RP>(acc, sm + L::oStage + warp * Rows::kWarpBytes, smem_addr(sm + L::oQ), warp, nrows,
-                               p.R, rs, p.scale_log2, row_code, logit, visible, scl);
+                               p.R, rs, p.scale_log2, row_code, logit, visible, Int8Rows{});
     } else {
         mma_attend_warp<D, RP>(acc, sm + L::oStage + warp * Rows::kWarpBytes, smem_addr(sm + L::oQ), warp, nrows,
                                p.R, rs, p.scale_log2, row_code, logit, visible);
@@ -715,7 +706,7 @@ template <int D, int RP>
 sd_status launch_attend_mma(const AttendParams& p, cudaStream_t st) {
     if constexpr (D == 128) {
         if (p.tier != nullptr) {  // int8 rows (validated: no ring)
-            using L = MmaLayout<D, RP, true>;
+            using L = MmaLayout<D, RP>;
             auto kern = attend_mma_kernel<D, RP, false, true>;
             SD_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes),
                           "sd_gather_attend: cudaFuncSetAttribute");

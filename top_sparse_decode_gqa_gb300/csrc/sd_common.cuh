@@ -152,6 +152,10 @@ SD_DEVINL void cp_async16(void* dst_smem, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src)
                  : "memory");
 }
+// 4-byte cp.async (through L1); both addresses 4-byte aligned.
+SD_DEVINL void cp_async4(void* dst_smem, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
+}
 // 16-byte cp.async that copies src_size (0 or 16) bytes and fills the rest with zeros.
 SD_DEVINL void cp_async16_zfill(void* dst_smem, const void* src, uint32_t src_size) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst_smem)), "l"(src),

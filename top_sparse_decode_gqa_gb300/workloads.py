@@ -47,6 +47,11 @@ available here):
   (sequence, KV head) -- every head starts from the generated resident positions -- and the
   pool is a cache: each step stages the selected rows the pool lacks, attends, and then
   promotes those rows from the stage into the pool (beside the next step's selection).
+* ``c11_tiered_attention``: the shape of ``c5`` (28 layers of 28/4 heads, T = 65536, batch
+  2) one decode step after tiering: the four tiers of a seeded importance score
+  (``importance_scores``, seed 2011; 20/40/30/10 %) drive every layer's dense attention --
+  T0 and T1 rows read at bf16 from HBM, T2 rows as int8 codes and per-row scales (the
+  int8 encode of each layer's K and V), T3 rows left out.
 
 Value recipe: indexer query and keys are integers drawn uniformly from [-8, 8] (exact in
 bf16 and fp32); attention q, K, V are standard normal, rounded to bf16 (nearest even)
@@ -92,6 +97,7 @@ class Workload:
     layer_indexers: bool = False  # one indexer query and key set per layer (selection per layer)
     drift_steps: int = 0    # > 0: decode steps whose V verify queries slide along a query sequence
     slot_per_head: bool = False  # residency (slot map) per (sequence, KV head) instead of per sequence
+    tiered_attention: bool = False  # the attention reads the four tiers of a seeded importance score
     cum_frac: tuple = (0.2, 0.6, 0.9)
     n_sink: int = 0
     n_recent: int = 0
@@ -163,6 +169,8 @@ WORKLOADS: Dict[str, Workload] = {
                  dI=128, k=1024, layers=4, ring_w=64),
         Workload("c9_lookahead_tiered", 8, B=2, V=8, Hq=32, Hkv=8, d=128, T=131072, dtype="bf16",
                  dI=128, k=2048, resident_frac=0.1, layers=4, layer_indexers=True),
+        Workload("c11_tiered_attention", 10, B=2, V=1, Hq=28, Hkv=4, d=128, T=65536, dtype="bf16", dI=128,
+                 k=65536, layers=28, steps=1, tiered_attention=True),
         Workload("c10_cached_tiered", 9, B=4, V=8, Hq=32, Hkv=8, d=128, T=131072, dtype="bf16",
                  dI=128, k=2048, resident_frac=0.1, drift_steps=16, slot_per_head=True),
     )
