@@ -75,8 +75,9 @@ struct BsParams {
     int nc;                // keys per CTA share (a multiple of 128)
     int ns;                // ring stages (even)
     int glg, gcnt;         // the selection's group maxima, taken while scoring: groups of
-                           // 2^glg keys, gcnt of them (glg = -1: not taken while scoring)
-    int oQ, oQi, oScore, oSel, oHist, oScan, oGmax, oInbox, oBars, oMisc;  // shared memory offsets
+                           // 2^glg keys, gcnt of them (glg = -1: no bound, the radix select)
+    int kr, cact;          // each of the cact CTAs holding keys bounds the top kr of its groups
+    int oQ, oQi, oScore, oSel, oHist, oScan, oGmax, oInbox, oAux, oBars, oMisc;  // shared memory offsets
     float scale_log2;
     unsigned long long wait_ns;
 };
@@ -181,125 +182,14 @@ SD_DEVINL void bs_select(const float* sc, int N, int k, int32_t* sel, uint32_t* 
     __syncthreads();
 }
 
-constexpr int kBsCandCap = 512;   // candidates the ranking takes
-constexpr int kBsMaxGroups = 512;  // group maxima the bound is taken over
+constexpr int kBsCandCap = 512;   // candidates of a group, over all the cluster's CTAs
+constexpr int kBsMaxGroups = 512;  // group maxima of a group's keys
 
-// Exact top-k of sc[0 .. N) (1 <= k < N) for k small against N, ties to the lower index, the
-// k indices ascending into sel[0 .. k).  Take G groups of gs consecutive entries (gs the
-// largest power of two, at least 4, that leaves about 2k of them; G a multiple of 4 and at
-// least k) and each group's maximum: the k-th
-// largest of those maxima, L, is at most the k-th largest entry (k distinct entries, one per
-// group, are >= L), so every entry of the top k has key >= L.  The entries with key >= L (the
-// candidates; about k plus a few for scores without heavy ties) are ranked exactly against
-// each other on the 64-bit key (order key, then the complement of the index, so ties go to
-// the lower index); the k of rank < k are marked in a bitmap over N, and one prefix sum over
-// the bitmap writes them ascending.  Every step is a handful of independent shared-memory
-// loads per thread (the warp's 32 lanes read 32 consecutive entries) and one barrier.
-// Returns false (uniformly, nothing written) when groups of 4 would not give k of them, when
-// the maxima exceed kBsMaxGroups, or when more than kBsCandCap entries reach L; `scratch`
-// holds the group maxima, the candidates and the bitmap.
-SD_DEVINL bool bs_select_fast(const float* sc, int N, int k, int32_t* sel, uint32_t* scratch, uint32_t* wt, int* bc,
-                               const uint32_t* gm_ready) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int NWARP = kBsThreads / 32;
-    int lg = 2;  // log2 of the group size
-    while ((N >> (lg + 1)) >= 2 * k) ++lg;
-    const int gs = 1 << lg, G = (N >> lg) & ~3;  // a multiple of 4: the maxima are read four at a time
-    if (G < k || G < 4 || G > kBsMaxGroups) return false;
-    uint32_t* gmax = gm_ready != nullptr ? const_cast<uint32_t*>(gm_ready) : scratch;  // [kBsMaxGroups]
-    unsigned long long* cand = reinterpret_cast<unsigned long long*>(scratch + kBsMaxGroups);  // [kBsCandCap]
-    uint32_t* bits = reinterpret_cast<uint32_t*>(cand + kBsCandCap);            // [ceil(N / 32)]
+// The k entries marked in bits[0 .. ceil(N/32)) written ascending into sel[0 .. k): thread t
+// owns bitmap words [t*W, t*W + W) and one prefix sum gives its first output slot.
+SD_DEVINL void bs_emit_bits(const uint32_t* bits, int N, int k, int32_t* sel, uint32_t* wt) {
+    const int tid = threadIdx.x;
     const int NW = (N + 31) / 32;
-    const int span = G * gs;  // the groups cover [0, span)
-    // the group maxima (unless the scoring took them): 32 consecutive entries per warp load,
-    // reduced within groups by shuffles
-    if (gm_ready != nullptr) {
-    } else if (gs <= 32) {
-        for (int base = warp * 32; base < span; base += 4 * kBsThreads) {
-            uint32_t m[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = base + u * kBsThreads + lane;
-                m[u] = i < span ? float_key(sc[i]) : 0u;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                for (int o = 1; o < gs; o <<= 1) m[u] = max(m[u], __shfl_xor_sync(0xffffffffu, m[u], o));
-                const int i = base + u * kBsThreads + lane;
-                if (i < span && (lane & (gs - 1)) == 0) gmax[i >> lg] = m[u];
-            }
-        }
-    } else {
-        for (int j = warp; j < G; j += NWARP) {
-            uint32_t m = 0u;
-            for (int i = (j << lg) + lane; i < ((j + 1) << lg); i += 32) m = max(m, float_key(sc[i]));
-            m = __reduce_max_sync(0xffffffffu, m);
-            if (lane == 0) gmax[j] = m;
-        }
-    }
-    for (int w = tid; w < NW; w += kBsThreads) bits[w] = 0u;
-    if (tid == 0) wt[0] = 0u;  // the bound; stays the least key if no maximum were found (impossible)
-    __syncthreads();
-    // L = the k-th largest group maximum: one with fewer than k above it and at least k at or
-    // above it
-    for (int gi = tid; gi < G; gi += kBsThreads) {
-        const uint32_t v = gmax[gi];
-        int gt = 0, ge = 0;
-        const uint4* g4 = reinterpret_cast<const uint4*>(gmax);
-#pragma unroll 4
-        for (int h = 0; h < G / 4; ++h) {
-            const uint4 u = g4[h];
-            gt += (u.x > v) + (u.y > v) + (u.z > v) + (u.w > v);
-            ge += (u.x >= v) + (u.y >= v) + (u.z >= v) + (u.w >= v);
-        }
-        if (gt < k && k <= ge) wt[0] = v;
-    }
-    __syncthreads();
-    const uint32_t L = wt[0];
-    // the candidates: each warp counts its own (chunks of 32 at warp*32 + 160c), reserves
-    // its slots after one barrier, and writes them
-    uint32_t mine = 0u;
-    for (int base = warp * 32; base < N; base += kBsThreads) {
-        const int i = base + lane;
-        mine += (uint32_t)__popc(__ballot_sync(0xffffffffu, i < N && float_key(sc[i]) >= L));
-    }
-    __syncthreads();  // everyone has read wt[0]
-    if (lane == 0) wt[warp] = mine;
-    __syncthreads();
-    uint32_t at = 0u, cnt = 0u;
-#pragma unroll
-    for (int w = 0; w < NWARP; ++w) {
-        at += w < warp ? wt[w] : 0u;
-        cnt += wt[w];
-    }
-    if (cnt > (uint32_t)kBsCandCap) return false;
-    for (int base = warp * 32; base < N; base += kBsThreads) {
-        const int i = base + lane;
-        const uint32_t key = i < N ? float_key(sc[i]) : 0u;
-        const bool c = i < N && key >= L;
-        const uint32_t m = __ballot_sync(0xffffffffu, c);
-        if (c) cand[at + (uint32_t)__popc(m & lanemask_lt())] =
-            ((unsigned long long)key << 32) | (unsigned long long)(0xffffffffu - (uint32_t)i);
-        at += (uint32_t)__popc(m);
-    }
-    __syncthreads();
-    // rank of each candidate among the candidates; rank < k: selected
-    for (int c = tid; c < (int)cnt; c += kBsThreads) {
-        const unsigned long long v = cand[c];
-        int r0 = 0, r1 = 0;
-        int j = 0;
-        for (; j + 2 <= (int)cnt; j += 2) {
-            r0 += cand[j] > v ? 1 : 0;
-            r1 += cand[j + 1] > v ? 1 : 0;
-        }
-        if (j < (int)cnt) r0 += cand[j] > v ? 1 : 0;
-        if (r0 + r1 < k) {
-            const uint32_t i = 0xffffffffu - (uint32_t)(v & 0xffffffffull);
-            atomicOr(&bits[i >> 5], 1u << (i & 31));
-        }
-    }
-    __syncthreads();
-    // ascending emit: thread t owns bitmap words [t*W, t*W + W)
     const int W = (NW + kBsThreads - 1) / kBsThreads;
     const int w0 = tid * W, w1 = min(NW, w0 + W);
     uint32_t n = 0u;
@@ -315,7 +205,6 @@ SD_DEVINL bool bs_select_fast(const float* sc, int N, int k, int32_t* sel, uint3
         }
     }
     __syncthreads();
-    return true;
 }
 
 template <bool F16, int NQ>
@@ -346,6 +235,7 @@ __global__ void __launch_bounds__(kBsThreads, 2)
         }
         mbar_init(qbar, 1);
         *abort_flag = 0;
+        reinterpret_cast<uint32_t*>(sm + p.oAux)[kBsMaxCluster] = 0u;  // this CTA's candidate count
         fence_mbarrier_init();
     }
     __syncthreads();
@@ -434,23 +324,45 @@ __global__ void __launch_bounds__(kBsThreads, 2)
                 const int gsz = 1 << p.glg;
                 if (gsz == 64) {
                     const uint32_t m = __reduce_max_sync(0xffffffffu, max(key[0], key[1]));
-                    if (lane == 0 && (jt >> 6) < p.gcnt)
-                        for (int c = 0; c < C; ++c) *cl.map_shared_rank(gmx + (jt >> 6), c) = m;
+                    if (lane == 0 && (jt >> 6) < p.gcnt) gmx[jt >> 6] = m;
                 } else {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         uint32_t m = key[h];
                         for (int o = 1; o < gsz; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
                         const int j = jt + 32 * h + lane;
-                        if ((lane & (gsz - 1)) == 0 && (j >> p.glg) < p.gcnt)
-                            for (int c = 0; c < C; ++c) *cl.map_shared_rank(gmx + (j >> p.glg), c) = m;
+                        if ((lane & (gsz - 1)) == 0 && (j >> p.glg) < p.gcnt) gmx[j >> p.glg] = m;
                     }
                 }
             }
         }
+        if (p.glg >= 0 && j_begin < p.N) {
+            // this CTA's bound: the kr-th largest maximum of its share's whole groups (kr of its
+            // entries, in distinct groups, reach it), pushed to every CTA of the cluster
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * kBsCons) : "memory");
+            if (warp == 0) {
+                const int g0 = j_begin >> p.glg, g1 = min(p.gcnt, j_end >> p.glg);
+                uint32_t lb = 0u;
+                for (int base = g0; base < g1; base += 32) {
+                    const int i = base + lane;
+                    if (i < g1) {
+                        const uint32_t v = gmx[i];
+                        int gt = 0, ge = 0;
+                        for (int u = g0; u < g1; ++u) {
+                            const uint32_t w = gmx[u];
+                            gt += w > v ? 1 : 0;
+                            ge += w >= v ? 1 : 0;
+                        }
+                        if (gt < p.kr && p.kr <= ge) lb = v;
+                    }
+                }
+                lb = __reduce_max_sync(0xffffffffu, lb);  // every lane that found it found the same value
+                if (lane < C) *cl.map_shared_rank(reinterpret_cast<uint32_t*>(sm + p.oAux) + r, lane) = lb;
+            }
+        }
     }
     __syncwarp();
-    cl.sync();  // (1) every CTA holds the whole score row (and the group maxima)
+    cl.sync();  // (1) every CTA holds the whole score row and every CTA's bound
 
     // ---------------------------------------------------------------- 2. select
     {
@@ -458,10 +370,80 @@ __global__ void __launch_bounds__(kBsThreads, 2)
             for (int i = tid; i < p.N; i += kBsThreads) sel[i] = i;
             __syncthreads();
         } else if (p.k > 0) {
-            // the ring is idle between the two phases: the candidates and the bitmap go there
             uint32_t* wt = reinterpret_cast<uint32_t*>(sm + p.oScan);
             int* bc = reinterpret_cast<int*>(sm + p.oScan + 32);
-            if (!bs_select_fast(sc, p.N, p.k, sel, reinterpret_cast<uint32_t*>(sm), wt, bc, p.glg >= 0 ? gmx : nullptr))
+            bool done = false;
+            if (p.glg >= 0) {
+                // L = the least of the CTAs' bounds: each holding CTA has kr >= k / cact entries
+                // at or above its own, so the top k all reach L.  Each CTA ranks the candidates
+                // (entries >= L) of the whole row: it takes those of its own share and pushes them
+                // into region r of every CTA's ring (idle between the phases), with their count.
+                const uint32_t* lbs = reinterpret_cast<const uint32_t*>(sm + p.oAux);
+                uint32_t* lcnt = reinterpret_cast<uint32_t*>(sm + p.oAux) + kBsMaxCluster;
+                uint32_t L = 0xffffffffu;
+                for (int c = 0; c < p.cact; ++c) L = min(L, lbs[c]);
+                uint32_t* cnt = reinterpret_cast<uint32_t*>(sm);  // [C] candidates from each CTA
+                unsigned long long* cand = reinterpret_cast<unsigned long long*>(sm + 64);  // [C][capr], then the list
+                uint32_t* bits = reinterpret_cast<uint32_t*>(sm + 64 + 2 * kBsCandCap * 8);  // [ceil(N / 32)]
+                const int capr = kBsCandCap / C;
+                for (int w = tid; w < (p.N + 31) / 32; w += kBsThreads) bits[w] = 0u;
+                const uint32_t lt = lanemask_lt();
+                for (int base = j_begin + warp * 32; base < j_end; base += kBsThreads) {
+                    const int i = base + lane;
+                    const uint32_t key = i < j_end ? float_key(sc[i]) : 0u;
+                    const bool on = i < j_end && key >= L;
+                    const uint32_t m = __ballot_sync(0xffffffffu, on);
+                    if (m == 0u) continue;
+                    uint32_t at = 0u;
+                    if (lane == 0) at = atomicAdd(lcnt, (uint32_t)__popc(m));
+                    at = __shfl_sync(0xffffffffu, at, 0) + (uint32_t)__popc(m & lt);
+                    if (on && at < (uint32_t)capr) {
+                        const unsigned long long v = ((unsigned long long)key << 32) | (0xffffffffu - (uint32_t)i);
+                        for (int c = 0; c < C; ++c) *cl.map_shared_rank(cand + r * capr + at, c) = v;
+                    }
+                }
+                __syncthreads();
+                if (tid < C) *cl.map_shared_rank(cnt + r, tid) = *lcnt;  // above capr: overflow
+                cl.sync();  // (1b) every CTA holds every CTA's candidates
+                bool ovf = false;
+                for (int c = 0; c < C; ++c) ovf = ovf || cnt[c] > (uint32_t)capr;
+                if (!ovf) {
+                    // the regions as one list, then the rank of each candidate among all of them
+                    // (order key, then the lower index), eight loads in flight per thread
+                    unsigned long long* lst = cand + kBsCandCap;  // [total], after the regions
+                    int total = 0;
+                    for (int c = 0; c < C; ++c) {
+                        const int n = (int)cnt[c];
+                        for (int s2 = tid; s2 < n; s2 += kBsThreads) lst[total + s2] = cand[c * capr + s2];
+                        total += n;
+                    }
+                    __syncthreads();
+                    for (int q = tid; q < total; q += kBsThreads) {
+                        const unsigned long long v = lst[q];
+                        int r0 = 0, r1 = 0;
+                        int t = 0;
+                        for (; t + 8 <= total; t += 8) {
+                            unsigned long long u[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) u[e] = lst[t + e];
+#pragma unroll
+                            for (int e = 0; e < 8; e += 2) {
+                                r0 += u[e] > v ? 1 : 0;
+                                r1 += u[e + 1] > v ? 1 : 0;
+                            }
+                        }
+                        for (; t < total; ++t) r0 += lst[t] > v ? 1 : 0;
+                        if (r0 + r1 < p.k) {
+                            const uint32_t i = 0xffffffffu - (uint32_t)(v & 0xffffffffull);
+                            atomicOr(&bits[i >> 5], 1u << (i & 31));
+                        }
+                    }
+                    __syncthreads();
+                    bs_emit_bits(bits, p.N, p.k, sel, wt);
+                    done = true;
+                }
+            }
+            if (!done)  // no bound, or too many entries reach it (heavy ties): radix over the row
                 bs_select(sc, p.N, p.k, sel, reinterpret_cast<uint32_t*>(sm + p.oHist), wt, bc);
         }
         if (r == 0)
@@ -616,7 +598,7 @@ __global__ void __launch_bounds__(kBsThreads, 2)
 
 struct BsPlan {
     int C, ns, nc, per_sm, bytes;
-    int oQ, oQi, oScore, oSel, oHist, oScan, oGmax, oInbox, oBars, oMisc;
+    int oQ, oQi, oScore, oSel, oHist, oScan, oGmax, oInbox, oAux, oBars, oMisc;
 };
 
 int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -643,6 +625,8 @@ BsPlan layout_for(int N, int k, int C, int ns) {
     off += kBsMaxGroups * 4;
     pl.oInbox = off;
     off += kBsInboxBytes;
+    pl.oAux = off;
+    off += 64;
     pl.oBars = off;
     off += align_up((2 * ns + 1) * 8, 16);
     pl.oMisc = off;
@@ -734,15 +718,24 @@ sd_status block_step_launch(const sd_decode_step_args* a, cudaStream_t st) {
     p.oScan = pl.oScan;
     p.oGmax = pl.oGmax;
     p.oInbox = pl.oInbox;
+    p.oAux = pl.oAux;
     // the selection's group maxima are taken while scoring when its fast path applies and a
     // group (2^glg keys, glg <= 6) lies within one 64-key scoring tile
     p.glg = -1;
     p.gcnt = 0;
+    p.cact = (N + pl.nc - 1) / pl.nc;
+    p.kr = (p.k + p.cact - 1) / std::max(1, p.cact);
     if (p.k > 0 && p.k < N) {
         int lg = 2;
         while ((N >> (lg + 1)) >= 2 * p.k) ++lg;
         const int G = (N >> lg) & ~3;
-        if (G >= p.k && G >= 4 && G <= kBsMaxGroups && lg <= 6) {
+        // every CTA holding keys needs kr whole groups of its own share for its bound
+        bool enough = G >= p.k && G >= 4 && G <= kBsMaxGroups && lg <= 6;
+        for (int c = 0; enough && c < p.cact; ++c) {
+            const int j0 = c * pl.nc, j1 = std::min(N, j0 + pl.nc);
+            enough = std::min(G, j1 >> lg) - (j0 >> lg) >= p.kr;
+        }
+        if (enough) {
             p.glg = lg;
             p.gcnt = G;
         }
