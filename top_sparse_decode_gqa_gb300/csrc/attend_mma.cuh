@@ -179,25 +179,30 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
         const uint32_t k_base = smem_addr(stages + st * L::kStage);
         const uint32_t v_base = k_base + kSub * L::kRowB;
         const int c = warp + NW * ci;
+        // with int8 rows: the chunk's row codes, one per lane (lanes 16..31 none)
+        int32_t my_code = kNoRow;
+        if constexpr (Scl::kInt8) my_code = lane < kSub ? code_of(c * kSub + lane) : kNoRow;
         if constexpr (Scl::kInt8) {
-            // widen the chunk's int8 rows in place: lane l reads codes 4l .. 4l + 3 (upper half
-            // of the slot), and after the whole warp has read, writes their bf16 values at
-            // elements 4l .. 4l + 3 (small integers are exact in bf16)
-#pragma unroll 1
-            for (int r = 0; r < kSub; ++r) {
-                const int32_t cd = code_of(c * kSub + r);
-                if (cd < kI8Base || cd >= kRingBase) continue;
-#pragma unroll
-                for (int which = 0; which < 2; ++which) {
-                    uint8_t* row = stages + st * L::kStage + which * kSub * L::kRowB + r * L::kRowB;
-                    const uint32_t w4 = *reinterpret_cast<const uint32_t*>(row + D + 4 * lane);
-                    __syncwarp();
-                    const float f0 = (float)(int8_t)(w4 & 0xffu), f1 = (float)(int8_t)((w4 >> 8) & 0xffu);
-                    const float f2 = (float)(int8_t)((w4 >> 16) & 0xffu), f3 = (float)(int8_t)(w4 >> 24);
-                    *reinterpret_cast<uint2*>(row + 8 * lane) = make_uint2(pack_bf16x2(f0, f1), pack_bf16x2(f2, f3));
-                    __syncwarp();
-                }
+            // widen the chunk's int8 rows in place: lane l reads codes 4l .. 4l + 3 of the K and
+            // the V row (upper half of their slots), and after the whole warp has read, writes
+            // their bf16 values at elements 4l .. 4l + 3 (small integers are exact in bf16)
+            uint32_t i8 = __ballot_sync(0xffffffffu, my_code >= kI8Base && my_code < kRingBase);
+            while (i8 != 0u) {
+                const int r = __ffs(i8) - 1;
+                i8 &= i8 - 1u;
+                uint8_t* krow = stages + st * L::kStage + r * L::kRowB;
+                uint8_t* vrow = krow + kSub * L::kRowB;
+                const uint32_t wk = *reinterpret_cast<const uint32_t*>(krow + D + 4 * lane);
+                const uint32_t wv = *reinterpret_cast<const uint32_t*>(vrow + D + 4 * lane);
+                __syncwarp();
+                *reinterpret_cast<uint2*>(krow + 8 * lane) =
+                    make_uint2(pack_bf16x2((float)(int8_t)(wk & 0xffu), (float)(int8_t)((wk >> 8) & 0xffu)),
+                               pack_bf16x2((float)(int8_t)((wk >> 16) & 0xffu), (float)(int8_t)(wk >> 24)));
+                *reinterpret_cast<uint2*>(vrow + 8 * lane) =
+                    make_uint2(pack_bf16x2((float)(int8_t)(wv & 0xffu), (float)(int8_t)((wv >> 8) & 0xffu)),
+                               pack_bf16x2((float)(int8_t)((wv >> 16) & 0xffu), (float)(int8_t)(wv >> 24)));
             }
+            __syncwarp();
         }
 
         // ---- S = Q K^T for this warp's 16 rows: [MT][2 n-tiles][4].  Even and odd k-steps
@@ -239,7 +244,12 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) kval[nt][e] = code_of(c * kSub + nt * 8 + 2 * t4 + e) != kNoRow;
+            for (int e = 0; e < 2; ++e) {
+                if constexpr (Scl::kInt8)
+                    kval[nt][e] = __shfl_sync(0xffffffffu, my_code, nt * 8 + 2 * t4 + e) != kNoRow;
+                else
+                    kval[nt][e] = code_of(c * kSub + nt * 8 + 2 * t4 + e) != kNoRow;
+            }
         uint32_t ph[MT][4], pl[MT][4];  // P as A fragments (hi, lo)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {

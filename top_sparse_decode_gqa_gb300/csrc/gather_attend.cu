@@ -573,7 +573,15 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
         rs.k_scl = p.ksc + (size_t)kvsrc * p.T;
         rs.v_scl = p.vsc + (size_t)kvsrc * p.T;
     }
-    auto row_code = [&](int j) -> int32_t { return p.resolve ? src[j] : (int32_t)(j0 + j); };
+    auto row_code = [&](int j) -> int32_t {
+        if (p.resolve) return src[j];
+        const int32_t pos = j0 + j;
+        if constexpr (I8) {  // dense over the cache: the position's tier decides, read as needed
+            const uint8_t t = __ldg(p.tier + (size_t)b * p.T + pos);
+            return t == 3 ? kNoRow : t == 2 ? kI8Base + pos : pos;
+        }
+        return pos;
+    };
     float* lbase = nullptr;  // logits of query row 0 of this group, at list row j0
     if (p.logits != nullptr) lbase = p.logits + ((size_t)b * p.V * p.Hq + kvh * p.G) * p.n_rows + j0;
     auto logit = [&](int r, int j, float x) {
@@ -670,7 +678,7 @@ SplitPlan plan_splits(const sd_attend_args* a) {
     const long bk = (long)a->B * (a->per_head ? a->Hq : a->Hkv);
     sp.RP = kernel_rows(a->dtype, a->per_head ? a->V : (a->Hkv > 0 ? (a->Hq / a->Hkv) * a->V : 0));
     const long chunks = (n_rows + kCH - 1) / kCH;
-    const bool resolve = a->idx != nullptr || a->slot_map != nullptr || a->ring_w > 0 || a->tier != nullptr;
+    const bool resolve = a->idx != nullptr || a->slot_map != nullptr || a->ring_w > 0;
     long splits;
     if (a->splits > 0) {
         splits = a->splits;
@@ -879,7 +887,8 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
         p.ksc = a->k_scale;
         p.vsc = a->v_scale;
     }
-    p.resolve = (a->idx != nullptr || a->slot_map != nullptr || a->ring_w > 0 || a->tier != nullptr) ? 1 : 0;
+    // tiers alone (dense over the cache) need no resolving: a row's code follows from its tier
+    p.resolve = (a->idx != nullptr || a->slot_map != nullptr || a->ring_w > 0) ? 1 : 0;
     cudaStream_t st = as_stream(stream);
     const sd_status s1 = a->d == 128 ? dispatch_rp<128>(p, a->dtype, sp.RP, st) : dispatch_rp<64>(p, a->dtype, sp.RP, st);
     if (s1 != SD_OK || sp.splits == 1) return s1;
