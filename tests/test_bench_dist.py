@@ -126,3 +126,57 @@ def test_spawn_command_runs_torchrun_on_localhost():
     assert cmd[cmd.index("--nproc-per-node") + 1] == "4"
     assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
     assert cmd[-2:] == ["--steps", "5"]
+
+
+def test_rotation_count_keeps_three_l2_between_uses():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class FakeStep:
+        def __init__(self, hbm):
+            self.hbm = hbm
+
+        def bytes(self):
+            return {"hbm": self.hbm}
+
+    l2 = 126 << 20
+    for hbm in (84 << 20, 571 << 20, 10 << 20, 3 << 30):
+        n = bench.rotation_count(FakeStep(hbm), l2)
+        assert n >= 2
+        assert (n - 1) * hbm >= 3 * l2          # enough other traffic between two uses of a copy
+        assert n == 2 or (n - 2) * hbm < 3 * l2  # and no more copies than that needs
+
+
+def test_cluster_step_takes_block_selection_over_short_rows():
+    sys.path.insert(0, ROOT)
+    import bench
+    from top_sparse_decode_gqa_gb300.workloads import WORKLOADS
+    assert bench.cluster_step_supported(WORKLOADS["c3_block_sparse"])
+    for name in ("c1_tiny", "c2_llama3_8b_gqa", "c4_tiered_verify", "c6_window_blocks", "c7_head_topk"):
+        assert not bench.cluster_step_supported(WORKLOADS[name])
+    w = WORKLOADS["c3_block_sparse"]
+    assert not bench.cluster_step_supported(w.scaled(block=48))   # runs must be whole 16/32-row pieces
+    assert not bench.cluster_step_supported(w.scaled(T=64 * 8196))  # more blocks than one cluster holds
+
+
+def test_tiered_attention_oracle_step_leaves_t3_out():
+    # the CPU reference of the tiered step at a small size: with every position in T0 it is the
+    # plain dense attention; with the tiers it differs (T2 quantised, T3 gone)
+    import math
+
+    import numpy as np
+
+    import oracle
+    sys.path.insert(0, ROOT)
+    import bench
+    from top_sparse_decode_gqa_gb300.workloads import WORKLOADS, generate
+    w = WORKLOADS["c11_tiered_attention"].scaled(T=1024, layers=2, Hq=8, Hkv=2)
+    x = generate(w)
+    res = bench.oracle_step(w, x, 0, 1)
+    assert len(res) == w.layers
+    plain = oracle.gather_attend(x["q"][0, 0, 0:1].contiguous(), x["k"][0][0:1].contiguous(),
+                                 x["v"][0][0:1].contiguous(), None, 1, w.V, w.Hq, w.Hkv, w.d, w.T, w.T, 1,
+                                 1 / math.sqrt(w.d))[0]
+    out, lse = res[0]
+    assert out.shape == plain.shape and np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    assert not np.allclose(out, plain, atol=1e-6)
