@@ -145,6 +145,7 @@ struct SaMisc {
     uint32_t cgt[kSaMaxCluster], ceq[kSaMaxCluster];  // per part: above / equal to the threshold
     uint32_t nfb;                     // this CTA's final-bin entries
     uint32_t ncand;                   // candidates of this part (may exceed kSaCand)
+    uint32_t nabove;                  // entries of this part marked in sel so far
     uint32_t wgt[kSaWarps], weq[kSaWarps];
     uint32_t wsum[kSaWarps];
     uint32_t sel_digit, sel_above, tot;
@@ -190,38 +191,61 @@ SD_DEVNOINL uint32_t cta_exclusive_scan(uint32_t v, SaMisc* ms, uint32_t& total)
     return incl - v;
 }
 
-// Given the histogram of one digit (nb bins, higher bins = larger keys) of the entries
-// still in the running, the digit holding the krem-th largest and how many entries lie in
-// higher bins.  Thread t owns bins [nb - per*(t+1), nb - per*t).  If no bin crosses (a
-// histogram that does not match the scores) the answer is digit 0, 0 above.
-SD_DEVNOINL void cta_select_digit(const uint32_t* hist, int nb, uint32_t krem, SaMisc* ms, uint32_t& digit,
-                                uint32_t& above) {
+// Given the histogram of one digit (128 * PER bins, higher bins = larger keys) of the
+// entries still in the running, the digit holding the krem-th largest and how many entries
+// lie in higher bins.  Thread t holds its bins [PER*(127-t), PER*(128-t)) in registers (v,
+// four bins per word), so thread order is descending bin order; the bins are read as 16-byte
+// words, a few lanes to a shared-memory bank.  If no bin crosses (a histogram that does not
+// match the scores) the answer is digit 0, 0 above.
+template <int PER>
+SD_DEVINL void cta_select_digit_regs(const uint4 (&v)[PER / 4], uint32_t krem, SaMisc* ms, uint32_t& digit,
+                                     uint32_t& above) {
+    static_assert(kSaThreads == 128 && PER % 4 == 0, "digit select layout");
     const int tid = threadIdx.x;
     if (tid == 0) {
         ms->sel_digit = 0;
         ms->sel_above = 0;
     }
-    const int per = nb / kSaThreads;
-    const int hi = nb - per * tid;
     uint32_t local = 0;
-    for (int b = hi - per; b < hi; ++b) local += hist[b];
+#pragma unroll
+    for (int q = 0; q < PER / 4; ++q) local += v[q].x + v[q].y + v[q].z + v[q].w;
     const uint32_t incl = cta_inclusive_scan(local, ms->wsum);
     const uint32_t excl = incl - local;
     if (excl < krem && krem <= incl) {
+        const uint32_t lo = (uint32_t)(PER * (kSaThreads - 1 - tid));
         uint32_t acc = excl;
-        for (int b = hi - 1; b >= hi - per; --b) {
-            if (acc + hist[b] >= krem) {
-                ms->sel_digit = (uint32_t)b;
+        bool found = false;
+#pragma unroll
+        for (int i = PER - 1; i >= 0; --i) {
+            const uint4 w = v[i / 4];
+            const uint32_t h = (i & 3) == 0 ? w.x : (i & 3) == 1 ? w.y : (i & 3) == 2 ? w.z : w.w;
+            if (!found && acc + h >= krem) {
+                ms->sel_digit = lo + (uint32_t)i;
                 ms->sel_above = acc;
-                break;
+                found = true;
             }
-            acc += hist[b];
+            acc += h;
         }
     }
     __syncthreads();
     digit = ms->sel_digit;
     above = ms->sel_above;
     __syncthreads();
+}
+
+// The same over a histogram in shared memory (16-byte aligned) of nb = 2048 or 1024 bins.
+SD_DEVNOINL void cta_select_digit(const uint32_t* hist, int nb, uint32_t krem, SaMisc* ms, uint32_t& digit,
+                                uint32_t& above) {
+    const int t = kSaThreads - 1 - (int)threadIdx.x;
+    if (nb == kSaHist) {
+        const uint4* h4 = reinterpret_cast<const uint4*>(hist) + 4 * t;
+        const uint4 v[4] = {h4[0], h4[1], h4[2], h4[3]};
+        cta_select_digit_regs<16>(v, krem, ms, digit, above);
+    } else {
+        const uint4* h4 = reinterpret_cast<const uint4*>(hist) + 2 * t;
+        const uint4 v[2] = {h4[0], h4[1]};
+        cta_select_digit_regs<8>(v, krem, ms, digit, above);
+    }
 }
 
 // dst[i] = sum over the cluster's P CTAs of their copy of src[i], i < n (n a multiple of 4).
@@ -252,50 +276,121 @@ SD_DEVINL float key_float(uint32_t k) {
 }
 
 // One pass over the part [p0, p1): sel word w = the entries of 32-score group w above the
-// d0 bin, tie word w = those in it.  Lanes 0..U-1 store the U groups a warp just scanned, so
-// nothing diverges; the staging and compare modes are compile-time, so the U loads and
-// compares of a round interleave.
+// d0 bin, tie word w cleared.  The entries in the bin (the candidates) are listed with their
+// order keys and positions in the part (in no particular order; only the first kSaCand are
+// kept) and their next digit (bits 20..10) is counted into hist1; *ncand ends as the part's
+// candidate count and *nabove the part's entries above the bin.  Staged scores: each lane builds the bits of its own word in registers,
+// reading entry (j + lane) mod 32 at step j so the warp's reads fall in 32 distinct banks;
+// the listing takes one warp prefix sum and one atomic per warp.  Scores read from global
+// memory: each warp votes on 32-score groups (coalesced), U groups per round.
 template <bool STAGED, bool FCMP>
 SD_DEVNOINL void sa_scan(const uint32_t* keys_s, const float* srow, int p0, int p1, int nw, uint32_t d0, float f_lo,
-                       float f_hi, uint32_t k_hi, uint32_t* sel, uint32_t* tie) {
-    constexpr int U = 8;
+                       float f_hi, uint32_t k_hi, uint32_t* sel, uint32_t* tie, uint32_t* cand_k, uint32_t* cand_i,
+                       uint32_t* hist1, uint32_t* ncand, uint32_t* nabove) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int g0 = warp; g0 < nw; g0 += U * kSaWarps) {
-        float f[U];
-        uint32_t sure[U], cm[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = p0 + (g0 + u * kSaWarps) * 32 + lane;
-            if constexpr (STAGED)
-                f[u] = i < p1 ? __uint_as_float(keys_s[i - p0]) : 0.f;
-            else
-                f[u] = i < p1 ? __ldcg(srow + i) : 0.f;
+    auto classify = [&](float f, bool& above, bool& in) {
+        if constexpr (FCMP) {
+            above = f > f_hi;
+            in = f >= f_lo && f <= f_hi;
+        } else {
+            const uint32_t kk = float_key(f);
+            above = kk > k_hi;
+            in = (kk >> 21) == d0;
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const bool valid = p0 + (g0 + u * kSaWarps) * 32 + lane < p1;  // also false past nw
-            bool above, in;
-            if constexpr (FCMP) {
-                above = f[u] > f_hi;
-                in = f[u] >= f_lo && f[u] <= f_hi;
-            } else {
-                const uint32_t kk = float_key(f[u]);
-                above = kk > k_hi;
-                in = (kk >> 21) == d0;
+    };
+    if constexpr (STAGED) {
+        const int np = p1 - p0;
+        for (int wb = warp * 32; wb < nw; wb += kSaThreads) {  // warp-uniform bounds (shuffles below)
+            const int w = wb + lane;
+            const uint32_t* row = keys_s + w * 32;
+            uint32_t sb = 0u, cb = 0u;
+            if (w < nw) {
+                const int nv = min(32, np - w * 32);  // entries of the word
+#pragma unroll 8
+                for (int j = 0; j < 32; ++j) {
+                    const int e = (j + lane) & 31;
+                    bool above, in;
+                    classify(__uint_as_float(row[e]), above, in);
+                    sb |= (uint32_t)(e < nv && above) << e;
+                    cb |= (uint32_t)(e < nv && in) << e;
+                }
+                sel[w] = sb;
+                tie[w] = 0u;
             }
-            sure[u] = __ballot_sync(0xffffffffu, valid && above);
-            cm[u] = __ballot_sync(0xffffffffu, valid && in);
-        }
-        uint32_t my_s = 0, my_c = 0;  // lane u keeps group u's words
+            const uint32_t na = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(sb));
+            if (lane == 0 && na != 0u) atomicAdd(nabove, na);
+            const uint32_t c = (uint32_t)__popc(cb);
+            uint32_t incl = c;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            my_s = lane == u ? sure[u] : my_s;
-            my_c = lane == u ? cm[u] : my_c;
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            uint32_t at = 0u;
+            if (lane == 31 && incl != 0u) at = atomicAdd(ncand, incl);
+            at = __shfl_sync(0xffffffffu, at, 31) + incl - c;
+            while (cb != 0u) {
+                const int e = __ffs(cb) - 1;
+                cb &= cb - 1u;
+                const uint32_t key = float_key(__uint_as_float(row[e]));
+                atomicAdd(&hist1[(key >> 10) & (kSaHist - 1)], 1u);
+                if (at < (uint32_t)kSaCand) {
+                    cand_k[at] = key;
+                    cand_i[at] = (uint32_t)(w * 32 + e);
+                }
+                ++at;
+            }
         }
-        const int gw = g0 + lane * kSaWarps;
-        if (lane < U && gw < nw) {
-            sel[gw] = my_s;
-            tie[gw] = my_c;
+    } else {
+        constexpr int U = 8;
+        const uint32_t lt = lanemask_lt();
+        for (int g0 = warp; g0 < nw; g0 += U * kSaWarps) {
+            float f[U];
+            uint32_t sure[U], cm[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = p0 + (g0 + u * kSaWarps) * 32 + lane;
+                f[u] = i < p1 ? __ldcg(srow + i) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const bool valid = p0 + (g0 + u * kSaWarps) * 32 + lane < p1;  // also false past nw
+                bool above, in;
+                classify(f[u], above, in);
+                sure[u] = __ballot_sync(0xffffffffu, valid && above);
+                cm[u] = __ballot_sync(0xffffffffu, valid && in);
+            }
+            uint32_t my_s = 0, nc = 0, na = 0;  // lane u keeps group u's word
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                my_s = lane == u ? sure[u] : my_s;
+                nc += __popc(cm[u]);
+                na += __popc(sure[u]);
+            }
+            if (lane == 0 && na != 0u) atomicAdd(nabove, na);
+            const int gw = g0 + lane * kSaWarps;
+            if (lane < U && gw < nw) {
+                sel[gw] = my_s;
+                tie[gw] = 0u;
+            }
+            if (nc != 0u) {
+                uint32_t at = 0u;
+                if (lane == 0) at = atomicAdd(ncand, nc);
+                at = __shfl_sync(0xffffffffu, at, 0);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if ((cm[u] >> lane) & 1u) {
+                        const uint32_t key = float_key(f[u]);
+                        const uint32_t slot = at + __popc(cm[u] & lt);
+                        atomicAdd(&hist1[(key >> 10) & (kSaHist - 1)], 1u);
+                        if (slot < (uint32_t)kSaCand) {
+                            cand_k[slot] = key;
+                            cand_i[slot] = (uint32_t)((g0 + u * kSaWarps) * 32 + lane);
+                        }
+                    }
+                    at += __popc(cm[u]);
+                }
+            }
         }
     }
 }
@@ -444,7 +539,10 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
         mbar_init(&ms->bar, 1);
         fence_mbarrier_init();
     }
-    if (tid == 0) ms->ncand = 0;
+    if (tid == 0) {
+        ms->ncand = 0;
+        ms->nabove = 0;
+    }
     for (int i = tid; i < 2 * kSaHist + kSaHist / 2; i += kSaThreads) hist0[i] = 0u;  // hist0, hist1, hist2
     cl.sync();  // B0
 
@@ -472,14 +570,13 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
         }
     }
     cp_async_commit();
-    if (hrow != nullptr && !trivial)
-        for (int i = tid; i < kSaHist / 4; i += kSaThreads)
-            reinterpret_cast<uint4*>(hist0)[i] = __ldcg(reinterpret_cast<const uint4*>(hrow) + i);
-    // the top digit first when the indexer's histogram is given: it overlaps the staging
+    // the top digit first when the indexer's histogram is given (read straight into
+    // registers): it overlaps the staging
     uint32_t d0 = 0, above0 = 0;
     if (!trivial && hrow != nullptr) {
-        __syncthreads();
-        cta_select_digit(hist0, kSaHist, (uint32_t)k, ms, d0, above0);
+        const uint4* h4 = reinterpret_cast<const uint4*>(hrow) + 4 * (kSaThreads - 1 - tid);
+        const uint4 hv[4] = {__ldcg(h4), __ldcg(h4 + 1), __ldcg(h4 + 2), __ldcg(h4 + 3)};
+        cta_select_digit_regs<16>(hv, (uint32_t)k, ms, d0, above0);
         d0 &= kSaHist - 1;
     }
     if (staged) {
@@ -511,9 +608,9 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
     uint32_t krem = (uint32_t)k - above0;
     const uint32_t krem0 = krem;  // still needed from the d0 bin (the fallback restarts there)
 
-    // ---- one pass over the part: bitmaps of the entries above d0's bin (sel) and in it (the
-    // candidates, in tie for now), written by lanes 0..U-1 without divergence; then the
-    // candidates are listed with one scan and their next digit is added to every CTA's hist1
+    // ---- one pass over the part: the bitmap of the entries above d0's bin (sel), written by
+    // lanes 0..U-1 without divergence, and the list of the entries in it (the candidates) with
+    // their next digit counted into hist1; then hist1's coarse sums go to every CTA
     if (!trivial) {
         // the d0 bin as the closed float interval [f_lo, f_hi]: a score lies above the bin iff
         // f > f_hi and in it iff f_lo <= f <= f_hi (-0 and +0 compare equal, as their order
@@ -522,64 +619,28 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
         const bool fcmp = d0 > 0x003u && d0 < 0x7FCu;
         const float f_lo = key_float(k_lo), f_hi = key_float(k_hi);
         if (staged) {
-            if (fcmp) sa_scan<true, true>(keys_s, srow, p0, p1, nw, d0, f_lo, f_hi, k_hi, sel, tie);
-            else sa_scan<true, false>(keys_s, srow, p0, p1, nw, d0, f_lo, f_hi, k_hi, sel, tie);
+            if (fcmp) sa_scan<true, true>(keys_s, srow, p0, p1, nw, d0, f_lo, f_hi, k_hi, sel, tie, cand_k, cand_i, hist1, &ms->ncand, &ms->nabove);
+            else sa_scan<true, false>(keys_s, srow, p0, p1, nw, d0, f_lo, f_hi, k_hi, sel, tie, cand_k, cand_i, hist1, &ms->ncand, &ms->nabove);
         } else {
-            if (fcmp) sa_scan<false, true>(keys_s, srow, p0, p1, nw, d0, f_lo, f_hi, k_hi, sel, tie);
-            else sa_scan<false, false>(keys_s, srow, p0, p1, nw, d0, f_lo, f_hi, k_hi, sel, tie);
+            if (fcmp) sa_scan<false, true>(keys_s, srow, p0, p1, nw, d0, f_lo, f_hi, k_hi, sel, tie, cand_k, cand_i, hist1, &ms->ncand, &ms->nabove);
+            else sa_scan<false, false>(keys_s, srow, p0, p1, nw, d0, f_lo, f_hi, k_hi, sel, tie, cand_k, cand_i, hist1, &ms->ncand, &ms->nabove);
         }
         __syncthreads();
-        // list the candidates: thread t owns words [t*W, t*W + W)
-        const int W = (nw + kSaThreads - 1) / kSaThreads;
-        const int w0 = tid * W, w1 = min(nw, w0 + W);
-        uint32_t cnt = 0, n_cand;
-        for (int w = w0; w < w1; ++w) cnt += __popc(tie[w]);
-        uint32_t slot = cta_exclusive_scan(cnt, ms, n_cand);
-        for (int w = w0; w < w1; ++w) {
-            uint32_t bits = tie[w];
-            tie[w] = 0u;  // the tie bitmap proper starts empty
-            while (bits != 0u) {
-                const int li = w * 32 + __ffs(bits) - 1;
-                bits &= bits - 1u;
-                if (slot < (uint32_t)kSaCand) {
-                    cand_k[slot] = float_key(staged ? __uint_as_float(keys_s[li]) : __ldcg(srow + p0 + li));
-                    cand_i[slot] = (uint32_t)li;
-                }
-                ++slot;
-            }
-        }
-        if (tid == 0) ms->ncand = n_cand;
-        __syncthreads();
-        // the next digit of the candidates into this CTA's hist1
-        if (n_cand <= (uint32_t)kSaCand) {
-            for (uint32_t c = tid; c < n_cand; c += kSaThreads) atomicAdd(&hist1[(cand_k[c] >> 10) & (kSaHist - 1)], 1u);
-        } else {
-            // more candidates than the list holds: count their next digit over the keys
-            for (int base0 = p0 + warp * 32; base0 < p1; base0 += kSaThreads) {
-                const int i = base0 + lane;
-                const bool valid = i < p1;
-                const uint32_t kk = valid ? key_at(i) : 0u;
-                const bool in = valid && (kk >> 21) == d0;
-                const uint32_t bin = (kk >> 10) & (kSaHist - 1);
-                const uint32_t peers = __match_any_sync(0xffffffffu, in ? bin : 0xffffffffu);
-                if (in && lane == __ffs(peers) - 1) atomicAdd(&hist1[bin], (uint32_t)__popc(peers));
-            }
-            if (tid == 0)
-                for (int c = 0; c < P; ++c) atomicOr(cl.map_shared_rank(&ms->ovf, c), 1u);
-        }
-        // 64 coarse sums of 32 bins each, pushed to every CTA (the fine bins stay here)
-        __syncthreads();
-        for (int g = tid; g < kSaCoarse; g += kSaThreads) {
-            uint32_t sum = 0;
-#pragma unroll 8
-            for (int j = 0; j < kSaHist / kSaCoarse; ++j) sum += hist1[g * (kSaHist / kSaCoarse) + j];
-            for (int c = 0; c < P; ++c) cl.map_shared_rank(coarse, c)[rank * kSaCoarse + g] = sum;
+        if (tid == 0 && ms->ncand > (uint32_t)kSaCand)  // the list overflowed: every CTA resolves from global
+            for (int c = 0; c < P; ++c) atomicOr(cl.map_shared_rank(&ms->ovf, c), 1u);
+        // 64 coarse sums of 32 bins each (a warp reads one group, a lane one bin), pushed to
+        // every CTA (the fine bins stay here)
+        static_assert(kSaHist / kSaCoarse == 32, "a coarse group is one warp's bins");
+#pragma unroll 4
+        for (int g = warp; g < kSaCoarse; g += kSaWarps) {
+            const uint32_t sum = __reduce_add_sync(0xffffffffu, hist1[g * 32 + lane]);
+            if (lane < P) cl.map_shared_rank(coarse, lane)[rank * kSaCoarse + g] = sum;
         }
     }
     cl.sync();  // B1: coarse sums and ovf pushed, every hist1 complete; every CTA has read key_hist
     if (hrow != nullptr && rank == 0)
         for (int i = tid; i < kSaHist / 4; i += kSaThreads) reinterpret_cast<uint4*>(hrow)[i] = make_uint4(0u, 0u, 0u, 0u);
-    // candidate c of the per-warp lists, or false past a warp's count
+    // the listed candidates: the first kSaCand of the part's
     const uint32_t n_cand = min(ms->ncand, (uint32_t)kSaCand);
     uint32_t* fbk = hist0;             // final-bin keys pushed by the cluster (hist0 is done with)
     uint32_t* fbp = hist0 + kSaFb;     // and their positions in the row
@@ -632,20 +693,24 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
         const uint32_t d1 = ms->sel_digit & (kSaHist - 1), ab1 = ms->sel_above;
         krem -= ab1;
         pre21 = (d0 << 11) | d1;
-        for (uint32_t c = tid; c < n_cand; c += kSaThreads) {
-            const uint32_t ck = cand_k[c], ci = cand_i[c], dg = (ck >> 10) & (kSaHist - 1);
-            if (dg > d1) {
-                atomicOr(&sel[ci >> 5], 1u << (ci & 31));
-            } else if (dg == d1) {
-                const uint32_t q = atomicAdd(&ms->nfb, 1u);
-                if (q < (uint32_t)kSaList) lst[q] = c;
+        for (uint32_t cb = (uint32_t)(tid - lane); cb < n_cand; cb += kSaThreads) {  // warp-uniform bounds
+            const uint32_t c = cb + (uint32_t)lane;
+            bool up = false;
+            if (c < n_cand) {
+                const uint32_t ck = cand_k[c], ci = cand_i[c], dg = (ck >> 10) & (kSaHist - 1);
+                if (dg > d1) {
+                    atomicOr(&sel[ci >> 5], 1u << (ci & 31));
+                    up = true;
+                } else if (dg == d1) {
+                    const uint32_t q = atomicAdd(&ms->nfb, 1u);
+                    if (q < (uint32_t)kSaList) lst[q] = c;
+                }
             }
+            const uint32_t nu = (uint32_t)__popc(__ballot_sync(0xffffffffu, up));
+            if (lane == 0 && nu != 0u) atomicAdd(&ms->nabove, nu);
         }
         __syncthreads();
-        uint32_t cnt = 0;
-        for (int w = tid; w < nw; w += kSaThreads) cnt += __popc(sel[w]);
-        uint32_t total;
-        cta_exclusive_scan(cnt, ms, total);
+        const uint32_t total = ms->nabove;  // this part's entries above the final bin
         const uint32_t nfb = min(ms->nfb, (uint32_t)kSaList);
         if (tid < P) {
             SaMisc* rm = cl.map_shared_rank(ms, tid);
@@ -671,21 +736,47 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
 
     uint32_t thr = 0, base = 0, take = 0, my_gt = 0, my_eq = 0;
     if (!trivial && !fallback) {
-        // ---- digit 2 (bits 9..0) among the final-bin entries: the threshold key
+        // ---- the threshold key: the krem-th largest among the final-bin entries
         const uint32_t n_fb = ms->fb_n;
-        for (int i = tid; i < kSaHist / 2; i += kSaThreads) hist2[i] = 0u;
         if (tid < kSaMaxCluster) {
             ms->cgt[tid] = tid < P ? ms->dsure[tid] : 0u;
             ms->ceq[tid] = 0u;
         }
-        __syncthreads();
-        for (uint32_t e = tid; e < n_fb; e += kSaThreads) atomicAdd(&hist2[fbk[e] & 1023u], 1u);
-        __syncthreads();
-        uint32_t d2, ab2;
-        cta_select_digit(hist2, kSaHist / 2, krem, ms, d2, ab2);
-        d2 &= 1023u;
-        krem -= ab2;
-        thr = (pre21 << 10) | d2;
+        if (n_fb <= 32u) {
+            // few entries (the usual case): one warp ranks them by key, then position (all
+            // distinct); the entry ranked krem - 1 holds the threshold key
+            if (warp == 0) {
+                const bool have = (uint32_t)lane < n_fb;
+                const uint32_t ky = have ? fbk[lane] : 0u, ps = have ? fbp[lane] : 0xffffffffu;
+                uint32_t rk = 0u;
+                for (uint32_t j = 0; j < n_fb; ++j) {
+                    const uint32_t kj = __shfl_sync(0xffffffffu, ky, (int)j);
+                    const uint32_t pj = __shfl_sync(0xffffffffu, ps, (int)j);
+                    rk += (kj > ky || (kj == ky && pj < ps)) ? 1u : 0u;
+                }
+                const uint32_t hit = __ballot_sync(0xffffffffu, have && rk + 1u == krem);
+                const uint32_t tk = __shfl_sync(0xffffffffu, ky, hit != 0u ? __ffs(hit) - 1 : 0);
+                const uint32_t ngt = (uint32_t)__popc(__ballot_sync(0xffffffffu, have && ky > tk));
+                if (lane == 0) {
+                    ms->sel_digit = tk;
+                    ms->sel_above = ngt;
+                }
+            }
+            __syncthreads();
+            thr = ms->sel_digit;
+            krem -= ms->sel_above;
+        } else {
+            // digit 2 (bits 9..0) of the final-bin entries
+            for (int i = tid; i < kSaHist / 2; i += kSaThreads) hist2[i] = 0u;
+            __syncthreads();
+            for (uint32_t e = tid; e < n_fb; e += kSaThreads) atomicAdd(&hist2[fbk[e] & 1023u], 1u);
+            __syncthreads();
+            uint32_t d2, ab2;
+            cta_select_digit(hist2, kSaHist / 2, krem, ms, d2, ab2);
+            d2 &= 1023u;
+            krem -= ab2;
+            thr = (pre21 << 10) | d2;
+        }
         // ---- every part's counts above / equal to the threshold, from the final bin
         for (uint32_t e = tid; e < n_fb; e += kSaThreads) {
             const uint32_t key = fbk[e], r = min(fbp[e] / (uint32_t)p.part, (uint32_t)(P - 1));
