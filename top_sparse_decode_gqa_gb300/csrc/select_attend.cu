@@ -181,15 +181,41 @@ SD_DEVINL uint32_t warp_inclusive_scan(uint32_t v) {
     return v;
 }
 
-// Block-wide exclusive prefix sum; also returns the total.
-SD_DEVNOINL uint32_t cta_exclusive_scan(uint32_t v, SaMisc* ms, uint32_t& total) {
-    const uint32_t incl = cta_inclusive_scan(v, ms->wsum);
-    if ((int)threadIdx.x == kSaThreads - 1) ms->tot = incl;
+// Block-wide exclusive prefix sums of two values per thread at once (the total of each
+// comes from the warp sums): two barriers.
+SD_DEVNOINL void cta_exclusive_scan2(uint32_t a, uint32_t b, SaMisc* ms, uint32_t& ea, uint32_t& eb, uint32_t& ta,
+                                     uint32_t& tb) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t ia = a, ib = b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t na = __shfl_up_sync(0xffffffffu, ia, o), nb = __shfl_up_sync(0xffffffffu, ib, o);
+        if (lane >= o) {
+            ia += na;
+            ib += nb;
+        }
+    }
+    if (lane == 31) {
+        ms->wsum[warp] = ia;
+        ms->wgt[warp] = ib;
+    }
     __syncthreads();
-    total = ms->tot;
-    __syncthreads();
-    return incl - v;
+    uint32_t oa = 0, ob = 0, sa = 0, sb = 0;
+#pragma unroll
+    for (int w = 0; w < kSaWarps; ++w) {
+        const uint32_t xa = ms->wsum[w], xb = ms->wgt[w];
+        oa += w < warp ? xa : 0u;
+        ob += w < warp ? xb : 0u;
+        sa += xa;
+        sb += xb;
+    }
+    __syncthreads();  // the warp sums are rewritten by the next scan
+    ea = ia - a + oa;
+    eb = ib - b + ob;
+    ta = sa;
+    tb = sb;
 }
+
 
 // Given the histogram of one digit (128 * PER bins, higher bins = larger keys) of the
 // entries still in the running, the digit holding the krem-th largest and how many entries
@@ -279,10 +305,11 @@ SD_DEVINL float key_float(uint32_t k) {
 // d0 bin, tie word w cleared.  The entries in the bin (the candidates) are listed with their
 // order keys and positions in the part (in no particular order; only the first kSaCand are
 // kept) and their next digit (bits 20..10) is counted into hist1; *ncand ends as the part's
-// candidate count and *nabove the part's entries above the bin.  Staged scores: each lane builds the bits of its own word in registers,
-// reading entry (j + lane) mod 32 at step j so the warp's reads fall in 32 distinct banks;
-// the listing takes one warp prefix sum and one atomic per warp.  Scores read from global
-// memory: each warp votes on 32-score groups (coalesced), U groups per round.
+// candidate count and *nabove as its entries above the bin.  Staged scores: each lane builds
+// the bits of two words in registers, reading entry (j + lane) mod 32 of each at step j so
+// the warp's reads fall in 32 distinct banks; the listing takes one warp prefix sum and one
+// atomic per warp.  Scores read from global memory: each warp votes on 32-score groups
+// (coalesced), U groups per round.
 template <bool STAGED, bool FCMP>
 SD_DEVNOINL void sa_scan(const uint32_t* keys_s, const float* srow, int p0, int p1, int nw, uint32_t d0, float f_lo,
                        float f_hi, uint32_t k_hi, uint32_t* sel, uint32_t* tie, uint32_t* cand_k, uint32_t* cand_i,
@@ -300,26 +327,49 @@ SD_DEVNOINL void sa_scan(const uint32_t* keys_s, const float* srow, int p0, int 
     };
     if constexpr (STAGED) {
         const int np = p1 - p0;
-        for (int wb = warp * 32; wb < nw; wb += kSaThreads) {  // warp-uniform bounds (shuffles below)
-            const int w = wb + lane;
-            const uint32_t* row = keys_s + w * 32;
-            uint32_t sb = 0u, cb = 0u;
-            if (w < nw) {
-                const int nv = min(32, np - w * 32);  // entries of the word
+        // lane words wa = wb + lane and wb + kSaThreads + lane (warp-uniform bounds: shuffles below)
+        for (int wb = warp * 32; wb < nw; wb += 2 * kSaThreads) {
+            const int wa = wb + lane, wz = wa + kSaThreads;
+            const int na = wa < nw ? min(32, np - wa * 32) : 0, nz = wz < nw ? min(32, np - wz * 32) : 0;
+            const uint32_t* ra = keys_s + (na > 0 ? wa : 0) * 32;
+            const uint32_t* rz = keys_s + (nz > 0 ? wz : 0) * 32;
+            // above the bin (s) and at or above its low end (g); in the bin = g and not s
+            uint32_t sa = 0u, ga = 0u, sz = 0u, gz = 0u;
+            uint32_t bit = 1u << lane;  // the bit of entry (j + lane) mod 32 at step j
 #pragma unroll 8
-                for (int j = 0; j < 32; ++j) {
-                    const int e = (j + lane) & 31;
-                    bool above, in;
-                    classify(__uint_as_float(row[e]), above, in);
-                    sb |= (uint32_t)(e < nv && above) << e;
-                    cb |= (uint32_t)(e < nv && in) << e;
+            for (int j = 0; j < 32; ++j) {
+                const int e = (j + lane) & 31;
+                const float fa = __uint_as_float(ra[e]), fz = __uint_as_float(rz[e]);
+                if constexpr (FCMP) {
+                    sa |= fa > f_hi ? bit : 0u;
+                    ga |= fa >= f_lo ? bit : 0u;
+                    sz |= fz > f_hi ? bit : 0u;
+                    gz |= fz >= f_lo ? bit : 0u;
+                } else {
+                    const uint32_t ka = float_key(fa), kz = float_key(fz);
+                    sa |= ka > k_hi ? bit : 0u;
+                    ga |= (ka >> 21) >= d0 ? bit : 0u;
+                    sz |= kz > k_hi ? bit : 0u;
+                    gz |= (kz >> 21) >= d0 ? bit : 0u;
                 }
-                sel[w] = sb;
-                tie[w] = 0u;
+                bit = __funnelshift_l(bit, bit, 1);
             }
-            const uint32_t na = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(sb));
-            if (lane == 0 && na != 0u) atomicAdd(nabove, na);
-            const uint32_t c = (uint32_t)__popc(cb);
+            const uint32_t ma = na >= 32 ? 0xffffffffu : (1u << na) - 1u;
+            const uint32_t mz = nz >= 32 ? 0xffffffffu : (1u << nz) - 1u;
+            sa &= ma;
+            sz &= mz;
+            uint32_t ca = ga & ~sa & ma, cz = gz & ~sz & mz;
+            if (na > 0) {
+                sel[wa] = sa;
+                tie[wa] = 0u;
+            }
+            if (nz > 0) {
+                sel[wz] = sz;
+                tie[wz] = 0u;
+            }
+            const uint32_t nab = __reduce_add_sync(0xffffffffu, (uint32_t)(__popc(sa) + __popc(sz)));
+            if (lane == 0 && nab != 0u) atomicAdd(nabove, nab);
+            const uint32_t c = (uint32_t)(__popc(ca) + __popc(cz));
             uint32_t incl = c;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -329,16 +379,22 @@ SD_DEVNOINL void sa_scan(const uint32_t* keys_s, const float* srow, int p0, int 
             uint32_t at = 0u;
             if (lane == 31 && incl != 0u) at = atomicAdd(ncand, incl);
             at = __shfl_sync(0xffffffffu, at, 31) + incl - c;
-            while (cb != 0u) {
-                const int e = __ffs(cb) - 1;
-                cb &= cb - 1u;
-                const uint32_t key = float_key(__uint_as_float(row[e]));
-                atomicAdd(&hist1[(key >> 10) & (kSaHist - 1)], 1u);
-                if (at < (uint32_t)kSaCand) {
-                    cand_k[at] = key;
-                    cand_i[at] = (uint32_t)(w * 32 + e);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t cb = h == 0 ? ca : cz;
+                const uint32_t* row = h == 0 ? ra : rz;
+                const int w = h == 0 ? wa : wz;
+                while (cb != 0u) {
+                    const int e = __ffs(cb) - 1;
+                    cb &= cb - 1u;
+                    const uint32_t key = float_key(__uint_as_float(row[e]));
+                    atomicAdd(&hist1[(key >> 10) & (kSaHist - 1)], 1u);
+                    if (at < (uint32_t)kSaCand) {
+                        cand_k[at] = key;
+                        cand_i[at] = (uint32_t)(w * 32 + e);
+                    }
+                    ++at;
                 }
-                ++at;
             }
         }
     } else {
@@ -839,9 +895,8 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
             cs += __popc(sel[w]);
             ct += __popc(tie[w]);
         }
-        uint32_t tot_s, tot_t;
-        const uint32_t sel_before = cta_exclusive_scan(cs, ms, tot_s);
-        const uint32_t tie_before = cta_exclusive_scan(ct, ms, tot_t);
+        uint32_t tot_s, tot_t, sel_before, tie_before;
+        cta_exclusive_scan2(cs, ct, ms, sel_before, tie_before, tot_s, tot_t);
         uint32_t ties_left = take > tie_before ? take - tie_before : 0u;
         uint32_t at = sel_before + min(tie_before, take);
         for (int w = w0; w < w1; ++w) {
