@@ -1285,6 +1285,26 @@ def path_description(step, w) -> str:
     return "dense attention + score accumulate per layer"
 
 
+def capture_graph(step):
+    """One step's C-ABI calls captured into a CUDA graph (its launches and the events that
+    order its streams), for steps whose time is mostly launches; None (with the reason on
+    stderr) when the capture fails, and the steps then run eagerly."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    try:
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            step.run()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+    except RuntimeError as e:
+        print(f"bench: CUDA graph capture failed, steps run eagerly: {e}", file=sys.stderr)
+        torch.cuda.synchronize()
+        return None
+    return g
+
+
 def rotation_count(step, l2_bytes) -> int:
     """Input sets a back-to-back run rotates through: enough that at least three times L2 of
     other steps' traffic passes between two uses of one set (at least two sets)."""
@@ -1434,6 +1454,9 @@ def run_ours(args):
             for c in calls:
                 c()
         torch.cuda.synchronize()
+    graph = capture_graph(step) if args.graph and rot is None else None
+    if graph is not None and int(step.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(step.err.item())} after the graph's first replay")
     marks = [StepMarks(0) for _ in range(K)]
     kmarks = [StepMarks(step.dominant_per_step, step.phases) for _ in range(K2)]
     clocks = ClockSampler(local)
@@ -1447,7 +1470,12 @@ def run_ours(args):
     else:
         for i in range(K):
             clean_l2()
-            step.run(marks[i])
+            if graph is not None:
+                marks[i].start.record()
+                graph.replay()
+                marks[i].end.record()
+            else:
+                step.run(marks[i])
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -1505,6 +1533,8 @@ def run_ours(args):
                    "queries_per_step": w.queries_per_step,
                    "path": path_description(step, w),
                    "l2": l2_note,
+                   "launch": ("each timed step one replay of a CUDA graph of the step's C-ABI calls (the per-kernel "
+                              "pass runs them eagerly)" if graph is not None else "C-ABI calls from Python"),
                    "parallelism": f"replica x{world} (each rank its own batch)"},
         "roofline": {"bound": "hbm", "kernel": step.dominant, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -1901,6 +1931,8 @@ def main(argv=None):
                     help="sparse decode workloads: one persistent launch (step), indexer + fused select/attend, "
                          "or three launches; auto takes indexer + fused select/attend for token-level bf16 "
                          "selection and three launches otherwise")
+    ap.add_argument("--graph", action="store_true",
+                    help="time each flushed step as one replay of a CUDA graph of its calls")
     ap.add_argument("--no-lookahead", action="store_true",
                     help="lookahead and cached tiered workloads: run every call in order on one stream "
                          "(no selection of the next layer, or promotion of the previous step, beside others)")
