@@ -347,12 +347,12 @@ SD_DEVINL void mma_attend_warp(WarpAcc<D, RP>& acc, uint8_t* stages, uint32_t q_
 
 // Combines the NW warps' (m, l, O) of a CTA; called by all NW*32 threads after every
 // warp's loop.  Scratch: mlw [2*NW*RP] floats, rowv [(2+NW)*RP] floats, ow [NW][RP][D]
-// floats (the warps' stage area may be reused: the call starts with a barrier).  Leaves
-// rowM = rowv[0, RP) (the CTA's row maxima), rowL = rowv[RP, 2RP) (sums of l rescaled to
-// them) and ow[w][r] = warp w's O row r rescaled to rowM[r]; the CTA's unnormalised O row is
-// the sum over w.
+// floats (the warps' stage area may be reused: the call starts with a barrier).  Leaves, for
+// the nq real query rows r < nq (the padding rows are not combined), rowM = rowv[0, RP) (the
+// CTA's row maxima), rowL = rowv[RP, 2RP) (sums of l rescaled to them) and ow[w][r] = warp
+// w's O row r rescaled to rowM[r]; the CTA's unnormalised O row is the sum over w.
 template <int D, int RP, int NW = kMmaWarps>
-SD_DEVINL void mma_combine_warps(const WarpAcc<D, RP>& acc, float* mlw, float* rowv, float* ow) {
+SD_DEVINL void mma_combine_warps(const WarpAcc<D, RP>& acc, float* mlw, float* rowv, float* ow, int nq) {
     constexpr int MT = RP / 16, NT = D / 8;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t4 = lane & 3;
@@ -370,7 +370,7 @@ SD_DEVINL void mma_combine_warps(const WarpAcc<D, RP>& acc, float* mlw, float* r
     float* rowM = rowv;
     float* rowL = rowv + RP;
     float* fac = rowv + 2 * RP;  // [NW][RP]
-    if (tid < RP) {
+    if (tid < RP && tid < nq) {
         const int r = tid;
         float M = mlw[r];
 #pragma unroll
@@ -392,6 +392,7 @@ SD_DEVINL void mma_combine_warps(const WarpAcc<D, RP>& acc, float* mlw, float* r
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             const int r = mt * 16 + g + 8 * hf;
+            if (r >= nq) continue;
             const float f = fac[warp * RP + r];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {

@@ -611,7 +611,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_mma_kernel(const AttendPar
     }
 
     float* ow = reinterpret_cast<float*>(sm + L::oStage);  // [4][RP][D]
-    mma_combine_warps<D, RP>(acc, mlw, rowv, ow);
+    mma_combine_warps<D, RP>(acc, mlw, rowv, ow, p.R);
     const float* rowM = rowv;
     const float* rowL = rowv + RP;
     for (int e = tid; e < p.R * (D / 4); e += kAttThreads) {

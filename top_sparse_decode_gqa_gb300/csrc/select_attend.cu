@@ -977,7 +977,7 @@ __global__ void __launch_bounds__(kSaThreads) select_attend_kernel(const SelAttP
     float* mlw = reinterpret_cast<float*>(sm + L.oML);
     float* rowv = reinterpret_cast<float*>(sm + L.oRow);
     float* ow = reinterpret_cast<float*>(sm + L.oU);
-    mma_combine_warps<D, RP>(acc, mlw, rowv, ow);
+    mma_combine_warps<D, RP>(acc, mlw, rowv, ow, p.R);
     const int R = p.R;
     const int own = (R + P - 1) / P;  // query rows per owner
     // the inbox either has its own memory, or reuses H once every CTA is past its selection
