@@ -127,13 +127,14 @@ def test_tiers_with_pool_and_host_rows():
 
 
 def test_tiers_without_t2_or_t3_give_the_untiered_bits():
-    # every position in T0 or T1: the tiered call reads the same rows at the same values
+    # every position in T0 or T1: the tiered call reads the same rows at the same values, so
+    # it gives the bits of the untiered call through the same row loop
     q, K, Vv, _, kc, ks, vc, vs = make(3, T=2500)
     B, T = K.shape[0], K.shape[2]
     tier = np.zeros((B, T), dtype=np.uint8)
     tier[:, 1::2] = 1
     qd, Kd, Vd = q.cuda(), K.cuda(), Vv.cuda()
-    a0, out0, lse0, _ = sd().make_attend_args(qd, Kd, Vd, None, T=T)
+    a0, out0, lse0, _ = sd().make_attend_args(qd, Kd, Vd, None, T=T, row_loop=True)
     run(a0)
     tk = tier_kwargs(tier, kc, ks, vc, vs)
     a1, out1, lse1, _ = sd().make_attend_args(qd, Kd, Vd, None, T=T, **tk)

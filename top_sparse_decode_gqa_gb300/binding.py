@@ -54,7 +54,7 @@ class sd_attend_args(ctypes.Structure):
         ("ring_k", ctypes.c_void_p), ("ring_v", ctypes.c_void_p), ("ring_pos", ctypes.c_void_p),
         ("qpos", ctypes.c_void_p), ("ring_w", ctypes.c_int), ("slot_per_head", ctypes.c_int),
         ("tier", ctypes.c_void_p), ("k_int8", ctypes.c_void_p), ("v_int8", ctypes.c_void_p),
-        ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p), ("row_loop", ctypes.c_int),
     ]
 
 
@@ -248,10 +248,11 @@ def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=No
                      k_host=None, v_host=None, slot_map=None, out=None, lse=None, logits=None,
                      want_logits=False, err_word=None, splits=0, per_head=False, k_stage=None,
                      v_stage=None, ring_k=None, ring_v=None, ring_pos=None, qpos=None, tier=None,
-                     k_int8=None, v_int8=None, k_scale=None, v_scale=None) -> tuple:
+                     k_int8=None, v_int8=None, k_scale=None, v_scale=None, row_loop=False) -> tuple:
     """Fill an sd_attend_args from tensors; returns (args, out, lse, logits).  slot_map is
     [B,T] (residency per sequence) or [B,Hkv,T] (per KV head).  tier [B,T] uint8 with
-    k_int8/v_int8 [B,Hkv,T,d] int8 and k_scale/v_scale [B,Hkv,T] fp32: the tiered rows."""
+    k_int8/v_int8 [B,Hkv,T,d] int8 and k_scale/v_scale [B,Hkv,T] fp32: the tiered rows.
+    row_loop: a dense call runs the general row loop (the one tiered calls take)."""
     _dev(q, "q")
     B, V, Hq, d = q.shape
     Hkv = k_cache.shape[1]
@@ -299,6 +300,7 @@ def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=No
             setattr(a, name, t.data_ptr())
     a.ring_w = ring_w
     a.slot_per_head = 1 if slot_map is not None and slot_map.dim() == 3 else 0
+    a.row_loop = 1 if row_loop else 0
     return a, out, lse, logits
 
 

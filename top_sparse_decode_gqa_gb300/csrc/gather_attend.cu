@@ -683,7 +683,10 @@ SplitPlan plan_splits(const sd_attend_args* a) {
     if (a->splits > 0) {
         splits = a->splits;
     } else {
-        const long slots = (long)num_sms() * att_ctas_per_sm(layout_bytes(a->dtype, a->d, sp.RP));
+        // one wave of the kernel that will run (the dense tiled path has its own occupancy)
+        const int per_sm = dense_tma_eligible(a) ? dense_tma_ctas_per_sm(a)
+                                                 : att_ctas_per_sm(layout_bytes(a->dtype, a->d, sp.RP));
+        const long slots = (long)num_sms() * per_sm;
         splits = bk > 0 ? slots / bk : 1;
     }
     splits = std::max(1L, std::min(splits, std::max(1L, chunks)));
@@ -890,7 +893,18 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
     // tiers alone (dense over the cache) need no resolving: a row's code follows from its tier
     p.resolve = (a->idx != nullptr || a->slot_map != nullptr || a->ring_w > 0) ? 1 : 0;
     cudaStream_t st = as_stream(stream);
-    const sd_status s1 = a->d == 128 ? dispatch_rp<128>(p, a->dtype, sp.RP, st) : dispatch_rp<64>(p, a->dtype, sp.RP, st);
+    SD_REQUIRE(a->row_loop == 0 || a->row_loop == 1, "sd_gather_attend: row_loop must be 0 or 1");
+    sd_status s1;
+    if (dense_tma_eligible(a)) {
+        // whole 64-row tiles of a dense cache in HBM; its split count, at most the plan's,
+        // is the merge's
+        int used = 1;
+        s1 = dense_tma_launch(a, sp.splits, sp.RP, p.ws_o, p.ws_m, p.ws_l, &used, st);
+        p.splits = used;
+        sp.splits = used;
+    } else {
+        s1 = a->d == 128 ? dispatch_rp<128>(p, a->dtype, sp.RP, st) : dispatch_rp<64>(p, a->dtype, sp.RP, st);
+    }
     if (s1 != SD_OK || sp.splits == 1) return s1;
     // the splits' partials merged by (group, query row), all in parallel
     const dim3 mgrid((unsigned)((long)a->B * p.Hkv), (unsigned)p.R);

@@ -261,12 +261,18 @@ SD_DEVINL void att_init_t(AttAccT<NQ>& acc) {
     }
 }
 
+// A logit sink that keeps nothing.
+struct NoLogits {
+    SD_DEVINL void operator()(int, int, float) const {}
+};
+
 // 32 K rows at kb and the 32 V rows at vb (swizzled 32-row tiles) for the query rows of
-// qf, one warp; keys whose bit is clear in `valid` take no part.
-template <int NQ>
+// qf, one warp; keys whose bit is clear in `valid` take no part.  logit(query row, key,
+// scaled logit in base 2) receives every valid key's logit of every query row of the tile.
+template <int NQ, class Logit = NoLogits>
 SD_DEVINL void attend_stage_t(uint32_t kb, uint32_t vb, int lane, const uint32_t (&qf)[8][NQ][2], uint32_t valid,
-                              float scale_log2, AttAccT<NQ>& acc) {
-    const int g8 = lane >> 2;
+                              float scale_log2, AttAccT<NQ>& acc, const Logit& logit = Logit()) {
+    const int g8 = lane >> 2, t4 = lane & 3;
     float s[2][NQ][4];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
@@ -296,7 +302,9 @@ SD_DEVINL void attend_stage_t(uint32_t kb, uint32_t vb, int lane, const uint32_t
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int key = 16 * mt + g8 + 8 * h;
-                    const float x = ((valid >> key) & 1u) ? s[mt][nq][2 * h + e] * scale_log2 : -INFINITY;
+                    const bool on = (valid >> key) & 1u;
+                    const float x = on ? s[mt][nq][2 * h + e] * scale_log2 : -INFINITY;
+                    if (on) logit(8 * nq + 2 * t4 + e, key, x);
                     s[mt][nq][2 * h + e] = x;
                     tmax = fmaxf(tmax, x);
                 }
