@@ -1574,17 +1574,18 @@ def cuda_runtime():
 
 def measure_e2e_pipelined(step, w, K, n_sets=2):
     """End to end through the C ABI with host buffers, with `n_sets` batches in flight: every
-    step copies its queries in from pinned host memory (one packed copy) and its results (out,
-    lse, idx) back to pinned host memory (one packed copy), on a copy stream, while the
-    kernels of the step before run on the compute stream; events order each set's copy in,
-    kernels and copy out, and a set is refilled only after its previous results left.  Host
-    wall clock over K steps, ending with a synchronize."""
+    step copies its queries in from pinned host memory (one packed copy, on an input stream)
+    and its results (out, lse, idx) back to pinned host memory (one packed copy, on an output
+    stream), while the kernels of the step before run on the compute stream; events order each
+    set's copy in, kernels and copy out: a set's inputs are refilled once its previous kernels
+    are done, and its kernels run once its previous results left.  Host wall clock over K
+    steps, ending with a synchronize."""
     import ctypes
     import torch
     rt = cuda_runtime()
     rt.cudaStreamWaitEvent.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
     rt.cudaEventRecord.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
-    s_c, s_x = torch.cuda.Stream(), torch.cuda.Stream()
+    s_c, s_x, s_o = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     sets = [step.io_set(s_c) for _ in range(n_sets)]
     h_in = []
     for d_in, _, _, _ in sets:
@@ -1603,11 +1604,13 @@ def measure_e2e_pipelined(step, w, K, n_sets=2):
     ev_in = [ev() for _ in sets]
     ev_done = [ev() for _ in sets]
     ev_out = [ev() for _ in sets]
-    cx, cc = ctypes.c_void_p(s_x.cuda_stream), ctypes.c_void_p(s_c.cuda_stream)
+    cx, cc, co = ctypes.c_void_p(s_x.cuda_stream), ctypes.c_void_p(s_c.cuda_stream), ctypes.c_void_p(s_o.cuda_stream)
 
     def one(i):
         j = i % n_sets
         d_in, d_out, calls, _ = sets[j]
+        if i >= n_sets:  # the set's previous kernels have read its inputs
+            rt.cudaStreamWaitEvent(cx, ev_done[j], 0)
         if rt.cudaMemcpyAsync(ctypes.c_void_p(d_in.data_ptr()), ctypes.c_void_p(h_in[j].data_ptr()), d_in.numel(), 1,
                               cx) != 0:
             raise RuntimeError("cudaMemcpyAsync (inputs) failed")
@@ -1618,11 +1621,11 @@ def measure_e2e_pipelined(step, w, K, n_sets=2):
         for c in calls:
             c()
         rt.cudaEventRecord(ev_done[j], cc)
-        rt.cudaStreamWaitEvent(cx, ev_done[j], 0)
+        rt.cudaStreamWaitEvent(co, ev_done[j], 0)
         if rt.cudaMemcpyAsync(ctypes.c_void_p(h_out[j].data_ptr()), ctypes.c_void_p(d_out.data_ptr()), d_out.numel(), 2,
-                              cx) != 0:
+                              co) != 0:
             raise RuntimeError("cudaMemcpyAsync (results) failed")
-        rt.cudaEventRecord(ev_out[j], cx)
+        rt.cudaEventRecord(ev_out[j], co)
 
     for i in range(2 * n_sets):  # warm-up, untimed
         one(i)
@@ -1648,9 +1651,9 @@ def measure_e2e_pipelined(step, w, K, n_sets=2):
     return {"value": round(w.queries_per_step * K / dt, 1), "unit": "queries/s",
             "h2d_bytes_per_step": int(sets[0][0].numel()), "d2h_bytes_per_step": int(sets[0][1].numel()),
             "timing": (f"host wall clock over {K} steps with {n_sets} batches in flight: per step one packed copy "
-                       "of the queries in from pinned memory and one of out, lse and idx back, on a copy stream "
-                       "beside the compute stream; prebound C-ABI calls"),
-            "ctypes_calls_per_step": len(sets[0][2]) + 8}
+                       "of the queries in from pinned memory and one of out, lse and idx back, on input and output "
+                       "copy streams beside the compute stream; prebound C-ABI calls"),
+            "ctypes_calls_per_step": len(sets[0][2]) + 9}
 
 
 def measure_e2e_packed(step, w, clean_l2, K):
