@@ -289,9 +289,18 @@ __global__ void __launch_bounds__(NT, kTkThreads / NT)
     uint32_t* hrow = key_hist + (size_t)blockIdx.x * kHistBins;
     pdl_wait();
     pdl_launch_dependents();
-    for (int b = tid; b < kHistBins; b += NT) {
-        sh.hist[b] = hrow[b];
-        hrow[b] = 0u;
+    {
+        // every load before any store: a load queued behind the store to the same row of
+        // bins, one at a time, cost ~4 us each
+        static_assert(kHistBins % NT == 0, "bins per thread");
+        uint32_t hv[kHistBins / NT];
+#pragma unroll
+        for (int i = 0; i < kHistBins / NT; ++i) hv[i] = __ldcg(hrow + tid + i * NT);
+#pragma unroll
+        for (int i = 0; i < kHistBins / NT; ++i) {
+            sh.hist[tid + i * NT] = hv[i];
+            hrow[tid + i * NT] = 0u;
+        }
     }
     for (int w = tid; w < NW; w += NT) {
         sel[w] = 0u;
