@@ -1146,8 +1146,10 @@ def step_report(step, w, workload, kmarks, dom_ms, ms_per_step, peak, device, K,
                                    ("decode_step.cu", "step_tiles.cuh", "tc_common.cuh", "sd_common.cuh")), "decode_step"
     elif isinstance(step, (SparseDecodeStep, WindowStep, HeadsStep, VerifyGroupStep, LookaheadStep, CachedTieredStep)):
         kernel_file, kernel_tag = ("index_score.cu", "index_score_tc.cu", "tc_common.cuh", "sd_common.cuh"), "index_score"
+    elif isinstance(step, DenseScoringStep):  # dense over the cache: the tiled path
+        kernel_file, kernel_tag = ("dense_attend.cu", "step_tiles.cuh", "tc_common.cuh", "sd_common.cuh"), "dense_attend"
     else:
-        kernel_file, kernel_tag = ("gather_attend.cu", "sd_common.cuh"), "gather_attend"
+        kernel_file, kernel_tag = ("gather_attend.cu", "attend_mma.cuh", "sd_common.cuh"), "gather_attend"
     traffic = profiled_traffic(workload, kernel_tag, source_digest(*kernel_file))
     step_s = ms_per_step / 1e3
     step_roof = {"bound": "hbm", "hbm_bytes": by["hbm"], "unit": "GB/s",
