@@ -38,7 +38,22 @@ __global__ void __launch_bounds__(kWinThreads)
     if (valid) {
         const float* srow = scores + (size_t)r * N;
         const long t0 = (long)n * stride, t1 = t0 + kernel < (long)N ? t0 + kernel : (long)N;
-        for (long t = t0; t < t1; ++t) m = fmaxf(m, __ldg(srow + t));
+        if (((t0 | t1) & 3) == 0 && (reinterpret_cast<uintptr_t>(srow) & 15) == 0) {
+            // 16-byte loads, eight issued before any is used (a window of 32 scores: one
+            // round trip instead of one per score behind the running max)
+            const float4* p4 = reinterpret_cast<const float4*>(srow + t0);
+            const int n4 = (int)((t1 - t0) >> 2);
+            for (int i0 = 0; i0 < n4; i0 += 8) {
+                float4 x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    x[u] = i0 + u < n4 ? __ldg(p4 + i0 + u) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) m = fmaxf(m, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
+            }
+        } else {
+            for (long t = t0; t < t1; ++t) m = fmaxf(m, __ldg(srow + t));
+        }
         w[(size_t)r * NW + n] = m;
     }
     if (key_hist != nullptr) {
