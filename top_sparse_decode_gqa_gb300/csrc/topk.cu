@@ -5,6 +5,8 @@
 // scoring tokens; SparDA (gist.science summary), sec. 2 item 1, selects top-k blocks the
 // same way.  The pages are silent on ties; the lower index wins.
 //
+// Rows of at most 4096 entries: one 256-thread CTA per row, the row in registers, four 8-bit
+// radix passes (topk_small_kernel).
 // Rows of 16384 entries or more, when clusters of two or more CTAs per row fit in one wave,
 // go to the cluster selection of select_attend.cu (each CTA owns a part of the row; the
 // digits are summed over distributed shared memory).  Otherwise one CTA per row (1024
@@ -238,6 +240,126 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         krem -= (int)above;
     }
     emit_selected<kTkThreads>(sh, key_at, N, k, prefix, krem, orow);
+}
+
+// Short rows (N <= kSmallN): one 256-thread CTA per row holds the whole row in registers —
+// warp w the entries [w*32*EPT, (w+1)*32*EPT), lane l those at 32j + l, so the loads coalesce
+// whatever the row's alignment — and resolves the threshold key in four 8-bit radix passes
+// over warp-private shared histograms (equal digits of a warp merged with one match, one
+// atomic per distinct digit).  The emit goes in index order: one scan over the warps of the
+// packed (above, equal) counts, then ballots within each warp.  A key histogram passed in is
+// only cleared: ranking a row this short from registers costs less than reading the seed.
+constexpr int kSmallThreads = 256;
+constexpr int kSmallWarps = kSmallThreads / 32;
+constexpr int kSmallN = 4096;
+
+struct SmallShared {
+    uint32_t h[2][kSmallWarps][256];  // per-warp histograms, alternating between passes
+    uint32_t wtot[3][kSmallWarps];
+    uint32_t dig[2], abv[2];
+};
+
+template <int EPT>
+__global__ void __launch_bounds__(kSmallThreads)
+    topk_small_kernel(const float* __restrict__ scores, int N, int k, int32_t* __restrict__ idx_out,
+                      uint32_t* __restrict__ key_hist) {
+    static_assert(kSmallThreads == 256, "thread t owns radix bin 255 - t");
+    static_assert(kSmallWarps * 32 * EPT <= 65535, "packed 16-bit counts");
+    __shared__ SmallShared sh;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float* srow = scores + (size_t)blockIdx.x * N;
+    int32_t* orow = idx_out + (size_t)blockIdx.x * k;
+    pdl_wait();
+    pdl_launch_dependents();
+    const int seg0 = warp * 32 * EPT;
+    uint32_t kk[EPT];
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+        const int i = seg0 + 32 * j + lane;
+        kk[j] = i < N ? float_key(__ldcg(srow + i)) : 0u;
+    }
+    if (key_hist != nullptr) {
+        uint32_t* hrow = key_hist + (size_t)blockIdx.x * kHistBins;
+        for (int b = tid; b < kHistBins; b += kSmallThreads) hrow[b] = 0u;
+    }
+    if (k == 0) return;
+    if (k == N) {
+        for (int i = tid; i < N; i += kSmallThreads) orow[i] = i;
+        return;
+    }
+    uint32_t prefix = 0, pmask = 0;
+    int krem = k;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass, buf = pass & 1;
+        uint32_t* wh = sh.h[buf][warp];
+        // this buffer was last read two passes ago, before the barriers of the pass between
+        for (int b = lane; b < 256; b += 32) wh[b] = 0u;
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+            const bool in = seg0 + 32 * j + lane < N && (kk[j] & pmask) == prefix;
+            if (__any_sync(0xffffffffu, in)) {
+                const uint32_t dg = (kk[j] >> shift) & 255u;
+                const uint32_t peers = __match_any_sync(0xffffffffu, in ? dg : 0xffffffffu);
+                if (in && lane == __ffs(peers) - 1) atomicAdd(&wh[dg], (uint32_t)__popc(peers));
+            }
+        }
+        __syncthreads();
+        // thread t owns bin 255 - t: an inclusive scan over t counts the keys at or above it
+        const int bin = 255 - tid;
+        uint32_t c = 0;
+#pragma unroll
+        for (int w = 0; w < kSmallWarps; ++w) c += sh.h[buf][w][bin];
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        if (lane == 31) sh.wtot[buf][warp] = incl;
+        __syncthreads();
+        for (int w = 0; w < warp; ++w) incl += sh.wtot[buf][w];
+        const uint32_t excl = incl - c;
+        if (excl < (uint32_t)krem && (uint32_t)krem <= incl) {
+            sh.dig[buf] = (uint32_t)bin;
+            sh.abv[buf] = excl;
+        }
+        __syncthreads();
+        prefix |= sh.dig[buf] << shift;
+        pmask |= 255u << shift;
+        krem -= (int)sh.abv[buf];
+    }
+    const uint32_t thr = prefix;
+    uint32_t gt = 0, eq = 0;
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+        const bool valid = seg0 + 32 * j + lane < N;
+        gt += (valid && kk[j] > thr) ? 1u : 0u;
+        eq += (valid && kk[j] == thr) ? 1u : 0u;
+    }
+    const uint32_t packed = __reduce_add_sync(0xffffffffu, (gt << 16) | eq);
+    if (lane == 0) sh.wtot[2][warp] = packed;
+    __syncthreads();
+    uint32_t before = 0;
+    for (int w = 0; w < warp; ++w) before += sh.wtot[2][w];
+    uint32_t eq_seen = before & 0xffffu;
+    uint32_t pos = (before >> 16) + min(eq_seen, (uint32_t)krem);
+    const uint32_t lt = lanemask_lt();
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+        const int i = seg0 + 32 * j + lane;
+        const bool valid = i < N;
+        const bool is_gt = valid && kk[j] > thr;
+        const bool is_eq = valid && kk[j] == thr;
+        const uint32_t eqm = __ballot_sync(0xffffffffu, is_eq);
+        const bool sel = is_gt || (is_eq && eq_seen + __popc(eqm & lt) < (uint32_t)krem);
+        const uint32_t selm = __ballot_sync(0xffffffffu, sel);
+        const uint32_t at = pos + __popc(selm & lt);
+        if (sel && at < (uint32_t)k) orow[at] = i;
+        pos += __popc(selm);
+        eq_seen += __popc(eqm);
+    }
 }
 
 constexpr int kCandCap = 4096;
@@ -511,6 +633,15 @@ extern "C" sd_status sd_topk(const float* scores, int rows, int N, int k, int32_
     if (key_hist == nullptr && k == 0) return SD_OK;
     SD_REQUIRE(scores && (k == 0 || idx), "sd_topk: null pointer");
     cudaStream_t st = as_stream(stream);
+    if (N <= kSmallN) {  // the row in registers, one CTA per row
+        if (N <= kSmallWarps * 32 * 8)
+            SD_CUDA_CHECK(launch_pdl(topk_small_kernel<8>, rows, kSmallThreads, 0, st, scores, N, k, idx, key_hist),
+                          "sd_topk: launch");
+        else
+            SD_CUDA_CHECK(launch_pdl(topk_small_kernel<16>, rows, kSmallThreads, 0, st, scores, N, k, idx, key_hist),
+                          "sd_topk: launch");
+        return launch_status("sd_topk");
+    }
     // few long rows: several CTAs per row in a thread-block cluster
     if (N >= kClusterMinN) {
         sd_status cs = SD_OK;
