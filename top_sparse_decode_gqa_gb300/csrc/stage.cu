@@ -21,6 +21,7 @@ namespace {
 constexpr int kStThreads = 256;
 constexpr int kStPieces = 8;  // 16-byte pieces a lane moves per chunk (all loads before any store)
 constexpr int kStTailShare = 4;  // the last 1/kStTailShare of the list rows go out as short tickets
+constexpr int kStGrid = 64;      // CTAs of the copy (at most one per SM)
 
 struct StageParams {
     const uint8_t* kh;  // mapped host cache [B, kv_heads, T, d]
@@ -58,7 +59,7 @@ SD_DEVINL int nth_set_bit(uint32_t mask, int n) {
 // serves most rows) except over the last 1/kStTailShare of the list, where they hold one copy
 // batch: when most rows are misses a 32-row ticket takes four batches in a row, and the last
 // such tickets would keep a few warps copying after the rest have finished.
-// No shared memory, and registers capped at 80 (the bound's 3 CTAs; the grid has one per SM):
+// No shared memory, and registers capped at 80 (the bound's 3 CTAs; the grid has at most one per SM):
 // the kernel runs beside the indexer, whose CTAs need most of an SM's shared memory, and
 // beside the attention.
 __global__ void __launch_bounds__(kStThreads, 3) stage_host_rows_kernel(const StageParams p) {
@@ -193,10 +194,13 @@ extern "C" sd_status sd_stage_host_rows(const sd_attend_args* a, uint32_t* count
     p.err = a->err_word;
     p.slot_per_head = a->slot_per_head;
     if (p.total_rows == 0) return SD_OK;
-    // one CTA (8 warps, 32 KB of host reads in flight) per SM is several times what the host
-    // link can serve, and leaves each SM room for other kernels running beside the copy
-    // (the next layer's indexer, the current layer's attention)
-    const int grid = num_sms();
+    // 64 CTAs of 8 warps (2 MB of host reads in flight) keep the host link busy (~200 GB/s:
+    // the same rate as one CTA per SM) and leave most SMs to the kernels running beside the
+    // copy (the next layer's indexer, the current layer's attention); a grid of one CTA per
+    // SM slowed those enough to cost ~10 % of a lookahead step, while fewer than ~32 CTAs
+    // no longer fill the link and calls whose rows are mostly pooled lose to the longer
+    // resolve per warp
+    const int grid = num_sms() < kStGrid ? num_sms() : kStGrid;
     SD_CUDA_CHECK(launch_pdl(stage_host_rows_kernel, dim3((unsigned)grid), dim3(kStThreads), 0, as_stream(stream), p),
                   "sd_stage_host_rows: launch");
     return launch_status("sd_stage_host_rows");
