@@ -203,16 +203,20 @@ sd_status sd_topk(const float* scores, int rows, int N, int k, int32_t* idx, uin
  * read as without tiers (from the pool, or host memory at slot -1, or the cache).  The
  * codes enter the tensor cores unchanged (small integers are exact in bf16) and the
  * scales multiply the row's logit and its softmax weight in fp32.  A call in which no
- * selected row has tier 2 or 3 gives the bits of the same call without tiers (for a dense
- * call: the one with row_loop = 1).  Limits: bf16, d = 128, not per_head, no ring, no
+ * selected row has tier 2 or 3 gives the bits of the same call without tiers and with
+ * row_loop = 1.  Limits: bf16, d = 128, not per_head, no ring, no
  * stage; T and pool_rows < 2^29.
  * Dense calls over a cache in HBM (idx, slot_map, tier, ring and stage all unset, not
  * per_head; bf16, d = 128, G*V <= 16) move each split's contiguous rows as whole 64-row
  * tiles (tiled TMA into a two-stage ring per CTA) through a tile that puts the keys on the
  * tensor cores' M side; their splits are ranges of whole tiles (never more than the
- * workspace holds).  Same values within rounding, in another summation order; row_loop = 1
- * makes such a call run the general row loop instead, e.g. to compare its bits with a
- * tiered call's.
+ * workspace holds).  Block-sparse calls over a cache in HBM (idx set, block a multiple of
+ * 16, T a multiple of block, logits NULL, otherwise as dense calls) take the same tiles,
+ * each 64-row stage made of four 16-row boxes at the selected blocks' rows (an empty or bad
+ * index loads nothing and is masked; a bad one is reported as without tiles).  Same values
+ * within rounding, in another summation order; row_loop = 1 makes such a call run the
+ * general row loop instead, e.g. to compare its bits with a tiered, pooled or staged
+ * call's.
  * The kernel is launched as a programmatic dependent of the preceding kernel in the
  * stream (it waits for that kernel's results before reading anything).
  */
@@ -248,7 +252,7 @@ typedef struct {
     const int8_t* v_int8;     /* same layout, of V */
     const float* k_scale;     /* [B,Hkv,T] fp32 scales of the T2 rows of K */
     const float* v_scale;     /* [B,Hkv,T] fp32, of V */
-    int row_loop;             /* 1: a dense call runs the general row loop (see above) */
+    int row_loop;             /* 1: a dense or tiled block-sparse call runs the general row loop (see above) */
 } sd_attend_args;
 
 size_t sd_gather_attend_workspace_bytes(const sd_attend_args* args);

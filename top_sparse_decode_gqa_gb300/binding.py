@@ -252,7 +252,8 @@ def make_attend_args(q, k_cache, v_cache, idx=None, *, n_idx=None, block=1, T=No
     """Fill an sd_attend_args from tensors; returns (args, out, lse, logits).  slot_map is
     [B,T] (residency per sequence) or [B,Hkv,T] (per KV head).  tier [B,T] uint8 with
     k_int8/v_int8 [B,Hkv,T,d] int8 and k_scale/v_scale [B,Hkv,T] fp32: the tiered rows.
-    row_loop: a dense call runs the general row loop (the one tiered calls take)."""
+    row_loop: a dense or tiled block-sparse call runs the general row loop (the one tiered
+    calls take)."""
     _dev(q, "q")
     B, V, Hq, d = q.shape
     Hkv = k_cache.shape[1]

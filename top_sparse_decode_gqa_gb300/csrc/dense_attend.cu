@@ -1,6 +1,8 @@
-// dense_attend.cu -- sd_gather_attend's path for dense attention over a cache resident in
-// HBM: every one of the T rows of each KV group, bf16, d = 128, at most 16 query rows per
-// group (the per-layer step of importance scoring, which keeps every logit).
+// dense_attend.cu -- sd_gather_attend's path for attention over a cache resident in HBM
+// read as whole tiles: every one of the T rows of each KV group (the per-layer step of
+// importance scoring, which keeps every logit), or the rows of selected blocks of 16 or more
+// rows (block-sparse selection; compression windows as 16-token segments); bf16, d = 128, at
+// most 16 query rows per group.
 //
 // "Nem Todos os Pensamentos Necessitam de HBM" (gist.science summary), Metodologia 2: the
 // importance of a position accumulates the attention weight every query head gives it, so
@@ -9,7 +11,9 @@
 // (news page), "Metodologia": the query rows of a group share each fetched row.
 //
 // The rows of a group are contiguous, so they move as whole tiles: CTA (split, kvh, b)
-// streams its contiguous range of the group's rows through a two-stage ring of 64-row
+// streams its contiguous range of the group's rows (or of its list of selected rows, whose
+// 16-row sub-tiles are contiguous in the cache and are resolved once into shared memory)
+// through a two-stage ring of 64-row
 // stages (tiled TMA, 128-byte swizzle; warp 4 issues the copies), and consumer warps 0-3
 // take the 32-row halves of the stages (stage n to warps 2(n % 2) and 2(n % 2) + 1) with the
 // transposed mma.sync tile of step_tiles.cuh, each keeping its own online softmax over all
@@ -36,7 +40,9 @@ constexpr int kDaRing = 2;                  // stages (stage n in slot n % 2, ta
 constexpr int kDaQ = kDaRing * kDaSlot;     // query rows: 16 x 256 bytes
 constexpr int kDaBars = kDaQ + 16 * 256;    // full[2], empty[2], q
 constexpr int kDaMisc = kDaBars + 64;       // the abort flag
-constexpr int kDaBytes = kDaMisc + 16 + 1024;  // slack for the 1024-byte alignment of the ring
+constexpr int kDaMaxSub = 1024;             // 16-row sub-tiles a split of a block-sparse call covers
+constexpr int kDaYs = kDaMisc + 16;         // their first rows in the cache, or -1: [kDaMaxSub] int32
+constexpr int kDaBytes = kDaYs + kDaMaxSub * 4 + 1024;  // slack for the 1024-byte alignment of the ring
 // after the loop, in the ring: the warps' O rows [4][16][128] floats, then their (m, l) [4][16]
 constexpr int kDaPartML = kDaCons * 16 * 128 * 4;
 static_assert(kDaPartML + kDaCons * 16 * 8 <= kDaRing * kDaSlot, "the warps' states fit in the ring");
@@ -50,6 +56,10 @@ struct DaParams {
     float* ws_o;       // with splits > 1: [B*Hkv][splits][RP][128], then m and l [..][RP]
     float* ws_m;
     float* ws_l;
+    const int32_t* idx;  // block-sparse: [B*Hkv][n_idx] selected blocks, else null (dense)
+    int n_idx, block;
+    int n_rows;          // rows of a group's list: n_idx * block (T when dense)
+    int total_rows;      // rows of the cache tensor (B*Hkv*T): a coordinate past them loads zeros
     int V, Hq, Hkv, G, R, T, rps, splits, RP;
     float scale_log2;
     unsigned long long wait_ns;
@@ -97,8 +107,30 @@ __global__ void __launch_bounds__(kDaThreads, NQ == 1 ? 3 : 2)
     __syncthreads();
     pdl_wait();  // q and the cache may be the preceding kernels' results
 
-    const int t0 = split * p.rps, n_rows = max(0, min(p.T, t0 + p.rps) - t0);
+    const int t0 = split * p.rps, n_rows = max(0, min(p.n_rows, t0 + p.rps) - t0);
     const int n_st = (n_rows + kDaRows - 1) / kDaRows;
+    // block-sparse: the split's 16-row sub-tiles (one block holds whole sub-tiles) resolved to
+    // their first cache row, or -1 for an empty slot (-1) or a bad index (reported)
+    const int32_t* ys = reinterpret_cast<const int32_t*>(sm + kDaYs);
+    const int n_sub = (n_rows + 15) / 16;
+    if (p.idx != nullptr) {
+        int32_t* yw = reinterpret_cast<int32_t*>(sm + kDaYs);
+        for (int i = tid; i < n_sub; i += kDaThreads) {
+            const int j0 = t0 + 16 * i;
+            const long sel = p.idx[(size_t)g * p.n_idx + j0 / p.block];
+            const long pos = sel * p.block + j0 % p.block;
+            int32_t y = -1;
+            if (sel == -1) {
+                // empty slot
+            } else if (sel < 0 || pos >= p.T) {
+                report(p.err, SD_DEVERR_INDEX);
+            } else {
+                y = (int32_t)((long)g * p.T + pos);
+            }
+            yw[i] = y;
+        }
+        __syncthreads();
+    }
     int n_issued = 0;  // stages the producer filled (its lane 0)
     AttAccT<NQ> acc;
     if (warp == kDaProd) {
@@ -117,16 +149,34 @@ __global__ void __launch_bounds__(kDaThreads, NQ == 1 ? 3 : 2)
                 }
                 uint8_t* st = sm + s * kDaSlot;
                 mbar_arrive_expect_tx(&full[s], kDaSlot);
-                // rows past the group's end load the next group's rows (or the tensor's fill)
-                // and are masked out
-                const int row = g * p.T + t0 + n * kDaRows;
+                if (p.idx == nullptr) {
+                    // rows past the group's end load the next group's rows (or the tensor's
+                    // fill) and are masked out
+                    const int row = g * p.T + t0 + n * kDaRows;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint8_t* dk = st + h * 16384;
-                    tma_load_2d_hint(dk, &kvk, 0, row + 32 * h, &full[s], pol);
-                    tma_load_2d_hint(dk + 4096, &kvk, 64, row + 32 * h, &full[s], pol);
-                    tma_load_2d_hint(dk + 8192, &kvv, 0, row + 32 * h, &full[s], pol);
-                    tma_load_2d_hint(dk + 12288, &kvv, 64, row + 32 * h, &full[s], pol);
+                    for (int h = 0; h < 2; ++h) {
+                        uint8_t* dk = st + h * 16384;
+                        tma_load_2d_hint(dk, &kvk, 0, row + 32 * h, &full[s], pol);
+                        tma_load_2d_hint(dk + 4096, &kvk, 64, row + 32 * h, &full[s], pol);
+                        tma_load_2d_hint(dk + 8192, &kvv, 0, row + 32 * h, &full[s], pol);
+                        tma_load_2d_hint(dk + 12288, &kvv, 64, row + 32 * h, &full[s], pol);
+                    }
+                } else {
+                    // four 16-row boxes per stage, each where its sub-tile's rows are; a
+                    // sub-tile without rows loads past the tensor (zeros) and is masked out.
+                    // Two 16-row boxes 2 KB apart land as one 32-row box would (swizzle atoms
+                    // of 8 rows, every box 1024-byte aligned).
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int i = 4 * n + q;
+                        const int y0 = i < n_sub ? ys[i] : -1;
+                        const int y = y0 >= 0 ? y0 : p.total_rows;
+                        uint8_t* dk = st + (q >> 1) * 16384 + (q & 1) * 2048;
+                        tma_load_2d_hint(dk, &kvk, 0, y, &full[s], pol);
+                        tma_load_2d_hint(dk + 4096, &kvk, 64, y, &full[s], pol);
+                        tma_load_2d_hint(dk + 8192, &kvv, 0, y, &full[s], pol);
+                        tma_load_2d_hint(dk + 12288, &kvv, 64, y, &full[s], pol);
+                    }
                 }
                 n_issued = n + 1;
             }
@@ -149,7 +199,12 @@ __global__ void __launch_bounds__(kDaThreads, NQ == 1 ? 3 : 2)
             if (!warp_wait(&full[s], (uint32_t)((n / kDaRing) & 1), abort_flag, lim)) break;
             const int jb = n * kDaRows + 32 * h;  // this half's first row in the CTA's range
             const int nv = max(0, min(32, n_rows - jb));
-            const uint32_t valid = nv >= 32 ? 0xffffffffu : ((1u << nv) - 1u);
+            uint32_t valid = nv >= 32 ? 0xffffffffu : ((1u << nv) - 1u);
+            if (p.idx != nullptr) {  // the half's two sub-tiles
+                const int i0 = 4 * n + 2 * h;
+                valid &= ((i0 < n_sub && ys[i0] >= 0) ? 0x0000ffffu : 0u) |
+                         ((i0 + 1 < n_sub && ys[i0 + 1] >= 0) ? 0xffff0000u : 0u);
+            }
             const uint32_t kb = ring + s * kDaSlot + h * 16384;
             lg.t0 = t0 + jb;
             if (valid != 0u) attend_stage_t<NQ>(kb, kb + 8192, lane, qf, valid, p.scale_log2, acc, lg);
@@ -232,28 +287,44 @@ __global__ void __launch_bounds__(kDaThreads, NQ == 1 ? 3 : 2)
 
 int dense_tma_ctas_per_sm(const sd_attend_args* a) { return (a->Hq / a->Hkv) * a->V <= 8 ? 3 : 2; }
 
+int dense_tma_max_split_rows() { return kDaMaxSub * 16; }
+
 bool dense_tma_eligible(const sd_attend_args* a) {
     const int R = (a->Hq / a->Hkv) * a->V;
-    return a->idx == nullptr && a->slot_map == nullptr && a->ring_w == 0 && !a->per_head && a->tier == nullptr &&
-           a->k_stage == nullptr && a->row_loop == 0 && a->dtype == SD_BF16 && a->d == 128 && R >= 1 && R <= 16 &&
-           (long)a->n_idx * a->block == a->T && a->T > 0 && (long)a->B * a->Hkv * a->T < (1L << 31);
+    const bool common = a->slot_map == nullptr && a->ring_w == 0 && !a->per_head && a->tier == nullptr &&
+                        a->k_stage == nullptr && a->row_loop == 0 && a->dtype == SD_BF16 && a->d == 128 && R >= 1 &&
+                        R <= 16 && a->T > 0 && (long)a->B * a->Hkv * a->T < (1L << 31);
+    if (!common) return false;
+    if (a->idx == nullptr) return (long)a->n_idx * a->block == a->T;
+    // block-sparse: whole 16-row sub-tiles per block, whole blocks per cache, and no logits
+    // (the row loop defines those of empty slots)
+    return a->logits == nullptr && a->n_idx > 0 && a->block % 16 == 0 && a->T % a->block == 0;
 }
 
 sd_status dense_tma_launch(const sd_attend_args* a, int max_splits, int RP, float* ws_o, float* ws_m, float* ws_l,
                            int* splits_used, cudaStream_t st) {
     const char* who = "sd_gather_attend";
     const int NG = a->B * a->Hkv;
+    const bool sparse = a->idx != nullptr;
+    const int n_rows = sparse ? a->n_idx * a->block : a->T;  // a group's list rows
     // contiguous ranges of whole 64-row stages, no more splits than the workspace holds and,
-    // unless the caller asked for a count, one wave of CTAs
+    // unless the caller asked for a count, one wave of CTAs; a block-sparse range at most
+    // kDaMaxSub sub-tiles (the plan's splits are at most that long, so they still fit)
     int S0 = std::max(1, max_splits);
     if (a->splits <= 0 && NG > 0) S0 = std::min(S0, std::max(1, dense_tma_ctas_per_sm(a) * num_sms() / NG));
-    int rps = (a->T + S0 - 1) / S0;
+    int rps = (n_rows + S0 - 1) / S0;
     rps = (rps + kDaRows - 1) / kDaRows * kDaRows;
-    const int S = (a->T + rps - 1) / rps;
+    if (sparse) rps = std::min(rps, kDaMaxSub * 16);
+    const int S = (n_rows + rps - 1) / rps;
+    if (S > std::max(1, max_splits)) {
+        set_error("%s: %d splits exceed the workspace's %d", who, S, max_splits);
+        return SD_ERR_INVALID_ARG;
+    }
     *splits_used = S;
+    const int box_rows = sparse ? 16 : 32;
     CUtensorMap kvk, kvv;
-    if (!make_tensor_map_2d(&kvk, a->k_cache, (uint64_t)NG * a->T, 128, 32, false) ||
-        !make_tensor_map_2d(&kvv, a->v_cache, (uint64_t)NG * a->T, 128, 32, false)) {
+    if (!make_tensor_map_2d(&kvk, a->k_cache, (uint64_t)NG * a->T, 128, box_rows, false) ||
+        !make_tensor_map_2d(&kvv, a->v_cache, (uint64_t)NG * a->T, 128, box_rows, false)) {
         set_error("%s: cuTensorMapEncodeTiled failed", who);
         return SD_ERR_CUDA;
     }
@@ -266,6 +337,11 @@ sd_status dense_tma_launch(const sd_attend_args* a, int max_splits, int RP, floa
     p.ws_o = ws_o;
     p.ws_m = ws_m;
     p.ws_l = ws_l;
+    p.idx = a->idx;
+    p.n_idx = a->n_idx;
+    p.block = a->block;
+    p.n_rows = n_rows;
+    p.total_rows = NG * a->T;
     p.V = a->V;
     p.Hq = a->Hq;
     p.Hkv = a->Hkv;

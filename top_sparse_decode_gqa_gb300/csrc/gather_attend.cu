@@ -679,19 +679,22 @@ SplitPlan plan_splits(const sd_attend_args* a) {
     sp.RP = kernel_rows(a->dtype, a->per_head ? a->V : (a->Hkv > 0 ? (a->Hq / a->Hkv) * a->V : 0));
     const long chunks = (n_rows + kCH - 1) / kCH;
     const bool resolve = a->idx != nullptr || a->slot_map != nullptr || a->ring_w > 0;
+    const bool tiled = dense_tma_eligible(a);
     long splits;
     if (a->splits > 0) {
         splits = a->splits;
     } else {
-        // one wave of the kernel that will run (the dense tiled path has its own occupancy)
-        const int per_sm = dense_tma_eligible(a) ? dense_tma_ctas_per_sm(a)
-                                                 : att_ctas_per_sm(layout_bytes(a->dtype, a->d, sp.RP));
+        // one wave of the kernel that will run (the tiled path has its own occupancy)
+        const int per_sm = tiled ? dense_tma_ctas_per_sm(a) : att_ctas_per_sm(layout_bytes(a->dtype, a->d, sp.RP));
         const long slots = (long)num_sms() * per_sm;
         splits = bk > 0 ? slots / bk : 1;
     }
     splits = std::max(1L, std::min(splits, std::max(1L, chunks)));
     long rps = n_rows > 0 ? (n_rows + splits - 1) / splits : 1;
-    if (resolve && rps > kMaxSplitRows) rps = kMaxSplitRows;
+    // rows whose sources a CTA resolves up front: the row loop's list, or the tiled path's
+    // table of 16-row sub-tiles
+    const long max_rps = tiled ? dense_tma_max_split_rows() : kMaxSplitRows;
+    if (resolve && rps > max_rps) rps = max_rps;
     splits = n_rows > 0 ? (n_rows + rps - 1) / rps : 1;
     sp.splits = (int)splits;
     sp.rows_per_split = (int)rps;
@@ -896,8 +899,8 @@ extern "C" sd_status sd_gather_attend(const sd_attend_args* a, void* stream) {
     SD_REQUIRE(a->row_loop == 0 || a->row_loop == 1, "sd_gather_attend: row_loop must be 0 or 1");
     sd_status s1;
     if (dense_tma_eligible(a)) {
-        // whole 64-row tiles of a dense cache in HBM; its split count, at most the plan's,
-        // is the merge's
+        // whole 64-row tiles of a cache in HBM (dense, or blocks of 16 or more rows); its
+        // split count, at most the plan's, is the merge's
         int used = 1;
         s1 = dense_tma_launch(a, sp.splits, sp.RP, p.ws_o, p.ws_m, p.ws_l, &used, st);
         p.splits = used;

@@ -37,11 +37,13 @@ bool topk_by_clusters(const float* scores, int rows, int N, int k, int32_t* idx,
 // per KV group): whether a validated request takes it, and its launch.
 bool block_step_eligible(const sd_decode_step_args* a);
 sd_status block_step_launch(const sd_decode_step_args* a, cudaStream_t st);
-// sd_gather_attend's dense path over a cache in HBM (dense_attend.cu): whether it applies,
+// sd_gather_attend's tiled path over a cache in HBM, dense or blocks of 16 or more rows
+// (dense_attend.cu): whether it applies,
 // and its launch, at most max_splits splits (partials in ws_o/ws_m/ws_l with RP rows per
 // split when more than one; *splits_used tells how many).
 bool dense_tma_eligible(const sd_attend_args* a);
 int dense_tma_ctas_per_sm(const sd_attend_args* a);
+int dense_tma_max_split_rows();  // list rows a split of a block-sparse call may hold
 sd_status dense_tma_launch(const sd_attend_args* a, int max_splits, int RP, float* ws_o, float* ws_m, float* ws_l,
                            int* splits_used, cudaStream_t st);
 
