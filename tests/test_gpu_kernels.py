@@ -103,8 +103,10 @@ def test_fp16_pooled_keys_on_the_tensor_cores(T, dI, block, V):
 # --------------------------------------------------------------------------- top-k
 
 
-@pytest.mark.parametrize("N", [1, 7, 100, 1000, 2048, 4096, 32768, 65536, 131072])
+@pytest.mark.parametrize("N", [1, 7, 100, 1000, 2048, 4096, 5000, 12000, 32768, 65536, 131072])
 def test_topk_bit_exact_with_ties(N):
+    # N <= 4096: the short-row kernel; 4096 < N < 16384: one CTA per row with three digit
+    # passes; longer rows: thread-block clusters
     rng = np.random.default_rng(N)
     rows = 5
     # heavy ties: integer scores in a narrow range, one row all equal
@@ -137,10 +139,12 @@ def test_topk_float_scores_and_signed_zero():
     (1, 1, 1, 3000, 0, False),
     (1, 1, 1, 3000, 3000, False),
     (3, 1, 3, 777, 13, False),
-    (2, 3, 1, 2048, 64, False),       # block-selection shape: static + dynamic smem > 48 KB
+    (2, 3, 1, 2048, 64, False),       # block-selection shape (the short-row kernel)
     (1, 2, 1, 12000, 50, False),      # N between the cached and uncached sizes
+    (1, 2, 1, 9000, 100, True),       # every score equal, one 1024-thread CTA per row: its full-pass fallback
     (8, 32, 1, 4096 + 5, 300, False),  # more rows than SMs: the 512-thread variant
-    (10, 16, 1, 3000, 100, True),     # ... and its full-pass fallback
+    (10, 16, 1, 3000, 100, True),     # every score equal, short rows: the short-row kernel
+    (10, 16, 1, 5000, 100, True),     # ... longer rows: the 512-thread variant's full-pass fallback
     (4, 40, 2, 2048, 2047, False),
 ])
 def test_index_topk_with_key_histogram(B, Hkv, V, N, k, flat):
