@@ -42,6 +42,8 @@ constexpr int kAtomB = kQN * 128;     // one 64-element K slice of the query til
 // stores and histogram updates per token.
 int tc_epilogue_groups(int V, int per_query) { return !per_query || V == 1 ? 1 : V == 2 ? 2 : 4; }
 
+constexpr int kTcMaxAcc = 8;  // accumulators NB = 2E for up to E = 4 epilogue warpgroups
+
 template <int DI>
 struct TcLayout {
     static constexpr int kAtoms = DI / 64;
@@ -49,7 +51,7 @@ struct TcLayout {
     static constexpr int kStageB = kAtoms * kAtomB;
     static constexpr int kStage = kStageA + kStageB;
     static constexpr int oBars = kTcStages * kStage;              // 1024-aligned stages first
-    static constexpr int kBars = 2 * kTcStages + 8;                // full, empty, tfull[<=4], tempty[<=4]
+    static constexpr int kBars = 2 * kTcStages + 2 * kTcMaxAcc;    // full, empty, tfull[NB], tempty[NB]
     static constexpr int oMisc = oBars + kBars * 8;                // tmem slot, abort flag, consumed
     static constexpr int kBytes = oMisc + 16 + 1024;               // + alignment slack
 };
@@ -61,6 +63,7 @@ __global__ void __launch_bounds__(32 * (4 * E + 2), 1) index_score_tc_kernel(
     uint32_t idesc) {
     using L = TcLayout<DI>;
     constexpr int NB = 2 * E;                   // accumulators (16 TMEM columns each)
+    static_assert(NB <= kTcMaxAcc, "the barrier block holds tfull and tempty for kTcMaxAcc accumulators");
     constexpr uint32_t kTmemCols = 32u * E;     // a power of two >= 32
     constexpr int kProducer = 4 * E, kIssuer = 4 * E + 1;
     extern __shared__ uint8_t smem_raw[];
